@@ -1,0 +1,223 @@
+/*
+ * oracle.c — plain, slow, double-precision CPU oracle for the embedding
+ * similarity scan.  TEST INFRASTRUCTURE ONLY: the CUDA library never links,
+ * loads or calls this file; only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark do.
+ *
+ * Two computations are restated here, each from its plain definition, in
+ * double precision, with every sum taken in ascending index order and no
+ * blocking, fusion or reordering:
+ *
+ *  1. Greedy diversity sequences ("Issue 9-014: Tile Diversity Shader Inner
+ *     Loop For L2 Cache Locality", sections Current Behavior and Intended
+ *     Behavior).  Each sequence repeatedly picks the unmasked candidate that
+ *     is most different from what it already holds.  The running criterion
+ *     is the max-min (farthest-first) reading: every candidate keeps the
+ *     smallest cosine distance to any row picked so far, and the pick is the
+ *     candidate whose kept distance is largest, lowest index on ties.  The
+ *     scan may walk the candidates in tiles of T with the running
+ *     (best, index) carried from tile to tile; by associativity of max the
+ *     result equals one pass (same issue, Intended Behavior; Suggested
+ *     Implementation Steps, the tile loop and its "do not reset the running
+ *     max between tiles" warning; Risks, the last partial tile).
+ *
+ *  2. Best-matching-unit search ("From 80x to 385x: A Best-Matching-Unit
+ *     Search at the L2 Roof", section 3, Background): for each sample the
+ *     index of the codebook row at the smallest squared Euclidean distance,
+ *     taken in the direct form sum_k (x_k - w_k)^2, lowest index on ties.
+ *
+ * Readings where the pages are silent:
+ *   - cosine distance d(p, c) = 1 - <e_p, e_c> / (|e_p| |e_c|), in [0, 2];
+ *   - the start row seeds the running minimum and is masked; L counts the
+ *     picks after the start; the running minimum starts at +infinity;
+ *   - the BMU distance is the squared distance (no square root).
+ *
+ * Parallelism: OpenMP only across independent units (sequences, samples);
+ * the arithmetic inside one unit is strictly sequential.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static void set_threads(int threads) {
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#else
+    (void)threads;
+#endif
+}
+
+/* Threads an OpenMP parallel region will use with this setting. */
+int oracle_threads(int threads) {
+#ifdef _OPENMP
+    set_threads(threads);
+    return omp_get_max_threads();
+#else
+    (void)threads;
+    return 1;
+#endif
+}
+
+/* |e_c| = sqrt(sum_k E[c,k]^2), k ascending, for every row c. */
+void oracle_row_norms(const float *E, int64_t N, int32_t D, double *nrm) {
+    for (int64_t c = 0; c < N; ++c) {
+        double s = 0.0;
+        for (int32_t k = 0; k < D; ++k) {
+            double v = (double)E[c * (int64_t)D + k];
+            s += v * v;
+        }
+        nrm[c] = sqrt(s);
+    }
+}
+
+/* Cosine distance between rows p and c. */
+static double cosine_distance(const float *E, int32_t D, const double *nrm,
+                              int64_t p, int64_t c) {
+    double s = 0.0;
+    const float *ep = E + p * (int64_t)D;
+    const float *ec = E + c * (int64_t)D;
+    for (int32_t k = 0; k < D; ++k) s += (double)ep[k] * (double)ec[k];
+    return 1.0 - s / (nrm[p] * nrm[c]);
+}
+
+/* The fold of the newest pick p into the running minimum:
+ * m[c] <- min(m[c], d(p, c)) for every candidate c. */
+void oracle_fold(const float *E, int64_t N, int32_t D, const double *nrm,
+                 int64_t p, double *m) {
+    for (int64_t c = 0; c < N; ++c) {
+        double d = cosine_distance(E, D, nrm, p, c);
+        if (d < m[c]) m[c] = d;
+    }
+}
+
+/* The fold for R independent sequences at once (teacher forcing):
+ * row r of m (length N) takes the fold of pick p[r]. */
+void oracle_fold_batch(const float *E, int64_t N, int32_t D, const double *nrm,
+                       const int64_t *p, int32_t R, double *m, int threads) {
+    set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t r = 0; r < R; ++r) oracle_fold(E, N, D, nrm, p[r], m + (int64_t)r * N);
+}
+
+/* Argmax of m over the unmasked candidates, scanning c ascending in tiles of
+ * T candidates ([t*T, min((t+1)*T, N))); T <= 0 means one pass over all N.
+ * The running (best, index) is carried across tiles and a candidate replaces
+ * it only when strictly larger, so ties go to the lowest index.
+ * Returns -1 when every candidate is masked. */
+int64_t oracle_argmax(const double *m, const uint8_t *masked, int64_t N, int64_t T) {
+    if (T <= 0) T = N;
+    double best = -INFINITY;
+    int64_t best_idx = -1;
+    for (int64_t t0 = 0; t0 < N; t0 += T) {
+        int64_t t1 = t0 + T < N ? t0 + T : N;
+        for (int64_t c = t0; c < t1; ++c) {
+            if (masked[c]) continue;
+            if (best_idx < 0 || m[c] > best) {
+                best = m[c];
+                best_idx = c;
+            }
+        }
+    }
+    return best_idx;
+}
+
+/* Greedy max-min diversity sequences.
+ * E: N x D row-major; starts[B]; mask[N] (NULL = none) excludes candidates
+ * from every sequence; picks[B*L] receives the L picks after each start;
+ * radius[B*L] (NULL = not wanted) receives the running minimum distance of
+ * each pick at the time it was picked.  T is the scan tile (<= 0: one pass).
+ * Returns 0, or -1 if a sequence runs out of candidates (its remaining picks
+ * are set to -1). */
+int oracle_dseq(const float *E, int64_t N, int32_t D, const int32_t *starts,
+                int32_t B, int32_t L, const uint8_t *mask, int64_t T,
+                int32_t *picks, double *radius, int threads) {
+    double *nrm = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!nrm) return -2;
+    oracle_row_norms(E, N, D, nrm);
+    int status = 0;
+    set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(min : status)
+    for (int32_t b = 0; b < B; ++b) {
+        double *m = (double *)malloc(sizeof(double) * (size_t)N);
+        uint8_t *masked = (uint8_t *)malloc((size_t)N);
+        if (!m || !masked) {
+            free(m);
+            free(masked);
+            status = -2;
+            continue;
+        }
+        for (int64_t c = 0; c < N; ++c) {
+            m[c] = INFINITY;
+            masked[c] = mask ? (mask[c] != 0) : 0;
+        }
+        int64_t p = starts[b];
+        masked[p] = 1;
+        for (int32_t t = 0; t < L; ++t) {
+            oracle_fold(E, N, D, nrm, p, m);
+            int64_t w = oracle_argmax(m, masked, N, T);
+            picks[(int64_t)b * L + t] = (int32_t)w;
+            if (w < 0) {
+                for (int32_t u = t; u < L; ++u) picks[(int64_t)b * L + u] = -1;
+                status = -1;
+                break;
+            }
+            if (radius) radius[(int64_t)b * L + t] = m[w];
+            masked[w] = 1;
+            p = w;
+        }
+        free(m);
+        free(masked);
+    }
+    free(nrm);
+    return status;
+}
+
+/* Squared Euclidean distance in the direct form, k ascending. */
+static double sqdist(const float *x, const float *w, int32_t D) {
+    double s = 0.0;
+    for (int32_t k = 0; k < D; ++k) {
+        double diff = (double)x[k] - (double)w[k];
+        s += diff * diff;
+    }
+    return s;
+}
+
+/* Best-matching unit of every sample.
+ * X: n x D, W: M x D, both row-major.  idx[i] = the first j reaching the
+ * minimum of sqdist(X_i, W_j) (strict '<' while scanning j ascending);
+ * dist[i] = that minimum; second[i] (NULL = not wanted) = the smallest
+ * distance over j != idx[i], used to recognise near-ties. */
+void oracle_bmu(const float *X, int64_t n, const float *W, int64_t M, int32_t D,
+                int32_t *idx, double *dist, double *second, int threads) {
+    set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < n; ++i) {
+        const float *x = X + i * (int64_t)D;
+        double best = INFINITY, runner = INFINITY;
+        int64_t best_j = -1;
+        for (int64_t j = 0; j < M; ++j) {
+            double d = sqdist(x, W + j * (int64_t)D, D);
+            if (best_j < 0 || d < best) {
+                runner = best;
+                best = d;
+                best_j = j;
+            } else if (d < runner) {
+                runner = d;
+            }
+        }
+        idx[i] = (int32_t)best_j;
+        dist[i] = best;
+        if (second) second[i] = runner;
+    }
+}
+
+/* sqdist(X_{ii[r]}, W_{jj[r]}) for R given (sample, neuron) pairs. */
+void oracle_sqdist_pairs(const float *X, const float *W, int32_t D, const int64_t *ii,
+                         const int64_t *jj, int64_t R, double *out) {
+    for (int64_t r = 0; r < R; ++r)
+        out[r] = sqdist(X + ii[r] * (int64_t)D, W + jj[r] * (int64_t)D, D);
+}

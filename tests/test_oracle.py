@@ -1,0 +1,335 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, never against the oracle itself.
+
+Each pin function returns a list of failure strings for a given build of the
+oracle.  The real build must pass every pin; copies of the oracle with one
+planted mistake (a flipped comparison, a wrong norm, a dropped fold, a reset
+of the running max between tiles, a sign error, a dropped mask) must each fail
+at least one pin, which shows the pins are not vacuous (the same idea as the
+mutated-FMA check of the Metal GEMV audit, "opus_r22_gr", on the
+non-vacuity of a bitwise parity suite).
+"""
+from __future__ import annotations
+
+import math
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# --------------------------------------------------------------------------
+# independent routines (no oracle code): brute-force references
+
+
+def _brute_cosine_matrix(E: np.ndarray) -> list[list[float]]:
+    """All pairwise cosine distances in pure Python (math.fsum of products)."""
+    rows = [[float(v) for v in r] for r in E]
+    norms = [math.sqrt(math.fsum(v * v for v in r)) for r in rows]
+    n = len(rows)
+    return [[1.0 - math.fsum(a * b for a, b in zip(rows[i], rows[j])) / (norms[i] * norms[j])
+             for j in range(n)] for i in range(n)]
+
+
+def _farthest_first(dist: list[list[float]], start: int, L: int, excluded=()) -> list[int]:
+    """Gonzalez's farthest-first traversal recomputed from scratch each step:
+    the next point maximises its minimum distance to the chosen set."""
+    chosen = [start]
+    out = []
+    for _ in range(L):
+        best, best_c = -math.inf, -1
+        for c in range(len(dist)):
+            if c in chosen or c in excluded:
+                continue
+            r = min(dist[p][c] for p in chosen)
+            if r > best:
+                best, best_c = r, c
+        out.append(best_c)
+        chosen.append(best_c)
+    return out
+
+
+def _read_square4():
+    table, cases = None, []
+    with open(os.path.join(GOLDEN, "dseq_square4.txt")) as f:
+        for line in f:
+            if line.startswith("table"):
+                table = np.array([[float(v) for v in tok.split(",")] for tok in line.split()[1:]],
+                                 np.float32)
+            elif line.startswith("case"):
+                _, s, L, mask, picks, radius = line.split()
+                cases.append((int(s), int(L), None if mask == "-" else [int(v) for v in
+                                                                        mask.split(",")],
+                              [int(v) for v in picks.split(",")],
+                              [float(v) for v in radius.split(",")]))
+    return table, cases
+
+
+def _read_lattice():
+    out = []
+    with open(os.path.join(GOLDEN, "bmu_lattice.txt")) as f:
+        for line in f:
+            if line.startswith("sample"):
+                _, x, y, j, d = line.split()
+                out.append((float(x), float(y), int(j), float(d)))
+    return out
+
+
+def _lattice_codebook():
+    return np.array([[a, b] for a in range(-3, 4) for b in range(-3, 4)], np.float32)
+
+
+# --------------------------------------------------------------------------
+# pins for the diversity oracle
+
+
+def pins_dseq(lib) -> list[str]:
+    fails: list[str] = []
+
+    # 1. hand-worked 4-point example, and the same table with rows rescaled
+    #    (cosine distance ignores row length, so nothing may change).
+    table, cases = _read_square4()
+    for scale in (None, np.array([2.0, 0.5, 3.0, 7.0], np.float32)):
+        E = table if scale is None else table * scale[:, None]
+        for s, L, mask_list, picks, radius in cases:
+            mask = None
+            if mask_list is not None:
+                mask = np.zeros(4, np.uint8)
+                mask[mask_list] = 1
+            got, rad, st = oracle.dseq(E, [s], L, mask=mask, lib=lib)
+            if st != 0 or got[0].tolist() != picks:
+                fails.append(f"square4 start={s} scale={scale is not None}: {got[0].tolist()} != {picks}")
+            elif not np.allclose(rad[0], radius, atol=1e-12):
+                fails.append(f"square4 radius start={s}: {rad[0].tolist()} != {radius}")
+    # exhaustion: with row 2 masked only rows 1 and 3 remain after start 0
+    mask = np.zeros(4, np.uint8)
+    mask[2] = 1
+    _, _, st = oracle.dseq(table, [0], 3, mask=mask, lib=lib)
+    if st != -1:
+        fails.append("square4: exhaustion not reported")
+
+    # 2. orthonormal table: every distance between distinct rows is exactly 1,
+    #    so every pick is a tie and the picks are the ascending indices.
+    N = 11
+    E = np.eye(N, dtype=np.float32)
+    for s in (0, 4, 10):
+        for T in (0, 1, 2, 3, 5, N):
+            got, rad, st = oracle.dseq(E, [s], N - 1, tile=T, lib=lib)
+            want = [c for c in range(N) if c != s]
+            if st != 0 or got[0].tolist() != want:
+                fails.append(f"orthonormal start={s} T={T}: {got[0].tolist()}")
+            elif not np.all(rad[0] == 1.0):
+                fails.append(f"orthonormal radius start={s}")
+
+    # 3. duplicate rows: rows 3 and 5 equal (never a start), row 6 equals the
+    #    start row 0.  The first of {3, 5} picked must be 3; the start's
+    #    duplicate has distance ~0 and comes only after every row with a
+    #    positive distance.
+    rng = np.random.default_rng(7)
+    E = rng.standard_normal((8, 5)).astype(np.float32)
+    E[5] = E[3]
+    E[6] = E[0]
+    got, rad, st = oracle.dseq(E, [0], 7, lib=lib)
+    order = got[0].tolist()
+    if st != 0 or sorted(order) != list(range(1, 8)):
+        fails.append(f"duplicates: not a permutation {order}")
+    else:
+        if order.index(3) > order.index(5):
+            fails.append(f"duplicates: 5 before 3 in {order}")
+        if order[-1] != 6 and not (order[-1] == 5 and order[-2] == 6) \
+                and not (order[-2] == 5 and order[-1] == 6):
+            fails.append(f"duplicates: start duplicate not last {order}")
+        # the duplicate of a picked row is picked only at distance ~0
+        if abs(rad[0][order.index(6)]) > 1e-12:
+            fails.append("duplicates: start duplicate picked at positive distance")
+
+    # 4. associativity of max: a tiled scan equals one pass for every tile
+    #    size, including a last partial tile and tiles larger than N.
+    E = workloads.clustered_table(50, 8, n_centres=4, sigma=0.3, seed=3)
+    st0 = [0, 17, 33, 49]
+    mask = np.zeros(50, np.uint8)
+    mask[[5, 6, 40]] = 1
+    base, _, _ = oracle.dseq(E, st0, 20, mask=mask, tile=0, lib=lib)
+    for T in (1, 2, 7, 64, 49, 50, 55):
+        got, _, _ = oracle.dseq(E, st0, 20, mask=mask, tile=T, lib=lib)
+        if not np.array_equal(got, base):
+            fails.append(f"associativity: tile {T} differs from one pass")
+
+    # 5. brute force: farthest-first traversal from a full distance matrix
+    #    built by an independent routine, on tiny tables.
+    for seed, (n, d) in enumerate([(6, 3), (9, 4), (12, 7), (12, 2)]):
+        E = np.random.default_rng(100 + seed).standard_normal((n, d)).astype(np.float32)
+        dist = _brute_cosine_matrix(E)
+        for s in range(0, n, 3):
+            want = _farthest_first(dist, s, n - 1)
+            got, _, st = oracle.dseq(E, [s], n - 1, lib=lib)
+            if st != 0 or got[0].tolist() != want:
+                fails.append(f"brute force n={n} start={s}: {got[0].tolist()} != {want}")
+        excl = {1, n - 2}
+        mask = np.zeros(n, np.uint8)
+        mask[list(excl)] = 1
+        want = _farthest_first(dist, 0, n - 3, excluded=excl)
+        got, _, st = oracle.dseq(E, [0], n - 3, mask=mask, lib=lib)
+        if st != 0 or got[0].tolist() != want:
+            fails.append(f"brute force masked n={n}: {got[0].tolist()} != {want}")
+
+    # 6. invariants on a medium table, stepping the fold and argmax by hand:
+    #    the running minimum never grows, the radius of successive picks never
+    #    grows, picks are distinct, never masked, never the start; and the
+    #    full run equals the stepped run.
+    E = workloads.clustered_table(300, 16, n_centres=8, sigma=0.3, seed=5)
+    nrm = oracle.row_norms(E, lib=lib)
+    mask = np.zeros(300, np.uint8)
+    mask[::37] = 1
+    for s in (1, 150, 299):
+        m = np.full(300, np.inf)
+        masked = mask.copy()
+        masked[s] = 1
+        p, picks, radii = s, [], []
+        for t in range(40):
+            prev = m.copy()
+            oracle.fold(E, nrm, p, m, lib=lib)
+            if np.any(m > prev):
+                fails.append(f"invariant: m grew at t={t}")
+                break
+            w = oracle.argmax(m, masked, lib=lib)
+            if w < 0 or masked[w]:
+                fails.append(f"invariant: masked pick {w}")
+                break
+            picks.append(w)
+            radii.append(m[w])
+            masked[w] = 1
+            p = w
+        if any(radii[i + 1] > radii[i] for i in range(len(radii) - 1)):
+            fails.append(f"invariant: radius grew from start {s}")
+        got, rad, _ = oracle.dseq(E, [s], 40, mask=mask, lib=lib)
+        if got[0].tolist() != picks or not np.array_equal(rad[0], radii):
+            fails.append(f"invariant: full run differs from stepped run, start {s}")
+    return fails
+
+
+# --------------------------------------------------------------------------
+# pins for the BMU oracle
+
+
+def pins_bmu(lib) -> list[str]:
+    fails: list[str] = []
+
+    # 1. codebook containing the samples: distance 0 at the first matching
+    #    neuron; neurons 20 (= 17) and 33 (= 3) are duplicates of lower ones.
+    rng = np.random.default_rng(11)
+    W = rng.uniform(-1, 1, (40, 6)).astype(np.float32)
+    W[20] = W[17]
+    W[33] = W[3]
+    X = W[[5, 17, 20, 33, 3, 39]].copy()
+    idx, dist, second = oracle.bmu(X, W, lib=lib)
+    if idx.tolist() != [5, 17, 17, 3, 3, 39] or np.any(dist != 0.0):
+        fails.append(f"contained: {idx.tolist()} {dist.tolist()}")
+    if second[1] != 0.0 or second[0] <= 0.0:
+        fails.append(f"contained: second-best {second.tolist()}")
+
+    # 2. integer lattice codebook: the BMU is the nearest grid point, exact
+    #    halves go to the lower linear index.
+    W = _lattice_codebook()
+    cases = _read_lattice()
+    X = np.array([[x, y] for x, y, _, _ in cases], np.float32)
+    idx, dist, _ = oracle.bmu(X, W, lib=lib)
+    for (x, y, j, d), gi, gd in zip(cases, idx, dist):
+        if gi != j or abs(gd - d) > 1e-6:
+            fails.append(f"lattice ({x},{y}): {gi},{gd} != {j},{d}")
+
+    # 3. brute force against an independent argmin (numpy broadcasting,
+    #    first occurrence) on tiny random inputs.
+    for seed, (n, M, D) in enumerate([(7, 5, 3), (33, 64, 9), (64, 17, 64)]):
+        r = np.random.default_rng(200 + seed)
+        X = r.standard_normal((n, D)).astype(np.float32)
+        W = r.standard_normal((M, D)).astype(np.float32)
+        full = ((X[:, None, :].astype(np.float64) - W[None].astype(np.float64)) ** 2).sum(-1)
+        want = full.argmin(axis=1)
+        idx, dist, second = oracle.bmu(X, W, lib=lib)
+        srt = np.sort(full, axis=1)
+        if not np.array_equal(idx, want):
+            fails.append(f"brute bmu n={n} M={M}: idx differ")
+        elif not np.allclose(dist, full[np.arange(n), want], rtol=1e-12, atol=0):
+            fails.append(f"brute bmu n={n} M={M}: dist differ")
+        elif not np.allclose(second, srt[:, 1], rtol=1e-12, atol=0):
+            fails.append(f"brute bmu n={n} M={M}: second differ")
+        ii = np.repeat(np.arange(n), 2)
+        jj = np.tile([0, M - 1], n)
+        pairs = oracle.sqdist_pairs(X, W, ii, jj, lib=lib)
+        if not np.allclose(pairs, full[ii, jj], rtol=1e-12, atol=0):
+            fails.append(f"sqdist_pairs n={n} M={M} differ")
+    return fails
+
+
+# --------------------------------------------------------------------------
+
+
+def test_dseq_pins(oracle_lib):
+    assert pins_dseq(oracle_lib) == []
+
+
+def test_bmu_pins(oracle_lib):
+    assert pins_bmu(oracle_lib) == []
+
+
+def test_threads_and_parallel_equals_serial(oracle_lib):
+    assert oracle.threads(1) == 1
+    E = workloads.gaussian_table(200, 12, seed=9)
+    st = workloads.starts(200, 16, seed=9)
+    a, ra, _ = oracle.dseq(E, st, 25, threads=1)
+    b, rb, _ = oracle.dseq(E, st, 25, threads=4)
+    assert np.array_equal(a, b) and np.array_equal(ra, rb)
+    X = workloads.bmu_samples(50, 8, seed=1)
+    W = workloads.codebook(70, 8, seed=1)
+    assert all(np.array_equal(u, v) for u, v in zip(oracle.bmu(X, W, threads=1),
+                                                     oracle.bmu(X, W, threads=3)))
+
+
+# --------------------------------------------------------------------------
+# non-vacuity: plant one mistake in a copy of the oracle, on the CPU
+
+_SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "ties_to_highest": ("if (best_idx < 0 || m[c] > best) {",
+                        "if (best_idx < 0 || m[c] >= best) {", "dseq"),
+    "wrong_norm": ("return 1.0 - s / (nrm[p] * nrm[c]);",
+                   "return 1.0 - s / (nrm[p] * nrm[p]);", "dseq"),
+    "no_min_fold": ("if (d < m[c]) m[c] = d;", "m[c] = d;", "dseq"),
+    "reset_between_tiles": ("int64_t t1 = t0 + T < N ? t0 + T : N;",
+                            "int64_t t1 = t0 + T < N ? t0 + T : N; best_idx = -1;", "dseq"),
+    "start_unmasked": ("masked[p] = 1;\n        for", "masked[p] = 0;\n        for", "dseq"),
+    "pick_unmasked": ("masked[w] = 1;\n            p = w;", "p = w;", "dseq"),
+    "transposed_dot": ("s += (double)ep[k] * (double)ec[k];",
+                       "s += (double)ep[k] * (double)ec[(k + 1) % D];", "dseq"),
+    "diff_sign": ("double diff = (double)x[k] - (double)w[k];",
+                  "double diff = (double)x[k] + (double)w[k];", "bmu"),
+    "bmu_ties_to_highest": ("if (best_j < 0 || d < best) {",
+                            "if (best_j < 0 || d <= best) {", "bmu"),
+    "bmu_dropped_term": ("for (int32_t k = 0; k < D; ++k) {\n        double diff",
+                         "for (int32_t k = 1; k < D; ++k) {\n        double diff", "bmu"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_fails_a_pin(name, tmp_path):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    old, new, which = MUTANTS[name]
+    src = open(_SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mut = tmp_path / f"oracle_{name}.c"
+    mut.write_text(src.replace(old, new))
+    lib_path = str(tmp_path / f"liboracle_{name}.so")
+    oracle.compile_library(str(mut), lib_path)
+    lib = oracle.load(lib_path)
+    fails = pins_dseq(lib) if which == "dseq" else pins_bmu(lib)
+    assert fails, f"mutant {name} passed every pin"
