@@ -1,0 +1,422 @@
+"""Benchmark of the embedding similarity scan on GB300.
+
+One step = one full pass of the hot path over one batch of synthetic input:
+for the diversity workload, one ``dseq_run`` of B sequences x L iterations
+(every iteration: contraction, min-fold, masked argmax, commit) on a table
+already resident in HBM; for the BMU workload, one ``bmu_search`` of n
+samples against M neurons.
+
+Prints ONE JSON line (rank 0).  ``value`` is whole-job throughput
+(sequence-iterations/s, or samples/s) from CUDA events on the launching
+stream around each timed step, with the L2 flushed (a 512 MB write) between
+steps; ``e2e`` is the same metric through the C ABI with host buffers (the
+table upload, start/pick copies inside the timed region); ``roofline`` is the
+dominant kernel's algorithmic FLOP rate against the measured tensor peak;
+``cpu_baseline`` is the CPU oracle timed on a bounded sample on this host.
+
+``--impl reference`` times the CPU oracle itself as the reference arm.
+Multi-GPU (torchrun): every rank runs the full workload on its own GPU
+(independent replicas, weak scaling); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = {
+    "tc_dseq_kernel": ["tc_dseq.cu", "common.cuh", "internal.h"],
+    "tc_bmu_kernel": ["tc_bmu.cu", "common.cuh", "internal.h"],
+}
+
+
+def _peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "embedding_similarity_scan_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel source; else None."""
+    path = os.path.join(PROFILES, f"{kernel}.{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_traffic or m_hash.group(1) != _kernel_hash(kernel):
+        return None
+    return float(m_traffic.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [r.split(", ") for r in (self.out or "").strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for name, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+
+    cores = os.cpu_count() or 1
+    threads = oracle.threads(cores)
+    if args.workload in workloads.DIVERSITY:
+        cfg = workloads.DIVERSITY[args.workload]
+        E = cfg.table(seed=0)
+        starts = cfg.starts(seed=0)
+        nseq = args.ref_sample or max(1, min(cfg.B, threads))
+        sample = f"{nseq} of {cfg.B} sequences x the full L={cfg.L} per step"
+        unit = "sequence-iterations/s"
+        metric = "sequence-iterations/s"
+
+        def step(i):
+            sel = starts[(np.arange(nseq) + i * nseq) % cfg.B]
+            oracle.dseq(E, sel, cfg.L, threads=threads)
+            return nseq * cfg.L
+    else:
+        cfg = workloads.BMU[args.workload]
+        X = cfg.samples(seed=0)
+        W = cfg.codebook(seed=0)
+        nsamp = args.ref_sample or 4 * threads
+        sample = f"{nsamp} of {cfg.n} samples per step"
+        unit = "samples/s"
+        metric = "BMU samples/s"
+
+        def step(i):
+            lo = (i * nsamp) % cfg.n
+            oracle.bmu(X[lo:lo + nsamp], W, threads=threads)
+            return nsamp
+
+    for i in range(args.warmup):
+        step(i)
+    work = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        work += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = work / dt
+    line = {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def _cpu_baseline(args, cfg):
+    """The oracle as it stands, on all host cores, on a bounded sample."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    threads = oracle.threads(cores)
+    t_target = args.cpu_seconds
+    if isinstance(cfg, workloads.DiversityConfig):
+        E = cfg.table(seed=0)
+        starts = cfg.starts(seed=0)
+        # calibrate on one sequence per thread, then size the sample
+        n = threads
+        t0 = time.perf_counter()
+        oracle.dseq(E, starts[:n], cfg.L, threads=threads)
+        dt = time.perf_counter() - t0
+        reps = max(1, int(t_target / max(dt, 1e-3)) - 1)
+        n_total = n
+        t0 = time.perf_counter()
+        for r in range(reps):
+            sel = starts[(np.arange(n) + (r + 1) * n) % cfg.B]
+            oracle.dseq(E, sel, cfg.L, threads=threads)
+            n_total += n
+        dt2 = time.perf_counter() - t0
+        total_t, total_n = dt + dt2, n_total
+        return {"value": total_n * cfg.L / total_t, "unit": "sequence-iterations/s",
+                "cores": threads, "kind": "oracle",
+                "sample": f"{total_n} of {cfg.B} sequences x L={cfg.L} "
+                          f"({total_t:.1f} s of CPU work)"}
+    X = cfg.samples(seed=0)
+    W = cfg.codebook(seed=0)
+    n = 2 * threads
+    t0 = time.perf_counter()
+    oracle.bmu(X[:n], W, threads=threads)
+    dt = time.perf_counter() - t0
+    n2 = max(n, int(n * t_target / max(dt, 1e-3)))
+    t0 = time.perf_counter()
+    oracle.bmu(X[n:n + n2], W, threads=threads)
+    dt2 = time.perf_counter() - t0
+    return {"value": (n + n2) / (dt + dt2), "unit": "samples/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n + n2} of {cfg.n} samples ({dt + dt2:.1f} s of CPU work)"}
+
+
+def run_ours(args):
+    import torch
+
+    import embedding_similarity_scan_gb300 as es
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    es.load()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    bf16_peak, hbm_peak, peak_src = _peaks()
+    # fp32-equivalent tensor peak of the split contraction: three fp16 MMAs per
+    # fp32 multiply-add (fp16 and bf16 run at the same nominal rate)
+    split_peak = bf16_peak / 3.0
+
+    is_div = args.workload in workloads.DIVERSITY
+    if is_div:
+        cfg = workloads.DIVERSITY[args.workload]
+        E_host = torch.from_numpy(cfg.table(seed=0)).pin_memory()
+        starts_host = torch.from_numpy(cfg.starts(seed=0)).pin_memory()
+        ctx = es.dseq_create(E_host.to(dev))
+        starts_dev = starts_host.to(dev)
+        picks_dev = torch.empty((cfg.B, cfg.L), dtype=torch.int32, device=dev)
+        units = cfg.B * cfg.L
+        flop = 2.0 * cfg.N * cfg.D * cfg.B * cfg.L
+        stream_bytes = 8.0 * cfg.N * cfg.B * cfg.L  # running-minimum read + write
+        kernel_name = "tc_dseq_kernel"
+        metric, unit = "sequence-iterations/s", "sequence-iterations/s"
+
+        def step():
+            es.dseq_run(ctx, starts_dev, cfg.L, picks=picks_dev)
+            return es.dseq_last_stat("kernel_ns"), es.dseq_last_stat("launches")
+
+        def e2e_step():
+            picks_host = torch.empty((cfg.B, cfg.L), dtype=torch.int32).pin_memory()
+            c = es.dseq_create(E_host)
+            try:
+                es.dseq_run(c, starts_host, cfg.L, picks=picks_host)
+            finally:
+                c.close()
+            return E_host.numel() * 4 + starts_host.numel() * 4, picks_host.numel() * 4
+
+        config = {"workload": args.workload, "N": cfg.N, "D": cfg.D, "B": cfg.B, "L": cfg.L,
+                  "l2": "flushed between steps (512 MB write)"}
+    else:
+        cfg = workloads.BMU[args.workload]
+        X_host = torch.from_numpy(cfg.samples(seed=0)).pin_memory()
+        W_host = torch.from_numpy(cfg.codebook(seed=0)).pin_memory()
+        X_dev, W_dev = X_host.to(dev), W_host.to(dev)
+        idx_dev = torch.empty(cfg.n, dtype=torch.int32, device=dev)
+        dist_dev = torch.empty(cfg.n, dtype=torch.float32, device=dev)
+        units = cfg.n
+        flop = 2.0 * cfg.n * cfg.M * cfg.D
+        stream_bytes = None
+        kernel_name = "tc_bmu_kernel"
+        metric, unit = "BMU samples/s", "samples/s"
+
+        def step():
+            es.bmu_search(X_dev, W_dev, idx=idx_dev, dist=dist_dev)
+            return es.dseq_last_stat("kernel_ns"), es.dseq_last_stat("launches")
+
+        def e2e_step():
+            idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
+            dist_h = torch.empty(cfg.n, dtype=torch.float32).pin_memory()
+            es.bmu_search(X_host, W_host, idx=idx_h, dist=dist_h)
+            return (X_host.numel() + W_host.numel()) * 4, cfg.n * 8
+
+        config = {"workload": args.workload, "n": cfg.n, "M": cfg.M, "D": cfg.D,
+                  "l2": "flushed between steps (512 MB write)"}
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    kernel_ns, launches = [], 0
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            kns, nl = step()
+            ev[i][1].record(stream)
+            kernel_ns.append(kns)
+            launches += nl
+            flush.zero_()
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if pg is not None:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = ws * units * args.steps / (total_ms / 1e3)
+
+    # end to end through the C ABI with host buffers
+    e2e_steps = max(1, min(args.steps, 3))
+    e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        h2d, d2h = e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if pg is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = ws * units * e2e_steps / e2e_s
+
+    k_avg_s = statistics.mean(kernel_ns) / 1e9 if kernel_ns and min(kernel_ns) > 0 else None
+    achieved = flop / k_avg_s / 1e12 if k_avg_s else None
+    roof = {"bound": "tensor", "achieved": achieved, "peak": split_peak, "unit": "TFLOP/s",
+            "frac": (achieved / split_peak) if achieved else None,
+            "traffic": _profiled_traffic(kernel_name, args.workload),
+            "kernel": kernel_name,
+            "note": (f"achieved = algorithmic fp32-equivalent FLOP (2*{'N*D*B*L' if is_div else 'n*M*D'})"
+                     f" / kernel time (CUDA events on the launching stream); peak = {peak_src} "
+                     f"bf16 {bf16_peak:.1f} TFLOP/s / 3 (three fp16 MMAs per fp32 multiply-add)")}
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16x3-split (fp32-accurate), f32 accumulate",
+        "data": "synthetic", "config": config, "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches), "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    if stream_bytes is not None and k_avg_s:
+        line["min_distance_stream"] = {
+            "achieved_gbs": stream_bytes / k_avg_s / 1e9, "peak_gbs": hbm_peak,
+            "frac": stream_bytes / k_avg_s / 1e9 / hbm_peak,
+            "note": "running-minimum read+write bytes (8*B*N per iteration) / kernel time"}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(args, cfg)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if is_div:
+        ctx.close()
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="page1",
+                    choices=sorted(workloads.DIVERSITY) + sorted(workloads.BMU))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-sample", type=int, default=0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

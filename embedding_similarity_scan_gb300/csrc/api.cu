@@ -1,0 +1,686 @@
+// api.cu — the C ABI of libdseq.so: argument checks, pointer-kind detection
+// and staging, device workspace, tensor-map encoding, work planning, and the
+// launches of the kernels in tc_dseq.cu, tc_bmu.cu, ffma.cu and prep.cu.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/dseq.h"
+#include "internal.h"
+
+using namespace dseq;
+
+namespace {
+
+// --------------------------------------------------------------------------
+// errors and statistics (per calling thread)
+thread_local std::string g_err;
+struct Stats {
+    int64_t units = 0, tile_n = 0, grid = 0, launches = 0, kernel_ns = 0;
+};
+thread_local Stats g_stats;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_code(cudaError_t e) {
+    return e == cudaErrorMemoryAllocation ? DSEQ_ENOMEM
+           : (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorLaunchOutOfResources)
+               ? DSEQ_ELAUNCH
+               : DSEQ_ECUDA;
+}
+
+#define CUDA_TRY(expr)                                                                        \
+    do {                                                                                      \
+        cudaError_t e_ = (expr);                                                              \
+        if (e_ != cudaSuccess) {                                                              \
+            cudaGetLastError();                                                               \
+            return fail(cuda_code(e_), "%s failed: %s (%s:%d)", #expr, cudaGetErrorString(e_), \
+                        __FILE__, __LINE__);                                                  \
+        }                                                                                     \
+    } while (0)
+
+#define TRY(expr)              \
+    do {                       \
+        int r_ = (expr);       \
+        if (r_ != DSEQ_OK) return r_; \
+    } while (0)
+
+// --------------------------------------------------------------------------
+// options
+struct Options {
+    int64_t engine = 0;
+    int64_t tile_n = 0;
+    int64_t grid = 0;
+    int64_t timeout_ms = 10000;
+    int64_t fault_skip_arrive = 0;
+};
+std::mutex g_opt_mu;
+Options g_defaults;
+
+int set_opt(Options &o, const char *name, int64_t v) {
+    if (!name) return fail(DSEQ_EINVAL, "option name is NULL");
+    const std::string n(name);
+    if (n == "engine") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "engine must be 0 or 1");
+        o.engine = v;
+    } else if (n == "tile_n") {
+        if (v != 0 && (v < 32 || v > 256 || v % 32)) return fail(DSEQ_EINVAL, "tile_n must be 0 or a multiple of 32 in [32, 256]");
+        o.tile_n = v;
+    } else if (n == "grid") {
+        if (v < 0 || v > 65535) return fail(DSEQ_EINVAL, "grid out of range");
+        o.grid = v;
+    } else if (n == "timeout_ms") {
+        if (v < 1 || v > 3600000) return fail(DSEQ_EINVAL, "timeout_ms out of range");
+        o.timeout_ms = v;
+    } else if (n == "fault_skip_arrive") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "fault_skip_arrive must be 0 or 1");
+        o.fault_skip_arrive = v;
+    } else {
+        return fail(DSEQ_EINVAL, "unknown option '%s'", name);
+    }
+    return DSEQ_OK;
+}
+
+int64_t get_opt(const Options &o, const char *name) {
+    if (!name) return -1;
+    const std::string n(name);
+    if (n == "engine") return o.engine;
+    if (n == "tile_n") return o.tile_n;
+    if (n == "grid") return o.grid;
+    if (n == "timeout_ms") return o.timeout_ms;
+    if (n == "fault_skip_arrive") return o.fault_skip_arrive;
+    return -1;
+}
+
+// --------------------------------------------------------------------------
+// device memory helpers
+struct DevBuf {
+    void *p = nullptr;
+    size_t bytes = 0;
+    int ensure(size_t n) {
+        if (n <= bytes) return DSEQ_OK;
+        release();
+        cudaError_t e = cudaMalloc(&p, n);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            p = nullptr;
+            return fail(DSEQ_ENOMEM, "cudaMalloc of %zu bytes failed: %s", n, cudaGetErrorString(e));
+        }
+        bytes = n;
+        return DSEQ_OK;
+    }
+    void release() {
+        if (p) cudaFree(p);
+        p = nullptr;
+        bytes = 0;
+    }
+    template <class T>
+    T *as() const {
+        return static_cast<T *>(p);
+    }
+};
+
+bool is_device_ptr(const void *p) {
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// input array: the device pointer itself, or a staged device copy of host data
+template <class T>
+int stage_in(const T *src, size_t count, DevBuf &buf, const T *&dev, cudaStream_t st) {
+    if (is_device_ptr(src)) {
+        dev = src;
+        return DSEQ_OK;
+    }
+    TRY(buf.ensure(count * sizeof(T)));
+    CUDA_TRY(cudaMemcpyAsync(buf.p, src, count * sizeof(T), cudaMemcpyHostToDevice, st));
+    dev = buf.as<T>();
+    return DSEQ_OK;
+}
+
+// host copy of a small argument array (for validation)
+template <class T>
+int to_host(const T *src, size_t count, std::vector<T> &out, cudaStream_t st) {
+    out.resize(count);
+    if (count == 0) return DSEQ_OK;
+    if (is_device_ptr(src)) {
+        CUDA_TRY(cudaMemcpyAsync(out.data(), src, count * sizeof(T), cudaMemcpyDeviceToHost, st));
+        CUDA_TRY(cudaStreamSynchronize(st));
+    } else {
+        std::memcpy(out.data(), src, count * sizeof(T));
+    }
+    return DSEQ_OK;
+}
+
+struct DeviceInfo {
+    int sms = 0, l2 = 0;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+int device_info(int dev, DeviceInfo &info) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev < 0 || dev >= 64) return fail(DSEQ_ECUDA, "device ordinal %d out of range", dev);
+    if (g_dev[dev].sms == 0) {
+        CUDA_TRY(cudaDeviceGetAttribute(&g_dev[dev].sms, cudaDevAttrMultiProcessorCount, dev));
+        CUDA_TRY(cudaDeviceGetAttribute(&g_dev[dev].l2, cudaDevAttrL2CacheSize, dev));
+    }
+    info = g_dev[dev];
+    return DSEQ_OK;
+}
+
+// --------------------------------------------------------------------------
+// tensor maps (driver entry point fetched at run time: no link against libcuda)
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encoder(EncodeTiledFn &fn) {
+    static std::mutex mu;
+    static EncodeTiledFn cached = nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cached) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                  cudaEnableDefault, &q));
+        if (q != cudaDriverEntryPointSuccess || !p)
+            return fail(DSEQ_ECUDA, "cuTensorMapEncodeTiled entry point not found");
+        cached = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    fn = cached;
+    return DSEQ_OK;
+}
+
+// 2-D fp16 map over a row-major [rows][cols] buffer, box = 32 columns (64 B,
+// 64-byte swizzle) x box_rows rows; out-of-range rows read as zero.
+int encode_f16_map(CUtensorMap &map, const void *base, int64_t cols, int64_t rows, int box_rows) {
+    EncodeTiledFn fn;
+    TRY(get_encoder(fn));
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kKBlock, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DSEQ_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return DSEQ_OK;
+}
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Candidate columns per unit: the multiple of 32 in [32, 256] that minimises
+// the makespan ceil(units / grid) * (tile_n + 64), the 64 standing for the
+// fixed cost of a unit (pipeline refill, epilogue drain, key atomics);
+// ties go to the wider tile.
+int choose_tile_n(int64_t n_rows_blocks, int64_t ncols, int grid) {
+    int best = 256;
+    int64_t best_cost = INT64_MAX;
+    for (int tn = 256; tn >= 32; tn -= 32) {
+        const int64_t units = n_rows_blocks * ((ncols + tn - 1) / tn);
+        const int64_t rounds = (units + grid - 1) / grid;
+        const int64_t cost = rounds * (tn + 64);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = tn;
+        }
+    }
+    return best;
+}
+
+int read_status(int *status_dev, cudaStream_t st) {
+    int s = 0;
+    CUDA_TRY(cudaMemcpyAsync(&s, status_dev, sizeof(int), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(cudaStreamSynchronize(st));
+    if (s == 0) return DSEQ_OK;
+    if (s & kStatusNonFinite) return fail(DSEQ_ENONFINITE, "non-finite value or zero-norm row in input");
+    if (s & (kStatusBarrierTimeout | kStatusPipeTimeout))
+        return fail(DSEQ_ETIMEOUT, "device wait timed out (status 0x%x)", s);
+    return fail(DSEQ_EINTERNAL, "device consistency check failed (status 0x%x)", s);
+}
+
+struct EventTimer {
+    cudaEvent_t a = nullptr, b = nullptr;
+    ~EventTimer() {
+        if (a) cudaEventDestroy(a);
+        if (b) cudaEventDestroy(b);
+    }
+    int start(cudaStream_t st) {
+        CUDA_TRY(cudaEventCreate(&a));
+        CUDA_TRY(cudaEventCreate(&b));
+        CUDA_TRY(cudaEventRecord(a, st));
+        return DSEQ_OK;
+    }
+    int stop(cudaStream_t st) {
+        CUDA_TRY(cudaEventRecord(b, st));
+        return DSEQ_OK;
+    }
+    int64_t ns() {
+        float ms = 0.f;
+        if (!a || !b || cudaEventElapsedTime(&ms, a, b) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return (int64_t)(ms * 1.0e6);
+    }
+};
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+struct dseq_ctx {
+    int device = 0;
+    int64_t N = 0;
+    int32_t D = 0, Dp = 0;
+    Options opt;
+    DevBuf e_unit, e_split;
+    // run workspace
+    DevBuf m, keys, q, status, barrier, starts, mask, picks, trace_slot;
+    ~dseq_ctx() {
+        DevBuf *all[] = {&e_unit, &e_split, &m,     &keys,  &q,          &status,
+                         &barrier, &starts, &mask, &picks, &trace_slot};
+        for (DevBuf *b : all) b->release();
+    }
+};
+
+extern "C" {
+
+const char *dseq_last_error(void) { return g_err.c_str(); }
+
+int64_t dseq_last_stat(const char *name) {
+    if (!name) return -1;
+    const std::string n(name);
+    if (n == "units") return g_stats.units;
+    if (n == "tile_n") return g_stats.tile_n;
+    if (n == "grid") return g_stats.grid;
+    if (n == "launches") return g_stats.launches;
+    if (n == "kernel_ns") return g_stats.kernel_ns;
+    return -1;
+}
+
+int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value) {
+    g_err.clear();
+    if (ctx) return set_opt(ctx->opt, name, value);
+    std::lock_guard<std::mutex> lk(g_opt_mu);
+    return set_opt(g_defaults, name, value);
+}
+
+int64_t dseq_get_option(dseq_ctx *ctx, const char *name) {
+    if (ctx) return get_opt(ctx->opt, name);
+    std::lock_guard<std::mutex> lk(g_opt_mu);
+    return get_opt(g_defaults, name);
+}
+
+int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device, void *cuda_stream,
+                dseq_ctx **out) {
+    (void)table_on_device;
+    g_err.clear();
+    if (!out) return fail(DSEQ_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (!table) return fail(DSEQ_EINVAL, "table is NULL");
+    if (N < 1 || N >= (int64_t(1) << 31)) return fail(DSEQ_EINVAL, "N=%lld out of range", (long long)N);
+    if (D < 1 || D > 16384) return fail(DSEQ_EINVAL, "D=%d out of range", D);
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    dseq_ctx *ctx = new dseq_ctx();
+    {
+        std::lock_guard<std::mutex> lk(g_opt_mu);
+        ctx->opt = g_defaults;
+    }
+    auto bail = [&](int code) {
+        delete ctx;
+        return code;
+    };
+    cudaError_t e = cudaGetDevice(&ctx->device);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete ctx;
+        return fail(DSEQ_ECUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    }
+    ctx->N = N;
+    ctx->D = D;
+    ctx->Dp = (int32_t)round_up(D, kKBlock);
+    int r;
+    if ((r = ctx->e_unit.ensure((size_t)N * ctx->Dp * sizeof(float))) != DSEQ_OK) return bail(r);
+    if ((r = ctx->e_split.ensure((size_t)N * 2 * ctx->Dp * sizeof(__half))) != DSEQ_OK) return bail(r);
+    if ((r = ctx->status.ensure(sizeof(int))) != DSEQ_OK) return bail(r);
+    DevBuf staged;
+    const float *tdev = nullptr;
+    if ((r = stage_in(table, (size_t)N * D, staged, tdev, st)) != DSEQ_OK) return bail(r);
+    e = cudaMemsetAsync(ctx->status.p, 0, sizeof(int), st);
+    if (e == cudaSuccess) {
+        launch_table_prepare(tdev, N, D, ctx->Dp, ctx->e_unit.as<float>(),
+                             ctx->e_split.as<__half>(), ctx->status.as<int>(), st);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return bail(fail(cuda_code(e), "table preparation failed: %s", cudaGetErrorString(e)));
+    }
+    if ((r = read_status(ctx->status.as<int>(), st)) != DSEQ_OK) return bail(r);
+    staged.release();
+    *out = ctx;
+    return DSEQ_OK;
+}
+
+void dseq_destroy(dseq_ctx *ctx) { delete ctx; }
+
+static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
+                    const uint8_t *mask, int32_t *picks, const int32_t *trace_seqs,
+                    int32_t n_trace, float *trace_mindist, void *cuda_stream) {
+    g_err.clear();
+    g_stats = Stats();
+    if (!ctx) return fail(DSEQ_EINVAL, "ctx is NULL");
+    if (!starts) return fail(DSEQ_EINVAL, "starts is NULL");
+    if (!picks && L > 0) return fail(DSEQ_EINVAL, "picks is NULL");
+    if (B < 1) return fail(DSEQ_EINVAL, "B=%d must be >= 1", B);
+    if (L < 0) return fail(DSEQ_EINVAL, "L=%d must be >= 0", L);
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    int cur = -1;
+    CUDA_TRY(cudaGetDevice(&cur));
+    if (cur != ctx->device) return fail(DSEQ_EINVAL, "context belongs to device %d, current is %d", ctx->device, cur);
+    const int64_t N = ctx->N;
+
+    // ---- validate on the host ----
+    std::vector<int32_t> h_starts;
+    TRY(to_host(starts, (size_t)B, h_starts, st));
+    std::vector<uint8_t> h_mask;
+    if (mask) TRY(to_host(mask, (size_t)N, h_mask, st));
+    {
+        std::vector<uint8_t> seen((size_t)N, 0);
+        int64_t n_masked = 0;
+        if (mask)
+            for (int64_t c = 0; c < N; ++c) n_masked += h_mask[c] != 0;
+        for (int32_t b = 0; b < B; ++b) {
+            const int32_t s = h_starts[b];
+            if (s < 0 || s >= N) return fail(DSEQ_EINVAL, "starts[%d]=%d out of range [0, %lld)", b, s, (long long)N);
+            if (seen[s]) return fail(DSEQ_EINVAL, "start %d repeated", s);
+            seen[s] = 1;
+            const int64_t avail = N - n_masked - ((mask && h_mask[s]) ? 0 : 1);
+            if (L > avail) return fail(DSEQ_EINVAL, "L=%d exceeds the %lld candidates left to sequence %d", L, (long long)avail, b);
+        }
+    }
+    std::vector<int32_t> h_slot;
+    const int64_t Bp = round_up(B, kUnitRows);
+    if (n_trace > 0) {
+        if (!trace_seqs || !trace_mindist) return fail(DSEQ_EINVAL, "trace arrays are NULL");
+        if (!is_device_ptr(trace_mindist)) return fail(DSEQ_EINVAL, "trace_mindist must be device memory");
+        std::vector<int32_t> h_tr;
+        TRY(to_host(trace_seqs, (size_t)n_trace, h_tr, st));
+        h_slot.assign((size_t)Bp, -1);
+        for (int32_t k = 0; k < n_trace; ++k) {
+            const int32_t b = h_tr[k];
+            if (b < 0 || b >= B || h_slot[b] >= 0) return fail(DSEQ_EINVAL, "trace_seqs[%d]=%d invalid or repeated", k, b);
+            h_slot[b] = k;
+        }
+    } else if (n_trace < 0) {
+        return fail(DSEQ_EINVAL, "n_trace < 0");
+    }
+    if (L == 0) return DSEQ_OK;
+
+    // ---- stage the small inputs and outputs ----
+    TRY(ctx->starts.ensure((size_t)B * sizeof(int32_t)));
+    CUDA_TRY(cudaMemcpyAsync(ctx->starts.p, h_starts.data(), (size_t)B * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+    const uint8_t *d_mask = nullptr;
+    if (mask) {
+        TRY(ctx->mask.ensure((size_t)N));
+        CUDA_TRY(cudaMemcpyAsync(ctx->mask.p, h_mask.data(), (size_t)N, cudaMemcpyHostToDevice, st));
+        d_mask = ctx->mask.as<uint8_t>();
+    }
+    const int32_t *d_slot = nullptr;
+    if (n_trace > 0) {
+        TRY(ctx->trace_slot.ensure((size_t)Bp * sizeof(int32_t)));
+        CUDA_TRY(cudaMemcpyAsync(ctx->trace_slot.p, h_slot.data(), (size_t)Bp * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+        d_slot = ctx->trace_slot.as<int32_t>();
+    }
+    const bool picks_on_dev = is_device_ptr(picks);
+    int32_t *d_picks = picks;
+    if (!picks_on_dev) {
+        TRY(ctx->picks.ensure((size_t)B * L * sizeof(int32_t)));
+        d_picks = ctx->picks.as<int32_t>();
+    }
+    TRY(ctx->keys.ensure((size_t)Bp * sizeof(unsigned long long)));
+    TRY(ctx->barrier.ensure(sizeof(unsigned)));
+    CUDA_TRY(cudaMemsetAsync(ctx->status.p, 0, sizeof(int), st));
+
+    DeviceInfo info;
+    TRY(device_info(ctx->device, info));
+    EventTimer timer;
+
+    if (ctx->opt.engine == 0) {
+        // ---- tensor-core persistent kernel ----
+        TcPlan plan;
+        plan.n_beta = (int)(Bp / kUnitRows);
+        const int grid_cap = ctx->opt.grid > 0 ? (int)std::min<int64_t>(ctx->opt.grid, info.sms) : info.sms;
+        plan.tile_n = ctx->opt.tile_n > 0 ? (int)ctx->opt.tile_n : choose_tile_n(plan.n_beta, N, grid_cap);
+        plan.n_chunk = (int)((N + plan.tile_n - 1) / plan.tile_n);
+        plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
+        TRY(ctx->m.ensure((size_t)plan.units() * kUnitRows * plan.tile_n * sizeof(float)));
+        TRY(ctx->q.ensure((size_t)Bp * 3 * ctx->Dp * sizeof(__half)));
+        CUtensorMap tq, te;
+        TRY(encode_f16_map(tq, ctx->q.p, 3 * ctx->Dp, Bp, kUnitRows));
+        TRY(encode_f16_map(te, ctx->e_split.p, 2 * ctx->Dp, N, plan.tile_n));
+        TcDseqArgs a;
+        a.e_split = ctx->e_split.as<__half>();
+        a.q_split = ctx->q.as<__half>();
+        a.m = ctx->m.as<float>();
+        a.keys = ctx->keys.as<unsigned long long>();
+        a.picks = d_picks;
+        a.trace_slot = d_slot;
+        a.trace = trace_mindist;
+        a.status = ctx->status.as<int>();
+        a.barrier = ctx->barrier.as<unsigned>();
+        a.N = N;
+        a.B = B;
+        a.L = L;
+        a.Dp = ctx->Dp;
+        a.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
+        a.fault_skip_arrive = (int)ctx->opt.fault_skip_arrive;
+        CUDA_TRY(cudaMemsetAsync(ctx->barrier.p, 0, sizeof(unsigned), st));
+        launch_tc_dseq_init(a, plan, ctx->starts.as<int32_t>(), d_mask, st);
+        CUDA_TRY(cudaGetLastError());
+        TRY(timer.start(st));
+        CUDA_TRY(launch_tc_dseq(a, plan, tq, te, st));
+        TRY(timer.stop(st));
+        g_stats.units = plan.units();
+        g_stats.tile_n = plan.tile_n;
+        g_stats.grid = plan.grid;
+        g_stats.launches = 2;
+    } else {
+        // ---- FP32 FFMA path, one launch pair per iteration ----
+        FfmaDseqArgs a;
+        a.Nf = round_up(N, 64);
+        a.Bp = (int)Bp;
+        TRY(ctx->m.ensure((size_t)Bp * a.Nf * sizeof(float)));
+        TRY(ctx->q.ensure((size_t)Bp * ctx->Dp * sizeof(float)));
+        a.e_unit = ctx->e_unit.as<float>();
+        a.q = ctx->q.as<float>();
+        a.m = ctx->m.as<float>();
+        a.keys = ctx->keys.as<unsigned long long>();
+        a.picks = d_picks;
+        a.trace_slot = d_slot;
+        a.trace = trace_mindist;
+        a.status = ctx->status.as<int>();
+        a.N = N;
+        a.B = B;
+        a.L = L;
+        a.Dp = ctx->Dp;
+        launch_ffma_dseq_init(a, ctx->starts.as<int32_t>(), d_mask, st);
+        CUDA_TRY(cudaGetLastError());
+        TRY(timer.start(st));
+        for (int t = 0; t < L; ++t) launch_ffma_dseq_iteration(a, t, st);
+        CUDA_TRY(cudaGetLastError());
+        TRY(timer.stop(st));
+        g_stats.units = (Bp / 64) * (a.Nf / 64);
+        g_stats.tile_n = 64;
+        g_stats.grid = (int64_t)g_stats.units;
+        g_stats.launches = 1 + 2 * (int64_t)L;
+    }
+    TRY(read_status(ctx->status.as<int>(), st));
+    g_stats.kernel_ns = timer.ns();
+    if (!picks_on_dev) {
+        CUDA_TRY(cudaMemcpyAsync(picks, d_picks, (size_t)B * L * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+        CUDA_TRY(cudaStreamSynchronize(st));
+    }
+    return DSEQ_OK;
+}
+
+int dseq_run(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L, const uint8_t *mask,
+             int32_t *picks, void *cuda_stream) {
+    return run_impl(ctx, starts, B, L, mask, picks, nullptr, 0, nullptr, cuda_stream);
+}
+
+int dseq_run_trace(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
+                   const uint8_t *mask, int32_t *picks, const int32_t *trace_seqs,
+                   int32_t n_trace, float *trace_mindist, void *cuda_stream) {
+    if (n_trace < 1) return fail(DSEQ_EINVAL, "n_trace must be >= 1");
+    return run_impl(ctx, starts, B, L, mask, picks, trace_seqs, n_trace, trace_mindist,
+                    cuda_stream);
+}
+
+// ----------------------------------------------------------------------------
+// BMU: stateless entry point; its workspace is kept per device between calls.
+namespace {
+struct BmuWorkspace {
+    std::mutex mu;
+    DevBuf x_split, w_split, xn, wn, x_inv, w_inv, keys, status, x_stage, w_stage, idx_out, dist_out;
+};
+std::mutex g_bmu_mu;
+BmuWorkspace *g_bmu[64] = {};
+}  // namespace
+
+int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, int32_t *idx,
+               float *dist, void *cuda_stream) {
+    g_err.clear();
+    g_stats = Stats();
+    if (!X || !W || !idx || !dist) return fail(DSEQ_EINVAL, "NULL pointer argument");
+    if (n < 1 || n >= (int64_t(1) << 31)) return fail(DSEQ_EINVAL, "n=%lld out of range", (long long)n);
+    if (M < 1 || M >= (int64_t(1) << 31)) return fail(DSEQ_EINVAL, "M=%lld out of range", (long long)M);
+    if (D < 1 || D > 16384) return fail(DSEQ_EINVAL, "D=%d out of range", D);
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(DSEQ_ECUDA, "device ordinal out of range");
+    Options opt;
+    {
+        std::lock_guard<std::mutex> lk(g_opt_mu);
+        opt = g_defaults;
+    }
+    BmuWorkspace *ws;
+    {
+        std::lock_guard<std::mutex> lk(g_bmu_mu);
+        if (!g_bmu[dev]) g_bmu[dev] = new BmuWorkspace();
+        ws = g_bmu[dev];
+    }
+    std::lock_guard<std::mutex> lk(ws->mu);
+    DeviceInfo info;
+    TRY(device_info(dev, info));
+    const float *dX, *dW;
+    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st));
+    TRY(stage_in(W, (size_t)M * D, ws->w_stage, dW, st));
+    const bool idx_dev = is_device_ptr(idx), dist_dev = is_device_ptr(dist);
+    int32_t *d_idx = idx;
+    float *d_dist = dist;
+    if (!idx_dev) {
+        TRY(ws->idx_out.ensure((size_t)n * sizeof(int32_t)));
+        d_idx = ws->idx_out.as<int32_t>();
+    }
+    if (!dist_dev) {
+        TRY(ws->dist_out.ensure((size_t)n * sizeof(float)));
+        d_dist = ws->dist_out.as<float>();
+    }
+    const int Dp = (int)round_up(D, kKBlock);
+    TRY(ws->xn.ensure((size_t)n * sizeof(float)));
+    TRY(ws->wn.ensure((size_t)M * sizeof(float)));
+    TRY(ws->keys.ensure((size_t)n * sizeof(unsigned long long)));
+    TRY(ws->status.ensure(sizeof(int)));
+    CUDA_TRY(cudaMemsetAsync(ws->status.p, 0, sizeof(int), st));
+    BmuArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.X = dX;
+    a.W = dW;
+    a.xn = ws->xn.as<float>();
+    a.wn = ws->wn.as<float>();
+    a.keys = ws->keys.as<unsigned long long>();
+    a.idx = d_idx;
+    a.dist = d_dist;
+    a.status = ws->status.as<int>();
+    a.n = n;
+    a.M = M;
+    a.D = D;
+    a.Dp = Dp;
+    a.timeout_ns = (uint64_t)opt.timeout_ms * 1000000ull;
+    EventTimer timer;
+    launch_bmu_keys_init(a.keys, n, st);
+    if (opt.engine == 0) {
+        TRY(ws->x_split.ensure((size_t)n * 3 * Dp * sizeof(__half)));
+        TRY(ws->w_split.ensure((size_t)M * 2 * Dp * sizeof(__half)));
+        TRY(ws->x_inv.ensure((size_t)n * sizeof(float)));
+        TRY(ws->w_inv.ensure((size_t)M * sizeof(float)));
+        a.x_split = ws->x_split.as<__half>();
+        a.w_split = ws->w_split.as<__half>();
+        a.x_inv_scale = ws->x_inv.as<float>();
+        a.w_inv_scale = ws->w_inv.as<float>();
+        launch_bmu_prepare(dX, n, D, Dp, 1, ws->x_split.as<__half>(), ws->xn.as<float>(),
+                           ws->x_inv.as<float>(), a.status, st);
+        launch_bmu_prepare(dW, M, D, Dp, 0, ws->w_split.as<__half>(), ws->wn.as<float>(),
+                           ws->w_inv.as<float>(), a.status, st);
+        CUDA_TRY(cudaGetLastError());
+        TcPlan plan;
+        plan.n_beta = (int)((n + kUnitRows - 1) / kUnitRows);
+        const int grid_cap = opt.grid > 0 ? (int)std::min<int64_t>(opt.grid, info.sms) : info.sms;
+        plan.tile_n = opt.tile_n > 0 ? (int)opt.tile_n : 256;
+        plan.n_chunk = (int)((M + plan.tile_n - 1) / plan.tile_n);
+        plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
+        CUtensorMap tx, tw;
+        TRY(encode_f16_map(tx, a.x_split, 3 * Dp, n, kUnitRows));
+        TRY(encode_f16_map(tw, a.w_split, 2 * Dp, M, plan.tile_n));
+        TRY(timer.start(st));
+        CUDA_TRY(launch_tc_bmu(a, plan, tx, tw, st));
+        TRY(timer.stop(st));
+        g_stats.units = plan.units();
+        g_stats.tile_n = plan.tile_n;
+        g_stats.grid = plan.grid;
+        g_stats.launches = 5;
+    } else {
+        launch_row_sqnorm(dX, n, D, ws->xn.as<float>(), a.status, st);
+        launch_row_sqnorm(dW, M, D, ws->wn.as<float>(), a.status, st);
+        CUDA_TRY(cudaGetLastError());
+        TRY(timer.start(st));
+        launch_ffma_bmu(a, st);
+        CUDA_TRY(cudaGetLastError());
+        TRY(timer.stop(st));
+        g_stats.units = ((n + 63) / 64) * ((M + 63) / 64);
+        g_stats.tile_n = 64;
+        g_stats.grid = g_stats.units;
+        g_stats.launches = 5;
+    }
+    launch_bmu_finalize(a, st);
+    CUDA_TRY(cudaGetLastError());
+    TRY(read_status(a.status, st));
+    g_stats.kernel_ns = timer.ns();
+    if (!idx_dev) CUDA_TRY(cudaMemcpyAsync(idx, d_idx, (size_t)n * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    if (!dist_dev) CUDA_TRY(cudaMemcpyAsync(dist, d_dist, (size_t)n * sizeof(float), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(cudaStreamSynchronize(st));
+    return DSEQ_OK;
+}
+
+}  // extern "C"

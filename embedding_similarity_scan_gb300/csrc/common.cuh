@@ -1,0 +1,270 @@
+// common.cuh — device helpers shared by the kernels of libdseq.so:
+// order-preserving (value, index) keys, the device status word, bounded
+// waits, and the inline-PTX wrappers for mbarriers, TMA and tcgen05.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace dseq {
+
+// ---------------------------------------------------------------------------
+// (value, index) keys.  A float maps to a uint32 whose unsigned order is the
+// float order (-inf lowest, +inf highest).  Max keys put ~index in the low
+// half so that u64 max = (largest value, then lowest index); min keys put the
+// index itself so that u64 min = (smallest value, then lowest index).
+__host__ __device__ __forceinline__ uint32_t float_order(float f) {
+    uint32_t u;
+#ifdef __CUDA_ARCH__
+    u = __float_as_uint(f);
+#else
+    union { float f; uint32_t u; } cv;
+    cv.f = f;
+    u = cv.u;
+#endif
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__host__ __device__ __forceinline__ float float_unorder(uint32_t k) {
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+#ifdef __CUDA_ARCH__
+    return __uint_as_float(u);
+#else
+    union { float f; uint32_t u; } cv;
+    cv.u = u;
+    return cv.f;
+#endif
+}
+__host__ __device__ __forceinline__ unsigned long long max_key(float v, uint32_t idx) {
+    return ((unsigned long long)float_order(v) << 32) | (unsigned long long)(0xffffffffu - idx);
+}
+__host__ __device__ __forceinline__ uint32_t max_key_index(unsigned long long k) {
+    return 0xffffffffu - (uint32_t)(k & 0xffffffffull);
+}
+__host__ __device__ __forceinline__ unsigned long long min_key(float v, uint32_t idx) {
+    return ((unsigned long long)float_order(v) << 32) | (unsigned long long)idx;
+}
+
+// ---------------------------------------------------------------------------
+// time and bounded waiting
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ int ld_volatile(const int *p) {
+    return *reinterpret_cast<const volatile int *>(p);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses and mbarriers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// after timeout_ns (setting `code` in the status word and the CTA's abort
+// flag) or as soon as the abort flag is already set.  Returns true when the
+// phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort_flag, int *status,
+                                                  uint64_t timeout_ns, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((spin & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
+            atomicOr(status, code);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tiled tensor copies, global -> shared, completion on an mbarrier)
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory, MMA, commit, loads
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 inputs, fp32 accumulator).
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 consecutive 32-bit columns of the calling thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile whose rows are
+// 64 bytes (32 fp16) long, written by TMA with the 64-byte swizzle: core
+// matrices of 8 rows x 64 bytes, 512 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3ffffu) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                    // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(512u >> 4) << 32;          // stride byte offset: 8 rows x 64 B
+    d |= (uint64_t)1 << 46;                    // descriptor version
+    d |= (uint64_t)4 << 61;                    // layout: 64-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with fp16 A and B (both K-major) and an
+// fp32 accumulator of M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+    return (1u << 4)             // D format: f32
+           | (0u << 7)           // A format: f16
+           | (0u << 10)          // B format: f16
+           | ((N >> 3) << 17)    // N / 8
+           | ((M >> 4) << 24);   // M / 16
+}
+
+// ---------------------------------------------------------------------------
+// grid-wide barrier over all CTAs of a co-resident (cooperative) launch.
+// `counter` grows monotonically within one launch; the k-th barrier (k = 0,
+// 1, ...) completes when it reaches (k + 1) * gridDim.x.  Every CTA calls it
+// with all its threads.  Returns false (and sets the abort flag) if the
+// status word is already set or the wait ran out.
+__device__ __forceinline__ bool grid_barrier(unsigned *counter, unsigned target, int *status,
+                                             volatile int *abort_flag, uint64_t timeout_ns,
+                                             bool skip_arrive) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        fence_proxy_async_global();
+        __threadfence();
+        if (!skip_arrive) red_release_gpu_add(counter, 1u);
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t spin = 0;; ++spin) {
+            if (ld_acquire_gpu(counter) >= target) break;
+            if (ld_volatile(status) != 0) {
+                *abort_flag = 1;
+                break;
+            }
+            if ((spin & 31u) == 31u && globaltimer_ns() - t0 > timeout_ns) {
+                atomicOr(status, kStatusBarrierTimeout);
+                *abort_flag = 1;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+        fence_proxy_async_global();
+    }
+    __syncthreads();
+    return *abort_flag == 0;
+}
+
+}  // namespace dseq

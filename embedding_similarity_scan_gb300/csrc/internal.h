@@ -1,0 +1,134 @@
+// internal.h — launchers and layouts shared between the host API (api.cu)
+// and the kernel translation units of libdseq.so.  Plain pointers only.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dseq {
+
+// device status word bits (OR-ed by any thread that gives up)
+enum : int {
+    kStatusBarrierTimeout = 1,
+    kStatusPipeTimeout = 2,
+    kStatusNoWinner = 4,
+    kStatusNonFinite = 8,
+    kStatusInternal = 16,
+};
+
+
+// Rows of the query side (sequences / samples) per work unit: the 128 TMEM
+// lanes of one tensor-core accumulator.
+constexpr int kUnitRows = 128;
+// K extent of one pipeline stage (fp16 elements = 64 bytes per row).
+constexpr int kKBlock = 32;
+// Pipeline stages of the tensor-core kernels.
+constexpr int kStages = 4;
+// Epilogue warps of the tensor-core kernels (two per TMEM lane quadrant).
+constexpr int kEpiWarps = 8;
+// Threads per CTA: TMA producer warp, MMA warp, epilogue warps.
+constexpr int kTcThreads = 32 * (2 + kEpiWarps);
+// Bytes of one pipeline stage for a unit of tile_n candidate columns:
+// A = 3 x (128 x 32) fp16 (hi*2^12, hi, lo*2^12), B = 2 x (tile_n x 32) fp16.
+__host__ __device__ constexpr uint32_t tc_stage_bytes_a() { return 3u * kUnitRows * kKBlock * 2u; }
+__host__ __device__ constexpr uint32_t tc_stage_bytes_b_max() { return 2u * 256u * kKBlock * 2u; }
+__host__ __device__ constexpr uint32_t tc_smem_bytes() {
+    return kStages * (tc_stage_bytes_a() + tc_stage_bytes_b_max()) + 1024u /*align*/ + 256u;
+}
+
+// Layout of the running-minimum array of the tensor-core path.  Work unit u
+// (sequence block beta, candidate chunk j, u = j * n_beta + beta) owns a
+// contiguous tile of 128 x tile_n floats.  Inside a tile, element (row r,
+// column c) with r = 32 q + t (TMEM lane quadrant q, lane t) and
+// c = 32 g + 4 v + e sits at ((((g * 4 + q) * 8 + v) * 32 + t) * 4 + e), so
+// each warp's 16-byte accesses of one column group are 512 contiguous bytes.
+__host__ __device__ __forceinline__ int64_t tc_m_offset(int64_t unit, int tile_n, int r, int c) {
+    const int q = r >> 5, t = r & 31, g = c >> 5, v = (c >> 2) & 7, e = c & 3;
+    return unit * (int64_t)(kUnitRows * tile_n) + ((((g * 4 + q) * 8 + v) * 32 + t) * 4 + e);
+}
+
+struct TcPlan {
+    int n_beta;    // sequence blocks (ceil(B / 128))
+    int n_chunk;   // candidate chunks (ceil(N / tile_n))
+    int tile_n;    // candidate columns per unit
+    int grid;      // persistent CTAs
+    __host__ __device__ int64_t units() const { return (int64_t)n_beta * n_chunk; }
+};
+
+// ---- table preparation (api.cu calls; prep.cu defines) ---------------------
+// One warp per row: checks finiteness and a non-zero norm, writes the unit
+// row (float, zero-padded to Dp) and its split (hi | lo * 2^12) in fp16.
+void launch_table_prepare(const float *E, int64_t N, int D, int Dp, float *e_unit,
+                          __half *e_split, int *status, cudaStream_t st);
+
+// Rows of a BMU operand scaled by a per-row power of two (max |.| in [0.5, 1))
+// and split into fp16.  triple = 1: [hi*2^12 | hi | lo*2^12] (A side);
+// triple = 0: [hi | lo*2^12] (B side).  norm2[r] = |row|^2 (double sum),
+// inv_scale[r] = 1 / scale.
+void launch_bmu_prepare(const float *A, int64_t rows, int D, int Dp, int triple, __half *split,
+                        float *norm2, float *inv_scale, int *status, cudaStream_t st);
+
+// ---- diversity, tensor-core path (tc_dseq.cu) -------------------------------
+struct TcDseqArgs {
+    const __half *e_split;   // N x 2Dp
+    __half *q_split;         // Bp x 3Dp
+    float *m;                // units x 128 x tile_n
+    unsigned long long *keys;  // Bp
+    int32_t *picks;          // B x L
+    const int32_t *trace_slot;  // Bp (-1 = not traced) or nullptr
+    float *trace;            // n_trace x L x N
+    int *status;
+    unsigned *barrier;
+    int64_t N;
+    int B, L, Dp;
+    uint64_t timeout_ns;
+    int fault_skip_arrive;
+};
+void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *starts,
+                         const uint8_t *mask, cudaStream_t st);
+cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
+                           const CUtensorMap &tmap_e, cudaStream_t st);
+
+// ---- diversity, FFMA path (ffma.cu) -----------------------------------------
+struct FfmaDseqArgs {
+    const float *e_unit;   // N x Dp
+    float *q;              // Bp64 x Dp
+    float *m;              // Bp64 x Nf
+    unsigned long long *keys;
+    int32_t *picks;
+    const int32_t *trace_slot;
+    float *trace;
+    int *status;
+    int64_t N, Nf;
+    int B, Bp, L, Dp;
+};
+void launch_ffma_dseq_init(const FfmaDseqArgs &a, const int32_t *starts, const uint8_t *mask,
+                           cudaStream_t st);
+void launch_ffma_dseq_iteration(const FfmaDseqArgs &a, int t, cudaStream_t st);
+
+// ---- BMU ----------------------------------------------------------------------
+struct BmuArgs {
+    const float *X, *W;          // fp32 inputs (FFMA path)
+    const __half *x_split;       // n x 3Dp (tensor path)
+    const __half *w_split;       // M x 2Dp (tensor path)
+    const float *xn, *wn;        // squared norms
+    const float *x_inv_scale, *w_inv_scale;
+    unsigned long long *keys;    // n
+    int32_t *idx;
+    float *dist;
+    int *status;
+    int64_t n, M;
+    int D, Dp;
+    uint64_t timeout_ns;
+};
+void launch_bmu_keys_init(unsigned long long *keys, int64_t n, cudaStream_t st);
+void launch_ffma_bmu(const BmuArgs &a, cudaStream_t st);
+cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
+                          const CUtensorMap &tmap_w, cudaStream_t st);
+void launch_bmu_finalize(const BmuArgs &a, cudaStream_t st);
+void launch_row_sqnorm(const float *A, int64_t rows, int D, float *out, int *status,
+                       cudaStream_t st);
+
+}  // namespace dseq

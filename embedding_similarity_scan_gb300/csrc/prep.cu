@@ -1,0 +1,203 @@
+// prep.cu — one-pass preparation kernels: candidate-table normalisation and
+// fp16 hi/lo split, BMU operand scaling and split, squared norms, and the
+// BMU key initialisation / finalisation.
+//
+// The split: a float x with |x| <= 1 becomes hi = fp16(x) and
+// lo = fp16((x - hi) * 2^12).  x - hi is exact in fp32; scaling the residual
+// by 2^12 keeps it in fp16's normal range, so hi + lo * 2^-12 carries about
+// 22 significant bits, and a product of two split values needs three fp16
+// products (hi*hi, hi*lo, lo*hi) for fp32-level accuracy.  The tensor-core
+// kernels fold the 2^-12 into a pre-scaled copy of hi on the query side
+// (hi * 2^12), so all three products land in one fp32 accumulator scaled by
+// 2^12.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dseq {
+
+namespace {
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_or_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void split_f16(float x, __half &hi, __half &lo) {
+    hi = __float2half_rn(x);
+    const float r = x - __half2float(hi);
+    lo = __float2half_rn(r * 4096.0f);
+}
+
+__global__ void table_prepare_kernel(const float *__restrict__ E, int64_t N, int D, int Dp,
+                                     float *__restrict__ e_unit, __half *__restrict__ e_split,
+                                     int *status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= N) return;
+    const float *src = E + row * (int64_t)D;
+    double ss = 0.0;
+    int bad = 0;
+    for (int k = lane; k < D; k += 32) {
+        const float v = src[k];
+        if (!isfinite(v)) bad = 1;
+        ss += (double)v * (double)v;
+    }
+    ss = warp_sum_d(ss);
+    bad = warp_or_i(bad);
+    if (bad || !(ss > 0.0) || !isfinite(ss)) {
+        if (lane == 0) atomicOr(status, kStatusNonFinite);
+        return;
+    }
+    const double inv = 1.0 / sqrt(ss);
+    float *dst = e_unit + row * (int64_t)Dp;
+    __half *sp = e_split + row * (int64_t)(2 * Dp);
+    for (int k = lane; k < Dp; k += 32) {
+        const float u = k < D ? (float)((double)src[k] * inv) : 0.0f;
+        dst[k] = u;
+        __half hi, lo;
+        split_f16(u, hi, lo);
+        sp[k] = hi;
+        sp[Dp + k] = lo;
+    }
+}
+
+__global__ void bmu_prepare_kernel(const float *__restrict__ A, int64_t rows, int D, int Dp,
+                                   int triple, __half *__restrict__ split,
+                                   float *__restrict__ norm2, float *__restrict__ inv_scale,
+                                   int *status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const float *src = A + row * (int64_t)D;
+    double ss = 0.0;
+    float mx = 0.0f;
+    int bad = 0;
+    for (int k = lane; k < D; k += 32) {
+        const float v = src[k];
+        if (!isfinite(v)) bad = 1;
+        ss += (double)v * (double)v;
+        mx = fmaxf(mx, fabsf(v));
+    }
+    ss = warp_sum_d(ss);
+    mx = warp_max_f(mx);
+    bad = warp_or_i(bad);
+    if (bad) {
+        if (lane == 0) atomicOr(status, kStatusNonFinite);
+        return;
+    }
+    // scale = 2^-e with mx = f * 2^e, f in [0.5, 1): max |row * scale| < 1.
+    int e = 0;
+    if (mx > 0.0f) frexpf(mx, &e);
+    const float scale = ldexpf(1.0f, -e);
+    if (lane == 0) {
+        norm2[row] = (float)ss;
+        inv_scale[row] = ldexpf(1.0f, e);
+    }
+    const int w = triple ? 3 * Dp : 2 * Dp;
+    __half *sp = split + row * (int64_t)w;
+    for (int k = lane; k < Dp; k += 32) {
+        const float u = k < D ? src[k] * scale : 0.0f;
+        __half hi, lo;
+        split_f16(u, hi, lo);
+        if (triple) {
+            sp[k] = __float2half_rn(__half2float(hi) * 4096.0f);  // exact: power-of-two scale
+            sp[Dp + k] = hi;
+            sp[2 * Dp + k] = lo;
+        } else {
+            sp[k] = hi;
+            sp[Dp + k] = lo;
+        }
+    }
+}
+
+__global__ void row_sqnorm_kernel(const float *__restrict__ A, int64_t rows, int D,
+                                  float *__restrict__ out, int *status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const float *src = A + row * (int64_t)D;
+    double ss = 0.0;
+    int bad = 0;
+    for (int k = lane; k < D; k += 32) {
+        const float v = src[k];
+        if (!isfinite(v)) bad = 1;
+        ss += (double)v * (double)v;
+    }
+    ss = warp_sum_d(ss);
+    bad = warp_or_i(bad);
+    if (lane == 0) {
+        if (bad) atomicOr(status, kStatusNonFinite);
+        out[row] = (float)ss;
+    }
+}
+
+__global__ void fill_u64_kernel(unsigned long long *p, int64_t n, unsigned long long v) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        p[i] = v;
+}
+
+__global__ void bmu_finalize_kernel(const unsigned long long *__restrict__ keys,
+                                    const float *__restrict__ xn, int64_t n,
+                                    int32_t *__restrict__ idx, float *__restrict__ dist,
+                                    int *status) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const unsigned long long k = keys[i];
+        if (k == ~0ull) {
+            atomicOr(status, kStatusNoWinner);
+            idx[i] = -1;
+            dist[i] = 0.0f;
+            continue;
+        }
+        const float s = float_unorder((uint32_t)(k >> 32));
+        idx[i] = (int32_t)(uint32_t)(k & 0xffffffffull);
+        dist[i] = fmaxf(0.0f, xn[i] + s);
+    }
+}
+
+inline unsigned blocks_for_rows(int64_t rows, int warps_per_block) {
+    return (unsigned)((rows + warps_per_block - 1) / warps_per_block);
+}
+
+}  // namespace
+
+void launch_table_prepare(const float *E, int64_t N, int D, int Dp, float *e_unit,
+                          __half *e_split, int *status, cudaStream_t st) {
+    table_prepare_kernel<<<blocks_for_rows(N, 8), 256, 0, st>>>(E, N, D, Dp, e_unit, e_split,
+                                                                  status);
+}
+
+void launch_bmu_prepare(const float *A, int64_t rows, int D, int Dp, int triple, __half *split,
+                        float *norm2, float *inv_scale, int *status, cudaStream_t st) {
+    bmu_prepare_kernel<<<blocks_for_rows(rows, 8), 256, 0, st>>>(A, rows, D, Dp, triple, split,
+                                                                   norm2, inv_scale, status);
+}
+
+void launch_row_sqnorm(const float *A, int64_t rows, int D, float *out, int *status,
+                       cudaStream_t st) {
+    row_sqnorm_kernel<<<blocks_for_rows(rows, 8), 256, 0, st>>>(A, rows, D, out, status);
+}
+
+void launch_bmu_keys_init(unsigned long long *keys, int64_t n, cudaStream_t st) {
+    fill_u64_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(
+        keys, n, ~0ull);
+}
+
+void launch_bmu_finalize(const BmuArgs &a, cudaStream_t st) {
+    bmu_finalize_kernel<<<(unsigned)((a.n + 255) / 256 < 4096 ? (a.n + 255) / 256 : 4096), 256, 0,
+                          st>>>(a.keys, a.xn, a.n, a.idx, a.dist, a.status);
+}
+
+}  // namespace dseq

@@ -1,0 +1,271 @@
+// tc_bmu.cu — best-matching-unit search as a persistent, warp-specialised
+// tcgen05 kernel for sm_103a.
+//
+// The method ("From 80x to 385x: A Best-Matching-Unit Search at the L2
+// Roof", section 3 Background and section 4): for every sample x_i the
+// neuron j minimising |x_i - w_j|^2 = |x_i|^2 + (|w_j|^2 - 2 <x_i, w_j>),
+// with the argmin fused into the product so the sample x neuron score block
+// is never materialised, and the neuron axis split into chunks whose partial
+// (min, index) results are merged (section 4.2, neuron-axis chunking).
+//
+// Here a work unit is 128 samples (the TMEM lanes of one accumulator) times
+// a chunk of tile_n neurons.  Units are ordered neuron-slice-major, then by
+// sample block, then by chunk inside the slice, where a slice is as many
+// chunks as fit a fraction of L2: all CTAs sweep one L2-resident slice of the
+// codebook against every sample block before moving to the next slice, so
+// the codebook is read from HBM once and the samples once per slice.
+//
+// Operands are pre-scaled per row by a power of two (max |.| in [0.5, 1))
+// and split into fp16 hi + lo * 2^-12 (prep.cu); three kind::f16 MMAs per
+// 32-wide K block accumulate 2^12 <x~, w~> in fp32 TMEM.  The epilogue forms
+// score_j = |w_j|^2 + acc * (1 / s_w[j]) * (-2^-11 / s_x[i]), keeps the
+// running (min score, lowest j) per row and folds it into the row's 64-bit
+// key with one atomicMin per unit; a finalize pass turns keys into
+// (idx, max(0, |x|^2 + score)).
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dseq {
+
+namespace {
+
+constexpr int kBmuStages = 3;
+constexpr uint32_t kSubA = kUnitRows * kKBlock * 2;
+constexpr uint32_t kSubBMax = 256 * kKBlock * 2;
+constexpr uint32_t kStageBytes = 3 * kSubA + 2 * kSubBMax;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                       ~static_cast<uintptr_t>(1023));
+}
+
+struct BmuSchedule {
+    int n_beta, n_chunk, tile_n, slice_chunks;
+    // unit u -> (sample block beta, neuron chunk j)
+    __device__ __forceinline__ void decode(int64_t u, int &beta, int &j) const {
+        const int64_t per_slice = (int64_t)n_beta * slice_chunks;
+        const int64_t sl = u / per_slice;
+        const int64_t rem = u - sl * per_slice;
+        const int first = (int)(sl * slice_chunks);
+        const int width = min(slice_chunks, n_chunk - first);
+        beta = (int)(rem / width);
+        j = first + (int)(rem - (int64_t)beta * width);
+    }
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_bmu_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                  const __grid_constant__ CUtensorMap tmap_w, const BmuArgs a, const TcPlan p,
+                  const int slice_chunks) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBmuStages * kStageBytes);
+    uint64_t *empty = full + kBmuStages;
+    uint64_t *acc_full = empty + kBmuStages;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *final_bar = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(final_bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float2 *colc = reinterpret_cast<float2 *>(smem + kBmuStages * kStageBytes + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t tmo = a.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBmuStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], kEpiWarps);
+        }
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const BmuSchedule sched{p.n_beta, p.n_chunk, p.tile_n, slice_chunks};
+    const int64_t units = p.units();
+    const uint32_t tile_n = (uint32_t)p.tile_n;
+    const uint32_t sub_b = tile_n * kKBlock * 2;
+    const uint32_t tx_bytes = 3 * kSubA + 2 * sub_b;
+    const int kblocks = a.Dp / kKBlock;
+    const uint32_t idesc = idesc_f16_f32(kUnitRows, tile_n);
+    const int groups = (int)(tile_n / 32);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t fills = 0;
+            for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+                int beta, j;
+                sched.decode(u, beta, j);
+                const int yx = beta * kUnitRows, yw = j * (int)tile_n;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const uint32_t s = fills % kBmuStages, par = (fills / kBmuStages) & 1u;
+                    if (!mbar_wait_bounded(&empty[s], par ^ 1u, abort_flag, a.status, tmo,
+                                           kStatusPipeTimeout))
+                        break;
+                    uint8_t *sa = smem + s * kStageBytes;
+                    uint8_t *sb = sa + 3 * kSubA;
+                    mbar_arrive_expect_tx(&full[s], tx_bytes);
+                    const int x = kb * kKBlock;
+                    tma_load_2d(sa, &tmap_x, &full[s], x, yx);
+                    tma_load_2d(sa + kSubA, &tmap_x, &full[s], a.Dp + x, yx);
+                    tma_load_2d(sa + 2 * kSubA, &tmap_x, &full[s], 2 * a.Dp + x, yx);
+                    tma_load_2d(sb, &tmap_w, &full[s], x, yw);
+                    tma_load_2d(sb + kSubBMax, &tmap_w, &full[s], a.Dp + x, yw);
+                    ++fills;
+                }
+            }
+            if (*abort_flag) {
+                volatile int never = 0;
+                for (uint32_t s = 0; s < kBmuStages && s < fills; ++s) {
+                    const uint32_t n_s = fills / kBmuStages + (s < fills % kBmuStages ? 1u : 0u);
+                    mbar_wait_bounded(&full[s], (n_s - 1) & 1u, &never, a.status,
+                                      tmo < 1000000000ull ? tmo : 1000000000ull,
+                                      kStatusPipeTimeout);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t consumed = 0, acc_uses = 0;
+            for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+                const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+                if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
+                                       kStatusPipeTimeout))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * kAccCols;
+                bool ok = true;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const uint32_t s = consumed % kBmuStages, par = (consumed / kBmuStages) & 1u;
+                    if (!mbar_wait_bounded(&full[s], par, abort_flag, a.status, tmo,
+                                           kStatusPipeTimeout)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * kStageBytes);
+                    const uint32_t sb = sa + 3 * kSubA;
+#pragma unroll
+                    for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
+                        const uint32_t off = k16 * 32;
+                        umma_f16(d_tmem, smem_desc_sw64(sa + off), smem_desc_sw64(sb + off), idesc,
+                                 (kb | k16) != 0);
+                        umma_f16(d_tmem, smem_desc_sw64(sa + kSubA + off),
+                                 smem_desc_sw64(sb + kSubBMax + off), idesc, 1u);
+                        umma_f16(d_tmem, smem_desc_sw64(sa + 2 * kSubA + off),
+                                 smem_desc_sw64(sb + off), idesc, 1u);
+                    }
+                    umma_commit(&empty[s]);
+                    ++consumed;
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[buf]);
+                ++acc_uses;
+            }
+            volatile int never = 0;
+            umma_commit(final_bar);
+            mbar_wait_bounded(final_bar, 0, &never, a.status,
+                              tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
+        }
+        __syncwarp();
+    } else {
+        const int e = warp - 2, q = warp & 3, h = e >> 2;
+        const int r = 32 * q + lane;
+        float2 *my_colc = colc + e * 32;
+        uint32_t acc_uses = 0;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+            int beta, j;
+            sched.decode(u, beta, j);
+            const int64_t row = (int64_t)beta * kUnitRows + r;
+            const float cx = row < a.n ? -a.x_inv_scale[row] * (1.0f / 2048.0f) : 0.0f;
+            const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+            // every lane waits; the warp proceeds only if all of them saw the phase
+            const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status, tmo,
+                                                 kStatusPipeTimeout);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            float best = INFINITY;
+            uint32_t best_j = 0xffffffffu;
+            const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+            for (int g = h; g < groups; g += 2) {
+                const int64_t col = (int64_t)j * tile_n + 32 * g + lane;
+                __syncwarp();
+                my_colc[lane] = col < a.M ? make_float2(a.wn[col], a.w_inv_scale[col])
+                                          : make_float2(INFINITY, 0.0f);
+                __syncwarp();
+                float acc[32];
+                tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
+                tmem_wait_ld();
+                const uint32_t cbase = (uint32_t)j * tile_n + 32u * (uint32_t)g;
+#pragma unroll
+                for (int z = 0; z < 32; ++z) {
+                    const float2 cc = my_colc[z];
+                    const float s = fmaf(acc[z] * cc.y, cx, cc.x);
+                    if (s < best) {
+                        best = s;
+                        best_j = cbase + z;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            ++acc_uses;
+            if (row < a.n && best_j != 0xffffffffu) atomicMin(a.keys + row, min_key(best, best_j));
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
+                          const CUtensorMap &tmap_w, cudaStream_t st) {
+    const size_t smem = kBmuStages * kStageBytes + 1024 + 256 + kEpiWarps * 32 * sizeof(float2);
+    cudaError_t err =
+        cudaFuncSetAttribute(tc_bmu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    // neuron slice: chunks whose split rows fill about half of L2
+    int dev = 0, l2 = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    const double row_bytes = 2.0 * a.Dp * 2.0;
+    int slice = (int)((0.5 * (double)l2) / (row_bytes * p.tile_n));
+    if (slice < 1) slice = 1;
+    if (slice > p.n_chunk) slice = p.n_chunk;
+    BmuArgs aa = a;
+    TcPlan pp = p;
+    CUtensorMap mx = tmap_x, mw = tmap_w;
+    int sl = slice;
+    void *args[] = {&mx, &mw, &aa, &pp, &sl};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(tc_bmu_kernel), dim3((unsigned)p.grid),
+                            dim3(kTcThreads), args, smem, st);
+}
+
+}  // namespace dseq

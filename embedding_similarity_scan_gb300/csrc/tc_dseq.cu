@@ -1,0 +1,406 @@
+// tc_dseq.cu — the greedy max-min diversity scan as one persistent,
+// warp-specialised tcgen05 kernel for sm_103a.
+//
+// The method ("Issue 9-014: Tile Diversity Shader Inner Loop For L2 Cache
+// Locality"): every iteration, each sequence compares its newest pick with
+// every candidate, folds the cosine distance into its running minimum, and
+// takes the unmasked candidate with the largest running minimum (lowest index
+// on ties).  The issue asks for a tiled candidate scan that every workgroup
+// walks together, with a hard grid-wide sync between steps (Intended
+// Behavior, "dispatch per tile"); here the loop over iterations lives on the
+// device and the sync is a grid barrier.
+//
+// Work decomposition.  One iteration is the contraction S = Q * E^T of the
+// B current query rows against the N table rows.  A work unit is a block of
+// 128 sequences (the 128 TMEM lanes of one accumulator) times a chunk of
+// tile_n candidates; units are ordered candidate-chunk-major and dealt to the
+// persistent CTAs round-robin, so at any moment all CTAs work on the same
+// few candidate chunks (the grid marches over the table together, and each
+// chunk is read from HBM once per iteration while the query block set stays
+// resident in L2).
+//
+// Precision.  Rows are unit-norm and split into fp16 pairs hi + lo * 2^-12
+// (see prep.cu).  The query side carries (hi * 2^12, hi, lo), the table side
+// (hi, lo); per 32-wide K block three kind::f16 MMAs accumulate
+// hi*2^12 . hi + hi . lo + lo . hi into one fp32 TMEM accumulator, which
+// equals 2^12 <q, e> up to about 2^-22 relative per product.
+//
+// CTA roles (320 threads):
+//   warp 0      TMA producer: Q and E K-blocks into a 4-stage smem ring;
+//   warp 1      TMEM owner and MMA issuer (one thread), double-buffered
+//               128 x 256 fp32 accumulators (512 TMEM columns);
+//   warps 2-9   epilogue: TMEM -> registers, d = 1 - S, m = min(m, d) on the
+//               running-minimum tile (read and written once per unit, 16-byte
+//               coalesced), running (max m, lowest index) per row, one 64-bit
+//               atomicMax per row and unit into the sequence's key.
+// After the last unit of an iteration: grid barrier; commit (one warp per
+// sequence: decode the winner, record it, mask it in m, write its split row
+// as the next query); grid barrier.  Every wait is bounded in time and sets
+// the status word instead of hanging.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dseq {
+
+namespace {
+
+constexpr uint32_t kSubA = kUnitRows * kKBlock * 2;  // one 128 x 32 fp16 sub-tile: 8 KB
+constexpr uint32_t kSubBMax = 256 * kKBlock * 2;     // one 256 x 32 fp16 sub-tile: 16 KB
+constexpr uint32_t kStageBytes = 3 * kSubA + 2 * kSubBMax;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                       ~static_cast<uintptr_t>(1023));
+}
+
+__global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__restrict__ starts,
+                                    const uint8_t *__restrict__ mask) {
+    const int64_t tile = (int64_t)kUnitRows * p.tile_n;
+    const int64_t total = p.units() * tile;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t u = i / tile;
+        const int s = (int)(i - u * tile);
+        const int e = s & 3, t = (s >> 2) & 31, v = (s >> 7) & 7, q = (s >> 10) & 3, g = s >> 12;
+        const int r = 32 * q + t, c = 32 * g + 4 * v + e;
+        const int beta = (int)(u % p.n_beta), j = (int)(u / p.n_beta);
+        const int b = beta * kUnitRows + r;
+        const int64_t cand = (int64_t)j * p.tile_n + c;
+        bool live = b < a.B && cand < a.N;
+        if (live && mask && mask[cand]) live = false;
+        if (live && cand == starts[b]) live = false;
+        a.m[i] = live ? INFINITY : -INFINITY;
+    }
+    // query rows: the split start rows, zero rows for padded sequences
+    const int vec = a.Dp / 8;  // 16-byte vectors per row segment
+    const int64_t qtotal = (int64_t)p.n_beta * kUnitRows * vec;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < qtotal; i += stride) {
+        const int b = (int)(i / vec), k = (int)(i - (int64_t)b * vec);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * 3 * a.Dp);
+        if (b < a.B) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.e_split +
+                                                               (int64_t)starts[b] * 2 * a.Dp);
+            const uint4 hi = src[k], lo = src[vec + k];
+            uint4 hi12 = hi;
+            __half2 *h2 = reinterpret_cast<__half2 *>(&hi12);
+            const __half2 scale = __float2half2_rn(4096.0f);
+#pragma unroll
+            for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
+            dst[k] = hi12;
+            dst[vec + k] = hi;
+            dst[2 * vec + k] = lo;
+        } else {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            dst[k] = z;
+            dst[vec + k] = z;
+            dst[2 * vec + k] = z;
+        }
+    }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+         i < (int64_t)p.n_beta * kUnitRows; i += stride)
+        a.keys[i] = 0ull;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_dseq_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                   const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
+                   const TcPlan p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *acc_full = empty + kStages;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *final_bar = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(final_bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t tmo = a.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], kEpiWarps);
+        }
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_e);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int64_t units = p.units();
+    const uint32_t tile_n = (uint32_t)p.tile_n;
+    const uint32_t sub_b = tile_n * kKBlock * 2;
+    const uint32_t tx_bytes = 3 * kSubA + 2 * sub_b;
+    const int kblocks = a.Dp / kKBlock;
+    const uint32_t idesc = idesc_f16_f32(kUnitRows, tile_n);
+    const int groups = (int)(tile_n / 32);
+
+    uint32_t fills = 0;     // producer: stages filled so far
+    uint32_t consumed = 0;  // MMA: stages consumed so far
+    uint32_t acc_uses = 0;  // MMA and epilogue: accumulators used so far
+    unsigned barrier_no = 0;
+    bool skip_arrive = a.fault_skip_arrive && blockIdx.x == 0;
+
+    for (int t = 0; t < a.L; ++t) {
+        if (*abort_flag) break;
+        if (warp == 0) {
+            // ---------------- TMA producer ----------------
+            if (lane == 0) {
+                fence_proxy_async_global();
+                for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+                    const int beta = (int)(u % p.n_beta), j = (int)(u / p.n_beta);
+                    const int yq = beta * kUnitRows, ye = j * (int)tile_n;
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        const uint32_t s = fills % kStages, par = (fills / kStages) & 1u;
+                        if (!mbar_wait_bounded(&empty[s], par ^ 1u, abort_flag, a.status, tmo,
+                                               kStatusPipeTimeout))
+                            break;
+                        uint8_t *sa = smem + s * kStageBytes;
+                        uint8_t *sb = sa + 3 * kSubA;
+                        mbar_arrive_expect_tx(&full[s], tx_bytes);
+                        const int x = kb * kKBlock;
+                        tma_load_2d(sa, &tmap_q, &full[s], x, yq);
+                        tma_load_2d(sa + kSubA, &tmap_q, &full[s], a.Dp + x, yq);
+                        tma_load_2d(sa + 2 * kSubA, &tmap_q, &full[s], 2 * a.Dp + x, yq);
+                        tma_load_2d(sb, &tmap_e, &full[s], x, ye);
+                        tma_load_2d(sb + kSubBMax, &tmap_e, &full[s], a.Dp + x, ye);
+                        ++fills;
+                    }
+                }
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            // ---------------- MMA issuer ----------------
+            if (lane == 0) {
+                for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+                    const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+                    if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
+                                           kStatusPipeTimeout))
+                        break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * kAccCols;
+                    bool ok = true;
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        const uint32_t s = consumed % kStages, par = (consumed / kStages) & 1u;
+                        if (!mbar_wait_bounded(&full[s], par, abort_flag, a.status, tmo,
+                                               kStatusPipeTimeout)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(smem + s * kStageBytes);
+                        const uint32_t sb = sa + 3 * kSubA;
+#pragma unroll
+                        for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
+                            const uint32_t off = k16 * 32;  // 16 fp16 = 32 bytes along K
+                            umma_f16(d_tmem, smem_desc_sw64(sa + off), smem_desc_sw64(sb + off),
+                                     idesc, (kb | k16) != 0);
+                            umma_f16(d_tmem, smem_desc_sw64(sa + kSubA + off),
+                                     smem_desc_sw64(sb + kSubBMax + off), idesc, 1u);
+                            umma_f16(d_tmem, smem_desc_sw64(sa + 2 * kSubA + off),
+                                     smem_desc_sw64(sb + off), idesc, 1u);
+                        }
+                        umma_commit(&empty[s]);
+                        ++consumed;
+                    }
+                    if (!ok) break;
+                    umma_commit(&acc_full[buf]);
+                    ++acc_uses;
+                }
+            }
+            __syncwarp();
+        } else {
+            // ---------------- epilogue ----------------
+            const int e = warp - 2, q = warp & 3, h = e >> 2;
+            const int r = 32 * q + lane;
+            for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+                const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+                const int beta = (int)(u % p.n_beta), j = (int)(u / p.n_beta);
+                float4 *mt = reinterpret_cast<float4 *>(a.m + u * (int64_t)(kUnitRows * tile_n));
+                // prefetch the first group's running minima before waiting
+                float4 mcur[8], mnext[8];
+                if (h < groups) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) mcur[v] = mt[((h * 4 + q) * 8 + v) * 32 + lane];
+                }
+                // every lane waits; the warp proceeds only if all of them saw the phase
+                const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status,
+                                                     tmo, kStatusPipeTimeout);
+                if (!__all_sync(0xffffffffu, ready)) break;
+                tc_fence_after();
+                float best = -INFINITY;
+                uint32_t best_c = 0;
+                const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+                for (int g = h; g < groups; g += 2) {
+                    const int gn = g + 2;
+                    if (gn < groups) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            mnext[v] = mt[((gn * 4 + q) * 8 + v) * 32 + lane];
+                    }
+                    float acc[32];
+                    tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
+                    tmem_wait_ld();
+                    const uint32_t cbase = (uint32_t)j * tile_n + 32u * (uint32_t)g;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        float mv[4] = {mcur[v].x, mcur[v].y, mcur[v].z, mcur[v].w};
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) {
+                            // d = 1 - <q, e>, the accumulator holding 2^12 <q, e>
+                            const float d = fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
+                            mv[z] = fminf(mv[z], d);
+                            if (mv[z] > best) {
+                                best = mv[z];
+                                best_c = cbase + 4 * v + z;
+                            }
+                        }
+                        mt[((g * 4 + q) * 8 + v) * 32 + lane] = make_float4(mv[0], mv[1], mv[2],
+                                                                            mv[3]);
+                    }
+                    if (gn < groups) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) mcur[v] = mnext[v];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                ++acc_uses;
+                const int b = beta * kUnitRows + r;
+                if (best > -INFINITY && b < a.B) atomicMax(a.keys + b, max_key(best, best_c));
+            }
+        }
+
+        // ---- all partial winners of iteration t are in the keys ----
+        if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
+                          skip_arrive))
+            break;
+        skip_arrive = false;
+
+        // ---- commit: one warp per sequence ----
+        {
+            const int gw = blockIdx.x * (kTcThreads / 32) + warp;
+            const int nw = gridDim.x * (kTcThreads / 32);
+            const int vec = a.Dp / 8;
+            for (int b = gw; b < a.B; b += nw) {
+                const unsigned long long key = a.keys[b];
+                __syncwarp();
+                if (key == 0ull) {
+                    if (lane == 0) {
+                        atomicOr(a.status, kStatusNoWinner);
+                        a.picks[(int64_t)b * a.L + t] = -1;
+                    }
+                    continue;
+                }
+                const uint32_t w = max_key_index(key);
+                const int beta = b / kUnitRows, r = b % kUnitRows;
+                if (lane == 0) {
+                    a.keys[b] = 0ull;
+                    a.picks[(int64_t)b * a.L + t] = (int32_t)w;
+                }
+                if (a.trace_slot) {
+                    const int slot = a.trace_slot[b];
+                    if (slot >= 0) {
+                        float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
+                        for (int64_t c = lane; c < a.N; c += 32) {
+                            const int jj = (int)(c / tile_n), cc = (int)(c - (int64_t)jj * tile_n);
+                            dst[c] = a.m[tc_m_offset((int64_t)jj * p.n_beta + beta, tile_n, r, cc)];
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    const int jw = (int)(w / tile_n), cw = (int)(w - (uint32_t)jw * tile_n);
+                    a.m[tc_m_offset((int64_t)jw * p.n_beta + beta, tile_n, r, cw)] = -INFINITY;
+                }
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.e_split + (int64_t)w * 2 * a.Dp);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * 3 * a.Dp);
+                const __half2 scale = __float2half2_rn(4096.0f);
+                for (int k = lane; k < vec; k += 32) {
+                    const uint4 hi = src[k], lo = src[vec + k];
+                    uint4 hi12 = hi;
+                    __half2 *h2 = reinterpret_cast<__half2 *>(&hi12);
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
+                    dst[k] = hi12;
+                    dst[vec + k] = hi;
+                    dst[2 * vec + k] = lo;
+                }
+            }
+            fence_proxy_async_global();
+        }
+
+        // ---- the next queries are written ----
+        if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
+                          false))
+            break;
+    }
+
+    // ---- teardown: drain what this CTA still has in flight, free TMEM ----
+    __syncthreads();
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        // wait (bounded) for the last fill of every stage that was ever filled
+        volatile int never = 0;
+        for (uint32_t s = 0; s < kStages && s < fills; ++s) {
+            const uint32_t n_s = fills / kStages + (s < fills % kStages ? 1u : 0u);
+            mbar_wait_bounded(&full[s], (n_s - 1) & 1u, &never, a.status,
+                              tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
+        }
+    }
+    if (warp == 1) {
+        if (lane == 0) {
+            volatile int never = 0;
+            umma_commit(final_bar);
+            mbar_wait_bounded(final_bar, 0, &never, a.status,
+                              tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *starts,
+                         const uint8_t *mask, cudaStream_t st) {
+    tc_dseq_init_kernel<<<2048, 256, 0, st>>>(a, p, starts, mask);
+}
+
+cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
+                           const CUtensorMap &tmap_e, cudaStream_t st) {
+    const size_t smem = tc_smem_bytes();
+    cudaError_t err =
+        cudaFuncSetAttribute(tc_dseq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    TcDseqArgs aa = a;
+    TcPlan pp = p;
+    CUtensorMap mq = tmap_q, me = tmap_e;
+    void *args[] = {&mq, &me, &aa, &pp};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(tc_dseq_kernel),
+                                       dim3((unsigned)p.grid), dim3(kTcThreads), args, smem, st);
+}
+
+}  // namespace dseq

@@ -1,0 +1,163 @@
+/*
+ * dseq.h — C ABI of the embedding similarity scan library (libdseq.so).
+ *
+ * One data-parallel hot path serves two uses:
+ *
+ *  - Greedy diversity sequences ("Issue 9-014: Tile Diversity Shader Inner
+ *    Loop For L2 Cache Locality", Current Behavior and Intended Behavior).
+ *    Each of B independent sequences holds its newest pick; every iteration
+ *    computes the cosine distance of that pick to all N candidate rows,
+ *    folds it into the sequence's running minimum distance, and picks the
+ *    unmasked candidate whose running minimum is largest, lowest index on
+ *    ties (the max-min, farthest-first reading of "most different").  The
+ *    candidate scan is tiled and the running (max, index) carried across
+ *    tiles, which by associativity of max gives the one-pass winner (same
+ *    issue, Intended Behavior).
+ *
+ *  - Best-matching-unit search ("From 80x to 385x: A Best-Matching-Unit
+ *    Search at the L2 Roof", section 3 Background, and section 4.2, neuron-
+ *    axis chunking): for every sample, the codebook row at the smallest
+ *    squared Euclidean distance, lowest index on ties, with the argmin fused
+ *    into the product so the sample x neuron score block is never stored.
+ *
+ * Conventions shared by every call:
+ *  - Return value: DSEQ_OK (0) on success, a negative DSEQ_E* code on error;
+ *    dseq_last_error() then returns a message for the calling thread.
+ *    Outputs are unspecified after an error.
+ *  - Array arguments may be host or device pointers (the library inspects
+ *    each with cudaPointerGetAttributes); host arrays are staged through
+ *    library-owned device buffers on the given stream.  Pinned host memory
+ *    makes those copies asynchronous.
+ *  - cuda_stream is a cudaStream_t (NULL = the legacy default stream) on the
+ *    current device.  Every call is synchronous at return: it enqueues its
+ *    work on the stream, synchronizes the stream and reads back the device
+ *    status word.
+ *  - All tables are row-major float32, rows contiguous.  The caller owns
+ *    every array it passes; the library never frees or retains them past
+ *    the call (dseq_create copies the table).
+ *  - Calls on one dseq_ctx must not overlap; bmu_search and distinct
+ *    contexts may be used from different threads.
+ */
+#ifndef DSEQ_H
+#define DSEQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    DSEQ_OK = 0,
+    DSEQ_EINVAL = -1,     /* NULL pointer, bad size, start out of range or repeated, L too large */
+    DSEQ_ENONFINITE = -2, /* NaN / Inf in an input table, or an all-zero table row */
+    DSEQ_ENOMEM = -3,     /* device allocation failed */
+    DSEQ_ELAUNCH = -4,    /* the persistent grid could not be made co-resident */
+    DSEQ_ETIMEOUT = -5,   /* a device-side wait gave up (the kernel returned cleanly) */
+    DSEQ_ECUDA = -6,      /* any other CUDA runtime / driver error */
+    DSEQ_EINTERNAL = -7   /* an internal consistency check failed on the device */
+};
+
+/* Opaque context: owns the device copy of one candidate table (unit-norm
+ * rows, float32 and the split half-precision pair used by the tensor-core
+ * path) and the workspace of its runs (running minimum distances, current
+ * query rows, per-sequence argmax keys, barrier counters, status word). */
+typedef struct dseq_ctx dseq_ctx;
+
+/* Upload a candidate table of N rows x D float32 columns and prepare it.
+ *   table            N*D floats, row-major; host or device memory.
+ *   N                number of candidates, 1 <= N < 2^31.
+ *   D                embedding dimension, 1 <= D <= 16384.
+ *   table_on_device  ignored (kept for source compatibility: the pointer
+ *                    kind is detected); pass 0 or 1.
+ *   cuda_stream      stream for the upload and preparation kernels.
+ *   out              receives the new context (NULL on error).
+ * Errors: DSEQ_EINVAL (NULL pointer, N or D out of range), DSEQ_ENONFINITE
+ * (a NaN/Inf element or a row whose norm is zero: cosine distance is
+ * undefined there), DSEQ_ENOMEM, DSEQ_ECUDA.  The table is copied; the
+ * caller may free it when the call returns. */
+int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device,
+                void *cuda_stream, dseq_ctx **out);
+
+/* Run B greedy max-min diversity sequences of L picks each.
+ *   starts   int32[B]: the start row of each sequence; distinct, in [0, N).
+ *   B        number of sequences, >= 1.
+ *   L        picks per sequence after its start, >= 0.
+ *   mask     uint8[N] or NULL: mask[c] != 0 excludes row c from every
+ *            sequence (a start may itself be masked).
+ *   picks    int32[B*L], out: picks[b*L + t] is the t-th pick of sequence b
+ *            after its start (the start itself is not included); may be
+ *            NULL when L = 0.
+ * Semantics (one iteration t, every sequence b, p = the newest row of b):
+ *   m_b[c] <- min(m_b[c], 1 - <e_p, e_c> / (|e_p| |e_c|)) for every c,
+ *   pick = argmax over unmasked c of m_b[c], ties to the lowest c,
+ *   with m_b initialised to +inf and the start masked.
+ * Errors: DSEQ_EINVAL (NULL pointers, B < 1, L < 0, a start out of range or
+ * repeated, or L larger than the candidates some sequence has left:
+ * N - |mask U {start_b}|), DSEQ_ENOMEM, DSEQ_ELAUNCH, DSEQ_ETIMEOUT,
+ * DSEQ_ECUDA, DSEQ_EINTERNAL. */
+int dseq_run(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L, const uint8_t *mask,
+             int32_t *picks, void *cuda_stream);
+
+/* dseq_run that also records the running minimum distances of selected
+ * sequences after every fold (for parity checks).
+ *   trace_seqs      int32[n_trace]: distinct sequence indices in [0, B).
+ *   trace_mindist   float[n_trace * L * N], out, DEVICE memory only:
+ *                   trace_mindist[(k*L + t)*N + c] = m_{trace_seqs[k]}[c]
+ *                   after the fold of iteration t, before pick t is masked.
+ *                   Masked candidates (the global mask, the start and the
+ *                   picks before t) hold -inf.
+ * Errors: as dseq_run, plus DSEQ_EINVAL for a host trace buffer or bad
+ * trace indices. */
+int dseq_run_trace(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
+                   const uint8_t *mask, int32_t *picks, const int32_t *trace_seqs,
+                   int32_t n_trace, float *trace_mindist, void *cuda_stream);
+
+/* Free the context and everything it owns.  NULL is accepted. */
+void dseq_destroy(dseq_ctx *ctx);
+
+/* Best-matching-unit search of n samples against an M-neuron codebook.
+ *   X     float[n*D] samples, row-major; host or device.
+ *   W     float[M*D] codebook, row-major (neuron j = row j); host or device.
+ *   idx   int32[n], out: argmin_j |X_i - W_j|^2, ties to the lowest j.
+ *   dist  float[n], out: that squared distance, clamped at 0 (computed as
+ *         |x|^2 + (|w_j|^2 - 2<x, w_j>) with both norms precomputed).
+ * Sizes: 1 <= n, M < 2^31, 1 <= D <= 16384.
+ * Errors: DSEQ_EINVAL, DSEQ_ENONFINITE (NaN/Inf in X or W), DSEQ_ENOMEM,
+ * DSEQ_ETIMEOUT, DSEQ_ECUDA. */
+int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, int32_t *idx,
+               float *dist, void *cuda_stream);
+
+/* Tuning and test knobs.  ctx = NULL sets the process-wide default used by
+ * bmu_search and by contexts created afterwards; otherwise the setting
+ * applies to that context only.  Names:
+ *   "engine"      0 = tensor-core path (default), 1 = FP32 FFMA path.
+ *   "tile_n"      candidate (or neuron) columns per work unit, a multiple of
+ *                 32 in [32, 256]; 0 = chosen from the shape (default).
+ *   "grid"        persistent CTAs; 0 = one per SM (default).
+ *   "timeout_ms"  limit of every device-side wait (default 10000).
+ *   "fault_skip_arrive"  test only: 1 makes CTA 0 skip its first grid-barrier
+ *                 arrival, so the other CTAs' waits run out (the kernel then
+ *                 returns DSEQ_ETIMEOUT without hanging).
+ * Errors: DSEQ_EINVAL for an unknown name or a value out of range. */
+int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value);
+
+/* Read back a knob (the value in effect; -1 for an unknown name). */
+int64_t dseq_get_option(dseq_ctx *ctx, const char *name);
+
+/* Statistics of the last successful dseq_run / bmu_search on this thread:
+ *   "units"        work units (sequence block x candidate chunk) per iteration,
+ *   "tile_n"       candidate columns per unit,
+ *   "grid"         CTAs launched,
+ *   "launches"     kernels launched by the call,
+ *   "kernel_ns"    device time of the main kernel (CUDA events; 0 if unknown). */
+int64_t dseq_last_stat(const char *name);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char *dseq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSEQ_H */

@@ -1,0 +1,140 @@
+"""GPU parity of the best-matching-unit search (both engines) against the
+CPU oracle, through the C ABI; worked cases, edge cases, full sizes."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+
+import workloads
+from parity import check_bmu
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module")
+def es():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from embedding_similarity_scan_gb300 import build as esb
+
+    esb.build()
+    import embedding_similarity_scan_gb300 as mod
+
+    mod.load()
+    return mod
+
+
+@pytest.fixture(autouse=True)
+def _reset_options(es):
+    yield
+    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0)):
+        es.dseq_set_option(name, v)
+
+
+def _bmu(es, X, W, engine=0, tile_n=0):
+    es.dseq_set_option("engine", engine)
+    es.dseq_set_option("tile_n", tile_n)
+    idx, dist = es.bmu_search(torch.from_numpy(X).cuda(), torch.from_numpy(W).cuda())
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), dist.cpu().numpy()
+
+
+SMALL = [
+    (300, 1000, 40),    # ragged n, M, D
+    (128, 256, 256),    # exactly one unit
+    (1, 1, 1),
+    (5, 3000, 7),
+    (1000, 700, 300),   # D not a multiple of 32, several K blocks
+]
+
+
+@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"n{c[0]}_M{c[1]}_D{c[2]}")
+def test_small(es, engine, case):
+    n, M, D = case
+    X = workloads.bmu_samples(n, D, seed=n + M)
+    W = workloads.codebook(M, D, seed=n + M)
+    idx, dist = _bmu(es, X, W, engine)
+    check_bmu(X, W, np.arange(n), idx, dist)
+
+
+def test_lattice_golden(es):
+    W = np.array([[a, b] for a in range(-3, 4) for b in range(-3, 4)], np.float32)
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "bmu_lattice.txt"))
+            if l.startswith("sample")]
+    X = np.array([[float(r[1]), float(r[2])] for r in rows], np.float32)
+    want = [int(r[3]) for r in rows]
+    dwant = np.array([float(r[4]) for r in rows])
+    for engine in (0, 1):
+        idx, dist = _bmu(es, X, W, engine)
+        assert idx.tolist() == want
+        assert np.allclose(dist, dwant, atol=1e-5)
+
+
+def test_samples_in_codebook_and_duplicates(es):
+    rng = np.random.default_rng(4)
+    W = rng.uniform(-1, 1, (500, 64)).astype(np.float32)
+    W[300] = W[17]
+    W[499] = W[2]
+    X = W[[17, 300, 2, 499, 123]].copy()
+    for engine in (0, 1):
+        idx, dist = _bmu(es, X, W, engine)
+        assert idx.tolist() == [17, 17, 2, 2, 123]
+        assert np.all(np.abs(dist) <= 1e-5 * 2 * (W[[17, 17, 2, 2, 123]] ** 2).sum(1))
+
+
+def test_scale_invariance_of_split(es):
+    """Rows of very different magnitudes (the per-row power-of-two scaling)."""
+    rng = np.random.default_rng(8)
+    W = rng.uniform(-1, 1, (700, 32)).astype(np.float32)
+    W[::3] *= 1e3
+    W[1::3] *= 1e-3
+    X = (W[rng.integers(0, 700, 400)] + rng.normal(0, 1e-2, (400, 32))).astype(np.float32)
+    idx, dist = _bmu(es, X, W)
+    check_bmu(X, W, np.arange(400), idx, dist)
+
+
+def test_tile_width_does_not_change_result(es):
+    X = workloads.bmu_samples(2000, 96, seed=2)
+    W = workloads.codebook(3000, 96, seed=2)
+    ref = _bmu(es, X, W, tile_n=256)
+    for tn in (32, 128, 160):
+        got = _bmu(es, X, W, tile_n=tn)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+def test_host_buffers(es):
+    X = workloads.bmu_samples(257, 24, seed=6)
+    W = workloads.codebook(513, 24, seed=6)
+    idx, dist = es.bmu_search(X, W)
+    assert isinstance(idx, np.ndarray)
+    check_bmu(X, W, np.arange(257), idx, dist)
+
+
+def test_invalid(es):
+    X = np.zeros((4, 8), np.float32)
+    W = np.ones((6, 8), np.float32)
+    W[2, 2] = np.inf
+    with pytest.raises(es.DseqError) as ei:
+        es.bmu_search(torch.from_numpy(X).cuda(), torch.from_numpy(W).cuda())
+    assert ei.value.code == es.DSEQ_ENONFINITE
+    with pytest.raises(ValueError):
+        es.bmu_search(X, np.ones((6, 9), np.float32))
+
+
+@pytest.mark.parametrize("name", ["som256", "som512"])
+def test_full_size_sampled(es, name):
+    """The full configurations, checked on a seeded sample of rows."""
+    cfg = workloads.BMU[name]
+    X = cfg.samples(seed=0)
+    W = cfg.codebook(seed=0)
+    idx, dist = _bmu(es, X, W)
+    sample = np.sort(np.random.default_rng(0).choice(cfg.n, cfg.oracle_samples, replace=False))
+    check_bmu(X, W, sample, idx, dist)
+    assert np.all((idx >= 0) & (idx < cfg.M)) and np.all(dist >= 0)

@@ -1,0 +1,219 @@
+"""GPU parity of the diversity scan (both engines) against the CPU oracle,
+through the C ABI, under teacher forcing; edge cases and error paths."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import workloads
+from parity import check_dseq_teacher_forced, check_picks_valid
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def es():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from embedding_similarity_scan_gb300 import build as esb
+
+    esb.build()
+    import embedding_similarity_scan_gb300 as mod
+
+    mod.load()
+    return mod
+
+
+@pytest.fixture(autouse=True)
+def _reset_options(es):
+    yield
+    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("timeout_ms", 10000),
+                    ("fault_skip_arrive", 0)):
+        es.dseq_set_option(name, v)
+
+
+def _run(es, E, starts, L, mask=None, trace_seqs=None, engine=0, tile_n=0, grid=0):
+    dev = torch.device("cuda")
+    es.dseq_set_option("engine", engine)
+    es.dseq_set_option("tile_n", tile_n)
+    es.dseq_set_option("grid", grid)
+    ctx = es.dseq_create(torch.from_numpy(E).to(dev))
+    try:
+        st = torch.from_numpy(np.asarray(starts, np.int32)).to(dev)
+        mk = None if mask is None else torch.from_numpy(np.asarray(mask, np.uint8)).to(dev)
+        if trace_seqs is None:
+            picks = es.dseq_run(ctx, st, L, mask=mk)
+            torch.cuda.synchronize()
+            return picks.cpu().numpy(), None
+        tr = torch.from_numpy(np.asarray(trace_seqs, np.int32)).to(dev)
+        picks, trace = es.dseq_run_trace(ctx, st, L, tr, mask=mk)
+        torch.cuda.synchronize()
+        return picks.cpu().numpy(), trace.cpu().numpy()
+    finally:
+        ctx.close()
+
+
+SMALL = [
+    # (N, D, B, L, kind, masked fraction)
+    (512, 64, 8, 32, "gaussian", 0.0),      # the tiny configuration
+    (1000, 96, 200, 16, "clustered", 0.0),  # ragged N, B, several tiles
+    (777, 33, 130, 20, "gaussian", 0.05),   # D not a multiple of 32, masked rows
+    (300, 1, 5, 10, "gaussian", 0.0),       # D = 1: every distance is 0 or 2
+    (2049, 200, 129, 12, "clustered", 0.1),
+]
+
+
+@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
+def test_small_teacher_forced(es, engine, case):
+    N, D, B, L, kind, frac = case
+    E = workloads.gaussian_table(N, D, seed=N) if kind == "gaussian" else \
+        workloads.clustered_table(N, D, n_centres=16, seed=N)
+    starts = workloads.starts(N, B, seed=N)
+    mask = None
+    if frac > 0:
+        rng = np.random.default_rng(N)
+        mask = (rng.random(N) < frac).astype(np.uint8)
+        mask[starts[: B // 3]] = 1  # some starts are masked themselves
+    trace_seqs = np.arange(B, dtype=np.int32) if B <= 200 else \
+        np.sort(np.random.default_rng(1).choice(B, 64, replace=False)).astype(np.int32)
+    picks, trace = _run(es, E, starts, L, mask, trace_seqs, engine=engine)
+    check_picks_valid(starts, mask, picks, N)
+    check_dseq_teacher_forced(E, starts, mask, picks, trace, trace_seqs)
+
+
+def test_picks_identical_across_candidate_tiles(es):
+    """Candidate tiling does not reorder any dot product, so the picks (and
+    the running minima) must be bit-identical for every tile width."""
+    N, D, B, L = 3000, 128, 300, 24
+    E = workloads.clustered_table(N, D, n_centres=8, seed=11)
+    starts = workloads.starts(N, B, seed=11)
+    ref, ref_tr = _run(es, E, starts, L, trace_seqs=[0, 7, 299], tile_n=256)
+    for tn in (32, 96, 128, 224):
+        got, tr = _run(es, E, starts, L, trace_seqs=[0, 7, 299], tile_n=tn)
+        assert np.array_equal(got, ref), f"tile_n={tn} changes the picks"
+        assert np.array_equal(tr, ref_tr), f"tile_n={tn} changes the running minima"
+    got, _ = _run(es, E, starts, L, grid=7)
+    assert np.array_equal(got, ref), "grid size changes the picks"
+
+
+def test_exhaustion_boundary(es):
+    """L = every candidate a sequence has left: the last picks are forced."""
+    N, D = 97, 16
+    E = workloads.gaussian_table(N, D, seed=3)
+    mask = np.zeros(N, np.uint8)
+    mask[[3, 50, 96]] = 1
+    starts = np.array([0, 50, 96, 10], np.int32)  # two masked starts
+    L = N - 3 - 1  # sequences whose start is unmasked have N - 4 left
+    with pytest.raises(es.DseqError) as ei:
+        _run(es, E, starts, L + 1, mask)
+    assert ei.value.code == es.DSEQ_EINVAL
+    picks, trace = _run(es, E, starts, L, mask, trace_seqs=[0, 1, 2, 3])
+    check_picks_valid(starts, mask, picks, N)
+    check_dseq_teacher_forced(E, starts, mask, picks, trace, [0, 1, 2, 3])
+
+
+def test_orthonormal_ties_lowest_index(es):
+    """Every distance between distinct rows of the identity is exactly 1, so
+    every pick is a tie and the picks are the ascending unmasked indices."""
+    N = 64
+    E = np.eye(N, dtype=np.float32)
+    starts = np.array([0, 5, 63], np.int32)
+    for engine in (0, 1):
+        picks, _ = _run(es, E, starts, N - 1, engine=engine)
+        for b, s in enumerate(starts):
+            assert picks[b].tolist() == [c for c in range(N) if c != s]
+
+
+def test_square4_worked_example(es):
+    E = np.array([[1, 0], [0, 1], [-1, 0], [0, -1]], np.float32) * \
+        np.array([[2.0], [0.5], [3.0], [7.0]], np.float32)
+    for engine in (0, 1):
+        picks, _ = _run(es, E, np.array([0, 3, 1], np.int32), 3, engine=engine)
+        assert picks.tolist() == [[2, 1, 3], [1, 0, 2], [3, 0, 2]]
+
+
+def test_single_candidate_and_zero_length(es):
+    E = workloads.gaussian_table(1, 8, seed=0)
+    picks, _ = _run(es, E, np.array([0], np.int32), 0)
+    assert picks.shape == (1, 0)
+    E = workloads.gaussian_table(2, 8, seed=0)
+    picks, _ = _run(es, E, np.array([1], np.int32), 1)
+    assert picks.tolist() == [[0]]
+
+
+def test_invalid_arguments(es):
+    N = 50
+    E = workloads.gaussian_table(N, 8, seed=0)
+    for bad_starts in ([0, 50], [-1], [3, 3]):
+        with pytest.raises(es.DseqError) as ei:
+            _run(es, E, np.array(bad_starts, np.int32), 2)
+        assert ei.value.code == es.DSEQ_EINVAL
+    with pytest.raises(es.DseqError) as ei:
+        _run(es, E, np.array([0], np.int32), N)
+    assert ei.value.code == es.DSEQ_EINVAL
+    bad = E.copy()
+    bad[7, 3] = np.nan
+    with pytest.raises(es.DseqError) as ei:
+        es.dseq_create(torch.from_numpy(bad).cuda())
+    assert ei.value.code == es.DSEQ_ENONFINITE
+    bad = E.copy()
+    bad[9] = 0.0
+    with pytest.raises(es.DseqError) as ei:
+        es.dseq_create(torch.from_numpy(bad).cuda())
+    assert ei.value.code == es.DSEQ_ENONFINITE
+
+
+def test_host_buffers(es):
+    """Host (numpy) table, starts and picks: the library stages the copies."""
+    N, D, B, L = 600, 48, 20, 10
+    E = workloads.gaussian_table(N, D, seed=21)
+    starts = workloads.starts(N, B, seed=21)
+    ctx = es.dseq_create(E)
+    try:
+        host_picks = es.dseq_run(ctx, starts, L)
+    finally:
+        ctx.close()
+    assert isinstance(host_picks, np.ndarray)
+    dev_picks, _ = _run(es, E, starts, L)
+    assert np.array_equal(host_picks, dev_picks)
+
+
+def test_barrier_timeout_returns_cleanly(es):
+    """One CTA skips its grid-barrier arrival: every wait runs out after the
+    time limit, the call returns DSEQ_ETIMEOUT, and the GPU stays usable."""
+    N, D, B, L = 2000, 64, 256, 4
+    E = workloads.gaussian_table(N, D, seed=5)
+    starts = workloads.starts(N, B, seed=5)
+    ref, _ = _run(es, E, starts, L)
+    es.dseq_set_option("timeout_ms", 500)
+    es.dseq_set_option("fault_skip_arrive", 1)
+    with pytest.raises(es.DseqError) as ei:
+        _run(es, E, starts, L)
+    assert ei.value.code == es.DSEQ_ETIMEOUT
+    es.dseq_set_option("fault_skip_arrive", 0)
+    es.dseq_set_option("timeout_ms", 10000)
+    again, _ = _run(es, E, starts, L)
+    assert np.array_equal(again, ref)
+
+
+FULL = ["page1", "d384", "d1024", "scale"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_teacher_forced(es, name):
+    """The full configurations, in the launch configuration the benchmark
+    times, with a seeded subset of sequences followed by the oracle."""
+    cfg = workloads.DIVERSITY[name]
+    E = cfg.table(seed=0)
+    starts = cfg.starts(seed=0)
+    tr = np.sort(np.random.default_rng(0).choice(cfg.B, cfg.oracle_seqs, replace=False))
+    picks, trace = _run(es, E, starts, cfg.L, trace_seqs=tr.astype(np.int32))
+    check_dseq_teacher_forced(E, starts[tr], None, picks[tr], trace, np.arange(tr.size))
+    # picks of every sequence: in range, distinct, never the start
+    assert np.all((picks >= 0) & (picks < cfg.N))
+    srt = np.sort(picks, axis=1)
+    assert not np.any(srt[:, 1:] == srt[:, :-1]), "a sequence repeats a pick"
+    assert not np.any(picks == starts[:, None]), "a sequence picks its start"
