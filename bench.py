@@ -79,7 +79,7 @@ def _profiled_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -93,7 +93,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -227,17 +227,15 @@ def _cpu_baseline(args, cfg):
                           f"({total_t:.1f} s of CPU work)"}
     X = cfg.samples(seed=0)
     W = cfg.codebook(seed=0)
-    n = 2 * threads
-    t0 = time.perf_counter()
-    oracle.bmu(X[:n], W, threads=threads)
-    dt = time.perf_counter() - t0
-    n2 = max(n, int(n * t_target / max(dt, 1e-3)))
-    t0 = time.perf_counter()
-    oracle.bmu(X[n:n + n2], W, threads=threads)
-    dt2 = time.perf_counter() - t0
-    return {"value": (n + n2) / (dt + dt2), "unit": "samples/s", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{n + n2} of {cfg.n} samples ({dt + dt2:.1f} s of CPU work)"}
+    n, done, total_t = 2 * threads, 0, 0.0
+    while total_t < t_target and done + n <= cfg.n:
+        t0 = time.perf_counter()
+        oracle.bmu(X[done:done + n], W, threads=threads)
+        total_t += time.perf_counter() - t0
+        done += n
+        n *= 2
+    return {"value": done / total_t, "unit": "samples/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} of {cfg.n} samples ({total_t:.1f} s of CPU work)"}
 
 
 def run_ours(args):
@@ -404,7 +402,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="page1",
