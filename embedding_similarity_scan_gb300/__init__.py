@@ -36,7 +36,8 @@ _CODES = {v: k for k, v in list(globals().items()) if k.startswith("DSEQ_")}
 
 # every extern "C" symbol declared in include/dseq.h
 EXPORTS = ("dseq_create", "dseq_run", "dseq_run_trace", "dseq_destroy", "bmu_search",
-           "dseq_set_option", "dseq_get_option", "dseq_last_stat", "dseq_last_error")
+           "bmu_search_noalloc", "dseq_set_option", "dseq_get_option", "dseq_last_stat",
+           "dseq_last_error")
 
 _lib = None
 
@@ -66,6 +67,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dseq_destroy.restype = None
     lib.bmu_search.argtypes = [vp, i64, vp, i64, i32, vp, vp, vp]
     lib.bmu_search.restype = ctypes.c_int
+    lib.bmu_search_noalloc.argtypes = [vp, i64, vp, i64, i32, vp, vp, vp]
+    lib.bmu_search_noalloc.restype = ctypes.c_int
     lib.dseq_set_option.argtypes = [vp, ctypes.c_char_p, i64]
     lib.dseq_set_option.restype = ctypes.c_int
     lib.dseq_get_option.argtypes = [vp, ctypes.c_char_p]
@@ -225,6 +228,17 @@ def bmu_search(X, W, idx=None, dist=None, stream=None):
         dist = _empty_like_kind(X, (n,), "float32")
     _check(lib.bmu_search(_ptr(X), n, _ptr(W), M, D, _ptr(idx), _ptr(dist),
                           _stream(stream, X, W, idx, dist)))
+    return idx, dist
+
+
+def bmu_search_noalloc(X, W, idx, dist, stream=None):
+    """bmu_search into caller-provided device outputs, using the library's
+    fixed scratch instead of allocating (for callers that cannot allocate
+    device memory); X, W, idx and dist must be CUDA tensors."""
+    lib = load()
+    n, D = int(X.shape[0]), int(X.shape[1])
+    _check(lib.bmu_search_noalloc(_ptr(X), n, _ptr(W), int(W.shape[0]), D, _ptr(idx),
+                                  _ptr(dist), _stream(stream, X, W, idx, dist)))
     return idx, dist
 
 

@@ -287,6 +287,29 @@ struct EventTimer {
 }  // namespace
 
 // ----------------------------------------------------------------------------
+// Host helpers shared with the allocation-free entry point (noalloc.cu).
+namespace dseq {
+namespace host {
+int fail_msg(int code, const char *msg) { return fail(code, "%s", msg); }
+void clear_error() {
+    g_err.clear();
+    g_stats = Stats();
+}
+bool is_device(const void *p) { return is_device_ptr(p); }
+int sm_count(int dev, int *sms) {
+    DeviceInfo info;
+    TRY(device_info(dev, info));
+    *sms = info.sms;
+    return DSEQ_OK;
+}
+int encode_map(CUtensorMap &map, const void *base, int64_t cols, int64_t rows, int box_rows) {
+    return encode_f16_map(map, base, cols, rows, box_rows);
+}
+int read_device_status(int *status_dev, cudaStream_t st) { return read_status(status_dev, st); }
+}  // namespace host
+}  // namespace dseq
+
+// ----------------------------------------------------------------------------
 struct dseq_ctx {
     int device = 0;
     int64_t N = 0;

@@ -131,4 +131,14 @@ void launch_bmu_finalize(const BmuArgs &a, cudaStream_t st);
 void launch_row_sqnorm(const float *A, int64_t rows, int D, float *out, int *status,
                        cudaStream_t st);
 
+// ---- host helpers of api.cu used by noalloc.cu --------------------------------
+namespace host {
+int fail_msg(int code, const char *msg);
+void clear_error();
+bool is_device(const void *p);
+int sm_count(int dev, int *sms);
+int encode_map(CUtensorMap &map, const void *base, int64_t cols, int64_t rows, int box_rows);
+int read_device_status(int *status_dev, cudaStream_t st);
+}  // namespace host
+
 }  // namespace dseq

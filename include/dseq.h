@@ -128,6 +128,32 @@ void dseq_destroy(dseq_ctx *ctx);
 int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, int32_t *idx,
                float *dist, void *cuda_stream);
 
+/* bmu_search for callers that cannot allocate device memory: a framework
+ * whose pooling allocator already holds nearly all of the GPU's memory, or a
+ * latency-critical loop that cannot absorb the device-wide synchronisation
+ * cudaMalloc / cudaFree may imply.  The method pages have no counterpart of
+ * this entry point; it exists for such callers only.
+ * Same arguments, semantics and results as bmu_search, except:
+ *  - X, W, idx and dist must all be device memory (nothing is staged);
+ *  - no call allocates: the scratch (split operands, norms, scales, keys,
+ *    status) lives in one fixed 64 MiB array inside the library, which every
+ *    GPU that loads the library holds until the process exits.  A request
+ *    needing more (about n*(6*Dp + 16) + M*(4*Dp + 8) bytes, Dp = D rounded
+ *    up to 32) fails with DSEQ_EINVAL and says how much it needed;
+ *  - every call shares that one array, so calls whose GPU work overlaps
+ *    (other threads, other streams) race and give wrong results: serialise
+ *    them.  Each call resets the parts that must start from a known value;
+ *  - the first call on a device looks up the array's device address (once per
+ *    device, with that device current), so make that first call before any
+ *    stream capture;
+ *  - the process-wide "engine", "tile_n", "grid" and "timeout_ms" options do
+ *    not apply: the tensor-core path always runs, 256 neurons per unit, one
+ *    CTA per SM, 10 s wait limit.
+ * Errors: DSEQ_EINVAL (as bmu_search, host pointers, scratch too small),
+ * DSEQ_ENONFINITE, DSEQ_ETIMEOUT, DSEQ_ECUDA. */
+int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int32_t D,
+                       int32_t *idx, float *dist, void *cuda_stream);
+
 /* Tuning and test knobs.  ctx = NULL sets the process-wide default used by
  * bmu_search and by contexts created afterwards; otherwise the setting
  * applies to that context only.  Names:
