@@ -37,7 +37,7 @@ _CODES = {v: k for k, v in list(globals().items()) if k.startswith("DSEQ_")}
 # every extern "C" symbol declared in include/dseq.h
 EXPORTS = ("dseq_create", "dseq_run", "dseq_run_trace", "dseq_destroy", "bmu_search",
            "bmu_search_noalloc", "dseq_set_option", "dseq_get_option", "dseq_last_stat",
-           "dseq_last_error")
+           "dseq_last_error", "dseq_get_timeline")
 
 _lib = None
 
@@ -63,6 +63,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dseq_run.restype = ctypes.c_int
     lib.dseq_run_trace.argtypes = [vp, vp, i32, i32, vp, vp, vp, i32, vp, vp]
     lib.dseq_run_trace.restype = ctypes.c_int
+    lib.dseq_get_timeline.argtypes = [vp, vp, i64, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.dseq_get_timeline.restype = ctypes.c_int
     lib.dseq_destroy.argtypes = [vp]
     lib.dseq_destroy.restype = None
     lib.bmu_search.argtypes = [vp, i64, vp, i64, i32, vp, vp, vp]
@@ -176,6 +178,21 @@ def dseq_create(table, stream=None) -> Context:
 
 def dseq_destroy(ctx: Context) -> None:
     ctx.close()
+
+
+def dseq_get_timeline(ctx: Context):
+    """Phase stamps [iters, grid, 8] (int64 ns) of the last timed run, or None."""
+    import numpy as np
+
+    lib = load()
+    it, gr = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.dseq_get_timeline(ctx.handle, None, 0, ctypes.byref(it), ctypes.byref(gr)))
+    if it.value == 0:
+        return None
+    out = np.empty((it.value, gr.value, 8), np.int64)
+    _check(lib.dseq_get_timeline(ctx.handle, out.ctypes.data, out.size, ctypes.byref(it),
+                                 ctypes.byref(gr)))
+    return out
 
 
 def dseq_run(ctx: Context, starts, L: int, mask=None, picks=None, stream=None):

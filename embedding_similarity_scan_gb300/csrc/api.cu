@@ -65,6 +65,7 @@ struct Options {
     int64_t grid = 0;
     int64_t timeout_ms = 10000;
     int64_t fault_skip_arrive = 0;
+    int64_t timeline = 0;
 };
 std::mutex g_opt_mu;
 Options g_defaults;
@@ -84,6 +85,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "timeout_ms") {
         if (v < 1 || v > 3600000) return fail(DSEQ_EINVAL, "timeout_ms out of range");
         o.timeout_ms = v;
+    } else if (n == "timeline") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "timeline must be 0 or 1");
+        o.timeline = v;
     } else if (n == "fault_skip_arrive") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "fault_skip_arrive must be 0 or 1");
         o.fault_skip_arrive = v;
@@ -101,6 +105,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "grid") return o.grid;
     if (n == "timeout_ms") return o.timeout_ms;
     if (n == "fault_skip_arrive") return o.fault_skip_arrive;
+    if (n == "timeline") return o.timeline;
     return -1;
 }
 
@@ -317,10 +322,11 @@ struct dseq_ctx {
     Options opt;
     DevBuf e_unit, e_split;
     // run workspace
-    DevBuf m, keys, q, status, barrier, starts, mask, picks, trace_slot;
+    DevBuf m, keys, q, status, barrier, starts, mask, picks, trace_slot, timeline;
+    int64_t timeline_iters = 0, timeline_grid = 0;
     ~dseq_ctx() {
-        DevBuf *all[] = {&e_unit, &e_split, &m,     &keys,  &q,          &status,
-                         &barrier, &starts, &mask, &picks, &trace_slot};
+        DevBuf *all[] = {&e_unit, &e_split, &m,     &keys,       &q,       &status, &barrier,
+                         &starts, &mask,    &picks, &trace_slot, &timeline};
         for (DevBuf *b : all) b->release();
     }
 };
@@ -405,6 +411,19 @@ int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device, v
 }
 
 void dseq_destroy(dseq_ctx *ctx) { delete ctx; }
+
+int dseq_get_timeline(dseq_ctx *ctx, int64_t *out, int64_t capacity, int32_t *iters,
+                      int32_t *grid) {
+    g_err.clear();
+    if (!ctx || !iters || !grid) return fail(DSEQ_EINVAL, "NULL argument");
+    *iters = (int32_t)ctx->timeline_iters;
+    *grid = (int32_t)ctx->timeline_grid;
+    const int64_t n = ctx->timeline_iters * ctx->timeline_grid * kTimelineSlots;
+    if (n == 0 || !out) return DSEQ_OK;
+    if (capacity < n) return fail(DSEQ_EINVAL, "timeline needs %lld slots", (long long)n);
+    CUDA_TRY(cudaMemcpy(out, ctx->timeline.p, (size_t)n * sizeof(int64_t), cudaMemcpyDeviceToHost));
+    return DSEQ_OK;
+}
 
 static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
                     const uint8_t *mask, int32_t *picks, const int32_t *trace_seqs,
@@ -517,6 +536,18 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.Dp = ctx->Dp;
         a.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
         a.fault_skip_arrive = (int)ctx->opt.fault_skip_arrive;
+        // the split table stays L2-resident across iterations only if it is a
+        // small part of L2; larger tables stream through once per iteration
+        a.keep_table = (double)N * 2 * ctx->Dp * sizeof(__half) <= info.l2 / 3.0 ? 1 : 0;
+        a.timeline = nullptr;
+        ctx->timeline_iters = ctx->timeline_grid = 0;
+        if (ctx->opt.timeline) {
+            TRY(ctx->timeline.ensure((size_t)L * plan.grid * kTimelineSlots * sizeof(unsigned long long)));
+            CUDA_TRY(cudaMemsetAsync(ctx->timeline.p, 0, (size_t)L * plan.grid * kTimelineSlots * sizeof(unsigned long long), st));
+            a.timeline = ctx->timeline.as<unsigned long long>();
+            ctx->timeline_iters = L;
+            ctx->timeline_grid = plan.grid;
+        }
         CUDA_TRY(cudaMemsetAsync(ctx->barrier.p, 0, sizeof(unsigned), st));
         launch_tc_dseq_init(a, plan, ctx->starts.as<int32_t>(), d_mask, st);
         CUDA_TRY(cudaGetLastError());

@@ -49,6 +49,12 @@ __host__ __device__ __forceinline__ int64_t tc_m_offset(int64_t unit, int tile_n
     return unit * (int64_t)(kUnitRows * tile_n) + ((((g * 4 + q) * 8 + v) * 32 + t) * 4 + e);
 }
 
+// Phase stamps per CTA and iteration of the persistent diversity kernel:
+// 0 iteration start, 1 first TMA issued, 2 first MMA issued, 3 last MMA
+// committed, 4 epilogue done (first epilogue warp), 5 after the first grid
+// barrier, 6 after the commit (CTA thread 0), 7 after the second grid barrier.
+constexpr int kTimelineSlots = 8;
+
 struct TcPlan {
     int n_beta;    // sequence blocks (ceil(B / 128))
     int n_chunk;   // candidate chunks (ceil(N / tile_n))
@@ -85,6 +91,9 @@ struct TcDseqArgs {
     int B, L, Dp;
     uint64_t timeout_ns;
     int fault_skip_arrive;
+    int keep_table;  // 1: load table tiles with the evict-last L2 policy (table fits L2)
+    // optional [L][grid][kTimelineSlots] globaltimer stamps (nullptr = off)
+    unsigned long long *timeline;
 };
 void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *starts,
                          const uint8_t *mask, cudaStream_t st);

@@ -112,6 +112,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            // the codebook slice is reused by every sample block: keep it in L2;
+            // a sample block is reused only by the units running at the same time
+            const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
             uint32_t fills = 0;
             for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
                 int beta, j;
@@ -126,11 +129,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint8_t *sb = sa + 3 * kSubA;
                     mbar_arrive_expect_tx(&full[s], tx_bytes);
                     const int x = kb * kKBlock;
-                    tma_load_2d(sa, &tmap_x, &full[s], x, yx);
-                    tma_load_2d(sa + kSubA, &tmap_x, &full[s], a.Dp + x, yx);
-                    tma_load_2d(sa + 2 * kSubA, &tmap_x, &full[s], 2 * a.Dp + x, yx);
-                    tma_load_2d(sb, &tmap_w, &full[s], x, yw);
-                    tma_load_2d(sb + kSubBMax, &tmap_w, &full[s], a.Dp + x, yw);
+                    tma_load_2d_hint(sa, &tmap_x, &full[s], x, yx, once);
+                    tma_load_2d_hint(sa + kSubA, &tmap_x, &full[s], a.Dp + x, yx, once);
+                    tma_load_2d_hint(sa + 2 * kSubA, &tmap_x, &full[s], 2 * a.Dp + x, yx, once);
+                    tma_load_2d_hint(sb, &tmap_w, &full[s], x, yw, keep);
+                    tma_load_2d_hint(sb + kSubBMax, &tmap_w, &full[s], a.Dp + x, yw, keep);
                     ++fills;
                 }
             }

@@ -105,6 +105,11 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
         a.keys[i] = 0ull;
 }
 
+__device__ __forceinline__ void stamp(const TcDseqArgs &a, int t, int slot) {
+    if (a.timeline)
+        a.timeline[((size_t)t * gridDim.x + blockIdx.x) * kTimelineSlots + slot] = globaltimer_ns();
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_dseq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
@@ -164,10 +169,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     for (int t = 0; t < a.L; ++t) {
         if (*abort_flag) break;
+        if (threadIdx.x == 0) stamp(a, t, 0);
         if (warp == 0) {
             // ---------------- TMA producer ----------------
             if (lane == 0) {
                 fence_proxy_async_global();
+                const uint64_t keep = l2_policy_evict_last();
+                const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
+                bool first = true;
                 for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
                     const int beta = (int)(u % p.n_beta), j = (int)(u / p.n_beta);
                     const int yq = beta * kUnitRows, ye = j * (int)tile_n;
@@ -179,12 +188,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         uint8_t *sa = smem + s * kStageBytes;
                         uint8_t *sb = sa + 3 * kSubA;
                         mbar_arrive_expect_tx(&full[s], tx_bytes);
+                        if (first) {
+                            stamp(a, t, 1);
+                            first = false;
+                        }
                         const int x = kb * kKBlock;
-                        tma_load_2d(sa, &tmap_q, &full[s], x, yq);
-                        tma_load_2d(sa + kSubA, &tmap_q, &full[s], a.Dp + x, yq);
-                        tma_load_2d(sa + 2 * kSubA, &tmap_q, &full[s], 2 * a.Dp + x, yq);
-                        tma_load_2d(sb, &tmap_e, &full[s], x, ye);
-                        tma_load_2d(sb + kSubBMax, &tmap_e, &full[s], a.Dp + x, ye);
+                        tma_load_2d_hint(sa, &tmap_q, &full[s], x, yq, keep);
+                        tma_load_2d_hint(sa + kSubA, &tmap_q, &full[s], a.Dp + x, yq, keep);
+                        tma_load_2d_hint(sa + 2 * kSubA, &tmap_q, &full[s], 2 * a.Dp + x, yq, keep);
+                        tma_load_2d_hint(sb, &tmap_e, &full[s], x, ye, table_pol);
+                        tma_load_2d_hint(sb + kSubBMax, &tmap_e, &full[s], a.Dp + x, ye, table_pol);
                         ++fills;
                     }
                 }
@@ -193,6 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } else if (warp == 1) {
             // ---------------- MMA issuer ----------------
             if (lane == 0) {
+                bool first = true;
                 for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
                     const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
                     if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
@@ -209,6 +223,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             break;
                         }
                         tc_fence_after();
+                        if (first) {
+                            stamp(a, t, 2);
+                            first = false;
+                        }
                         const uint32_t sa = smem_u32(smem + s * kStageBytes);
                         const uint32_t sb = sa + 3 * kSubA;
 #pragma unroll
@@ -228,12 +246,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     umma_commit(&acc_full[buf]);
                     ++acc_uses;
                 }
+                stamp(a, t, 3);
             }
             __syncwarp();
         } else {
             // ---------------- epilogue ----------------
             const int e = warp - 2, q = warp & 3, h = e >> 2;
             const int r = 32 * q + lane;
+            const uint64_t stream = l2_policy_evict_first();
             for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
                 const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
                 const int beta = (int)(u % p.n_beta), j = (int)(u / p.n_beta);
@@ -242,7 +262,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float4 mcur[8], mnext[8];
                 if (h < groups) {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) mcur[v] = mt[((h * 4 + q) * 8 + v) * 32 + lane];
+                    for (int v = 0; v < 8; ++v)
+                        mcur[v] = ld_cg_hint(&mt[((h * 4 + q) * 8 + v) * 32 + lane], stream);
                 }
                 // every lane waits; the warp proceeds only if all of them saw the phase
                 const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status,
@@ -257,7 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (gn < groups) {
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            mnext[v] = mt[((gn * 4 + q) * 8 + v) * 32 + lane];
+                            mnext[v] = ld_cg_hint(&mt[((gn * 4 + q) * 8 + v) * 32 + lane], stream);
                     }
                     float acc[32];
                     tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
@@ -276,8 +297,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 best_c = cbase + 4 * v + z;
                             }
                         }
-                        mt[((g * 4 + q) * 8 + v) * 32 + lane] = make_float4(mv[0], mv[1], mv[2],
-                                                                            mv[3]);
+                        st_cg_hint(&mt[((g * 4 + q) * 8 + v) * 32 + lane],
+                                   make_float4(mv[0], mv[1], mv[2], mv[3]), stream);
                     }
                     if (gn < groups) {
 #pragma unroll
@@ -291,6 +312,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int b = beta * kUnitRows + r;
                 if (best > -INFINITY && b < a.B) atomicMax(a.keys + b, max_key(best, best_c));
             }
+            if (warp == 2 && lane == 0) stamp(a, t, 4);
         }
 
         // ---- all partial winners of iteration t are in the keys ----
@@ -298,64 +320,82 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           skip_arrive))
             break;
         skip_arrive = false;
+        if (threadIdx.x == 0) stamp(a, t, 5);
 
-        // ---- commit: one warp per sequence ----
+        // ---- commit: each warp takes a contiguous run of sequences ----
         {
-            const int gw = blockIdx.x * (kTcThreads / 32) + warp;
             const int nw = gridDim.x * (kTcThreads / 32);
-            const int vec = a.Dp / 8;
-            for (int b = gw; b < a.B; b += nw) {
-                const unsigned long long key = a.keys[b];
-                __syncwarp();
-                if (key == 0ull) {
-                    if (lane == 0) {
+            const int gw = blockIdx.x * (kTcThreads / 32) + warp;
+            const int per = (a.B + nw - 1) / nw;
+            const int b_lo = gw * per, b_hi = min(a.B, b_lo + per);
+            const int vec = a.Dp / 8;  // 16-byte vectors per row segment
+            for (int base = b_lo; base < b_hi; base += 32) {
+                const int cnt = min(32, b_hi - base);
+                const int b = base + lane;
+                const bool mine = lane < cnt;
+                const unsigned long long key = mine ? __ldcg(a.keys + b) : 0ull;
+                const uint32_t w = max_key_index(key);
+                if (mine) {
+                    if (key == 0ull) {
                         atomicOr(a.status, kStatusNoWinner);
                         a.picks[(int64_t)b * a.L + t] = -1;
+                    } else {
+                        a.keys[b] = 0ull;
+                        a.picks[(int64_t)b * a.L + t] = (int32_t)w;
                     }
-                    continue;
-                }
-                const uint32_t w = max_key_index(key);
-                const int beta = b / kUnitRows, r = b % kUnitRows;
-                if (lane == 0) {
-                    a.keys[b] = 0ull;
-                    a.picks[(int64_t)b * a.L + t] = (int32_t)w;
                 }
                 if (a.trace_slot) {
-                    const int slot = a.trace_slot[b];
-                    if (slot >= 0) {
+                    // parity-check path: copy the traced rows of m before masking
+                    for (int i = 0; i < cnt; ++i) {
+                        const int bi = base + i;
+                        const int slot = a.trace_slot[bi];
+                        if (slot < 0) continue;
+                        const int beta = bi / kUnitRows, r = bi % kUnitRows;
                         float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
                         for (int64_t c = lane; c < a.N; c += 32) {
                             const int jj = (int)(c / tile_n), cc = (int)(c - (int64_t)jj * tile_n);
-                            dst[c] = a.m[tc_m_offset((int64_t)jj * p.n_beta + beta, tile_n, r, cc)];
+                            dst[c] = __ldcg(a.m + tc_m_offset((int64_t)jj * p.n_beta + beta, tile_n, r, cc));
                         }
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
-                if (lane == 0) {
+                if (mine && key != 0ull) {
+                    const int beta = b / kUnitRows, r = b % kUnitRows;
                     const int jw = (int)(w / tile_n), cw = (int)(w - (uint32_t)jw * tile_n);
                     a.m[tc_m_offset((int64_t)jw * p.n_beta + beta, tile_n, r, cw)] = -INFINITY;
                 }
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.e_split + (int64_t)w * 2 * a.Dp);
-                uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * 3 * a.Dp);
+                // next queries: the split rows of the winners, all rows of the run
+                // copied by the whole warp, loads first (read-only path)
                 const __half2 scale = __float2half2_rn(4096.0f);
-                for (int k = lane; k < vec; k += 32) {
-                    const uint4 hi = src[k], lo = src[vec + k];
-                    uint4 hi12 = hi;
-                    __half2 *h2 = reinterpret_cast<__half2 *>(&hi12);
+                for (int i = 0; i < cnt; ++i) {
+                    const unsigned long long ki = __shfl_sync(0xffffffffu, key, i);
+                    const uint32_t wi = __shfl_sync(0xffffffffu, w, i);
+                    if (ki == 0ull) continue;
+                    const uint4 *src =
+                        reinterpret_cast<const uint4 *>(a.e_split + (int64_t)wi * 2 * a.Dp);
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * 3 * a.Dp);
+#pragma unroll 4
+                    for (int k = lane; k < vec; k += 32) {
+                        const uint4 hi = __ldg(src + k), lo = __ldg(src + vec + k);
+                        uint4 hi12 = hi;
+                        __half2 *h2 = reinterpret_cast<__half2 *>(&hi12);
 #pragma unroll
-                    for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
-                    dst[k] = hi12;
-                    dst[vec + k] = hi;
-                    dst[2 * vec + k] = lo;
+                        for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
+                        dst[k] = hi12;
+                        dst[vec + k] = hi;
+                        dst[2 * vec + k] = lo;
+                    }
                 }
             }
             fence_proxy_async_global();
+            if (threadIdx.x == 0) stamp(a, t, 6);
         }
 
         // ---- the next queries are written ----
         if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
                           false))
             break;
+        if (threadIdx.x == 0) stamp(a, t, 7);
     }
 
     // ---- teardown: drain what this CTA still has in flight, free TMEM ----

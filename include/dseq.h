@@ -113,6 +113,18 @@ int dseq_run_trace(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
                    const uint8_t *mask, int32_t *picks, const int32_t *trace_seqs,
                    int32_t n_trace, float *trace_mindist, void *cuda_stream);
 
+/* Phase timestamps of the last dseq_run on ctx made with the "timeline"
+ * option on (tensor-core path).  out receives iters x grid x 8 int64
+ * nanosecond stamps (%globaltimer): per iteration and CTA, 0 iteration start,
+ * 1 first TMA issued, 2 first MMA issued, 3 last MMA committed, 4 epilogue
+ * done, 5 after the first grid barrier, 6 commit done, 7 after the second
+ * grid barrier.  *iters and *grid receive the dimensions (0 when no timeline
+ * was recorded); capacity is the length of out in elements; out = NULL only
+ * queries the dimensions.
+ * Errors: DSEQ_EINVAL (NULL ctx/iters/grid, capacity too small), DSEQ_ECUDA. */
+int dseq_get_timeline(dseq_ctx *ctx, int64_t *out, int64_t capacity, int32_t *iters,
+                      int32_t *grid);
+
 /* Free the context and everything it owns.  NULL is accepted. */
 void dseq_destroy(dseq_ctx *ctx);
 
@@ -162,6 +174,9 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 32 in [32, 256]; 0 = chosen from the shape (default).
  *   "grid"        persistent CTAs; 0 = one per SM (default).
  *   "timeout_ms"  limit of every device-side wait (default 10000).
+ *   "timeline"    1 = dseq_run records, per CTA and iteration of the
+ *                 tensor-core kernel, device timestamps of its phases (read
+ *                 them back with dseq_get_timeline); default 0.
  *   "fault_skip_arrive"  test only: 1 makes CTA 0 skip its first grid-barrier
  *                 arrival, so the other CTAs' waits run out (the kernel then
  *                 returns DSEQ_ETIMEOUT without hanging).
