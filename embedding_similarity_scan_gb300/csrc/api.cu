@@ -66,6 +66,7 @@ struct Options {
     int64_t timeout_ms = 10000;
     int64_t fault_skip_arrive = 0;
     int64_t timeline = 0;
+    int64_t pair = 1;
 };
 std::mutex g_opt_mu;
 Options g_defaults;
@@ -85,6 +86,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "timeout_ms") {
         if (v < 1 || v > 3600000) return fail(DSEQ_EINVAL, "timeout_ms out of range");
         o.timeout_ms = v;
+    } else if (n == "pair") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "pair must be 0 or 1");
+        o.pair = v;
     } else if (n == "timeline") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "timeline must be 0 or 1");
         o.timeline = v;
@@ -106,6 +110,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "timeout_ms") return o.timeout_ms;
     if (n == "fault_skip_arrive") return o.fault_skip_arrive;
     if (n == "timeline") return o.timeline;
+    if (n == "pair") return o.pair;
     return -1;
 }
 
@@ -461,7 +466,9 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         }
     }
     std::vector<int32_t> h_slot;
-    const int64_t Bp = round_up(B, kUnitRows);
+    // CTA pairs work on pairs of 128-sequence blocks: pad B to 256 there
+    const bool pair = ctx->opt.engine == 0 && ctx->opt.pair != 0;
+    const int64_t Bp = round_up(B, pair ? 2 * kUnitRows : kUnitRows);
     if (n_trace > 0) {
         if (!trace_seqs || !trace_mindist) return fail(DSEQ_EINVAL, "trace arrays are NULL");
         if (!is_device_ptr(trace_mindist)) return fail(DSEQ_EINVAL, "trace_mindist must be device memory");
@@ -509,17 +516,29 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
 
     if (ctx->opt.engine == 0) {
         // ---- tensor-core persistent kernel ----
-        TcPlan plan;
+        TcPlan plan{};
         plan.n_beta = (int)(Bp / kUnitRows);
-        const int grid_cap = ctx->opt.grid > 0 ? (int)std::min<int64_t>(ctx->opt.grid, info.sms) : info.sms;
-        plan.tile_n = ctx->opt.tile_n > 0 ? (int)ctx->opt.tile_n : choose_tile_n(plan.n_beta, N, grid_cap);
-        plan.n_chunk = (int)((N + plan.tile_n - 1) / plan.tile_n);
-        plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
+        plan.pair = pair ? 1 : 0;
+        int grid_cap = ctx->opt.grid > 0 ? (int)std::min<int64_t>(ctx->opt.grid, info.sms) : info.sms;
+        if (pair) {
+            // whole clusters of two, no more than can be co-resident
+            const int max_clusters = tc_dseq_pair_max_clusters(256);
+            if (max_clusters < 1) return fail(DSEQ_ELAUNCH, "no CTA pair of the pair kernel fits on this device");
+            grid_cap = std::max(2, std::min(grid_cap / 2, max_clusters) * 2);
+            plan.tile_n = ctx->opt.tile_n > 0 ? (int)ctx->opt.tile_n
+                                              : choose_tile_n(plan.n_beta / 2, N, grid_cap / 2);
+            plan.n_chunk = (int)((N + plan.tile_n - 1) / plan.tile_n);
+            plan.grid = 2 * (int)std::min<int64_t>(grid_cap / 2, (int64_t)(plan.n_beta / 2) * plan.n_chunk);
+        } else {
+            plan.tile_n = ctx->opt.tile_n > 0 ? (int)ctx->opt.tile_n : choose_tile_n(plan.n_beta, N, grid_cap);
+            plan.n_chunk = (int)((N + plan.tile_n - 1) / plan.tile_n);
+            plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
+        }
         TRY(ctx->m.ensure((size_t)plan.units() * kUnitRows * plan.tile_n * sizeof(float)));
         TRY(ctx->q.ensure((size_t)Bp * 3 * ctx->Dp * sizeof(__half)));
         CUtensorMap tq, te;
         TRY(encode_f16_map(tq, ctx->q.p, 3 * ctx->Dp, Bp, kUnitRows));
-        TRY(encode_f16_map(te, ctx->e_split.p, 2 * ctx->Dp, N, plan.tile_n));
+        TRY(encode_f16_map(te, ctx->e_split.p, 2 * ctx->Dp, N, pair ? plan.tile_n / 2 : plan.tile_n));
         TcDseqArgs a;
         a.e_split = ctx->e_split.as<__half>();
         a.q_split = ctx->q.as<__half>();
@@ -698,7 +717,7 @@ int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, 
         launch_bmu_prepare(dW, M, D, Dp, 0, ws->w_split.as<__half>(), ws->wn.as<float>(),
                            ws->w_inv.as<float>(), a.status, st);
         CUDA_TRY(cudaGetLastError());
-        TcPlan plan;
+        TcPlan plan{};
         plan.n_beta = (int)((n + kUnitRows - 1) / kUnitRows);
         const int grid_cap = opt.grid > 0 ? (int)std::min<int64_t>(opt.grid, info.sms) : info.sms;
         plan.tile_n = opt.tile_n > 0 ? (int)opt.tile_n : 256;

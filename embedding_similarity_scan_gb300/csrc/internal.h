@@ -59,7 +59,8 @@ struct TcPlan {
     int n_beta;    // sequence blocks (ceil(B / 128))
     int n_chunk;   // candidate chunks (ceil(N / tile_n))
     int tile_n;    // candidate columns per unit
-    int grid;      // persistent CTAs
+    int grid;      // persistent CTAs (pair mode: even, two CTAs per cluster)
+    int pair;      // 1: CTA pairs share each MMA (cta_group::2), n_beta even
     __host__ __device__ int64_t units() const { return (int64_t)n_beta * n_chunk; }
 };
 
@@ -99,6 +100,8 @@ void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *st
                          const uint8_t *mask, cudaStream_t st);
 cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st);
+// clusters of two that can be co-resident for the pair kernel (0 on error)
+int tc_dseq_pair_max_clusters(int tile_n);
 
 // ---- diversity, FFMA path (ffma.cu) -----------------------------------------
 struct FfmaDseqArgs {

@@ -127,7 +127,7 @@ extern "C" int bmu_search_noalloc(const float *X, int64_t n, const float *W, int
                        const_cast<float *>(a.w_inv_scale), a.status, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return host::fail_msg(DSEQ_ECUDA, cudaGetErrorString(e));
-    TcPlan plan;
+    TcPlan plan{};
     plan.n_beta = (int)((n + kUnitRows - 1) / kUnitRows);
     plan.tile_n = 256;
     plan.n_chunk = (int)((M + plan.tile_n - 1) / plan.tile_n);

@@ -47,10 +47,19 @@ namespace dseq {
 namespace {
 
 constexpr uint32_t kSubA = kUnitRows * kKBlock * 2;  // one 128 x 32 fp16 sub-tile: 8 KB
-constexpr uint32_t kSubBMax = 256 * kKBlock * 2;     // one 256 x 32 fp16 sub-tile: 16 KB
-constexpr uint32_t kStageBytes = 3 * kSubA + 2 * kSubBMax;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
+
+// Stage geometry.  One CTA: A = 3 x (128 x 32), B = 2 x (tile_n x 32) fp16,
+// tile_n <= 256, 4 stages.  CTA pair: the B sub-tiles hold half of the
+// candidate chunk (<= 128 rows), so a stage is 40 KB and 5 stages fit.
+template <bool kPair>
+struct DseqCfg {
+    static constexpr int kStagesT = kPair ? 5 : kStages;
+    static constexpr uint32_t kSubB = (kPair ? 128u : 256u) * kKBlock * 2;
+    static constexpr uint32_t kStage = 3 * kSubA + 2 * kSubB;
+    static constexpr size_t kSmemBytes = (size_t)kStagesT * kStage + 1024 + 256;
+};
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -110,15 +119,20 @@ __device__ __forceinline__ void stamp(const TcDseqArgs &a, int t, int slot) {
         a.timeline[((size_t)t * gridDim.x + blockIdx.x) * kTimelineSlots + slot] = globaltimer_ns();
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_dseq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
                    const TcPlan p) {
+    using Cfg = DseqCfg<kPair>;
+    constexpr int kSt = Cfg::kStagesT;
+    constexpr uint32_t kSubB = Cfg::kSubB;
+    constexpr uint32_t kStageB = Cfg::kStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *acc_full = empty + kStages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kSt * kStageB);
+    uint64_t *empty = full + kSt;
+    uint64_t *acc_full = empty + kSt;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *final_bar = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(final_bar + 1);
@@ -126,15 +140,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t tmo = a.timeout_ns;
+    // pair mode: CTA rank 0 of each cluster leads (issues the MMAs, owns the
+    // full / acc_empty barriers that both CTAs feed)
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kSt; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&acc_full[s], 1);
-            mbar_init(&acc_empty[s], kEpiWarps);
+            mbar_init(&acc_empty[s], kEpiWarps * (kPair ? 2 : 1));
         }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
@@ -145,21 +163,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tmap_e);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        if (kPair) {
+            tmem_alloc_pair(tmem_slot, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    // both CTAs' barriers must be initialised before either signals the other
+    if (kPair) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int64_t units = p.units();
     const uint32_t tile_n = (uint32_t)p.tile_n;
-    const uint32_t sub_b = tile_n * kKBlock * 2;
-    const uint32_t tx_bytes = 3 * kSubA + 2 * sub_b;
+    // rows of this CTA's B sub-tile (pair: half of the candidate chunk)
+    const uint32_t b_rows = kPair ? tile_n / 2 : tile_n;
+    const uint32_t sub_b = b_rows * kKBlock * 2;
+    const uint32_t tx_bytes = (kPair ? 2u : 1u) * (3 * kSubA + 2 * sub_b);
     const int kblocks = a.Dp / kKBlock;
-    const uint32_t idesc = idesc_f16_f32(kUnitRows, tile_n);
+    const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kUnitRows : kUnitRows, tile_n);
     const int groups = (int)(tile_n / 32);
+    // work items: (sequence block, chunk) units, or (sequence block pair,
+    // chunk) for a cluster; both ordered candidate-chunk-major
+    const int n_pairs = p.n_beta / 2;
+    const int64_t work = kPair ? (int64_t)n_pairs * p.n_chunk : p.units();
+    const int64_t first_item = kPair ? (blockIdx.x >> 1) : blockIdx.x;
+    const int64_t item_stride = kPair ? (gridDim.x >> 1) : gridDim.x;
+    auto decode = [&](int64_t v, int &beta, int &j) {
+        if (kPair) {
+            beta = 2 * (int)(v % n_pairs) + (int)rank;
+            j = (int)(v / n_pairs);
+        } else {
+            beta = (int)(v % p.n_beta);
+            j = (int)(v / p.n_beta);
+        }
+    };
 
     uint32_t fills = 0;     // producer: stages filled so far
     uint32_t consumed = 0;  // MMA: stages consumed so far
@@ -177,37 +218,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint64_t keep = l2_policy_evict_last();
                 const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
                 bool first = true;
-                for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
-                    const int beta = (int)(u % p.n_beta), j = (int)(u / p.n_beta);
-                    const int yq = beta * kUnitRows, ye = j * (int)tile_n;
+                for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride) {
+                    int beta, j;
+                    decode(v, beta, j);
+                    const int yq = beta * kUnitRows;
+                    const int ye = j * (int)tile_n + (int)(rank * b_rows);
                     for (int kb = 0; kb < kblocks; ++kb) {
-                        const uint32_t s = fills % kStages, par = (fills / kStages) & 1u;
+                        const uint32_t s = fills % kSt, par = (fills / kSt) & 1u;
                         if (!mbar_wait_bounded(&empty[s], par ^ 1u, abort_flag, a.status, tmo,
                                                kStatusPipeTimeout))
                             break;
-                        uint8_t *sa = smem + s * kStageBytes;
+                        uint8_t *sa = smem + s * kStageB;
                         uint8_t *sb = sa + 3 * kSubA;
-                        mbar_arrive_expect_tx(&full[s], tx_bytes);
+                        if (leader) mbar_arrive_expect_tx(&full[s], tx_bytes);
                         if (first) {
                             stamp(a, t, 1);
                             first = false;
                         }
                         const int x = kb * kKBlock;
-                        tma_load_2d_hint(sa, &tmap_q, &full[s], x, yq, keep);
-                        tma_load_2d_hint(sa + kSubA, &tmap_q, &full[s], a.Dp + x, yq, keep);
-                        tma_load_2d_hint(sa + 2 * kSubA, &tmap_q, &full[s], 2 * a.Dp + x, yq, keep);
-                        tma_load_2d_hint(sb, &tmap_e, &full[s], x, ye, table_pol);
-                        tma_load_2d_hint(sb + kSubBMax, &tmap_e, &full[s], a.Dp + x, ye, table_pol);
+                        if (kPair) {
+                            // completion goes to the leader's barrier for this stage
+                            const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+                            tma_load_2d_pair(sa, &tmap_q, fb, x, yq, keep);
+                            tma_load_2d_pair(sa + kSubA, &tmap_q, fb, a.Dp + x, yq, keep);
+                            tma_load_2d_pair(sa + 2 * kSubA, &tmap_q, fb, 2 * a.Dp + x, yq, keep);
+                            tma_load_2d_pair(sb, &tmap_e, fb, x, ye, table_pol);
+                            tma_load_2d_pair(sb + kSubB, &tmap_e, fb, a.Dp + x, ye, table_pol);
+                        } else {
+                            tma_load_2d_hint(sa, &tmap_q, &full[s], x, yq, keep);
+                            tma_load_2d_hint(sa + kSubA, &tmap_q, &full[s], a.Dp + x, yq, keep);
+                            tma_load_2d_hint(sa + 2 * kSubA, &tmap_q, &full[s], 2 * a.Dp + x, yq,
+                                             keep);
+                            tma_load_2d_hint(sb, &tmap_e, &full[s], x, ye, table_pol);
+                            tma_load_2d_hint(sb + kSubB, &tmap_e, &full[s], a.Dp + x, ye,
+                                             table_pol);
+                        }
                         ++fills;
                     }
                 }
             }
             __syncwarp();
         } else if (warp == 1) {
-            // ---------------- MMA issuer ----------------
-            if (lane == 0) {
+            // ---------------- MMA issuer (pair: the leader only) ----------------
+            if (lane == 0 && leader) {
                 bool first = true;
-                for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+                for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride) {
                     const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
                     if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
                                            kStatusPipeTimeout))
@@ -216,7 +271,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t d_tmem = tmem_base + buf * kAccCols;
                     bool ok = true;
                     for (int kb = 0; kb < kblocks; ++kb) {
-                        const uint32_t s = consumed % kStages, par = (consumed / kStages) & 1u;
+                        const uint32_t s = consumed % kSt, par = (consumed / kSt) & 1u;
                         if (!mbar_wait_bounded(&full[s], par, abort_flag, a.status, tmo,
                                                kStatusPipeTimeout)) {
                             ok = false;
@@ -227,23 +282,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             stamp(a, t, 2);
                             first = false;
                         }
-                        const uint32_t sa = smem_u32(smem + s * kStageBytes);
+                        const uint32_t sa = smem_u32(smem + s * kStageB);
                         const uint32_t sb = sa + 3 * kSubA;
 #pragma unroll
                         for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
                             const uint32_t off = k16 * 32;  // 16 fp16 = 32 bytes along K
-                            umma_f16(d_tmem, smem_desc_sw64(sa + off), smem_desc_sw64(sb + off),
-                                     idesc, (kb | k16) != 0);
-                            umma_f16(d_tmem, smem_desc_sw64(sa + kSubA + off),
-                                     smem_desc_sw64(sb + kSubBMax + off), idesc, 1u);
-                            umma_f16(d_tmem, smem_desc_sw64(sa + 2 * kSubA + off),
-                                     smem_desc_sw64(sb + off), idesc, 1u);
+                            const uint64_t a0 = smem_desc_sw64(sa + off);
+                            const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
+                            const uint64_t a2 = smem_desc_sw64(sa + 2 * kSubA + off);
+                            const uint64_t b0 = smem_desc_sw64(sb + off);
+                            const uint64_t b1 = smem_desc_sw64(sb + kSubB + off);
+                            if (kPair) {
+                                umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                                umma_f16_pair(d_tmem, a1, b1, idesc, 1u);
+                                umma_f16_pair(d_tmem, a2, b0, idesc, 1u);
+                            } else {
+                                umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                                umma_f16(d_tmem, a1, b1, idesc, 1u);
+                                umma_f16(d_tmem, a2, b0, idesc, 1u);
+                            }
                         }
-                        umma_commit(&empty[s]);
+                        if (kPair)
+                            umma_commit_pair_multicast(&empty[s], 0x3);
+                        else
+                            umma_commit(&empty[s]);
                         ++consumed;
                     }
                     if (!ok) break;
-                    umma_commit(&acc_full[buf]);
+                    if (kPair)
+                        umma_commit_pair_multicast(&acc_full[buf], 0x3);
+                    else
+                        umma_commit(&acc_full[buf]);
                     ++acc_uses;
                 }
                 stamp(a, t, 3);
@@ -254,9 +323,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int e = warp - 2, q = warp & 3, h = e >> 2;
             const int r = 32 * q + lane;
             const uint64_t stream = l2_policy_evict_first();
-            for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+            // the leader's acc_empty barriers collect both CTAs' epilogue warps
+            const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+            for (int64_t v = first_item; v < work; v += item_stride) {
                 const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
-                const int beta = (int)(u % p.n_beta), j = (int)(u / p.n_beta);
+                int beta, j;
+                decode(v, beta, j);
+                const int64_t u = (int64_t)j * p.n_beta + beta;  // running-minimum tile
                 float4 *mt = reinterpret_cast<float4 *>(a.m + u * (int64_t)(kUnitRows * tile_n));
                 // prefetch the first group's running minima before waiting
                 float4 mcur[8], mnext[8];
@@ -287,18 +360,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
                         float mv[4] = {mcur[v].x, mcur[v].y, mcur[v].z, mcur[v].w};
+                        bool changed = false;
 #pragma unroll
                         for (int z = 0; z < 4; ++z) {
                             // d = 1 - <q, e>, the accumulator holding 2^12 <q, e>
                             const float d = fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
+                            changed |= d < mv[z];
                             mv[z] = fminf(mv[z], d);
                             if (mv[z] > best) {
                                 best = mv[z];
                                 best_c = cbase + 4 * v + z;
                             }
                         }
-                        st_cg_hint(&mt[((g * 4 + q) * 8 + v) * 32 + lane],
-                                   make_float4(mv[0], mv[1], mv[2], mv[3]), stream);
+                        // a candidate's running minimum changes with probability
+                        // about 1/(t+1) after t picks: write back only what moved
+                        if (changed)
+                            st_cg_hint(&mt[((g * 4 + q) * 8 + v) * 32 + lane],
+                                       make_float4(mv[0], mv[1], mv[2], mv[3]), stream);
                     }
                     if (gn < groups) {
 #pragma unroll
@@ -307,7 +385,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                if (lane == 0) {
+                    if (kPair)
+                        mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
+                    else
+                        mbar_arrive(&acc_empty[buf]);
+                }
                 ++acc_uses;
                 const int b = beta * kUnitRows + r;
                 if (best > -INFINITY && b < a.B) atomicMax(a.keys + b, max_key(best, best_c));
@@ -401,24 +484,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- teardown: drain what this CTA still has in flight, free TMEM ----
     __syncthreads();
     if (warp == 0 && lane == 0 && *abort_flag) {
-        // wait (bounded) for the last fill of every stage that was ever filled
         volatile int never = 0;
-        for (uint32_t s = 0; s < kStages && s < fills; ++s) {
-            const uint32_t n_s = fills / kStages + (s < fills % kStages ? 1u : 0u);
-            mbar_wait_bounded(&full[s], (n_s - 1) & 1u, &never, a.status,
-                              tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
+        if (kPair) {
+            // the pair's copies complete on the leader's barriers: give the
+            // ones still in flight time to land
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 200000ull) {
+            }
+        }
+        if (!kPair || leader) {
+            // wait (bounded) for the last fill of every stage that was ever filled
+            for (uint32_t s = 0; s < (uint32_t)kSt && s < fills; ++s) {
+                const uint32_t n_s = fills / kSt + (s < fills % kSt ? 1u : 0u);
+                mbar_wait_bounded(&full[s], (n_s - 1) & 1u, &never, a.status,
+                                  tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
+            }
         }
     }
-    if (warp == 1) {
-        if (lane == 0) {
-            volatile int never = 0;
+    if (warp == 1 && lane == 0 && leader) {
+        volatile int never = 0;
+        if (kPair)
+            umma_commit_pair(final_bar);
+        else
             umma_commit(final_bar);
-            mbar_wait_bounded(final_bar, 0, &never, a.status,
-                              tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
-        }
+        mbar_wait_bounded(final_bar, 0, &never, a.status,
+                          tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
+    }
+    __syncthreads();
+    // the leader's MMAs into both CTAs' TMEM are done before either frees it
+    if (kPair) cluster_sync_all();
+    if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (kPair)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -431,16 +532,71 @@ void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *st
 
 cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st) {
-    const size_t smem = tc_smem_bytes();
-    cudaError_t err =
-        cudaFuncSetAttribute(tc_dseq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
     TcDseqArgs aa = a;
     TcPlan pp = p;
     CUtensorMap mq = tmap_q, me = tmap_e;
-    void *args[] = {&mq, &me, &aa, &pp};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(tc_dseq_kernel),
-                                       dim3((unsigned)p.grid), dim3(kTcThreads), args, smem, st);
+    if (!p.pair) {
+        const size_t smem = DseqCfg<false>::kSmemBytes;
+        cudaError_t err = cudaFuncSetAttribute(tc_dseq_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        void *args[] = {&mq, &me, &aa, &pp};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(tc_dseq_kernel<false>),
+                                           dim3((unsigned)p.grid), dim3(kTcThreads), args, smem, st);
+    }
+    const size_t smem = DseqCfg<true>::kSmemBytes;
+    cudaError_t err = cudaFuncSetAttribute(tc_dseq_kernel<true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    err = cudaLaunchKernelEx(&cfg, tc_dseq_kernel<true>, mq, me, aa, pp);
+    if (err == cudaSuccess) return err;
+    // cooperative + cluster launch refused: launch the clusters plainly.  The
+    // caller sized the grid to the co-resident cluster count, and every grid
+    // barrier is time-bounded, so a non-resident grid fails with a timeout.
+    cudaGetLastError();
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_dseq_kernel<true>, mq, me, aa, pp);
+}
+
+int tc_dseq_pair_max_clusters(int tile_n) {
+    (void)tile_n;
+    const size_t smem = DseqCfg<true>::kSmemBytes;
+    if (cudaFuncSetAttribute(tc_dseq_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_dseq_kernel<true>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace dseq

@@ -174,6 +174,9 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 32 in [32, 256]; 0 = chosen from the shape (default).
  *   "grid"        persistent CTAs; 0 = one per SM (default).
  *   "timeout_ms"  limit of every device-side wait (default 10000).
+ *   "pair"        1 = the diversity kernel runs on CTA pairs (clusters of
+ *                 two SMs) that share each tensor-core MMA (each SM stages
+ *                 half of the candidate tile; default); 0 = one CTA per MMA.
  *   "timeline"    1 = dseq_run records, per CTA and iteration of the
  *                 tensor-core kernel, device timestamps of its phases (read
  *                 them back with dseq_get_timeline); default 0.

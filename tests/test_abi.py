@@ -74,6 +74,7 @@ def test_argument_errors_before_any_gpu_work(lib):
 def test_options(lib):
     assert es.dseq_get_option("engine") == 0
     assert es.dseq_get_option("timeout_ms") == 10000
+    assert es.dseq_get_option("pair") == 1
     assert es.dseq_get_option("nonsense") == -1
     with pytest.raises(es.DseqError) as ei:
         es.dseq_set_option("nonsense", 1)

@@ -10,6 +10,8 @@ from parity import check_dseq_teacher_forced, check_picks_valid
 
 pytestmark = pytest.mark.gpu
 
+DEFAULT_PAIR = 1
+
 torch = pytest.importorskip("torch")
 
 
@@ -30,15 +32,17 @@ def es():
 def _reset_options(es):
     yield
     for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("timeout_ms", 10000),
-                    ("fault_skip_arrive", 0)):
+                    ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR)):
         es.dseq_set_option(name, v)
 
 
-def _run(es, E, starts, L, mask=None, trace_seqs=None, engine=0, tile_n=0, grid=0):
+def _run(es, E, starts, L, mask=None, trace_seqs=None, engine=0, tile_n=0, grid=0,
+         pair=None):
     dev = torch.device("cuda")
     es.dseq_set_option("engine", engine)
     es.dseq_set_option("tile_n", tile_n)
     es.dseq_set_option("grid", grid)
+    es.dseq_set_option("pair", DEFAULT_PAIR if pair is None else pair)
     ctx = es.dseq_create(torch.from_numpy(E).to(dev))
     try:
         st = torch.from_numpy(np.asarray(starts, np.int32)).to(dev)
@@ -65,7 +69,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("engine", ["tc", "tc_pair", "ffma"])
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
 def test_small_teacher_forced(es, engine, case):
     N, D, B, L, kind, frac = case
@@ -79,7 +83,8 @@ def test_small_teacher_forced(es, engine, case):
         mask[starts[: B // 3]] = 1  # some starts are masked themselves
     trace_seqs = np.arange(B, dtype=np.int32) if B <= 200 else \
         np.sort(np.random.default_rng(1).choice(B, 64, replace=False)).astype(np.int32)
-    picks, trace = _run(es, E, starts, L, mask, trace_seqs, engine=engine)
+    picks, trace = _run(es, E, starts, L, mask, trace_seqs, engine=int(engine == "ffma"),
+                        pair=int(engine == "tc_pair"))
     check_picks_valid(starts, mask, picks, N)
     check_dseq_teacher_forced(E, starts, mask, picks, trace, trace_seqs)
 
@@ -90,13 +95,20 @@ def test_picks_identical_across_candidate_tiles(es):
     N, D, B, L = 3000, 128, 300, 24
     E = workloads.clustered_table(N, D, n_centres=8, seed=11)
     starts = workloads.starts(N, B, seed=11)
-    ref, ref_tr = _run(es, E, starts, L, trace_seqs=[0, 7, 299], tile_n=256)
+    ref, ref_tr = _run(es, E, starts, L, trace_seqs=[0, 7, 299], tile_n=256, pair=0)
     for tn in (32, 96, 128, 224):
-        got, tr = _run(es, E, starts, L, trace_seqs=[0, 7, 299], tile_n=tn)
+        got, tr = _run(es, E, starts, L, trace_seqs=[0, 7, 299], tile_n=tn, pair=0)
         assert np.array_equal(got, ref), f"tile_n={tn} changes the picks"
         assert np.array_equal(tr, ref_tr), f"tile_n={tn} changes the running minima"
-    got, _ = _run(es, E, starts, L, grid=7)
+    got, _ = _run(es, E, starts, L, grid=7, pair=0)
     assert np.array_equal(got, ref), "grid size changes the picks"
+    # CTA pairs run the same K order into the same fp32 accumulators
+    for tn in (64, 224, 256):
+        got, tr = _run(es, E, starts, L, trace_seqs=[0, 7, 299], tile_n=tn, pair=1)
+        assert np.array_equal(got, ref), f"pair mode, tile_n={tn} changes the picks"
+        assert np.array_equal(tr, ref_tr), f"pair mode, tile_n={tn} changes the running minima"
+    got, _ = _run(es, E, starts, L, grid=6, pair=1)
+    assert np.array_equal(got, ref), "pair mode with 3 clusters changes the picks"
 
 
 def test_exhaustion_boundary(es):
