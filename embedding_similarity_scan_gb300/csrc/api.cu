@@ -718,14 +718,21 @@ int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, 
                            ws->w_inv.as<float>(), a.status, st);
         CUDA_TRY(cudaGetLastError());
         TcPlan plan{};
+        plan.pair = opt.pair ? 1 : 0;
         plan.n_beta = (int)((n + kUnitRows - 1) / kUnitRows);
-        const int grid_cap = opt.grid > 0 ? (int)std::min<int64_t>(opt.grid, info.sms) : info.sms;
+        if (plan.pair) plan.n_beta += plan.n_beta & 1;  // whole pairs of sample blocks
+        int grid_cap = opt.grid > 0 ? (int)std::min<int64_t>(opt.grid, info.sms) : info.sms;
         plan.tile_n = opt.tile_n > 0 ? (int)opt.tile_n : 256;
         plan.n_chunk = (int)((M + plan.tile_n - 1) / plan.tile_n);
-        plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
+        if (plan.pair) {
+            grid_cap = std::max(2, grid_cap / 2 * 2);
+            plan.grid = 2 * (int)std::min<int64_t>(grid_cap / 2, plan.units() / 2);
+        } else {
+            plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
+        }
         CUtensorMap tx, tw;
         TRY(encode_f16_map(tx, a.x_split, 3 * Dp, n, kUnitRows));
-        TRY(encode_f16_map(tw, a.w_split, 2 * Dp, M, plan.tile_n));
+        TRY(encode_f16_map(tw, a.w_split, 2 * Dp, M, plan.pair ? plan.tile_n / 2 : plan.tile_n));
         TRY(timer.start(st));
         CUDA_TRY(launch_tc_bmu(a, plan, tx, tw, st));
         TRY(timer.stop(st));

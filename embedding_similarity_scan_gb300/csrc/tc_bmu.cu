@@ -31,12 +31,21 @@ namespace dseq {
 
 namespace {
 
-constexpr int kBmuStages = 3;
 constexpr uint32_t kSubA = kUnitRows * kKBlock * 2;
-constexpr uint32_t kSubBMax = 256 * kKBlock * 2;
-constexpr uint32_t kStageBytes = 3 * kSubA + 2 * kSubBMax;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
+
+// Stage geometry.  One CTA: B sub-tiles of up to 256 neuron rows, 3 stages
+// (the epilogue also needs 2 KB of column constants).  CTA pair: each CTA
+// stages half of the neuron chunk (<= 128 rows), 5 stages.
+template <bool kPair>
+struct BmuCfg {
+    static constexpr int kStagesT = kPair ? 5 : 3;
+    static constexpr uint32_t kSubB = (kPair ? 128u : 256u) * kKBlock * 2;
+    static constexpr uint32_t kStage = 3 * kSubA + 2 * kSubB;
+    static constexpr size_t kSmemBytes =
+        (size_t)kStagesT * kStage + 1024 + 256 + kEpiWarps * 32 * sizeof(float2);
+};
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -44,10 +53,10 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 }
 
 struct BmuSchedule {
-    int n_beta, n_chunk, tile_n, slice_chunks;
-    // unit u -> (sample block beta, neuron chunk j)
+    int n_blocks, n_chunk, tile_n, slice_chunks;
+    // work item u -> (sample block, or sample block pair, "beta"; neuron chunk j)
     __device__ __forceinline__ void decode(int64_t u, int &beta, int &j) const {
-        const int64_t per_slice = (int64_t)n_beta * slice_chunks;
+        const int64_t per_slice = (int64_t)n_blocks * slice_chunks;
         const int64_t sl = u / per_slice;
         const int64_t rem = u - sl * per_slice;
         const int first = (int)(sl * slice_chunks);
@@ -57,10 +66,15 @@ struct BmuSchedule {
     }
 };
 
+template <bool kPair>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_bmu_kernel(const __grid_constant__ CUtensorMap tmap_x,
                   const __grid_constant__ CUtensorMap tmap_w, const BmuArgs a, const TcPlan p,
                   const int slice_chunks) {
+    using Cfg = BmuCfg<kPair>;
+    constexpr int kBmuStages = Cfg::kStagesT;
+    constexpr uint32_t kSubB = Cfg::kSubB;
+    constexpr uint32_t kStageBytes = Cfg::kStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kBmuStages * kStageBytes);
@@ -74,6 +88,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t tmo = a.timeout_ns;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBmuStages; ++s) {
@@ -82,7 +98,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&acc_full[s], 1);
-            mbar_init(&acc_empty[s], kEpiWarps);
+            mbar_init(&acc_empty[s], kEpiWarps * (kPair ? 2 : 1));
         }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
@@ -93,21 +109,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tmap_w);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        if (kPair) {
+            tmem_alloc_pair(tmem_slot, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (kPair) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const BmuSchedule sched{p.n_beta, p.n_chunk, p.tile_n, slice_chunks};
-    const int64_t units = p.units();
+    // pair mode: work items are (sample block pair, chunk); this CTA takes
+    // sample block 2 * pair + rank and rows [rank * tile_n / 2, ...) of the chunk
+    const BmuSchedule sched{kPair ? p.n_beta / 2 : p.n_beta, p.n_chunk, p.tile_n, slice_chunks};
+    const int64_t units = (int64_t)sched.n_blocks * p.n_chunk;
+    const int64_t first_item = kPair ? (blockIdx.x >> 1) : blockIdx.x;
+    const int64_t item_stride = kPair ? (gridDim.x >> 1) : gridDim.x;
     const uint32_t tile_n = (uint32_t)p.tile_n;
-    const uint32_t sub_b = tile_n * kKBlock * 2;
-    const uint32_t tx_bytes = 3 * kSubA + 2 * sub_b;
+    const uint32_t b_rows = kPair ? tile_n / 2 : tile_n;
+    const uint32_t sub_b = b_rows * kKBlock * 2;
+    const uint32_t tx_bytes = (kPair ? 2u : 1u) * (3 * kSubA + 2 * sub_b);
     const int kblocks = a.Dp / kKBlock;
-    const uint32_t idesc = idesc_f16_f32(kUnitRows, tile_n);
+    const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kUnitRows : kUnitRows, tile_n);
     const int groups = (int)(tile_n / 32);
 
     if (warp == 0) {
@@ -116,10 +143,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // a sample block is reused only by the units running at the same time
             const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
             uint32_t fills = 0;
-            for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
-                int beta, j;
-                sched.decode(u, beta, j);
-                const int yx = beta * kUnitRows, yw = j * (int)tile_n;
+            for (int64_t u = first_item; u < units && !*abort_flag; u += item_stride) {
+                int blk, j;
+                sched.decode(u, blk, j);
+                const int beta = kPair ? 2 * blk + (int)rank : blk;
+                const int yx = beta * kUnitRows, yw = j * (int)tile_n + (int)(rank * b_rows);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     const uint32_t s = fills % kBmuStages, par = (fills / kBmuStages) & 1u;
                     if (!mbar_wait_bounded(&empty[s], par ^ 1u, abort_flag, a.status, tmo,
@@ -127,17 +155,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     uint8_t *sa = smem + s * kStageBytes;
                     uint8_t *sb = sa + 3 * kSubA;
-                    mbar_arrive_expect_tx(&full[s], tx_bytes);
+                    if (leader) mbar_arrive_expect_tx(&full[s], tx_bytes);
                     const int x = kb * kKBlock;
-                    tma_load_2d_hint(sa, &tmap_x, &full[s], x, yx, once);
-                    tma_load_2d_hint(sa + kSubA, &tmap_x, &full[s], a.Dp + x, yx, once);
-                    tma_load_2d_hint(sa + 2 * kSubA, &tmap_x, &full[s], 2 * a.Dp + x, yx, once);
-                    tma_load_2d_hint(sb, &tmap_w, &full[s], x, yw, keep);
-                    tma_load_2d_hint(sb + kSubBMax, &tmap_w, &full[s], a.Dp + x, yw, keep);
+                    if (kPair) {
+                        const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+                        tma_load_2d_pair(sa, &tmap_x, fb, x, yx, once);
+                        tma_load_2d_pair(sa + kSubA, &tmap_x, fb, a.Dp + x, yx, once);
+                        tma_load_2d_pair(sa + 2 * kSubA, &tmap_x, fb, 2 * a.Dp + x, yx, once);
+                        tma_load_2d_pair(sb, &tmap_w, fb, x, yw, keep);
+                        tma_load_2d_pair(sb + kSubB, &tmap_w, fb, a.Dp + x, yw, keep);
+                    } else {
+                        tma_load_2d_hint(sa, &tmap_x, &full[s], x, yx, once);
+                        tma_load_2d_hint(sa + kSubA, &tmap_x, &full[s], a.Dp + x, yx, once);
+                        tma_load_2d_hint(sa + 2 * kSubA, &tmap_x, &full[s], 2 * a.Dp + x, yx, once);
+                        tma_load_2d_hint(sb, &tmap_w, &full[s], x, yw, keep);
+                        tma_load_2d_hint(sb + kSubB, &tmap_w, &full[s], a.Dp + x, yw, keep);
+                    }
                     ++fills;
                 }
             }
-            if (*abort_flag) {
+            if (*abort_flag && kPair) {
+                // the pair's copies complete on the leader's barriers: give the
+                // ones still in flight time to land
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
+                }
+            }
+            if (*abort_flag && leader) {
                 volatile int never = 0;
                 for (uint32_t s = 0; s < kBmuStages && s < fills; ++s) {
                     const uint32_t n_s = fills / kBmuStages + (s < fills % kBmuStages ? 1u : 0u);
@@ -149,9 +193,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             uint32_t consumed = 0, acc_uses = 0;
-            for (int64_t u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+            for (int64_t u = first_item; u < units && !*abort_flag; u += item_stride) {
                 const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
                 if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
                                        kStatusPipeTimeout))
@@ -172,22 +216,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
                         const uint32_t off = k16 * 32;
-                        umma_f16(d_tmem, smem_desc_sw64(sa + off), smem_desc_sw64(sb + off), idesc,
-                                 (kb | k16) != 0);
-                        umma_f16(d_tmem, smem_desc_sw64(sa + kSubA + off),
-                                 smem_desc_sw64(sb + kSubBMax + off), idesc, 1u);
-                        umma_f16(d_tmem, smem_desc_sw64(sa + 2 * kSubA + off),
-                                 smem_desc_sw64(sb + off), idesc, 1u);
+                        const uint64_t a0 = smem_desc_sw64(sa + off);
+                        const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
+                        const uint64_t a2 = smem_desc_sw64(sa + 2 * kSubA + off);
+                        const uint64_t b0 = smem_desc_sw64(sb + off);
+                        const uint64_t b1 = smem_desc_sw64(sb + kSubB + off);
+                        if (kPair) {
+                            umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                            umma_f16_pair(d_tmem, a1, b1, idesc, 1u);
+                            umma_f16_pair(d_tmem, a2, b0, idesc, 1u);
+                        } else {
+                            umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                            umma_f16(d_tmem, a1, b1, idesc, 1u);
+                            umma_f16(d_tmem, a2, b0, idesc, 1u);
+                        }
                     }
-                    umma_commit(&empty[s]);
+                    if (kPair)
+                        umma_commit_pair_multicast(&empty[s], 0x3);
+                    else
+                        umma_commit(&empty[s]);
                     ++consumed;
                 }
                 if (!ok) break;
-                umma_commit(&acc_full[buf]);
+                if (kPair)
+                    umma_commit_pair_multicast(&acc_full[buf], 0x3);
+                else
+                    umma_commit(&acc_full[buf]);
                 ++acc_uses;
             }
             volatile int never = 0;
-            umma_commit(final_bar);
+            if (kPair)
+                umma_commit_pair(final_bar);
+            else
+                umma_commit(final_bar);
             mbar_wait_bounded(final_bar, 0, &never, a.status,
                               tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
         }
@@ -197,9 +258,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int r = 32 * q + lane;
         float2 *my_colc = colc + e * 32;
         uint32_t acc_uses = 0;
-        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-            int beta, j;
-            sched.decode(u, beta, j);
+        const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+        for (int64_t u = first_item; u < units; u += item_stride) {
+            int blk, j;
+            sched.decode(u, blk, j);
+            const int beta = kPair ? 2 * blk + (int)rank : blk;
             const int64_t row = (int64_t)beta * kUnitRows + r;
             const float cx = row < a.n ? -a.x_inv_scale[row] * (1.0f / 2048.0f) : 0.0f;
             const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
@@ -233,16 +296,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            if (lane == 0) {
+                if (kPair)
+                    mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
+                else
+                    mbar_arrive(&acc_empty[buf]);
+            }
             ++acc_uses;
             if (row < a.n && best_j != 0xffffffffu) atomicMin(a.keys + row, min_key(best, best_j));
         }
     }
 
     __syncthreads();
+    // the leader's MMAs into both CTAs' TMEM are done before either frees it
+    if (kPair) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (kPair)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -250,10 +323,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
                           const CUtensorMap &tmap_w, cudaStream_t st) {
-    const size_t smem = kBmuStages * kStageBytes + 1024 + 256 + kEpiWarps * 32 * sizeof(float2);
-    cudaError_t err =
-        cudaFuncSetAttribute(tc_bmu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
     // neuron slice: chunks whose split rows fill about half of L2
     int dev = 0, l2 = 0;
     cudaGetDevice(&dev);
@@ -266,9 +335,32 @@ cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &
     TcPlan pp = p;
     CUtensorMap mx = tmap_x, mw = tmap_w;
     int sl = slice;
-    void *args[] = {&mx, &mw, &aa, &pp, &sl};
-    return cudaLaunchKernel(reinterpret_cast<const void *>(tc_bmu_kernel), dim3((unsigned)p.grid),
-                            dim3(kTcThreads), args, smem, st);
+    if (!p.pair) {
+        const size_t smem = BmuCfg<false>::kSmemBytes;
+        cudaError_t err = cudaFuncSetAttribute(tc_bmu_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        void *args[] = {&mx, &mw, &aa, &pp, &sl};
+        return cudaLaunchKernel(reinterpret_cast<const void *>(tc_bmu_kernel<false>),
+                                dim3((unsigned)p.grid), dim3(kTcThreads), args, smem, st);
+    }
+    const size_t smem = BmuCfg<true>::kSmemBytes;
+    cudaError_t err = cudaFuncSetAttribute(tc_bmu_kernel<true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_bmu_kernel<true>, mx, mw, aa, pp, sl);
 }
 
 }  // namespace dseq

@@ -33,13 +33,14 @@ def es():
 @pytest.fixture(autouse=True)
 def _reset_options(es):
     yield
-    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0)):
+    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("pair", 1)):
         es.dseq_set_option(name, v)
 
 
-def _bmu(es, X, W, engine=0, tile_n=0):
+def _bmu(es, X, W, engine=0, tile_n=0, pair=1):
     es.dseq_set_option("engine", engine)
     es.dseq_set_option("tile_n", tile_n)
+    es.dseq_set_option("pair", pair)
     idx, dist = es.bmu_search(torch.from_numpy(X).cuda(), torch.from_numpy(W).cuda())
     torch.cuda.synchronize()
     return idx.cpu().numpy(), dist.cpu().numpy()
@@ -54,13 +55,13 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("engine", ["tc_pair", "tc", "ffma"])
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"n{c[0]}_M{c[1]}_D{c[2]}")
 def test_small(es, engine, case):
     n, M, D = case
     X = workloads.bmu_samples(n, D, seed=n + M)
     W = workloads.codebook(M, D, seed=n + M)
-    idx, dist = _bmu(es, X, W, engine)
+    idx, dist = _bmu(es, X, W, int(engine == "ffma"), pair=int(engine == "tc_pair"))
     check_bmu(X, W, np.arange(n), idx, dist)
 
 
@@ -71,8 +72,8 @@ def test_lattice_golden(es):
     X = np.array([[float(r[1]), float(r[2])] for r in rows], np.float32)
     want = [int(r[3]) for r in rows]
     dwant = np.array([float(r[4]) for r in rows])
-    for engine in (0, 1):
-        idx, dist = _bmu(es, X, W, engine)
+    for engine, pair in ((0, 1), (0, 0), (1, 0)):
+        idx, dist = _bmu(es, X, W, engine, pair=pair)
         assert idx.tolist() == want
         assert np.allclose(dist, dwant, atol=1e-5)
 
@@ -101,12 +102,14 @@ def test_scale_invariance_of_split(es):
 
 
 def test_tile_width_does_not_change_result(es):
+    """Neither the neuron-chunk width nor CTA pairs reorder a dot product."""
     X = workloads.bmu_samples(2000, 96, seed=2)
     W = workloads.codebook(3000, 96, seed=2)
-    ref = _bmu(es, X, W, tile_n=256)
+    ref = _bmu(es, X, W, tile_n=256, pair=0)
     for tn in (32, 128, 160):
-        got = _bmu(es, X, W, tile_n=tn)
-        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+        for pair in (0, 1):
+            got = _bmu(es, X, W, tile_n=tn, pair=pair)
+            assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
 
 
 def test_host_buffers(es):
