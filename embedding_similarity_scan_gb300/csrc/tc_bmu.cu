@@ -139,9 +139,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // the codebook slice is reused by every sample block: keep it in L2;
-            // a sample block is reused only by the units running at the same time
-            const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
+            // the codebook slice is reused by every sample block: keep it in L2.
+            // A sample block is read by every cluster working on it at about
+            // the same time; evict-first would drop it between those reads.
+            const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_normal();
             uint32_t fills = 0;
             for (int64_t u = first_item; u < units && !*abort_flag; u += item_stride) {
                 int blk, j;
