@@ -67,6 +67,7 @@ struct Options {
     int64_t fault_skip_arrive = 0;
     int64_t timeline = 0;
     int64_t pair = 1;
+    int64_t storage = 0;
 };
 std::mutex g_opt_mu;
 Options g_defaults;
@@ -86,6 +87,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "timeout_ms") {
         if (v < 1 || v > 3600000) return fail(DSEQ_EINVAL, "timeout_ms out of range");
         o.timeout_ms = v;
+    } else if (n == "storage") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "storage must be 0 (split) or 1 (fp16)");
+        o.storage = v;
     } else if (n == "pair") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "pair must be 0 or 1");
         o.pair = v;
@@ -111,6 +115,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "fault_skip_arrive") return o.fault_skip_arrive;
     if (n == "timeline") return o.timeline;
     if (n == "pair") return o.pair;
+    if (n == "storage") return o.storage;
     return -1;
 }
 
@@ -325,13 +330,14 @@ struct dseq_ctx {
     int64_t N = 0;
     int32_t D = 0, Dp = 0;
     Options opt;
-    DevBuf e_unit, e_split;
+    DevBuf e_unit, e_split, e_f16, rn;
     // run workspace
-    DevBuf m, keys, q, status, barrier, starts, mask, picks, trace_slot, timeline;
+    DevBuf m, keys, q, q_rn, status, barrier, starts, mask, picks, trace_slot, timeline;
     int64_t timeline_iters = 0, timeline_grid = 0;
     ~dseq_ctx() {
-        DevBuf *all[] = {&e_unit, &e_split, &m,     &keys,       &q,       &status, &barrier,
-                         &starts, &mask,    &picks, &trace_slot, &timeline};
+        DevBuf *all[] = {&e_unit, &e_split, &e_f16, &rn,     &m,          &keys,
+                         &q,      &q_rn,    &status, &barrier, &starts, &mask,
+                         &picks,  &trace_slot, &timeline};
         for (DevBuf *b : all) b->release();
     }
 };
@@ -395,6 +401,8 @@ int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device, v
     int r;
     if ((r = ctx->e_unit.ensure((size_t)N * ctx->Dp * sizeof(float))) != DSEQ_OK) return bail(r);
     if ((r = ctx->e_split.ensure((size_t)N * 2 * ctx->Dp * sizeof(__half))) != DSEQ_OK) return bail(r);
+    if ((r = ctx->e_f16.ensure((size_t)N * ctx->Dp * sizeof(__half))) != DSEQ_OK) return bail(r);
+    if ((r = ctx->rn.ensure((size_t)N * sizeof(float))) != DSEQ_OK) return bail(r);
     if ((r = ctx->status.ensure(sizeof(int))) != DSEQ_OK) return bail(r);
     DevBuf staged;
     const float *tdev = nullptr;
@@ -403,6 +411,8 @@ int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device, v
     if (e == cudaSuccess) {
         launch_table_prepare(tdev, N, D, ctx->Dp, ctx->e_unit.as<float>(),
                              ctx->e_split.as<__half>(), ctx->status.as<int>(), st);
+        launch_table_prepare_f16(tdev, N, D, ctx->Dp, ctx->e_f16.as<__half>(),
+                                 ctx->rn.as<float>(), ctx->status.as<int>(), st);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) {
@@ -535,13 +545,22 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
         }
         TRY(ctx->m.ensure((size_t)plan.units() * kUnitRows * plan.tile_n * sizeof(float)));
-        TRY(ctx->q.ensure((size_t)Bp * 3 * ctx->Dp * sizeof(__half)));
+        // split storage: queries [hi*2^12 | hi | lo], table [hi | lo];
+        // fp16 storage: one fp16 part each, plus inverse norms
+        const bool f16 = ctx->opt.storage == 1;
+        const int qparts = f16 ? 1 : 3, eparts = f16 ? 1 : 2;
+        TRY(ctx->q.ensure((size_t)Bp * qparts * ctx->Dp * sizeof(__half)));
+        TRY(ctx->q_rn.ensure((size_t)Bp * sizeof(float)));
         CUtensorMap tq, te;
-        TRY(encode_f16_map(tq, ctx->q.p, 3 * ctx->Dp, Bp, kUnitRows));
-        TRY(encode_f16_map(te, ctx->e_split.p, 2 * ctx->Dp, N, pair ? plan.tile_n / 2 : plan.tile_n));
-        TcDseqArgs a;
+        TRY(encode_f16_map(tq, ctx->q.p, qparts * ctx->Dp, Bp, kUnitRows));
+        TRY(encode_f16_map(te, f16 ? ctx->e_f16.p : ctx->e_split.p, eparts * ctx->Dp, N,
+                           pair ? plan.tile_n / 2 : plan.tile_n));
+        TcDseqArgs a{};
         a.e_split = ctx->e_split.as<__half>();
         a.q_split = ctx->q.as<__half>();
+        a.e_f16 = f16 ? ctx->e_f16.as<__half>() : nullptr;
+        a.rn = ctx->rn.as<float>();
+        a.q_rn = ctx->q_rn.as<float>();
         a.m = ctx->m.as<float>();
         a.keys = ctx->keys.as<unsigned long long>();
         a.picks = d_picks;
@@ -557,7 +576,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.fault_skip_arrive = (int)ctx->opt.fault_skip_arrive;
         // the split table stays L2-resident across iterations only if it is a
         // small part of L2; larger tables stream through once per iteration
-        a.keep_table = (double)N * 2 * ctx->Dp * sizeof(__half) <= info.l2 / 3.0 ? 1 : 0;
+        a.keep_table = (double)N * eparts * ctx->Dp * sizeof(__half) <= info.l2 / 3.0 ? 1 : 0;
         a.timeline = nullptr;
         ctx->timeline_iters = ctx->timeline_grid = 0;
         if (ctx->opt.timeline) {

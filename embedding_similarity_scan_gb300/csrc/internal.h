@@ -70,6 +70,11 @@ struct TcPlan {
 void launch_table_prepare(const float *E, int64_t N, int D, int Dp, float *e_unit,
                           __half *e_split, int *status, cudaStream_t st);
 
+// fp16 storage of the candidate table: row * 2^-e (max |.| in [0.5, 1)) rounded
+// to fp16, zero-padded to Dp; rn[r] = 1 / |stored row| (double sum).
+void launch_table_prepare_f16(const float *E, int64_t N, int D, int Dp, __half *e_f16,
+                              float *rn, int *status, cudaStream_t st);
+
 // Rows of a BMU operand scaled by a per-row power of two (max |.| in [0.5, 1))
 // and split into fp16.  triple = 1: [hi*2^12 | hi | lo*2^12] (A side);
 // triple = 0: [hi | lo*2^12] (B side).  norm2[r] = |row|^2 (double sum),
@@ -79,8 +84,13 @@ void launch_bmu_prepare(const float *A, int64_t rows, int D, int Dp, int triple,
 
 // ---- diversity, tensor-core path (tc_dseq.cu) -------------------------------
 struct TcDseqArgs {
-    const __half *e_split;   // N x 2Dp
-    __half *q_split;         // Bp x 3Dp
+    const __half *e_split;   // N x 2Dp: [hi | lo * 2^12] of the unit rows (split storage)
+    __half *q_split;         // Bp x 3Dp (split) or Bp x Dp (fp16 storage)
+    // fp16 storage (nullptr = split storage): rows scaled by a power of two
+    // and rounded to fp16, N x Dp; inverse norms of those stored rows
+    const __half *e_f16;
+    const float *rn;
+    float *q_rn;             // Bp: inverse norm of each current query row
     float *m;                // units x 128 x tile_n
     unsigned long long *keys;  // Bp
     int32_t *picks;          // B x L

@@ -72,6 +72,46 @@ __global__ void table_prepare_kernel(const float *__restrict__ E, int64_t N, int
     }
 }
 
+__global__ void table_prepare_f16_kernel(const float *__restrict__ E, int64_t N, int D, int Dp,
+                                         __half *__restrict__ e_f16, float *__restrict__ rn,
+                                         int *status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= N) return;
+    const float *src = E + row * (int64_t)D;
+    float mx = 0.0f;
+    int bad = 0;
+    for (int k = lane; k < D; k += 32) {
+        const float v = src[k];
+        if (!isfinite(v)) bad = 1;
+        mx = fmaxf(mx, fabsf(v));
+    }
+    mx = warp_max_f(mx);
+    bad = warp_or_i(bad);
+    if (bad || !(mx > 0.0f)) {
+        if (lane == 0) atomicOr(status, kStatusNonFinite);
+        return;
+    }
+    // a power-of-two scale keeps the row inside fp16's range without changing
+    // its direction; the cosine uses the norm of the stored (rounded) row
+    int e = 0;
+    frexpf(mx, &e);
+    const float scale = ldexpf(1.0f, -e);
+    __half *dst = e_f16 + row * (int64_t)Dp;
+    double ss = 0.0;
+    for (int k = lane; k < Dp; k += 32) {
+        const __half h = __float2half_rn(k < D ? src[k] * scale : 0.0f);
+        dst[k] = h;
+        const double hv = (double)__half2float(h);
+        ss += hv * hv;
+    }
+    ss = warp_sum_d(ss);
+    if (lane == 0) {
+        if (!(ss > 0.0)) atomicOr(status, kStatusNonFinite);
+        rn[row] = (float)(1.0 / sqrt(ss));
+    }
+}
+
 __global__ void bmu_prepare_kernel(const float *__restrict__ A, int64_t rows, int D, int Dp,
                                    int triple, __half *__restrict__ split,
                                    float *__restrict__ norm2, float *__restrict__ inv_scale,
@@ -177,6 +217,12 @@ void launch_table_prepare(const float *E, int64_t N, int D, int Dp, float *e_uni
                           __half *e_split, int *status, cudaStream_t st) {
     table_prepare_kernel<<<blocks_for_rows(N, 8), 256, 0, st>>>(E, N, D, Dp, e_unit, e_split,
                                                                   status);
+}
+
+void launch_table_prepare_f16(const float *E, int64_t N, int D, int Dp, __half *e_f16,
+                              float *rn, int *status, cudaStream_t st) {
+    table_prepare_f16_kernel<<<blocks_for_rows(N, 8), 256, 0, st>>>(E, N, D, Dp, e_f16, rn,
+                                                                       status);
 }
 
 void launch_bmu_prepare(const float *A, int64_t rows, int D, int Dp, int triple, __half *split,

@@ -50,15 +50,20 @@ constexpr uint32_t kSubA = kUnitRows * kKBlock * 2;  // one 128 x 32 fp16 sub-ti
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 
-// Stage geometry.  One CTA: A = 3 x (128 x 32), B = 2 x (tile_n x 32) fp16,
-// tile_n <= 256, 4 stages.  CTA pair: the B sub-tiles hold half of the
-// candidate chunk (<= 128 rows), so a stage is 40 KB and 5 stages fit.
-template <bool kPair>
+// Stage geometry.  Split storage (fp32-accurate): A = 3 x (128 x 32),
+// B = 2 x (rows x 32) fp16; fp16 storage: one part each.  One CTA stages up
+// to 256 candidate rows, a CTA pair half of the chunk (<= 128 rows) per SM.
+// Stage counts fill about 200-225 KB of shared memory.
+template <bool kPair, bool kF16>
 struct DseqCfg {
-    static constexpr int kStagesT = kPair ? 5 : kStages;
+    static constexpr int kPartsA = kF16 ? 1 : 3;
+    static constexpr int kPartsB = kF16 ? 1 : 2;
     static constexpr uint32_t kSubB = (kPair ? 128u : 256u) * kKBlock * 2;
-    static constexpr uint32_t kStage = 3 * kSubA + 2 * kSubB;
-    static constexpr size_t kSmemBytes = (size_t)kStagesT * kStage + 1024 + 256;
+    static constexpr uint32_t kStage = kPartsA * kSubA + kPartsB * kSubB;
+    static constexpr int kStagesT = kF16 ? (kPair ? 12 : 9) : (kPair ? 5 : kStages);
+    // + alignment slack, barriers and flags, per-warp column norms (fp16 storage)
+    static constexpr size_t kSmemBytes =
+        (size_t)kStagesT * kStage + 1024 + 256 + (kF16 ? kEpiWarps * 32 * sizeof(float) : 0);
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -84,10 +89,22 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
         if (live && cand == starts[b]) live = false;
         a.m[i] = live ? INFINITY : -INFINITY;
     }
-    // query rows: the split start rows, zero rows for padded sequences
+    // query rows: the start rows, zero rows for padded sequences
     const int vec = a.Dp / 8;  // 16-byte vectors per row segment
     const int64_t qtotal = (int64_t)p.n_beta * kUnitRows * vec;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < qtotal; i += stride) {
+    if (a.e_f16) {  // fp16 storage: the stored row and its inverse norm
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < qtotal;
+             i += stride) {
+            const int b = (int)(i / vec), k = (int)(i - (int64_t)b * vec);
+            uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * a.Dp);
+            dst[k] = b < a.B ? reinterpret_cast<const uint4 *>(a.e_f16 +
+                                                               (int64_t)starts[b] * a.Dp)[k]
+                             : make_uint4(0, 0, 0, 0);
+            if (k == 0) a.q_rn[b] = b < a.B ? a.rn[starts[b]] : 0.0f;
+        }
+    }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < qtotal && !a.e_f16;
+         i += stride) {
         const int b = (int)(i / vec), k = (int)(i - (int64_t)b * vec);
         uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * 3 * a.Dp);
         if (b < a.B) {
@@ -119,12 +136,13 @@ __device__ __forceinline__ void stamp(const TcDseqArgs &a, int t, int slot) {
         a.timeline[((size_t)t * gridDim.x + blockIdx.x) * kTimelineSlots + slot] = globaltimer_ns();
 }
 
-template <bool kPair>
+template <bool kPair, bool kF16>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_dseq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
                    const TcPlan p) {
-    using Cfg = DseqCfg<kPair>;
+    using Cfg = DseqCfg<kPair, kF16>;
+    constexpr int kPartsA = Cfg::kPartsA, kPartsB = Cfg::kPartsB;
     constexpr int kSt = Cfg::kStagesT;
     constexpr uint32_t kSubB = Cfg::kSubB;
     constexpr uint32_t kStageB = Cfg::kStage;
@@ -137,6 +155,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *final_bar = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(final_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // fp16 storage: per epilogue warp, the inverse norms of its 32 columns
+    float *col_rn = reinterpret_cast<float *>(smem + kSt * kStageB + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t tmo = a.timeout_ns;
@@ -182,7 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // rows of this CTA's B sub-tile (pair: half of the candidate chunk)
     const uint32_t b_rows = kPair ? tile_n / 2 : tile_n;
     const uint32_t sub_b = b_rows * kKBlock * 2;
-    const uint32_t tx_bytes = (kPair ? 2u : 1u) * (3 * kSubA + 2 * sub_b);
+    const uint32_t tx_bytes = (kPair ? 2u : 1u) * (kPartsA * kSubA + kPartsB * sub_b);
     const int kblocks = a.Dp / kKBlock;
     const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kUnitRows : kUnitRows, tile_n);
     const int groups = (int)(tile_n / 32);
@@ -229,29 +249,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                kStatusPipeTimeout))
                             break;
                         uint8_t *sa = smem + s * kStageB;
-                        uint8_t *sb = sa + 3 * kSubA;
+                        uint8_t *sb = sa + kPartsA * kSubA;
                         if (leader) mbar_arrive_expect_tx(&full[s], tx_bytes);
                         if (first) {
                             stamp(a, t, 1);
                             first = false;
                         }
                         const int x = kb * kKBlock;
-                        if (kPair) {
-                            // completion goes to the leader's barrier for this stage
-                            const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-                            tma_load_2d_pair(sa, &tmap_q, fb, x, yq, keep);
-                            tma_load_2d_pair(sa + kSubA, &tmap_q, fb, a.Dp + x, yq, keep);
-                            tma_load_2d_pair(sa + 2 * kSubA, &tmap_q, fb, 2 * a.Dp + x, yq, keep);
-                            tma_load_2d_pair(sb, &tmap_e, fb, x, ye, table_pol);
-                            tma_load_2d_pair(sb + kSubB, &tmap_e, fb, a.Dp + x, ye, table_pol);
-                        } else {
-                            tma_load_2d_hint(sa, &tmap_q, &full[s], x, yq, keep);
-                            tma_load_2d_hint(sa + kSubA, &tmap_q, &full[s], a.Dp + x, yq, keep);
-                            tma_load_2d_hint(sa + 2 * kSubA, &tmap_q, &full[s], 2 * a.Dp + x, yq,
-                                             keep);
-                            tma_load_2d_hint(sb, &tmap_e, &full[s], x, ye, table_pol);
-                            tma_load_2d_hint(sb + kSubB, &tmap_e, &full[s], a.Dp + x, ye,
-                                             table_pol);
+                        // completion goes to the pair leader's barrier for this stage
+                        const uint32_t fb = kPair ? mapa_shared(smem_u32(&full[s]), 0) : 0u;
+#pragma unroll
+                        for (int part = 0; part < kPartsA; ++part) {  // (hi*2^12, hi, lo) or fp16
+                            if (kPair)
+                                tma_load_2d_pair(sa + part * kSubA, &tmap_q, fb,
+                                                 part * a.Dp + x, yq, keep);
+                            else
+                                tma_load_2d_hint(sa + part * kSubA, &tmap_q, &full[s],
+                                                 part * a.Dp + x, yq, keep);
+                        }
+#pragma unroll
+                        for (int part = 0; part < kPartsB; ++part) {  // (hi, lo) or fp16
+                            if (kPair)
+                                tma_load_2d_pair(sb + part * kSubB, &tmap_e, fb,
+                                                 part * a.Dp + x, ye, table_pol);
+                            else
+                                tma_load_2d_hint(sb + part * kSubB, &tmap_e, &full[s],
+                                                 part * a.Dp + x, ye, table_pol);
                         }
                         ++fills;
                     }
@@ -283,14 +306,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             first = false;
                         }
                         const uint32_t sa = smem_u32(smem + s * kStageB);
-                        const uint32_t sb = sa + 3 * kSubA;
+                        const uint32_t sb = sa + kPartsA * kSubA;
 #pragma unroll
                         for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
                             const uint32_t off = k16 * 32;  // 16 fp16 = 32 bytes along K
                             const uint64_t a0 = smem_desc_sw64(sa + off);
+                            const uint64_t b0 = smem_desc_sw64(sb + off);
+                            if (kF16) {  // one product: the stored fp16 rows
+                                if (kPair)
+                                    umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                                else
+                                    umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                                continue;
+                            }
                             const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
                             const uint64_t a2 = smem_desc_sw64(sa + 2 * kSubA + off);
-                            const uint64_t b0 = smem_desc_sw64(sb + off);
                             const uint64_t b1 = smem_desc_sw64(sb + kSubB + off);
                             if (kPair) {
                                 umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
@@ -346,7 +376,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float best = -INFINITY;
                 uint32_t best_c = 0;
                 const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+                // fp16 storage: d = 1 - acc * rn_q * rn_c with the rows' inverse norms
+                const int brow = beta * kUnitRows + r;
+                const float neg_rnq = kF16 ? -a.q_rn[brow] : 0.0f;
+                float *my_rn = col_rn + e * 32;
                 for (int g = h; g < groups; g += 2) {
+                    if (kF16) {
+                        const int64_t col = (int64_t)j * tile_n + 32 * g + lane;
+                        __syncwarp();
+                        my_rn[lane] = col < a.N ? a.rn[col] : 0.0f;
+                        __syncwarp();
+                    }
                     const int gn = g + 2;
                     if (gn < groups) {
 #pragma unroll
@@ -363,8 +403,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         bool changed = false;
 #pragma unroll
                         for (int z = 0; z < 4; ++z) {
-                            // d = 1 - <q, e>, the accumulator holding 2^12 <q, e>
-                            const float d = fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
+                            // split storage: d = 1 - <q, e>, the accumulator holding
+                            // 2^12 <q, e> of unit rows
+                            const float d =
+                                kF16 ? fmaf(acc[4 * v + z] * my_rn[4 * v + z], neg_rnq, 1.0f)
+                                     : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
                             changed |= d < mv[z];
                             mv[z] = fminf(mv[z], d);
                             if (mv[z] > best) {
@@ -454,6 +497,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const unsigned long long ki = __shfl_sync(0xffffffffu, key, i);
                     const uint32_t wi = __shfl_sync(0xffffffffu, w, i);
                     if (ki == 0ull) continue;
+                    if (kF16) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(a.e_f16 + (int64_t)wi * a.Dp);
+                        uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * a.Dp);
+                        for (int k = lane; k < vec; k += 32) dst[k] = __ldg(src + k);
+                        if (lane == 0) a.q_rn[base + i] = a.rn[wi];
+                        continue;
+                    }
                     const uint4 *src =
                         reinterpret_cast<const uint4 *>(a.e_split + (int64_t)wi * 2 * a.Dp);
                     uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * 3 * a.Dp);
@@ -523,31 +573,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-}  // namespace
-
-void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *starts,
+void launch_tc_dseq_init_impl(const TcDseqArgs &a, const TcPlan &p, const int32_t *starts,
                          const uint8_t *mask, cudaStream_t st) {
     tc_dseq_init_kernel<<<2048, 256, 0, st>>>(a, p, starts, mask);
 }
 
-cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
+template <bool kPair, bool kF16>
+cudaError_t launch_variant(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st) {
     TcDseqArgs aa = a;
     TcPlan pp = p;
     CUtensorMap mq = tmap_q, me = tmap_e;
-    if (!p.pair) {
-        const size_t smem = DseqCfg<false>::kSmemBytes;
-        cudaError_t err = cudaFuncSetAttribute(tc_dseq_kernel<false>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
+    const size_t smem = DseqCfg<kPair, kF16>::kSmemBytes;
+    auto kernel = tc_dseq_kernel<kPair, kF16>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    if (!kPair) {
         void *args[] = {&mq, &me, &aa, &pp};
-        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(tc_dseq_kernel<false>),
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kernel),
                                            dim3((unsigned)p.grid), dim3(kTcThreads), args, smem, st);
     }
-    const size_t smem = DseqCfg<true>::kSmemBytes;
-    cudaError_t err = cudaFuncSetAttribute(tc_dseq_kernel<true>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3(kTcThreads);
@@ -562,20 +608,37 @@ cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorM
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    err = cudaLaunchKernelEx(&cfg, tc_dseq_kernel<true>, mq, me, aa, pp);
+    err = cudaLaunchKernelEx(&cfg, kernel, mq, me, aa, pp);
     if (err == cudaSuccess) return err;
     // cooperative + cluster launch refused: launch the clusters plainly.  The
     // caller sized the grid to the co-resident cluster count, and every grid
     // barrier is time-bounded, so a non-resident grid fails with a timeout.
     cudaGetLastError();
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_dseq_kernel<true>, mq, me, aa, pp);
+    return cudaLaunchKernelEx(&cfg, kernel, mq, me, aa, pp);
+}
+
+}  // namespace
+
+void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *starts,
+                         const uint8_t *mask, cudaStream_t st) {
+    launch_tc_dseq_init_impl(a, p, starts, mask, st);
+}
+
+cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
+                           const CUtensorMap &tmap_e, cudaStream_t st) {
+    const bool f16 = a.e_f16 != nullptr;
+    if (p.pair)
+        return f16 ? launch_variant<true, true>(a, p, tmap_q, tmap_e, st)
+                   : launch_variant<true, false>(a, p, tmap_q, tmap_e, st);
+    return f16 ? launch_variant<false, true>(a, p, tmap_q, tmap_e, st)
+               : launch_variant<false, false>(a, p, tmap_q, tmap_e, st);
 }
 
 int tc_dseq_pair_max_clusters(int tile_n) {
     (void)tile_n;
-    const size_t smem = DseqCfg<true>::kSmemBytes;
-    if (cudaFuncSetAttribute(tc_dseq_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = DseqCfg<true, false>::kSmemBytes;
+    if (cudaFuncSetAttribute(tc_dseq_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -592,7 +655,7 @@ int tc_dseq_pair_max_clusters(int tile_n) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_dseq_kernel<true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_dseq_kernel<true, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

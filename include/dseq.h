@@ -174,6 +174,12 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 32 in [32, 256]; 0 = chosen from the shape (default).
  *   "grid"        persistent CTAs; 0 = one per SM (default).
  *   "timeout_ms"  limit of every device-side wait (default 10000).
+ *   "storage"     how the diversity kernel holds the table: 0 = fp16 hi/lo
+ *                 split of the unit rows, three tensor-core products per
+ *                 step, fp32-level distances (default); 1 = fp16 rows (each
+ *                 row scaled by a power of two, then rounded once to fp16),
+ *                 one product per step, distances exact for the stored rows
+ *                 up to fp32 accumulation ("load FP16, compute FP32").
  *   "pair"        1 = the diversity kernel runs on CTA pairs (clusters of
  *                 two SMs) that share each tensor-core MMA (each SM stages
  *                 half of the candidate tile; default); 0 = one CTA per MMA.
