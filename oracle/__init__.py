@@ -14,6 +14,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   row_norms, fold, argmax, dseq   -- pinned: hand-worked 4-point example,
       orthonormal table, duplicate rows, tiled == one pass for every tile
       size, brute-force farthest-first traversal on tiny tables, invariants.
+  centroid_dist, dseq_centroid    -- pinned: hand-worked example where the
+      centroid and max-min criteria disagree, the zero-centroid reading,
+      brute force against an independent centroid routine, tiled == one pass.
   bmu, sqdist_pairs               -- pinned: codebook containing the samples,
       integer lattice codebook (BMU = nearest lattice point), duplicate
       neurons, brute force against an independent argmin on tiny inputs.
@@ -72,6 +75,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_dseq.argtypes = [_f32p, i64, i32, _i32p, i32, i32, ctypes.c_void_p, i64,
                                 _i32p, ctypes.c_void_p, ctypes.c_int]
     lib.oracle_dseq.restype = ctypes.c_int
+    lib.oracle_centroid_dist.argtypes = [_f32p, i64, i32, _f64p, _i64p, i32, _f64p]
+    lib.oracle_centroid_dist.restype = None
+    lib.oracle_dseq_centroid.argtypes = [_f32p, i64, i32, _i32p, i32, i32, ctypes.c_void_p, i64,
+                                         _i32p, ctypes.c_void_p, ctypes.c_int]
+    lib.oracle_dseq_centroid.restype = ctypes.c_int
     lib.oracle_bmu.argtypes = [_f32p, i64, _f32p, i64, i32, _i32p, _f64p, ctypes.c_void_p,
                                ctypes.c_int]
     lib.oracle_bmu.restype = None
@@ -149,6 +157,32 @@ def dseq(E, starts, L: int, mask=None, tile: int = 0, threads: int = 0, lib=None
         mask_arr = np.ascontiguousarray(mask, np.uint8)
         assert mask_arr.size == E.shape[0]
     st = (lib or load()).oracle_dseq(
+        E, E.shape[0], E.shape[1], starts, B, int(L),
+        None if mask_arr is None else mask_arr.ctypes.data, int(tile), picks,
+        radius.ctypes.data, int(threads))
+    return picks, radius, int(st)
+
+
+def centroid_dist(E, nrm, members, lib=None) -> np.ndarray:
+    """Cosine distances of every row to the mean of the rows `members`."""
+    E = _f32(E)
+    members = np.ascontiguousarray(members, np.int64)
+    out = np.empty(E.shape[0], np.float64)
+    (lib or load()).oracle_centroid_dist(E, E.shape[0], E.shape[1],
+                                         np.ascontiguousarray(nrm, np.float64), members,
+                                         members.size, out)
+    return out
+
+
+def dseq_centroid(E, starts, L: int, mask=None, tile: int = 0, threads: int = 0, lib=None):
+    """Greedy centroid-criterion sequences: (picks, radius, status) as dseq()."""
+    E = _f32(E)
+    starts = np.ascontiguousarray(starts, np.int32)
+    B = starts.size
+    picks = np.empty((B, L), np.int32)
+    radius = np.empty((B, L), np.float64)
+    mask_arr = None if mask is None else np.ascontiguousarray(mask, np.uint8)
+    st = (lib or load()).oracle_dseq_centroid(
         E, E.shape[0], E.shape[1], starts, B, int(L),
         None if mask_arr is None else mask_arr.ctypes.data, int(tile), picks,
         radius.ctypes.data, int(threads))

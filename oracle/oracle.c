@@ -21,6 +21,12 @@
  *     Implementation Steps, the tile loop and its "do not reset the running
  *     max between tiles" warning; Risks, the last partial tile).
  *
+ *  1b. The centroid criterion named in the same issue (FP16 storage
+ *     section: "most different from the centroid"): each sequence picks the
+ *     unmasked candidate at the largest cosine distance from the centroid
+ *     (plain mean) of the rows it holds, lowest index on ties.  A zero
+ *     centroid makes every distance 1 (cosine taken as 0).
+ *
  *  2. Best-matching-unit search ("From 80x to 385x: A Best-Matching-Unit
  *     Search at the L2 Roof", section 3, Background): for each sample the
  *     index of the codebook row at the smallest squared Euclidean distance,
@@ -171,6 +177,79 @@ int oracle_dseq(const float *E, int64_t N, int32_t D, const int32_t *starts,
         }
         free(m);
         free(masked);
+    }
+    free(nrm);
+    return status;
+}
+
+/* Cosine distances of every row to the centroid (plain mean, double) of the
+ * rows listed in members[0..n_members): d[c] = 1 - <C, e_c> / (|C| |e_c|),
+ * or 1 for every c when the centroid is zero. */
+void oracle_centroid_dist(const float *E, int64_t N, int32_t D, const double *nrm,
+                          const int64_t *members, int32_t n_members, double *d) {
+    double *C = (double *)calloc((size_t)D, sizeof(double));
+    if (!C) return;
+    for (int32_t i = 0; i < n_members; ++i)
+        for (int32_t k = 0; k < D; ++k) C[k] += (double)E[members[i] * (int64_t)D + k];
+    double cn = 0.0;
+    for (int32_t k = 0; k < D; ++k) {
+        C[k] /= (double)n_members;
+        cn += C[k] * C[k];
+    }
+    cn = sqrt(cn);
+    for (int64_t c = 0; c < N; ++c) {
+        if (cn == 0.0) {
+            d[c] = 1.0;
+            continue;
+        }
+        double s = 0.0;
+        for (int32_t k = 0; k < D; ++k) s += C[k] * (double)E[c * (int64_t)D + k];
+        d[c] = 1.0 - s / (cn * nrm[c]);
+    }
+    free(C);
+}
+
+/* Greedy centroid-criterion sequences (arguments as oracle_dseq); radius
+ * receives the centroid distance of each pick. */
+int oracle_dseq_centroid(const float *E, int64_t N, int32_t D, const int32_t *starts, int32_t B,
+                         int32_t L, const uint8_t *mask, int64_t T, int32_t *picks,
+                         double *radius, int threads) {
+    double *nrm = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!nrm) return -2;
+    oracle_row_norms(E, N, D, nrm);
+    int status = 0;
+    set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(min : status)
+    for (int32_t b = 0; b < B; ++b) {
+        double *d = (double *)malloc(sizeof(double) * (size_t)N);
+        uint8_t *masked = (uint8_t *)malloc((size_t)N);
+        int64_t *members = (int64_t *)malloc(sizeof(int64_t) * (size_t)(L + 1));
+        if (!d || !masked || !members) {
+            free(d);
+            free(masked);
+            free(members);
+            status = -2;
+            continue;
+        }
+        for (int64_t c = 0; c < N; ++c) masked[c] = mask ? (mask[c] != 0) : 0;
+        members[0] = starts[b];
+        masked[starts[b]] = 1;
+        for (int32_t t = 0; t < L; ++t) {
+            oracle_centroid_dist(E, N, D, nrm, members, t + 1, d);
+            int64_t w = oracle_argmax(d, masked, N, T);
+            picks[(int64_t)b * L + t] = (int32_t)w;
+            if (w < 0) {
+                for (int32_t u = t; u < L; ++u) picks[(int64_t)b * L + u] = -1;
+                status = -1;
+                break;
+            }
+            if (radius) radius[(int64_t)b * L + t] = d[w];
+            masked[w] = 1;
+            members[t + 1] = w;
+        }
+        free(d);
+        free(masked);
+        free(members);
     }
     free(nrm);
     return status;

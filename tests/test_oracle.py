@@ -72,6 +72,43 @@ def _read_square4():
     return table, cases
 
 
+def _read_centroid_golden():
+    table, out = None, {}
+    with open(os.path.join(GOLDEN, "dseq_square4.txt")) as f:
+        for line in f:
+            if line.startswith("ctable"):
+                table = np.array([[float(v) for v in tok.split(",")] for tok in line.split()[1:]],
+                                 np.float32)
+            elif line.startswith("maxmin"):
+                _, s, L, picks = line.split()
+                out["maxmin"] = (int(s), int(L), [int(v) for v in picks.split(",")])
+            elif line.startswith("centroid"):
+                _, s, L, picks, radius = line.split()
+                out["centroid"] = (int(s), int(L), [int(v) for v in picks.split(",")],
+                                   [float(v) for v in radius.split(",")])
+    return table, out
+
+
+def _brute_centroid(E, start, L, excluded=()):
+    """Centroid criterion recomputed from scratch with math.fsum each step."""
+    rows = [[float(v) for v in r] for r in E]
+    norms = [math.sqrt(math.fsum(v * v for v in r)) for r in rows]
+    held, out = [start], []
+    for _ in range(L):
+        C = [math.fsum(rows[p][k] for p in held) / len(held) for k in range(len(rows[0]))]
+        cn = math.sqrt(math.fsum(v * v for v in C))
+        best, best_c = -math.inf, -1
+        for c in range(len(rows)):
+            if c in held or c in excluded:
+                continue
+            d = 1.0 if cn == 0.0 else 1.0 - math.fsum(a * b for a, b in zip(C, rows[c])) / (cn * norms[c])
+            if d > best:
+                best, best_c = d, c
+        out.append(best_c)
+        held.append(best_c)
+    return out
+
+
 def _read_lattice():
     out = []
     with open(os.path.join(GOLDEN, "bmu_lattice.txt")) as f:
@@ -215,6 +252,49 @@ def pins_dseq(lib) -> list[str]:
     return fails
 
 
+def pins_centroid(lib) -> list[str]:
+    fails: list[str] = []
+    # 1. worked example where the two criteria disagree
+    E, gold = _read_centroid_golden()
+    s0, L, want = gold["maxmin"]
+    got, _, _ = oracle.dseq(E, [s0], L, lib=lib)
+    if got[0].tolist() != want:
+        fails.append(f"centroid golden (max-min side): {got[0].tolist()} != {want}")
+    s0, L, want, radius = gold["centroid"]
+    got, rad, st = oracle.dseq_centroid(E, [s0], L, lib=lib)
+    if st != 0 or got[0].tolist() != want:
+        fails.append(f"centroid golden: {got[0].tolist()} != {want}")
+    elif not np.allclose(rad[0], radius, atol=1e-7):
+        fails.append(f"centroid golden radius: {rad[0].tolist()} != {radius}")
+    # 2. the zero-centroid reading directly
+    nrm = oracle.row_norms(E, lib=lib)
+    d = oracle.centroid_dist(E, nrm, [0, 2], lib=lib)
+    if not np.all(d == 1.0):
+        fails.append(f"zero centroid distances {d.tolist()}")
+    # 3. brute force on tiny random tables (no ties) and with a mask
+    for seed, (n, dd) in enumerate([(7, 3), (11, 5), (12, 8)]):
+        E = np.random.default_rng(300 + seed).standard_normal((n, dd)).astype(np.float32)
+        for s in (0, n // 2):
+            want = _brute_centroid(E, s, n - 1)
+            got, _, st = oracle.dseq_centroid(E, [s], n - 1, lib=lib)
+            if st != 0 or got[0].tolist() != want:
+                fails.append(f"centroid brute n={n} start={s}: {got[0].tolist()} != {want}")
+        mask = np.zeros(n, np.uint8)
+        mask[[1, 3]] = 1
+        want = _brute_centroid(E, 0, n - 3, excluded={1, 3})
+        got, _, st = oracle.dseq_centroid(E, [0], n - 3, mask=mask, lib=lib)
+        if st != 0 or got[0].tolist() != want:
+            fails.append(f"centroid brute masked n={n}: {got[0].tolist()} != {want}")
+    # 4. tiled scan == one pass
+    E = workloads.clustered_table(60, 8, n_centres=4, sigma=0.3, seed=8)
+    base, _, _ = oracle.dseq_centroid(E, [0, 31, 59], 25, lib=lib)
+    for T in (1, 7, 59, 64):
+        got, _, _ = oracle.dseq_centroid(E, [0, 31, 59], 25, tile=T, lib=lib)
+        if not np.array_equal(got, base):
+            fails.append(f"centroid tile {T} differs")
+    return fails
+
+
 # --------------------------------------------------------------------------
 # pins for the BMU oracle
 
@@ -276,6 +356,10 @@ def test_dseq_pins(oracle_lib):
     assert pins_dseq(oracle_lib) == []
 
 
+def test_centroid_pins(oracle_lib):
+    assert pins_centroid(oracle_lib) == []
+
+
 def test_bmu_pins(oracle_lib):
     assert pins_bmu(oracle_lib) == []
 
@@ -310,6 +394,14 @@ MUTANTS = {
     "pick_unmasked": ("masked[w] = 1;\n            p = w;", "p = w;", "dseq"),
     "transposed_dot": ("s += (double)ep[k] * (double)ec[k];",
                        "s += (double)ep[k] * (double)ec[(k + 1) % D];", "dseq"),
+    "centroid_newest_only": ("for (int32_t i = 0; i < n_members; ++i)\n        for (int32_t k = 0; k < D; ++k) C[k]",
+                             "for (int32_t i = n_members - 1; i < n_members; ++i)\n        for (int32_t k = 0; k < D; ++k) C[k]",
+                             "centroid"),
+    "centroid_drops_start": ("for (int32_t i = 0; i < n_members; ++i)\n        for (int32_t k = 0; k < D; ++k) C[k]",
+                             "for (int32_t i = 1; i < n_members; ++i)\n        for (int32_t k = 0; k < D; ++k) C[k]",
+                             "centroid"),
+    "centroid_zero_reading": ("            d[c] = 1.0;\n            continue;", "            d[c] = 0.0;\n            continue;",
+                              "centroid"),
     "diff_sign": ("double diff = (double)x[k] - (double)w[k];",
                   "double diff = (double)x[k] + (double)w[k];", "bmu"),
     "bmu_ties_to_highest": ("if (best_j < 0 || d < best) {",
@@ -331,5 +423,5 @@ def test_mutant_fails_a_pin(name, tmp_path):
     lib_path = str(tmp_path / f"liboracle_{name}.so")
     oracle.compile_library(str(mut), lib_path)
     lib = oracle.load(lib_path)
-    fails = pins_dseq(lib) if which == "dseq" else pins_bmu(lib)
+    fails = {"dseq": pins_dseq, "bmu": pins_bmu, "centroid": pins_centroid}[which](lib)
     assert fails, f"mutant {name} passed every pin"
