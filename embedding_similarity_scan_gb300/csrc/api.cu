@@ -68,6 +68,7 @@ struct Options {
     int64_t timeline = 0;
     int64_t pair = 1;
     int64_t storage = 0;
+    int64_t criterion = 0;
 };
 std::mutex g_opt_mu;
 Options g_defaults;
@@ -87,6 +88,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "timeout_ms") {
         if (v < 1 || v > 3600000) return fail(DSEQ_EINVAL, "timeout_ms out of range");
         o.timeout_ms = v;
+    } else if (n == "criterion") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "criterion must be 0 (max-min) or 1 (centroid)");
+        o.criterion = v;
     } else if (n == "storage") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "storage must be 0 (split) or 1 (fp16)");
         o.storage = v;
@@ -116,6 +120,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "timeline") return o.timeline;
     if (n == "pair") return o.pair;
     if (n == "storage") return o.storage;
+    if (n == "criterion") return o.criterion;
     return -1;
 }
 
@@ -330,14 +335,14 @@ struct dseq_ctx {
     int64_t N = 0;
     int32_t D = 0, Dp = 0;
     Options opt;
-    DevBuf e_unit, e_split, e_f16, rn;
+    DevBuf e_unit, e_split, e_f16, rn, nrm;
     // run workspace
-    DevBuf m, keys, q, q_rn, status, barrier, starts, mask, picks, trace_slot, timeline;
+    DevBuf m, keys, q, q_rn, csum, status, barrier, starts, mask, picks, trace_slot, timeline;
     int64_t timeline_iters = 0, timeline_grid = 0;
     ~dseq_ctx() {
-        DevBuf *all[] = {&e_unit, &e_split, &e_f16, &rn,     &m,          &keys,
-                         &q,      &q_rn,    &status, &barrier, &starts, &mask,
-                         &picks,  &trace_slot, &timeline};
+        DevBuf *all[] = {&e_unit, &e_split, &e_f16,  &rn,      &nrm,    &m,
+                         &keys,   &q,       &q_rn,   &csum,    &status, &barrier,
+                         &starts, &mask,    &picks,  &trace_slot, &timeline};
         for (DevBuf *b : all) b->release();
     }
 };
@@ -403,6 +408,7 @@ int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device, v
     if ((r = ctx->e_split.ensure((size_t)N * 2 * ctx->Dp * sizeof(__half))) != DSEQ_OK) return bail(r);
     if ((r = ctx->e_f16.ensure((size_t)N * ctx->Dp * sizeof(__half))) != DSEQ_OK) return bail(r);
     if ((r = ctx->rn.ensure((size_t)N * sizeof(float))) != DSEQ_OK) return bail(r);
+    if ((r = ctx->nrm.ensure((size_t)N * sizeof(float))) != DSEQ_OK) return bail(r);
     if ((r = ctx->status.ensure(sizeof(int))) != DSEQ_OK) return bail(r);
     DevBuf staged;
     const float *tdev = nullptr;
@@ -410,7 +416,8 @@ int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device, v
     e = cudaMemsetAsync(ctx->status.p, 0, sizeof(int), st);
     if (e == cudaSuccess) {
         launch_table_prepare(tdev, N, D, ctx->Dp, ctx->e_unit.as<float>(),
-                             ctx->e_split.as<__half>(), ctx->status.as<int>(), st);
+                             ctx->e_split.as<__half>(), ctx->nrm.as<float>(),
+                             ctx->status.as<int>(), st);
         launch_table_prepare_f16(tdev, N, D, ctx->Dp, ctx->e_f16.as<__half>(),
                                  ctx->rn.as<float>(), ctx->status.as<int>(), st);
         e = cudaGetLastError();
@@ -561,6 +568,14 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.e_f16 = f16 ? ctx->e_f16.as<__half>() : nullptr;
         a.rn = ctx->rn.as<float>();
         a.q_rn = ctx->q_rn.as<float>();
+        a.centroid = (int)ctx->opt.criterion;
+        if (a.centroid) {
+            if (f16) return fail(DSEQ_EINVAL, "the centroid criterion runs on split storage (storage=0)");
+            TRY(ctx->csum.ensure((size_t)Bp * ctx->Dp * sizeof(double)));
+            a.csum = ctx->csum.as<double>();
+        }
+        a.e_unit = ctx->e_unit.as<float>();
+        a.nrm = ctx->nrm.as<float>();
         a.m = ctx->m.as<float>();
         a.keys = ctx->keys.as<unsigned long long>();
         a.picks = d_picks;
@@ -598,6 +613,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         g_stats.launches = 2;
     } else {
         // ---- FP32 FFMA path, one launch pair per iteration ----
+        if (ctx->opt.criterion != 0) return fail(DSEQ_EINVAL, "the FFMA engine runs the max-min criterion only");
         FfmaDseqArgs a;
         a.Nf = round_up(N, 64);
         a.Bp = (int)Bp;

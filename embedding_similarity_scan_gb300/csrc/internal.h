@@ -66,9 +66,10 @@ struct TcPlan {
 
 // ---- table preparation (api.cu calls; prep.cu defines) ---------------------
 // One warp per row: checks finiteness and a non-zero norm, writes the unit
-// row (float, zero-padded to Dp) and its split (hi | lo * 2^12) in fp16.
+// row (float, zero-padded to Dp), its split (hi | lo * 2^12) in fp16 and the
+// row's norm.
 void launch_table_prepare(const float *E, int64_t N, int D, int Dp, float *e_unit,
-                          __half *e_split, int *status, cudaStream_t st);
+                          __half *e_split, float *nrm, int *status, cudaStream_t st);
 
 // fp16 storage of the candidate table: row * 2^-e (max |.| in [0.5, 1)) rounded
 // to fp16, zero-padded to Dp; rn[r] = 1 / |stored row| (double sum).
@@ -91,6 +92,13 @@ struct TcDseqArgs {
     const __half *e_f16;
     const float *rn;
     float *q_rn;             // Bp: inverse norm of each current query row
+    // centroid criterion (centroid = 1): the query is the unit centroid of the
+    // rows a sequence holds; csum (Bp x Dp, double) keeps their sum, rebuilt
+    // from the unit rows e_unit (N x Dp) times the row norms nrm (N)
+    int centroid;
+    double *csum;
+    const float *e_unit;
+    const float *nrm;
     float *m;                // units x 128 x tile_n
     unsigned long long *keys;  // Bp
     int32_t *picks;          // B x L

@@ -41,7 +41,7 @@ __device__ __forceinline__ void split_f16(float x, __half &hi, __half &lo) {
 
 __global__ void table_prepare_kernel(const float *__restrict__ E, int64_t N, int D, int Dp,
                                      float *__restrict__ e_unit, __half *__restrict__ e_split,
-                                     int *status) {
+                                     float *__restrict__ nrm, int *status) {
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= N) return;
@@ -60,6 +60,7 @@ __global__ void table_prepare_kernel(const float *__restrict__ E, int64_t N, int
         return;
     }
     const double inv = 1.0 / sqrt(ss);
+    if (lane == 0) nrm[row] = (float)sqrt(ss);
     float *dst = e_unit + row * (int64_t)Dp;
     __half *sp = e_split + row * (int64_t)(2 * Dp);
     for (int k = lane; k < Dp; k += 32) {
@@ -214,9 +215,9 @@ inline unsigned blocks_for_rows(int64_t rows, int warps_per_block) {
 }  // namespace
 
 void launch_table_prepare(const float *E, int64_t N, int D, int Dp, float *e_unit,
-                          __half *e_split, int *status, cudaStream_t st) {
+                          __half *e_split, float *nrm, int *status, cudaStream_t st) {
     table_prepare_kernel<<<blocks_for_rows(N, 8), 256, 0, st>>>(E, N, D, Dp, e_unit, e_split,
-                                                                  status);
+                                                                  nrm, status);
 }
 
 void launch_table_prepare_f16(const float *E, int64_t N, int D, int Dp, __half *e_f16,

@@ -129,6 +129,16 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
          i < (int64_t)p.n_beta * kUnitRows; i += stride)
         a.keys[i] = 0ull;
+    if (a.centroid) {  // centroid sums start at the start rows
+        const int64_t ctotal = (int64_t)p.n_beta * kUnitRows * a.Dp;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ctotal;
+             i += stride) {
+            const int b = (int)(i / a.Dp), k = (int)(i - (int64_t)b * a.Dp);
+            a.csum[i] = b < a.B ? (double)a.e_unit[(int64_t)starts[b] * a.Dp + k] *
+                                      (double)a.nrm[starts[b]]
+                                : 0.0;
+        }
+    }
 }
 
 __device__ __forceinline__ void stamp(const TcDseqArgs &a, int t, int slot) {
@@ -136,7 +146,7 @@ __device__ __forceinline__ void stamp(const TcDseqArgs &a, int t, int slot) {
         a.timeline[((size_t)t * gridDim.x + blockIdx.x) * kTimelineSlots + slot] = globaltimer_ns();
 }
 
-template <bool kPair, bool kF16>
+template <bool kPair, bool kF16, bool kCentroid>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_dseq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
@@ -401,6 +411,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int v = 0; v < 8; ++v) {
                         float mv[4] = {mcur[v].x, mcur[v].y, mcur[v].z, mcur[v].w};
                         bool changed = false;
+                        // max-min: m keeps the running minimum.  Centroid: m is
+                        // -inf for held / masked rows and this iteration's
+                        // distance otherwise.
 #pragma unroll
                         for (int z = 0; z < 4; ++z) {
                             // split storage: d = 1 - <q, e>, the accumulator holding
@@ -408,8 +421,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const float d =
                                 kF16 ? fmaf(acc[4 * v + z] * my_rn[4 * v + z], neg_rnq, 1.0f)
                                      : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
-                            changed |= d < mv[z];
-                            mv[z] = fminf(mv[z], d);
+                            const float nv = kCentroid ? (mv[z] == -INFINITY ? -INFINITY : d)
+                                                       : fminf(mv[z], d);
+                            changed |= nv != mv[z];
+                            mv[z] = nv;
                             if (mv[z] > best) {
                                 best = mv[z];
                                 best_c = cbase + 4 * v + z;
@@ -497,6 +512,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const unsigned long long ki = __shfl_sync(0xffffffffu, key, i);
                     const uint32_t wi = __shfl_sync(0xffffffffu, w, i);
                     if (ki == 0ull) continue;
+                    if (kCentroid) {
+                        // add the winner to the sequence's centroid sum (double),
+                        // then write the split unit centroid as the next query
+                        const int bq = base + i;
+                        double *cs = a.csum + (int64_t)bq * a.Dp;
+                        const float *eu = a.e_unit + (int64_t)wi * a.Dp;
+                        const double nw = (double)a.nrm[wi];
+                        double ss = 0.0;
+                        for (int k = lane; k < a.Dp; k += 32) {
+                            const double cv = cs[k] + (double)eu[k] * nw;
+                            cs[k] = cv;
+                            ss += cv * cv;
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                        const double inv = ss > 0.0 ? 1.0 / sqrt(ss) : 0.0;
+                        __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
+                        for (int k = lane; k < a.Dp; k += 32) {
+                            const float u = (float)(cs[k] * inv);
+                            const __half hi = __float2half_rn(u);
+                            const __half lo = __float2half_rn((u - __half2float(hi)) * 4096.0f);
+                            qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
+                            qd[a.Dp + k] = hi;
+                            qd[2 * a.Dp + k] = lo;
+                        }
+                        continue;
+                    }
                     if (kF16) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(a.e_f16 + (int64_t)wi * a.Dp);
                         uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * a.Dp);
@@ -578,14 +620,14 @@ void launch_tc_dseq_init_impl(const TcDseqArgs &a, const TcPlan &p, const int32_
     tc_dseq_init_kernel<<<2048, 256, 0, st>>>(a, p, starts, mask);
 }
 
-template <bool kPair, bool kF16>
+template <bool kPair, bool kF16, bool kCentroid>
 cudaError_t launch_variant(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st) {
     TcDseqArgs aa = a;
     TcPlan pp = p;
     CUtensorMap mq = tmap_q, me = tmap_e;
     const size_t smem = DseqCfg<kPair, kF16>::kSmemBytes;
-    auto kernel = tc_dseq_kernel<kPair, kF16>;
+    auto kernel = tc_dseq_kernel<kPair, kF16, kCentroid>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -628,17 +670,22 @@ void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *st
 cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st) {
     const bool f16 = a.e_f16 != nullptr;
+    if (a.centroid) {  // split storage only
+        if (f16) return cudaErrorInvalidValue;
+        return p.pair ? launch_variant<true, false, true>(a, p, tmap_q, tmap_e, st)
+                      : launch_variant<false, false, true>(a, p, tmap_q, tmap_e, st);
+    }
     if (p.pair)
-        return f16 ? launch_variant<true, true>(a, p, tmap_q, tmap_e, st)
-                   : launch_variant<true, false>(a, p, tmap_q, tmap_e, st);
-    return f16 ? launch_variant<false, true>(a, p, tmap_q, tmap_e, st)
-               : launch_variant<false, false>(a, p, tmap_q, tmap_e, st);
+        return f16 ? launch_variant<true, true, false>(a, p, tmap_q, tmap_e, st)
+                   : launch_variant<true, false, false>(a, p, tmap_q, tmap_e, st);
+    return f16 ? launch_variant<false, true, false>(a, p, tmap_q, tmap_e, st)
+               : launch_variant<false, false, false>(a, p, tmap_q, tmap_e, st);
 }
 
 int tc_dseq_pair_max_clusters(int tile_n) {
     (void)tile_n;
     const size_t smem = DseqCfg<true, false>::kSmemBytes;
-    if (cudaFuncSetAttribute(tc_dseq_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_dseq_kernel<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -655,7 +702,7 @@ int tc_dseq_pair_max_clusters(int tile_n) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_dseq_kernel<true, false>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_dseq_kernel<true, false, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

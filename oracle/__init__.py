@@ -77,6 +77,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_dseq.restype = ctypes.c_int
     lib.oracle_centroid_dist.argtypes = [_f32p, i64, i32, _f64p, _i64p, i32, _f64p]
     lib.oracle_centroid_dist.restype = None
+    lib.oracle_centroid_dist_batch.argtypes = [_f32p, i64, i32, _f64p, _i64p, i32, i32, _f64p,
+                                               ctypes.c_int]
+    lib.oracle_centroid_dist_batch.restype = None
     lib.oracle_dseq_centroid.argtypes = [_f32p, i64, i32, _i32p, i32, i32, ctypes.c_void_p, i64,
                                          _i32p, ctypes.c_void_p, ctypes.c_int]
     lib.oracle_dseq_centroid.restype = ctypes.c_int
@@ -171,6 +174,18 @@ def centroid_dist(E, nrm, members, lib=None) -> np.ndarray:
     (lib or load()).oracle_centroid_dist(E, E.shape[0], E.shape[1],
                                          np.ascontiguousarray(nrm, np.float64), members,
                                          members.size, out)
+    return out
+
+
+def centroid_dist_batch(E, nrm, members, threads: int = 0, lib=None) -> np.ndarray:
+    """centroid_dist for every row of members (R x n_members) -> R x N."""
+    E = _f32(E)
+    members = np.ascontiguousarray(members, np.int64)
+    R, k = members.shape
+    out = np.empty((R, E.shape[0]), np.float64)
+    (lib or load()).oracle_centroid_dist_batch(E, E.shape[0], E.shape[1],
+                                               np.ascontiguousarray(nrm, np.float64), members,
+                                               R, k, out, int(threads))
     return out
 
 

@@ -209,6 +209,18 @@ void oracle_centroid_dist(const float *E, int64_t N, int32_t D, const double *nr
     free(C);
 }
 
+/* oracle_centroid_dist for R sequences at once (teacher forcing): row r of
+ * members (R x n_members) lists sequence r's rows; d is R x N. */
+void oracle_centroid_dist_batch(const float *E, int64_t N, int32_t D, const double *nrm,
+                                const int64_t *members, int32_t R, int32_t n_members, double *d,
+                                int threads) {
+    set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t r = 0; r < R; ++r)
+        oracle_centroid_dist(E, N, D, nrm, members + (int64_t)r * n_members, n_members,
+                             d + (int64_t)r * N);
+}
+
 /* Greedy centroid-criterion sequences (arguments as oracle_dseq); radius
  * receives the centroid distance of each pick. */
 int oracle_dseq_centroid(const float *E, int64_t N, int32_t D, const int32_t *starts, int32_t B,

@@ -66,6 +66,46 @@ def check_dseq_teacher_forced(E, starts, mask, picks, trace, trace_seqs, threads
     return worst
 
 
+def check_centroid_teacher_forced(E, starts, mask, picks, trace, trace_seqs, threads=0):
+    """Centroid criterion under teacher forcing: at every iteration the GPU's
+    centroid distances equal the oracle's (centroid of the start and the
+    GPU's earlier picks) within 1e-5 on unmasked rows, masked rows are -inf,
+    and each pick's oracle distance is within 1e-5 of the oracle maximum."""
+    E = np.ascontiguousarray(E, np.float32)
+    N = E.shape[0]
+    picks = np.asarray(picks)
+    trace_seqs = np.asarray(trace_seqs, np.int64)
+    R = trace_seqs.size
+    L = picks.shape[1]
+    nrm = oracle.row_norms(E)
+    masked = np.zeros((R, N), bool)
+    if mask is not None:
+        masked |= np.asarray(mask, bool)[None, :]
+    members = np.empty((R, L + 1), np.int64)
+    members[:, 0] = np.asarray(starts, np.int64)[trace_seqs]
+    rows = np.arange(R)
+    masked[rows, members[:, 0]] = True
+    worst = 0.0
+    for t in range(L):
+        d = oracle.centroid_dist_batch(E, nrm, members[:, :t + 1], threads=threads)
+        g = np.asarray(trace[:, t, :], np.float64)
+        live = ~masked
+        if live.any():
+            err = np.abs(g - d)[live].max()
+            worst = max(worst, float(err))
+            assert err <= TOL, f"t={t}: centroid distance differs by {err}"
+        assert np.all(np.isneginf(g[masked])), f"t={t}: masked candidate not -inf"
+        pk = picks[trace_seqs, t].astype(np.int64)
+        assert np.all((pk >= 0) & (pk < N)), f"t={t}: pick out of range"
+        assert not masked[rows, pk].any(), f"t={t}: masked or repeated pick"
+        best = np.where(live, d, -np.inf).max(axis=1)
+        gap = best - d[rows, pk]
+        assert np.all(gap <= TOL), f"t={t}: pick is {gap.max()} below the oracle maximum"
+        masked[rows, pk] = True
+        members[:, t + 1] = pk
+    return worst
+
+
 def check_picks_valid(starts, mask, picks, N):
     """Every pick is in range, unmasked, never a start of its sequence, and
     distinct within its sequence."""

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import workloads
-from parity import check_dseq_teacher_forced, check_picks_valid
+from parity import check_centroid_teacher_forced, check_dseq_teacher_forced, check_picks_valid
 
 pytestmark = pytest.mark.gpu
 
@@ -32,18 +32,20 @@ def es():
 def _reset_options(es):
     yield
     for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("timeout_ms", 10000),
-                    ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR), ("storage", 0)):
+                    ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR), ("storage", 0),
+                    ("criterion", 0)):
         es.dseq_set_option(name, v)
 
 
 def _run(es, E, starts, L, mask=None, trace_seqs=None, engine=0, tile_n=0, grid=0,
-         pair=None, storage=0):
+         pair=None, storage=0, criterion=0):
     dev = torch.device("cuda")
     es.dseq_set_option("engine", engine)
     es.dseq_set_option("tile_n", tile_n)
     es.dseq_set_option("grid", grid)
     es.dseq_set_option("pair", DEFAULT_PAIR if pair is None else pair)
     es.dseq_set_option("storage", storage)
+    es.dseq_set_option("criterion", criterion)
     ctx = es.dseq_create(torch.from_numpy(E).to(dev))
     try:
         st = torch.from_numpy(np.asarray(starts, np.int32)).to(dev)
@@ -279,3 +281,55 @@ def test_fp16_storage_full_size_and_agreement(es):
     same_seq = float(np.mean(np.all(ref == got, axis=1)))
     same_pick = float(np.mean(ref == got))
     print(f"fp16 storage vs split: identical sequences {same_seq:.3f}, identical picks {same_pick:.3f}")
+
+
+# --------------------------------------------------------------------------
+# centroid criterion (the issue's "most different from the centroid")
+
+
+@pytest.mark.parametrize("pair", [1, 0])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
+def test_centroid_teacher_forced(es, pair, case):
+    N, D, B, L, kind, frac = case
+    E = workloads.gaussian_table(N, D, seed=N) if kind == "gaussian" else \
+        workloads.clustered_table(N, D, n_centres=16, seed=N)
+    starts = workloads.starts(N, B, seed=N)
+    mask = None
+    if frac > 0:
+        rng = np.random.default_rng(N)
+        mask = (rng.random(N) < frac).astype(np.uint8)
+        mask[starts[: B // 3]] = 1
+    trace_seqs = np.arange(min(B, 64), dtype=np.int32)
+    picks, trace = _run(es, E, starts, L, mask, trace_seqs, pair=pair, criterion=1)
+    check_picks_valid(starts, mask, picks, N)
+    check_centroid_teacher_forced(E, starts, mask, picks, trace, trace_seqs)
+
+
+def test_centroid_worked_example(es):
+    """Four rows on which the two criteria disagree (hand-derived)."""
+    c, s = np.float32(np.cos(np.radians(10.0))), np.float32(np.sin(np.radians(10.0)))
+    E = np.array([[1, 0], [c, s], [-1, 0], [0, 1]], np.float32)
+    for pair in (1, 0):
+        got, _ = _run(es, E, np.array([0], np.int32), 3, pair=pair, criterion=1)
+        assert got.tolist() == [[2, 1, 3]]
+        got, _ = _run(es, E, np.array([0], np.int32), 3, pair=pair, criterion=0)
+        assert got.tolist() == [[2, 3, 1]]
+
+
+def test_centroid_full_size(es):
+    cfg = workloads.DIVERSITY["page1"]
+    E = cfg.table(seed=0)
+    starts = cfg.starts(seed=0)
+    tr = np.sort(np.random.default_rng(2).choice(cfg.B, 16, replace=False)).astype(np.int32)
+    picks, trace = _run(es, E, starts, cfg.L, trace_seqs=tr, criterion=1)
+    check_centroid_teacher_forced(E, starts[tr], None, picks[tr], trace, np.arange(tr.size))
+    srt = np.sort(picks, axis=1)
+    assert not np.any(srt[:, 1:] == srt[:, :-1]) and not np.any(picks == starts[:, None])
+
+
+def test_centroid_rejects_fp16_storage_and_ffma(es):
+    E = workloads.gaussian_table(100, 16, seed=1)
+    with pytest.raises(es.DseqError):
+        _run(es, E, np.array([0], np.int32), 3, storage=1, criterion=1)
+    with pytest.raises(es.DseqError):
+        _run(es, E, np.array([0], np.int32), 3, engine=1, criterion=1)
