@@ -69,6 +69,7 @@ struct Options {
     int64_t pair = 1;
     int64_t storage = 0;
     int64_t criterion = 0;
+    int64_t resume = 0;
 };
 std::mutex g_opt_mu;
 Options g_defaults;
@@ -88,6 +89,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "timeout_ms") {
         if (v < 1 || v > 3600000) return fail(DSEQ_EINVAL, "timeout_ms out of range");
         o.timeout_ms = v;
+    } else if (n == "resume") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "resume must be 0 or 1");
+        o.resume = v;
     } else if (n == "criterion") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "criterion must be 0 (max-min) or 1 (centroid)");
         o.criterion = v;
@@ -121,6 +125,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "pair") return o.pair;
     if (n == "storage") return o.storage;
     if (n == "criterion") return o.criterion;
+    if (n == "resume") return o.resume;
     return -1;
 }
 
@@ -339,6 +344,13 @@ struct dseq_ctx {
     // run workspace
     DevBuf m, keys, q, q_rn, csum, status, barrier, starts, mask, picks, trace_slot, timeline;
     int64_t timeline_iters = 0, timeline_grid = 0;
+    // state left on the device by the last successful run, for "resume"
+    bool has_state = false;
+    int64_t state_picks = 0;  // picks per sequence made so far
+    int64_t state_sig = -1;   // engine / pair / storage / criterion of that run
+    TcPlan state_plan{};
+    std::vector<int32_t> state_starts;
+    std::vector<uint8_t> state_mask;
     ~dseq_ctx() {
         DevBuf *all[] = {&e_unit, &e_split, &e_f16,  &rn,      &nrm,    &m,
                          &keys,   &q,       &q_rn,   &csum,    &status, &barrier,
@@ -468,6 +480,18 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     TRY(to_host(starts, (size_t)B, h_starts, st));
     std::vector<uint8_t> h_mask;
     if (mask) TRY(to_host(mask, (size_t)N, h_mask, st));
+    // resume: continue the last run on this context from the state it left
+    // on the device (same sequences, mask and mode; picks continue)
+    const bool resume = ctx->opt.resume != 0;
+    const int64_t sig = ctx->opt.engine * 1000 + ctx->opt.pair * 100 + ctx->opt.storage * 10 +
+                        ctx->opt.criterion;
+    if (resume) {
+        if (!ctx->has_state) return fail(DSEQ_EINVAL, "resume: no earlier run state on this context");
+        if (sig != ctx->state_sig) return fail(DSEQ_EINVAL, "resume: engine, pair, storage or criterion differ from the earlier run");
+        if (h_starts != ctx->state_starts) return fail(DSEQ_EINVAL, "resume: starts differ from the earlier run");
+        if (h_mask != ctx->state_mask) return fail(DSEQ_EINVAL, "resume: mask differs from the earlier run");
+    }
+    const int64_t done_before = resume ? ctx->state_picks : 0;
     {
         std::vector<uint8_t> seen((size_t)N, 0);
         int64_t n_masked = 0;
@@ -478,10 +502,11 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             if (s < 0 || s >= N) return fail(DSEQ_EINVAL, "starts[%d]=%d out of range [0, %lld)", b, s, (long long)N);
             if (seen[s]) return fail(DSEQ_EINVAL, "start %d repeated", s);
             seen[s] = 1;
-            const int64_t avail = N - n_masked - ((mask && h_mask[s]) ? 0 : 1);
+            const int64_t avail = N - n_masked - ((mask && h_mask[s]) ? 0 : 1) - done_before;
             if (L > avail) return fail(DSEQ_EINVAL, "L=%d exceeds the %lld candidates left to sequence %d", L, (long long)avail, b);
         }
     }
+    if (!resume) ctx->has_state = false;
     std::vector<int32_t> h_slot;
     // CTA pairs work on pairs of 128-sequence blocks: pad B to 256 there
     const bool pair = ctx->opt.engine == 0 && ctx->opt.pair != 0;
@@ -537,7 +562,9 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         plan.n_beta = (int)(Bp / kUnitRows);
         plan.pair = pair ? 1 : 0;
         int grid_cap = ctx->opt.grid > 0 ? (int)std::min<int64_t>(ctx->opt.grid, info.sms) : info.sms;
-        if (pair) {
+        if (resume) {
+            plan = ctx->state_plan;  // the running-minimum layout depends on it
+        } else if (pair) {
             // whole clusters of two, no more than can be co-resident
             const int max_clusters = tc_dseq_pair_max_clusters(256);
             if (max_clusters < 1) return fail(DSEQ_ELAUNCH, "no CTA pair of the pair kernel fits on this device");
@@ -602,8 +629,9 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             ctx->timeline_grid = plan.grid;
         }
         CUDA_TRY(cudaMemsetAsync(ctx->barrier.p, 0, sizeof(unsigned), st));
-        launch_tc_dseq_init(a, plan, ctx->starts.as<int32_t>(), d_mask, st);
+        if (!resume) launch_tc_dseq_init(a, plan, ctx->starts.as<int32_t>(), d_mask, st);
         CUDA_TRY(cudaGetLastError());
+        ctx->state_plan = plan;
         TRY(timer.start(st));
         CUDA_TRY(launch_tc_dseq(a, plan, tq, te, st));
         TRY(timer.stop(st));
@@ -631,7 +659,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.B = B;
         a.L = L;
         a.Dp = ctx->Dp;
-        launch_ffma_dseq_init(a, ctx->starts.as<int32_t>(), d_mask, st);
+        if (!resume) launch_ffma_dseq_init(a, ctx->starts.as<int32_t>(), d_mask, st);
         CUDA_TRY(cudaGetLastError());
         TRY(timer.start(st));
         for (int t = 0; t < L; ++t) launch_ffma_dseq_iteration(a, t, st);
@@ -642,7 +670,18 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         g_stats.grid = (int64_t)g_stats.units;
         g_stats.launches = 1 + 2 * (int64_t)L;
     }
-    TRY(read_status(ctx->status.as<int>(), st));
+    {
+        const int rs = read_status(ctx->status.as<int>(), st);
+        if (rs != DSEQ_OK) {
+            ctx->has_state = false;
+            return rs;
+        }
+    }
+    ctx->has_state = true;
+    ctx->state_picks = done_before + L;
+    ctx->state_sig = sig;
+    ctx->state_starts = h_starts;
+    ctx->state_mask = h_mask;
     g_stats.kernel_ns = timer.ns();
     if (!picks_on_dev) {
         CUDA_TRY(cudaMemcpyAsync(picks, d_picks, (size_t)B * L * sizeof(int32_t), cudaMemcpyDeviceToHost, st));

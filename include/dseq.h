@@ -174,6 +174,15 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 32 in [32, 256]; 0 = chosen from the shape (default).
  *   "grid"        persistent CTAs; 0 = one per SM (default).
  *   "timeout_ms"  limit of every device-side wait (default 10000).
+ *   "resume"      1 = dseq_run continues the last successful run on this
+ *                 context from the state it left on the device (running
+ *                 minima, current queries): the same starts, mask and
+ *                 engine / pair / storage / criterion settings are required,
+ *                 picks[b*L + t] then holds pick (earlier picks + t) of
+ *                 sequence b, and L may use the candidates left after the
+ *                 earlier picks.  A long ordering (L up to N - 1) can so be
+ *                 made in chunks, with results identical to one long call.
+ *                 Default 0 (every call starts its sequences afresh).
  *   "criterion"   0 = max-min (default): a candidate's score is its smallest
  *                 cosine distance to any row the sequence holds; 1 = centroid:
  *                 its cosine distance to the centroid (plain mean) of those

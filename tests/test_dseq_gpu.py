@@ -33,7 +33,7 @@ def _reset_options(es):
     yield
     for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("timeout_ms", 10000),
                     ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR), ("storage", 0),
-                    ("criterion", 0)):
+                    ("criterion", 0), ("resume", 0)):
         es.dseq_set_option(name, v)
 
 
@@ -333,3 +333,62 @@ def test_centroid_rejects_fp16_storage_and_ffma(es):
         _run(es, E, np.array([0], np.int32), 3, storage=1, criterion=1)
     with pytest.raises(es.DseqError):
         _run(es, E, np.array([0], np.int32), 3, engine=1, criterion=1)
+
+
+# --------------------------------------------------------------------------
+# long orderings in chunks ("resume"): the issue's driver runs the sequences
+# in chunks of iterations; continuing from the state left on the device must
+# give exactly the picks of one long call.
+
+
+@pytest.mark.parametrize("engine,pair,criterion", [(0, 1, 0), (0, 0, 0), (1, 0, 0), (0, 1, 1)])
+def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion):
+    N, D, B = 300, 40, 9
+    E = workloads.clustered_table(N, D, n_centres=6, seed=12)
+    starts = workloads.starts(N, B, seed=12)
+    mask = np.zeros(N, np.uint8)
+    mask[::17] = 1
+    mask[starts] = 0
+    L_total = N - int(mask.sum()) - 1  # the full ordering of every sequence
+    traced = np.array([0, B - 1], np.int32)
+    es.dseq_set_option("engine", engine)
+    es.dseq_set_option("pair", pair)
+    es.dseq_set_option("criterion", criterion)
+    ctx = es.dseq_create(torch.from_numpy(E).cuda())
+    try:
+        st = torch.from_numpy(starts).cuda()
+        mk = torch.from_numpy(mask).cuda()
+        es.dseq_set_option("resume", 0, ctx)
+        whole = es.dseq_run(ctx, st, L_total, mask=mk).cpu().numpy()
+        parts, traces = [], []
+        for i, chunk in enumerate((50, 1, 100, L_total - 151)):
+            es.dseq_set_option("resume", 0 if i == 0 else 1, ctx)
+            pk, tr = es.dseq_run_trace(ctx, st, chunk, torch.from_numpy(traced).cuda(), mask=mk)
+            parts.append(pk.cpu().numpy())
+            traces.append(tr.cpu().numpy())
+        with pytest.raises(es.DseqError):  # nothing left to pick
+            es.dseq_run(ctx, st, 1, mask=mk)
+        with pytest.raises(es.DseqError):  # different starts
+            es.dseq_run(ctx, torch.flip(st, [0]), 1, mask=mk)
+        with pytest.raises(es.DseqError):  # different mask
+            es.dseq_run(ctx, st, 1)
+    finally:
+        ctx.close()
+    chunked = np.concatenate(parts, axis=1)
+    assert np.array_equal(chunked, whole)
+    check_picks_valid(starts, mask, whole, N)
+    # the chunks' traces, joined, follow the oracle from the starts on
+    trace = np.concatenate(traces, axis=1)
+    check = check_centroid_teacher_forced if criterion else check_dseq_teacher_forced
+    check(E, starts, mask, chunked, trace, traced)
+
+
+def test_resume_without_state_rejected(es):
+    E = workloads.gaussian_table(64, 16, seed=3)
+    ctx = es.dseq_create(torch.from_numpy(E).cuda())
+    try:
+        es.dseq_set_option("resume", 1, ctx)
+        with pytest.raises(es.DseqError):
+            es.dseq_run(ctx, torch.tensor([0, 5], dtype=torch.int32, device="cuda"), 3)
+    finally:
+        ctx.close()
