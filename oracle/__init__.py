@@ -20,6 +20,11 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   bmu, sqdist_pairs               -- pinned: codebook containing the samples,
       integer lattice codebook (BMU = nearest lattice point), duplicate
       neurons, brute force against an independent argmin on tiny inputs.
+  som_update                      -- pinned: sigma = 0 gives the per-neuron
+      mean of the assigned samples (independent group-by), identical samples,
+      a lattice map whose closed-form means are the grid coordinates (edge
+      neurons biased inward by the one-sided window), the window corner and
+      just-outside weights, mirror symmetry of the grid.
 """
 from __future__ import annotations
 
@@ -88,6 +93,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_bmu.restype = None
     lib.oracle_sqdist_pairs.argtypes = [_f32p, _f32p, i32, _i64p, _i64p, i64, _f64p]
     lib.oracle_sqdist_pairs.restype = None
+    lib.oracle_som_update.argtypes = [_f32p, i64, i32, _i32p, _f32p, i32, i32, ctypes.c_double,
+                                      i32, _i64p, i64, _f64p, ctypes.c_int]
+    lib.oracle_som_update.restype = None
     return lib
 
 
@@ -224,4 +232,21 @@ def sqdist_pairs(X, W, ii, jj, lib=None) -> np.ndarray:
     jj = np.ascontiguousarray(jj, np.int64)
     out = np.empty(ii.size, np.float64)
     (lib or load()).oracle_sqdist_pairs(X, W, X.shape[1], ii, jj, ii.size, out)
+    return out
+
+
+def som_update(X, bmu, W, side_x: int, side_y: int, sigma: float, radius: int,
+               neurons=None, threads: int = 0, lib=None) -> np.ndarray:
+    """Batch-map neighbourhood update: new rows (float64) of the listed
+    neurons (default all M = side_x * side_y), given every sample's BMU."""
+    X, W = _f32(X), _f32(W)
+    n, D = X.shape
+    M = int(side_x) * int(side_y)
+    assert W.shape == (M, D)
+    bmu = np.ascontiguousarray(bmu, np.int32)
+    assert bmu.size == n
+    neurons = np.arange(M, dtype=np.int64) if neurons is None else np.ascontiguousarray(neurons, np.int64)
+    out = np.empty((neurons.size, D), np.float64)
+    (lib or load()).oracle_som_update(X, n, D, bmu, W, int(side_x), int(side_y), float(sigma),
+                                      int(radius), neurons, neurons.size, out, int(threads))
     return out

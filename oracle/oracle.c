@@ -32,11 +32,25 @@
  *     index of the codebook row at the smallest squared Euclidean distance,
  *     taken in the direct form sum_k (x_k - w_k)^2, lowest index on ties.
  *
+ *  3. The neighbourhood update of a SOM epoch (same page, sections 3
+ *     Background and 6, the epoch's composition: every sample's closest
+ *     neuron is found first, then that neuron and its neighbours on the map
+ *     are updated).  Since the update follows a search over all samples it
+ *     is read as the batch map: each neuron becomes the mean of all samples
+ *     weighted by the neighbourhood function between the neuron and each
+ *     sample's BMU on the grid.
+ *
  * Readings where the pages are silent:
  *   - cosine distance d(p, c) = 1 - <e_p, e_c> / (|e_p| |e_c|), in [0, 2];
  *   - the start row seeds the running minimum and is masked; L counts the
  *     picks after the start; the running minimum starts at +infinity;
- *   - the BMU distance is the squared distance (no square root).
+ *   - the BMU distance is the squared distance (no square root);
+ *   - the map is a planar rectangular grid of side_x x side_y neurons,
+ *     neuron j at column j % side_x and row j / side_x; the neighbourhood
+ *     weight between grid points a and b is exp(-|a - b|^2 / (2 sigma^2))
+ *     inside the square window |dx| <= R, |dy| <= R and 0 outside it
+ *     (sigma = 0: 1 for a == b, else 0); a neuron whose weights sum to 0
+ *     keeps its weights.
  *
  * Parallelism: OpenMP only across independent units (sequences, samples);
  * the arithmetic inside one unit is strictly sequential.
@@ -311,4 +325,40 @@ void oracle_sqdist_pairs(const float *X, const float *W, int32_t D, const int64_
                          const int64_t *jj, int64_t R, double *out) {
     for (int64_t r = 0; r < R; ++r)
         out[r] = sqdist(X + ii[r] * (int64_t)D, W + jj[r] * (int64_t)D, D);
+}
+
+/* Batch-map update of the listed neurons.
+ * X: n x D samples, bmu[i] their BMUs, W: M x D codebook (M = side_x *
+ * side_y).  For each listed neuron j, visiting the samples in ascending
+ * order, num = sum_i h(j, bmu[i]) X_i and den = sum_i h(j, bmu[i]); the
+ * row out[r] (neuron neurons[r]) is num / den, or W_j when den is 0. */
+void oracle_som_update(const float *X, int64_t n, int32_t D, const int32_t *bmu, const float *W,
+                       int32_t side_x, int32_t side_y, double sigma, int32_t radius,
+                       const int64_t *neurons, int64_t n_neurons, double *out, int threads) {
+    (void)side_y;
+    set_threads(threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_neurons; ++r) {
+        const int64_t j = neurons[r];
+        const int64_t xj = j % side_x, yj = j / side_x;
+        double *num = out + r * (int64_t)D;
+        double den = 0.0;
+        for (int32_t k = 0; k < D; ++k) num[k] = 0.0;
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t c = bmu[i];
+            const int64_t dx = c % side_x - xj, dy = c / side_x - yj;
+            if (dx > radius || dx < -radius || dy > radius || dy < -radius) continue;
+            double h;
+            if (sigma > 0.0)
+                h = exp(-(double)(dx * dx + dy * dy) / (2.0 * sigma * sigma));
+            else
+                h = (dx == 0 && dy == 0) ? 1.0 : 0.0;
+            if (h == 0.0) continue;
+            den += h;
+            const float *x = X + i * (int64_t)D;
+            for (int32_t k = 0; k < D; ++k) num[k] += h * (double)x[k];
+        }
+        const float *w = W + j * (int64_t)D;
+        for (int32_t k = 0; k < D; ++k) num[k] = den > 0.0 ? num[k] / den : (double)w[k];
+    }
 }

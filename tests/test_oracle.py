@@ -349,6 +349,133 @@ def pins_bmu(lib) -> list[str]:
     return fails
 
 
+def _read_som_golden():
+    out = {"expect": []}
+    with open(os.path.join(GOLDEN, "som_grid3x2.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, *vals = line.split()
+            if key == "sides":
+                out["sides"] = (int(vals[0]), int(vals[1]))
+            elif key == "sigma":
+                out["sigma"] = float(vals[0])
+            elif key == "samples":
+                out["X"] = np.array([[float(v) for v in t.split(",")] for t in vals], np.float32)
+            elif key == "bmu":
+                out["bmu"] = np.array([int(v) for v in vals], np.int32)
+            elif key == "old":
+                out["old"] = float(vals[0])
+            elif key == "expect":
+                R = int(vals[0].split("=")[1])
+                out["expect"].append((R, np.array([[float(v) for v in t.split(",")]
+                                                    for t in vals[1:]])))
+    return out
+
+
+def pins_som(lib) -> list[str]:
+    fails: list[str] = []
+
+    # 0. the hand-worked 3 x 2 map
+    g = _read_som_golden()
+    sx, sy = g["sides"]
+    W = np.full((sx * sy, g["X"].shape[1]), g["old"], np.float32)
+    for R, want in g["expect"]:
+        got = oracle.som_update(g["X"], g["bmu"], W, sx, sy, g["sigma"], R, lib=lib)
+        if not np.allclose(got, want, rtol=0, atol=1e-12):
+            fails.append(f"golden R={R}: {got.tolist()}")
+    got = oracle.som_update(g["X"], g["bmu"], W, sx, sy, 0.0, 1, lib=lib)
+    if not np.allclose(got, g["expect"][1][1], rtol=0, atol=1e-12):
+        fails.append("golden sigma=0 differs from R=0")
+
+    # 1. sigma = 0: each neuron is the mean of its own samples (an independent
+    #    group-by); neurons without samples keep their rows.
+    rng = np.random.default_rng(31)
+    sx, sy, D, n = 6, 4, 5, 100
+    M = sx * sy
+    X = rng.standard_normal((n, D)).astype(np.float32)
+    bmu = rng.integers(0, M - 5, n).astype(np.int32)  # the last five neurons get nothing
+    W = rng.standard_normal((M, D)).astype(np.float32)
+    sums = np.zeros((M, D))
+    np.add.at(sums, bmu, X.astype(np.float64))
+    cnt = np.bincount(bmu, minlength=M)
+    want = np.where(cnt[:, None] > 0, sums / np.maximum(cnt, 1)[:, None], W.astype(np.float64))
+    for R in (0, 3):
+        got = oracle.som_update(X, bmu, W, sx, sy, 0.0, R, lib=lib)
+        if not np.allclose(got, want, rtol=1e-13, atol=1e-13):
+            fails.append(f"sigma=0 R={R}: not the per-neuron mean")
+
+    # 2. identical samples: every neuron some BMU's window reaches becomes
+    #    that sample; the rest keep their rows.
+    x0 = rng.standard_normal(D).astype(np.float32)
+    Xs = np.tile(x0, (7, 1))
+    bmu = np.array([0, 0, 9, 9, 9, 23, 23], np.int32)
+    got = oracle.som_update(Xs, bmu, W, sx, sy, 1.1, 1, lib=lib)
+    cols, rows = np.arange(M) % sx, np.arange(M) // sx
+    reach = np.zeros(M, bool)
+    for c in np.unique(bmu):
+        reach |= (np.abs(cols - c % sx) <= 1) & (np.abs(rows - c // sx) <= 1)
+    want = np.where(reach[:, None], x0.astype(np.float64)[None, :], W.astype(np.float64))
+    if not np.allclose(got, want, rtol=1e-13, atol=1e-13):
+        fails.append("identical samples: wrong rows")
+
+    # 3. lattice map, one sample per neuron holding the neuron's own grid
+    #    coordinates.  The Gaussian factorises over the axes and the window is
+    #    a product of intervals, so each coordinate of the new row is a 1-D
+    #    weighted mean of the coordinates in the window, which for neurons at
+    #    least R from every edge is the neuron's own coordinate.
+    sx, sy, R, sigma = 7, 5, 2, 1.3
+    M = sx * sy
+    cols, rows = np.arange(M) % sx, np.arange(M) // sx
+    Xl = np.stack([cols, rows], 1).astype(np.float32)
+    got = oracle.som_update(Xl, np.arange(M, dtype=np.int32), np.zeros((M, 2), np.float32), sx, sy,
+                            sigma, R, lib=lib)
+
+    def mean_1d(c, side):
+        ks = np.arange(max(0, c - R), min(side - 1, c + R) + 1)
+        w = np.exp(-((ks - c) ** 2) / (2 * sigma * sigma))
+        return float((w * ks).sum() / w.sum())
+
+    want = np.array([[mean_1d(c, sx), mean_1d(r, sy)] for c, r in zip(cols, rows)])
+    if not np.allclose(got, want, rtol=0, atol=1e-12):
+        fails.append("lattice map: edge or interior means wrong")
+    inner = (cols >= R) & (cols < sx - R) & (rows >= R) & (rows < sy - R)
+    if not np.allclose(got[inner], Xl[inner], rtol=0, atol=1e-12):
+        fails.append("lattice map: interior neurons moved")
+
+    # 4. the window: a sample at the corner (R, R) counts with exp(-R^2 / sigma^2),
+    #    one at (R + 1, 0) does not count.
+    sx = sy = 9
+    M = 81
+    R, sigma = 2, 1.7
+    j = 4 * sx + 4
+    Xw = np.array([[1.0], [5.0], [1000.0]], np.float32)
+    bmu = np.array([j, (4 + R) * sx + 4 + R, 4 * sx + 4 + R + 1], np.int32)
+    got = oracle.som_update(Xw, bmu, np.zeros((M, 1), np.float32), sx, sy, sigma, R,
+                            neurons=[j], lib=lib)
+    h = np.exp(-(R * R) / (sigma * sigma))
+    if abs(got[0, 0] - (1.0 + 5.0 * h) / (1.0 + h)) > 1e-12:
+        fails.append(f"window corner / outside: {got[0, 0]}")
+
+    # 5. mirror symmetry: reflecting the map's columns reflects the result.
+    sx, sy, D, n = 8, 6, 3, 60
+    M = sx * sy
+    X = rng.standard_normal((n, D)).astype(np.float32)
+    bmu = rng.integers(0, M, n).astype(np.int32)
+    W = rng.standard_normal((M, D)).astype(np.float32)
+    flip = (np.arange(M) // sx) * sx + (sx - 1 - np.arange(M) % sx)
+    a = oracle.som_update(X, bmu, W, sx, sy, 1.4, 2, lib=lib)
+    b = oracle.som_update(X, flip[bmu].astype(np.int32), W[flip], sx, sy, 1.4, 2, lib=lib)
+    if not np.allclose(a[flip], b, rtol=1e-12, atol=1e-12):
+        fails.append("mirror symmetry broken")
+    # a subset of neurons gives the same rows as the whole map
+    sub = np.array([5, 0, 47, 13])
+    if not np.array_equal(oracle.som_update(X, bmu, W, sx, sy, 1.4, 2, neurons=sub, lib=lib),
+                          a[sub]):
+        fails.append("neuron subset differs from the whole map")
+    return fails
+
+
 # --------------------------------------------------------------------------
 
 
@@ -358,6 +485,10 @@ def test_dseq_pins(oracle_lib):
 
 def test_centroid_pins(oracle_lib):
     assert pins_centroid(oracle_lib) == []
+
+
+def test_som_pins(oracle_lib):
+    assert pins_som(oracle_lib) == []
 
 
 def test_bmu_pins(oracle_lib):
@@ -406,6 +537,19 @@ MUTANTS = {
                   "double diff = (double)x[k] + (double)w[k];", "bmu"),
     "bmu_ties_to_highest": ("if (best_j < 0 || d < best) {",
                             "if (best_j < 0 || d <= best) {", "bmu"),
+    "som_dropped_dy": ("h = exp(-(double)(dx * dx + dy * dy) / (2.0 * sigma * sigma));",
+                       "h = exp(-(double)(dx * dx) / (2.0 * sigma * sigma));", "som"),
+    "som_no_half": ("h = exp(-(double)(dx * dx + dy * dy) / (2.0 * sigma * sigma));",
+                    "h = exp(-(double)(dx * dx + dy * dy) / (sigma * sigma));", "som"),
+    "som_circular_window": ("if (h == 0.0) continue;",
+                            "if (h == 0.0 || dx * dx + dy * dy > (int64_t)radius * radius) continue;",
+                            "som"),
+    "som_zero_unassigned": (": (double)w[k];", ": 0.0;", "som"),
+    "som_transposed_grid": ("const int64_t xj = j % side_x, yj = j / side_x;",
+                            "const int64_t xj = j / side_y, yj = j % side_y;", "som"),
+    "som_last_sample_dropped": ("for (int64_t i = 0; i < n; ++i) {\n            const int64_t c = bmu[i];",
+                                "for (int64_t i = 0; i < n - 1; ++i) {\n            const int64_t c = bmu[i];",
+                                "som"),
     "bmu_dropped_term": ("for (int32_t k = 0; k < D; ++k) {\n        double diff",
                          "for (int32_t k = 1; k < D; ++k) {\n        double diff", "bmu"),
 }
@@ -423,5 +567,6 @@ def test_mutant_fails_a_pin(name, tmp_path):
     lib_path = str(tmp_path / f"liboracle_{name}.so")
     oracle.compile_library(str(mut), lib_path)
     lib = oracle.load(lib_path)
-    fails = {"dseq": pins_dseq, "bmu": pins_bmu, "centroid": pins_centroid}[which](lib)
+    fails = {"dseq": pins_dseq, "bmu": pins_bmu, "centroid": pins_centroid,
+             "som": pins_som}[which](lib)
     assert fails, f"mutant {name} passed every pin"
