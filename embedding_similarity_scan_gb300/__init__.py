@@ -36,8 +36,8 @@ _CODES = {v: k for k, v in list(globals().items()) if k.startswith("DSEQ_")}
 
 # every extern "C" symbol declared in include/dseq.h
 EXPORTS = ("dseq_create", "dseq_run", "dseq_run_trace", "dseq_destroy", "bmu_search",
-           "bmu_search_noalloc", "dseq_set_option", "dseq_get_option", "dseq_last_stat",
-           "dseq_last_error", "dseq_get_timeline")
+           "bmu_search_noalloc", "som_update", "som_epoch", "dseq_set_option",
+           "dseq_get_option", "dseq_last_stat", "dseq_last_error", "dseq_get_timeline")
 
 _lib = None
 
@@ -71,6 +71,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bmu_search.restype = ctypes.c_int
     lib.bmu_search_noalloc.argtypes = [vp, i64, vp, i64, i32, vp, vp, vp]
     lib.bmu_search_noalloc.restype = ctypes.c_int
+    lib.som_update.argtypes = [vp, i64, vp, i32, i32, i32, vp, ctypes.c_double, i32, vp]
+    lib.som_update.restype = ctypes.c_int
+    lib.som_epoch.argtypes = [vp, i64, vp, i32, i32, i32, ctypes.c_double, i32, vp, vp, vp]
+    lib.som_epoch.restype = ctypes.c_int
     lib.dseq_set_option.argtypes = [vp, ctypes.c_char_p, i64]
     lib.dseq_set_option.restype = ctypes.c_int
     lib.dseq_get_option.argtypes = [vp, ctypes.c_char_p]
@@ -246,6 +250,48 @@ def bmu_search(X, W, idx=None, dist=None, stream=None):
     _check(lib.bmu_search(_ptr(X), n, _ptr(W), M, D, _ptr(idx), _ptr(dist),
                           _stream(stream, X, W, idx, dist)))
     return idx, dist
+
+
+def _codebook_inout(W, side_x: int, side_y: int, D: int):
+    """W is updated in place, so it must already be contiguous float32."""
+    dt = str(W.dtype).replace("torch.", "")
+    if dt != "float32" or not (W.is_contiguous() if _is_torch(W) else W.flags.c_contiguous):
+        raise ValueError("W must be a contiguous float32 array (it is updated in place)")
+    if tuple(W.shape) != (int(side_x) * int(side_y), D):
+        raise ValueError(f"W must be (side_x*side_y, D) = ({int(side_x) * int(side_y)}, {D})")
+    return W
+
+
+def som_update(X, bmu, W, side_x: int, side_y: int, sigma: float, radius: int, stream=None):
+    """Batch-map neighbourhood update of W (side_x*side_y x D, in place) from
+    the samples X (n x D) and their BMUs; returns W."""
+    lib = load()
+    X = _as(X, "float32")
+    bmu = _as(bmu, "int32")
+    n, D = int(X.shape[0]), int(X.shape[1])
+    _codebook_inout(W, side_x, side_y, D)
+    if int(bmu.shape[0]) != n:
+        raise ValueError("bmu must have one entry per sample")
+    _check(lib.som_update(_ptr(X), n, _ptr(W), int(side_x), int(side_y), D, _ptr(bmu),
+                          float(sigma), int(radius), _stream(stream, X, bmu, W)))
+    return W
+
+
+def som_epoch(X, W, side_x: int, side_y: int, sigma: float, radius: int, bmu=None, dist=None,
+              stream=None):
+    """One SOM epoch: BMU search of X against W, then the neighbourhood update
+    of W in place.  Returns (bmu, dist) of the search."""
+    lib = load()
+    X = _as(X, "float32")
+    n, D = int(X.shape[0]), int(X.shape[1])
+    _codebook_inout(W, side_x, side_y, D)
+    if bmu is None:
+        bmu = _empty_like_kind(X, (n,), "int32")
+    if dist is None:
+        dist = _empty_like_kind(X, (n,), "float32")
+    _check(lib.som_epoch(_ptr(X), n, _ptr(W), int(side_x), int(side_y), D, float(sigma),
+                         int(radius), _ptr(bmu), _ptr(dist), _stream(stream, X, W, bmu, dist)))
+    return bmu, dist
 
 
 def bmu_search_noalloc(X, W, idx, dist, stream=None):

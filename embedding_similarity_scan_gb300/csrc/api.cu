@@ -2,6 +2,7 @@
 // and staging, device workspace, tensor-map encoding, work planning, and the
 // launches of the kernels in tc_dseq.cu, tc_bmu.cu, ffma.cu and prep.cu.
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -20,7 +21,7 @@ namespace {
 // errors and statistics (per calling thread)
 thread_local std::string g_err;
 struct Stats {
-    int64_t units = 0, tile_n = 0, grid = 0, launches = 0, kernel_ns = 0;
+    int64_t units = 0, tile_n = 0, grid = 0, launches = 0, kernel_ns = 0, update_ns = 0;
 };
 thread_local Stats g_stats;
 
@@ -278,6 +279,7 @@ int read_status(int *status_dev, cudaStream_t st) {
     CUDA_TRY(cudaStreamSynchronize(st));
     if (s == 0) return DSEQ_OK;
     if (s & kStatusNonFinite) return fail(DSEQ_ENONFINITE, "non-finite value or zero-norm row in input");
+    if (s & kStatusBadIndex) return fail(DSEQ_EINVAL, "BMU index out of range [0, M)");
     if (s & (kStatusBarrierTimeout | kStatusPipeTimeout))
         return fail(DSEQ_ETIMEOUT, "device wait timed out (status 0x%x)", s);
     return fail(DSEQ_EINTERNAL, "device consistency check failed (status 0x%x)", s);
@@ -371,6 +373,7 @@ int64_t dseq_last_stat(const char *name) {
     if (n == "grid") return g_stats.grid;
     if (n == "launches") return g_stats.launches;
     if (n == "kernel_ns") return g_stats.kernel_ns;
+    if (n == "update_ns") return g_stats.update_ns;
     return -1;
 }
 
@@ -714,46 +717,39 @@ std::mutex g_bmu_mu;
 BmuWorkspace *g_bmu[64] = {};
 }  // namespace
 
-int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, int32_t *idx,
-               float *dist, void *cuda_stream) {
-    g_err.clear();
-    g_stats = Stats();
-    if (!X || !W || !idx || !dist) return fail(DSEQ_EINVAL, "NULL pointer argument");
+}  // extern "C"
+
+namespace {
+
+int bmu_validate(int64_t n, int64_t M, int32_t D) {
     if (n < 1 || n >= (int64_t(1) << 31)) return fail(DSEQ_EINVAL, "n=%lld out of range", (long long)n);
     if (M < 1 || M >= (int64_t(1) << 31)) return fail(DSEQ_EINVAL, "M=%lld out of range", (long long)M);
     if (D < 1 || D > 16384) return fail(DSEQ_EINVAL, "D=%d out of range", D);
-    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-    int dev = 0;
+    return DSEQ_OK;
+}
+
+int current_device(int &dev) {
     CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return fail(DSEQ_ECUDA, "device ordinal out of range");
-    Options opt;
-    {
-        std::lock_guard<std::mutex> lk(g_opt_mu);
-        opt = g_defaults;
-    }
-    BmuWorkspace *ws;
-    {
-        std::lock_guard<std::mutex> lk(g_bmu_mu);
-        if (!g_bmu[dev]) g_bmu[dev] = new BmuWorkspace();
-        ws = g_bmu[dev];
-    }
-    std::lock_guard<std::mutex> lk(ws->mu);
-    DeviceInfo info;
-    TRY(device_info(dev, info));
-    const float *dX, *dW;
-    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st));
-    TRY(stage_in(W, (size_t)M * D, ws->w_stage, dW, st));
-    const bool idx_dev = is_device_ptr(idx), dist_dev = is_device_ptr(dist);
-    int32_t *d_idx = idx;
-    float *d_dist = dist;
-    if (!idx_dev) {
-        TRY(ws->idx_out.ensure((size_t)n * sizeof(int32_t)));
-        d_idx = ws->idx_out.as<int32_t>();
-    }
-    if (!dist_dev) {
-        TRY(ws->dist_out.ensure((size_t)n * sizeof(float)));
-        d_dist = ws->dist_out.as<float>();
-    }
+    return DSEQ_OK;
+}
+
+Options default_options() {
+    std::lock_guard<std::mutex> lk(g_opt_mu);
+    return g_defaults;
+}
+
+BmuWorkspace *bmu_workspace(int dev) {
+    std::lock_guard<std::mutex> lk(g_bmu_mu);
+    if (!g_bmu[dev]) g_bmu[dev] = new BmuWorkspace();
+    return g_bmu[dev];
+}
+
+// The BMU search on device operands; results into the device arrays d_idx,
+// d_dist.  Leaves the stream running (status already read).
+int bmu_core(const float *dX, int64_t n, const float *dW, int64_t M, int32_t D, int32_t *d_idx,
+             float *d_dist, const Options &opt, const DeviceInfo &info, BmuWorkspace *ws,
+             cudaStream_t st) {
     const int Dp = (int)round_up(D, kKBlock);
     TRY(ws->xn.ensure((size_t)n * sizeof(float)));
     TRY(ws->wn.ensure((size_t)M * sizeof(float)));
@@ -831,8 +827,204 @@ int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, 
     CUDA_TRY(cudaGetLastError());
     TRY(read_status(a.status, st));
     g_stats.kernel_ns = timer.ns();
+    return DSEQ_OK;
+}
+
+// ---- SOM neighbourhood update ------------------------------------------------
+struct SomWorkspace {
+    std::mutex mu;
+    DevBuf S, cnt, T, Tc, status, x_stage, w_stage, bmu_stage, idx, dist;
+};
+std::mutex g_som_mu;
+SomWorkspace *g_som[64] = {};
+
+SomWorkspace *som_workspace(int dev) {
+    std::lock_guard<std::mutex> lk(g_som_mu);
+    if (!g_som[dev]) g_som[dev] = new SomWorkspace();
+    return g_som[dev];
+}
+
+// Checks the map arguments and fills the window weights.
+int som_validate(int64_t n, int32_t side_x, int32_t side_y, int32_t D, double sigma,
+                 int32_t radius, SomArgs &a) {
+    if (n < 0 || n >= (int64_t(1) << 31)) return fail(DSEQ_EINVAL, "n=%lld out of range", (long long)n);
+    if (side_x < 1 || side_y < 1) return fail(DSEQ_EINVAL, "map sides must be >= 1");
+    const int64_t M = (int64_t)side_x * side_y;
+    if (M >= (int64_t(1) << 31)) return fail(DSEQ_EINVAL, "map of %lld neurons too large", (long long)M);
+    if (D < 1 || D > 16384) return fail(DSEQ_EINVAL, "D=%d out of range", D);
+    if (!(sigma >= 0.0) || !std::isfinite(sigma)) return fail(DSEQ_EINVAL, "sigma must be finite and >= 0");
+    if (radius < 0 || radius > kSomMaxRadius)
+        return fail(DSEQ_EINVAL, "radius=%d out of range [0, %d]", radius, kSomMaxRadius);
+    // the corner weight g(R)^2 = exp(-R^2 / sigma^2) must stay a normal fp32
+    if (sigma > 0.0 && (double)radius > 9.0 * sigma)
+        return fail(DSEQ_EINVAL, "radius=%d exceeds 9 * sigma (window weights would underflow fp32)", radius);
+    std::memset(&a, 0, sizeof a);
+    a.n = n;
+    a.M = M;
+    a.D = D;
+    a.side_x = side_x;
+    a.side_y = side_y;
+    a.R = sigma > 0.0 ? radius : 0;
+    for (int k = 0; k <= a.R; ++k)
+        a.g[k] = sigma > 0.0 ? (float)std::exp(-(double)k * k / (2.0 * sigma * sigma)) : 1.0f;
+    return DSEQ_OK;
+}
+
+// The update on device operands (W updated in place).
+int som_core(SomArgs &a, const DeviceInfo &info, SomWorkspace *ws, cudaStream_t st) {
+    const size_t MD = (size_t)a.M * a.D;
+    TRY(ws->S.ensure(MD * sizeof(double)));
+    TRY(ws->cnt.ensure((size_t)a.M * sizeof(unsigned)));
+    TRY(ws->T.ensure(MD * sizeof(float)));
+    TRY(ws->Tc.ensure((size_t)a.M * sizeof(float)));
+    TRY(ws->status.ensure(sizeof(int)));
+    CUDA_TRY(cudaMemsetAsync(ws->status.p, 0, sizeof(int), st));
+    a.S = ws->S.as<double>();
+    a.cnt = ws->cnt.as<unsigned>();
+    a.T = ws->T.as<float>();
+    a.Tc = ws->Tc.as<float>();
+    a.status = ws->status.as<int>();
+    EventTimer timer;
+    TRY(timer.start(st));
+    launch_som_update(a, info.sms, st);
+    CUDA_TRY(cudaGetLastError());
+    TRY(timer.stop(st));
+    TRY(read_status(a.status, st));
+    g_stats.update_ns = timer.ns();
+    return DSEQ_OK;
+}
+
+// W as a device array: the pointer itself, or a staged copy of host data.
+int stage_mutable(float *W, size_t count, DevBuf &buf, float *&dev, bool &on_host, cudaStream_t st) {
+    on_host = !is_device_ptr(W);
+    if (!on_host) {
+        dev = W;
+        return DSEQ_OK;
+    }
+    TRY(buf.ensure(count * sizeof(float)));
+    CUDA_TRY(cudaMemcpyAsync(buf.p, W, count * sizeof(float), cudaMemcpyHostToDevice, st));
+    dev = buf.as<float>();
+    return DSEQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, int32_t *idx,
+               float *dist, void *cuda_stream) {
+    g_err.clear();
+    g_stats = Stats();
+    if (!X || !W || !idx || !dist) return fail(DSEQ_EINVAL, "NULL pointer argument");
+    TRY(bmu_validate(n, M, D));
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    int dev = 0;
+    TRY(current_device(dev));
+    const Options opt = default_options();
+    BmuWorkspace *ws = bmu_workspace(dev);
+    std::lock_guard<std::mutex> lk(ws->mu);
+    DeviceInfo info;
+    TRY(device_info(dev, info));
+    const float *dX, *dW;
+    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st));
+    TRY(stage_in(W, (size_t)M * D, ws->w_stage, dW, st));
+    const bool idx_dev = is_device_ptr(idx), dist_dev = is_device_ptr(dist);
+    int32_t *d_idx = idx;
+    float *d_dist = dist;
+    if (!idx_dev) {
+        TRY(ws->idx_out.ensure((size_t)n * sizeof(int32_t)));
+        d_idx = ws->idx_out.as<int32_t>();
+    }
+    if (!dist_dev) {
+        TRY(ws->dist_out.ensure((size_t)n * sizeof(float)));
+        d_dist = ws->dist_out.as<float>();
+    }
+    TRY(bmu_core(dX, n, dW, M, D, d_idx, d_dist, opt, info, ws, st));
     if (!idx_dev) CUDA_TRY(cudaMemcpyAsync(idx, d_idx, (size_t)n * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
     if (!dist_dev) CUDA_TRY(cudaMemcpyAsync(dist, d_dist, (size_t)n * sizeof(float), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(cudaStreamSynchronize(st));
+    return DSEQ_OK;
+}
+
+int som_update(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_y, int32_t D,
+               const int32_t *bmu, double sigma, int32_t radius, void *cuda_stream) {
+    g_err.clear();
+    g_stats = Stats();
+    SomArgs a;
+    TRY(som_validate(n, side_x, side_y, D, sigma, radius, a));
+    if (!W || (n > 0 && (!X || !bmu))) return fail(DSEQ_EINVAL, "NULL pointer argument");
+    if (n == 0) return DSEQ_OK;  // no sample reaches any neuron: W is unchanged
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    int dev = 0;
+    TRY(current_device(dev));
+    SomWorkspace *ws = som_workspace(dev);
+    std::lock_guard<std::mutex> lk(ws->mu);
+    DeviceInfo info;
+    TRY(device_info(dev, info));
+    const float *dX;
+    const int32_t *dB;
+    float *dW;
+    bool w_host;
+    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st));
+    TRY(stage_in(bmu, (size_t)n, ws->bmu_stage, dB, st));
+    TRY(stage_mutable(W, (size_t)a.M * D, ws->w_stage, dW, w_host, st));
+    a.X = dX;
+    a.bmu = dB;
+    a.W = dW;
+    TRY(som_core(a, info, ws, st));
+    g_stats.units = a.M;
+    g_stats.launches = 4;
+    if (w_host) CUDA_TRY(cudaMemcpyAsync(W, dW, (size_t)a.M * D * sizeof(float), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(cudaStreamSynchronize(st));
+    return DSEQ_OK;
+}
+
+int som_epoch(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_y, int32_t D,
+              double sigma, int32_t radius, int32_t *bmu_out, float *dist_out, void *cuda_stream) {
+    g_err.clear();
+    g_stats = Stats();
+    SomArgs a;
+    TRY(som_validate(n, side_x, side_y, D, sigma, radius, a));
+    if (!X || !W) return fail(DSEQ_EINVAL, "NULL pointer argument");
+    TRY(bmu_validate(n, a.M, D));
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    int dev = 0;
+    TRY(current_device(dev));
+    const Options opt = default_options();
+    BmuWorkspace *bws = bmu_workspace(dev);
+    SomWorkspace *ws = som_workspace(dev);
+    std::lock_guard<std::mutex> lk_bmu(bws->mu);  // always BMU first, then SOM
+    std::lock_guard<std::mutex> lk(ws->mu);
+    DeviceInfo info;
+    TRY(device_info(dev, info));
+    const float *dX;
+    float *dW;
+    bool w_host;
+    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st));
+    TRY(stage_mutable(W, (size_t)a.M * D, ws->w_stage, dW, w_host, st));
+    const bool idx_dev = bmu_out && is_device_ptr(bmu_out);
+    const bool dist_dev = dist_out && is_device_ptr(dist_out);
+    int32_t *d_idx = bmu_out;
+    float *d_dist = dist_out;
+    if (!idx_dev) {
+        TRY(ws->idx.ensure((size_t)n * sizeof(int32_t)));
+        d_idx = ws->idx.as<int32_t>();
+    }
+    if (!dist_dev) {
+        TRY(ws->dist.ensure((size_t)n * sizeof(float)));
+        d_dist = ws->dist.as<float>();
+    }
+    TRY(bmu_core(dX, n, dW, a.M, D, d_idx, d_dist, opt, info, bws, st));
+    a.X = dX;
+    a.bmu = d_idx;
+    a.W = dW;
+    TRY(som_core(a, info, ws, st));
+    g_stats.launches += 4;
+    if (bmu_out && !idx_dev)
+        CUDA_TRY(cudaMemcpyAsync(bmu_out, d_idx, (size_t)n * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    if (dist_out && !dist_dev)
+        CUDA_TRY(cudaMemcpyAsync(dist_out, d_dist, (size_t)n * sizeof(float), cudaMemcpyDeviceToHost, st));
+    if (w_host) CUDA_TRY(cudaMemcpyAsync(W, dW, (size_t)a.M * D * sizeof(float), cudaMemcpyDeviceToHost, st));
     CUDA_TRY(cudaStreamSynchronize(st));
     return DSEQ_OK;
 }

@@ -16,6 +16,7 @@ enum : int {
     kStatusNoWinner = 4,
     kStatusNonFinite = 8,
     kStatusInternal = 16,
+    kStatusBadIndex = 32,
 };
 
 
@@ -160,6 +161,24 @@ cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &
 void launch_bmu_finalize(const BmuArgs &a, cudaStream_t st);
 void launch_row_sqnorm(const float *A, int64_t rows, int D, float *out, int *status,
                        cudaStream_t st);
+
+// ---- SOM neighbourhood update -------------------------------------------------
+// Largest neighbourhood window half-width (grid steps).
+constexpr int kSomMaxRadius = 255;
+struct SomArgs {
+    const float *X;        // n x D samples
+    const int32_t *bmu;    // n
+    float *W;              // M x D codebook, updated in place
+    double *S;             // M x D per-neuron sample sums
+    unsigned *cnt;         // M per-neuron sample counts
+    float *T;              // M x D row-smoothed sums
+    float *Tc;             // M row-smoothed counts
+    int *status;
+    int64_t n, M;
+    int D, side_x, side_y, R;
+    float g[kSomMaxRadius + 1];  // g[k] = exp(-k^2 / (2 sigma^2)), k = 0..R
+};
+void launch_som_update(const SomArgs &a, int sms, cudaStream_t st);
 
 // ---- host helpers of api.cu used by noalloc.cu --------------------------------
 namespace host {

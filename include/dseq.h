@@ -140,6 +140,40 @@ void dseq_destroy(dseq_ctx *ctx);
 int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, int32_t *idx,
                float *dist, void *cuda_stream);
 
+/* Neighbourhood update of a self-organising map from every sample's BMU,
+ * the step that follows the BMU search in an epoch ("From 80x to 385x: A
+ * Best-Matching-Unit Search at the L2 Roof", section 3 Background: each
+ * sample's closest neuron is found, then that neuron and its neighbours are
+ * updated).  The batch map:
+ *   W_j <- sum_i h(j, bmu_i) X_i / sum_i h(j, bmu_i)   (W_j kept if the sum is 0)
+ * on a planar side_x x side_y grid, neuron j at column j % side_x and row
+ * j / side_x, with h = exp(-(dx^2 + dy^2) / (2 sigma^2)) for |dx|, |dy| <=
+ * radius and 0 outside that square window (sigma = 0: a neuron takes the
+ * mean of its own samples).
+ *   X       float[n*D] samples, row-major; host or device.
+ *   W       float[M*D], M = side_x * side_y, updated in place; host or device.
+ *   bmu     int32[n], every sample's neuron in [0, M); host or device.
+ *   sigma   >= 0; radius in [0, 255] and, for sigma > 0, radius <= 9 sigma
+ *           (wider windows would take weights below fp32's normal range).
+ * Sums over samples are taken in double, the smoothing and the division in
+ * fp32.  n = 0 leaves W unchanged.  On any error W is left unchanged.
+ * Errors: DSEQ_EINVAL (sizes, sigma, radius, a BMU out of range),
+ * DSEQ_ENONFINITE (NaN/Inf in X), DSEQ_ENOMEM, DSEQ_ECUDA. */
+int som_update(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_y, int32_t D,
+               const int32_t *bmu, double sigma, int32_t radius, void *cuda_stream);
+
+/* One SOM epoch: bmu_search of every sample against W, then som_update of W
+ * with those BMUs, on the stream.  bmu_out (int32[n]) and dist_out
+ * (float[n]) receive the search's results and may each be NULL; host or
+ * device.  The search follows the process-wide options as bmu_search does.
+ * dseq_last_stat("kernel_ns") is the search kernel's time and
+ * dseq_last_stat("update_ns") the update's.
+ * Sizes: n >= 1, otherwise as som_update.  Errors: those of bmu_search and
+ * som_update; on an error W is left unchanged. */
+int som_epoch(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_y, int32_t D,
+              double sigma, int32_t radius, int32_t *bmu_out, float *dist_out,
+              void *cuda_stream);
+
 /* bmu_search for callers that cannot allocate device memory: a framework
  * whose pooling allocator already holds nearly all of the GPU's memory, or a
  * latency-critical loop that cannot absorb the device-wide synchronisation
@@ -211,12 +245,15 @@ int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value);
 /* Read back a knob (the value in effect; -1 for an unknown name). */
 int64_t dseq_get_option(dseq_ctx *ctx, const char *name);
 
-/* Statistics of the last successful dseq_run / bmu_search on this thread:
- *   "units"        work units (sequence block x candidate chunk) per iteration,
+/* Statistics of the last successful dseq_run / bmu_search / som_update /
+ * som_epoch on this thread:
+ *   "units"        work units (sequence block x candidate chunk) per iteration;
+ *                  neurons for som_update,
  *   "tile_n"       candidate columns per unit,
  *   "grid"         CTAs launched,
  *   "launches"     kernels launched by the call,
- *   "kernel_ns"    device time of the main kernel (CUDA events; 0 if unknown). */
+ *   "kernel_ns"    device time of the main kernel (CUDA events; 0 if unknown),
+ *   "update_ns"    device time of the SOM update's kernels (0 if none ran). */
 int64_t dseq_last_stat(const char *name);
 
 /* Message of the last error on the calling thread ("" if none). */

@@ -138,3 +138,11 @@ BMU = {
     "som256": BMUConfig("SOM 256x256 M=65536 n=131072 D=256", 131072, 65536, 256, 4096),
     "som512": BMUConfig("SOM 512x512 M=262144 n=262144 D=256", 262144, 262144, 256, 1024),
 }
+
+
+# SOM epoch (BMU search, then the batch-map neighbourhood update) on the BMU
+# configurations' maps.  The pages give no neighbourhood width; these take a
+# mid-training Gaussian of sigma = 3 grid steps cut at radius 3 sigma.
+SOM_SIDES = {"som256": (256, 256), "som512": (512, 512)}
+SOM_SIGMA = 3.0
+SOM_RADIUS = 9
