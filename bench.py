@@ -4,7 +4,8 @@ One step = one full pass of the hot path over one batch of synthetic input:
 for the diversity workload, one ``dseq_run`` of B sequences x L iterations
 (every iteration: contraction, min-fold, masked argmax, commit) on a table
 already resident in HBM; for the BMU workload, one ``bmu_search`` of n
-samples against M neurons.
+samples against M neurons; for the SOM epoch workload, one ``som_epoch``
+(the BMU search, then the neighbourhood update of the map in place).
 
 Prints ONE JSON line (rank 0).  ``value`` is whole-job throughput
 (sequence-iterations/s, or samples/s) from CUDA events on the launching
@@ -157,7 +158,7 @@ def run_reference(args):
             sel = starts[(np.arange(nseq) + i * nseq) % cfg.B]
             oracle.dseq(E, sel, cfg.L, threads=threads)
             return nseq * cfg.L
-    else:
+    elif args.workload in workloads.BMU:
         cfg = workloads.BMU[args.workload]
         X = cfg.samples(seed=0)
         W = cfg.codebook(seed=0)
@@ -170,6 +171,32 @@ def run_reference(args):
             lo = (i * nsamp) % cfg.n
             oracle.bmu(X[lo:lo + nsamp], W, threads=threads)
             return nsamp
+    else:
+        name = workloads.SOM_EPOCH[args.workload]
+        cfg = workloads.BMU[name]
+        sx, sy = workloads.SOM_SIDES[name]
+        X = cfg.samples(seed=0)
+        W = cfg.codebook(seed=0)
+        bmu = np.random.default_rng(0).integers(0, cfg.M, cfg.n).astype(np.int32)
+        nsamp = args.ref_sample or 4 * threads
+        nneur = 4 * threads
+        sample = (f"per step: BMU of {nsamp} of {cfg.n} samples and the update of {nneur} of "
+                  f"{cfg.M} neurons, scaled to one epoch")
+        unit = "samples/s"
+        metric = "SOM epoch samples/s"
+
+        def step(i):
+            lo = (i * nsamp) % cfg.n
+            t0 = time.perf_counter()
+            oracle.bmu(X[lo:lo + nsamp], W, threads=threads)
+            t1 = time.perf_counter()
+            neur = (np.arange(nneur) * 7919 + i) % cfg.M
+            oracle.som_update(X, bmu, W, sx, sy, workloads.SOM_SIGMA, workloads.SOM_RADIUS,
+                              neurons=neur, threads=threads)
+            t2 = time.perf_counter()
+            epoch_s = (t1 - t0) / nsamp * cfg.n + (t2 - t1) / nneur * cfg.M
+            # samples processed at the epoch rate during this step's wall time
+            return cfg.n * (t2 - t0) / epoch_s
 
     for i in range(args.warmup):
         step(i)
@@ -197,7 +224,7 @@ def run_reference(args):
 # our arm
 
 
-def _cpu_baseline(args, cfg):
+def _cpu_baseline(args, cfg, epoch_of=None):
     """The oracle as it stands, on all host cores, on a bounded sample."""
     import oracle
 
@@ -227,6 +254,32 @@ def _cpu_baseline(args, cfg):
                           f"({total_t:.1f} s of CPU work)"}
     X = cfg.samples(seed=0)
     W = cfg.codebook(seed=0)
+    if epoch_of is not None:
+        # one epoch = the BMU of every sample + the update of every neuron; time
+        # a bounded sample of each and scale both to the whole epoch
+        sx, sy = workloads.SOM_SIDES[epoch_of]
+        bmu = np.random.default_rng(0).integers(0, cfg.M, cfg.n).astype(np.int32)
+        nb, tb, n = 0, 0.0, 2 * threads
+        while tb < t_target / 2 and nb + n <= cfg.n:
+            t0 = time.perf_counter()
+            oracle.bmu(X[nb:nb + n], W, threads=threads)
+            tb += time.perf_counter() - t0
+            nb += n
+            n *= 2
+        nu, tu, k = 0, 0.0, 2 * threads
+        while tu < t_target / 2 and nu + k <= cfg.M:
+            t0 = time.perf_counter()
+            oracle.som_update(X, bmu, W, sx, sy, workloads.SOM_SIGMA, workloads.SOM_RADIUS,
+                              neurons=np.arange(nu, nu + k), threads=threads)
+            tu += time.perf_counter() - t0
+            nu += k
+            k *= 2
+        epoch_s = tb / nb * cfg.n + tu / nu * cfg.M
+        return {"value": cfg.n / epoch_s, "unit": "samples/s", "cores": threads,
+                "kind": "oracle",
+                "sample": (f"BMU of {nb} of {cfg.n} samples ({tb:.1f} s) and update of {nu} of "
+                           f"{cfg.M} neurons ({tu:.1f} s), scaled to one epoch "
+                           f"({epoch_s:.0f} s)")}
     n, done, total_t = 2 * threads, 0, 0.0
     while total_t < t_target and done + n <= cfg.n:
         t0 = time.perf_counter()
@@ -265,6 +318,7 @@ def run_ours(args):
     split_peak = bf16_peak / 3.0
 
     is_div = args.workload in workloads.DIVERSITY
+    epoch_of = None
     if is_div:
         cfg = workloads.DIVERSITY[args.workload]
         E_host = torch.from_numpy(cfg.table(seed=0)).pin_memory()
@@ -295,6 +349,42 @@ def run_ours(args):
                   "l2": "flushed between steps (512 MB write)"}
         if args.opt:
             config["options"] = list(args.opt)
+    elif args.workload in workloads.SOM_EPOCH:
+        epoch_of = workloads.SOM_EPOCH[args.workload]
+        cfg = workloads.BMU[epoch_of]
+        sx, sy = workloads.SOM_SIDES[epoch_of]
+        sigma, radius = workloads.SOM_SIGMA, workloads.SOM_RADIUS
+        X_host = torch.from_numpy(cfg.samples(seed=0)).pin_memory()
+        W_host = torch.from_numpy(cfg.codebook(seed=0)).pin_memory()
+        X_dev, W_dev = X_host.to(dev), W_host.to(dev)
+        idx_dev = torch.empty(cfg.n, dtype=torch.int32, device=dev)
+        dist_dev = torch.empty(cfg.n, dtype=torch.float32, device=dev)
+        units = cfg.n
+        flop = 2.0 * cfg.n * cfg.M * cfg.D
+        stream_bytes = None
+        # the update's algorithmic bytes: read the samples and their BMUs,
+        # read and write the codebook
+        update_bytes = 4.0 * cfg.n * cfg.D + 4.0 * cfg.n + 8.0 * cfg.M * cfg.D
+        kernel_name = "tc_bmu_kernel"
+        metric, unit = "SOM epoch samples/s", "samples/s"
+        update_ns = []
+
+        def step():
+            # each step is the next epoch of training on the same map
+            es.som_epoch(X_dev, W_dev, sx, sy, sigma, radius, bmu=idx_dev, dist=dist_dev)
+            update_ns.append(es.dseq_last_stat("update_ns"))
+            return es.dseq_last_stat("kernel_ns"), es.dseq_last_stat("launches")
+
+        def e2e_step():
+            W_h = W_host.clone().pin_memory()
+            idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
+            dist_h = torch.empty(cfg.n, dtype=torch.float32).pin_memory()
+            es.som_epoch(X_host, W_h, sx, sy, sigma, radius, bmu=idx_h, dist=dist_h)
+            return (X_host.numel() + W_h.numel()) * 4, W_h.numel() * 4 + cfg.n * 8
+
+        config = {"workload": args.workload, "n": cfg.n, "M": cfg.M, "D": cfg.D,
+                  "map": f"{sx}x{sy}", "sigma": sigma, "radius": radius,
+                  "l2": "flushed between steps (512 MB write)"}
     else:
         cfg = workloads.BMU[args.workload]
         X_host = torch.from_numpy(cfg.samples(seed=0)).pin_memory()
@@ -381,7 +471,7 @@ def run_ours(args):
                      f"fp32 multiply-add)")
     roof = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
             "frac": (achieved / tensor_peak) if achieved else None,
-            "traffic": _profiled_traffic(kernel_name, args.workload),
+            "traffic": _profiled_traffic(kernel_name, epoch_of or args.workload),
             "kernel": kernel_name,
             "note": (f"achieved = algorithmic FLOP (2*{'N*D*B*L' if is_div else 'n*M*D'})"
                      f" / kernel time (CUDA events on the launching stream); {peak_note}")}
@@ -412,8 +502,16 @@ def run_ours(args):
             "achieved_gbs": stream_bytes / k_avg_s / 1e9, "peak_gbs": hbm_peak,
             "frac": stream_bytes / k_avg_s / 1e9 / hbm_peak,
             "note": "running-minimum read+write bytes (8*B*N per iteration) / kernel time"}
+    if epoch_of is not None and update_ns and min(update_ns) > 0:
+        u_s = statistics.mean(update_ns) / 1e9
+        line["som_update"] = {
+            "achieved_gbs": update_bytes / u_s / 1e9, "peak_gbs": hbm_peak,
+            "frac": update_bytes / u_s / 1e9 / hbm_peak, "ms": u_s * 1e3,
+            "share_of_step": u_s * 1e3 / (total_ms / args.steps),
+            "note": ("neighbourhood update kernels: algorithmic bytes (samples + BMUs read, "
+                     "codebook read + write) / their CUDA-event time")}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = _cpu_baseline(args, cfg)
+        line["cpu_baseline"] = _cpu_baseline(args, cfg, epoch_of)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if is_div:
@@ -431,7 +529,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="page1",
-                    choices=sorted(workloads.DIVERSITY) + sorted(workloads.BMU))
+                    choices=sorted(workloads.DIVERSITY) + sorted(workloads.BMU)
+                    + sorted(workloads.SOM_EPOCH))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-sample", type=int, default=0)

@@ -858,6 +858,12 @@ int som_validate(int64_t n, int32_t side_x, int32_t side_y, int32_t D, double si
     // the corner weight g(R)^2 = exp(-R^2 / sigma^2) must stay a normal fp32
     if (sigma > 0.0 && (double)radius > 9.0 * sigma)
         return fail(DSEQ_EINVAL, "radius=%d exceeds 9 * sigma (window weights would underflow fp32)", radius);
+    // one CTA per (32 dimensions, 128 neurons of a row) and per (32 dimensions,
+    // 64 neurons of a column): both grids must fit one launch
+    const int64_t nch = (D + 31) / 32;
+    if ((nch + 1) * ((side_x + 127) / 128) * side_y >= (int64_t(1) << 31) ||
+        nch * side_x * ((side_y + 63) / 64) >= (int64_t(1) << 31))
+        return fail(DSEQ_EINVAL, "map of %d x %d neurons with D=%d too large for one update", side_x, side_y, D);
     std::memset(&a, 0, sizeof a);
     a.n = n;
     a.M = M;
@@ -873,21 +879,21 @@ int som_validate(int64_t n, int32_t side_x, int32_t side_y, int32_t D, double si
 // The update on device operands (W updated in place).
 int som_core(SomArgs &a, const DeviceInfo &info, SomWorkspace *ws, cudaStream_t st) {
     const size_t MD = (size_t)a.M * a.D;
-    TRY(ws->S.ensure(MD * sizeof(double)));
+    TRY(ws->S.ensure(MD * sizeof(long long)));
     TRY(ws->cnt.ensure((size_t)a.M * sizeof(unsigned)));
     TRY(ws->T.ensure(MD * sizeof(float)));
     TRY(ws->Tc.ensure((size_t)a.M * sizeof(float)));
-    TRY(ws->status.ensure(sizeof(int)));
-    CUDA_TRY(cudaMemsetAsync(ws->status.p, 0, sizeof(int), st));
-    a.S = ws->S.as<double>();
+    TRY(ws->status.ensure(2 * sizeof(int)));  // status word, then max |x| bits
+    CUDA_TRY(cudaMemsetAsync(ws->status.p, 0, 2 * sizeof(int), st));
+    a.S = ws->S.as<long long>();
     a.cnt = ws->cnt.as<unsigned>();
     a.T = ws->T.as<float>();
     a.Tc = ws->Tc.as<float>();
     a.status = ws->status.as<int>();
+    a.maxbits = reinterpret_cast<unsigned *>(ws->status.as<int>() + 1);
     EventTimer timer;
     TRY(timer.start(st));
-    launch_som_update(a, info.sms, st);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launch_som_update(a, info.sms, st));
     TRY(timer.stop(st));
     TRY(read_status(a.status, st));
     g_stats.update_ns = timer.ns();

@@ -169,16 +169,17 @@ struct SomArgs {
     const float *X;        // n x D samples
     const int32_t *bmu;    // n
     float *W;              // M x D codebook, updated in place
-    double *S;             // M x D per-neuron sample sums
+    long long *S;          // M x D per-neuron sample sums, fixed point
     unsigned *cnt;         // M per-neuron sample counts
     float *T;              // M x D row-smoothed sums
     float *Tc;             // M row-smoothed counts
     int *status;
+    unsigned *maxbits;     // bits of max |x| (cleared by the host)
     int64_t n, M;
     int D, side_x, side_y, R;
     float g[kSomMaxRadius + 1];  // g[k] = exp(-k^2 / (2 sigma^2)), k = 0..R
 };
-void launch_som_update(const SomArgs &a, int sms, cudaStream_t st);
+cudaError_t launch_som_update(const SomArgs &a, int sms, cudaStream_t st);
 
 // ---- host helpers of api.cu used by noalloc.cu --------------------------------
 namespace host {

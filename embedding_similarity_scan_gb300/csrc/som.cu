@@ -13,18 +13,26 @@
 //
 // Grouping the samples by BMU turns the sum into a smoothing of the
 // per-neuron sums S_k = sum_{bmu_i = k} x_i and counts n_k, and the product
-// form of h makes that smoothing separable.  Three passes over the map:
-//   accumulate  S (f64 atomics) and n (u32 atomics), one warp per sample,
-//               into buffers the zero kernel cleared;
-//   rows        T = sum_dx g(|dx|) S[k + dx] along each map row, and the
-//               same for the counts (fp32 out);
-//   columns     num = sum_dy g(|dy|) T[k + dy * side_x], den likewise from
-//               the row-smoothed counts; W_j = num / den where den > 0.
-// Every map-sized array is laid out neuron-major (j * D + d), so a warp's
-// 32 consecutive threads touch 32 consecutive dimensions of one neuron and
-// every tap of the stencils is a coalesced 128-byte (fp32) or 256-byte
-// (f64) row segment; the 2R re-reads of each segment hit L1 (rows) or L2
-// (columns, one map row apart).
+// form of h makes that smoothing separable.  Four kernels:
+//   prepare     max |x| over all samples (its exponent fixes the fixed-point
+//               scale below) while clearing S and n;
+//   accumulate  S and n with 64-bit integer atomics, one warp per sample.
+//               Each x becomes the integer trunc(x 2^F), F chosen so that no
+//               sum of n samples can overflow, so the sums are exact and
+//               independent of the order the atomics land in: the update is
+//               bitwise reproducible.  The truncation costs at most
+//               2^-F <= max|x| n 2^-61 per sample;
+//   rows        T = sum_dx g(|dx|) S[k + dx] along each map row, and the same
+//               for the counts, from a shared-memory tile with an R-wide halo
+//               (fp32 out);
+//   columns     num = sum_dy g(|dy|) T[k + dy side_x], den likewise from the
+//               row-smoothed counts, again from a tile; W_j = num / den where
+//               den > 0, in place.
+// No step uses 64-bit floating point: GB300's FP64 rate is a small fraction
+// of its fp32 rate, and a conversion from or to double runs at that rate.
+// Every map-sized array is neuron-major (j * D + d); a warp covers 32
+// consecutive dimensions of one neuron, so each load is a full 128-byte
+// (fp32) or 256-byte (int64) segment.
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,20 +41,82 @@ namespace dseq {
 namespace {
 
 constexpr int kSomThreads = 256;
+constexpr int kRowTile = 128;  // neurons along a map row per CTA (rows pass)
+constexpr int kColTile = 64;   // neurons along a map column per CTA (columns pass)
 
-__global__ void som_zero_kernel(double *__restrict__ S, int64_t nS, unsigned *__restrict__ cnt,
-                                int64_t M) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nS + M; e += stride) {
-        if (e < nS)
-            S[e] = 0.0;
-        else
-            cnt[e - nS] = 0u;
-    }
+// Exponent bound E of the largest |x| (|x| < 2^(E+1)) and the fixed-point
+// scale F = 61 - E - ceil(log2 n): every |x| 2^F < 2^(62 - ceil(log2 n)), so
+// a sum of n of them stays below 2^62.
+__device__ __forceinline__ int fixed_scale(unsigned maxbits, int64_t n) {
+    const int ef = (int)(maxbits >> 23);
+    const int E = ef == 0 ? -126 : ef - 127;
+    const int L = n <= 1 ? 0 : 64 - __clzll((unsigned long long)(n - 1));
+    return 61 - E - L;
 }
 
-// one warp per sample: S[bmu_i] += x_i, n[bmu_i] += 1
+// trunc(x 2^F) from the bits of x (integer operations only; exact)
+__device__ __forceinline__ long long to_fixed(float x, int F) {
+    const uint32_t b = __float_as_uint(x);
+    int ef = (int)((b >> 23) & 0xffu);
+    uint32_t m = b & 0x7fffffu;
+    if (ef == 0) {
+        if (m == 0) return 0;
+        ef = 1;  // subnormal: no implicit bit
+    } else {
+        m |= 0x800000u;
+    }
+    const int s = ef - 150 + F;  // x = m 2^(ef - 150)
+    unsigned long long u;
+    if (s >= 0)
+        u = (unsigned long long)m << s;
+    else if (s > -32)
+        u = (unsigned long long)(m >> (-s));
+    else
+        u = 0;
+    return (b >> 31) ? -(long long)u : (long long)u;
+}
+
+// 2^-F as two normal fp32 factors (F ranges over about [-97, 187])
+__device__ __forceinline__ void fixed_unscale(int F, float &s1, float &s2) {
+    const int f1 = F / 2, f2 = F - f1;
+    s1 = __int_as_float((127 - f1) << 23);
+    s2 = __int_as_float((127 - f2) << 23);
+}
+
+// v 2^-F in fp32 (two 32-bit conversions; relative error below 2^-22)
+__device__ __forceinline__ float from_fixed(long long v, float s1, float s2) {
+    const unsigned long long u = v < 0 ? 0ull - (unsigned long long)v : (unsigned long long)v;
+    float f = fmaf(__uint2float_rn((unsigned)(u >> 32)), 4294967296.0f,
+                   __uint2float_rn((unsigned)(u & 0xffffffffu)));
+    f = (f * s1) * s2;
+    return v < 0 ? -f : f;
+}
+
+__global__ void som_prepare_kernel(SomArgs a) {
+    const int64_t nX = a.n * (int64_t)a.D, nS = a.M * (int64_t)a.D;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    unsigned mx = 0;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nX; e += stride)
+        mx = max(mx, __float_as_uint(__ldg(a.X + e)) & 0x7fffffffu);
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nS + a.M; e += stride) {
+        if (e < nS)
+            a.S[e] = 0;
+        else
+            a.cnt[e - nS] = 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0 && mx) atomicMax(a.maxbits, mx);
+}
+
+// one warp per sample: S[bmu_i] += fixed(x_i), n[bmu_i] += 1
 __global__ void som_accumulate_kernel(SomArgs a) {
+    const unsigned maxbits = *a.maxbits;
+    if (maxbits >= 0x7f800000u) {  // an infinity or NaN among the samples
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusNonFinite);
+        return;
+    }
+    const int F = fixed_scale(maxbits, a.n);
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < a.n;
@@ -57,68 +127,105 @@ __global__ void som_accumulate_kernel(SomArgs a) {
             continue;
         }
         const float *x = a.X + i * (int64_t)a.D;
-        double *s = a.S + (int64_t)c * a.D;
-        bool bad = false;
-        for (int d = lane; d < a.D; d += 32) {
-            const float v = __ldg(x + d);
-            bad |= !isfinite(v);
-            atomicAdd(s + d, (double)v);
-        }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, kStatusNonFinite);
+        unsigned long long *s = reinterpret_cast<unsigned long long *>(a.S + (int64_t)c * a.D);
+        for (int d = lane; d < a.D; d += 32)
+            atomicAdd(s + d, (unsigned long long)to_fixed(__ldg(x + d), F));
         if (lane == 0) atomicAdd(a.cnt + c, 1u);
     }
 }
 
-// rows: T[j, d] = sum_dx g(|dx|) S[j + dx, d]; the counts ride along as
-// M extra elements past the M x D data elements
-__global__ void som_rows_kernel(SomArgs a) {
-    __shared__ float g[kSomMaxRadius + 1];
-    for (int k = threadIdx.x; k <= a.R; k += blockDim.x) g[k] = a.g[k];
+// Rows pass.  CTA = (dimension chunk of 32, tile of kRowTile neurons of one
+// map row); chunk index nch (one past the data chunks) smooths the counts.
+// The tile holds the neurons [x0 - R, x0 + kRowTile + R) of the row, zero
+// outside the map (a zero term leaves a sum unchanged, so this equals
+// clipping the window at the map's edge).
+__global__ void __launch_bounds__(kSomThreads) som_rows_kernel(SomArgs a) {
+    extern __shared__ float tile[];  // (kRowTile + 2R) x 32, then g[R + 1]
+    const int R = a.R, span = kRowTile + 2 * R;
+    float *g = tile + span * 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nch = (a.D + 31) / 32;
+    const int ntx = (a.side_x + kRowTile - 1) / kRowTile;
+    const int64_t b = blockIdx.x;
+    const int chunk = (int)(b % (nch + 1));
+    const int64_t rest = b / (nch + 1);
+    const int x0 = (int)(rest % ntx) * kRowTile;
+    const int64_t y = rest / ntx;
+    for (int k = threadIdx.x; k <= R; k += blockDim.x) g[k] = a.g[k];
+    const bool counts = chunk == nch;
+    const int d = chunk * 32 + lane;
+    float s1, s2;
+    fixed_unscale(fixed_scale(*a.maxbits, a.n), s1, s2);
+    const int64_t row0 = y * a.side_x;
+    for (int xi = warp; xi < span; xi += kSomThreads / 32) {
+        const int xg = x0 - R + xi;
+        float v = 0.0f;
+        if (xg >= 0 && xg < a.side_x) {
+            const int64_t j = row0 + xg;
+            if (counts)
+                v = lane == 0 ? (float)a.cnt[j] : 0.0f;
+            else if (d < a.D)
+                v = from_fixed(a.S[j * a.D + d], s1, s2);
+        }
+        tile[xi * 32 + lane] = v;
+    }
     __syncthreads();
-    const int64_t nT = a.M * (int64_t)a.D;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nT + a.M; e += stride) {
-        const bool data = e < nT;
-        const int64_t j = data ? e / a.D : e - nT;
-        const int64_t col = j % a.side_x;
-        const int lo = (int)max((int64_t)-a.R, -col);
-        const int hi = (int)min((int64_t)a.R, (int64_t)a.side_x - 1 - col);
+    for (int xi = warp; xi < kRowTile; xi += kSomThreads / 32) {
+        const int x = x0 + xi;
+        if (x >= a.side_x) break;
         float acc = 0.0f;
-        if (data) {
-            const double *src = a.S + e;
-            for (int dx = lo; dx <= hi; ++dx)
-                acc = fmaf(g[dx < 0 ? -dx : dx], (float)src[(int64_t)dx * a.D], acc);
-            a.T[e] = acc;
-        } else {
-            for (int dx = lo; dx <= hi; ++dx)
-                acc = fmaf(g[dx < 0 ? -dx : dx], (float)a.cnt[j + dx], acc);
-            a.Tc[j] = acc;
+        const float *t = tile + xi * 32 + lane;
+        for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k < R ? R - k : k - R], t[k * 32], acc);
+        const int64_t j = row0 + x;
+        if (counts) {
+            if (lane == 0) a.Tc[j] = acc;
+        } else if (d < a.D) {
+            a.T[j * a.D + d] = acc;
         }
     }
 }
 
-// columns and the division, in place on W; nothing is written when an
-// earlier pass flagged an error, so W is left as it was
-__global__ void som_cols_kernel(SomArgs a) {
-    __shared__ float g[kSomMaxRadius + 1];
-    for (int k = threadIdx.x; k <= a.R; k += blockDim.x) g[k] = a.g[k];
-    __syncthreads();
+// Columns pass and the division, in place on W.  CTA = (dimension chunk of
+// 32, one map column, kColTile neurons down it).  Nothing is written when an
+// earlier kernel flagged an error, so W is then left as it was.
+__global__ void __launch_bounds__(kSomThreads) som_cols_kernel(SomArgs a) {
+    extern __shared__ float tile[];  // (kColTile + 2R) x 32, then counts, then g
+    const int R = a.R, span = kColTile + 2 * R;
+    float *tc = tile + span * 32;
+    float *g = tc + span;
     if (*(volatile int *)a.status != 0) return;
-    const int64_t nT = a.M * (int64_t)a.D;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t row_elems = (int64_t)a.side_x * a.D;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nT; e += stride) {
-        const int64_t j = e / a.D;
-        const int64_t row = j / a.side_x;
-        const int lo = (int)max((int64_t)-a.R, -row);
-        const int hi = (int)min((int64_t)a.R, (int64_t)a.side_y - 1 - row);
-        float num = 0.0f, den = 0.0f;
-        for (int dy = lo; dy <= hi; ++dy) {
-            const float w = g[dy < 0 ? -dy : dy];
-            num = fmaf(w, a.T[e + (int64_t)dy * row_elems], num);
-            den = fmaf(w, a.Tc[j + (int64_t)dy * a.side_x], den);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nch = (a.D + 31) / 32;
+    const int64_t b = blockIdx.x;
+    const int chunk = (int)(b % nch);
+    const int64_t rest = b / nch;
+    const int x = (int)(rest % a.side_x);
+    const int y0 = (int)(rest / a.side_x) * kColTile;
+    for (int k = threadIdx.x; k <= R; k += blockDim.x) g[k] = a.g[k];
+    const int d = chunk * 32 + lane;
+    for (int yi = warp; yi < span; yi += kSomThreads / 32) {
+        const int yg = y0 - R + yi;
+        float v = 0.0f, c = 0.0f;
+        if (yg >= 0 && yg < a.side_y) {
+            const int64_t j = (int64_t)yg * a.side_x + x;
+            if (d < a.D) v = a.T[j * a.D + d];
+            c = a.Tc[j];
         }
-        if (den > 0.0f) a.W[e] = num / den;
+        tile[yi * 32 + lane] = v;
+        if (lane == 0) tc[yi] = c;
+    }
+    __syncthreads();
+    for (int yi = warp; yi < kColTile; yi += kSomThreads / 32) {
+        const int yy = y0 + yi;
+        if (yy >= a.side_y) break;
+        float num = 0.0f, den = 0.0f;
+        const float *t = tile + yi * 32 + lane;
+        for (int k = 0; k <= 2 * R; ++k) {
+            const float w = g[k < R ? R - k : k - R];
+            num = fmaf(w, t[k * 32], num);
+            den = fmaf(w, tc[yi + k], den);
+        }
+        if (den > 0.0f && d < a.D) a.W[((int64_t)yy * a.side_x + x) * a.D + d] = num / den;
     }
 }
 
@@ -127,16 +234,36 @@ int grid_for(int64_t work, int per_block, int sms) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)sms * 16));
 }
 
+size_t rows_smem(int R) { return ((size_t)(kRowTile + 2 * R) * 32 + R + 1) * sizeof(float); }
+size_t cols_smem(int R) { return ((size_t)(kColTile + 2 * R) * 33 + R + 1) * sizeof(float); }
+
 }  // namespace
 
-void launch_som_update(const SomArgs &a, int sms, cudaStream_t st) {
-    const int64_t nT = a.M * (int64_t)a.D;
-    som_zero_kernel<<<grid_for(nT + a.M, kSomThreads, sms), kSomThreads, 0, st>>>(a.S, nT, a.cnt,
-                                                                                  a.M);
-    if (a.n > 0)
-        som_accumulate_kernel<<<grid_for(a.n, kSomThreads / 32, sms), kSomThreads, 0, st>>>(a);
-    som_rows_kernel<<<grid_for(nT + a.M, kSomThreads, sms), kSomThreads, 0, st>>>(a);
-    som_cols_kernel<<<grid_for(nT, kSomThreads, sms), kSomThreads, 0, st>>>(a);
+cudaError_t launch_som_update(const SomArgs &a, int sms, cudaStream_t st) {
+    static bool attrs_set[64] = {};  // the attribute is per function and device
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return de;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attrs_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(som_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)rows_smem(kSomMaxRadius));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(som_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)cols_smem(kSomMaxRadius));
+        if (e != cudaSuccess) return e;
+        attrs_set[dev] = true;
+    }
+    const int64_t nS = a.M * (int64_t)a.D;
+    const int nch = (a.D + 31) / 32;
+    som_prepare_kernel<<<grid_for(std::max<int64_t>(a.n * (int64_t)a.D, nS + a.M), kSomThreads, sms),
+                         kSomThreads, 0, st>>>(a);
+    som_accumulate_kernel<<<grid_for(a.n, kSomThreads / 32, sms), kSomThreads, 0, st>>>(a);
+    const int64_t ntx = (a.side_x + kRowTile - 1) / kRowTile;
+    som_rows_kernel<<<(unsigned)((nch + 1) * ntx * a.side_y), kSomThreads, rows_smem(a.R), st>>>(a);
+    const int64_t nty = (a.side_y + kColTile - 1) / kColTile;
+    som_cols_kernel<<<(unsigned)(nch * a.side_x * nty), kSomThreads, cols_smem(a.R), st>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace dseq

@@ -88,6 +88,32 @@ def test_update_parity(es, case, hot):
     _check_update(X, bmu, W, Wd.cpu().numpy(), sx, sy, sigma, R)
 
 
+def test_update_bitwise_reproducible(es):
+    # the per-neuron sums are exact integers, so the order in which the
+    # atomics land cannot change a bit of the result
+    X, W, bmu = _data(6000, 32, 32, 96, seed=21, hot=True)
+    Xd, Bd = torch.from_numpy(X).cuda(), torch.from_numpy(bmu).cuda()
+    outs = []
+    for _ in range(3):
+        Wd = torch.from_numpy(W.copy()).cuda()
+        es.som_update(Xd, Bd, Wd, 32, 32, 2.5, 7)
+        outs.append(Wd.cpu().numpy())
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e-6, 1e6, 1e30])
+def test_update_value_scale(es, scale):
+    # the fixed-point scale follows max |x|: parity holds at any magnitude
+    X, W, bmu = _data(2000, 16, 12, 40, seed=22)
+    X = (X * np.float32(scale)).astype(np.float32)
+    W = (W * np.float32(scale)).astype(np.float32)
+    Wd = torch.from_numpy(W.copy()).cuda()
+    es.som_update(torch.from_numpy(X).cuda(), torch.from_numpy(bmu).cuda(), Wd, 16, 12, 1.3, 3)
+    want = oracle.som_update(X, bmu, W, 16, 12, 1.3, 3)
+    err = np.abs(Wd.cpu().numpy().astype(np.float64) - want).max()
+    assert err <= TOL * float(np.abs(X).max()), f"error {err} at scale {scale}"
+
+
 def test_update_host_buffers(es):
     X, W, bmu = _data(2000, 20, 16, 48, seed=4)
     Wh = W.copy()

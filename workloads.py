@@ -146,3 +146,4 @@ BMU = {
 SOM_SIDES = {"som256": (256, 256), "som512": (512, 512)}
 SOM_SIGMA = 3.0
 SOM_RADIUS = 9
+SOM_EPOCH = {"som256_epoch": "som256", "som512_epoch": "som512"}
