@@ -17,11 +17,13 @@ namespace dseq {
 
 namespace {
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+
+
 __device__ __forceinline__ float warp_max_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -31,6 +33,41 @@ __device__ __forceinline__ int warp_or_i(int v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Compensated (Kahan) fp32 sum: error about 2 ulp of the total whatever the
+// number of terms.  All norms here are sums of squares of values scaled
+// into [0, 1) by a power of two, so nothing overflows and no step needs
+// double precision (GB300's FP64 rate is a small fraction of its fp32 rate).
+struct KahanSum {
+    float s = 0.0f, c = 0.0f;
+    __device__ __forceinline__ void add(float term) {
+        const float y = term - c;
+        const float t = s + y;
+        c = (t - s) - y;
+        s = t;
+    }
+    __device__ __forceinline__ float total() const { return s - c; }
+};
+
+// max |v| over a row (one warp), and whether every entry is finite
+__device__ __forceinline__ float row_absmax(const float *src, int D, int lane, int &bad) {
+    float mx = 0.0f;
+    int b = 0;
+    for (int k = lane; k < D; k += 32) {
+        const float v = src[k];
+        if (!isfinite(v)) b = 1;
+        mx = fmaxf(mx, fabsf(v));
+    }
+    bad = warp_or_i(b);
+    return warp_max_f(mx);
+}
+
+// exponent e with max |v| = f 2^e, f in [0.5, 1): v * 2^-e lies in (-1, 1)
+__device__ __forceinline__ int scale_exponent(float mx) {
+    int e = 0;
+    if (mx > 0.0f) frexpf(mx, &e);
+    return e;
 }
 
 __device__ __forceinline__ void split_f16(float x, __half &hi, __half &lo) {
@@ -46,25 +83,27 @@ __global__ void table_prepare_kernel(const float *__restrict__ E, int64_t N, int
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= N) return;
     const float *src = E + row * (int64_t)D;
-    double ss = 0.0;
-    int bad = 0;
-    for (int k = lane; k < D; k += 32) {
-        const float v = src[k];
-        if (!isfinite(v)) bad = 1;
-        ss += (double)v * (double)v;
-    }
-    ss = warp_sum_d(ss);
-    bad = warp_or_i(bad);
-    if (bad || !(ss > 0.0) || !isfinite(ss)) {
+    int bad;
+    const float mx = row_absmax(src, D, lane, bad);
+    if (bad || !(mx > 0.0f)) {
         if (lane == 0) atomicOr(status, kStatusNonFinite);
         return;
     }
-    const double inv = 1.0 / sqrt(ss);
-    if (lane == 0) nrm[row] = (float)sqrt(ss);
+    const int e = scale_exponent(mx);
+    const float scale = ldexpf(1.0f, -e);
+    KahanSum ss;
+    for (int k = lane; k < D; k += 32) {
+        const float v = src[k] * scale;
+        ss.add(v * v);
+    }
+    const float sum = warp_sum_f(ss.total());
+    const float len = sqrtf(sum);  // norm of the scaled row, in [2^-1, sqrt(D))
+    const float inv = scale / len;
+    if (lane == 0) nrm[row] = ldexpf(len, e);
     float *dst = e_unit + row * (int64_t)Dp;
     __half *sp = e_split + row * (int64_t)(2 * Dp);
     for (int k = lane; k < Dp; k += 32) {
-        const float u = k < D ? (float)((double)src[k] * inv) : 0.0f;
+        const float u = k < D ? src[k] * inv : 0.0f;
         dst[k] = u;
         __half hi, lo;
         split_f16(u, hi, lo);
@@ -99,17 +138,17 @@ __global__ void table_prepare_f16_kernel(const float *__restrict__ E, int64_t N,
     frexpf(mx, &e);
     const float scale = ldexpf(1.0f, -e);
     __half *dst = e_f16 + row * (int64_t)Dp;
-    double ss = 0.0;
+    KahanSum ss;
     for (int k = lane; k < Dp; k += 32) {
         const __half h = __float2half_rn(k < D ? src[k] * scale : 0.0f);
         dst[k] = h;
-        const double hv = (double)__half2float(h);
-        ss += hv * hv;
+        const float hv = __half2float(h);
+        ss.add(hv * hv);
     }
-    ss = warp_sum_d(ss);
+    const float sum = warp_sum_f(ss.total());
     if (lane == 0) {
-        if (!(ss > 0.0)) atomicOr(status, kStatusNonFinite);
-        rn[row] = (float)(1.0 / sqrt(ss));
+        if (!(sum > 0.0f)) atomicOr(status, kStatusNonFinite);
+        rn[row] = 1.0f / sqrtf(sum);
     }
 }
 
@@ -121,34 +160,21 @@ __global__ void bmu_prepare_kernel(const float *__restrict__ A, int64_t rows, in
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= rows) return;
     const float *src = A + row * (int64_t)D;
-    double ss = 0.0;
-    float mx = 0.0f;
-    int bad = 0;
-    for (int k = lane; k < D; k += 32) {
-        const float v = src[k];
-        if (!isfinite(v)) bad = 1;
-        ss += (double)v * (double)v;
-        mx = fmaxf(mx, fabsf(v));
-    }
-    ss = warp_sum_d(ss);
-    mx = warp_max_f(mx);
-    bad = warp_or_i(bad);
+    int bad;
+    const float mx = row_absmax(src, D, lane, bad);
     if (bad) {
         if (lane == 0) atomicOr(status, kStatusNonFinite);
         return;
     }
     // scale = 2^-e with mx = f * 2^e, f in [0.5, 1): max |row * scale| < 1.
-    int e = 0;
-    if (mx > 0.0f) frexpf(mx, &e);
+    const int e = scale_exponent(mx);
     const float scale = ldexpf(1.0f, -e);
-    if (lane == 0) {
-        norm2[row] = (float)ss;
-        inv_scale[row] = ldexpf(1.0f, e);
-    }
     const int w = triple ? 3 * Dp : 2 * Dp;
     __half *sp = split + row * (int64_t)w;
+    KahanSum ss;
     for (int k = lane; k < Dp; k += 32) {
         const float u = k < D ? src[k] * scale : 0.0f;
+        ss.add(u * u);
         __half hi, lo;
         split_f16(u, hi, lo);
         if (triple) {
@@ -160,6 +186,11 @@ __global__ void bmu_prepare_kernel(const float *__restrict__ A, int64_t rows, in
             sp[Dp + k] = lo;
         }
     }
+    const float sum = warp_sum_f(ss.total());
+    if (lane == 0) {
+        norm2[row] = ldexpf(sum, 2 * e);
+        inv_scale[row] = ldexpf(1.0f, e);
+    }
 }
 
 __global__ void row_sqnorm_kernel(const float *__restrict__ A, int64_t rows, int D,
@@ -168,18 +199,19 @@ __global__ void row_sqnorm_kernel(const float *__restrict__ A, int64_t rows, int
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= rows) return;
     const float *src = A + row * (int64_t)D;
-    double ss = 0.0;
-    int bad = 0;
+    int bad;
+    const float mx = row_absmax(src, D, lane, bad);
+    const int e = scale_exponent(mx);
+    const float scale = ldexpf(1.0f, -e);
+    KahanSum ss;
     for (int k = lane; k < D; k += 32) {
-        const float v = src[k];
-        if (!isfinite(v)) bad = 1;
-        ss += (double)v * (double)v;
+        const float u = src[k] * scale;
+        ss.add(u * u);
     }
-    ss = warp_sum_d(ss);
-    bad = warp_or_i(bad);
+    const float sum = warp_sum_f(ss.total());
     if (lane == 0) {
         if (bad) atomicOr(status, kStatusNonFinite);
-        out[row] = (float)ss;
+        out[row] = ldexpf(sum, 2 * e);
     }
 }
 
