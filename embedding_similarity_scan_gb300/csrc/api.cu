@@ -861,7 +861,7 @@ int som_validate(int64_t n, int32_t side_x, int32_t side_y, int32_t D, double si
     // one CTA per (32 dimensions, 128 neurons of a row) and per (32 dimensions,
     // 64 neurons of a column): both grids must fit one launch
     const int64_t nch = (D + 31) / 32;
-    if ((nch + 1) * ((side_x + 127) / 128) * side_y >= (int64_t(1) << 31) ||
+    if (nch * ((side_x + 127) / 128) * side_y >= (int64_t(1) << 31) ||
         nch * side_x * ((side_y + 63) / 64) >= (int64_t(1) << 31))
         return fail(DSEQ_EINVAL, "map of %d x %d neurons with D=%d too large for one update", side_x, side_y, D);
     std::memset(&a, 0, sizeof a);

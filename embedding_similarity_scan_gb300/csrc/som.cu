@@ -24,7 +24,8 @@
 //               2^-F <= max|x| n 2^-61 per sample;
 //   rows        T = sum_dx g(|dx|) S[k + dx] along each map row, and the same
 //               for the counts, from a shared-memory tile with an R-wide halo
-//               (fp32 out);
+//               (fp32 out; the tile's loads are issued in batches so that
+//               several are in flight per thread);
 //   columns     num = sum_dy g(|dy|) T[k + dy side_x], den likewise from the
 //               row-smoothed counts, again from a tile; W_j = num / den where
 //               den > 0, in place.
@@ -109,7 +110,10 @@ __global__ void som_prepare_kernel(SomArgs a) {
     if ((threadIdx.x & 31) == 0 && mx) atomicMax(a.maxbits, mx);
 }
 
-// one warp per sample: S[bmu_i] += fixed(x_i), n[bmu_i] += 1
+// one warp per sample: S[bmu_i] += fixed(x_i), n[bmu_i] += 1.  A lane loads
+// all of its (up to kAccBatch) elements of the row before any atomic, so the
+// loads are in flight together.
+constexpr int kAccBatch = 8;
 __global__ void som_accumulate_kernel(SomArgs a) {
     const unsigned maxbits = *a.maxbits;
     if (maxbits >= 0x7f800000u) {  // an infinity or NaN among the samples
@@ -128,47 +132,76 @@ __global__ void som_accumulate_kernel(SomArgs a) {
         }
         const float *x = a.X + i * (int64_t)a.D;
         unsigned long long *s = reinterpret_cast<unsigned long long *>(a.S + (int64_t)c * a.D);
-        for (int d = lane; d < a.D; d += 32)
-            atomicAdd(s + d, (unsigned long long)to_fixed(__ldg(x + d), F));
+        for (int d0 = 0; d0 < a.D; d0 += 32 * kAccBatch) {
+            float v[kAccBatch];
+#pragma unroll
+            for (int u = 0; u < kAccBatch; ++u) {
+                const int d = d0 + 32 * u + lane;
+                v[u] = d < a.D ? __ldg(x + d) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kAccBatch; ++u) {
+                const int d = d0 + 32 * u + lane;
+                if (d < a.D) atomicAdd(s + d, (unsigned long long)to_fixed(v[u], F));
+            }
+        }
         if (lane == 0) atomicAdd(a.cnt + c, 1u);
     }
 }
 
-// Rows pass.  CTA = (dimension chunk of 32, tile of kRowTile neurons of one
-// map row); chunk index nch (one past the data chunks) smooths the counts.
-// The tile holds the neurons [x0 - R, x0 + kRowTile + R) of the row, zero
-// outside the map (a zero term leaves a sum unchanged, so this equals
-// clipping the window at the map's edge).
+// Loads rows [0, span) of a (span x 32) tile, kLoadBatch rows per warp in
+// flight: fetch(r) returns the value for tile row r and this lane.
+constexpr int kLoadBatch = 4;
+template <class Fetch>
+__device__ __forceinline__ void load_tile(float *tile, int span, int warp, int lane, Fetch fetch) {
+    constexpr int kWarps = kSomThreads / 32;
+    for (int base = warp; base < span; base += kWarps * kLoadBatch) {
+        float v[kLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int r = base + kWarps * u;
+            v[u] = r < span ? fetch(r) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int r = base + kWarps * u;
+            if (r < span) tile[r * 32 + lane] = v[u];
+        }
+    }
+}
+
+// Rows pass.  CTA = (dimension chunk of 32, kRowTile neurons of one map
+// row).  The tile holds the neurons [x0 - R, x0 + kRowTile + R) of the row,
+// zero outside the map (a zero term leaves a sum unchanged, so this equals
+// clipping the window at the map's edge).  Chunk-0 CTAs also smooth the
+// counts of their neurons.
 __global__ void __launch_bounds__(kSomThreads) som_rows_kernel(SomArgs a) {
-    extern __shared__ float tile[];  // (kRowTile + 2R) x 32, then g[R + 1]
+    extern __shared__ float tile[];  // (kRowTile + 2R) x 32, counts (span), g[R + 1]
     const int R = a.R, span = kRowTile + 2 * R;
-    float *g = tile + span * 32;
+    float *tc = tile + span * 32;
+    float *g = tc + span;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nch = (a.D + 31) / 32;
     const int ntx = (a.side_x + kRowTile - 1) / kRowTile;
     const int64_t b = blockIdx.x;
-    const int chunk = (int)(b % (nch + 1));
-    const int64_t rest = b / (nch + 1);
+    const int chunk = (int)(b % nch);
+    const int64_t rest = b / nch;
     const int x0 = (int)(rest % ntx) * kRowTile;
-    const int64_t y = rest / ntx;
+    const int64_t row0 = (rest / ntx) * a.side_x;
     for (int k = threadIdx.x; k <= R; k += blockDim.x) g[k] = a.g[k];
-    const bool counts = chunk == nch;
     const int d = chunk * 32 + lane;
     float s1, s2;
     fixed_unscale(fixed_scale(*a.maxbits, a.n), s1, s2);
-    const int64_t row0 = y * a.side_x;
-    for (int xi = warp; xi < span; xi += kSomThreads / 32) {
-        const int xg = x0 - R + xi;
-        float v = 0.0f;
-        if (xg >= 0 && xg < a.side_x) {
-            const int64_t j = row0 + xg;
-            if (counts)
-                v = lane == 0 ? (float)a.cnt[j] : 0.0f;
-            else if (d < a.D)
-                v = from_fixed(a.S[j * a.D + d], s1, s2);
+    load_tile(tile, span, warp, lane, [&](int r) {
+        const int xg = x0 - R + r;
+        return (xg >= 0 && xg < a.side_x && d < a.D)
+                   ? from_fixed(a.S[(row0 + xg) * a.D + d], s1, s2) : 0.0f;
+    });
+    if (chunk == 0)
+        for (int r = threadIdx.x; r < span; r += blockDim.x) {
+            const int xg = x0 - R + r;
+            tc[r] = (xg >= 0 && xg < a.side_x) ? (float)a.cnt[row0 + xg] : 0.0f;
         }
-        tile[xi * 32 + lane] = v;
-    }
     __syncthreads();
     for (int xi = warp; xi < kRowTile; xi += kSomThreads / 32) {
         const int x = x0 + xi;
@@ -176,23 +209,26 @@ __global__ void __launch_bounds__(kSomThreads) som_rows_kernel(SomArgs a) {
         float acc = 0.0f;
         const float *t = tile + xi * 32 + lane;
         for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k < R ? R - k : k - R], t[k * 32], acc);
-        const int64_t j = row0 + x;
-        if (counts) {
-            if (lane == 0) a.Tc[j] = acc;
-        } else if (d < a.D) {
-            a.T[j * a.D + d] = acc;
-        }
+        if (d < a.D) a.T[(row0 + x) * a.D + d] = acc;
     }
+    if (chunk == 0)
+        for (int xi = threadIdx.x; xi < kRowTile && x0 + xi < a.side_x; xi += blockDim.x) {
+            float acc = 0.0f;
+            for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k < R ? R - k : k - R], tc[xi + k], acc);
+            a.Tc[row0 + x0 + xi] = acc;
+        }
 }
 
 // Columns pass and the division, in place on W.  CTA = (dimension chunk of
-// 32, one map column, kColTile neurons down it).  Nothing is written when an
-// earlier kernel flagged an error, so W is then left as it was.
+// 32, one map column, kColTile neurons down it); the denominators of the
+// tile's neurons are smoothed once into shared memory.  Nothing is written
+// when an earlier kernel flagged an error, so W is then left as it was.
 __global__ void __launch_bounds__(kSomThreads) som_cols_kernel(SomArgs a) {
-    extern __shared__ float tile[];  // (kColTile + 2R) x 32, then counts, then g
+    extern __shared__ float tile[];  // (kColTile + 2R) x 32, counts (span), den, g
     const int R = a.R, span = kColTile + 2 * R;
     float *tc = tile + span * 32;
-    float *g = tc + span;
+    float *den = tc + span;
+    float *g = den + kColTile;
     if (*(volatile int *)a.status != 0) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nch = (a.D + 31) / 32;
@@ -203,29 +239,30 @@ __global__ void __launch_bounds__(kSomThreads) som_cols_kernel(SomArgs a) {
     const int y0 = (int)(rest / a.side_x) * kColTile;
     for (int k = threadIdx.x; k <= R; k += blockDim.x) g[k] = a.g[k];
     const int d = chunk * 32 + lane;
-    for (int yi = warp; yi < span; yi += kSomThreads / 32) {
-        const int yg = y0 - R + yi;
-        float v = 0.0f, c = 0.0f;
-        if (yg >= 0 && yg < a.side_y) {
-            const int64_t j = (int64_t)yg * a.side_x + x;
-            if (d < a.D) v = a.T[j * a.D + d];
-            c = a.Tc[j];
-        }
-        tile[yi * 32 + lane] = v;
-        if (lane == 0) tc[yi] = c;
+    load_tile(tile, span, warp, lane, [&](int r) {
+        const int yg = y0 - R + r;
+        return (yg >= 0 && yg < a.side_y && d < a.D)
+                   ? a.T[((int64_t)yg * a.side_x + x) * a.D + d] : 0.0f;
+    });
+    for (int r = threadIdx.x; r < span; r += blockDim.x) {
+        const int yg = y0 - R + r;
+        tc[r] = (yg >= 0 && yg < a.side_y) ? a.Tc[(int64_t)yg * a.side_x + x] : 0.0f;
+    }
+    __syncthreads();
+    for (int yi = threadIdx.x; yi < kColTile; yi += blockDim.x) {
+        float acc = 0.0f;
+        for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k < R ? R - k : k - R], tc[yi + k], acc);
+        den[yi] = acc;
     }
     __syncthreads();
     for (int yi = warp; yi < kColTile; yi += kSomThreads / 32) {
         const int yy = y0 + yi;
         if (yy >= a.side_y) break;
-        float num = 0.0f, den = 0.0f;
+        float num = 0.0f;
         const float *t = tile + yi * 32 + lane;
-        for (int k = 0; k <= 2 * R; ++k) {
-            const float w = g[k < R ? R - k : k - R];
-            num = fmaf(w, t[k * 32], num);
-            den = fmaf(w, tc[yi + k], den);
-        }
-        if (den > 0.0f && d < a.D) a.W[((int64_t)yy * a.side_x + x) * a.D + d] = num / den;
+        for (int k = 0; k <= 2 * R; ++k) num = fmaf(g[k < R ? R - k : k - R], t[k * 32], num);
+        const float dn = den[yi];
+        if (dn > 0.0f && d < a.D) a.W[((int64_t)yy * a.side_x + x) * a.D + d] = num / dn;
     }
 }
 
@@ -234,8 +271,10 @@ int grid_for(int64_t work, int per_block, int sms) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)sms * 16));
 }
 
-size_t rows_smem(int R) { return ((size_t)(kRowTile + 2 * R) * 32 + R + 1) * sizeof(float); }
-size_t cols_smem(int R) { return ((size_t)(kColTile + 2 * R) * 33 + R + 1) * sizeof(float); }
+size_t rows_smem(int R) { return ((size_t)(kRowTile + 2 * R) * 33 + R + 1) * sizeof(float); }
+size_t cols_smem(int R) {
+    return ((size_t)(kColTile + 2 * R) * 33 + kColTile + R + 1) * sizeof(float);
+}
 
 }  // namespace
 
@@ -260,7 +299,7 @@ cudaError_t launch_som_update(const SomArgs &a, int sms, cudaStream_t st) {
                          kSomThreads, 0, st>>>(a);
     som_accumulate_kernel<<<grid_for(a.n, kSomThreads / 32, sms), kSomThreads, 0, st>>>(a);
     const int64_t ntx = (a.side_x + kRowTile - 1) / kRowTile;
-    som_rows_kernel<<<(unsigned)((nch + 1) * ntx * a.side_y), kSomThreads, rows_smem(a.R), st>>>(a);
+    som_rows_kernel<<<(unsigned)(nch * ntx * a.side_y), kSomThreads, rows_smem(a.R), st>>>(a);
     const int64_t nty = (a.side_y + kColTile - 1) / kColTile;
     som_cols_kernel<<<(unsigned)(nch * a.side_x * nty), kSomThreads, cols_smem(a.R), st>>>(a);
     return cudaGetLastError();
