@@ -176,7 +176,7 @@ __device__ __forceinline__ void load_tile(float *tile, int span, int warp, int l
 // clipping the window at the map's edge).  Chunk-0 CTAs also smooth the
 // counts of their neurons.
 __global__ void __launch_bounds__(kSomThreads) som_rows_kernel(SomArgs a) {
-    extern __shared__ float tile[];  // (kRowTile + 2R) x 32, counts (span), g[R + 1]
+    extern __shared__ float tile[];  // (kRowTile + 2R) x 32, counts (span), g[2R + 1]
     const int R = a.R, span = kRowTile + 2 * R;
     float *tc = tile + span * 32;
     float *g = tc + span;
@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(kSomThreads) som_rows_kernel(SomArgs a) {
     const int64_t rest = b / nch;
     const int x0 = (int)(rest % ntx) * kRowTile;
     const int64_t row0 = (rest / ntx) * a.side_x;
-    for (int k = threadIdx.x; k <= R; k += blockDim.x) g[k] = a.g[k];
+    // the whole window, g[k] = weight of offset k - R
+    for (int k = threadIdx.x; k <= 2 * R; k += blockDim.x) g[k] = a.g[k < R ? R - k : k - R];
     const int d = chunk * 32 + lane;
     float s1, s2;
     fixed_unscale(fixed_scale(*a.maxbits, a.n), s1, s2);
@@ -203,18 +204,28 @@ __global__ void __launch_bounds__(kSomThreads) som_rows_kernel(SomArgs a) {
             tc[r] = (xg >= 0 && xg < a.side_x) ? (float)a.cnt[row0 + xg] : 0.0f;
         }
     __syncthreads();
-    for (int xi = warp; xi < kRowTile; xi += kSomThreads / 32) {
-        const int x = x0 + xi;
-        if (x >= a.side_x) break;
-        float acc = 0.0f;
-        const float *t = tile + xi * 32 + lane;
-        for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k < R ? R - k : k - R], t[k * 32], acc);
-        if (d < a.D) a.T[(row0 + x) * a.D + d] = acc;
+    // each warp: kRowTile / 8 consecutive outputs, all taps of one weight at once
+    {
+        constexpr int V = kRowTile / (kSomThreads / 32);
+        const int xb = warp * V;
+        float acc[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = 0.0f;
+        const float *t = tile + xb * 32 + lane;
+        for (int k = 0; k <= 2 * R; ++k) {
+            const float w = g[k];
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = fmaf(w, t[(k + v) * 32], acc[v]);
+        }
+        if (d < a.D)
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                if (x0 + xb + v < a.side_x) a.T[(row0 + x0 + xb + v) * a.D + d] = acc[v];
     }
     if (chunk == 0)
         for (int xi = threadIdx.x; xi < kRowTile && x0 + xi < a.side_x; xi += blockDim.x) {
             float acc = 0.0f;
-            for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k < R ? R - k : k - R], tc[xi + k], acc);
+            for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k], tc[xi + k], acc);
             a.Tc[row0 + x0 + xi] = acc;
         }
 }
@@ -224,7 +235,7 @@ __global__ void __launch_bounds__(kSomThreads) som_rows_kernel(SomArgs a) {
 // tile's neurons are smoothed once into shared memory.  Nothing is written
 // when an earlier kernel flagged an error, so W is then left as it was.
 __global__ void __launch_bounds__(kSomThreads) som_cols_kernel(SomArgs a) {
-    extern __shared__ float tile[];  // (kColTile + 2R) x 32, counts (span), den, g
+    extern __shared__ float tile[];  // (kColTile + 2R) x 32, counts (span), den, g[2R + 1]
     const int R = a.R, span = kColTile + 2 * R;
     float *tc = tile + span * 32;
     float *den = tc + span;
@@ -237,7 +248,8 @@ __global__ void __launch_bounds__(kSomThreads) som_cols_kernel(SomArgs a) {
     const int64_t rest = b / nch;
     const int x = (int)(rest % a.side_x);
     const int y0 = (int)(rest / a.side_x) * kColTile;
-    for (int k = threadIdx.x; k <= R; k += blockDim.x) g[k] = a.g[k];
+    // the whole window, g[k] = weight of offset k - R
+    for (int k = threadIdx.x; k <= 2 * R; k += blockDim.x) g[k] = a.g[k < R ? R - k : k - R];
     const int d = chunk * 32 + lane;
     load_tile(tile, span, warp, lane, [&](int r) {
         const int yg = y0 - R + r;
@@ -251,18 +263,29 @@ __global__ void __launch_bounds__(kSomThreads) som_cols_kernel(SomArgs a) {
     __syncthreads();
     for (int yi = threadIdx.x; yi < kColTile; yi += blockDim.x) {
         float acc = 0.0f;
-        for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k < R ? R - k : k - R], tc[yi + k], acc);
+        for (int k = 0; k <= 2 * R; ++k) acc = fmaf(g[k], tc[yi + k], acc);
         den[yi] = acc;
     }
     __syncthreads();
-    for (int yi = warp; yi < kColTile; yi += kSomThreads / 32) {
-        const int yy = y0 + yi;
-        if (yy >= a.side_y) break;
-        float num = 0.0f;
-        const float *t = tile + yi * 32 + lane;
-        for (int k = 0; k <= 2 * R; ++k) num = fmaf(g[k < R ? R - k : k - R], t[k * 32], num);
-        const float dn = den[yi];
-        if (dn > 0.0f && d < a.D) a.W[((int64_t)yy * a.side_x + x) * a.D + d] = num / dn;
+    {
+        constexpr int V = kColTile / (kSomThreads / 32);
+        const int yb = warp * V;
+        float num[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) num[v] = 0.0f;
+        const float *t = tile + yb * 32 + lane;
+        for (int k = 0; k <= 2 * R; ++k) {
+            const float w = g[k];
+#pragma unroll
+            for (int v = 0; v < V; ++v) num[v] = fmaf(w, t[(k + v) * 32], num[v]);
+        }
+        if (d < a.D)
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int yy = y0 + yb + v;
+                const float dn = den[yb + v];
+                if (yy < a.side_y && dn > 0.0f) a.W[((int64_t)yy * a.side_x + x) * a.D + d] = num[v] / dn;
+            }
     }
 }
 
@@ -271,9 +294,9 @@ int grid_for(int64_t work, int per_block, int sms) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)sms * 16));
 }
 
-size_t rows_smem(int R) { return ((size_t)(kRowTile + 2 * R) * 33 + R + 1) * sizeof(float); }
+size_t rows_smem(int R) { return ((size_t)(kRowTile + 2 * R) * 33 + 2 * R + 1) * sizeof(float); }
 size_t cols_smem(int R) {
-    return ((size_t)(kColTile + 2 * R) * 33 + kColTile + R + 1) * sizeof(float);
+    return ((size_t)(kColTile + 2 * R) * 33 + kColTile + 2 * R + 1) * sizeof(float);
 }
 
 }  // namespace
