@@ -43,7 +43,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = {
-    "tc_dseq_kernel": ["tc_dseq.cu", "common.cuh", "internal.h"],
+    "tc_dseq_kernel": ["tc_dseq.cu", "common.cuh", "internal.h", "numeric.cuh"],
     "tc_bmu_kernel": ["tc_bmu.cu", "common.cuh", "internal.h"],
 }
 

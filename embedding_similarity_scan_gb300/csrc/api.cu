@@ -20,6 +20,8 @@ namespace {
 // --------------------------------------------------------------------------
 // errors and statistics (per calling thread)
 thread_local std::string g_err;
+constexpr int kNoShift = 1 << 30;
+
 struct Stats {
     int64_t units = 0, tile_n = 0, grid = 0, launches = 0, kernel_ns = 0, update_ns = 0;
 };
@@ -346,6 +348,7 @@ struct dseq_ctx {
     // run workspace
     DevBuf m, keys, q, q_rn, csum, status, barrier, starts, mask, picks, trace_slot, timeline;
     int64_t timeline_iters = 0, timeline_grid = 0;
+    int csum_shift = kNoShift;  // fixed-point scale of the centroid sums, set on first use
     // state left on the device by the last successful run, for "resume"
     bool has_state = false;
     int64_t state_picks = 0;  // picks per sequence made so far
@@ -601,8 +604,22 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.centroid = (int)ctx->opt.criterion;
         if (a.centroid) {
             if (f16) return fail(DSEQ_EINVAL, "the centroid criterion runs on split storage (storage=0)");
-            TRY(ctx->csum.ensure((size_t)Bp * ctx->Dp * sizeof(double)));
-            a.csum = ctx->csum.as<double>();
+            TRY(ctx->csum.ensure((size_t)Bp * ctx->Dp * sizeof(long long)));
+            a.csum = ctx->csum.as<long long>();
+            if (ctx->csum_shift == kNoShift) {
+                // every raw-row entry is below the largest row norm 2^e and a
+                // sequence holds at most N rows: F = 62 - e - ceil(log2 N)
+                std::vector<float> h_nrm;
+                TRY(to_host(ctx->nrm.as<float>(), (size_t)N, h_nrm, st));
+                float mx = 0.0f;
+                for (float v : h_nrm) mx = std::max(mx, v);
+                int e = 0;
+                std::frexp(mx, &e);
+                int L = 0;
+                while ((int64_t(1) << L) < N) ++L;
+                ctx->csum_shift = 62 - e - L;
+            }
+            a.csum_shift = ctx->csum_shift;
         }
         a.e_unit = ctx->e_unit.as<float>();
         a.nrm = ctx->nrm.as<float>();

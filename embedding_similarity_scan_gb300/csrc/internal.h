@@ -94,10 +94,12 @@ struct TcDseqArgs {
     const float *rn;
     float *q_rn;             // Bp: inverse norm of each current query row
     // centroid criterion (centroid = 1): the query is the unit centroid of the
-    // rows a sequence holds; csum (Bp x Dp, double) keeps their sum, rebuilt
-    // from the unit rows e_unit (N x Dp) times the row norms nrm (N)
+    // rows a sequence holds; csum (Bp x Dp) keeps their exact sum in fixed
+    // point (2^-csum_shift units), rebuilt from the unit rows e_unit (N x Dp)
+    // times the row norms nrm (N)
     int centroid;
-    double *csum;
+    long long *csum;
+    int csum_shift;
     const float *e_unit;
     const float *nrm;
     float *m;                // units x 128 x tile_n

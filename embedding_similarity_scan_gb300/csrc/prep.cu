@@ -12,63 +12,11 @@
 // 2^12.
 #include "common.cuh"
 #include "internal.h"
+#include "numeric.cuh"
 
 namespace dseq {
 
 namespace {
-
-__device__ __forceinline__ float warp_sum_f(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-
-__device__ __forceinline__ float warp_max_f(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ int warp_or_i(int v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Compensated (Kahan) fp32 sum: error about 2 ulp of the total whatever the
-// number of terms.  All norms here are sums of squares of values scaled
-// into [0, 1) by a power of two, so nothing overflows and no step needs
-// double precision (GB300's FP64 rate is a small fraction of its fp32 rate).
-struct KahanSum {
-    float s = 0.0f, c = 0.0f;
-    __device__ __forceinline__ void add(float term) {
-        const float y = term - c;
-        const float t = s + y;
-        c = (t - s) - y;
-        s = t;
-    }
-    __device__ __forceinline__ float total() const { return s - c; }
-};
-
-// max |v| over a row (one warp), and whether every entry is finite
-__device__ __forceinline__ float row_absmax(const float *src, int D, int lane, int &bad) {
-    float mx = 0.0f;
-    int b = 0;
-    for (int k = lane; k < D; k += 32) {
-        const float v = src[k];
-        if (!isfinite(v)) b = 1;
-        mx = fmaxf(mx, fabsf(v));
-    }
-    bad = warp_or_i(b);
-    return warp_max_f(mx);
-}
-
-// exponent e with max |v| = f 2^e, f in [0.5, 1): v * 2^-e lies in (-1, 1)
-__device__ __forceinline__ int scale_exponent(float mx) {
-    int e = 0;
-    if (mx > 0.0f) frexpf(mx, &e);
-    return e;
-}
 
 __device__ __forceinline__ void split_f16(float x, __half &hi, __half &lo) {
     hi = __float2half_rn(x);

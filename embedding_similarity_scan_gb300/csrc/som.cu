@@ -36,6 +36,7 @@
 // (fp32) or 256-byte (int64) segment.
 #include "common.cuh"
 #include "internal.h"
+#include "numeric.cuh"
 
 namespace dseq {
 
@@ -53,44 +54,6 @@ __device__ __forceinline__ int fixed_scale(unsigned maxbits, int64_t n) {
     const int E = ef == 0 ? -126 : ef - 127;
     const int L = n <= 1 ? 0 : 64 - __clzll((unsigned long long)(n - 1));
     return 61 - E - L;
-}
-
-// trunc(x 2^F) from the bits of x (integer operations only; exact)
-__device__ __forceinline__ long long to_fixed(float x, int F) {
-    const uint32_t b = __float_as_uint(x);
-    int ef = (int)((b >> 23) & 0xffu);
-    uint32_t m = b & 0x7fffffu;
-    if (ef == 0) {
-        if (m == 0) return 0;
-        ef = 1;  // subnormal: no implicit bit
-    } else {
-        m |= 0x800000u;
-    }
-    const int s = ef - 150 + F;  // x = m 2^(ef - 150)
-    unsigned long long u;
-    if (s >= 0)
-        u = (unsigned long long)m << s;
-    else if (s > -32)
-        u = (unsigned long long)(m >> (-s));
-    else
-        u = 0;
-    return (b >> 31) ? -(long long)u : (long long)u;
-}
-
-// 2^-F as two normal fp32 factors (F ranges over about [-97, 187])
-__device__ __forceinline__ void fixed_unscale(int F, float &s1, float &s2) {
-    const int f1 = F / 2, f2 = F - f1;
-    s1 = __int_as_float((127 - f1) << 23);
-    s2 = __int_as_float((127 - f2) << 23);
-}
-
-// v 2^-F in fp32 (two 32-bit conversions; relative error below 2^-22)
-__device__ __forceinline__ float from_fixed(long long v, float s1, float s2) {
-    const unsigned long long u = v < 0 ? 0ull - (unsigned long long)v : (unsigned long long)v;
-    float f = fmaf(__uint2float_rn((unsigned)(u >> 32)), 4294967296.0f,
-                   __uint2float_rn((unsigned)(u & 0xffffffffu)));
-    f = (f * s1) * s2;
-    return v < 0 ? -f : f;
 }
 
 __global__ void som_prepare_kernel(SomArgs a) {

@@ -41,6 +41,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "numeric.cuh"
 
 namespace dseq {
 
@@ -134,9 +135,10 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ctotal;
              i += stride) {
             const int b = (int)(i / a.Dp), k = (int)(i - (int64_t)b * a.Dp);
-            a.csum[i] = b < a.B ? (double)a.e_unit[(int64_t)starts[b] * a.Dp + k] *
-                                      (double)a.nrm[starts[b]]
-                                : 0.0;
+            a.csum[i] = b < a.B ? to_fixed(a.e_unit[(int64_t)starts[b] * a.Dp + k] *
+                                               a.nrm[starts[b]],
+                                           a.csum_shift)
+                                : 0ll;
         }
     }
 }
@@ -432,7 +434,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         // a candidate's running minimum changes with probability
                         // about 1/(t+1) after t picks: write back only what moved
-                        if (changed)
+                        // centroid: the next iteration needs only the -inf marks,
+                        // so this iteration's distances are stored only for a trace
+                        if (changed && (!kCentroid || a.trace_slot))
                             st_cg_hint(&mt[((g * 4 + q) * 8 + v) * 32 + lane],
                                        make_float4(mv[0], mv[1], mv[2], mv[3]), stream);
                     }
@@ -516,21 +520,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // add the winner to the sequence's centroid sum (double),
                         // then write the split unit centroid as the next query
                         const int bq = base + i;
-                        double *cs = a.csum + (int64_t)bq * a.Dp;
+                        long long *cs = a.csum + (int64_t)bq * a.Dp;
                         const float *eu = a.e_unit + (int64_t)wi * a.Dp;
-                        const double nw = (double)a.nrm[wi];
-                        double ss = 0.0;
+                        const float nw = a.nrm[wi];
+                        const int F = a.csum_shift;
+                        float s1, s2;
+                        fixed_unscale(F, s1, s2);
+                        // exact integer sum; then the centroid's largest |entry|
+                        float mx = 0.0f;
                         for (int k = lane; k < a.Dp; k += 32) {
-                            const double cv = cs[k] + (double)eu[k] * nw;
-                            cs[k] = cv;
-                            ss += cv * cv;
+                            const long long v = cs[k] + to_fixed(eu[k] * nw, F);
+                            cs[k] = v;
+                            mx = fmaxf(mx, fabsf(from_fixed(v, s1, s2)));
                         }
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                        const double inv = ss > 0.0 ? 1.0 / sqrt(ss) : 0.0;
+                        const float sc = ldexpf(1.0f, -scale_exponent(warp_max_f(mx)));
+                        KahanSum ss;
+                        for (int k = lane; k < a.Dp; k += 32) {
+                            const float c = from_fixed(cs[k], s1, s2) * sc;
+                            ss.add(c * c);
+                        }
+                        const float sum = warp_sum_f(ss.total());
+                        // a zero centroid gives a zero query: every distance is 1
+                        const float inv = sum > 0.0f ? sc / sqrtf(sum) : 0.0f;
                         __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
                         for (int k = lane; k < a.Dp; k += 32) {
-                            const float u = (float)(cs[k] * inv);
+                            const float u = from_fixed(cs[k], s1, s2) * inv;
                             const __half hi = __float2half_rn(u);
                             const __half lo = __float2half_rn((u - __half2float(hi)) * 4096.0f);
                             qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
