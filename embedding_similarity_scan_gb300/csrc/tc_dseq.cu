@@ -517,39 +517,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t wi = __shfl_sync(0xffffffffu, w, i);
                     if (ki == 0ull) continue;
                     if (kCentroid) {
-                        // add the winner to the sequence's centroid sum (double),
-                        // then write the split unit centroid as the next query
+                        // add the winner to the sequence's exact centroid sum,
+                        // then write the split unit centroid as the next query.
+                        // Sums stay below 2^62 units, so v 2^-62 lies in (-1, 1):
+                        // that fixed scaling gives the norm without overflow, and
+                        // its smallest nonzero square (2^-124) is a normal fp32.
                         const int bq = base + i;
                         long long *cs = a.csum + (int64_t)bq * a.Dp;
                         const float *eu = a.e_unit + (int64_t)wi * a.Dp;
                         const float nw = a.nrm[wi];
                         const int F = a.csum_shift;
                         float s1, s2;
-                        fixed_unscale(F, s1, s2);
-                        // exact integer sum; then the centroid's largest |entry|
-                        float mx = 0.0f;
-                        for (int k = lane; k < a.Dp; k += 32) {
-                            const long long v = cs[k] + to_fixed(eu[k] * nw, F);
-                            cs[k] = v;
-                            mx = fmaxf(mx, fabsf(from_fixed(v, s1, s2)));
-                        }
-                        const float sc = ldexpf(1.0f, -scale_exponent(warp_max_f(mx)));
+                        fixed_unscale(62, s1, s2);
+                        constexpr int kB = 8;  // loads in flight per lane
                         KahanSum ss;
-                        for (int k = lane; k < a.Dp; k += 32) {
-                            const float c = from_fixed(cs[k], s1, s2) * sc;
-                            ss.add(c * c);
+                        for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
+                            long long v[kB];
+                            float x[kB];
+#pragma unroll
+                            for (int u = 0; u < kB; ++u) {
+                                const int k = k0 + 32 * u + lane;
+                                v[u] = k < a.Dp ? cs[k] : 0ll;
+                                x[u] = k < a.Dp ? __ldg(eu + k) : 0.0f;
+                            }
+#pragma unroll
+                            for (int u = 0; u < kB; ++u) {
+                                const int k = k0 + 32 * u + lane;
+                                if (k < a.Dp) {
+                                    v[u] += to_fixed(x[u] * nw, F);
+                                    cs[k] = v[u];
+                                    const float c = from_fixed(v[u], s1, s2);
+                                    ss.add(c * c);
+                                }
+                            }
                         }
                         const float sum = warp_sum_f(ss.total());
                         // a zero centroid gives a zero query: every distance is 1
-                        const float inv = sum > 0.0f ? sc / sqrtf(sum) : 0.0f;
+                        const float inv = sum > 0.0f ? 1.0f / sqrtf(sum) : 0.0f;
                         __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
-                        for (int k = lane; k < a.Dp; k += 32) {
-                            const float u = from_fixed(cs[k], s1, s2) * inv;
-                            const __half hi = __float2half_rn(u);
-                            const __half lo = __float2half_rn((u - __half2float(hi)) * 4096.0f);
-                            qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
-                            qd[a.Dp + k] = hi;
-                            qd[2 * a.Dp + k] = lo;
+                        __syncwarp();
+                        for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
+                            long long v[kB];
+#pragma unroll
+                            for (int u = 0; u < kB; ++u) {
+                                const int k = k0 + 32 * u + lane;
+                                v[u] = k < a.Dp ? cs[k] : 0ll;
+                            }
+#pragma unroll
+                            for (int u = 0; u < kB; ++u) {
+                                const int k = k0 + 32 * u + lane;
+                                if (k < a.Dp) {
+                                    const float uval = from_fixed(v[u], s1, s2) * inv;
+                                    const __half hi = __float2half_rn(uval);
+                                    const __half lo =
+                                        __float2half_rn((uval - __half2float(hi)) * 4096.0f);
+                                    qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
+                                    qd[a.Dp + k] = hi;
+                                    qd[2 * a.Dp + k] = lo;
+                                }
+                            }
                         }
                         continue;
                     }
