@@ -185,7 +185,8 @@ def dseq_destroy(ctx: Context) -> None:
 
 
 def dseq_get_timeline(ctx: Context):
-    """Phase stamps [iters, grid, 8] (int64 ns) of the last timed run, or None."""
+    """Phase stamps and wait times [iters, grid, 12] (int64 ns) of the last
+    timed run, or None."""
     import numpy as np
 
     lib = load()
@@ -193,7 +194,7 @@ def dseq_get_timeline(ctx: Context):
     _check(lib.dseq_get_timeline(ctx.handle, None, 0, ctypes.byref(it), ctypes.byref(gr)))
     if it.value == 0:
         return None
-    out = np.empty((it.value, gr.value, 8), np.int64)
+    out = np.empty((it.value, gr.value, 12), np.int64)
     _check(lib.dseq_get_timeline(ctx.handle, out.ctypes.data, out.size, ctypes.byref(it),
                                  ctypes.byref(gr)))
     return out

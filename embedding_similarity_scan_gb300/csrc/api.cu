@@ -23,7 +23,8 @@ thread_local std::string g_err;
 constexpr int kNoShift = 1 << 30;
 
 struct Stats {
-    int64_t units = 0, tile_n = 0, grid = 0, launches = 0, kernel_ns = 0, update_ns = 0;
+    int64_t units = 0, tile_n = 0, tile_n2 = 0, n_wide = 0, grid = 0, launches = 0, kernel_ns = 0,
+            update_ns = 0;
 };
 thread_local Stats g_stats;
 
@@ -65,6 +66,7 @@ int cuda_code(cudaError_t e) {
 struct Options {
     int64_t engine = 0;
     int64_t tile_n = 0;
+    int64_t tile_n2 = 0;
     int64_t grid = 0;
     int64_t timeout_ms = 10000;
     int64_t fault_skip_arrive = 0;
@@ -86,6 +88,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "tile_n") {
         if (v != 0 && (v < 32 || v > 256 || v % 32)) return fail(DSEQ_EINVAL, "tile_n must be 0 or a multiple of 32 in [32, 256]");
         o.tile_n = v;
+    } else if (n == "tile_n2") {
+        if (v != 0 && (v < 32 || v > 256 || v % 32)) return fail(DSEQ_EINVAL, "tile_n2 must be 0 or a multiple of 32 in [32, 256]");
+        o.tile_n2 = v;
     } else if (n == "grid") {
         if (v < 0 || v > 65535) return fail(DSEQ_EINVAL, "grid out of range");
         o.grid = v;
@@ -121,6 +126,7 @@ int64_t get_opt(const Options &o, const char *name) {
     const std::string n(name);
     if (n == "engine") return o.engine;
     if (n == "tile_n") return o.tile_n;
+    if (n == "tile_n2") return o.tile_n2;
     if (n == "grid") return o.grid;
     if (n == "timeout_ms") return o.timeout_ms;
     if (n == "fault_skip_arrive") return o.fault_skip_arrive;
@@ -256,23 +262,63 @@ int encode_f16_map(CUtensorMap &map, const void *base, int64_t cols, int64_t row
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-// Candidate columns per unit: the multiple of 32 in [32, 256] that minimises
-// the makespan ceil(units / grid) * (tile_n + 64), the 64 standing for the
-// fixed cost of a unit (pipeline refill, epilogue drain, key atomics);
-// ties go to the wider tile.
-int choose_tile_n(int64_t n_rows_blocks, int64_t ncols, int grid) {
-    int best = 256;
-    int64_t best_cost = INT64_MAX;
-    for (int tn = 256; tn >= 32; tn -= 32) {
-        const int64_t units = n_rows_blocks * ((ncols + tn - 1) / tn);
-        const int64_t rounds = (units + grid - 1) / grid;
-        const int64_t cost = rounds * (tn + 64);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = tn;
+// Relative time of one work unit w candidate columns wide, from the phase
+// timeline of the persistent kernel on GB300.  Split storage: a unit costs
+// the same for any width up to 128 (the 128 query rows x 3 parts streamed
+// from L2 bound it), and above that grows with the width rounded up to a
+// multiple of 64 (a 224-wide MMA takes as long as a 256-wide one).  FP16
+// storage: nearly flat (the epilogue bounds it).
+double unit_cost(int w, bool f16) {
+    if (f16) return 0.87 + 0.13 * w / 256.0;
+    const int w64 = (w + 63) / 64 * 64;
+    return std::max(0.77, w64 / 256.0);
+}
+
+// Chunk widths of the diversity plan: chunks j < n_wide are w1 columns wide,
+// the rest w2 <= w1, covering ncols.  Units (blocks x chunks, chunk-major)
+// are dealt round-robin to `workers`; the widths and split are those that
+// minimise the most loaded worker's summed unit_cost (ties: fewer units,
+// then wider tiles).  forced_w1 / forced_w2 > 0 pin a width (w1 alone pins a
+// uniform plan).
+void choose_widths(TcPlan &plan, int64_t blocks, int64_t ncols, int workers, bool f16,
+                   int forced_w1, int forced_w2) {
+    double best_cost = 1e300;
+    int64_t best_units = INT64_MAX;
+    int best_w1 = 256, best_w2 = 256, best_nw = 0, best_nn = 0;
+    for (int w1 = 256; w1 >= 32; w1 -= 32) {
+        if (forced_w1 > 0 && w1 != forced_w1) continue;
+        for (int w2 = w1; w2 >= 32; w2 -= 32) {
+            if (forced_w2 > 0 ? w2 != forced_w2 : (forced_w1 > 0 && w2 != w1)) continue;
+            const int64_t max_wide = (ncols + w1 - 1) / w1;
+            // all-narrow splits are the uniform plan of width w2
+            for (int64_t nw = (w2 == w1 ? max_wide : 1); nw <= max_wide; ++nw) {
+                const int64_t rest = std::max<int64_t>(0, ncols - nw * w1);
+                const int64_t nn = (rest + w2 - 1) / w2;
+                const int64_t units = blocks * (nw + nn), wide = blocks * nw;
+                const double c1 = unit_cost(w1, f16), c2 = unit_cost(w2, f16);
+                double worst = 0.0;
+                for (int k = 0; k < workers && k < units; ++k) {
+                    const int64_t n_all = (units - 1 - k) / workers + 1;
+                    const int64_t n_wide = k < wide ? (wide - 1 - k) / workers + 1 : 0;
+                    worst = std::max(worst, n_wide * c1 + (n_all - n_wide) * c2);
+                }
+                const bool better = worst < best_cost - 1e-9 ||
+                                    (worst < best_cost + 1e-9 && units < best_units);
+                if (better) {
+                    best_cost = worst;
+                    best_units = units;
+                    best_w1 = w1;
+                    best_w2 = w2;
+                    best_nw = (int)nw;
+                    best_nn = (int)nn;
+                }
+            }
         }
     }
-    return best;
+    plan.tile_n = best_w1;
+    plan.tile_n2 = best_nn == 0 ? best_w1 : best_w2;
+    plan.n_wide = best_nw;
+    plan.n_chunk = best_nw + best_nn;
 }
 
 int read_status(int *status_dev, cudaStream_t st) {
@@ -373,6 +419,8 @@ int64_t dseq_last_stat(const char *name) {
     const std::string n(name);
     if (n == "units") return g_stats.units;
     if (n == "tile_n") return g_stats.tile_n;
+    if (n == "tile_n2") return g_stats.tile_n2;
+    if (n == "n_wide") return g_stats.n_wide;
     if (n == "grid") return g_stats.grid;
     if (n == "launches") return g_stats.launches;
     if (n == "kernel_ns") return g_stats.kernel_ns;
@@ -575,16 +623,15 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             const int max_clusters = tc_dseq_pair_max_clusters(256);
             if (max_clusters < 1) return fail(DSEQ_ELAUNCH, "no CTA pair of the pair kernel fits on this device");
             grid_cap = std::max(2, std::min(grid_cap / 2, max_clusters) * 2);
-            plan.tile_n = ctx->opt.tile_n > 0 ? (int)ctx->opt.tile_n
-                                              : choose_tile_n(plan.n_beta / 2, N, grid_cap / 2);
-            plan.n_chunk = (int)((N + plan.tile_n - 1) / plan.tile_n);
+            choose_widths(plan, plan.n_beta / 2, N, grid_cap / 2, ctx->opt.storage == 1,
+                          (int)ctx->opt.tile_n, (int)ctx->opt.tile_n2);
             plan.grid = 2 * (int)std::min<int64_t>(grid_cap / 2, (int64_t)(plan.n_beta / 2) * plan.n_chunk);
         } else {
-            plan.tile_n = ctx->opt.tile_n > 0 ? (int)ctx->opt.tile_n : choose_tile_n(plan.n_beta, N, grid_cap);
-            plan.n_chunk = (int)((N + plan.tile_n - 1) / plan.tile_n);
+            choose_widths(plan, plan.n_beta, N, grid_cap, ctx->opt.storage == 1,
+                          (int)ctx->opt.tile_n, (int)ctx->opt.tile_n2);
             plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
         }
-        TRY(ctx->m.ensure((size_t)plan.units() * kUnitRows * plan.tile_n * sizeof(float)));
+        TRY(ctx->m.ensure((size_t)plan.n_beta * kUnitRows * plan.columns() * sizeof(float)));
         // split storage: queries [hi*2^12 | hi | lo], table [hi | lo];
         // fp16 storage: one fp16 part each, plus inverse norms
         const bool f16 = ctx->opt.storage == 1;
@@ -657,6 +704,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         TRY(timer.stop(st));
         g_stats.units = plan.units();
         g_stats.tile_n = plan.tile_n;
+        g_stats.tile_n2 = plan.tile_n2;
+        g_stats.n_wide = plan.n_wide;
         g_stats.grid = plan.grid;
         g_stats.launches = 2;
     } else {
@@ -809,8 +858,7 @@ int bmu_core(const float *dX, int64_t n, const float *dW, int64_t M, int32_t D, 
         plan.n_beta = (int)((n + kUnitRows - 1) / kUnitRows);
         if (plan.pair) plan.n_beta += plan.n_beta & 1;  // whole pairs of sample blocks
         int grid_cap = opt.grid > 0 ? (int)std::min<int64_t>(opt.grid, info.sms) : info.sms;
-        plan.tile_n = opt.tile_n > 0 ? (int)opt.tile_n : 256;
-        plan.n_chunk = (int)((M + plan.tile_n - 1) / plan.tile_n);
+        plan.set_uniform(opt.tile_n > 0 ? (int)opt.tile_n : 256, M);
         if (plan.pair) {
             grid_cap = std::max(2, grid_cap / 2 * 2);
             plan.grid = 2 * (int)std::min<int64_t>(grid_cap / 2, plan.units() / 2);

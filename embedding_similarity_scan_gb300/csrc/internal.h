@@ -39,30 +39,56 @@ __host__ __device__ constexpr uint32_t tc_smem_bytes() {
     return kStages * (tc_stage_bytes_a() + tc_stage_bytes_b_max()) + 1024u /*align*/ + 256u;
 }
 
-// Layout of the running-minimum array of the tensor-core path.  Work unit u
-// (sequence block beta, candidate chunk j, u = j * n_beta + beta) owns a
-// contiguous tile of 128 x tile_n floats.  Inside a tile, element (row r,
-// column c) with r = 32 q + t (TMEM lane quadrant q, lane t) and
-// c = 32 g + 4 v + e sits at ((((g * 4 + q) * 8 + v) * 32 + t) * 4 + e), so
-// each warp's 16-byte accesses of one column group are 512 contiguous bytes.
-__host__ __device__ __forceinline__ int64_t tc_m_offset(int64_t unit, int tile_n, int r, int c) {
+// Layout of the running-minimum array of the tensor-core path.  Candidate
+// chunk j covers columns [col0(j), col0(j) + width(j)) (see TcPlan); the
+// tiles of one chunk are contiguous, sequence block after sequence block, and
+// work unit (beta, j) owns a tile of 128 x width(j) floats.  Inside a tile,
+// element (row r, column c) with r = 32 q + t (TMEM lane quadrant q, lane t)
+// and c = 32 g + 4 v + e sits at ((((g * 4 + q) * 8 + v) * 32 + t) * 4 + e),
+// so each warp's 16-byte accesses of one column group are 512 contiguous bytes.
+__host__ __device__ __forceinline__ int64_t tc_m_inner(int r, int c) {
     const int q = r >> 5, t = r & 31, g = c >> 5, v = (c >> 2) & 7, e = c & 3;
-    return unit * (int64_t)(kUnitRows * tile_n) + ((((g * 4 + q) * 8 + v) * 32 + t) * 4 + e);
+    return ((((g * 4 + q) * 8 + v) * 32 + t) * 4 + e);
 }
 
 // Phase stamps per CTA and iteration of the persistent diversity kernel:
 // 0 iteration start, 1 first TMA issued, 2 first MMA issued, 3 last MMA
 // committed, 4 epilogue done (first epilogue warp), 5 after the first grid
-// barrier, 6 after the commit (CTA thread 0), 7 after the second grid barrier.
-constexpr int kTimelineSlots = 8;
+// barrier, 6 after the commit (CTA thread 0), 7 after the second grid barrier;
+// then nanoseconds spent waiting during the iteration: 8 MMA issuer on
+// filled stages, 9 MMA issuer on a free accumulator, 10 producer on a free
+// stage, 11 first epilogue warp on a finished accumulator.
+constexpr int kTimelineSlots = 12;
 
 struct TcPlan {
     int n_beta;    // sequence blocks (ceil(B / 128))
-    int n_chunk;   // candidate chunks (ceil(N / tile_n))
-    int tile_n;    // candidate columns per unit
+    int n_chunk;   // candidate chunks
+    int tile_n;    // candidate columns of the wide chunks (the TMA box)
     int grid;      // persistent CTAs (pair mode: even, two CTAs per cluster)
     int pair;      // 1: CTA pairs share each MMA (cta_group::2), n_beta even
+    // chunks j < n_wide are tile_n columns wide, the others tile_n2 <= tile_n
+    // (a uniform plan has n_wide = n_chunk, tile_n2 = tile_n)
+    int n_wide;
+    int tile_n2;
     __host__ __device__ int64_t units() const { return (int64_t)n_beta * n_chunk; }
+    __host__ __device__ int width(int j) const { return j < n_wide ? tile_n : tile_n2; }
+    __host__ __device__ int64_t col0(int j) const {
+        return j <= n_wide ? (int64_t)j * tile_n
+                           : (int64_t)n_wide * tile_n + (int64_t)(j - n_wide) * tile_n2;
+    }
+    __host__ __device__ int64_t columns() const { return col0(n_chunk); }
+    __host__ __device__ int chunk_of(int64_t c) const {
+        const int64_t wide = (int64_t)n_wide * tile_n;
+        return c < wide ? (int)(c / tile_n) : n_wide + (int)((c - wide) / tile_n2);
+    }
+    // float offset of the running-minimum tile of unit (beta, j)
+    __host__ __device__ int64_t tile_base(int j, int beta) const {
+        return (col0(j) * n_beta + (int64_t)beta * width(j)) * kUnitRows;
+    }
+    __host__ __device__ void set_uniform(int tn, int64_t ncols) {
+        tile_n = tile_n2 = tn;
+        n_chunk = n_wide = (int)((ncols + tn - 1) / tn);
+    }
 };
 
 // ---- table preparation (api.cu calls; prep.cu defines) ---------------------

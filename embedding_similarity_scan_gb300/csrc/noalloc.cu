@@ -129,8 +129,7 @@ extern "C" int bmu_search_noalloc(const float *X, int64_t n, const float *W, int
     if (e != cudaSuccess) return host::fail_msg(DSEQ_ECUDA, cudaGetErrorString(e));
     TcPlan plan{};
     plan.n_beta = (int)((n + kUnitRows - 1) / kUnitRows);
-    plan.tile_n = 256;
-    plan.n_chunk = (int)((M + plan.tile_n - 1) / plan.tile_n);
+    plan.set_uniform(256, M);
     plan.grid = (int)(plan.units() < sms ? plan.units() : sms);
     CUtensorMap tx, tw;
     if ((r = host::encode_map(tx, a.x_split, 3 * Dp, n, kUnitRows)) != DSEQ_OK) return r;

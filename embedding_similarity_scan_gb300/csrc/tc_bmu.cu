@@ -90,6 +90,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t tmo = a.timeout_ns;
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
+    // the launch must have the shape the kernel is written for (a pair kernel
+    // addresses its peer's shared memory and TMEM): otherwise report and leave,
+    // uniformly across the grid, before touching anything
+    if (blockDim.x != kTcThreads || (kPair && (cluster_nctarank() != 2u || (gridDim.x & 1u)))) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusInternal);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBmuStages; ++s) {

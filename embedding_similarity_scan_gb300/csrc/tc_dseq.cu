@@ -74,17 +74,19 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__restrict__ starts,
                                     const uint8_t *__restrict__ mask) {
-    const int64_t tile = (int64_t)kUnitRows * p.tile_n;
-    const int64_t total = p.units() * tile;
+    const int64_t per_col = (int64_t)p.n_beta * kUnitRows;  // floats per candidate column
+    const int64_t total = p.columns() * per_col;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t u = i / tile;
-        const int s = (int)(i - u * tile);
+        const int j = p.chunk_of(i / per_col);
+        const int64_t tile = (int64_t)kUnitRows * p.width(j);
+        const int64_t local = i - p.col0(j) * per_col;
+        const int beta = (int)(local / tile);
+        const int s = (int)(local - beta * tile);
         const int e = s & 3, t = (s >> 2) & 31, v = (s >> 7) & 7, q = (s >> 10) & 3, g = s >> 12;
         const int r = 32 * q + t, c = 32 * g + 4 * v + e;
-        const int beta = (int)(u % p.n_beta), j = (int)(u / p.n_beta);
         const int b = beta * kUnitRows + r;
-        const int64_t cand = (int64_t)j * p.tile_n + c;
+        const int64_t cand = p.col0(j) + c;
         bool live = b < a.B && cand < a.N;
         if (live && mask && mask[cand]) live = false;
         if (live && cand == starts[b]) live = false;
@@ -147,6 +149,20 @@ __device__ __forceinline__ void stamp(const TcDseqArgs &a, int t, int slot) {
     if (a.timeline)
         a.timeline[((size_t)t * gridDim.x + blockIdx.x) * kTimelineSlots + slot] = globaltimer_ns();
 }
+__device__ __forceinline__ void record(const TcDseqArgs &a, int t, int slot, uint64_t value) {
+    if (a.timeline) a.timeline[((size_t)t * gridDim.x + blockIdx.x) * kTimelineSlots + slot] = value;
+}
+// with the timeline on, adds the time a bounded wait took to *acc
+__device__ __forceinline__ bool timed_wait(const TcDseqArgs &a, uint64_t *bar, uint32_t parity,
+                                           volatile int *abort_flag, uint64_t tmo,
+                                           uint64_t &acc) {
+    if (!a.timeline)
+        return mbar_wait_bounded(bar, parity, abort_flag, a.status, tmo, kStatusPipeTimeout);
+    const uint64_t t0 = globaltimer_ns();
+    const bool ok = mbar_wait_bounded(bar, parity, abort_flag, a.status, tmo, kStatusPipeTimeout);
+    acc += globaltimer_ns() - t0;
+    return ok;
+}
 
 template <bool kPair, bool kF16, bool kCentroid>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -176,6 +192,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // full / acc_empty barriers that both CTAs feed)
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
+    // the launch must have the shape the kernel is written for (a pair kernel
+    // addresses its peer's shared memory and TMEM): otherwise report and leave,
+    // uniformly across the grid, before touching anything
+    if (blockDim.x != kTcThreads || (kPair && (cluster_nctarank() != 2u || (gridDim.x & 1u)))) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusInternal);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSt; ++s) {
@@ -216,8 +239,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sub_b = b_rows * kKBlock * 2;
     const uint32_t tx_bytes = (kPair ? 2u : 1u) * (kPartsA * kSubA + kPartsB * sub_b);
     const int kblocks = a.Dp / kKBlock;
-    const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kUnitRows : kUnitRows, tile_n);
-    const int groups = (int)(tile_n / 32);
+
     // work items: (sequence block, chunk) units, or (sequence block pair,
     // chunk) for a cluster; both ordered candidate-chunk-major
     const int n_pairs = p.n_beta / 2;
@@ -250,15 +272,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint64_t keep = l2_policy_evict_last();
                 const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
                 bool first = true;
+                uint64_t waited = 0;
                 for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride) {
                     int beta, j;
                     decode(v, beta, j);
                     const int yq = beta * kUnitRows;
-                    const int ye = j * (int)tile_n + (int)(rank * b_rows);
+                    // a narrow chunk still loads a full box (its tail rows unused)
+                    const int ye = (int)p.col0(j) + (int)rank * (p.width(j) / (kPair ? 2 : 1));
                     for (int kb = 0; kb < kblocks; ++kb) {
                         const uint32_t s = fills % kSt, par = (fills / kSt) & 1u;
-                        if (!mbar_wait_bounded(&empty[s], par ^ 1u, abort_flag, a.status, tmo,
-                                               kStatusPipeTimeout))
+                        if (!timed_wait(a, &empty[s], par ^ 1u, abort_flag, tmo, waited))
                             break;
                         uint8_t *sa = smem + s * kStageB;
                         uint8_t *sb = sa + kPartsA * kSubA;
@@ -291,24 +314,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ++fills;
                     }
                 }
+                record(a, t, 10, waited);
             }
             __syncwarp();
         } else if (warp == 1) {
             // ---------------- MMA issuer (pair: the leader only) ----------------
             if (lane == 0 && leader) {
                 bool first = true;
+                uint64_t wait_full = 0, wait_acc = 0;
                 for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride) {
                     const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
-                    if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
-                                           kStatusPipeTimeout))
+                    int beta_u, j_u;
+                    decode(v, beta_u, j_u);
+                    const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kUnitRows : kUnitRows,
+                                                         (uint32_t)p.width(j_u));
+                    if (!timed_wait(a, &acc_empty[buf], apar ^ 1u, abort_flag, tmo, wait_acc))
                         break;
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kAccCols;
                     bool ok = true;
                     for (int kb = 0; kb < kblocks; ++kb) {
                         const uint32_t s = consumed % kSt, par = (consumed / kSt) & 1u;
-                        if (!mbar_wait_bounded(&full[s], par, abort_flag, a.status, tmo,
-                                               kStatusPipeTimeout)) {
+                        if (!timed_wait(a, &full[s], par, abort_flag, tmo, wait_full)) {
                             ok = false;
                             break;
                         }
@@ -358,6 +385,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ++acc_uses;
                 }
                 stamp(a, t, 3);
+                record(a, t, 8, wait_full);
+                record(a, t, 9, wait_acc);
             }
             __syncwarp();
         } else {
@@ -367,12 +396,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t stream = l2_policy_evict_first();
             // the leader's acc_empty barriers collect both CTAs' epilogue warps
             const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+            uint64_t epi_wait = 0;
             for (int64_t v = first_item; v < work; v += item_stride) {
                 const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
                 int beta, j;
                 decode(v, beta, j);
-                const int64_t u = (int64_t)j * p.n_beta + beta;  // running-minimum tile
-                float4 *mt = reinterpret_cast<float4 *>(a.m + u * (int64_t)(kUnitRows * tile_n));
+                const int groups = p.width(j) / 32;
+                const int64_t c0 = p.col0(j);
+                float4 *mt = reinterpret_cast<float4 *>(a.m + p.tile_base(j, beta));
                 // prefetch the first group's running minima before waiting
                 float4 mcur[8], mnext[8];
                 if (h < groups) {
@@ -381,8 +412,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mcur[v] = ld_cg_hint(&mt[((h * 4 + q) * 8 + v) * 32 + lane], stream);
                 }
                 // every lane waits; the warp proceeds only if all of them saw the phase
-                const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status,
-                                                     tmo, kStatusPipeTimeout);
+                const bool ready = timed_wait(a, &acc_full[buf], apar, abort_flag, tmo, epi_wait);
                 if (!__all_sync(0xffffffffu, ready)) break;
                 tc_fence_after();
                 float best = -INFINITY;
@@ -394,7 +424,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float *my_rn = col_rn + e * 32;
                 for (int g = h; g < groups; g += 2) {
                     if (kF16) {
-                        const int64_t col = (int64_t)j * tile_n + 32 * g + lane;
+                        const int64_t col = c0 + 32 * g + lane;
                         __syncwarp();
                         my_rn[lane] = col < a.N ? a.rn[col] : 0.0f;
                         __syncwarp();
@@ -408,7 +438,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float acc[32];
                     tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
                     tmem_wait_ld();
-                    const uint32_t cbase = (uint32_t)j * tile_n + 32u * (uint32_t)g;
+                    const uint32_t cbase = (uint32_t)c0 + 32u * (uint32_t)g;
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
                         float mv[4] = {mcur[v].x, mcur[v].y, mcur[v].z, mcur[v].w};
@@ -457,7 +487,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int b = beta * kUnitRows + r;
                 if (best > -INFINITY && b < a.B) atomicMax(a.keys + b, max_key(best, best_c));
             }
-            if (warp == 2 && lane == 0) stamp(a, t, 4);
+            if (warp == 2 && lane == 0) {
+                stamp(a, t, 4);
+                record(a, t, 11, epi_wait);
+            }
         }
 
         // ---- all partial winners of iteration t are in the keys ----
@@ -498,16 +531,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int beta = bi / kUnitRows, r = bi % kUnitRows;
                         float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
                         for (int64_t c = lane; c < a.N; c += 32) {
-                            const int jj = (int)(c / tile_n), cc = (int)(c - (int64_t)jj * tile_n);
-                            dst[c] = __ldcg(a.m + tc_m_offset((int64_t)jj * p.n_beta + beta, tile_n, r, cc));
+                            const int jj = p.chunk_of(c);
+                            const int cc = (int)(c - p.col0(jj));
+                            dst[c] = __ldcg(a.m + p.tile_base(jj, beta) + tc_m_inner(r, cc));
                         }
                     }
                     __syncwarp();
                 }
                 if (mine && key != 0ull) {
                     const int beta = b / kUnitRows, r = b % kUnitRows;
-                    const int jw = (int)(w / tile_n), cw = (int)(w - (uint32_t)jw * tile_n);
-                    a.m[tc_m_offset((int64_t)jw * p.n_beta + beta, tile_n, r, cw)] = -INFINITY;
+                    const int jw = p.chunk_of(w);
+                    const int cw = (int)(w - p.col0(jw));
+                    a.m[p.tile_base(jw, beta) + tc_m_inner(r, cw)] = -INFINITY;
                 }
                 // next queries: the split rows of the winners, all rows of the run
                 // copied by the whole warp, loads first (read-only path)

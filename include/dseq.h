@@ -114,11 +114,14 @@ int dseq_run_trace(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
                    int32_t n_trace, float *trace_mindist, void *cuda_stream);
 
 /* Phase timestamps of the last dseq_run on ctx made with the "timeline"
- * option on (tensor-core path).  out receives iters x grid x 8 int64
- * nanosecond stamps (%globaltimer): per iteration and CTA, 0 iteration start,
- * 1 first TMA issued, 2 first MMA issued, 3 last MMA committed, 4 epilogue
- * done, 5 after the first grid barrier, 6 commit done, 7 after the second
- * grid barrier.  *iters and *grid receive the dimensions (0 when no timeline
+ * option on (tensor-core path).  out receives iters x grid x 12 int64
+ * values: per iteration and CTA, nanosecond stamps (%globaltimer) 0 iteration
+ * start, 1 first TMA issued, 2 first MMA issued, 3 last MMA committed,
+ * 4 epilogue done, 5 after the first grid barrier, 6 commit done, 7 after the
+ * second grid barrier; then nanoseconds spent waiting in the iteration:
+ * 8 MMA issuer for filled stages, 9 MMA issuer for a free accumulator,
+ * 10 producer for a free stage, 11 epilogue for a finished accumulator
+ * (slots 2, 3, 8 and 9 only on CTAs that issue MMAs).  *iters and *grid receive the dimensions (0 when no timeline
  * was recorded); capacity is the length of out in elements; out = NULL only
  * queries the dimensions.
  * Errors: DSEQ_EINVAL (NULL ctx/iters/grid, capacity too small), DSEQ_ECUDA. */
@@ -206,6 +209,11 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *   "engine"      0 = tensor-core path (default), 1 = FP32 FFMA path.
  *   "tile_n"      candidate (or neuron) columns per work unit, a multiple of
  *                 32 in [32, 256]; 0 = chosen from the shape (default).
+ *                 Alone it fixes every diversity chunk to that width.
+ *   "tile_n2"     diversity path: width of the narrower chunks that follow
+ *                 the tile_n-wide ones (a multiple of 32, <= tile_n); 0 =
+ *                 chosen with tile_n (default).  Mixing two widths balances
+ *                 the work units over the SMs without narrowing every MMA.
  *   "grid"        persistent CTAs; 0 = one per SM (default).
  *   "timeout_ms"  limit of every device-side wait (default 10000).
  *   "resume"      1 = dseq_run continues the last successful run on this
@@ -249,7 +257,8 @@ int64_t dseq_get_option(dseq_ctx *ctx, const char *name);
  * som_epoch on this thread:
  *   "units"        work units (sequence block x candidate chunk) per iteration;
  *                  neurons for som_update,
- *   "tile_n"       candidate columns per unit,
+ *   "tile_n"       candidate columns per (wide) unit, "tile_n2" of the narrow
+ *                  units, "n_wide" the number of wide chunks (diversity path),
  *   "grid"         CTAs launched,
  *   "launches"     kernels launched by the call,
  *   "kernel_ns"    device time of the main kernel (CUDA events; 0 if unknown),

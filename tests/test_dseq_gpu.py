@@ -31,17 +31,18 @@ def es():
 @pytest.fixture(autouse=True)
 def _reset_options(es):
     yield
-    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("timeout_ms", 10000),
+    for name, v in (("engine", 0), ("tile_n", 0), ("tile_n2", 0), ("grid", 0), ("timeout_ms", 10000),
                     ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR), ("storage", 0),
                     ("criterion", 0), ("resume", 0)):
         es.dseq_set_option(name, v)
 
 
 def _run(es, E, starts, L, mask=None, trace_seqs=None, engine=0, tile_n=0, grid=0,
-         pair=None, storage=0, criterion=0):
+         pair=None, storage=0, criterion=0, tile_n2=0):
     dev = torch.device("cuda")
     es.dseq_set_option("engine", engine)
     es.dseq_set_option("tile_n", tile_n)
+    es.dseq_set_option("tile_n2", tile_n2)
     es.dseq_set_option("grid", grid)
     es.dseq_set_option("pair", DEFAULT_PAIR if pair is None else pair)
     es.dseq_set_option("storage", storage)
@@ -112,6 +113,28 @@ def test_picks_identical_across_candidate_tiles(es):
         assert np.array_equal(tr, ref_tr), f"pair mode, tile_n={tn} changes the running minima"
     got, _ = _run(es, E, starts, L, grid=6, pair=1)
     assert np.array_equal(got, ref), "pair mode with 3 clusters changes the picks"
+    # two chunk widths (wide chunks, then narrow ones)
+    for tn, tn2, pair in ((256, 192, 1), (256, 64, 1), (224, 32, 0), (128, 96, 0)):
+        got, tr = _run(es, E, starts, L, trace_seqs=[0, 7, 299], tile_n=tn, tile_n2=tn2,
+                       pair=pair)
+        assert es.dseq_last_stat("tile_n2") == tn2 or es.dseq_last_stat("n_wide") > 0
+        assert np.array_equal(got, ref), f"widths {tn}/{tn2} (pair {pair}) change the picks"
+        assert np.array_equal(tr, ref_tr), f"widths {tn}/{tn2} change the running minima"
+
+
+@pytest.mark.parametrize("pair", [1, 0])
+def test_mixed_widths_teacher_forced(es, pair):
+    """The default plan at a page-1-like width mix, against the oracle, with a
+    mask and a ragged last chunk."""
+    N, D, B, L = 2085, 96, 700, 20
+    E = workloads.clustered_table(N, D, n_centres=12, seed=5)
+    starts = workloads.starts(N, B, seed=5)
+    mask = (np.random.default_rng(5).random(N) < 0.1).astype(np.uint8)
+    mask[starts] = 0
+    tr = np.array([0, 1, 255, 256, 699], np.int32)
+    picks, trace = _run(es, E, starts, L, mask, tr, tile_n=256, tile_n2=96, pair=pair)
+    check_picks_valid(starts, mask, picks, N)
+    check_dseq_teacher_forced(E, starts, mask, picks, trace, tr)
 
 
 def test_exhaustion_boundary(es):
