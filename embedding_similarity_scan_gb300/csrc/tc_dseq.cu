@@ -50,6 +50,8 @@ namespace {
 constexpr uint32_t kSubA = kUnitRows * kKBlock * 2;  // one 128 x 32 fp16 sub-tile: 8 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
+// column groups of 32 in the widest unit (256 columns)
+constexpr int kMaxGroups = 8;
 
 // Stage geometry.  Split storage (fp32-accurate): A = 3 x (128 x 32),
 // B = 2 x (rows x 32) fp16; fp16 storage: one part each.  One CTA stages up
@@ -64,7 +66,8 @@ struct DseqCfg {
     static constexpr int kStagesT = kF16 ? (kPair ? 12 : 9) : (kPair ? 5 : kStages);
     // + alignment slack, barriers and flags, per-warp column norms (fp16 storage)
     static constexpr size_t kSmemBytes =
-        (size_t)kStagesT * kStage + 1024 + 256 + (kF16 ? kEpiWarps * 32 * sizeof(float) : 0);
+        (size_t)kStagesT * kStage + 1024 + 256 +
+        (kF16 ? kEpiWarps * (kMaxGroups / 2) * 32 * sizeof(float) : 0);
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -411,6 +414,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int v = 0; v < 8; ++v)
                         mcur[v] = ld_cg_hint(&mt[((h * 4 + q) * 8 + v) * 32 + lane], stream);
                 }
+                // fp16 storage: d = 1 - acc * rn_q * rn_c with the rows' inverse
+                // norms; this warp's (at most 4) column groups' norms are
+                // fetched before the wait too
+                float neg_rnq = 0.0f, rnv[kMaxGroups / 2];
+                if (kF16) {
+                    neg_rnq = -a.q_rn[beta * kUnitRows + r];
+#pragma unroll
+                    for (int k = 0; k < kMaxGroups / 2; ++k) {
+                        const int64_t col = c0 + 32 * (h + 2 * k) + lane;
+                        rnv[k] = (h + 2 * k < groups && col < a.N) ? __ldg(a.rn + col) : 0.0f;
+                    }
+                }
                 // every lane waits; the warp proceeds only if all of them saw the phase
                 const bool ready = timed_wait(a, &acc_full[buf], apar, abort_flag, tmo, epi_wait);
                 if (!__all_sync(0xffffffffu, ready)) break;
@@ -418,17 +433,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float best = -INFINITY;
                 uint32_t best_c = 0;
                 const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
-                // fp16 storage: d = 1 - acc * rn_q * rn_c with the rows' inverse norms
-                const int brow = beta * kUnitRows + r;
-                const float neg_rnq = kF16 ? -a.q_rn[brow] : 0.0f;
-                float *my_rn = col_rn + e * 32;
+                float *my_rn = col_rn + e * (kMaxGroups / 2) * 32;
+                if (kF16) {
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < kMaxGroups / 2; ++k) my_rn[k * 32 + lane] = rnv[k];
+                    __syncwarp();
+                }
                 for (int g = h; g < groups; g += 2) {
-                    if (kF16) {
-                        const int64_t col = c0 + 32 * g + lane;
-                        __syncwarp();
-                        my_rn[lane] = col < a.N ? a.rn[col] : 0.0f;
-                        __syncwarp();
-                    }
+                    const float *rn_g = my_rn + ((g - h) >> 1) * 32;
                     const int gn = g + 2;
                     if (gn < groups) {
 #pragma unroll
@@ -451,7 +464,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             // split storage: d = 1 - <q, e>, the accumulator holding
                             // 2^12 <q, e> of unit rows
                             const float d =
-                                kF16 ? fmaf(acc[4 * v + z] * my_rn[4 * v + z], neg_rnq, 1.0f)
+                                kF16 ? fmaf(acc[4 * v + z] * rn_g[4 * v + z], neg_rnq, 1.0f)
                                      : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
                             const float nv = kCentroid ? (mv[z] == -INFINITY ? -INFINITY : d)
                                                        : fminf(mv[z], d);
