@@ -603,7 +603,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         d_picks = ctx->picks.as<int32_t>();
     }
     TRY(ctx->keys.ensure((size_t)Bp * sizeof(unsigned long long)));
-    TRY(ctx->barrier.ensure(sizeof(unsigned)));
+    // grid barrier counter, then the overlapped kernels' done[2] and committed[2]
+    TRY(ctx->barrier.ensure(8 * sizeof(unsigned)));
     CUDA_TRY(cudaMemsetAsync(ctx->status.p, 0, sizeof(int), st));
 
     DeviceInfo info;
@@ -695,7 +696,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             ctx->timeline_iters = L;
             ctx->timeline_grid = plan.grid;
         }
-        CUDA_TRY(cudaMemsetAsync(ctx->barrier.p, 0, sizeof(unsigned), st));
+        CUDA_TRY(cudaMemsetAsync(ctx->barrier.p, 0, 8 * sizeof(unsigned), st));
         if (!resume) launch_tc_dseq_init(a, plan, ctx->starts.as<int32_t>(), d_mask, st);
         CUDA_TRY(cudaGetLastError());
         ctx->state_plan = plan;

@@ -362,6 +362,34 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
 // 1, ...) completes when it reaches (k + 1) * gridDim.x.  Every CTA calls it
 // with all its threads.  Returns false (and sets the abort flag) if the
 // status word is already set or the wait ran out.
+// Wait (acquire) until *counter >= target.  Gives up, setting the abort flag,
+// when another CTA reported an error or after timeout_ns (setting `code`).
+// With `waited`, adds the time spent waiting to it.
+__device__ __forceinline__ bool wait_counter(unsigned *counter, unsigned target, int *status,
+                                             volatile int *abort_flag, uint64_t timeout_ns,
+                                             int code, uint64_t *waited) {
+    // wrap-safe: counters may pass 2^32 on very long runs
+    if ((int)(ld_acquire_gpu(counter) - target) >= 0) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t spin = 0;; ++spin) {
+        if ((int)(ld_acquire_gpu(counter) - target) >= 0) {
+            if (waited) *waited += globaltimer_ns() - t0;
+            return true;
+        }
+        if (*abort_flag) return false;
+        if (ld_volatile(status) != 0) {
+            *abort_flag = 1;
+            return false;
+        }
+        if ((spin & 31u) == 31u && globaltimer_ns() - t0 > timeout_ns) {
+            atomicOr(status, code);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(32);
+    }
+}
+
 __device__ __forceinline__ bool grid_barrier(unsigned *counter, unsigned target, int *status,
                                              volatile int *abort_flag, uint64_t timeout_ns,
                                              bool skip_arrive) {
@@ -372,7 +400,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned *counter, unsigned target,
         if (!skip_arrive) red_release_gpu_add(counter, 1u);
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t spin = 0;; ++spin) {
-            if (ld_acquire_gpu(counter) >= target) break;
+            if ((int)(ld_acquire_gpu(counter) - target) >= 0) break;  // wrap-safe
             if (ld_volatile(status) != 0) {
                 *abort_flag = 1;
                 break;

@@ -167,12 +167,22 @@ __device__ __forceinline__ bool timed_wait(const TcDseqArgs &a, uint64_t *bar, u
     return ok;
 }
 
+// Max-min kernels overlap the commit of one half of the sequences with the
+// other half's units and add a commit warp; the centroid kernel, whose commit
+// is heavier, keeps one grid-wide phase per iteration.
+template <bool kCentroid>
+__host__ __device__ constexpr int dseq_threads() {
+    return kCentroid ? kTcThreads : kTcThreads + 32;
+}
+
 template <bool kPair, bool kF16, bool kCentroid>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     tc_dseq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
                    const TcPlan p) {
     using Cfg = DseqCfg<kPair, kF16>;
+    constexpr bool kOverlap = !kCentroid;
+    constexpr int kThreads = dseq_threads<kCentroid>();
     constexpr int kPartsA = Cfg::kPartsA, kPartsB = Cfg::kPartsB;
     constexpr int kSt = Cfg::kStagesT;
     constexpr uint32_t kSubB = Cfg::kSubB;
@@ -186,6 +196,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *final_bar = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(final_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // overlapped iterations: epilogue warps that finished each half, counted
+    unsigned *epi_arrive = reinterpret_cast<unsigned *>(tmem_slot + 2);
     // fp16 storage: per epilogue warp, the inverse norms of its 32 columns
     float *col_rn = reinterpret_cast<float *>(smem + kSt * kStageB + 256);
 
@@ -198,7 +210,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the launch must have the shape the kernel is written for (a pair kernel
     // addresses its peer's shared memory and TMEM): otherwise report and leave,
     // uniformly across the grid, before touching anything
-    if (blockDim.x != kTcThreads || (kPair && (cluster_nctarank() != 2u || (gridDim.x & 1u)))) {
+    if (blockDim.x != kThreads || (kPair && (cluster_nctarank() != 2u || (gridDim.x & 1u)))) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusInternal);
         return;
     }
@@ -214,6 +226,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
+        epi_arrive[0] = epi_arrive[1] = 0u;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -244,421 +257,589 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int kblocks = a.Dp / kKBlock;
 
     // work items: (sequence block, chunk) units, or (sequence block pair,
-    // chunk) for a cluster; both ordered candidate-chunk-major
-    const int n_pairs = p.n_beta / 2;
-    const int64_t work = kPair ? (int64_t)n_pairs * p.n_chunk : p.units();
+    // chunk) for a cluster.  Overlapped kernels split the blocks into two
+    // halves and order each iteration's items [half 0][half 1], each half
+    // candidate-chunk-major; the centroid kernel has one half.
+    const int n_blocks = kPair ? p.n_beta / 2 : p.n_beta;
+    const int n_h0 = kOverlap ? (n_blocks + 1) / 2 : n_blocks;
+    const int n_h1 = n_blocks - n_h0;
+    const int64_t work = (int64_t)n_blocks * p.n_chunk;
+    const int64_t half_units = (int64_t)n_h0 * p.n_chunk;
+    const int rows_per_block = kPair ? 2 * kUnitRows : kUnitRows;
+    const int seq_half[3] = {0, n_h0 * rows_per_block, n_blocks * rows_per_block};
     const int64_t first_item = kPair ? (blockIdx.x >> 1) : blockIdx.x;
     const int64_t item_stride = kPair ? (gridDim.x >> 1) : gridDim.x;
     auto decode = [&](int64_t v, int &beta, int &j) {
-        if (kPair) {
-            beta = 2 * (int)(v % n_pairs) + (int)rank;
-            j = (int)(v / n_pairs);
+        int blk;
+        if (v < half_units) {
+            blk = (int)(v % n_h0);
+            j = (int)(v / n_h0);
         } else {
-            beta = (int)(v % p.n_beta);
-            j = (int)(v / p.n_beta);
+            const int64_t k = v - half_units;
+            blk = n_h0 + (int)(k % n_h1);
+            j = (int)(k / n_h1);
         }
+        beta = kPair ? 2 * blk + (int)rank : blk;
     };
 
     uint32_t fills = 0;     // producer: stages filled so far
     uint32_t consumed = 0;  // MMA: stages consumed so far
     uint32_t acc_uses = 0;  // MMA and epilogue: accumulators used so far
-    unsigned barrier_no = 0;
-    bool skip_arrive = a.fault_skip_arrive && blockIdx.x == 0;
 
-    for (int t = 0; t < a.L; ++t) {
-        if (*abort_flag) break;
-        if (threadIdx.x == 0) stamp(a, t, 0);
+    // ---- per-unit work, shared by both iteration schemes ----
+    // producer: the kblocks stages of unit v
+    auto produce_unit = [&](int t, int64_t v, uint64_t keep, uint64_t table_pol, uint64_t &waited,
+                            bool &first) {
+        int beta, j;
+        decode(v, beta, j);
+        const int yq = beta * kUnitRows;
+        // a narrow chunk still loads a full box (its tail rows unused)
+        const int ye = (int)p.col0(j) + (int)rank * (p.width(j) / (kPair ? 2 : 1));
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const uint32_t s = fills % kSt, par = (fills / kSt) & 1u;
+            if (!timed_wait(a, &empty[s], par ^ 1u, abort_flag, tmo, waited))
+                break;
+            uint8_t *sa = smem + s * kStageB;
+            uint8_t *sb = sa + kPartsA * kSubA;
+            if (leader) mbar_arrive_expect_tx(&full[s], tx_bytes);
+            if (first) {
+                stamp(a, t, 1);
+                first = false;
+            }
+            const int x = kb * kKBlock;
+            // completion goes to the pair leader's barrier for this stage
+            const uint32_t fb = kPair ? mapa_shared(smem_u32(&full[s]), 0) : 0u;
+#pragma unroll
+            for (int part = 0; part < kPartsA; ++part) {  // (hi*2^12, hi, lo) or fp16
+                if (kPair)
+                    tma_load_2d_pair(sa + part * kSubA, &tmap_q, fb,
+                                     part * a.Dp + x, yq, keep);
+                else
+                    tma_load_2d_hint(sa + part * kSubA, &tmap_q, &full[s],
+                                     part * a.Dp + x, yq, keep);
+            }
+#pragma unroll
+            for (int part = 0; part < kPartsB; ++part) {  // (hi, lo) or fp16
+                if (kPair)
+                    tma_load_2d_pair(sb + part * kSubB, &tmap_e, fb,
+                                     part * a.Dp + x, ye, table_pol);
+                else
+                    tma_load_2d_hint(sb + part * kSubB, &tmap_e, &full[s],
+                                     part * a.Dp + x, ye, table_pol);
+            }
+            ++fills;
+        }
+    };
+    // MMA issuer: the unit's kblocks stages into one accumulator; false on abort
+    auto mma_unit = [&](int t, int64_t v, uint64_t &wait_full, uint64_t &wait_acc,
+                        bool &first) -> bool {
+        const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+        int beta_u, j_u;
+        decode(v, beta_u, j_u);
+        const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kUnitRows : kUnitRows,
+                                             (uint32_t)p.width(j_u));
+        if (!timed_wait(a, &acc_empty[buf], apar ^ 1u, abort_flag, tmo, wait_acc))
+            return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kAccCols;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const uint32_t s = consumed % kSt, par = (consumed / kSt) & 1u;
+            if (!timed_wait(a, &full[s], par, abort_flag, tmo, wait_full)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (first) {
+                stamp(a, t, 2);
+                first = false;
+            }
+            const uint32_t sa = smem_u32(smem + s * kStageB);
+            const uint32_t sb = sa + kPartsA * kSubA;
+#pragma unroll
+            for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
+                const uint32_t off = k16 * 32;  // 16 fp16 = 32 bytes along K
+                const uint64_t a0 = smem_desc_sw64(sa + off);
+                const uint64_t b0 = smem_desc_sw64(sb + off);
+                if (kF16) {  // one product: the stored fp16 rows
+                    if (kPair)
+                        umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                    else
+                        umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                    continue;
+                }
+                const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
+                const uint64_t a2 = smem_desc_sw64(sa + 2 * kSubA + off);
+                const uint64_t b1 = smem_desc_sw64(sb + kSubB + off);
+                if (kPair) {
+                    umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                    umma_f16_pair(d_tmem, a1, b1, idesc, 1u);
+                    umma_f16_pair(d_tmem, a2, b0, idesc, 1u);
+                } else {
+                    umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                    umma_f16(d_tmem, a1, b1, idesc, 1u);
+                    umma_f16(d_tmem, a2, b0, idesc, 1u);
+                }
+            }
+            if (kPair)
+                umma_commit_pair_multicast(&empty[s], 0x3);
+            else
+                umma_commit(&empty[s]);
+            ++consumed;
+        }
+        if (!ok) return false;
+        if (kPair)
+            umma_commit_pair_multicast(&acc_full[buf], 0x3);
+        else
+            umma_commit(&acc_full[buf]);
+        ++acc_uses;
+        return true;
+    };
+    // epilogue warp: distances, running minima, row winners of unit v; false on abort
+    auto epilogue_unit = [&](int64_t v, uint64_t stream, uint32_t acc_empty_leader0,
+                             uint64_t &epi_wait) -> bool {
+        // two warps per TMEM lane quadrant q, each taking every other column group
+        const int e = warp - 2, q = warp & 3, h = e >> 2;
+        const int r = 32 * q + lane;
+        const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+        int beta, j;
+        decode(v, beta, j);
+        const int groups = p.width(j) / 32;
+        const int64_t c0 = p.col0(j);
+        float4 *mt = reinterpret_cast<float4 *>(a.m + p.tile_base(j, beta));
+        // prefetch the first group's running minima before waiting
+        float4 mcur[8], mnext[8];
+        if (h < groups) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                mcur[v] = ld_cg_hint(&mt[((h * 4 + q) * 8 + v) * 32 + lane], stream);
+        }
+        // fp16 storage: d = 1 - acc * rn_q * rn_c with the rows' inverse
+        // norms; this warp's (at most 4) column groups' norms are
+        // fetched before the wait too
+        float neg_rnq = 0.0f, rnv[kMaxGroups / 2];
+        if (kF16) {
+            neg_rnq = -a.q_rn[beta * kUnitRows + r];
+#pragma unroll
+            for (int k = 0; k < kMaxGroups / 2; ++k) {
+                const int64_t col = c0 + 32 * (h + 2 * k) + lane;
+                rnv[k] = (h + 2 * k < groups && col < a.N) ? __ldg(a.rn + col) : 0.0f;
+            }
+        }
+        // every lane waits; the warp proceeds only if all of them saw the phase
+        const bool ready = timed_wait(a, &acc_full[buf], apar, abort_flag, tmo, epi_wait);
+        if (!__all_sync(0xffffffffu, ready)) return false;
+        tc_fence_after();
+        float best = -INFINITY;
+        uint32_t best_c = 0;
+        const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+        float *my_rn = col_rn + e * (kMaxGroups / 2) * 32;
+        if (kF16) {
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < kMaxGroups / 2; ++k) my_rn[k * 32 + lane] = rnv[k];
+            __syncwarp();
+        }
+        for (int g = h; g < groups; g += 2) {
+            const float *rn_g = my_rn + ((g - h) >> 1) * 32;
+            const int gn = g + 2;
+            if (gn < groups) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    mnext[v] = ld_cg_hint(&mt[((gn * 4 + q) * 8 + v) * 32 + lane], stream);
+            }
+            float acc[32];
+            tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
+            tmem_wait_ld();
+            const uint32_t cbase = (uint32_t)c0 + 32u * (uint32_t)g;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                float mv[4] = {mcur[v].x, mcur[v].y, mcur[v].z, mcur[v].w};
+                bool changed = false;
+                // max-min: m keeps the running minimum.  Centroid: m is
+                // -inf for held / masked rows and this iteration's
+                // distance otherwise.
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    // split storage: d = 1 - <q, e>, the accumulator holding
+                    // 2^12 <q, e> of unit rows
+                    const float d =
+                        kF16 ? fmaf(acc[4 * v + z] * rn_g[4 * v + z], neg_rnq, 1.0f)
+                             : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
+                    const float nv = kCentroid ? (mv[z] == -INFINITY ? -INFINITY : d)
+                                               : fminf(mv[z], d);
+                    changed |= nv != mv[z];
+                    mv[z] = nv;
+                    if (mv[z] > best) {
+                        best = mv[z];
+                        best_c = cbase + 4 * v + z;
+                    }
+                }
+                // a candidate's running minimum changes with probability
+                // about 1/(t+1) after t picks: write back only what moved
+                // centroid: the next iteration needs only the -inf marks,
+                // so this iteration's distances are stored only for a trace
+                if (changed && (!kCentroid || a.trace_slot))
+                    st_cg_hint(&mt[((g * 4 + q) * 8 + v) * 32 + lane],
+                               make_float4(mv[0], mv[1], mv[2], mv[3]), stream);
+            }
+            if (gn < groups) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v) mcur[v] = mnext[v];
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (kPair)
+                mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
+            else
+                mbar_arrive(&acc_empty[buf]);
+        }
+        ++acc_uses;
+        const int b = beta * kUnitRows + r;
+        if (best > -INFINITY && b < a.B) atomicMax(a.keys + b, max_key(best, best_c));
+        return true;
+    };
+    // commit of sequences [b_lo, b_hi) of iteration t by one warp: picks, keys
+    // reset, winner masked, next queries written
+    auto commit_range = [&](int t, int b_lo, int b_hi) {
+        const int vec = a.Dp / 8;  // 16-byte vectors per row segment
+        for (int base = b_lo; base < b_hi; base += 32) {
+            const int cnt = min(32, b_hi - base);
+            const int b = base + lane;
+            const bool mine = lane < cnt;
+            const unsigned long long key = mine ? __ldcg(a.keys + b) : 0ull;
+            const uint32_t w = max_key_index(key);
+            if (mine) {
+                if (key == 0ull) {
+                    atomicOr(a.status, kStatusNoWinner);
+                    a.picks[(int64_t)b * a.L + t] = -1;
+                } else {
+                    a.keys[b] = 0ull;
+                    a.picks[(int64_t)b * a.L + t] = (int32_t)w;
+                }
+            }
+            if (a.trace_slot) {
+                // parity-check path: copy the traced rows of m before masking
+                for (int i = 0; i < cnt; ++i) {
+                    const int bi = base + i;
+                    const int slot = a.trace_slot[bi];
+                    if (slot < 0) continue;
+                    const int beta = bi / kUnitRows, r = bi % kUnitRows;
+                    float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
+                    for (int64_t c = lane; c < a.N; c += 32) {
+                        const int jj = p.chunk_of(c);
+                        const int cc = (int)(c - p.col0(jj));
+                        dst[c] = __ldcg(a.m + p.tile_base(jj, beta) + tc_m_inner(r, cc));
+                    }
+                }
+                __syncwarp();
+            }
+            if (mine && key != 0ull) {
+                const int beta = b / kUnitRows, r = b % kUnitRows;
+                const int jw = p.chunk_of(w);
+                const int cw = (int)(w - p.col0(jw));
+                a.m[p.tile_base(jw, beta) + tc_m_inner(r, cw)] = -INFINITY;
+            }
+            // next queries: the split rows of the winners, all rows of the run
+            // copied by the whole warp, loads first (read-only path)
+            const __half2 scale = __float2half2_rn(4096.0f);
+            for (int i = 0; i < cnt; ++i) {
+                const unsigned long long ki = __shfl_sync(0xffffffffu, key, i);
+                const uint32_t wi = __shfl_sync(0xffffffffu, w, i);
+                if (ki == 0ull) continue;
+                if (kCentroid) {
+                    // add the winner to the sequence's exact centroid sum,
+                    // then write the split unit centroid as the next query.
+                    // Sums stay below 2^62 units, so v 2^-62 lies in (-1, 1):
+                    // that fixed scaling gives the norm without overflow, and
+                    // its smallest nonzero square (2^-124) is a normal fp32.
+                    const int bq = base + i;
+                    long long *cs = a.csum + (int64_t)bq * a.Dp;
+                    const float *eu = a.e_unit + (int64_t)wi * a.Dp;
+                    const float nw = a.nrm[wi];
+                    const int F = a.csum_shift;
+                    float s1, s2;
+                    fixed_unscale(62, s1, s2);
+                    constexpr int kB = 8;  // loads in flight per lane
+                    KahanSum ss;
+                    for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
+                        long long v[kB];
+                        float x[kB];
+#pragma unroll
+                        for (int u = 0; u < kB; ++u) {
+                            const int k = k0 + 32 * u + lane;
+                            v[u] = k < a.Dp ? cs[k] : 0ll;
+                            x[u] = k < a.Dp ? __ldg(eu + k) : 0.0f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < kB; ++u) {
+                            const int k = k0 + 32 * u + lane;
+                            if (k < a.Dp) {
+                                v[u] += to_fixed(x[u] * nw, F);
+                                cs[k] = v[u];
+                                const float c = from_fixed(v[u], s1, s2);
+                                ss.add(c * c);
+                            }
+                        }
+                    }
+                    const float sum = warp_sum_f(ss.total());
+                    // a zero centroid gives a zero query: every distance is 1
+                    const float inv = sum > 0.0f ? 1.0f / sqrtf(sum) : 0.0f;
+                    __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
+                    __syncwarp();
+                    for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
+                        long long v[kB];
+#pragma unroll
+                        for (int u = 0; u < kB; ++u) {
+                            const int k = k0 + 32 * u + lane;
+                            v[u] = k < a.Dp ? cs[k] : 0ll;
+                        }
+#pragma unroll
+                        for (int u = 0; u < kB; ++u) {
+                            const int k = k0 + 32 * u + lane;
+                            if (k < a.Dp) {
+                                const float uval = from_fixed(v[u], s1, s2) * inv;
+                                const __half hi = __float2half_rn(uval);
+                                const __half lo =
+                                    __float2half_rn((uval - __half2float(hi)) * 4096.0f);
+                                qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
+                                qd[a.Dp + k] = hi;
+                                qd[2 * a.Dp + k] = lo;
+                            }
+                        }
+                    }
+                    continue;
+                }
+                if (kF16) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.e_f16 + (int64_t)wi * a.Dp);
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * a.Dp);
+                    for (int k = lane; k < vec; k += 32) dst[k] = __ldg(src + k);
+                    if (lane == 0) a.q_rn[base + i] = a.rn[wi];
+                    continue;
+                }
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(a.e_split + (int64_t)wi * 2 * a.Dp);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * 3 * a.Dp);
+#pragma unroll 4
+                for (int k = lane; k < vec; k += 32) {
+                    const uint4 hi = __ldg(src + k), lo = __ldg(src + vec + k);
+                    uint4 hi12 = hi;
+                    __half2 *h2 = reinterpret_cast<__half2 *>(&hi12);
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
+                    dst[k] = hi12;
+                    dst[vec + k] = hi;
+                    dst[2 * vec + k] = lo;
+                }
+            }
+        }
+    };
+    // this CTA's first work item at or after index lo
+    auto first_from = [&](int64_t lo) -> int64_t {
+        if (lo <= first_item) return first_item;
+        return first_item + (lo - first_item + item_stride - 1) / item_stride * item_stride;
+    };
+
+    if (!kOverlap) {
+        // ---- one grid-wide phase per iteration: all units, barrier, commit, barrier ----
+        unsigned barrier_no = 0;
+        bool skip_arrive = a.fault_skip_arrive && blockIdx.x == 0;
+        for (int t = 0; t < a.L; ++t) {
+            if (*abort_flag) break;
+            if (threadIdx.x == 0) stamp(a, t, 0);
+            if (warp == 0) {
+                // ---------------- TMA producer ----------------
+                if (lane == 0) {
+                    fence_proxy_async_global();
+                    const uint64_t keep = l2_policy_evict_last();
+                    const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
+                    bool first = true;
+                    uint64_t waited = 0;
+                    for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride)
+                        produce_unit(t, v, keep, table_pol, waited, first);
+                    record(a, t, 10, waited);
+                }
+                __syncwarp();
+            } else if (warp == 1) {
+                // ---------------- MMA issuer (pair: the leader only) ----------------
+                if (lane == 0 && leader) {
+                    bool first = true;
+                    uint64_t wait_full = 0, wait_acc = 0;
+                    for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride)
+                        if (!mma_unit(t, v, wait_full, wait_acc, first)) break;
+                    stamp(a, t, 3);
+                    record(a, t, 8, wait_full);
+                    record(a, t, 9, wait_acc);
+                }
+                __syncwarp();
+            } else {
+                // ---------------- epilogue ----------------
+                const uint64_t stream = l2_policy_evict_first();
+                // the leader's acc_empty barriers collect both CTAs' epilogue warps
+                const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+                uint64_t epi_wait = 0;
+                for (int64_t v = first_item; v < work; v += item_stride)
+                    if (!epilogue_unit(v, stream, acc_empty_leader0, epi_wait)) break;
+                if (warp == 2 && lane == 0) {
+                    stamp(a, t, 4);
+                    record(a, t, 11, epi_wait);
+                }
+            }
+
+            // ---- all partial winners of iteration t are in the keys ----
+            if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
+                              skip_arrive))
+                break;
+            skip_arrive = false;
+            if (threadIdx.x == 0) stamp(a, t, 5);
+
+            // ---- commit: each warp takes a contiguous run of sequences ----
+            {
+                const int nw = gridDim.x * (kThreads / 32);
+                const int gw = blockIdx.x * (kThreads / 32) + warp;
+                const int per = (a.B + nw - 1) / nw;
+                const int b_lo = gw * per, b_hi = min(a.B, b_lo + per);
+                commit_range(t, b_lo, b_hi);
+                fence_proxy_async_global();
+                if (threadIdx.x == 0) stamp(a, t, 6);
+            }
+
+            // ---- the next queries are written ----
+            if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
+                              false))
+                break;
+            if (threadIdx.x == 0) stamp(a, t, 7);
+        }
+    } else {
+        // ---- two halves of the sequence blocks, overlapped ----
+        // Each iteration's units are ordered [half 0][half 1].  Counters in
+        // global memory replace the grid barriers: done[h] counts CTAs whose
+        // epilogue finished half h of an iteration (every partial winner in
+        // the keys), committed[h] counts commit warps that committed it.  A
+        // commit warp commits half h of iteration t once done[h] reaches
+        // G (t + 1) while the other warps already compute the other half; the
+        // producer loads half h of iteration t + 1 once committed[h] reaches
+        // G (t + 1).  No CTA ever waits for the whole grid to go idle.
+        unsigned *done = a.barrier + 1, *committed = a.barrier + 3;
+        const unsigned G = gridDim.x;
+        const int64_t hb[3] = {0, half_units, work};
         if (warp == 0) {
             // ---------------- TMA producer ----------------
             if (lane == 0) {
-                fence_proxy_async_global();
                 const uint64_t keep = l2_policy_evict_last();
                 const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
-                bool first = true;
-                uint64_t waited = 0;
-                for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride) {
-                    int beta, j;
-                    decode(v, beta, j);
-                    const int yq = beta * kUnitRows;
-                    // a narrow chunk still loads a full box (its tail rows unused)
-                    const int ye = (int)p.col0(j) + (int)rank * (p.width(j) / (kPair ? 2 : 1));
-                    for (int kb = 0; kb < kblocks; ++kb) {
-                        const uint32_t s = fills % kSt, par = (fills / kSt) & 1u;
-                        if (!timed_wait(a, &empty[s], par ^ 1u, abort_flag, tmo, waited))
-                            break;
-                        uint8_t *sa = smem + s * kStageB;
-                        uint8_t *sb = sa + kPartsA * kSubA;
-                        if (leader) mbar_arrive_expect_tx(&full[s], tx_bytes);
-                        if (first) {
-                            stamp(a, t, 1);
-                            first = false;
+                for (int t = 0; t < a.L && !*abort_flag; ++t) {
+                    stamp(a, t, 0);
+                    bool first = true;
+                    uint64_t waited = 0, gate = 0;
+                    for (int h = 0; h < 2 && !*abort_flag; ++h) {
+                        if (t > 0) {
+                            // the queries of half h were committed for iteration t
+                            if (!wait_counter(committed + h, G * (unsigned)t, a.status, abort_flag,
+                                              tmo, kStatusBarrierTimeout, &gate))
+                                break;
+                            fence_proxy_async_global();
                         }
-                        const int x = kb * kKBlock;
-                        // completion goes to the pair leader's barrier for this stage
-                        const uint32_t fb = kPair ? mapa_shared(smem_u32(&full[s]), 0) : 0u;
-#pragma unroll
-                        for (int part = 0; part < kPartsA; ++part) {  // (hi*2^12, hi, lo) or fp16
-                            if (kPair)
-                                tma_load_2d_pair(sa + part * kSubA, &tmap_q, fb,
-                                                 part * a.Dp + x, yq, keep);
-                            else
-                                tma_load_2d_hint(sa + part * kSubA, &tmap_q, &full[s],
-                                                 part * a.Dp + x, yq, keep);
-                        }
-#pragma unroll
-                        for (int part = 0; part < kPartsB; ++part) {  // (hi, lo) or fp16
-                            if (kPair)
-                                tma_load_2d_pair(sb + part * kSubB, &tmap_e, fb,
-                                                 part * a.Dp + x, ye, table_pol);
-                            else
-                                tma_load_2d_hint(sb + part * kSubB, &tmap_e, &full[s],
-                                                 part * a.Dp + x, ye, table_pol);
-                        }
-                        ++fills;
+                        for (int64_t v = first_from(hb[h]); v < hb[h + 1] && !*abort_flag;
+                             v += item_stride)
+                            produce_unit(t, v, keep, table_pol, waited, first);
                     }
+                    record(a, t, 7, gate);
+                    record(a, t, 10, waited);
                 }
-                record(a, t, 10, waited);
             }
             __syncwarp();
         } else if (warp == 1) {
             // ---------------- MMA issuer (pair: the leader only) ----------------
             if (lane == 0 && leader) {
-                bool first = true;
-                uint64_t wait_full = 0, wait_acc = 0;
-                for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride) {
-                    const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
-                    int beta_u, j_u;
-                    decode(v, beta_u, j_u);
-                    const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kUnitRows : kUnitRows,
-                                                         (uint32_t)p.width(j_u));
-                    if (!timed_wait(a, &acc_empty[buf], apar ^ 1u, abort_flag, tmo, wait_acc))
-                        break;
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + buf * kAccCols;
-                    bool ok = true;
-                    for (int kb = 0; kb < kblocks; ++kb) {
-                        const uint32_t s = consumed % kSt, par = (consumed / kSt) & 1u;
-                        if (!timed_wait(a, &full[s], par, abort_flag, tmo, wait_full)) {
+                for (int t = 0; t < a.L && !*abort_flag; ++t) {
+                    bool first = true, ok = true;
+                    uint64_t wait_full = 0, wait_acc = 0;
+                    for (int64_t v = first_item; v < work && ok && !*abort_flag; v += item_stride)
+                        ok = mma_unit(t, v, wait_full, wait_acc, first);
+                    stamp(a, t, 3);
+                    record(a, t, 8, wait_full);
+                    record(a, t, 9, wait_acc);
+                    if (!ok) break;
+                }
+            }
+            __syncwarp();
+        } else if (warp < 2 + kEpiWarps) {
+            // ---------------- epilogue ----------------
+            const uint64_t stream = l2_policy_evict_first();
+            const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+            bool skip_arrive = a.fault_skip_arrive && blockIdx.x == 0;
+            bool ok = true;
+            for (int t = 0; t < a.L && ok; ++t) {
+                uint64_t epi_wait = 0;
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (t > 0) {
+                        // keys reset and winners masked for half h (the running
+                        // minima this warp reads next)
+                        int pass = 1;
+                        if (lane == 0)
+                            pass = wait_counter(committed + h, G * (unsigned)t, a.status,
+                                                abort_flag, tmo, kStatusBarrierTimeout, nullptr);
+                        if (!__shfl_sync(0xffffffffu, pass, 0)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        if (first) {
-                            stamp(a, t, 2);
-                            first = false;
-                        }
-                        const uint32_t sa = smem_u32(smem + s * kStageB);
-                        const uint32_t sb = sa + kPartsA * kSubA;
-#pragma unroll
-                        for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
-                            const uint32_t off = k16 * 32;  // 16 fp16 = 32 bytes along K
-                            const uint64_t a0 = smem_desc_sw64(sa + off);
-                            const uint64_t b0 = smem_desc_sw64(sb + off);
-                            if (kF16) {  // one product: the stored fp16 rows
-                                if (kPair)
-                                    umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                                else
-                                    umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                                continue;
-                            }
-                            const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
-                            const uint64_t a2 = smem_desc_sw64(sa + 2 * kSubA + off);
-                            const uint64_t b1 = smem_desc_sw64(sb + kSubB + off);
-                            if (kPair) {
-                                umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                                umma_f16_pair(d_tmem, a1, b1, idesc, 1u);
-                                umma_f16_pair(d_tmem, a2, b0, idesc, 1u);
-                            } else {
-                                umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                                umma_f16(d_tmem, a1, b1, idesc, 1u);
-                                umma_f16(d_tmem, a2, b0, idesc, 1u);
-                            }
-                        }
-                        if (kPair)
-                            umma_commit_pair_multicast(&empty[s], 0x3);
-                        else
-                            umma_commit(&empty[s]);
-                        ++consumed;
                     }
+                    for (int64_t v = first_from(hb[h]); v < hb[h + 1] && ok; v += item_stride)
+                        ok = epilogue_unit(v, stream, acc_empty_leader0, epi_wait);
                     if (!ok) break;
-                    if (kPair)
-                        umma_commit_pair_multicast(&acc_full[buf], 0x3);
-                    else
-                        umma_commit(&acc_full[buf]);
-                    ++acc_uses;
+                    // the last of this CTA's epilogue warps to finish half h
+                    // publishes it (every key atomic of the CTA before it)
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence();
+                        const unsigned old = atomicAdd(&epi_arrive[h], 1u);
+                        if (old % kEpiWarps == kEpiWarps - 1) {
+                            __threadfence();
+                            if (!skip_arrive) red_release_gpu_add(done + h, 1u);
+                            skip_arrive = false;
+                        }
+                    }
+                    __syncwarp();
                 }
-                stamp(a, t, 3);
-                record(a, t, 8, wait_full);
-                record(a, t, 9, wait_acc);
+                if (warp == 2 && lane == 0) {
+                    stamp(a, t, 4);
+                    record(a, t, 11, epi_wait);
+                }
             }
-            __syncwarp();
         } else {
-            // ---------------- epilogue ----------------
-            const int e = warp - 2, q = warp & 3, h = e >> 2;
-            const int r = 32 * q + lane;
-            const uint64_t stream = l2_policy_evict_first();
-            // the leader's acc_empty barriers collect both CTAs' epilogue warps
-            const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
-            uint64_t epi_wait = 0;
-            for (int64_t v = first_item; v < work; v += item_stride) {
-                const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
-                int beta, j;
-                decode(v, beta, j);
-                const int groups = p.width(j) / 32;
-                const int64_t c0 = p.col0(j);
-                float4 *mt = reinterpret_cast<float4 *>(a.m + p.tile_base(j, beta));
-                // prefetch the first group's running minima before waiting
-                float4 mcur[8], mnext[8];
-                if (h < groups) {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        mcur[v] = ld_cg_hint(&mt[((h * 4 + q) * 8 + v) * 32 + lane], stream);
-                }
-                // fp16 storage: d = 1 - acc * rn_q * rn_c with the rows' inverse
-                // norms; this warp's (at most 4) column groups' norms are
-                // fetched before the wait too
-                float neg_rnq = 0.0f, rnv[kMaxGroups / 2];
-                if (kF16) {
-                    neg_rnq = -a.q_rn[beta * kUnitRows + r];
-#pragma unroll
-                    for (int k = 0; k < kMaxGroups / 2; ++k) {
-                        const int64_t col = c0 + 32 * (h + 2 * k) + lane;
-                        rnv[k] = (h + 2 * k < groups && col < a.N) ? __ldg(a.rn + col) : 0.0f;
+            // ---------------- commit warp ----------------
+            for (int t = 0; t < a.L; ++t) {
+                bool ok = true;
+                for (int h = 0; h < 2; ++h) {
+                    int pass = 1;
+                    if (lane == 0)
+                        pass = wait_counter(done + h, G * (unsigned)(t + 1), a.status, abort_flag,
+                                            tmo, kStatusBarrierTimeout, nullptr);
+                    if (!__shfl_sync(0xffffffffu, pass, 0)) {
+                        ok = false;
+                        break;
                     }
-                }
-                // every lane waits; the warp proceeds only if all of them saw the phase
-                const bool ready = timed_wait(a, &acc_full[buf], apar, abort_flag, tmo, epi_wait);
-                if (!__all_sync(0xffffffffu, ready)) break;
-                tc_fence_after();
-                float best = -INFINITY;
-                uint32_t best_c = 0;
-                const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
-                float *my_rn = col_rn + e * (kMaxGroups / 2) * 32;
-                if (kF16) {
+                    // this CTA's share of the sequences of half h
+                    const int s_lo = min(a.B, seq_half[h]);
+                    const int s_hi = min(a.B, seq_half[h + 1]);
+                    const int per = (s_hi - s_lo + (int)G - 1) / (int)G;
+                    const int b_lo = min(s_hi, s_lo + (int)blockIdx.x * per);
+                    commit_range(t, b_lo, min(s_hi, b_lo + per));
+                    fence_proxy_async_global();
                     __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < kMaxGroups / 2; ++k) my_rn[k * 32 + lane] = rnv[k];
+                    if (lane == 0) {
+                        __threadfence();
+                        red_release_gpu_add(committed + h, 1u);
+                        stamp(a, t, 5 + h);
+                    }
                     __syncwarp();
                 }
-                for (int g = h; g < groups; g += 2) {
-                    const float *rn_g = my_rn + ((g - h) >> 1) * 32;
-                    const int gn = g + 2;
-                    if (gn < groups) {
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            mnext[v] = ld_cg_hint(&mt[((gn * 4 + q) * 8 + v) * 32 + lane], stream);
-                    }
-                    float acc[32];
-                    tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
-                    tmem_wait_ld();
-                    const uint32_t cbase = (uint32_t)c0 + 32u * (uint32_t)g;
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        float mv[4] = {mcur[v].x, mcur[v].y, mcur[v].z, mcur[v].w};
-                        bool changed = false;
-                        // max-min: m keeps the running minimum.  Centroid: m is
-                        // -inf for held / masked rows and this iteration's
-                        // distance otherwise.
-#pragma unroll
-                        for (int z = 0; z < 4; ++z) {
-                            // split storage: d = 1 - <q, e>, the accumulator holding
-                            // 2^12 <q, e> of unit rows
-                            const float d =
-                                kF16 ? fmaf(acc[4 * v + z] * rn_g[4 * v + z], neg_rnq, 1.0f)
-                                     : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
-                            const float nv = kCentroid ? (mv[z] == -INFINITY ? -INFINITY : d)
-                                                       : fminf(mv[z], d);
-                            changed |= nv != mv[z];
-                            mv[z] = nv;
-                            if (mv[z] > best) {
-                                best = mv[z];
-                                best_c = cbase + 4 * v + z;
-                            }
-                        }
-                        // a candidate's running minimum changes with probability
-                        // about 1/(t+1) after t picks: write back only what moved
-                        // centroid: the next iteration needs only the -inf marks,
-                        // so this iteration's distances are stored only for a trace
-                        if (changed && (!kCentroid || a.trace_slot))
-                            st_cg_hint(&mt[((g * 4 + q) * 8 + v) * 32 + lane],
-                                       make_float4(mv[0], mv[1], mv[2], mv[3]), stream);
-                    }
-                    if (gn < groups) {
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) mcur[v] = mnext[v];
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (kPair)
-                        mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
-                    else
-                        mbar_arrive(&acc_empty[buf]);
-                }
-                ++acc_uses;
-                const int b = beta * kUnitRows + r;
-                if (best > -INFINITY && b < a.B) atomicMax(a.keys + b, max_key(best, best_c));
-            }
-            if (warp == 2 && lane == 0) {
-                stamp(a, t, 4);
-                record(a, t, 11, epi_wait);
+                if (!ok) break;
             }
         }
-
-        // ---- all partial winners of iteration t are in the keys ----
-        if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
-                          skip_arrive))
-            break;
-        skip_arrive = false;
-        if (threadIdx.x == 0) stamp(a, t, 5);
-
-        // ---- commit: each warp takes a contiguous run of sequences ----
-        {
-            const int nw = gridDim.x * (kTcThreads / 32);
-            const int gw = blockIdx.x * (kTcThreads / 32) + warp;
-            const int per = (a.B + nw - 1) / nw;
-            const int b_lo = gw * per, b_hi = min(a.B, b_lo + per);
-            const int vec = a.Dp / 8;  // 16-byte vectors per row segment
-            for (int base = b_lo; base < b_hi; base += 32) {
-                const int cnt = min(32, b_hi - base);
-                const int b = base + lane;
-                const bool mine = lane < cnt;
-                const unsigned long long key = mine ? __ldcg(a.keys + b) : 0ull;
-                const uint32_t w = max_key_index(key);
-                if (mine) {
-                    if (key == 0ull) {
-                        atomicOr(a.status, kStatusNoWinner);
-                        a.picks[(int64_t)b * a.L + t] = -1;
-                    } else {
-                        a.keys[b] = 0ull;
-                        a.picks[(int64_t)b * a.L + t] = (int32_t)w;
-                    }
-                }
-                if (a.trace_slot) {
-                    // parity-check path: copy the traced rows of m before masking
-                    for (int i = 0; i < cnt; ++i) {
-                        const int bi = base + i;
-                        const int slot = a.trace_slot[bi];
-                        if (slot < 0) continue;
-                        const int beta = bi / kUnitRows, r = bi % kUnitRows;
-                        float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
-                        for (int64_t c = lane; c < a.N; c += 32) {
-                            const int jj = p.chunk_of(c);
-                            const int cc = (int)(c - p.col0(jj));
-                            dst[c] = __ldcg(a.m + p.tile_base(jj, beta) + tc_m_inner(r, cc));
-                        }
-                    }
-                    __syncwarp();
-                }
-                if (mine && key != 0ull) {
-                    const int beta = b / kUnitRows, r = b % kUnitRows;
-                    const int jw = p.chunk_of(w);
-                    const int cw = (int)(w - p.col0(jw));
-                    a.m[p.tile_base(jw, beta) + tc_m_inner(r, cw)] = -INFINITY;
-                }
-                // next queries: the split rows of the winners, all rows of the run
-                // copied by the whole warp, loads first (read-only path)
-                const __half2 scale = __float2half2_rn(4096.0f);
-                for (int i = 0; i < cnt; ++i) {
-                    const unsigned long long ki = __shfl_sync(0xffffffffu, key, i);
-                    const uint32_t wi = __shfl_sync(0xffffffffu, w, i);
-                    if (ki == 0ull) continue;
-                    if (kCentroid) {
-                        // add the winner to the sequence's exact centroid sum,
-                        // then write the split unit centroid as the next query.
-                        // Sums stay below 2^62 units, so v 2^-62 lies in (-1, 1):
-                        // that fixed scaling gives the norm without overflow, and
-                        // its smallest nonzero square (2^-124) is a normal fp32.
-                        const int bq = base + i;
-                        long long *cs = a.csum + (int64_t)bq * a.Dp;
-                        const float *eu = a.e_unit + (int64_t)wi * a.Dp;
-                        const float nw = a.nrm[wi];
-                        const int F = a.csum_shift;
-                        float s1, s2;
-                        fixed_unscale(62, s1, s2);
-                        constexpr int kB = 8;  // loads in flight per lane
-                        KahanSum ss;
-                        for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
-                            long long v[kB];
-                            float x[kB];
-#pragma unroll
-                            for (int u = 0; u < kB; ++u) {
-                                const int k = k0 + 32 * u + lane;
-                                v[u] = k < a.Dp ? cs[k] : 0ll;
-                                x[u] = k < a.Dp ? __ldg(eu + k) : 0.0f;
-                            }
-#pragma unroll
-                            for (int u = 0; u < kB; ++u) {
-                                const int k = k0 + 32 * u + lane;
-                                if (k < a.Dp) {
-                                    v[u] += to_fixed(x[u] * nw, F);
-                                    cs[k] = v[u];
-                                    const float c = from_fixed(v[u], s1, s2);
-                                    ss.add(c * c);
-                                }
-                            }
-                        }
-                        const float sum = warp_sum_f(ss.total());
-                        // a zero centroid gives a zero query: every distance is 1
-                        const float inv = sum > 0.0f ? 1.0f / sqrtf(sum) : 0.0f;
-                        __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
-                        __syncwarp();
-                        for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
-                            long long v[kB];
-#pragma unroll
-                            for (int u = 0; u < kB; ++u) {
-                                const int k = k0 + 32 * u + lane;
-                                v[u] = k < a.Dp ? cs[k] : 0ll;
-                            }
-#pragma unroll
-                            for (int u = 0; u < kB; ++u) {
-                                const int k = k0 + 32 * u + lane;
-                                if (k < a.Dp) {
-                                    const float uval = from_fixed(v[u], s1, s2) * inv;
-                                    const __half hi = __float2half_rn(uval);
-                                    const __half lo =
-                                        __float2half_rn((uval - __half2float(hi)) * 4096.0f);
-                                    qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
-                                    qd[a.Dp + k] = hi;
-                                    qd[2 * a.Dp + k] = lo;
-                                }
-                            }
-                        }
-                        continue;
-                    }
-                    if (kF16) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(a.e_f16 + (int64_t)wi * a.Dp);
-                        uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * a.Dp);
-                        for (int k = lane; k < vec; k += 32) dst[k] = __ldg(src + k);
-                        if (lane == 0) a.q_rn[base + i] = a.rn[wi];
-                        continue;
-                    }
-                    const uint4 *src =
-                        reinterpret_cast<const uint4 *>(a.e_split + (int64_t)wi * 2 * a.Dp);
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * 3 * a.Dp);
-#pragma unroll 4
-                    for (int k = lane; k < vec; k += 32) {
-                        const uint4 hi = __ldg(src + k), lo = __ldg(src + vec + k);
-                        uint4 hi12 = hi;
-                        __half2 *h2 = reinterpret_cast<__half2 *>(&hi12);
-#pragma unroll
-                        for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
-                        dst[k] = hi12;
-                        dst[vec + k] = hi;
-                        dst[2 * vec + k] = lo;
-                    }
-                }
-            }
-            fence_proxy_async_global();
-            if (threadIdx.x == 0) stamp(a, t, 6);
-        }
-
-        // ---- the next queries are written ----
-        if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
-                          false))
-            break;
-        if (threadIdx.x == 0) stamp(a, t, 7);
     }
 
     // ---- teardown: drain what this CTA still has in flight, free TMEM ----
@@ -722,11 +903,12 @@ cudaError_t launch_variant(const TcDseqArgs &a, const TcPlan &p, const CUtensorM
     if (!kPair) {
         void *args[] = {&mq, &me, &aa, &pp};
         return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kernel),
-                                           dim3((unsigned)p.grid), dim3(kTcThreads), args, smem, st);
+                                           dim3((unsigned)p.grid), dim3(dseq_threads<kCentroid>()),
+                                           args, smem, st);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(dseq_threads<kCentroid>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -780,7 +962,7 @@ int tc_dseq_pair_max_clusters(int tile_n) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(dseq_threads<false>());
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -121,7 +121,10 @@ int dseq_run_trace(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
  * second grid barrier; then nanoseconds spent waiting in the iteration:
  * 8 MMA issuer for filled stages, 9 MMA issuer for a free accumulator,
  * 10 producer for a free stage, 11 epilogue for a finished accumulator
- * (slots 2, 3, 8 and 9 only on CTAs that issue MMAs).  *iters and *grid receive the dimensions (0 when no timeline
+ * (slots 2, 3, 8 and 9 only on CTAs that issue MMAs).  The max-min kernels
+ * overlap the two halves of the sequence blocks and have no grid barrier:
+ * there slot 5 and 6 are the CTA's commits of half 0 and half 1 done, and
+ * slot 7 the nanoseconds the producer waited for committed queries.  *iters and *grid receive the dimensions (0 when no timeline
  * was recorded); capacity is the length of out in elements; out = NULL only
  * queries the dimensions.
  * Errors: DSEQ_EINVAL (NULL ctx/iters/grid, capacity too small), DSEQ_ECUDA. */
@@ -244,9 +247,11 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *   "timeline"    1 = dseq_run records, per CTA and iteration of the
  *                 tensor-core kernel, device timestamps of its phases (read
  *                 them back with dseq_get_timeline); default 0.
- *   "fault_skip_arrive"  test only: 1 makes CTA 0 skip its first grid-barrier
- *                 arrival, so the other CTAs' waits run out (the kernel then
- *                 returns DSEQ_ETIMEOUT without hanging).
+ *   "fault_skip_arrive"  test only: 1 makes CTA 0 skip its first arrival on
+ *                 the cross-CTA synchronisation (the grid barrier, or the
+ *                 "half done" counter of the overlapped kernels), so the
+ *                 other CTAs' waits run out (the kernel then returns
+ *                 DSEQ_ETIMEOUT without hanging).
  * Errors: DSEQ_EINVAL for an unknown name or a value out of range. */
 int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value);
 

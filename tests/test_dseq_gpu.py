@@ -219,21 +219,24 @@ def test_host_buffers(es):
     assert np.array_equal(host_picks, dev_picks)
 
 
-def test_barrier_timeout_returns_cleanly(es):
-    """One CTA skips its grid-barrier arrival: every wait runs out after the
-    time limit, the call returns DSEQ_ETIMEOUT, and the GPU stays usable."""
-    N, D, B, L = 2000, 64, 256, 4
+@pytest.mark.parametrize("criterion,pair", [(0, 1), (0, 0), (1, 1)])
+def test_barrier_timeout_returns_cleanly(es, criterion, pair):
+    """One CTA skips its first cross-CTA arrival (the overlapped max-min
+    kernels' "half done" counter, the centroid kernel's grid barrier): every
+    wait runs out after the time limit, the call returns DSEQ_ETIMEOUT, and
+    the GPU stays usable."""
+    N, D, B, L = 2000, 64, 512, 4
     E = workloads.gaussian_table(N, D, seed=5)
     starts = workloads.starts(N, B, seed=5)
-    ref, _ = _run(es, E, starts, L)
+    ref, _ = _run(es, E, starts, L, criterion=criterion, pair=pair)
     es.dseq_set_option("timeout_ms", 500)
     es.dseq_set_option("fault_skip_arrive", 1)
     with pytest.raises(es.DseqError) as ei:
-        _run(es, E, starts, L)
+        _run(es, E, starts, L, criterion=criterion, pair=pair)
     assert ei.value.code == es.DSEQ_ETIMEOUT
     es.dseq_set_option("fault_skip_arrive", 0)
     es.dseq_set_option("timeout_ms", 10000)
-    again, _ = _run(es, E, starts, L)
+    again, _ = _run(es, E, starts, L, criterion=criterion, pair=pair)
     assert np.array_equal(again, ref)
 
 
