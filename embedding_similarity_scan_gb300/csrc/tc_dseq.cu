@@ -542,10 +542,10 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                 const int cw = (int)(w - p.col0(jw));
                 a.m[p.tile_base(jw, beta) + tc_m_inner(r, cw)] = -INFINITY;
             }
-            // next queries: the split rows of the winners, all rows of the run
-            // copied by the whole warp, loads first (read-only path)
+            // next queries: the centroid's (per sequence), else the winners'
+            // stored rows, all rows of the run by the whole warp
             const __half2 scale = __float2half2_rn(4096.0f);
-            for (int i = 0; i < cnt; ++i) {
+            for (int i = 0; kCentroid && i < cnt; ++i) {
                 const unsigned long long ki = __shfl_sync(0xffffffffu, key, i);
                 const uint32_t wi = __shfl_sync(0xffffffffu, w, i);
                 if (ki == 0ull) continue;
@@ -612,26 +612,55 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     }
                     continue;
                 }
-                if (kF16) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(a.e_f16 + (int64_t)wi * a.Dp);
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * a.Dp);
-                    for (int k = lane; k < vec; k += 32) dst[k] = __ldg(src + k);
-                    if (lane == 0) a.q_rn[base + i] = a.rn[wi];
-                    continue;
-                }
-                const uint4 *src =
-                    reinterpret_cast<const uint4 *>(a.e_split + (int64_t)wi * 2 * a.Dp);
-                uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)(base + i) * 3 * a.Dp);
-#pragma unroll 4
-                for (int k = lane; k < vec; k += 32) {
-                    const uint4 hi = __ldg(src + k), lo = __ldg(src + vec + k);
-                    uint4 hi12 = hi;
-                    __half2 *h2 = reinterpret_cast<__half2 *>(&hi12);
+            }
+            if (!kCentroid) {
+                // the winners' rows, flattened over (sequence, 16-byte vector)
+                // so that each lane has kCopyBatch rows' loads in flight
+                constexpr int kCopyBatch = 4;
+                const int total = cnt * vec;
+                for (int f0 = 0; f0 < total; f0 += 32 * kCopyBatch) {
+                    uint4 hv[kCopyBatch], lv[kCopyBatch];
+                    int ii[kCopyBatch];
+                    uint32_t wv[kCopyBatch];
+                    bool ok[kCopyBatch];
 #pragma unroll
-                    for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
-                    dst[k] = hi12;
-                    dst[vec + k] = hi;
-                    dst[2 * vec + k] = lo;
+                    for (int u = 0; u < kCopyBatch; ++u) {
+                        const int f = f0 + 32 * u + lane;
+                        ii[u] = min(f / vec, cnt - 1);
+                        wv[u] = __shfl_sync(0xffffffffu, w, ii[u]);
+                        const unsigned long long ku = __shfl_sync(0xffffffffu, key, ii[u]);
+                        ok[u] = f < total && ku != 0ull;
+                        const int k = f - ii[u] * vec;
+                        if (kF16) {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(a.e_f16 + (int64_t)wv[u] * a.Dp);
+                            hv[u] = ok[u] ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+                        } else {
+                            const uint4 *src =
+                                reinterpret_cast<const uint4 *>(a.e_split + (int64_t)wv[u] * 2 * a.Dp);
+                            hv[u] = ok[u] ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+                            lv[u] = ok[u] ? __ldg(src + vec + k) : make_uint4(0, 0, 0, 0);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kCopyBatch; ++u) {
+                        if (!ok[u]) continue;
+                        const int f = f0 + 32 * u + lane;
+                        const int k = f - ii[u] * vec;
+                        const int bq = base + ii[u];
+                        if (kF16) {
+                            reinterpret_cast<uint4 *>(a.q_split + (int64_t)bq * a.Dp)[k] = hv[u];
+                            if (k == 0) a.q_rn[bq] = a.rn[wv[u]];
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)bq * 3 * a.Dp);
+                            uint4 hi12 = hv[u];
+                            __half2 *h2 = reinterpret_cast<__half2 *>(&hi12);
+#pragma unroll
+                            for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
+                            dst[k] = hi12;
+                            dst[vec + k] = hv[u];
+                            dst[2 * vec + k] = lv[u];
+                        }
+                    }
                 }
             }
         }
@@ -813,11 +842,13 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
             // ---------------- commit warp ----------------
             for (int t = 0; t < a.L; ++t) {
                 bool ok = true;
+                uint64_t wait_done = 0, busy = 0;
                 for (int h = 0; h < 2; ++h) {
                     int pass = 1;
                     if (lane == 0)
                         pass = wait_counter(done + h, G * (unsigned)(t + 1), a.status, abort_flag,
-                                            tmo, kStatusBarrierTimeout, nullptr);
+                                            tmo, kStatusBarrierTimeout, &wait_done);
+                    const uint64_t t_start = a.timeline ? globaltimer_ns() : 0;
                     if (!__shfl_sync(0xffffffffu, pass, 0)) {
                         ok = false;
                         break;
@@ -833,9 +864,13 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     if (lane == 0) {
                         __threadfence();
                         red_release_gpu_add(committed + h, 1u);
-                        stamp(a, t, 5 + h);
+                        if (a.timeline) busy += globaltimer_ns() - t_start;
                     }
                     __syncwarp();
+                }
+                if (lane == 0) {
+                    record(a, t, 5, busy);
+                    record(a, t, 6, wait_done);
                 }
                 if (!ok) break;
             }

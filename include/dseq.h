@@ -123,8 +123,9 @@ int dseq_run_trace(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
  * 10 producer for a free stage, 11 epilogue for a finished accumulator
  * (slots 2, 3, 8 and 9 only on CTAs that issue MMAs).  The max-min kernels
  * overlap the two halves of the sequence blocks and have no grid barrier:
- * there slot 5 and 6 are the CTA's commits of half 0 and half 1 done, and
- * slot 7 the nanoseconds the producer waited for committed queries.  *iters and *grid receive the dimensions (0 when no timeline
+ * there slot 5 is the nanoseconds the CTA's commit warp spent committing,
+ * slot 6 the nanoseconds it waited for the halves to be done, and slot 7 the
+ * nanoseconds the producer waited for committed queries.  *iters and *grid receive the dimensions (0 when no timeline
  * was recorded); capacity is the length of out in elements; out = NULL only
  * queries the dimensions.
  * Errors: DSEQ_EINVAL (NULL ctx/iters/grid, capacity too small), DSEQ_ECUDA. */
