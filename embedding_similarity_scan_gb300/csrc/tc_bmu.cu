@@ -34,9 +34,11 @@ namespace {
 constexpr uint32_t kSubA = kUnitRows * kKBlock * 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
+// column groups of 32 in the widest unit (256 neurons)
+constexpr int kMaxGroups = 8;
 
 // Stage geometry.  One CTA: B sub-tiles of up to 256 neuron rows, 3 stages
-// (the epilogue also needs 2 KB of column constants).  CTA pair: each CTA
+// (the epilogue also needs 8 KB of column constants).  CTA pair: each CTA
 // stages half of the neuron chunk (<= 128 rows), 5 stages.
 template <bool kPair>
 struct BmuCfg {
@@ -44,7 +46,7 @@ struct BmuCfg {
     static constexpr uint32_t kSubB = (kPair ? 128u : 256u) * kKBlock * 2;
     static constexpr uint32_t kStage = 3 * kSubA + 2 * kSubB;
     static constexpr size_t kSmemBytes =
-        (size_t)kStagesT * kStage + 1024 + 256 + kEpiWarps * 32 * sizeof(float2);
+        (size_t)kStagesT * kStage + 1024 + 256 + kEpiWarps * (kMaxGroups / 2) * 32 * sizeof(float2);
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
         const int e = warp - 2, q = warp & 3, h = e >> 2;
         const int r = 32 * q + lane;
-        float2 *my_colc = colc + e * 32;
+        float2 *my_colc = colc + e * (kMaxGroups / 2) * 32;
         uint32_t acc_uses = 0;
         const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
         for (int64_t u = first_item; u < units; u += item_stride) {
@@ -273,6 +275,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int beta = kPair ? 2 * blk + (int)rank : blk;
             const int64_t row = (int64_t)beta * kUnitRows + r;
             const float cx = row < a.n ? -a.x_inv_scale[row] * (1.0f / 2048.0f) : 0.0f;
+            // this warp's (at most 4) column groups' constants, fetched before the wait
+            float2 cv[kMaxGroups / 2];
+#pragma unroll
+            for (int k = 0; k < kMaxGroups / 2; ++k) {
+                const int64_t col = (int64_t)j * tile_n + 32 * (h + 2 * k) + lane;
+                cv[k] = (h + 2 * k < groups && col < a.M)
+                            ? make_float2(__ldg(a.wn + col), __ldg(a.w_inv_scale + col))
+                            : make_float2(INFINITY, 0.0f);
+            }
             const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
             // every lane waits; the warp proceeds only if all of them saw the phase
             const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status, tmo,
@@ -282,19 +293,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float best = INFINITY;
             uint32_t best_j = 0xffffffffu;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < kMaxGroups / 2; ++k) my_colc[k * 32 + lane] = cv[k];
+            __syncwarp();
             for (int g = h; g < groups; g += 2) {
-                const int64_t col = (int64_t)j * tile_n + 32 * g + lane;
-                __syncwarp();
-                my_colc[lane] = col < a.M ? make_float2(a.wn[col], a.w_inv_scale[col])
-                                          : make_float2(INFINITY, 0.0f);
-                __syncwarp();
+                const float2 *cg = my_colc + ((g - h) >> 1) * 32;
                 float acc[32];
                 tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
                 tmem_wait_ld();
                 const uint32_t cbase = (uint32_t)j * tile_n + 32u * (uint32_t)g;
 #pragma unroll
                 for (int z = 0; z < 32; ++z) {
-                    const float2 cc = my_colc[z];
+                    const float2 cc = cg[z];
                     const float s = fmaf(acc[z] * cc.y, cx, cc.x);
                     if (s < best) {
                         best = s;
