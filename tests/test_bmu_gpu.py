@@ -52,6 +52,7 @@ SMALL = [
     (1, 1, 1),
     (5, 3000, 7),
     (1000, 700, 300),   # D not a multiple of 32, several K blocks
+    (40, 300, 16384),   # the largest D the API takes
 ]
 
 

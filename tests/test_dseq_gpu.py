@@ -93,6 +93,29 @@ def test_small_teacher_forced(es, engine, case):
     check_dseq_teacher_forced(E, starts, mask, picks, trace, trace_seqs)
 
 
+EXTREME = [
+    # (N, D, B, L): the largest D the API takes, a table narrower than one
+    # chunk run to its full ordering, one sequence, a wide D with many blocks
+    (300, 16384, 16, 4),
+    (20, 8, 3, 19),
+    (1500, 64, 1, 40),
+    (700, 4096, 520, 6),
+]
+
+
+@pytest.mark.parametrize("engine", ["tc", "tc_pair", "ffma"])
+@pytest.mark.parametrize("case", EXTREME, ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
+def test_extreme_shapes_teacher_forced(es, engine, case):
+    N, D, B, L = case
+    E = workloads.gaussian_table(N, D, seed=D + N)
+    starts = workloads.starts(N, B, seed=D + N)
+    tr = np.unique(np.array([0, B // 2, B - 1], np.int32))
+    picks, trace = _run(es, E, starts, L, None, tr, engine=1 if engine == "ffma" else 0,
+                        pair=1 if engine == "tc_pair" else 0)
+    check_picks_valid(starts, None, picks, N)
+    check_dseq_teacher_forced(E, starts, None, picks, trace, tr)
+
+
 def test_picks_identical_across_candidate_tiles(es):
     """Candidate tiling does not reorder any dot product, so the picks (and
     the running minima) must be bit-identical for every tile width."""
@@ -367,8 +390,9 @@ def test_centroid_rejects_fp16_storage_and_ffma(es):
 # give exactly the picks of one long call.
 
 
-@pytest.mark.parametrize("engine,pair,criterion", [(0, 1, 0), (0, 0, 0), (1, 0, 0), (0, 1, 1)])
-def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion):
+@pytest.mark.parametrize("engine,pair,criterion,storage",
+                         [(0, 1, 0, 0), (0, 0, 0, 0), (1, 0, 0, 0), (0, 1, 1, 0), (0, 1, 0, 1)])
+def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion, storage):
     N, D, B = 300, 40, 9
     E = workloads.clustered_table(N, D, n_centres=6, seed=12)
     starts = workloads.starts(N, B, seed=12)
@@ -377,9 +401,12 @@ def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion):
     mask[starts] = 0
     L_total = N - int(mask.sum()) - 1  # the full ordering of every sequence
     traced = np.array([0, B - 1], np.int32)
+    if storage:  # fp16 storage: a table of fp16 numbers keeps the oracle exact
+        E = E.astype(np.float16).astype(np.float32)
     es.dseq_set_option("engine", engine)
     es.dseq_set_option("pair", pair)
     es.dseq_set_option("criterion", criterion)
+    es.dseq_set_option("storage", storage)
     ctx = es.dseq_create(torch.from_numpy(E).cuda())
     try:
         st = torch.from_numpy(starts).cuda()
