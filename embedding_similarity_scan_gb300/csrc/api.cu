@@ -392,7 +392,7 @@ struct dseq_ctx {
     Options opt;
     DevBuf e_unit, e_split, e_f16, rn, nrm;
     // run workspace
-    DevBuf m, keys, q, q_rn, csum, status, barrier, starts, mask, picks, trace_slot, timeline;
+    DevBuf m, keys, q, q_rn, csum, c_exp, status, barrier, starts, mask, picks, trace_slot, timeline;
     int64_t timeline_iters = 0, timeline_grid = 0;
     int csum_shift = kNoShift;  // fixed-point scale of the centroid sums, set on first use
     // state left on the device by the last successful run, for "resume"
@@ -404,7 +404,7 @@ struct dseq_ctx {
     std::vector<uint8_t> state_mask;
     ~dseq_ctx() {
         DevBuf *all[] = {&e_unit, &e_split, &e_f16,  &rn,      &nrm,    &m,
-                         &keys,   &q,       &q_rn,   &csum,    &status, &barrier,
+                         &keys,   &q,       &q_rn,   &csum,    &c_exp,  &status, &barrier,
                          &starts, &mask,    &picks,  &trace_slot, &timeline};
         for (DevBuf *b : all) b->release();
     }
@@ -603,7 +603,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         d_picks = ctx->picks.as<int32_t>();
     }
     TRY(ctx->keys.ensure((size_t)Bp * sizeof(unsigned long long)));
-    // grid barrier counter, then the overlapped kernels' done[2] and committed[2]
+    // cross-CTA counters of the persistent kernel: [1..2] done, [3..4] committed
     TRY(ctx->barrier.ensure(8 * sizeof(unsigned)));
     CUDA_TRY(cudaMemsetAsync(ctx->status.p, 0, sizeof(int), st));
 
@@ -653,7 +653,9 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         if (a.centroid) {
             if (f16) return fail(DSEQ_EINVAL, "the centroid criterion runs on split storage (storage=0)");
             TRY(ctx->csum.ensure((size_t)Bp * ctx->Dp * sizeof(long long)));
+            TRY(ctx->c_exp.ensure((size_t)Bp * sizeof(int)));
             a.csum = ctx->csum.as<long long>();
+            a.c_exp = ctx->c_exp.as<int>();
             if (ctx->csum_shift == kNoShift) {
                 // every raw-row entry is below the largest row norm 2^e and a
                 // sequence holds at most N rows: F = 62 - e - ceil(log2 N)

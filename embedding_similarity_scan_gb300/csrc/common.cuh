@@ -390,33 +390,5 @@ __device__ __forceinline__ bool wait_counter(unsigned *counter, unsigned target,
     }
 }
 
-__device__ __forceinline__ bool grid_barrier(unsigned *counter, unsigned target, int *status,
-                                             volatile int *abort_flag, uint64_t timeout_ns,
-                                             bool skip_arrive) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        fence_proxy_async_global();
-        __threadfence();
-        if (!skip_arrive) red_release_gpu_add(counter, 1u);
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t spin = 0;; ++spin) {
-            if ((int)(ld_acquire_gpu(counter) - target) >= 0) break;  // wrap-safe
-            if (ld_volatile(status) != 0) {
-                *abort_flag = 1;
-                break;
-            }
-            if ((spin & 31u) == 31u && globaltimer_ns() - t0 > timeout_ns) {
-                atomicOr(status, kStatusBarrierTimeout);
-                *abort_flag = 1;
-                break;
-            }
-            __nanosleep(64);
-        }
-        __threadfence();
-        fence_proxy_async_global();
-    }
-    __syncthreads();
-    return *abort_flag == 0;
-}
 
 }  // namespace dseq

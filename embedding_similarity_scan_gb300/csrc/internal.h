@@ -52,12 +52,13 @@ __host__ __device__ __forceinline__ int64_t tc_m_inner(int r, int c) {
 }
 
 // Phase stamps per CTA and iteration of the persistent diversity kernel:
-// 0 iteration start, 1 first TMA issued, 2 first MMA issued, 3 last MMA
-// committed, 4 epilogue done (first epilogue warp), 5 after the first grid
-// barrier, 6 after the commit (CTA thread 0), 7 after the second grid barrier;
-// then nanoseconds spent waiting during the iteration: 8 MMA issuer on
-// filled stages, 9 MMA issuer on a free accumulator, 10 producer on a free
-// stage, 11 first epilogue warp on a finished accumulator.
+// 0 producer starts the iteration, 1 first copy issued, 2 first MMA issued,
+// 3 last MMA committed, 4 epilogue done (first epilogue warp); then
+// nanoseconds spent in the iteration: 5 committing and 6 waiting for done
+// halves (first commit warp), 7 producer waiting for committed queries,
+// 8 MMA issuer waiting for filled stages, 9 for a free accumulator,
+// 10 producer waiting for a free stage, 11 first epilogue warp waiting for a
+// finished accumulator.
 constexpr int kTimelineSlots = 12;
 
 struct TcPlan {
@@ -126,6 +127,7 @@ struct TcDseqArgs {
     int centroid;
     long long *csum;
     int csum_shift;
+    int *c_exp;              // Bp: exponent sb of each query's scale 2^-sb (centroid)
     const float *e_unit;
     const float *nrm;
     float *m;                // units x 128 x tile_n

@@ -8,35 +8,38 @@
 // on ties).  The issue asks for a tiled candidate scan that every workgroup
 // walks together, with a hard grid-wide sync between steps (Intended
 // Behavior, "dispatch per tile"); here the loop over iterations lives on the
-// device and the sync is a grid barrier.
+// device, and the sync is split per half of the sequences so that it never
+// idles the grid (below).
 //
 // Work decomposition.  One iteration is the contraction S = Q * E^T of the
 // B current query rows against the N table rows.  A work unit is a block of
-// 128 sequences (the 128 TMEM lanes of one accumulator) times a chunk of
-// tile_n candidates; units are ordered candidate-chunk-major and dealt to the
-// persistent CTAs round-robin, so at any moment all CTAs work on the same
-// few candidate chunks (the grid marches over the table together, and each
-// chunk is read from HBM once per iteration while the query block set stays
-// resident in L2).
+// 128 sequences (the 128 TMEM lanes of one accumulator; a pair of blocks for
+// a CTA pair) times a chunk of candidates (two chunk widths, see TcPlan).
+// The sequence blocks form two halves; each iteration's units are ordered
+// [half 0][half 1], each half candidate-chunk-major, and dealt to the
+// persistent CTAs round-robin, so the grid marches over the table together.
 //
 // Precision.  Rows are unit-norm and split into fp16 pairs hi + lo * 2^-12
 // (see prep.cu).  The query side carries (hi * 2^12, hi, lo), the table side
 // (hi, lo); per 32-wide K block three kind::f16 MMAs accumulate
 // hi*2^12 . hi + hi . lo + lo . hi into one fp32 TMEM accumulator, which
-// equals 2^12 <q, e> up to about 2^-22 relative per product.
+// equals 2^12 <q, e> up to about 2^-22 relative per product.  FP16 storage
+// uses one part on each side and the rows' inverse norms.
 //
-// CTA roles (320 threads):
-//   warp 0      TMA producer: Q and E K-blocks into a 4-stage smem ring;
+// CTA roles (352 threads; 384 for the centroid criterion):
+//   warp 0      TMA producer: Q and E K-blocks into a multi-stage smem ring;
 //   warp 1      TMEM owner and MMA issuer (one thread), double-buffered
 //               128 x 256 fp32 accumulators (512 TMEM columns);
 //   warps 2-9   epilogue: TMEM -> registers, d = 1 - S, m = min(m, d) on the
-//               running-minimum tile (read and written once per unit, 16-byte
-//               coalesced), running (max m, lowest index) per row, one 64-bit
-//               atomicMax per row and unit into the sequence's key.
-// After the last unit of an iteration: grid barrier; commit (one warp per
-// sequence: decode the winner, record it, mask it in m, write its split row
-// as the next query); grid barrier.  Every wait is bounded in time and sets
-// the status word instead of hanging.
+//               running-minimum tile (read once, written back only where it
+//               moved, 16-byte coalesced), running (max m, lowest index) per
+//               row, one 64-bit atomicMax per row and unit into its key;
+//   warps 10-   commit warps: once every CTA has published a half of an
+//               iteration, decode the winners of this CTA's share of that
+//               half, record them, mask them in m, write the next queries
+//               (the winners' stored rows, or the new centroids), and
+//               release the half to the producers of the next iteration.
+// Every wait is bounded in time and sets the status word instead of hanging.
 #include <math.h>
 
 #include "common.cuh"
@@ -136,6 +139,13 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
          i < (int64_t)p.n_beta * kUnitRows; i += stride)
         a.keys[i] = 0ull;
     if (a.centroid) {  // centroid sums start at the start rows
+        // the first query is the start's unit row (factor 2^-12); the
+        // centroid scale starts at the start row's norm exponent
+        for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+             b < (int64_t)p.n_beta * kUnitRows; b += stride) {
+            a.q_rn[b] = 1.0f / 4096.0f;
+            a.c_exp[b] = b < a.B ? scale_exponent(a.nrm[starts[b]]) : 0;
+        }
         const int64_t ctotal = (int64_t)p.n_beta * kUnitRows * a.Dp;
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ctotal;
              i += stride) {
@@ -167,12 +177,15 @@ __device__ __forceinline__ bool timed_wait(const TcDseqArgs &a, uint64_t *bar, u
     return ok;
 }
 
-// Max-min kernels overlap the commit of one half of the sequences with the
-// other half's units and add a commit warp; the centroid kernel, whose commit
-// is heavier, keeps one grid-wide phase per iteration.
+// Commit warps per CTA: the centroid commit (exact fixed-point centroid
+// update of every sequence) is heavier than copying a winner's stored row.
+template <bool kCentroid>
+__host__ __device__ constexpr int dseq_commit_warps() {
+    return kCentroid ? 4 : 1;
+}
 template <bool kCentroid>
 __host__ __device__ constexpr int dseq_threads() {
-    return kCentroid ? kTcThreads : kTcThreads + 32;
+    return kTcThreads + 32 * dseq_commit_warps<kCentroid>();
 }
 
 template <bool kPair, bool kF16, bool kCentroid>
@@ -181,8 +194,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                    const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
                    const TcPlan p) {
     using Cfg = DseqCfg<kPair, kF16>;
-    constexpr bool kOverlap = !kCentroid;
     constexpr int kThreads = dseq_threads<kCentroid>();
+    constexpr int kCommitWarps = dseq_commit_warps<kCentroid>();
     constexpr int kPartsA = Cfg::kPartsA, kPartsB = Cfg::kPartsB;
     constexpr int kSt = Cfg::kStagesT;
     constexpr uint32_t kSubB = Cfg::kSubB;
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     // halves and order each iteration's items [half 0][half 1], each half
     // candidate-chunk-major; the centroid kernel has one half.
     const int n_blocks = kPair ? p.n_beta / 2 : p.n_beta;
-    const int n_h0 = kOverlap ? (n_blocks + 1) / 2 : n_blocks;
+    const int n_h0 = (n_blocks + 1) / 2;
     const int n_h1 = n_blocks - n_h0;
     const int64_t work = (int64_t)n_blocks * p.n_chunk;
     const int64_t half_units = (int64_t)n_h0 * p.n_chunk;
@@ -418,6 +431,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         // norms; this warp's (at most 4) column groups' norms are
         // fetched before the wait too
         float neg_rnq = 0.0f, rnv[kMaxGroups / 2];
+        if (kCentroid) neg_rnq = -a.q_rn[beta * kUnitRows + r];
         if (kF16) {
             neg_rnq = -a.q_rn[beta * kUnitRows + r];
 #pragma unroll
@@ -465,7 +479,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     // 2^12 <q, e> of unit rows
                     const float d =
                         kF16 ? fmaf(acc[4 * v + z] * rn_g[4 * v + z], neg_rnq, 1.0f)
-                             : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
+                        : kCentroid ? fmaf(acc[4 * v + z], neg_rnq, 1.0f)
+                                    : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
                     const float nv = kCentroid ? (mv[z] == -INFINITY ? -INFINITY : d)
                                                : fminf(mv[z], d);
                     changed |= nv != mv[z];
@@ -550,20 +565,31 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                 const uint32_t wi = __shfl_sync(0xffffffffu, w, i);
                 if (ki == 0ull) continue;
                 if (kCentroid) {
-                    // add the winner to the sequence's exact centroid sum,
-                    // then write the split unit centroid as the next query.
-                    // Sums stay below 2^62 units, so v 2^-62 lies in (-1, 1):
-                    // that fixed scaling gives the norm without overflow, and
-                    // its smallest nonzero square (2^-124) is a normal fp32.
+                    // add the winner to the sequence's exact centroid sum and
+                    // write the centroid C, scaled by a power of two 2^-sb kept
+                    // per sequence, as the split query; the epilogue divides
+                    // by its norm (q_rn = 2^-12 / |C 2^-sb|), so one pass over
+                    // the row suffices.  When max |C 2^-sb| leaves [2^-6, 1)
+                    // the split is redone with sb corrected (max in [0.5, 1)).
                     const int bq = base + i;
                     long long *cs = a.csum + (int64_t)bq * a.Dp;
                     const float *eu = a.e_unit + (int64_t)wi * a.Dp;
+                    __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
                     const float nw = a.nrm[wi];
                     const int F = a.csum_shift;
+                    int sb = a.c_exp[bq];
                     float s1, s2;
-                    fixed_unscale(62, s1, s2);
-                    constexpr int kB = 8;  // loads in flight per lane
+                    fixed_unscale(F + sb, s1, s2);
+                    auto put = [&](int k, float c) {
+                        const __half hi = __float2half_rn(c);
+                        const __half lo = __float2half_rn((c - __half2float(hi)) * 4096.0f);
+                        qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
+                        qd[a.Dp + k] = hi;
+                        qd[2 * a.Dp + k] = lo;
+                    };
+                    constexpr int kB = 12;  // loads in flight per lane
                     KahanSum ss;
+                    float mx = 0.0f;
                     for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
                         long long v[kB];
                         float x[kB];
@@ -580,35 +606,41 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                                 v[u] += to_fixed(x[u] * nw, F);
                                 cs[k] = v[u];
                                 const float c = from_fixed(v[u], s1, s2);
+                                mx = fmaxf(mx, fabsf(c));
                                 ss.add(c * c);
+                                put(k, c);
+                            }
+                        }
+                    }
+                    mx = warp_max_f(mx);
+                    if (mx >= 1.0f || (mx > 0.0f && mx < 1.0f / 64.0f)) {
+                        sb += scale_exponent(mx);
+                        fixed_unscale(F + sb, s1, s2);
+                        ss = KahanSum();
+                        __syncwarp();
+                        for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
+                            long long v[kB];
+#pragma unroll
+                            for (int u = 0; u < kB; ++u) {
+                                const int k = k0 + 32 * u + lane;
+                                v[u] = k < a.Dp ? cs[k] : 0ll;
+                            }
+#pragma unroll
+                            for (int u = 0; u < kB; ++u) {
+                                const int k = k0 + 32 * u + lane;
+                                if (k < a.Dp) {
+                                    const float c = from_fixed(v[u], s1, s2);
+                                    ss.add(c * c);
+                                    put(k, c);
+                                }
                             }
                         }
                     }
                     const float sum = warp_sum_f(ss.total());
-                    // a zero centroid gives a zero query: every distance is 1
-                    const float inv = sum > 0.0f ? 1.0f / sqrtf(sum) : 0.0f;
-                    __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
-                    __syncwarp();
-                    for (int k0 = 0; k0 < a.Dp; k0 += 32 * kB) {
-                        long long v[kB];
-#pragma unroll
-                        for (int u = 0; u < kB; ++u) {
-                            const int k = k0 + 32 * u + lane;
-                            v[u] = k < a.Dp ? cs[k] : 0ll;
-                        }
-#pragma unroll
-                        for (int u = 0; u < kB; ++u) {
-                            const int k = k0 + 32 * u + lane;
-                            if (k < a.Dp) {
-                                const float uval = from_fixed(v[u], s1, s2) * inv;
-                                const __half hi = __float2half_rn(uval);
-                                const __half lo =
-                                    __float2half_rn((uval - __half2float(hi)) * 4096.0f);
-                                qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
-                                qd[a.Dp + k] = hi;
-                                qd[2 * a.Dp + k] = lo;
-                            }
-                        }
+                    if (lane == 0) {
+                        // a zero centroid gives a zero factor: every distance is 1
+                        a.q_rn[bq] = sum > 0.0f ? (1.0f / 4096.0f) / sqrtf(sum) : 0.0f;
+                        a.c_exp[bq] = sb;
                     }
                     continue;
                 }
@@ -671,88 +703,19 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         return first_item + (lo - first_item + item_stride - 1) / item_stride * item_stride;
     };
 
-    if (!kOverlap) {
-        // ---- one grid-wide phase per iteration: all units, barrier, commit, barrier ----
-        unsigned barrier_no = 0;
-        bool skip_arrive = a.fault_skip_arrive && blockIdx.x == 0;
-        for (int t = 0; t < a.L; ++t) {
-            if (*abort_flag) break;
-            if (threadIdx.x == 0) stamp(a, t, 0);
-            if (warp == 0) {
-                // ---------------- TMA producer ----------------
-                if (lane == 0) {
-                    fence_proxy_async_global();
-                    const uint64_t keep = l2_policy_evict_last();
-                    const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
-                    bool first = true;
-                    uint64_t waited = 0;
-                    for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride)
-                        produce_unit(t, v, keep, table_pol, waited, first);
-                    record(a, t, 10, waited);
-                }
-                __syncwarp();
-            } else if (warp == 1) {
-                // ---------------- MMA issuer (pair: the leader only) ----------------
-                if (lane == 0 && leader) {
-                    bool first = true;
-                    uint64_t wait_full = 0, wait_acc = 0;
-                    for (int64_t v = first_item; v < work && !*abort_flag; v += item_stride)
-                        if (!mma_unit(t, v, wait_full, wait_acc, first)) break;
-                    stamp(a, t, 3);
-                    record(a, t, 8, wait_full);
-                    record(a, t, 9, wait_acc);
-                }
-                __syncwarp();
-            } else {
-                // ---------------- epilogue ----------------
-                const uint64_t stream = l2_policy_evict_first();
-                // the leader's acc_empty barriers collect both CTAs' epilogue warps
-                const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
-                uint64_t epi_wait = 0;
-                for (int64_t v = first_item; v < work; v += item_stride)
-                    if (!epilogue_unit(v, stream, acc_empty_leader0, epi_wait)) break;
-                if (warp == 2 && lane == 0) {
-                    stamp(a, t, 4);
-                    record(a, t, 11, epi_wait);
-                }
-            }
-
-            // ---- all partial winners of iteration t are in the keys ----
-            if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
-                              skip_arrive))
-                break;
-            skip_arrive = false;
-            if (threadIdx.x == 0) stamp(a, t, 5);
-
-            // ---- commit: each warp takes a contiguous run of sequences ----
-            {
-                const int nw = gridDim.x * (kThreads / 32);
-                const int gw = blockIdx.x * (kThreads / 32) + warp;
-                const int per = (a.B + nw - 1) / nw;
-                const int b_lo = gw * per, b_hi = min(a.B, b_lo + per);
-                commit_range(t, b_lo, b_hi);
-                fence_proxy_async_global();
-                if (threadIdx.x == 0) stamp(a, t, 6);
-            }
-
-            // ---- the next queries are written ----
-            if (!grid_barrier(a.barrier, (++barrier_no) * gridDim.x, a.status, abort_flag, tmo,
-                              false))
-                break;
-            if (threadIdx.x == 0) stamp(a, t, 7);
-        }
-    } else {
+    {
         // ---- two halves of the sequence blocks, overlapped ----
         // Each iteration's units are ordered [half 0][half 1].  Counters in
-        // global memory replace the grid barriers: done[h] counts CTAs whose
+        // global memory synchronise the grid: done[h] counts CTAs whose
         // epilogue finished half h of an iteration (every partial winner in
-        // the keys), committed[h] counts commit warps that committed it.  A
-        // commit warp commits half h of iteration t once done[h] reaches
+        // the keys), committed[h] counts commit warps that committed it.  The
+        // commit warps commit half h of iteration t once done[h] reaches
         // G (t + 1) while the other warps already compute the other half; the
         // producer loads half h of iteration t + 1 once committed[h] reaches
-        // G (t + 1).  No CTA ever waits for the whole grid to go idle.
+        // GC (t + 1).  No CTA ever waits for the whole grid to go idle.
         unsigned *done = a.barrier + 1, *committed = a.barrier + 3;
         const unsigned G = gridDim.x;
+        const unsigned GC = G * kCommitWarps;  // commit warps in the grid
         const int64_t hb[3] = {0, half_units, work};
         if (warp == 0) {
             // ---------------- TMA producer ----------------
@@ -766,7 +729,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     for (int h = 0; h < 2 && !*abort_flag; ++h) {
                         if (t > 0) {
                             // the queries of half h were committed for iteration t
-                            if (!wait_counter(committed + h, G * (unsigned)t, a.status, abort_flag,
+                            if (!wait_counter(committed + h, GC * (unsigned)t, a.status, abort_flag,
                                               tmo, kStatusBarrierTimeout, &gate))
                                 break;
                             fence_proxy_async_global();
@@ -809,7 +772,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                         // minima this warp reads next)
                         int pass = 1;
                         if (lane == 0)
-                            pass = wait_counter(committed + h, G * (unsigned)t, a.status,
+                            pass = wait_counter(committed + h, GC * (unsigned)t, a.status,
                                                 abort_flag, tmo, kStatusBarrierTimeout, nullptr);
                         if (!__shfl_sync(0xffffffffu, pass, 0)) {
                             ok = false;
@@ -853,11 +816,12 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                         ok = false;
                         break;
                     }
-                    // this CTA's share of the sequences of half h
+                    // this commit warp's share of the sequences of half h
                     const int s_lo = min(a.B, seq_half[h]);
                     const int s_hi = min(a.B, seq_half[h + 1]);
-                    const int per = (s_hi - s_lo + (int)G - 1) / (int)G;
-                    const int b_lo = min(s_hi, s_lo + (int)blockIdx.x * per);
+                    const int per = (s_hi - s_lo + (int)GC - 1) / (int)GC;
+                    const int cw = (int)blockIdx.x * kCommitWarps + (warp - 2 - kEpiWarps);
+                    const int b_lo = min(s_hi, s_lo + cw * per);
                     commit_range(t, b_lo, min(s_hi, b_lo + per));
                     fence_proxy_async_global();
                     __syncwarp();
@@ -868,7 +832,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     }
                     __syncwarp();
                 }
-                if (lane == 0) {
+                if (lane == 0 && warp == 2 + kEpiWarps) {
                     record(a, t, 5, busy);
                     record(a, t, 6, wait_done);
                 }

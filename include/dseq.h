@@ -115,19 +115,17 @@ int dseq_run_trace(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
 
 /* Phase timestamps of the last dseq_run on ctx made with the "timeline"
  * option on (tensor-core path).  out receives iters x grid x 12 int64
- * values: per iteration and CTA, nanosecond stamps (%globaltimer) 0 iteration
- * start, 1 first TMA issued, 2 first MMA issued, 3 last MMA committed,
- * 4 epilogue done, 5 after the first grid barrier, 6 commit done, 7 after the
- * second grid barrier; then nanoseconds spent waiting in the iteration:
- * 8 MMA issuer for filled stages, 9 MMA issuer for a free accumulator,
- * 10 producer for a free stage, 11 epilogue for a finished accumulator
- * (slots 2, 3, 8 and 9 only on CTAs that issue MMAs).  The max-min kernels
- * overlap the two halves of the sequence blocks and have no grid barrier:
- * there slot 5 is the nanoseconds the CTA's commit warp spent committing,
- * slot 6 the nanoseconds it waited for the halves to be done, and slot 7 the
- * nanoseconds the producer waited for committed queries.  *iters and *grid receive the dimensions (0 when no timeline
- * was recorded); capacity is the length of out in elements; out = NULL only
- * queries the dimensions.
+ * values per iteration and CTA: nanosecond stamps (%globaltimer) 0 the
+ * producer starts the iteration, 1 its first copy issued, 2 first MMA
+ * issued, 3 last MMA committed, 4 epilogue done; then nanoseconds spent in
+ * the iteration: 5 by the CTA's first commit warp committing, 6 by it
+ * waiting for the halves to be done, 7 by the producer waiting for
+ * committed queries, 8 by the MMA issuer waiting for filled stages, 9 by it
+ * waiting for a free accumulator, 10 by the producer waiting for a free
+ * stage, 11 by the first epilogue warp waiting for a finished accumulator
+ * (slots 2, 3, 8 and 9 only on CTAs that issue MMAs).  *iters and *grid
+ * receive the dimensions (0 when no timeline was recorded); capacity is the
+ * length of out in elements; out = NULL only queries the dimensions.
  * Errors: DSEQ_EINVAL (NULL ctx/iters/grid, capacity too small), DSEQ_ECUDA. */
 int dseq_get_timeline(dseq_ctx *ctx, int64_t *out, int64_t capacity, int32_t *iters,
                       int32_t *grid);
@@ -249,10 +247,9 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 tensor-core kernel, device timestamps of its phases (read
  *                 them back with dseq_get_timeline); default 0.
  *   "fault_skip_arrive"  test only: 1 makes CTA 0 skip its first arrival on
- *                 the cross-CTA synchronisation (the grid barrier, or the
- *                 "half done" counter of the overlapped kernels), so the
- *                 other CTAs' waits run out (the kernel then returns
- *                 DSEQ_ETIMEOUT without hanging).
+ *                 the cross-CTA "half done" counter, so the other CTAs'
+ *                 waits run out (the kernel then returns DSEQ_ETIMEOUT
+ *                 without hanging).
  * Errors: DSEQ_EINVAL for an unknown name or a value out of range. */
 int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value);
 
