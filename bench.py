@@ -72,18 +72,26 @@ def _kernel_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if it was taken on the current kernel source; else None."""
+def _profiled_traffic(kernel: str, workload: str, variant: str = ""):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    variant and workload, taken from the section whose source hash is the
+    current kernel source's; None if there is none.  The variant ("" for the
+    default launch, "_pair0" for single-CTA tensor kernels) keys the line, so
+    one variant's counters never stand in for another's."""
     path = os.path.join(PROFILES, f"{kernel}.{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_traffic or m_hash.group(1) != _kernel_hash(kernel):
-        return None
-    return float(m_traffic.group(1))
+    current = _kernel_hash(kernel)
+    marks = list(re.finditer(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text))
+    for k, m in enumerate(marks):
+        if m.group(1) != current:
+            continue
+        end = marks[k + 1].start() if k + 1 < len(marks) else len(text)
+        t = re.search(rf"traffic_bytes_per_launch{variant}:\s*([0-9.eE+]+)", text[m.end():end])
+        if t:
+            return float(t.group(1))
+    return None
 
 
 class ClockSampler:
@@ -490,7 +498,8 @@ def run_ours(args):
             "frac": (achieved / tensor_peak) if achieved else None,
             "peak_kind": peak_kind,
             "frac_of_burst": (achieved / burst_peak) if achieved else None,
-            "traffic": _profiled_traffic(kernel_name, epoch_of or args.workload),
+            "traffic": _profiled_traffic(kernel_name, epoch_of or args.workload,
+                                         "_pair0" if "pair=0" in args.opt else ""),
             "kernel": kernel_name,
             "note": (f"achieved = algorithmic FLOP (2*{'N*D*B*L' if is_div else 'n*M*D'})"
                      f" / kernel time (CUDA events on the launching stream); {peak_note}")}
