@@ -290,8 +290,12 @@ void choose_widths(TcPlan &plan, int64_t blocks, int64_t ncols, int workers, boo
         for (int w2 = w1; w2 >= 32; w2 -= 32) {
             if (forced_w2 > 0 ? w2 != forced_w2 : (forced_w1 > 0 && w2 != w1)) continue;
             const int64_t max_wide = (ncols + w1 - 1) / w1;
-            // all-narrow splits are the uniform plan of width w2
-            for (int64_t nw = (w2 == w1 ? max_wide : 1); nw <= max_wide; ++nw) {
+            // all-narrow splits are the uniform plan of width w2; the narrow
+            // chunks only balance the last rounds, so at most 64 of them are
+            // considered (this bounds the search for very wide tables)
+            const int64_t lo_wide =
+                w2 == w1 ? max_wide : std::max<int64_t>(1, max_wide - (64 * w2 + w1 - 1) / w1);
+            for (int64_t nw = lo_wide; nw <= max_wide; ++nw) {
                 const int64_t rest = std::max<int64_t>(0, ncols - nw * w1);
                 const int64_t nn = (rest + w2 - 1) / w2;
                 const int64_t units = blocks * (nw + nn), wide = blocks * nw;
