@@ -29,7 +29,8 @@ constexpr int kKBlock = 32;
 constexpr int kStages = 4;
 // Epilogue warps of the tensor-core kernels (two per TMEM lane quadrant).
 constexpr int kEpiWarps = 8;
-// Threads per CTA: TMA producer warp, MMA warp, epilogue warps.
+// Threads per CTA of the BMU kernel: TMA producer warp, MMA warp, epilogue
+// warps (the diversity kernel adds its commit warps).
 constexpr int kTcThreads = 32 * (2 + kEpiWarps);
 // Bytes of one pipeline stage for a unit of tile_n candidate columns:
 // A = 3 x (128 x 32) fp16 (hi*2^12, hi, lo*2^12), B = 2 x (tile_n x 32) fp16.

@@ -244,10 +244,9 @@ def test_host_buffers(es):
 
 @pytest.mark.parametrize("criterion,pair", [(0, 1), (0, 0), (1, 1)])
 def test_barrier_timeout_returns_cleanly(es, criterion, pair):
-    """One CTA skips its first cross-CTA arrival (the overlapped max-min
-    kernels' "half done" counter, the centroid kernel's grid barrier): every
-    wait runs out after the time limit, the call returns DSEQ_ETIMEOUT, and
-    the GPU stays usable."""
+    """One CTA skips its first arrival on the cross-CTA "half done" counter:
+    every wait runs out after the time limit, the call returns DSEQ_ETIMEOUT,
+    and the GPU stays usable (max-min pair and single CTA, centroid)."""
     N, D, B, L = 2000, 64, 512, 4
     E = workloads.gaussian_table(N, D, seed=5)
     starts = workloads.starts(N, B, seed=5)
