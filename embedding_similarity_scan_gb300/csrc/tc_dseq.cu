@@ -81,22 +81,32 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__restrict__ starts,
                                     const uint8_t *__restrict__ mask) {
     const int64_t per_col = (int64_t)p.n_beta * kUnitRows;  // floats per candidate column
-    const int64_t total = p.columns() * per_col;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    // running minima, one 16-byte vector (4 consecutive candidates of one
+    // row, 16-byte aligned in the tile layout) per step
+    const int64_t total4 = p.columns() * per_col / 4;
+    for (int64_t i4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i4 < total4; i4 += stride) {
+        const int64_t i = 4 * i4;
         const int j = p.chunk_of(i / per_col);
         const int64_t tile = (int64_t)kUnitRows * p.width(j);
         const int64_t local = i - p.col0(j) * per_col;
         const int beta = (int)(local / tile);
         const int s = (int)(local - beta * tile);
-        const int e = s & 3, t = (s >> 2) & 31, v = (s >> 7) & 7, q = (s >> 10) & 3, g = s >> 12;
-        const int r = 32 * q + t, c = 32 * g + 4 * v + e;
+        const int t = (s >> 2) & 31, v = (s >> 7) & 7, q = (s >> 10) & 3, g = s >> 12;
+        const int r = 32 * q + t;
         const int b = beta * kUnitRows + r;
-        const int64_t cand = p.col0(j) + c;
-        bool live = b < a.B && cand < a.N;
-        if (live && mask && mask[cand]) live = false;
-        if (live && cand == starts[b]) live = false;
-        a.m[i] = live ? INFINITY : -INFINITY;
+        const int64_t cand0 = p.col0(j) + 32 * g + 4 * v;
+        const int st = b < a.B ? starts[b] : -1;
+        float out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t cand = cand0 + e;
+            bool live = b < a.B && cand < a.N;
+            if (live && mask && mask[cand]) live = false;
+            if (live && cand == st) live = false;
+            out[e] = live ? INFINITY : -INFINITY;
+        }
+        reinterpret_cast<float4 *>(a.m)[i4] = make_float4(out[0], out[1], out[2], out[3]);
     }
     // query rows: the start rows, zero rows for padded sequences
     const int vec = a.Dp / 8;  // 16-byte vectors per row segment
