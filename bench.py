@@ -126,19 +126,24 @@ class ClockSampler:
 
     def summary(self):
         rows = [r.split(", ") for r in (self.out or "").strip().splitlines() if r.strip()]
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, watts = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
                 sm.append(float(r[1]))
                 mx = float(r[2])
+                try:
+                    watts.append(float(r[3]))
+                except ValueError:
+                    pass
                 for name, v in zip(names, r[5:9]):
                     if v.strip().lower() == "active":
                         reasons.add(name)
             except (ValueError, IndexError):
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": statistics.median(watts) if watts else None}
 
 
 def _dist():
