@@ -143,7 +143,8 @@ class ClockSampler:
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm),
-                "power_w": statistics.median(watts) if watts else None}
+                "power_w": statistics.median(watts) if watts else None,
+                "power_w_max": max(watts) if watts else None}
 
 
 def _dist():
