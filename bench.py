@@ -340,7 +340,8 @@ def run_ours(args):
     if is_div:
         cfg = workloads.DIVERSITY[args.workload]
         E_host = torch.from_numpy(cfg.table(seed=0)).pin_memory()
-        starts_host = torch.from_numpy(cfg.starts(seed=0)).pin_memory()
+        # each rank runs its own shard: the same table, its own sequences
+        starts_host = torch.from_numpy(cfg.starts(seed=rank)).pin_memory()
         ctx = es.dseq_create(E_host.to(dev))
         starts_dev = starts_host.to(dev)
         picks_dev = torch.empty((cfg.B, cfg.L), dtype=torch.int32, device=dev)
@@ -372,7 +373,8 @@ def run_ours(args):
         cfg = workloads.BMU[epoch_of]
         sx, sy = workloads.SOM_SIDES[epoch_of]
         sigma, radius = workloads.SOM_SIGMA, workloads.SOM_RADIUS
-        X_host = torch.from_numpy(cfg.samples(seed=0)).pin_memory()
+        # each rank runs its own shard: the same codebook, its own samples
+        X_host = torch.from_numpy(cfg.samples(seed=rank)).pin_memory()
         W_host = torch.from_numpy(cfg.codebook(seed=0)).pin_memory()
         X_dev, W_dev = X_host.to(dev), W_host.to(dev)
         idx_dev = torch.empty(cfg.n, dtype=torch.int32, device=dev)
@@ -405,7 +407,8 @@ def run_ours(args):
                   "l2": "flushed between steps (512 MB write)"}
     else:
         cfg = workloads.BMU[args.workload]
-        X_host = torch.from_numpy(cfg.samples(seed=0)).pin_memory()
+        # each rank runs its own shard: the same codebook, its own samples
+        X_host = torch.from_numpy(cfg.samples(seed=rank)).pin_memory()
         W_host = torch.from_numpy(cfg.codebook(seed=0)).pin_memory()
         X_dev, W_dev = X_host.to(dev), W_host.to(dev)
         idx_dev = torch.empty(cfg.n, dtype=torch.int32, device=dev)
