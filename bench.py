@@ -512,6 +512,17 @@ def run_ours(args):
             "kernel": kernel_name,
             "note": (f"achieved = algorithmic FLOP (2*{'N*D*B*L' if is_div else 'n*M*D'})"
                      f" / kernel time (CUDA events on the launching stream); {peak_note}")}
+    if "engine=1" in args.opt:
+        # the plain fp32 SIMT variant: bound by the FP32 pipe, 128 fp32 FMA
+        # lanes per SM, 2 FLOP each, at the maximum SM clock
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = clocks.get("sm_max_mhz") or 2070.0
+        alu_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+        roof.update({"bound": "alu", "peak": alu_peak, "frac": (achieved / alu_peak) if achieved else None,
+                     "peak_kind": "fp32 pipe, derived", "frac_of_burst": None,
+                     "kernel": "ffma_dseq_fold_kernel" if is_div else "ffma_bmu_kernel",
+                     "note": (f"achieved = algorithmic FLOP / kernel time ({'fold + commit launches' if is_div else 'one launch'}, CUDA events); peak = {sms} SMs x 128 "
+                              f"FP32 lanes x 2 FLOP x {mhz:.0f} MHz (derived, not measured)")})
     if stream_bytes is not None and k_avg_s:
         hbm_achieved = stream_bytes / k_avg_s / 1e9
         if hbm_achieved / hbm_peak > (roof["frac"] or 0.0):
