@@ -366,8 +366,6 @@ def run_ours(args):
 
         config = {"workload": args.workload, "N": cfg.N, "D": cfg.D, "B": cfg.B, "L": cfg.L,
                   "l2": "flushed between steps (512 MB write)"}
-        if args.opt:
-            config["options"] = list(args.opt)
     elif args.workload in workloads.SOM_EPOCH:
         epoch_of = workloads.SOM_EPOCH[args.workload]
         cfg = workloads.BMU[epoch_of]
@@ -431,6 +429,9 @@ def run_ours(args):
 
         config = {"workload": args.workload, "n": cfg.n, "M": cfg.M, "D": cfg.D,
                   "l2": "flushed between steps (512 MB write)"}
+
+    if args.opt:
+        config["options"] = list(args.opt)
 
     def barrier():
         torch.cuda.synchronize()
@@ -537,7 +538,8 @@ def run_ours(args):
         "metric": metric, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("f16 storage, f32 accumulate" if fp16_storage
+        "dtype": ("f32 (FFMA)" if "engine=1" in args.opt
+                  else "f16 storage, f32 accumulate" if fp16_storage
                   else "fp16x3-split (fp32-accurate), f32 accumulate"),
         "data": "synthetic", "config": config, "roofline": roof,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": int(h2d),

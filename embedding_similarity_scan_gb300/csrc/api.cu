@@ -718,9 +718,11 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     } else {
         // ---- FP32 FFMA path, one launch pair per iteration ----
         if (ctx->opt.criterion != 0) return fail(DSEQ_EINVAL, "the FFMA engine runs the max-min criterion only");
+        if (Bp / 128 > 65535) return fail(DSEQ_EINVAL, "the FFMA engine takes at most %d sequences", 65535 * 128);
         FfmaDseqArgs a;
-        a.Nf = round_up(N, 64);
+        a.Nf = round_up(N, 128);
         a.Bp = (int)Bp;
+        CUDA_TRY(ffma_configure());
         TRY(ctx->m.ensure((size_t)Bp * a.Nf * sizeof(float)));
         TRY(ctx->q.ensure((size_t)Bp * ctx->Dp * sizeof(float)));
         a.e_unit = ctx->e_unit.as<float>();
@@ -741,8 +743,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         for (int t = 0; t < L; ++t) launch_ffma_dseq_iteration(a, t, st);
         CUDA_TRY(cudaGetLastError());
         TRY(timer.stop(st));
-        g_stats.units = (Bp / 64) * (a.Nf / 64);
-        g_stats.tile_n = 64;
+        g_stats.units = (Bp / 128) * (a.Nf / 128);
+        g_stats.tile_n = 128;
         g_stats.grid = (int64_t)g_stats.units;
         g_stats.launches = 1 + 2 * (int64_t)L;
     }
@@ -883,15 +885,18 @@ int bmu_core(const float *dX, int64_t n, const float *dW, int64_t M, int32_t D, 
         g_stats.grid = plan.grid;
         g_stats.launches = 5;
     } else {
+        if (((n + 127) / 128) * ((M + 127) / 128) > INT32_MAX)
+            return fail(DSEQ_EINVAL, "the FFMA engine takes at most 2^31 - 1 tiles of 128 x 128");
         launch_row_sqnorm(dX, n, D, ws->xn.as<float>(), a.status, st);
         launch_row_sqnorm(dW, M, D, ws->wn.as<float>(), a.status, st);
         CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(ffma_configure());
         TRY(timer.start(st));
         launch_ffma_bmu(a, st);
         CUDA_TRY(cudaGetLastError());
         TRY(timer.stop(st));
-        g_stats.units = ((n + 63) / 64) * ((M + 63) / 64);
-        g_stats.tile_n = 64;
+        g_stats.units = ((n + 127) / 128) * ((M + 127) / 128);
+        g_stats.tile_n = 128;
         g_stats.grid = g_stats.units;
         g_stats.launches = 5;
     }

@@ -156,8 +156,8 @@ int tc_dseq_pair_max_clusters(int tile_n);
 // ---- diversity, FFMA path (ffma.cu) -----------------------------------------
 struct FfmaDseqArgs {
     const float *e_unit;   // N x Dp
-    float *q;              // Bp64 x Dp
-    float *m;              // Bp64 x Nf
+    float *q;              // Bp x Dp
+    float *m;              // Bp x Nf (Nf: N rounded up to 128)
     unsigned long long *keys;
     int32_t *picks;
     const int32_t *trace_slot;
@@ -166,6 +166,8 @@ struct FfmaDseqArgs {
     int64_t N, Nf;
     int B, Bp, L, Dp;
 };
+// Sets the FFMA kernels' shared-memory limit; call before their launches.
+cudaError_t ffma_configure();
 void launch_ffma_dseq_init(const FfmaDseqArgs &a, const int32_t *starts, const uint8_t *mask,
                            cudaStream_t st);
 void launch_ffma_dseq_iteration(const FfmaDseqArgs &a, int t, cudaStream_t st);

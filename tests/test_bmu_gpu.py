@@ -113,6 +113,32 @@ def test_tile_width_does_not_change_result(es):
             assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
 
 
+@pytest.mark.parametrize("D", [64, 30])
+def test_unaligned_operands(es, D):
+    """Operands that start 4 bytes past a 16-byte boundary: the FFMA engine
+    stages them element by element, and both engines give the same result
+    as for aligned copies of the same values."""
+    n, M = 300, 700
+    X = workloads.bmu_samples(n, D, seed=11)
+    W = workloads.codebook(M, D, seed=11)
+
+    def unaligned(A):
+        buf = torch.zeros(A.size + 1, dtype=torch.float32, device="cuda")
+        buf[1:].copy_(torch.from_numpy(A).reshape(-1).cuda())
+        view = buf[1:].view(A.shape)
+        assert view.data_ptr() % 16 == 4
+        return view
+
+    Xu, Wu = unaligned(X), unaligned(W)
+    for engine in (1, 0):
+        ref = _bmu(es, X, W, engine)
+        es.dseq_set_option("engine", engine)
+        idx, dist = es.bmu_search(Xu, Wu)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy(), ref[0]) and np.array_equal(dist.cpu().numpy(), ref[1])
+        check_bmu(X, W, np.arange(n), ref[0], ref[1])
+
+
 def test_host_buffers(es):
     X = workloads.bmu_samples(257, 24, seed=6)
     W = workloads.codebook(513, 24, seed=6)
