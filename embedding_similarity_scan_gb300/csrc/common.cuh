@@ -172,6 +172,14 @@ __device__ __forceinline__ void st_cg_hint(float4 *p, float4 v, uint64_t policy)
                  : "memory");
 }
 
+// Asynchronous prefetch of [p, p + bytes) into L2 under a cache policy; p
+// and bytes are multiples of 16.
+__device__ __forceinline__ void prefetch_l2_hint(const void *p, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes),
+                 "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));

@@ -311,10 +311,14 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
 
     // ---- per-unit work, shared by both iteration schemes ----
     // producer: the kblocks stages of unit v
-    auto produce_unit = [&](int t, int64_t v, uint64_t keep, uint64_t table_pol, uint64_t &waited,
-                            bool &first) {
+    auto produce_unit = [&](int t, int64_t v, uint64_t keep, uint64_t table_pol, uint64_t m_pol,
+                            uint64_t &waited, bool &first) {
         int beta, j;
         decode(v, beta, j);
+        // the unit's running minima (one contiguous tile), brought into L2
+        // ahead of the epilogue that reads them
+        prefetch_l2_hint(a.m + p.tile_base(j, beta),
+                         (uint32_t)p.width(j) * kUnitRows * (uint32_t)sizeof(float), m_pol);
         const int yq = beta * kUnitRows;
         // a narrow chunk still loads a full box (its tail rows unused)
         const int ye = (int)p.col0(j) + (int)rank * (p.width(j) / (kPair ? 2 : 1));
@@ -732,6 +736,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
             if (lane == 0) {
                 const uint64_t keep = l2_policy_evict_last();
                 const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
+                const uint64_t m_pol = l2_policy_evict_first();
                 for (int t = 0; t < a.L && !*abort_flag; ++t) {
                     stamp(a, t, 0);
                     bool first = true;
@@ -746,7 +751,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                         }
                         for (int64_t v = first_from(hb[h]); v < hb[h + 1] && !*abort_flag;
                              v += item_stride)
-                            produce_unit(t, v, keep, table_pol, waited, first);
+                            produce_unit(t, v, keep, table_pol, m_pol, waited, first);
                     }
                     record(a, t, 7, gate);
                     record(a, t, 10, waited);
