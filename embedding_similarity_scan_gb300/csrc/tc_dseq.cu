@@ -315,10 +315,13 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                             uint64_t &waited, bool &first) {
         int beta, j;
         decode(v, beta, j);
-        // the unit's running minima (one contiguous tile), brought into L2
-        // ahead of the epilogue that reads them
-        prefetch_l2_hint(a.m + p.tile_base(j, beta),
-                         (uint32_t)p.width(j) * kUnitRows * (uint32_t)sizeof(float), m_pol);
+        // fp16 storage, where the epilogue is the critical path: the unit's
+        // running minima (one contiguous tile) are brought into L2 ahead of
+        // the epilogue that reads them.  (The split-storage kernels are
+        // tensor-bound; there the prefetch only added DRAM reads.)
+        if (kF16)
+            prefetch_l2_hint(a.m + p.tile_base(j, beta),
+                             (uint32_t)p.width(j) * kUnitRows * (uint32_t)sizeof(float), m_pol);
         const int yq = beta * kUnitRows;
         // a narrow chunk still loads a full box (its tail rows unused)
         const int ye = (int)p.col0(j) + (int)rank * (p.width(j) / (kPair ? 2 : 1));
@@ -736,7 +739,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
             if (lane == 0) {
                 const uint64_t keep = l2_policy_evict_last();
                 const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
-                const uint64_t m_pol = l2_policy_evict_first();
+                const uint64_t m_pol = l2_policy_evict_normal();
                 for (int t = 0; t < a.L && !*abort_flag; ++t) {
                     stamp(a, t, 0);
                     bool first = true;
