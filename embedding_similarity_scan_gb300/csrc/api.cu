@@ -849,17 +849,17 @@ int bmu_core(const float *dX, int64_t n, const float *dW, int64_t M, int32_t D, 
     EventTimer timer;
     launch_bmu_keys_init(a.keys, n, st);
     if (opt.engine == 0) {
-        TRY(ws->x_split.ensure((size_t)n * 3 * Dp * sizeof(__half)));
-        TRY(ws->w_split.ensure((size_t)M * 2 * Dp * sizeof(__half)));
+        TRY(ws->x_split.ensure((size_t)n * kBmuPartsX * Dp * sizeof(__half)));
+        TRY(ws->w_split.ensure((size_t)M * kBmuPartsW * Dp * sizeof(__half)));
         TRY(ws->x_inv.ensure((size_t)n * sizeof(float)));
         TRY(ws->w_inv.ensure((size_t)M * sizeof(float)));
         a.x_split = ws->x_split.as<__half>();
         a.w_split = ws->w_split.as<__half>();
         a.x_inv_scale = ws->x_inv.as<float>();
         a.w_inv_scale = ws->w_inv.as<float>();
-        launch_bmu_prepare(dX, n, D, Dp, 1, ws->x_split.as<__half>(), ws->xn.as<float>(),
+        launch_bmu_prepare(dX, n, D, Dp, 0, ws->x_split.as<__half>(), ws->xn.as<float>(),
                            ws->x_inv.as<float>(), a.status, st);
-        launch_bmu_prepare(dW, M, D, Dp, 0, ws->w_split.as<__half>(), ws->wn.as<float>(),
+        launch_bmu_prepare(dW, M, D, Dp, 1, ws->w_split.as<__half>(), ws->wn.as<float>(),
                            ws->w_inv.as<float>(), a.status, st);
         CUDA_TRY(cudaGetLastError());
         TcPlan plan{};
@@ -875,8 +875,8 @@ int bmu_core(const float *dX, int64_t n, const float *dW, int64_t M, int32_t D, 
             plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
         }
         CUtensorMap tx, tw;
-        TRY(encode_f16_map(tx, a.x_split, 3 * Dp, n, kUnitRows));
-        TRY(encode_f16_map(tw, a.w_split, 2 * Dp, M, plan.pair ? plan.tile_n / 2 : plan.tile_n));
+        TRY(encode_f16_map(tx, a.x_split, kBmuPartsX * Dp, n, kUnitRows));
+        TRY(encode_f16_map(tw, a.w_split, kBmuPartsW * Dp, M, plan.pair ? plan.tile_n / 2 : plan.tile_n));
         TRY(timer.start(st));
         CUDA_TRY(launch_tc_bmu(a, plan, tx, tw, st));
         TRY(timer.stop(st));

@@ -101,14 +101,16 @@ void launch_table_prepare(const float *E, int64_t N, int D, int Dp, float *e_uni
                           __half *e_split, float *nrm, int *status, cudaStream_t st);
 
 // fp16 storage of the candidate table: row * 2^-e (max |.| in [0.5, 1)) rounded
-// to fp16, zero-padded to Dp; rn[r] = 1 / |stored row| (double sum).
+// to fp16, zero-padded to Dp; rn[r] = 1 / |stored row| (compensated fp32 sum).
 void launch_table_prepare_f16(const float *E, int64_t N, int D, int Dp, __half *e_f16,
                               float *rn, int *status, cudaStream_t st);
 
 // Rows of a BMU operand scaled by a per-row power of two (max |.| in [0.5, 1))
-// and split into fp16.  triple = 1: [hi*2^12 | hi | lo*2^12] (A side);
-// triple = 0: [hi | lo*2^12] (B side).  norm2[r] = |row|^2 (double sum),
-// inv_scale[r] = 1 / scale.
+// and split into fp16.  triple = 1: [hi*2^12 | hi | lo*2^12] (the codebook,
+// kBmuPartsW parts); triple = 0: [hi | lo*2^12] (the samples, kBmuPartsX
+// parts).  norm2[r] = |row|^2 (compensated fp32 sum), inv_scale[r] = 1 / scale.
+constexpr int kBmuPartsX = 2;
+constexpr int kBmuPartsW = 3;
 void launch_bmu_prepare(const float *A, int64_t rows, int D, int Dp, int triple, __half *split,
                         float *norm2, float *inv_scale, int *status, cudaStream_t st);
 
@@ -175,8 +177,8 @@ void launch_ffma_dseq_iteration(const FfmaDseqArgs &a, int t, cudaStream_t st);
 // ---- BMU ----------------------------------------------------------------------
 struct BmuArgs {
     const float *X, *W;          // fp32 inputs (FFMA path)
-    const __half *x_split;       // n x 3Dp (tensor path)
-    const __half *w_split;       // M x 2Dp (tensor path)
+    const __half *x_split;       // n x kBmuPartsX*Dp (tensor path)
+    const __half *w_split;       // M x kBmuPartsW*Dp (tensor path)
     const float *xn, *wn;        // squared norms
     const float *x_inv_scale, *w_inv_scale;
     unsigned long long *keys;    // n

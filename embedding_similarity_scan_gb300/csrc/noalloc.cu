@@ -70,8 +70,8 @@ extern "C" int bmu_search_noalloc(const float *X, int64_t n, const float *W, int
     const int Dp = (D + kKBlock - 1) / kKBlock * kKBlock;
     // scratch layout, every piece 256-byte aligned
     const size_t off_xs = 0;
-    const size_t off_ws = off_xs + align256((size_t)n * 3 * Dp * sizeof(__half));
-    const size_t off_xn = off_ws + align256((size_t)M * 2 * Dp * sizeof(__half));
+    const size_t off_ws = off_xs + align256((size_t)n * kBmuPartsX * Dp * sizeof(__half));
+    const size_t off_xn = off_ws + align256((size_t)M * kBmuPartsW * Dp * sizeof(__half));
     const size_t off_wn = off_xn + align256((size_t)n * sizeof(float));
     const size_t off_xi = off_wn + align256((size_t)M * sizeof(float));
     const size_t off_wi = off_xi + align256((size_t)n * sizeof(float));
@@ -121,9 +121,9 @@ extern "C" int bmu_search_noalloc(const float *X, int64_t n, const float *W, int
     e = cudaMemsetAsync(a.status, 0, sizeof(int), st);
     if (e != cudaSuccess) return host::fail_msg(DSEQ_ECUDA, cudaGetErrorString(e));
     launch_bmu_keys_init(a.keys, n, st);
-    launch_bmu_prepare(X, n, D, Dp, 1, const_cast<__half *>(a.x_split), const_cast<float *>(a.xn),
+    launch_bmu_prepare(X, n, D, Dp, 0, const_cast<__half *>(a.x_split), const_cast<float *>(a.xn),
                        const_cast<float *>(a.x_inv_scale), a.status, st);
-    launch_bmu_prepare(W, M, D, Dp, 0, const_cast<__half *>(a.w_split), const_cast<float *>(a.wn),
+    launch_bmu_prepare(W, M, D, Dp, 1, const_cast<__half *>(a.w_split), const_cast<float *>(a.wn),
                        const_cast<float *>(a.w_inv_scale), a.status, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return host::fail_msg(DSEQ_ECUDA, cudaGetErrorString(e));
@@ -132,8 +132,8 @@ extern "C" int bmu_search_noalloc(const float *X, int64_t n, const float *W, int
     plan.set_uniform(256, M);
     plan.grid = (int)(plan.units() < sms ? plan.units() : sms);
     CUtensorMap tx, tw;
-    if ((r = host::encode_map(tx, a.x_split, 3 * Dp, n, kUnitRows)) != DSEQ_OK) return r;
-    if ((r = host::encode_map(tw, a.w_split, 2 * Dp, M, plan.tile_n)) != DSEQ_OK) return r;
+    if ((r = host::encode_map(tx, a.x_split, kBmuPartsX * Dp, n, kUnitRows)) != DSEQ_OK) return r;
+    if ((r = host::encode_map(tw, a.w_split, kBmuPartsW * Dp, M, plan.tile_n)) != DSEQ_OK) return r;
     e = launch_tc_bmu(a, plan, tx, tw, st);
     if (e != cudaSuccess) return host::fail_msg(DSEQ_ECUDA, cudaGetErrorString(e));
     launch_bmu_finalize(a, st);

@@ -15,9 +15,19 @@
 // codebook against every sample block before moving to the next slice, so
 // the codebook is read from HBM once and the samples once per slice.
 //
+// Two kernels.  tc_bmu_kernel streams both operands through its stage ring.
+// tc_bmu_resident_kernel (CTA pairs, D <= 256) keeps a CTA's 128 split
+// sample rows in shared memory for a whole segment of a slice's chunks and
+// streams only the codebook, which removes the sample tiles' share of the
+// L2 -> SM operand traffic; both issue the same MMAs on the same data, so
+// their results are bitwise equal.
+//
 // Operands are pre-scaled per row by a power of two (max |.| in [0.5, 1))
-// and split into fp16 hi + lo * 2^-12 (prep.cu); three kind::f16 MMAs per
-// 32-wide K block accumulate 2^12 <x~, w~> in fp32 TMEM.  The epilogue forms
+// and split into fp16 (prep.cu): samples [hi | lo * 2^12], codebook
+// [hi * 2^12 | hi | lo * 2^12].  Three kind::f16 MMAs per 16-wide k step,
+// x_hi . (2^12 w_hi) + x_hi . (2^12 w_lo) + (2^12 x_lo) . w_hi, accumulate
+// 2^12 <x~, w~> in fp32 TMEM (the dropped lo . lo term is 2^-22 relative).
+// The epilogue forms
 // score_j = |w_j|^2 + acc * (1 / s_w[j]) * (-2^-11 / s_x[i]), keeps the
 // running (min score, lowest j) per row and folds it into the row's 64-bit
 // key with one atomicMin per unit; a finalize pass turns keys into
@@ -44,14 +54,46 @@ template <bool kPair>
 struct BmuCfg {
     static constexpr int kStagesT = kPair ? 5 : 3;
     static constexpr uint32_t kSubB = (kPair ? 128u : 256u) * kKBlock * 2;
-    static constexpr uint32_t kStage = 3 * kSubA + 2 * kSubB;
+    static constexpr uint32_t kStage = kBmuPartsX * kSubA + kBmuPartsW * kSubB;
     static constexpr size_t kSmemBytes =
         (size_t)kStagesT * kStage + 1024 + 256 + kEpiWarps * (kMaxGroups / 2) * 32 * sizeof(float2);
+};
+
+// Resident-sample kernel (CTA pairs): the sample rows of up to kResKBlocks
+// K blocks (D <= 256) stay in shared memory; 3 stages of codebook rows.
+struct BmuResCfg {
+    static constexpr int kResKBlocks = 8;
+    static constexpr uint32_t kSubB = 128u * kKBlock * 2;
+    static constexpr uint32_t kABytes = kBmuPartsX * kResKBlocks * kSubA;  // 128 KB
+    static constexpr int kStages = 3;
+    static constexpr uint32_t kStage = kBmuPartsW * kSubB;                 // 24 KB
+    static constexpr size_t kSmemBytes = 1024 + (size_t)kABytes + (size_t)kStages * kStage + 256 +
+                                         kEpiWarps * (kMaxGroups / 2) * 32 * sizeof(float2);
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
                                        ~static_cast<uintptr_t>(1023));
+}
+
+// The three MMAs of one 16-wide k step: sample parts at a, a + a_step
+// ([hi | lo]), codebook parts at b, b + b_step, b + 2 b_step
+// ([hi * 2^12 | hi | lo]); accumulate = 0 starts a new sum.
+template <bool kPair>
+__device__ __forceinline__ void bmu_mma_k16(uint32_t d_tmem, uint32_t a, uint32_t a_step, uint32_t b,
+                                            uint32_t b_step, uint32_t idesc, bool accumulate) {
+    const uint64_t x_hi = smem_desc_sw64(a), x_lo = smem_desc_sw64(a + a_step);
+    const uint64_t w_hi12 = smem_desc_sw64(b), w_hi = smem_desc_sw64(b + b_step),
+                   w_lo = smem_desc_sw64(b + 2 * b_step);
+    if (kPair) {
+        umma_f16_pair(d_tmem, x_hi, w_hi12, idesc, accumulate ? 1u : 0u);
+        umma_f16_pair(d_tmem, x_hi, w_lo, idesc, 1u);
+        umma_f16_pair(d_tmem, x_lo, w_hi, idesc, 1u);
+    } else {
+        umma_f16(d_tmem, x_hi, w_hi12, idesc, accumulate ? 1u : 0u);
+        umma_f16(d_tmem, x_hi, w_lo, idesc, 1u);
+        umma_f16(d_tmem, x_lo, w_hi, idesc, 1u);
+    }
 }
 
 struct BmuSchedule {
@@ -141,7 +183,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tile_n = (uint32_t)p.tile_n;
     const uint32_t b_rows = kPair ? tile_n / 2 : tile_n;
     const uint32_t sub_b = b_rows * kKBlock * 2;
-    const uint32_t tx_bytes = (kPair ? 2u : 1u) * (3 * kSubA + 2 * sub_b);
+    const uint32_t tx_bytes = (kPair ? 2u : 1u) * (kBmuPartsX * kSubA + kBmuPartsW * sub_b);
     const int kblocks = a.Dp / kKBlock;
     const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kUnitRows : kUnitRows, tile_n);
     const int groups = (int)(tile_n / 32);
@@ -164,22 +206,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                            kStatusPipeTimeout))
                         break;
                     uint8_t *sa = smem + s * kStageBytes;
-                    uint8_t *sb = sa + 3 * kSubA;
+                    uint8_t *sb = sa + kBmuPartsX * kSubA;
                     if (leader) mbar_arrive_expect_tx(&full[s], tx_bytes);
                     const int x = kb * kKBlock;
                     if (kPair) {
                         const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-                        tma_load_2d_pair(sa, &tmap_x, fb, x, yx, once);
-                        tma_load_2d_pair(sa + kSubA, &tmap_x, fb, a.Dp + x, yx, once);
-                        tma_load_2d_pair(sa + 2 * kSubA, &tmap_x, fb, 2 * a.Dp + x, yx, once);
-                        tma_load_2d_pair(sb, &tmap_w, fb, x, yw, keep);
-                        tma_load_2d_pair(sb + kSubB, &tmap_w, fb, a.Dp + x, yw, keep);
+#pragma unroll
+                        for (int part = 0; part < kBmuPartsX; ++part)
+                            tma_load_2d_pair(sa + part * kSubA, &tmap_x, fb, part * a.Dp + x, yx, once);
+#pragma unroll
+                        for (int part = 0; part < kBmuPartsW; ++part)
+                            tma_load_2d_pair(sb + part * kSubB, &tmap_w, fb, part * a.Dp + x, yw, keep);
                     } else {
-                        tma_load_2d_hint(sa, &tmap_x, &full[s], x, yx, once);
-                        tma_load_2d_hint(sa + kSubA, &tmap_x, &full[s], a.Dp + x, yx, once);
-                        tma_load_2d_hint(sa + 2 * kSubA, &tmap_x, &full[s], 2 * a.Dp + x, yx, once);
-                        tma_load_2d_hint(sb, &tmap_w, &full[s], x, yw, keep);
-                        tma_load_2d_hint(sb + kSubB, &tmap_w, &full[s], a.Dp + x, yw, keep);
+#pragma unroll
+                        for (int part = 0; part < kBmuPartsX; ++part)
+                            tma_load_2d_hint(sa + part * kSubA, &tmap_x, &full[s], part * a.Dp + x, yx, once);
+#pragma unroll
+                        for (int part = 0; part < kBmuPartsW; ++part)
+                            tma_load_2d_hint(sb + part * kSubB, &tmap_w, &full[s], part * a.Dp + x, yw, keep);
                     }
                     ++fills;
                 }
@@ -222,25 +266,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + s * kStageBytes);
-                    const uint32_t sb = sa + 3 * kSubA;
+                    const uint32_t sb = sa + kBmuPartsX * kSubA;
 #pragma unroll
-                    for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
-                        const uint32_t off = k16 * 32;
-                        const uint64_t a0 = smem_desc_sw64(sa + off);
-                        const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
-                        const uint64_t a2 = smem_desc_sw64(sa + 2 * kSubA + off);
-                        const uint64_t b0 = smem_desc_sw64(sb + off);
-                        const uint64_t b1 = smem_desc_sw64(sb + kSubB + off);
-                        if (kPair) {
-                            umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                            umma_f16_pair(d_tmem, a1, b1, idesc, 1u);
-                            umma_f16_pair(d_tmem, a2, b0, idesc, 1u);
-                        } else {
-                            umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                            umma_f16(d_tmem, a1, b1, idesc, 1u);
-                            umma_f16(d_tmem, a2, b0, idesc, 1u);
-                        }
-                    }
+                    for (int k16 = 0; k16 < kKBlock / 16; ++k16)
+                        bmu_mma_k16<kPair>(d_tmem, sa + k16 * 32, kSubA, sb + k16 * 32, kSubB, idesc,
+                                           (kb | k16) != 0);
                     if (kPair)
                         umma_commit_pair_multicast(&empty[s], 0x3);
                     else
@@ -338,6 +368,294 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
+// Work item of the resident-sample kernel: (sample block pair pb, a segment
+// [c0, c1) of one slice's chunks).  Items run slice-major, then by sample
+// block pair, then by segment, so consecutive items (dealt to neighbouring
+// CTA pairs) share their sample rows while those are in L2.  A segment may
+// be empty when a narrow last slice has fewer chunks than segments.
+struct BmuResSchedule {
+    int n_pb, n_chunk, slice_chunks, segs;
+    __device__ __forceinline__ void decode(int64_t u, int &pb, int &c0, int &c1) const {
+        const int64_t per_slice = (int64_t)n_pb * segs;
+        const int sl = (int)(u / per_slice);
+        const int64_t rem = u - (int64_t)sl * per_slice;
+        pb = (int)(rem / segs);
+        const int sg = (int)(rem - (int64_t)pb * segs);
+        const int first = sl * slice_chunks;
+        const int width = min(slice_chunks, n_chunk - first);
+        const int len = (width + segs - 1) / segs;
+        c0 = first + min(width, sg * len);
+        c1 = first + min(width, (sg + 1) * len);
+    }
+};
+
+// CTA-pair BMU kernel with the samples resident in shared memory.  Per item
+// each CTA loads its 128 sample rows (both parts, all K blocks) once, on the
+// a_full barrier; the MMA issuer releases them on a_empty after the item's
+// last MMA; the stage ring carries only codebook rows.
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_bmu_resident_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                           const __grid_constant__ CUtensorMap tmap_w, const BmuArgs a,
+                           const TcPlan p, const int slice_chunks, const int segs) {
+    using Cfg = BmuResCfg;
+    constexpr int kSt = Cfg::kStages;
+    constexpr uint32_t kSubB = Cfg::kSubB;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *s_x = smem;                          // [part][kblock] sample sub-tiles
+    uint8_t *s_w = smem + Cfg::kABytes;           // stage ring of codebook rows
+    uint64_t *full = reinterpret_cast<uint64_t *>(s_w + kSt * Cfg::kStage);
+    uint64_t *empty = full + kSt;
+    uint64_t *acc_full = empty + kSt;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *a_full = acc_empty + 2;
+    uint64_t *a_empty = a_full + 1;
+    uint64_t *final_bar = a_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(final_bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float2 *colc = reinterpret_cast<float2 *>(s_w + kSt * Cfg::kStage + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t tmo = a.timeout_ns;
+    const int kblocks = a.Dp / kKBlock;
+    // launch shape and operand geometry this kernel is written for; otherwise
+    // report and leave, uniformly across the grid, before touching anything
+    if (blockDim.x != kTcThreads || cluster_nctarank() != 2u || (gridDim.x & 1u) ||
+        kblocks > Cfg::kResKBlocks || p.tile_n > 256 || (p.n_beta & 1)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusInternal);
+        return;
+    }
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSt; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], kEpiWarps * 2);
+        }
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const BmuResSchedule sched{p.n_beta / 2, p.n_chunk, slice_chunks, segs};
+    const int64_t n_slices = (p.n_chunk + slice_chunks - 1) / slice_chunks;
+    const int64_t items = n_slices * sched.n_pb * segs;
+    const int64_t first_item = blockIdx.x >> 1, item_stride = gridDim.x >> 1;
+    const uint32_t tile_n = (uint32_t)p.tile_n;
+    const uint32_t b_rows = tile_n / 2;
+    const uint32_t sub_b = b_rows * kKBlock * 2;
+    const uint32_t tx_w = 2u * kBmuPartsW * sub_b;
+    const uint32_t tx_x = 2u * kBmuPartsX * (uint32_t)kblocks * kSubA;
+    const uint32_t idesc = idesc_f16_f32(2 * kUnitRows, tile_n);
+    const int groups = (int)(tile_n / 32);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_normal();
+            uint32_t fills = 0, x_loads = 0;
+            for (int64_t u = first_item; u < items && !*abort_flag; u += item_stride) {
+                int pb, c0, c1;
+                sched.decode(u, pb, c0, c1);
+                if (c0 >= c1) continue;
+                const int yx = (2 * pb + (int)rank) * kUnitRows;
+                // the previous item's MMAs have finished reading the samples
+                if (x_loads > 0 && !mbar_wait_bounded(a_empty, (x_loads - 1) & 1u, abort_flag,
+                                                       a.status, tmo, kStatusPipeTimeout))
+                    break;
+                if (leader) mbar_arrive_expect_tx(a_full, tx_x);
+                const uint32_t fa = mapa_shared(smem_u32(a_full), 0);
+                for (int part = 0; part < kBmuPartsX; ++part)
+                    for (int kb = 0; kb < kblocks; ++kb)
+                        tma_load_2d_pair(s_x + (part * kblocks + kb) * kSubA, &tmap_x, fa,
+                                         part * a.Dp + kb * kKBlock, yx, once);
+                ++x_loads;
+                bool ok = true;
+                for (int j = c0; j < c1 && ok; ++j) {
+                    const int yw = j * (int)tile_n + (int)(rank * b_rows);
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        const uint32_t s = fills % kSt, par = (fills / kSt) & 1u;
+                        if (!mbar_wait_bounded(&empty[s], par ^ 1u, abort_flag, a.status, tmo,
+                                               kStatusPipeTimeout)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *sb = s_w + s * Cfg::kStage;
+                        if (leader) mbar_arrive_expect_tx(&full[s], tx_w);
+                        const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+#pragma unroll
+                        for (int part = 0; part < kBmuPartsW; ++part)
+                            tma_load_2d_pair(sb + part * kSubB, &tmap_w, fb, part * a.Dp + kb * kKBlock,
+                                             yw, keep);
+                        ++fills;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {
+                // the pair's copies complete on the leader's barriers: give the
+                // ones still in flight time to land
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
+                }
+            }
+            if (*abort_flag && leader) {
+                volatile int never = 0;
+                const uint64_t lim = tmo < 1000000000ull ? tmo : 1000000000ull;
+                for (uint32_t s = 0; s < kSt && s < fills; ++s) {
+                    const uint32_t n_s = fills / kSt + (s < fills % kSt ? 1u : 0u);
+                    mbar_wait_bounded(&full[s], (n_s - 1) & 1u, &never, a.status, lim, kStatusPipeTimeout);
+                }
+                if (x_loads > 0)
+                    mbar_wait_bounded(a_full, (x_loads - 1) & 1u, &never, a.status, lim, kStatusPipeTimeout);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            uint32_t consumed = 0, acc_uses = 0, x_uses = 0;
+            bool ok = true;
+            for (int64_t u = first_item; u < items && ok && !*abort_flag; u += item_stride) {
+                int pb, c0, c1;
+                sched.decode(u, pb, c0, c1);
+                if (c0 >= c1) continue;
+                if (!mbar_wait_bounded(a_full, x_uses & 1u, abort_flag, a.status, tmo, kStatusPipeTimeout))
+                    break;
+                tc_fence_after();
+                const uint32_t sx = smem_u32(s_x);
+                for (int j = c0; j < c1 && ok; ++j) {
+                    const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+                    if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
+                                           kStatusPipeTimeout)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * kAccCols;
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        const uint32_t s = consumed % kSt, par = (consumed / kSt) & 1u;
+                        if (!mbar_wait_bounded(&full[s], par, abort_flag, a.status, tmo,
+                                               kStatusPipeTimeout)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sb = smem_u32(s_w + s * Cfg::kStage);
+                        const uint32_t sa = sx + (uint32_t)kb * kSubA;
+#pragma unroll
+                        for (int k16 = 0; k16 < kKBlock / 16; ++k16)
+                            bmu_mma_k16<true>(d_tmem, sa + k16 * 32, (uint32_t)kblocks * kSubA,
+                                              sb + k16 * 32, kSubB, idesc, (kb | k16) != 0);
+                        umma_commit_pair_multicast(&empty[s], 0x3);
+                        ++consumed;
+                    }
+                    if (!ok) break;
+                    umma_commit_pair_multicast(&acc_full[buf], 0x3);
+                    ++acc_uses;
+                }
+                if (!ok) break;
+                // the samples are free once this item's MMAs have completed
+                umma_commit_pair_multicast(a_empty, 0x3);
+                ++x_uses;
+            }
+            volatile int never = 0;
+            umma_commit_pair(final_bar);
+            mbar_wait_bounded(final_bar, 0, &never, a.status,
+                              tmo < 1000000000ull ? tmo : 1000000000ull, kStatusPipeTimeout);
+        }
+        __syncwarp();
+    } else {
+        const int e = warp - 2, q = warp & 3, h = e >> 2;
+        const int r = 32 * q + lane;
+        float2 *my_colc = colc + e * (kMaxGroups / 2) * 32;
+        uint32_t acc_uses = 0;
+        const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+        bool ok = true;
+        for (int64_t u = first_item; u < items && ok; u += item_stride) {
+            int pb, c0, c1;
+            sched.decode(u, pb, c0, c1);
+            const int beta = 2 * pb + (int)rank;
+            const int64_t row = (int64_t)beta * kUnitRows + r;
+            const float cx = row < a.n ? -a.x_inv_scale[row] * (1.0f / 2048.0f) : 0.0f;
+            for (int j = c0; j < c1; ++j) {
+                // this warp's (at most 4) column groups' constants, fetched before the wait
+                float2 cv[kMaxGroups / 2];
+#pragma unroll
+                for (int k = 0; k < kMaxGroups / 2; ++k) {
+                    const int64_t col = (int64_t)j * tile_n + 32 * (h + 2 * k) + lane;
+                    cv[k] = (h + 2 * k < groups && col < a.M)
+                                ? make_float2(__ldg(a.wn + col), __ldg(a.w_inv_scale + col))
+                                : make_float2(INFINITY, 0.0f);
+                }
+                const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+                // every lane waits; the warp proceeds only if all of them saw the phase
+                const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status, tmo,
+                                                     kStatusPipeTimeout);
+                if (!__all_sync(0xffffffffu, ready)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float best = INFINITY;
+                uint32_t best_j = 0xffffffffu;
+                const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < kMaxGroups / 2; ++k) my_colc[k * 32 + lane] = cv[k];
+                __syncwarp();
+                for (int g = h; g < groups; g += 2) {
+                    const float2 *cg = my_colc + ((g - h) >> 1) * 32;
+                    float acc[32];
+                    tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
+                    tmem_wait_ld();
+                    const uint32_t cbase = (uint32_t)j * tile_n + 32u * (uint32_t)g;
+#pragma unroll
+                    for (int z = 0; z < 32; ++z) {
+                        const float2 cc = cg[z];
+                        const float sc = fmaf(acc[z] * cc.y, cx, cc.x);
+                        if (sc < best) {
+                            best = sc;
+                            best_j = cbase + z;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
+                ++acc_uses;
+                if (row < a.n && best_j != 0xffffffffu) atomicMin(a.keys + row, min_key(best, best_j));
+            }
+        }
+    }
+
+    __syncthreads();
+    // the leader's MMAs into both CTAs' TMEM are done before either frees it
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
@@ -346,7 +664,7 @@ cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &
     int dev = 0, l2 = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
-    const double row_bytes = 2.0 * a.Dp * 2.0;
+    const double row_bytes = (double)kBmuPartsW * a.Dp * 2.0;
     int slice = (int)((0.5 * (double)l2) / (row_bytes * p.tile_n));
     if (slice < 1) slice = 1;
     if (slice > p.n_chunk) slice = p.n_chunk;
@@ -354,6 +672,33 @@ cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &
     TcPlan pp = p;
     CUtensorMap mx = tmap_x, mw = tmap_w;
     int sl = slice;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.pair && a.Dp <= BmuResCfg::kResKBlocks * kKBlock) {
+        // samples resident: enough segments per slice that every CTA pair
+        // gets about 32 items (the last ones then leave little imbalance)
+        const int64_t n_slices = (p.n_chunk + slice - 1) / slice;
+        const int64_t n_pb = p.n_beta / 2;
+        int64_t segs = (32 * (int64_t)(p.grid / 2) + n_pb * n_slices - 1) / (n_pb * n_slices);
+        if (segs < 1) segs = 1;
+        if (segs > slice) segs = slice;
+        int sg = (int)segs;
+        const size_t smem = BmuResCfg::kSmemBytes;
+        cudaError_t err = cudaFuncSetAttribute(tc_bmu_resident_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        cfg.dynamicSmemBytes = smem;
+        return cudaLaunchKernelEx(&cfg, tc_bmu_resident_kernel, mx, mw, aa, pp, sl, sg);
+    }
     if (!p.pair) {
         const size_t smem = BmuCfg<false>::kSmemBytes;
         cudaError_t err = cudaFuncSetAttribute(tc_bmu_kernel<false>,
@@ -367,18 +712,7 @@ cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &
     cudaError_t err = cudaFuncSetAttribute(tc_bmu_kernel<true>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, tc_bmu_kernel<true>, mx, mw, aa, pp, sl);
 }
 

@@ -189,7 +189,7 @@ int som_epoch(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_
  *  - no call allocates: the scratch (split operands, norms, scales, keys,
  *    status) lives in one fixed 64 MiB array inside the library, which every
  *    GPU that loads the library holds until the process exits.  A request
- *    needing more (about n*(6*Dp + 16) + M*(4*Dp + 8) bytes, Dp = D rounded
+ *    needing more (about n*(4*Dp + 16) + M*(6*Dp + 8) bytes, Dp = D rounded
  *    up to 32) fails with DSEQ_EINVAL and says how much it needed;
  *  - every call shares that one array, so calls whose GPU work overlaps
  *    (other threads, other streams) race and give wrong results: serialise

@@ -158,13 +158,15 @@ def test_invalid(es):
         es.bmu_search(X, np.ones((6, 9), np.float32))
 
 
-@pytest.mark.parametrize("name", ["som256", "som512"])
-def test_full_size_sampled(es, name):
-    """The full configurations, checked on a seeded sample of rows."""
+@pytest.mark.parametrize("name,engine", [("som256", 0), ("som512", 0), ("som256", 1)],
+                         ids=lambda c: str(c))
+def test_full_size_sampled(es, name, engine):
+    """The full configurations (and som256 on the FFMA engine), checked on a
+    seeded sample of rows."""
     cfg = workloads.BMU[name]
     X = cfg.samples(seed=0)
     W = cfg.codebook(seed=0)
-    idx, dist = _bmu(es, X, W)
+    idx, dist = _bmu(es, X, W, engine)
     sample = np.sort(np.random.default_rng(0).choice(cfg.n, cfg.oracle_samples, replace=False))
     check_bmu(X, W, sample, idx, dist)
     assert np.all((idx >= 0) & (idx < cfg.M)) and np.all(dist >= 0)

@@ -265,15 +265,17 @@ def test_barrier_timeout_returns_cleanly(es, criterion, pair):
 FULL = ["page1", "d384", "d1024", "scale"]
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_teacher_forced(es, name):
+@pytest.mark.parametrize("name,engine", [(n, 0) for n in FULL] + [("page1", 1)],
+                         ids=lambda c: str(c))
+def test_full_size_teacher_forced(es, name, engine):
     """The full configurations, in the launch configuration the benchmark
-    times, with a seeded subset of sequences followed by the oracle."""
+    times (and the page-1 shape on the FFMA engine), with a seeded subset of
+    sequences followed by the oracle."""
     cfg = workloads.DIVERSITY[name]
     E = cfg.table(seed=0)
     starts = cfg.starts(seed=0)
     tr = np.sort(np.random.default_rng(0).choice(cfg.B, cfg.oracle_seqs, replace=False))
-    picks, trace = _run(es, E, starts, cfg.L, trace_seqs=tr.astype(np.int32))
+    picks, trace = _run(es, E, starts, cfg.L, trace_seqs=tr.astype(np.int32), engine=engine)
     check_dseq_teacher_forced(E, starts[tr], None, picks[tr], trace, np.arange(tr.size))
     # picks of every sequence: in range, distinct, never the start
     assert np.all((picks >= 0) & (picks < cfg.N))
