@@ -45,7 +45,14 @@ PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = {
     "tc_dseq_kernel": ["tc_dseq.cu", "common.cuh", "internal.h", "numeric.cuh"],
     "tc_bmu_kernel": ["tc_bmu.cu", "common.cuh", "internal.h"],
+    "tc_bmu_resident_kernel": ["tc_bmu.cu", "common.cuh", "internal.h"],
 }
+
+
+def _bmu_kernel_name(D: int, opts) -> str:
+    """The BMU kernel the library launches: the resident-sample CTA-pair
+    kernel for D <= 256, else the streaming one."""
+    return "tc_bmu_resident_kernel" if D <= 256 and "pair=0" not in opts else "tc_bmu_kernel"
 
 
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
@@ -383,7 +390,7 @@ def run_ours(args):
         # the update's algorithmic bytes: read the samples and their BMUs,
         # read and write the codebook
         update_bytes = 4.0 * cfg.n * cfg.D + 4.0 * cfg.n + 8.0 * cfg.M * cfg.D
-        kernel_name = "tc_bmu_kernel"
+        kernel_name = _bmu_kernel_name(cfg.D, args.opt)
         metric, unit = "SOM epoch samples/s", "samples/s"
         update_ns = []
 
@@ -414,7 +421,7 @@ def run_ours(args):
         units = cfg.n
         flop = 2.0 * cfg.n * cfg.M * cfg.D
         stream_bytes = None
-        kernel_name = "tc_bmu_kernel"
+        kernel_name = _bmu_kernel_name(cfg.D, args.opt)
         metric, unit = "BMU samples/s", "samples/s"
 
         def step():
