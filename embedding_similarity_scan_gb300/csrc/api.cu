@@ -75,6 +75,7 @@ struct Options {
     int64_t storage = 0;
     int64_t criterion = 0;
     int64_t resume = 0;
+    int64_t slice = 0;
 };
 std::mutex g_opt_mu;
 Options g_defaults;
@@ -115,6 +116,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "fault_skip_arrive") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "fault_skip_arrive must be 0 or 1");
         o.fault_skip_arrive = v;
+    } else if (n == "slice") {
+        if (v < 0 || v > (int64_t(1) << 24)) return fail(DSEQ_EINVAL, "slice out of range");
+        o.slice = v;
     } else {
         return fail(DSEQ_EINVAL, "unknown option '%s'", name);
     }
@@ -130,6 +134,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "grid") return o.grid;
     if (n == "timeout_ms") return o.timeout_ms;
     if (n == "fault_skip_arrive") return o.fault_skip_arrive;
+    if (n == "slice") return o.slice;
     if (n == "timeline") return o.timeline;
     if (n == "pair") return o.pair;
     if (n == "storage") return o.storage;
@@ -878,7 +883,7 @@ int bmu_core(const float *dX, int64_t n, const float *dW, int64_t M, int32_t D, 
         TRY(encode_f16_map(tx, a.x_split, kBmuPartsX * Dp, n, kUnitRows));
         TRY(encode_f16_map(tw, a.w_split, kBmuPartsW * Dp, M, plan.pair ? plan.tile_n / 2 : plan.tile_n));
         TRY(timer.start(st));
-        CUDA_TRY(launch_tc_bmu(a, plan, tx, tw, st));
+        CUDA_TRY(launch_tc_bmu(a, plan, tx, tw, (int)opt.slice, st));
         TRY(timer.stop(st));
         g_stats.units = plan.units();
         g_stats.tile_n = plan.tile_n;

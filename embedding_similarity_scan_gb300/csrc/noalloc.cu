@@ -134,7 +134,7 @@ extern "C" int bmu_search_noalloc(const float *X, int64_t n, const float *W, int
     CUtensorMap tx, tw;
     if ((r = host::encode_map(tx, a.x_split, kBmuPartsX * Dp, n, kUnitRows)) != DSEQ_OK) return r;
     if ((r = host::encode_map(tw, a.w_split, kBmuPartsW * Dp, M, plan.tile_n)) != DSEQ_OK) return r;
-    e = launch_tc_bmu(a, plan, tx, tw, st);
+    e = launch_tc_bmu(a, plan, tx, tw, 0, st);
     if (e != cudaSuccess) return host::fail_msg(DSEQ_ECUDA, cudaGetErrorString(e));
     launch_bmu_finalize(a, st);
     e = cudaGetLastError();

@@ -659,13 +659,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }  // namespace
 
 cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
-                          const CUtensorMap &tmap_w, cudaStream_t st) {
+                          const CUtensorMap &tmap_w, int slice_chunks, cudaStream_t st) {
     // neuron slice: chunks whose split rows fill about half of L2
     int dev = 0, l2 = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
     const double row_bytes = (double)kBmuPartsW * a.Dp * 2.0;
     int slice = (int)((0.5 * (double)l2) / (row_bytes * p.tile_n));
+    if (slice_chunks > 0) slice = slice_chunks;
     if (slice < 1) slice = 1;
     if (slice > p.n_chunk) slice = p.n_chunk;
     BmuArgs aa = a;

@@ -240,9 +240,13 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 row scaled by a power of two, then rounded once to fp16),
  *                 one product per step, distances exact for the stored rows
  *                 up to fp32 accumulation ("load FP16, compute FP32").
- *   "pair"        1 = the diversity kernel runs on CTA pairs (clusters of
- *                 two SMs) that share each tensor-core MMA (each SM stages
- *                 half of the candidate tile; default); 0 = one CTA per MMA.
+ *   "pair"        1 = the tensor-core kernels run on CTA pairs (clusters of
+ *                 two SMs) that share each MMA (each SM stages half of the
+ *                 candidate or neuron tile; default); 0 = one CTA per MMA.
+ *   "slice"       bmu_search: neuron chunks per codebook slice, the part of
+ *                 the codebook every CTA sweeps against all samples before
+ *                 moving on; 0 = as many as fill about half of L2 (default).
+ *                 Any value gives the same results.
  *   "timeline"    1 = dseq_run records, per CTA and iteration of the
  *                 tensor-core kernel, device timestamps of its phases (read
  *                 them back with dseq_get_timeline); default 0.

@@ -33,7 +33,7 @@ def es():
 @pytest.fixture(autouse=True)
 def _reset_options(es):
     yield
-    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("pair", 1)):
+    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("pair", 1), ("slice", 0)):
         es.dseq_set_option(name, v)
 
 
@@ -137,6 +137,21 @@ def test_unaligned_operands(es, D):
         torch.cuda.synchronize()
         assert np.array_equal(idx.cpu().numpy(), ref[0]) and np.array_equal(dist.cpu().numpy(), ref[1])
         check_bmu(X, W, np.arange(n), ref[0], ref[1])
+
+
+@pytest.mark.parametrize("slice_chunks,grid", [(3, 0), (2, 8), (1, 4), (5, 2)])
+def test_slices_and_segments_do_not_change_result(es, slice_chunks, grid):
+    """Several codebook slices, a narrow last slice and (with few CTA pairs
+    and many segments) empty segments: the same bits as one slice and as the
+    single-CTA streaming kernel."""
+    X = workloads.bmu_samples(700, 64, seed=12)    # 6 sample blocks (3 pairs)
+    W = workloads.codebook(1700, 64, seed=12)      # 7 chunks of 256 neurons
+    ref = _bmu(es, X, W, pair=0)
+    check_bmu(X, W, np.arange(700), ref[0], ref[1])
+    es.dseq_set_option("slice", slice_chunks)
+    es.dseq_set_option("grid", grid)
+    got = _bmu(es, X, W, pair=1)
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
 
 
 def test_host_buffers(es):
