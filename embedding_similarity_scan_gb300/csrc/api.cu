@@ -70,6 +70,7 @@ struct Options {
     int64_t grid = 0;
     int64_t timeout_ms = 10000;
     int64_t fault_skip_arrive = 0;
+    int64_t fault_skip_copy = 0;
     int64_t timeline = 0;
     int64_t pair = 1;
     int64_t storage = 0;
@@ -116,6 +117,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "fault_skip_arrive") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "fault_skip_arrive must be 0 or 1");
         o.fault_skip_arrive = v;
+    } else if (n == "fault_skip_copy") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "fault_skip_copy must be 0 or 1");
+        o.fault_skip_copy = v;
     } else if (n == "slice") {
         if (v < 0 || v > (int64_t(1) << 24)) return fail(DSEQ_EINVAL, "slice out of range");
         o.slice = v;
@@ -135,6 +139,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "timeout_ms") return o.timeout_ms;
     if (n == "fault_skip_arrive") return o.fault_skip_arrive;
     if (n == "slice") return o.slice;
+    if (n == "fault_skip_copy") return o.fault_skip_copy;
     if (n == "timeline") return o.timeline;
     if (n == "pair") return o.pair;
     if (n == "storage") return o.storage;
@@ -851,6 +856,7 @@ int bmu_core(const float *dX, int64_t n, const float *dW, int64_t M, int32_t D, 
     a.D = D;
     a.Dp = Dp;
     a.timeout_ns = (uint64_t)opt.timeout_ms * 1000000ull;
+    a.fault_skip_copy = (int)opt.fault_skip_copy;
     EventTimer timer;
     launch_bmu_keys_init(a.keys, n, st);
     if (opt.engine == 0) {

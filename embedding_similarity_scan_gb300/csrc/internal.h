@@ -188,6 +188,9 @@ struct BmuArgs {
     int64_t n, M;
     int D, Dp;
     uint64_t timeout_ns;
+    // test only: CTA 0 leaves out one copy of its first codebook stage, so
+    // that stage never fills and the waits on it run out
+    int fault_skip_copy;
 };
 void launch_bmu_keys_init(unsigned long long *keys, int64_t n, cudaStream_t st);
 void launch_ffma_bmu(const BmuArgs &a, cudaStream_t st);

@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // the same time; evict-first would drop it between those reads.
             const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_normal();
             uint32_t fills = 0;
+            bool skip_copy = a.fault_skip_copy && blockIdx.x == 0;
             for (int64_t u = first_item; u < units && !*abort_flag; u += item_stride) {
                 int blk, j;
                 sched.decode(u, blk, j);
@@ -214,17 +215,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                         for (int part = 0; part < kBmuPartsX; ++part)
                             tma_load_2d_pair(sa + part * kSubA, &tmap_x, fb, part * a.Dp + x, yx, once);
-#pragma unroll
-                        for (int part = 0; part < kBmuPartsW; ++part)
+                        for (int part = 0; part < kBmuPartsW - (skip_copy ? 1 : 0); ++part)
                             tma_load_2d_pair(sb + part * kSubB, &tmap_w, fb, part * a.Dp + x, yw, keep);
                     } else {
 #pragma unroll
                         for (int part = 0; part < kBmuPartsX; ++part)
                             tma_load_2d_hint(sa + part * kSubA, &tmap_x, &full[s], part * a.Dp + x, yx, once);
-#pragma unroll
-                        for (int part = 0; part < kBmuPartsW; ++part)
+                        for (int part = 0; part < kBmuPartsW - (skip_copy ? 1 : 0); ++part)
                             tma_load_2d_hint(sb + part * kSubB, &tmap_w, &full[s], part * a.Dp + x, yw, keep);
                     }
+                    skip_copy = false;
                     ++fills;
                 }
             }
@@ -473,6 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_normal();
             uint32_t fills = 0, x_loads = 0;
+            bool skip_copy = a.fault_skip_copy && blockIdx.x == 0;
             for (int64_t u = first_item; u < items && !*abort_flag; u += item_stride) {
                 int pb, c0, c1;
                 sched.decode(u, pb, c0, c1);
@@ -502,10 +503,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         uint8_t *sb = s_w + s * Cfg::kStage;
                         if (leader) mbar_arrive_expect_tx(&full[s], tx_w);
                         const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-#pragma unroll
-                        for (int part = 0; part < kBmuPartsW; ++part)
+                        for (int part = 0; part < kBmuPartsW - (skip_copy ? 1 : 0); ++part)
                             tma_load_2d_pair(sb + part * kSubB, &tmap_w, fb, part * a.Dp + kb * kKBlock,
                                              yw, keep);
+                        skip_copy = false;
                         ++fills;
                     }
                 }

@@ -254,6 +254,10 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 the cross-CTA "half done" counter, so the other CTAs'
  *                 waits run out (the kernel then returns DSEQ_ETIMEOUT
  *                 without hanging).
+ *   "fault_skip_copy"    test only: 1 makes CTA 0 of the tensor-core BMU
+ *                 kernels leave out one copy of its first codebook stage, so
+ *                 that stage never fills and the waits on it run out
+ *                 (bmu_search then returns DSEQ_ETIMEOUT without hanging).
  * Errors: DSEQ_EINVAL for an unknown name or a value out of range. */
 int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value);
 

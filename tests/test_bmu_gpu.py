@@ -33,7 +33,8 @@ def es():
 @pytest.fixture(autouse=True)
 def _reset_options(es):
     yield
-    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("pair", 1), ("slice", 0)):
+    for name, v in (("engine", 0), ("tile_n", 0), ("grid", 0), ("pair", 1), ("slice", 0),
+                    ("fault_skip_copy", 0), ("timeout_ms", 10000)):
         es.dseq_set_option(name, v)
 
 
@@ -151,6 +152,26 @@ def test_slices_and_segments_do_not_change_result(es, slice_chunks, grid):
     es.dseq_set_option("slice", slice_chunks)
     es.dseq_set_option("grid", grid)
     got = _bmu(es, X, W, pair=1)
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+@pytest.mark.parametrize("pair,D", [(1, 64), (1, 300), (0, 64)],
+                         ids=["resident", "streaming_pair", "single_cta"])
+def test_pipeline_timeout_returns_cleanly(es, pair, D):
+    """CTA 0 leaves out one copy of its first codebook stage: the waits on
+    that stage run out after the time limit, the call returns DSEQ_ETIMEOUT,
+    and the GPU stays usable (the next call gives the same bits as before)."""
+    X = workloads.bmu_samples(600, D, seed=13)
+    W = workloads.codebook(900, D, seed=13)
+    ref = _bmu(es, X, W, pair=pair)
+    es.dseq_set_option("timeout_ms", 300)
+    es.dseq_set_option("fault_skip_copy", 1)
+    with pytest.raises(es.DseqError) as ei:
+        _bmu(es, X, W, pair=pair)
+    assert ei.value.code == es.DSEQ_ETIMEOUT
+    es.dseq_set_option("fault_skip_copy", 0)
+    es.dseq_set_option("timeout_ms", 10000)
+    got = _bmu(es, X, W, pair=pair)
     assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
 
 
