@@ -60,15 +60,19 @@ struct BmuCfg {
 };
 
 // Resident-sample kernel (CTA pairs): the sample rows of up to kResKBlocks
-// K blocks (D <= 256) stay in shared memory; 3 stages of codebook rows.
+// K blocks (D <= 256) stay in shared memory; 4 stages of codebook rows; each
+// epilogue warp stages one 32-neuron group's constants at a time.  The
+// layout fills 231,680 of the 232,448 bytes a CTA may have, so it leaves no
+// room to align the base: the kernel requires (and checks) that the dynamic
+// shared memory starts on a 1024-byte boundary.
 struct BmuResCfg {
     static constexpr int kResKBlocks = 8;
     static constexpr uint32_t kSubB = 128u * kKBlock * 2;
     static constexpr uint32_t kABytes = kBmuPartsX * kResKBlocks * kSubA;  // 128 KB
-    static constexpr int kStages = 3;
+    static constexpr int kStages = 4;
     static constexpr uint32_t kStage = kBmuPartsW * kSubB;                 // 24 KB
-    static constexpr size_t kSmemBytes = 1024 + (size_t)kABytes + (size_t)kStages * kStage + 256 +
-                                         kEpiWarps * (kMaxGroups / 2) * 32 * sizeof(float2);
+    static constexpr size_t kSmemBytes =
+        (size_t)kABytes + (size_t)kStages * kStage + 256 + kEpiWarps * 32 * sizeof(float2);
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -400,8 +404,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     using Cfg = BmuResCfg;
     constexpr int kSt = Cfg::kStages;
     constexpr uint32_t kSubB = Cfg::kSubB;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
+    extern __shared__ __align__(1024) uint8_t smem_res[];
+    uint8_t *smem = smem_res;
     uint8_t *s_x = smem;                          // [part][kblock] sample sub-tiles
     uint8_t *s_w = smem + Cfg::kABytes;           // stage ring of codebook rows
     uint64_t *full = reinterpret_cast<uint64_t *>(s_w + kSt * Cfg::kStage);
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // launch shape and operand geometry this kernel is written for; otherwise
     // report and leave, uniformly across the grid, before touching anything
     if (blockDim.x != kTcThreads || cluster_nctarank() != 2u || (gridDim.x & 1u) ||
-        kblocks > Cfg::kResKBlocks || p.tile_n > 256 || (p.n_beta & 1)) {
+        kblocks > Cfg::kResKBlocks || p.tile_n > 256 || (p.n_beta & 1) || (smem_u32(smem) & 1023u)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusInternal);
         return;
     }
@@ -587,7 +591,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
         const int e = warp - 2, q = warp & 3, h = e >> 2;
         const int r = 32 * q + lane;
-        float2 *my_colc = colc + e * (kMaxGroups / 2) * 32;
+        float2 *my_colc = colc + e * 32;
         uint32_t acc_uses = 0;
         const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
         bool ok = true;
@@ -619,12 +623,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float best = INFINITY;
                 uint32_t best_j = 0xffffffffu;
                 const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
-                __syncwarp();
 #pragma unroll
-                for (int k = 0; k < kMaxGroups / 2; ++k) my_colc[k * 32 + lane] = cv[k];
-                __syncwarp();
-                for (int g = h; g < groups; g += 2) {
-                    const float2 *cg = my_colc + ((g - h) >> 1) * 32;
+                for (int k = 0; k < kMaxGroups / 2; ++k) {
+                    const int g = h + 2 * k;
+                    if (g >= groups) break;
+                    __syncwarp();
+                    my_colc[lane] = cv[k];
+                    __syncwarp();
+                    const float2 *cg = my_colc;
                     float acc[32];
                     tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
                     tmem_wait_ld();
