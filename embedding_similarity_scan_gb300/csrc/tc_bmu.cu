@@ -494,6 +494,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tma_load_2d_pair(s_x + (part * kblocks + kb) * kSubA, &tmap_x, fa,
                                          part * a.Dp + kb * kKBlock, yx, once);
                 ++x_loads;
+                // bring the next item's sample rows (one contiguous block of
+                // the split samples) into L2 while this item runs, so its
+                // reload at the item boundary is an L2 hit
+                if (u + item_stride < items) {
+                    int pb2, d0, d1;
+                    sched.decode(u + item_stride, pb2, d0, d1);
+                    const int64_t row2 = (int64_t)(2 * pb2 + (int)rank) * kUnitRows;
+                    if (pb2 != pb && row2 < a.n) {
+                        const int64_t rows = min((int64_t)kUnitRows, a.n - row2);
+                        prefetch_l2_hint(a.x_split + row2 * kBmuPartsX * a.Dp,
+                                         (uint32_t)(rows * kBmuPartsX * a.Dp * (int64_t)sizeof(__half)), once);
+                    }
+                }
                 bool ok = true;
                 for (int j = c0; j < c1 && ok; ++j) {
                     const int yw = j * (int)tile_n + (int)(rank * b_rows);
