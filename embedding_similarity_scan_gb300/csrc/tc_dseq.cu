@@ -59,24 +59,26 @@ constexpr int kMaxGroups = 8;
 // Stage geometry.  Split storage (fp32-accurate): A = 3 x (128 x 32),
 // B = 2 x (rows x 32) fp16; fp16 storage: one part each.  One CTA stages up
 // to 256 candidate rows, a CTA pair half of the chunk (<= 128 rows) per SM.
-// Stage counts fill about 200-225 KB of shared memory.
+// Stage counts fill 194-231 KB of shared memory.
+// The stages start at the dynamic shared memory base, which the kernel
+// requires (and checks) to be 1024-byte aligned: there is no room for slack.
 template <bool kPair, bool kF16>
 struct DseqCfg {
     static constexpr int kPartsA = kF16 ? 1 : 3;
     static constexpr int kPartsB = kF16 ? 1 : 2;
     static constexpr uint32_t kSubB = (kPair ? 128u : 256u) * kKBlock * 2;
-    static constexpr uint32_t kStage = kPartsA * kSubA + kPartsB * kSubB;
-    static constexpr int kStagesT = kF16 ? (kPair ? 12 : 9) : (kPair ? 5 : kStages);
-    // + alignment slack, barriers and flags, per-warp column norms (fp16 storage)
+    // one K block's operands; an fp16-storage stage holds two K blocks, so
+    // that its single issuing thread waits and commits once per four MMAs
+    static constexpr uint32_t kKbBytes = kPartsA * kSubA + kPartsB * kSubB;
+    static constexpr int kKbPerStage = kF16 ? 2 : 1;
+    static constexpr uint32_t kStage = kKbPerStage * kKbBytes;
+    static constexpr int kStagesT = kF16 ? (kPair ? 7 : 4) : (kPair ? 5 : kStages);
+    static constexpr uint32_t kBarrierBytes = 512;  // barriers, TMEM slot, flags
+    // + per-warp column norms of one 32-column group (fp16 storage)
     static constexpr size_t kSmemBytes =
-        (size_t)kStagesT * kStage + 1024 + 256 +
-        (kF16 ? kEpiWarps * (kMaxGroups / 2) * 32 * sizeof(float) : 0);
+        (size_t)kStagesT * kStage + kBarrierBytes + (kF16 ? kEpiWarps * 32 * sizeof(float) : 0);
 };
 
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                       ~static_cast<uintptr_t>(1023));
-}
 
 __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__restrict__ starts,
                                     const uint8_t *__restrict__ mask) {
@@ -210,8 +212,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     constexpr int kSt = Cfg::kStagesT;
     constexpr uint32_t kSubB = Cfg::kSubB;
     constexpr uint32_t kStageB = Cfg::kStage;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kSt * kStageB);
     uint64_t *empty = full + kSt;
     uint64_t *acc_full = empty + kSt;
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     // overlapped iterations: epilogue warps that finished each half, counted
     unsigned *epi_arrive = reinterpret_cast<unsigned *>(tmem_slot + 2);
     // fp16 storage: per epilogue warp, the inverse norms of its 32 columns
-    float *col_rn = reinterpret_cast<float *>(smem + kSt * kStageB + 256);
+    float *col_rn = reinterpret_cast<float *>(smem + kSt * kStageB + Cfg::kBarrierBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t tmo = a.timeout_ns;
@@ -233,7 +235,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     // the launch must have the shape the kernel is written for (a pair kernel
     // addresses its peer's shared memory and TMEM): otherwise report and leave,
     // uniformly across the grid, before touching anything
-    if (blockDim.x != kThreads || (kPair && (cluster_nctarank() != 2u || (gridDim.x & 1u)))) {
+    if (blockDim.x != kThreads || (kPair && (cluster_nctarank() != 2u || (gridDim.x & 1u))) ||
+        (smem_u32(smem) & 1023u)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusInternal);
         return;
     }
@@ -325,37 +328,42 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         const int yq = beta * kUnitRows;
         // a narrow chunk still loads a full box (its tail rows unused)
         const int ye = (int)p.col0(j) + (int)rank * (p.width(j) / (kPair ? 2 : 1));
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb0 = 0; kb0 < kblocks; kb0 += Cfg::kKbPerStage) {
+            const int nkb = min(Cfg::kKbPerStage, kblocks - kb0);
             const uint32_t s = fills % kSt, par = (fills / kSt) & 1u;
             if (!timed_wait(a, &empty[s], par ^ 1u, abort_flag, tmo, waited))
                 break;
-            uint8_t *sa = smem + s * kStageB;
-            uint8_t *sb = sa + kPartsA * kSubA;
-            if (leader) mbar_arrive_expect_tx(&full[s], tx_bytes);
+            if (leader) mbar_arrive_expect_tx(&full[s], tx_bytes * (uint32_t)nkb);
             if (first) {
                 stamp(a, t, 1);
                 first = false;
             }
-            const int x = kb * kKBlock;
             // completion goes to the pair leader's barrier for this stage
             const uint32_t fb = kPair ? mapa_shared(smem_u32(&full[s]), 0) : 0u;
 #pragma unroll
-            for (int part = 0; part < kPartsA; ++part) {  // (hi*2^12, hi, lo) or fp16
-                if (kPair)
-                    tma_load_2d_pair(sa + part * kSubA, &tmap_q, fb,
-                                     part * a.Dp + x, yq, keep);
-                else
-                    tma_load_2d_hint(sa + part * kSubA, &tmap_q, &full[s],
-                                     part * a.Dp + x, yq, keep);
-            }
+            for (int i = 0; i < Cfg::kKbPerStage; ++i) {
+                if (i >= nkb) break;
+                uint8_t *sa = smem + s * kStageB + i * Cfg::kKbBytes;
+                uint8_t *sb = sa + kPartsA * kSubA;
+                const int x = (kb0 + i) * kKBlock;
 #pragma unroll
-            for (int part = 0; part < kPartsB; ++part) {  // (hi, lo) or fp16
-                if (kPair)
-                    tma_load_2d_pair(sb + part * kSubB, &tmap_e, fb,
-                                     part * a.Dp + x, ye, table_pol);
-                else
-                    tma_load_2d_hint(sb + part * kSubB, &tmap_e, &full[s],
-                                     part * a.Dp + x, ye, table_pol);
+                for (int part = 0; part < kPartsA; ++part) {  // (hi*2^12, hi, lo) or fp16
+                    if (kPair)
+                        tma_load_2d_pair(sa + part * kSubA, &tmap_q, fb,
+                                         part * a.Dp + x, yq, keep);
+                    else
+                        tma_load_2d_hint(sa + part * kSubA, &tmap_q, &full[s],
+                                         part * a.Dp + x, yq, keep);
+                }
+#pragma unroll
+                for (int part = 0; part < kPartsB; ++part) {  // (hi, lo) or fp16
+                    if (kPair)
+                        tma_load_2d_pair(sb + part * kSubB, &tmap_e, fb,
+                                         part * a.Dp + x, ye, table_pol);
+                    else
+                        tma_load_2d_hint(sb + part * kSubB, &tmap_e, &full[s],
+                                         part * a.Dp + x, ye, table_pol);
+                }
             }
             ++fills;
         }
@@ -373,7 +381,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kAccCols;
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb0 = 0; kb0 < kblocks; kb0 += Cfg::kKbPerStage) {
+            const int nkb = min(Cfg::kKbPerStage, kblocks - kb0);
             const uint32_t s = consumed % kSt, par = (consumed / kSt) & 1u;
             if (!timed_wait(a, &full[s], par, abort_flag, tmo, wait_full)) {
                 ok = false;
@@ -384,31 +393,36 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                 stamp(a, t, 2);
                 first = false;
             }
-            const uint32_t sa = smem_u32(smem + s * kStageB);
-            const uint32_t sb = sa + kPartsA * kSubA;
 #pragma unroll
-            for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
-                const uint32_t off = k16 * 32;  // 16 fp16 = 32 bytes along K
-                const uint64_t a0 = smem_desc_sw64(sa + off);
-                const uint64_t b0 = smem_desc_sw64(sb + off);
-                if (kF16) {  // one product: the stored fp16 rows
-                    if (kPair)
+            for (int i = 0; i < Cfg::kKbPerStage; ++i) {
+                if (i >= nkb) break;
+                const int kb = kb0 + i;
+                const uint32_t sa = smem_u32(smem + s * kStageB + i * Cfg::kKbBytes);
+                const uint32_t sb = sa + kPartsA * kSubA;
+#pragma unroll
+                for (int k16 = 0; k16 < kKBlock / 16; ++k16) {
+                    const uint32_t off = k16 * 32;  // 16 fp16 = 32 bytes along K
+                    const uint64_t a0 = smem_desc_sw64(sa + off);
+                    const uint64_t b0 = smem_desc_sw64(sb + off);
+                    if (kF16) {  // one product: the stored fp16 rows
+                        if (kPair)
+                            umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                        else
+                            umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                        continue;
+                    }
+                    const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
+                    const uint64_t a2 = smem_desc_sw64(sa + 2 * kSubA + off);
+                    const uint64_t b1 = smem_desc_sw64(sb + kSubB + off);
+                    if (kPair) {
                         umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                    else
+                        umma_f16_pair(d_tmem, a1, b1, idesc, 1u);
+                        umma_f16_pair(d_tmem, a2, b0, idesc, 1u);
+                    } else {
                         umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                    continue;
-                }
-                const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
-                const uint64_t a2 = smem_desc_sw64(sa + 2 * kSubA + off);
-                const uint64_t b1 = smem_desc_sw64(sb + kSubB + off);
-                if (kPair) {
-                    umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                    umma_f16_pair(d_tmem, a1, b1, idesc, 1u);
-                    umma_f16_pair(d_tmem, a2, b0, idesc, 1u);
-                } else {
-                    umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
-                    umma_f16(d_tmem, a1, b1, idesc, 1u);
-                    umma_f16(d_tmem, a2, b0, idesc, 1u);
+                        umma_f16(d_tmem, a1, b1, idesc, 1u);
+                        umma_f16(d_tmem, a2, b0, idesc, 1u);
+                    }
                 }
             }
             if (kPair)
@@ -464,15 +478,20 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         float best = -INFINITY;
         uint32_t best_c = 0;
         const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
-        float *my_rn = col_rn + e * (kMaxGroups / 2) * 32;
-        if (kF16) {
-            __syncwarp();
-#pragma unroll
-            for (int k = 0; k < kMaxGroups / 2; ++k) my_rn[k * 32 + lane] = rnv[k];
-            __syncwarp();
-        }
+        float *my_rn = col_rn + e * 32;
         for (int g = h; g < groups; g += 2) {
-            const float *rn_g = my_rn + ((g - h) >> 1) * 32;
+            if (kF16) {
+                // this group's column norms, from the registers they were
+                // fetched into before the wait
+                float rv = rnv[0];
+#pragma unroll
+                for (int k = 1; k < kMaxGroups / 2; ++k)
+                    if (((g - h) >> 1) == k) rv = rnv[k];
+                __syncwarp();
+                my_rn[lane] = rv;
+                __syncwarp();
+            }
+            const float *rn_g = my_rn;
             const int gn = g + 2;
             if (gn < groups) {
 #pragma unroll
