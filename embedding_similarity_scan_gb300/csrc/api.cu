@@ -77,6 +77,7 @@ struct Options {
     int64_t criterion = 0;
     int64_t resume = 0;
     int64_t slice = 0;
+    int64_t compact = 1;
 };
 std::mutex g_opt_mu;
 Options g_defaults;
@@ -120,6 +121,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "fault_skip_copy") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "fault_skip_copy must be 0 or 1");
         o.fault_skip_copy = v;
+    } else if (n == "compact") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "compact must be 0 or 1");
+        o.compact = v;
     } else if (n == "slice") {
         if (v < 0 || v > (int64_t(1) << 24)) return fail(DSEQ_EINVAL, "slice out of range");
         o.slice = v;
@@ -139,6 +143,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "timeout_ms") return o.timeout_ms;
     if (n == "fault_skip_arrive") return o.fault_skip_arrive;
     if (n == "slice") return o.slice;
+    if (n == "compact") return o.compact;
     if (n == "fault_skip_copy") return o.fault_skip_copy;
     if (n == "timeline") return o.timeline;
     if (n == "pair") return o.pair;
@@ -407,6 +412,8 @@ struct dseq_ctx {
     DevBuf e_unit, e_split, e_f16, rn, nrm;
     // run workspace
     DevBuf m, keys, q, q_rn, csum, c_exp, status, barrier, starts, mask, picks, trace_slot, timeline;
+    // global-mask compaction: the unmasked rows' tables and the index maps
+    DevBuf col_map, comp_of, e_split_c, e_f16_c, rn_c;
     int64_t timeline_iters = 0, timeline_grid = 0;
     int csum_shift = kNoShift;  // fixed-point scale of the centroid sums, set on first use
     // state left on the device by the last successful run, for "resume"
@@ -419,7 +426,8 @@ struct dseq_ctx {
     ~dseq_ctx() {
         DevBuf *all[] = {&e_unit, &e_split, &e_f16,  &rn,      &nrm,    &m,
                          &keys,   &q,       &q_rn,   &csum,    &c_exp,  &status, &barrier,
-                         &starts, &mask,    &picks,  &trace_slot, &timeline};
+                         &starts, &mask,    &picks,  &trace_slot, &timeline,
+                         &col_map, &comp_of, &e_split_c, &e_f16_c, &rn_c};
         for (DevBuf *b : all) b->release();
     }
 };
@@ -551,20 +559,20 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     // resume: continue the last run on this context from the state it left
     // on the device (same sequences, mask and mode; picks continue)
     const bool resume = ctx->opt.resume != 0;
-    const int64_t sig = ctx->opt.engine * 1000 + ctx->opt.pair * 100 + ctx->opt.storage * 10 +
-                        ctx->opt.criterion;
+    const int64_t sig = ctx->opt.compact * 10000 + ctx->opt.engine * 1000 + ctx->opt.pair * 100 +
+                        ctx->opt.storage * 10 + ctx->opt.criterion;
     if (resume) {
         if (!ctx->has_state) return fail(DSEQ_EINVAL, "resume: no earlier run state on this context");
-        if (sig != ctx->state_sig) return fail(DSEQ_EINVAL, "resume: engine, pair, storage or criterion differ from the earlier run");
+        if (sig != ctx->state_sig) return fail(DSEQ_EINVAL, "resume: engine, pair, storage, criterion or compact differ from the earlier run");
         if (h_starts != ctx->state_starts) return fail(DSEQ_EINVAL, "resume: starts differ from the earlier run");
         if (h_mask != ctx->state_mask) return fail(DSEQ_EINVAL, "resume: mask differs from the earlier run");
     }
     const int64_t done_before = resume ? ctx->state_picks : 0;
+    int64_t n_masked = 0;
+    if (mask)
+        for (int64_t c = 0; c < N; ++c) n_masked += h_mask[c] != 0;
     {
         std::vector<uint8_t> seen((size_t)N, 0);
-        int64_t n_masked = 0;
-        if (mask)
-            for (int64_t c = 0; c < N; ++c) n_masked += h_mask[c] != 0;
         for (int32_t b = 0; b < B; ++b) {
             const int32_t s = h_starts[b];
             if (s < 0 || s >= N) return fail(DSEQ_EINVAL, "starts[%d]=%d out of range [0, %lld)", b, s, (long long)N);
@@ -627,6 +635,39 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
 
     if (ctx->opt.engine == 0) {
         // ---- tensor-core persistent kernel ----
+        const bool f16 = ctx->opt.storage == 1;
+        // a global mask that removes at least 1/16 of the table: scan only
+        // the unmasked rows (option "compact"); picks are mapped back to
+        // table rows, ties still go to the lowest table row (the map is
+        // increasing), and results are identical to the full scan
+        const bool compact = mask && ctx->opt.compact != 0 && n_masked * 16 >= N;
+        int64_t Nk = N;
+        if (compact) {
+            std::vector<int32_t> h_map, h_comp((size_t)N, -1);
+            h_map.reserve((size_t)(N - n_masked));
+            for (int64_t c = 0; c < N; ++c)
+                if (!h_mask[c]) {
+                    h_comp[c] = (int32_t)h_map.size();
+                    h_map.push_back((int32_t)c);
+                }
+            Nk = (int64_t)h_map.size();
+            TRY(ctx->col_map.ensure((size_t)Nk * sizeof(int32_t)));
+            TRY(ctx->comp_of.ensure((size_t)N * sizeof(int32_t)));
+            CUDA_TRY(cudaMemcpyAsync(ctx->col_map.p, h_map.data(), (size_t)Nk * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+            CUDA_TRY(cudaMemcpyAsync(ctx->comp_of.p, h_comp.data(), (size_t)N * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+            const int32_t *d_map = ctx->col_map.as<int32_t>();
+            if (f16) {
+                TRY(ctx->e_f16_c.ensure((size_t)Nk * ctx->Dp * sizeof(__half)));
+                TRY(ctx->rn_c.ensure((size_t)Nk * sizeof(float)));
+                launch_gather_rows(ctx->e_f16.p, ctx->e_f16_c.p, d_map, Nk, (int64_t)ctx->Dp * sizeof(__half), st);
+                launch_gather_rows(ctx->rn.p, ctx->rn_c.p, d_map, Nk, sizeof(float), st);
+            } else {
+                TRY(ctx->e_split_c.ensure((size_t)Nk * 2 * ctx->Dp * sizeof(__half)));
+                launch_gather_rows(ctx->e_split.p, ctx->e_split_c.p, d_map, Nk,
+                                   (int64_t)2 * ctx->Dp * sizeof(__half), st);
+            }
+            CUDA_TRY(cudaGetLastError());
+        }
         TcPlan plan{};
         plan.n_beta = (int)(Bp / kUnitRows);
         plan.pair = pair ? 1 : 0;
@@ -638,30 +679,38 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             const int max_clusters = tc_dseq_pair_max_clusters(256);
             if (max_clusters < 1) return fail(DSEQ_ELAUNCH, "no CTA pair of the pair kernel fits on this device");
             grid_cap = std::max(2, std::min(grid_cap / 2, max_clusters) * 2);
-            choose_widths(plan, plan.n_beta / 2, N, grid_cap / 2, ctx->opt.storage == 1,
+            choose_widths(plan, plan.n_beta / 2, Nk, grid_cap / 2, ctx->opt.storage == 1,
                           (int)ctx->opt.tile_n, (int)ctx->opt.tile_n2);
             plan.grid = 2 * (int)std::min<int64_t>(grid_cap / 2, (int64_t)(plan.n_beta / 2) * plan.n_chunk);
         } else {
-            choose_widths(plan, plan.n_beta, N, grid_cap, ctx->opt.storage == 1,
+            choose_widths(plan, plan.n_beta, Nk, grid_cap, ctx->opt.storage == 1,
                           (int)ctx->opt.tile_n, (int)ctx->opt.tile_n2);
             plan.grid = (int)std::min<int64_t>(grid_cap, plan.units());
         }
         TRY(ctx->m.ensure((size_t)plan.n_beta * kUnitRows * plan.columns() * sizeof(float)));
         // split storage: queries [hi*2^12 | hi | lo], table [hi | lo];
         // fp16 storage: one fp16 part each, plus inverse norms
-        const bool f16 = ctx->opt.storage == 1;
         const int qparts = f16 ? 1 : 3, eparts = f16 ? 1 : 2;
+        const __half *t_split = compact ? ctx->e_split_c.as<__half>() : ctx->e_split.as<__half>();
+        const __half *t_f16 = compact ? ctx->e_f16_c.as<__half>() : ctx->e_f16.as<__half>();
+        const float *t_rn = compact ? ctx->rn_c.as<float>() : ctx->rn.as<float>();
         TRY(ctx->q.ensure((size_t)Bp * qparts * ctx->Dp * sizeof(__half)));
         TRY(ctx->q_rn.ensure((size_t)Bp * sizeof(float)));
         CUtensorMap tq, te;
         TRY(encode_f16_map(tq, ctx->q.p, qparts * ctx->Dp, Bp, kUnitRows));
-        TRY(encode_f16_map(te, f16 ? ctx->e_f16.p : ctx->e_split.p, eparts * ctx->Dp, N,
+        TRY(encode_f16_map(te, f16 ? (const void *)t_f16 : (const void *)t_split, eparts * ctx->Dp, Nk,
                            pair ? plan.tile_n / 2 : plan.tile_n));
         TcDseqArgs a{};
-        a.e_split = ctx->e_split.as<__half>();
+        a.e_split = t_split;
         a.q_split = ctx->q.as<__half>();
-        a.e_f16 = f16 ? ctx->e_f16.as<__half>() : nullptr;
-        a.rn = ctx->rn.as<float>();
+        a.e_f16 = f16 ? t_f16 : nullptr;
+        a.rn = t_rn;
+        a.e_split_full = ctx->e_split.as<__half>();
+        a.e_f16_full = ctx->e_f16.as<__half>();
+        a.rn_full = ctx->rn.as<float>();
+        a.col_map = compact ? ctx->col_map.as<int32_t>() : nullptr;
+        a.comp_of = compact ? ctx->comp_of.as<int32_t>() : nullptr;
+        a.n_table = N;
         a.q_rn = ctx->q_rn.as<float>();
         a.centroid = (int)ctx->opt.criterion;
         if (a.centroid) {
@@ -694,7 +743,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.trace = trace_mindist;
         a.status = ctx->status.as<int>();
         a.barrier = ctx->barrier.as<unsigned>();
-        a.N = N;
+        a.N = Nk;
         a.B = B;
         a.L = L;
         a.Dp = ctx->Dp;
@@ -702,7 +751,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.fault_skip_arrive = (int)ctx->opt.fault_skip_arrive;
         // the split table stays L2-resident across iterations only if it is a
         // small part of L2; larger tables stream through once per iteration
-        a.keep_table = (double)N * eparts * ctx->Dp * sizeof(__half) <= info.l2 / 3.0 ? 1 : 0;
+        a.keep_table = (double)Nk * eparts * ctx->Dp * sizeof(__half) <= info.l2 / 3.0 ? 1 : 0;
         a.timeline = nullptr;
         ctx->timeline_iters = ctx->timeline_grid = 0;
         if (ctx->opt.timeline) {
@@ -713,7 +762,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             ctx->timeline_grid = plan.grid;
         }
         CUDA_TRY(cudaMemsetAsync(ctx->barrier.p, 0, 8 * sizeof(unsigned), st));
-        if (!resume) launch_tc_dseq_init(a, plan, ctx->starts.as<int32_t>(), d_mask, st);
+        if (!resume) launch_tc_dseq_init(a, plan, ctx->starts.as<int32_t>(), compact ? nullptr : d_mask, st);
         CUDA_TRY(cudaGetLastError());
         ctx->state_plan = plan;
         TRY(timer.start(st));

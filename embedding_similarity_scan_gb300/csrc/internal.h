@@ -100,6 +100,11 @@ struct TcPlan {
 void launch_table_prepare(const float *E, int64_t N, int D, int Dp, float *e_unit,
                           __half *e_split, float *nrm, int *status, cudaStream_t st);
 
+// dst row i = src row map[i] for i < rows; rows of row_bytes bytes (a
+// multiple of 4; of 16 for 16-byte copies, with both arrays 16-byte aligned).
+void launch_gather_rows(const void *src, void *dst, const int32_t *map, int64_t rows,
+                        int64_t row_bytes, cudaStream_t st);
+
 // fp16 storage of the candidate table: row * 2^-e (max |.| in [0.5, 1)) rounded
 // to fp16, zero-padded to Dp; rn[r] = 1 / |stored row| (compensated fp32 sum).
 void launch_table_prepare_f16(const float *E, int64_t N, int D, int Dp, __half *e_f16,
@@ -140,10 +145,23 @@ struct TcDseqArgs {
     float *trace;            // n_trace x L x N
     int *status;
     unsigned *barrier;
-    int64_t N;
+    int64_t N;               // candidate columns the kernel scans
     int B, L, Dp;
     uint64_t timeout_ns;
     int fault_skip_arrive;
+    // global-mask compaction (col_map == nullptr: none).  The kernel then
+    // scans only the unmasked rows: e_split / e_f16 / rn hold them in table
+    // order, col_map[c] (N) is the table row of column c and comp_of[r]
+    // (n_table) the column of table row r, or -1 for a masked row.  The
+    // *_full pointers always address the whole table (the first queries are
+    // the start rows, which may be masked); n_table is its row count, the
+    // width of a trace row.
+    const int32_t *col_map;
+    const int32_t *comp_of;
+    const __half *e_split_full;
+    const __half *e_f16_full;
+    const float *rn_full;
+    int64_t n_table;
     int keep_table;  // 1: load table tiles with the evict-last L2 policy (table fits L2)
     // optional [L][grid][kTimelineSlots] globaltimer stamps (nullptr = off)
     unsigned long long *timeline;

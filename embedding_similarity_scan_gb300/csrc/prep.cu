@@ -141,6 +141,17 @@ __global__ void bmu_prepare_kernel(const float *__restrict__ A, int64_t rows, in
     }
 }
 
+template <typename T>
+__global__ void gather_rows_kernel(const T *__restrict__ src, T *__restrict__ dst,
+                                   const int32_t *__restrict__ map, int64_t rows, int64_t vecs) {
+    const int64_t total = rows * vecs;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / vecs, k = i - r * vecs;
+        dst[i] = src[(int64_t)map[r] * vecs + k];
+    }
+}
+
 __global__ void row_sqnorm_kernel(const float *__restrict__ A, int64_t rows, int D,
                                   float *__restrict__ out, int *status) {
     const int lane = threadIdx.x & 31;
@@ -204,6 +215,21 @@ void launch_table_prepare_f16(const float *E, int64_t N, int D, int Dp, __half *
                               float *rn, int *status, cudaStream_t st) {
     table_prepare_f16_kernel<<<blocks_for_rows(N, 8), 256, 0, st>>>(E, N, D, Dp, e_f16, rn,
                                                                        status);
+}
+
+void launch_gather_rows(const void *src, void *dst, const int32_t *map, int64_t rows,
+                        int64_t row_bytes, cudaStream_t st) {
+    const bool wide = row_bytes % 16 == 0;
+    const int64_t vecs = wide ? row_bytes / 16 : row_bytes / 4;
+    const int64_t total = rows * vecs;
+    if (total <= 0) return;
+    const unsigned blocks = (unsigned)((total + 255) / 256 < 8192 ? (total + 255) / 256 : 8192);
+    if (wide)
+        gather_rows_kernel<uint4><<<blocks, 256, 0, st>>>(static_cast<const uint4 *>(src),
+                                                          static_cast<uint4 *>(dst), map, rows, vecs);
+    else
+        gather_rows_kernel<uint32_t><<<blocks, 256, 0, st>>>(static_cast<const uint32_t *>(src),
+                                                             static_cast<uint32_t *>(dst), map, rows, vecs);
 }
 
 void launch_bmu_prepare(const float *A, int64_t rows, int D, int Dp, int triple, __half *split,

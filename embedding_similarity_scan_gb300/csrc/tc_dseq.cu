@@ -98,7 +98,9 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
         const int r = 32 * q + t;
         const int b = beta * kUnitRows + r;
         const int64_t cand0 = p.col0(j) + 32 * g + 4 * v;
-        const int st = b < a.B ? starts[b] : -1;
+        // the start's column (-1 when compaction dropped it: a masked start)
+        const int st0 = b < a.B ? starts[b] : -1;
+        const int st = (a.comp_of && st0 >= 0) ? a.comp_of[st0] : st0;
         float out[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -118,10 +120,10 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
              i += stride) {
             const int b = (int)(i / vec), k = (int)(i - (int64_t)b * vec);
             uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * a.Dp);
-            dst[k] = b < a.B ? reinterpret_cast<const uint4 *>(a.e_f16 +
+            dst[k] = b < a.B ? reinterpret_cast<const uint4 *>(a.e_f16_full +
                                                                (int64_t)starts[b] * a.Dp)[k]
                              : make_uint4(0, 0, 0, 0);
-            if (k == 0) a.q_rn[b] = b < a.B ? a.rn[starts[b]] : 0.0f;
+            if (k == 0) a.q_rn[b] = b < a.B ? a.rn_full[starts[b]] : 0.0f;
         }
     }
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < qtotal && !a.e_f16;
@@ -129,7 +131,7 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
         const int b = (int)(i / vec), k = (int)(i - (int64_t)b * vec);
         uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * 3 * a.Dp);
         if (b < a.B) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.e_split +
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.e_split_full +
                                                                (int64_t)starts[b] * 2 * a.Dp);
             const uint4 hi = src[k], lo = src[vec + k];
             uint4 hi12 = hi;
@@ -568,7 +570,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     a.picks[(int64_t)b * a.L + t] = -1;
                 } else {
                     a.keys[b] = 0ull;
-                    a.picks[(int64_t)b * a.L + t] = (int32_t)w;
+                    a.picks[(int64_t)b * a.L + t] = a.col_map ? a.col_map[w] : (int32_t)w;
                 }
             }
             if (a.trace_slot) {
@@ -578,11 +580,17 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     const int slot = a.trace_slot[bi];
                     if (slot < 0) continue;
                     const int beta = bi / kUnitRows, r = bi % kUnitRows;
-                    float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
-                    for (int64_t c = lane; c < a.N; c += 32) {
+                    float *dst = a.trace + ((int64_t)slot * a.L + t) * a.n_table;
+                    for (int64_t row = lane; row < a.n_table; row += 32) {
+                        // a row dropped by compaction is masked: -inf, as in m
+                        const int64_t c = a.comp_of ? a.comp_of[row] : row;
+                        if (c < 0) {
+                            dst[row] = -INFINITY;
+                            continue;
+                        }
                         const int jj = p.chunk_of(c);
                         const int cc = (int)(c - p.col0(jj));
-                        dst[c] = __ldcg(a.m + p.tile_base(jj, beta) + tc_m_inner(r, cc));
+                        dst[row] = __ldcg(a.m + p.tile_base(jj, beta) + tc_m_inner(r, cc));
                     }
                 }
                 __syncwarp();
@@ -609,9 +617,10 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     // the split is redone with sb corrected (max in [0.5, 1)).
                     const int bq = base + i;
                     long long *cs = a.csum + (int64_t)bq * a.Dp;
-                    const float *eu = a.e_unit + (int64_t)wi * a.Dp;
+                    const int64_t wr = a.col_map ? a.col_map[wi] : wi;  // table row
+                    const float *eu = a.e_unit + wr * a.Dp;
                     __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
-                    const float nw = a.nrm[wi];
+                    const float nw = a.nrm[wr];
                     const int F = a.csum_shift;
                     int sb = a.c_exp[bq];
                     float s1, s2;

@@ -243,6 +243,11 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *   "pair"        1 = the tensor-core kernels run on CTA pairs (clusters of
  *                 two SMs) that share each MMA (each SM stages half of the
  *                 candidate or neuron tile; default); 0 = one CTA per MMA.
+ *   "compact"     1 = when dseq_run's mask removes at least 1/16 of the
+ *                 table, the tensor-core kernel scans only the unmasked rows
+ *                 (gathered once per call; picks are mapped back to table
+ *                 rows, ties still go to the lowest row; results identical to
+ *                 the full scan); default.  0 = always scan the whole table.
  *   "slice"       bmu_search: neuron chunks per codebook slice, the part of
  *                 the codebook every CTA sweeps against all samples before
  *                 moving on; 0 = as many as fill about half of L2 (default).

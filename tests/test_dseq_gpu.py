@@ -33,7 +33,7 @@ def _reset_options(es):
     yield
     for name, v in (("engine", 0), ("tile_n", 0), ("tile_n2", 0), ("grid", 0), ("timeout_ms", 10000),
                     ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR), ("storage", 0),
-                    ("criterion", 0), ("resume", 0)):
+                    ("criterion", 0), ("resume", 0), ("compact", 1)):
         es.dseq_set_option(name, v)
 
 
@@ -435,6 +435,53 @@ def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion, storage):
     trace = np.concatenate(traces, axis=1)
     check = check_centroid_teacher_forced if criterion else check_dseq_teacher_forced
     check(E, starts, mask, chunked, trace, traced)
+
+
+@pytest.mark.parametrize("pair,storage,criterion", [(1, 0, 0), (0, 0, 0), (1, 1, 0), (1, 0, 1)],
+                         ids=["pair", "single", "fp16", "centroid"])
+def test_global_mask_compaction_identical(es, pair, storage, criterion):
+    """A global mask that removes about a third of the table: the kernel
+    scans only the unmasked rows, with the same picks and the same running
+    minima (masked rows -inf in the trace) as the full scan, in one call or
+    resumed in chunks; and it follows the oracle."""
+    N, D, B, L = 1500, 64, 150, 24
+    E = workloads.clustered_table(N, D, n_centres=12, seed=21)
+    if storage:
+        E = _fp16_table(E)
+    starts = workloads.starts(N, B, seed=21)
+    rng = np.random.default_rng(21)
+    mask = (rng.random(N) < 0.33).astype(np.uint8)
+    mask[starts[: B // 4]] = 1  # some starts are masked themselves
+    tr = np.array([0, 7, B // 4, B - 1], np.int32)
+    got = {}
+    for compact in (0, 1):
+        es.dseq_set_option("compact", compact)
+        got[compact] = _run(es, E, starts, L, mask, tr, pair=pair, storage=storage,
+                            criterion=criterion)
+    assert np.array_equal(got[0][0], got[1][0])
+    assert np.array_equal(got[0][1], got[1][1])
+    picks, trace = got[1]
+    check_picks_valid(starts, mask, picks, N)
+    check = check_centroid_teacher_forced if criterion else check_dseq_teacher_forced
+    check(E, starts, mask, picks, trace, tr)
+    # the compacted run resumed in two chunks gives the same picks
+    es.dseq_set_option("compact", 1)
+    es.dseq_set_option("pair", pair)
+    es.dseq_set_option("storage", storage)
+    es.dseq_set_option("criterion", criterion)
+    ctx = es.dseq_create(torch.from_numpy(E).cuda())
+    try:
+        st = torch.from_numpy(starts).cuda()
+        mk = torch.from_numpy(mask).cuda()
+        first = es.dseq_run(ctx, st, 10, mask=mk).cpu().numpy()
+        es.dseq_set_option("resume", 1, ctx)
+        rest = es.dseq_run(ctx, st, L - 10, mask=mk).cpu().numpy()
+        es.dseq_set_option("compact", 0, ctx)
+        with pytest.raises(es.DseqError):  # a different scan layout cannot resume
+            es.dseq_run(ctx, st, 1, mask=mk)
+    finally:
+        ctx.close()
+    assert np.array_equal(np.concatenate([first, rest], axis=1), picks)
 
 
 def test_resume_without_state_rejected(es):
