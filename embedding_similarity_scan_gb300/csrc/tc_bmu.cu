@@ -47,8 +47,8 @@ constexpr uint32_t kAccCols = 256;
 // column groups of 32 in the widest unit (256 neurons)
 constexpr int kMaxGroups = 8;
 
-// Stage geometry.  One CTA: B sub-tiles of up to 256 neuron rows, 3 stages
-// (the epilogue also needs 8 KB of column constants).  CTA pair: each CTA
+// Stage geometry.  One CTA: B sub-tiles of up to 256 neuron rows, 3 stages.
+// CTA pair: each CTA
 // stages half of the neuron chunk (<= 128 rows), 5 stages.
 template <bool kPair>
 struct BmuCfg {
@@ -56,7 +56,7 @@ struct BmuCfg {
     static constexpr uint32_t kSubB = (kPair ? 128u : 256u) * kKBlock * 2;
     static constexpr uint32_t kStage = kBmuPartsX * kSubA + kBmuPartsW * kSubB;
     static constexpr size_t kSmemBytes =
-        (size_t)kStagesT * kStage + 1024 + 256 + kEpiWarps * (kMaxGroups / 2) * 32 * sizeof(float2);
+        (size_t)kStagesT * kStage + 1024 + 256 + kEpiWarps * 32 * sizeof(float2);
 };
 
 // Resident-sample kernel (CTA pairs): the sample rows of up to kResKBlocks
@@ -98,6 +98,73 @@ __device__ __forceinline__ void bmu_mma_k16(uint32_t d_tmem, uint32_t a, uint32_
         umma_f16(d_tmem, x_hi, w_lo, idesc, 1u);
         umma_f16(d_tmem, x_lo, w_hi, idesc, 1u);
     }
+}
+
+// Epilogue of one unit (128 samples x tile_n neurons of chunk j) by one
+// epilogue warp: the warp's lane quadrant q of the accumulator, every other
+// 32-neuron group from h; score = |w|^2 + acc / s_w * (-2^-11 / s_x), the
+// running (min score, lowest neuron) folded into the row's key.  The
+// neuron constants are fetched before the accumulator wait and staged one
+// group at a time in the warp's 256 bytes of shared memory (my_colc).
+// Returns false if the wait gave up.
+template <bool kPair>
+__device__ __forceinline__ bool bmu_epilogue_unit(const BmuArgs &a, int beta, int j, uint32_t tile_n,
+                                                  int groups, uint32_t tmem_base, uint32_t &acc_uses,
+                                                  uint64_t *acc_full, uint64_t *acc_empty,
+                                                  uint32_t acc_empty_leader0, float2 *my_colc,
+                                                  volatile int *abort_flag, int warp, int lane) {
+    const int e = warp - 2, q = warp & 3, h = e >> 2;
+    const int64_t row = (int64_t)beta * kUnitRows + 32 * q + lane;
+    const float cx = row < a.n ? -a.x_inv_scale[row] * (1.0f / 2048.0f) : 0.0f;
+    float2 cv[kMaxGroups / 2];
+#pragma unroll
+    for (int k = 0; k < kMaxGroups / 2; ++k) {
+        const int64_t col = (int64_t)j * tile_n + 32 * (h + 2 * k) + lane;
+        cv[k] = (h + 2 * k < groups && col < a.M)
+                    ? make_float2(__ldg(a.wn + col), __ldg(a.w_inv_scale + col))
+                    : make_float2(INFINITY, 0.0f);
+    }
+    const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+    // every lane waits; the warp proceeds only if all of them saw the phase
+    const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status, a.timeout_ns,
+                                         kStatusPipeTimeout);
+    if (!__all_sync(0xffffffffu, ready)) return false;
+    tc_fence_after();
+    float best = INFINITY;
+    uint32_t best_j = 0xffffffffu;
+    const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+#pragma unroll
+    for (int k = 0; k < kMaxGroups / 2; ++k) {
+        const int g = h + 2 * k;
+        if (g >= groups) break;
+        __syncwarp();
+        my_colc[lane] = cv[k];
+        __syncwarp();
+        float acc[32];
+        tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
+        tmem_wait_ld();
+        const uint32_t cbase = (uint32_t)j * tile_n + 32u * (uint32_t)g;
+#pragma unroll
+        for (int z = 0; z < 32; ++z) {
+            const float2 cc = my_colc[z];
+            const float sc = fmaf(acc[z] * cc.y, cx, cc.x);
+            if (sc < best) {
+                best = sc;
+                best_j = cbase + z;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+        if (kPair)
+            mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
+        else
+            mbar_arrive(&acc_empty[buf]);
+    }
+    ++acc_uses;
+    if (row < a.n && best_j != 0xffffffffu) atomicMin(a.keys + row, min_key(best, best_j));
+    return true;
 }
 
 struct BmuSchedule {
@@ -298,65 +365,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        const int e = warp - 2, q = warp & 3, h = e >> 2;
-        const int r = 32 * q + lane;
-        float2 *my_colc = colc + e * (kMaxGroups / 2) * 32;
+        float2 *my_colc = colc + (warp - 2) * 32;
         uint32_t acc_uses = 0;
-        const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+        const uint32_t acc_empty_leader0 = kPair ? mapa_shared(smem_u32(&acc_empty[0]), 0) : 0u;
         for (int64_t u = first_item; u < units; u += item_stride) {
             int blk, j;
             sched.decode(u, blk, j);
             const int beta = kPair ? 2 * blk + (int)rank : blk;
-            const int64_t row = (int64_t)beta * kUnitRows + r;
-            const float cx = row < a.n ? -a.x_inv_scale[row] * (1.0f / 2048.0f) : 0.0f;
-            // this warp's (at most 4) column groups' constants, fetched before the wait
-            float2 cv[kMaxGroups / 2];
-#pragma unroll
-            for (int k = 0; k < kMaxGroups / 2; ++k) {
-                const int64_t col = (int64_t)j * tile_n + 32 * (h + 2 * k) + lane;
-                cv[k] = (h + 2 * k < groups && col < a.M)
-                            ? make_float2(__ldg(a.wn + col), __ldg(a.w_inv_scale + col))
-                            : make_float2(INFINITY, 0.0f);
-            }
-            const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
-            // every lane waits; the warp proceeds only if all of them saw the phase
-            const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status, tmo,
-                                                 kStatusPipeTimeout);
-            if (!__all_sync(0xffffffffu, ready)) break;
-            tc_fence_after();
-            float best = INFINITY;
-            uint32_t best_j = 0xffffffffu;
-            const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
-            __syncwarp();
-#pragma unroll
-            for (int k = 0; k < kMaxGroups / 2; ++k) my_colc[k * 32 + lane] = cv[k];
-            __syncwarp();
-            for (int g = h; g < groups; g += 2) {
-                const float2 *cg = my_colc + ((g - h) >> 1) * 32;
-                float acc[32];
-                tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
-                tmem_wait_ld();
-                const uint32_t cbase = (uint32_t)j * tile_n + 32u * (uint32_t)g;
-#pragma unroll
-                for (int z = 0; z < 32; ++z) {
-                    const float2 cc = cg[z];
-                    const float s = fmaf(acc[z] * cc.y, cx, cc.x);
-                    if (s < best) {
-                        best = s;
-                        best_j = cbase + z;
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (kPair)
-                    mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
-                else
-                    mbar_arrive(&acc_empty[buf]);
-            }
-            ++acc_uses;
-            if (row < a.n && best_j != 0xffffffffu) atomicMin(a.keys + row, min_key(best, best_j));
+            if (!bmu_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses, acc_full,
+                                          acc_empty, acc_empty_leader0, my_colc, abort_flag, warp, lane))
+                break;
         }
     }
 
@@ -602,68 +620,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        const int e = warp - 2, q = warp & 3, h = e >> 2;
-        const int r = 32 * q + lane;
-        float2 *my_colc = colc + e * 32;
+        float2 *my_colc = colc + (warp - 2) * 32;
         uint32_t acc_uses = 0;
         const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
         bool ok = true;
         for (int64_t u = first_item; u < items && ok; u += item_stride) {
             int pb, c0, c1;
             sched.decode(u, pb, c0, c1);
-            const int beta = 2 * pb + (int)rank;
-            const int64_t row = (int64_t)beta * kUnitRows + r;
-            const float cx = row < a.n ? -a.x_inv_scale[row] * (1.0f / 2048.0f) : 0.0f;
-            for (int j = c0; j < c1; ++j) {
-                // this warp's (at most 4) column groups' constants, fetched before the wait
-                float2 cv[kMaxGroups / 2];
-#pragma unroll
-                for (int k = 0; k < kMaxGroups / 2; ++k) {
-                    const int64_t col = (int64_t)j * tile_n + 32 * (h + 2 * k) + lane;
-                    cv[k] = (h + 2 * k < groups && col < a.M)
-                                ? make_float2(__ldg(a.wn + col), __ldg(a.w_inv_scale + col))
-                                : make_float2(INFINITY, 0.0f);
-                }
-                const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
-                // every lane waits; the warp proceeds only if all of them saw the phase
-                const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status, tmo,
-                                                     kStatusPipeTimeout);
-                if (!__all_sync(0xffffffffu, ready)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float best = INFINITY;
-                uint32_t best_j = 0xffffffffu;
-                const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
-#pragma unroll
-                for (int k = 0; k < kMaxGroups / 2; ++k) {
-                    const int g = h + 2 * k;
-                    if (g >= groups) break;
-                    __syncwarp();
-                    my_colc[lane] = cv[k];
-                    __syncwarp();
-                    const float2 *cg = my_colc;
-                    float acc[32];
-                    tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
-                    tmem_wait_ld();
-                    const uint32_t cbase = (uint32_t)j * tile_n + 32u * (uint32_t)g;
-#pragma unroll
-                    for (int z = 0; z < 32; ++z) {
-                        const float2 cc = cg[z];
-                        const float sc = fmaf(acc[z] * cc.y, cx, cc.x);
-                        if (sc < best) {
-                            best = sc;
-                            best_j = cbase + z;
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
-                ++acc_uses;
-                if (row < a.n && best_j != 0xffffffffu) atomicMin(a.keys + row, min_key(best, best_j));
-            }
+            for (int j = c0; j < c1 && ok; ++j)
+                ok = bmu_epilogue_unit<true>(a, 2 * pb + (int)rank, j, tile_n, groups, tmem_base, acc_uses,
+                                             acc_full, acc_empty, acc_empty_leader0, my_colc, abort_flag,
+                                             warp, lane);
         }
     }
 
