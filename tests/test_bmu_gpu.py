@@ -175,6 +175,23 @@ def test_pipeline_timeout_returns_cleanly(es, pair, D):
     assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_random_shapes(es, seed):
+    """Seeded random sample counts, codebook sizes, dimensions (both sides of
+    the resident-sample limit), chunk widths and pair modes, against the
+    oracle."""
+    rng = np.random.default_rng(2000 + seed)
+    n = int(rng.integers(1, 1500))
+    M = int(rng.integers(1, 3000))
+    D = int(rng.choice([1, 5, 32, 100, 256, 300, 513]))
+    tile_n = int(rng.choice([0, 32, 96, 256]))
+    pair = int(rng.integers(0, 2))
+    X = workloads.bmu_samples(n, D, seed=seed)
+    W = workloads.codebook(M, D, seed=seed)
+    idx, dist = _bmu(es, X, W, 0, tile_n=tile_n, pair=pair)
+    check_bmu(X, W, np.arange(n), idx, dist)
+
+
 def test_host_buffers(es):
     X = workloads.bmu_samples(257, 24, seed=6)
     W = workloads.codebook(513, 24, seed=6)

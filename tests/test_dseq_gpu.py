@@ -484,6 +484,41 @@ def test_global_mask_compaction_identical(es, pair, storage, criterion):
     assert np.array_equal(np.concatenate([first, rest], axis=1), picks)
 
 
+def _random_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.integers(2, 3000))
+    D = int(rng.choice([1, 3, 17, 32, 64, 100, 257, 768]))
+    B = int(rng.integers(1, min(N, 300) + 1))
+    frac = float(rng.choice([0.0, 0.02, 0.1, 0.4]))
+    mask = (rng.random(N) < frac).astype(np.uint8) if frac > 0 else None
+    starts = rng.choice(N, B, replace=False).astype(np.int32)
+    n_masked = 0 if mask is None else int(mask.sum())
+    L = int(rng.integers(1, max(2, min(N - n_masked - 1, 40) + 1))) if N - n_masked - 1 >= 1 else 0
+    return N, D, B, L, mask, starts
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("pair", [1, 0])
+def test_random_shapes_teacher_forced(es, seed, pair):
+    """Seeded random shapes, masks (dense enough to be compacted or not),
+    sequence counts and lengths, against the oracle."""
+    N, D, B, L, mask, starts = _random_case(seed)
+    if L == 0:
+        pytest.skip("no candidate left to pick")
+    E = workloads.gaussian_table(N, D, seed=seed) if seed % 2 else \
+        workloads.clustered_table(N, D, n_centres=8, seed=seed)
+    if mask is not None:
+        # every sequence must have L candidates left
+        avail = N - int(mask.sum()) - (mask[starts] == 0).astype(int)
+        L = int(min(L, avail.min()))
+        if L < 1:
+            pytest.skip("no candidate left to pick")
+    tr = np.unique(np.linspace(0, B - 1, num=min(B, 4)).astype(np.int32))
+    picks, trace = _run(es, E, starts, L, mask, tr, pair=pair)
+    check_picks_valid(starts, mask, picks, N)
+    check_dseq_teacher_forced(E, starts, mask, picks, trace, tr)
+
+
 def test_resume_without_state_rejected(es):
     E = workloads.gaussian_table(64, 16, seed=3)
     ctx = es.dseq_create(torch.from_numpy(E).cuda())
