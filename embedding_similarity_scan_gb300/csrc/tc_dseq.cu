@@ -7,7 +7,7 @@
 // takes the unmasked candidate with the largest running minimum (lowest index
 // on ties).  The issue asks for a tiled candidate scan that every workgroup
 // walks together, with a hard grid-wide sync between steps (Intended
-// Behavior, "dispatch per tile"); here the loop over iterations lives on the
+// Behavior, one dispatch per tile); here the loop over iterations lives on the
 // device, and the sync is split per half of the sequences so that it never
 // idles the grid (below).
 //

@@ -9,7 +9,7 @@
  *    computes the cosine distance of that pick to all N candidate rows,
  *    folds it into the sequence's running minimum distance, and picks the
  *    unmasked candidate whose running minimum is largest, lowest index on
- *    ties (the max-min, farthest-first reading of "most different").  The
+ *    ties (the max-min, farthest-first reading of the issue's criterion).  The
  *    candidate scan is tiled and the running (max, index) carried across
  *    tiles, which by associativity of max gives the one-pass winner (same
  *    issue, Intended Behavior).
@@ -239,7 +239,7 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 step, fp32-level distances (default); 1 = fp16 rows (each
  *                 row scaled by a power of two, then rounded once to fp16),
  *                 one product per step, distances exact for the stored rows
- *                 up to fp32 accumulation ("load FP16, compute FP32").
+ *                 up to fp32 accumulation (fp16 in memory, fp32 arithmetic).
  *   "pair"        1 = the tensor-core kernels run on CTA pairs (clusters of
  *                 two SMs) that share each MMA (each SM stages half of the
  *                 candidate or neuron tile; default); 0 = one CTA per MMA.

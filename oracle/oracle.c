@@ -11,21 +11,22 @@
  *  1. Greedy diversity sequences ("Issue 9-014: Tile Diversity Shader Inner
  *     Loop For L2 Cache Locality", sections Current Behavior and Intended
  *     Behavior).  Each sequence repeatedly picks the unmasked candidate that
- *     is most different from what it already holds.  The running criterion
+ *     is farthest from what it already holds.  The running criterion
  *     is the max-min (farthest-first) reading: every candidate keeps the
  *     smallest cosine distance to any row picked so far, and the pick is the
  *     candidate whose kept distance is largest, lowest index on ties.  The
  *     scan may walk the candidates in tiles of T with the running
  *     (best, index) carried from tile to tile; by associativity of max the
  *     result equals one pass (same issue, Intended Behavior; Suggested
- *     Implementation Steps, the tile loop and its "do not reset the running
- *     max between tiles" warning; Risks, the last partial tile).
+ *     Implementation Steps, the tile loop, whose running maximum carries
+ *     over from tile to tile; Risks, the last partial tile).
  *
  *  1b. The centroid criterion named in the same issue (FP16 storage
- *     section: "most different from the centroid"): each sequence picks the
- *     unmasked candidate at the largest cosine distance from the centroid
- *     (plain mean) of the rows it holds, lowest index on ties.  A zero
- *     centroid makes every distance 1 (cosine taken as 0).
+ *     section, where a candidate is judged by its distance from the
+ *     centroid of the held rows): each sequence picks the unmasked
+ *     candidate at the largest cosine distance from the centroid (plain
+ *     mean) of the rows it holds, lowest index on ties.  A zero centroid
+ *     makes every distance 1 (cosine taken as 0).
  *
  *  2. Best-matching-unit search ("From 80x to 385x: A Best-Matching-Unit
  *     Search at the L2 Roof", section 3, Background): for each sample the

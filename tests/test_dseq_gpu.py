@@ -285,7 +285,7 @@ def test_full_size_teacher_forced(es, name, engine):
 
 
 # --------------------------------------------------------------------------
-# fp16 table storage ("load FP16, compute FP32"): on tables whose values are
+# fp16 table storage (fp16 in memory, fp32 arithmetic): on tables whose values are
 # already fp16 numbers the stored rows equal the input up to a power-of-two
 # scale, so the distances match the oracle's exact cosine distances to fp32
 # accumulation error, and the same teacher-forced tolerance applies.
@@ -334,7 +334,7 @@ def test_fp16_storage_full_size_and_agreement(es):
 
 
 # --------------------------------------------------------------------------
-# centroid criterion (the issue's "most different from the centroid")
+# centroid criterion (the issue's distance-from-the-centroid reading)
 
 
 @pytest.mark.parametrize("pair", [1, 0])
