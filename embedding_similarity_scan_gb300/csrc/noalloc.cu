@@ -127,13 +127,18 @@ extern "C" int bmu_search_noalloc(const float *X, int64_t n, const float *W, int
                        const_cast<float *>(a.w_inv_scale), a.status, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return host::fail_msg(DSEQ_ECUDA, cudaGetErrorString(e));
+    // CTA pairs on whole pairs of sample blocks, as bmu_search by default
     TcPlan plan{};
+    plan.pair = 1;
     plan.n_beta = (int)((n + kUnitRows - 1) / kUnitRows);
+    plan.n_beta += plan.n_beta & 1;
     plan.set_uniform(256, M);
-    plan.grid = (int)(plan.units() < sms ? plan.units() : sms);
+    const int64_t pair_units = plan.units() / 2;
+    const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
+    plan.grid = 2 * (int)(pair_units < pairs ? (pair_units > 0 ? pair_units : 1) : pairs);
     CUtensorMap tx, tw;
     if ((r = host::encode_map(tx, a.x_split, kBmuPartsX * Dp, n, kUnitRows)) != DSEQ_OK) return r;
-    if ((r = host::encode_map(tw, a.w_split, kBmuPartsW * Dp, M, plan.tile_n)) != DSEQ_OK) return r;
+    if ((r = host::encode_map(tw, a.w_split, kBmuPartsW * Dp, M, plan.tile_n / 2)) != DSEQ_OK) return r;
     e = launch_tc_bmu(a, plan, tx, tw, 0, st);
     if (e != cudaSuccess) return host::fail_msg(DSEQ_ECUDA, cudaGetErrorString(e));
     launch_bmu_finalize(a, st);

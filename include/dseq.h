@@ -198,8 +198,8 @@ int som_epoch(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_
  *    device, with that device current), so make that first call before any
  *    stream capture;
  *  - the process-wide "engine", "tile_n", "grid" and "timeout_ms" options do
- *    not apply: the tensor-core path always runs, 256 neurons per unit, one
- *    CTA per SM, 10 s wait limit.
+ *    not apply: the tensor-core path always runs on CTA pairs, 256 neurons
+ *    per unit, one CTA per SM, 10 s wait limit.
  * Errors: DSEQ_EINVAL (as bmu_search, host pointers, scratch too small),
  * DSEQ_ENONFINITE, DSEQ_ETIMEOUT, DSEQ_ECUDA. */
 int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int32_t D,

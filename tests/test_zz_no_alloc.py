@@ -85,7 +85,10 @@ def test_noalloc_matches_bmu_search_on_two_calls_in_a_row(lib):
     results = [_call_noalloc(lib, X, W) for X, W in inputs]
     torch.cuda.synchronize()
     for (X, W), got in zip(inputs, results):
-        _agree(X, W, got, _call_reference(lib, X, W))
+        ref = _call_reference(lib, X, W)
+        _agree(X, W, got, ref)
+        # the same kernels on the same split operands: the same bits
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
 
 
 def test_noalloc_rejects_what_it_cannot_serve(lib):
