@@ -26,7 +26,7 @@
 // equals 2^12 <q, e> up to about 2^-22 relative per product.  FP16 storage
 // uses one part on each side and the rows' inverse norms.
 //
-// CTA roles (352 threads; 384 for the centroid criterion):
+// CTA roles (352 threads; 448 for the centroid criterion, four commit warps):
 //   warp 0      TMA producer: Q and E K-blocks into a multi-stage smem ring;
 //   warp 1      TMEM owner and MMA issuer (one thread), double-buffered
 //               128 x 256 fp32 accumulators (512 TMEM columns);
