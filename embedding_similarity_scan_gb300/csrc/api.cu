@@ -1,6 +1,7 @@
 // api.cu — the C ABI of libdseq.so: argument checks, pointer-kind detection
-// and staging, device workspace, tensor-map encoding, work planning, and the
-// launches of the kernels in tc_dseq.cu, tc_bmu.cu, ffma.cu and prep.cu.
+// and staging, device workspace, tensor-map encoding, work planning
+// (chunk widths, global-mask compaction, BMU slices), and the launches of
+// the kernels in tc_dseq.cu, tc_bmu.cu, ffma.cu, prep.cu and som.cu.
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>

@@ -1,15 +1,16 @@
 // prep.cu — one-pass preparation kernels: candidate-table normalisation and
-// fp16 hi/lo split, BMU operand scaling and split, squared norms, and the
-// BMU key initialisation / finalisation.
+// fp16 hi/lo split, BMU operand scaling and split, squared norms, the BMU key
+// initialisation / finalisation, and the row gather of global-mask
+// compaction.
 //
 // The split: a float x with |x| <= 1 becomes hi = fp16(x) and
 // lo = fp16((x - hi) * 2^12).  x - hi is exact in fp32; scaling the residual
 // by 2^12 keeps it in fp16's normal range, so hi + lo * 2^-12 carries about
 // 22 significant bits, and a product of two split values needs three fp16
 // products (hi*hi, hi*lo, lo*hi) for fp32-level accuracy.  The tensor-core
-// kernels fold the 2^-12 into a pre-scaled copy of hi on the query side
-// (hi * 2^12), so all three products land in one fp32 accumulator scaled by
-// 2^12.
+// kernels fold the 2^-12 into a pre-scaled copy of hi on one side (the
+// diversity queries, the BMU codebook: hi * 2^12), so all three products land
+// in one fp32 accumulator scaled by 2^12.
 #include "common.cuh"
 #include "internal.h"
 #include "numeric.cuh"
