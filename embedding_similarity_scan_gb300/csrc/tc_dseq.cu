@@ -26,7 +26,8 @@
 // equals 2^12 <q, e> up to about 2^-22 relative per product.  FP16 storage
 // uses one part on each side and the rows' inverse norms.
 //
-// CTA roles (352 threads; 448 for the centroid criterion, four commit warps):
+// CTA roles (384 threads, two commit warps; 448 for the centroid criterion,
+// four commit warps):
 //   warp 0      TMA producer: Q and E K-blocks into a multi-stage smem ring;
 //   warp 1      TMEM owner and MMA issuer (one thread), double-buffered
 //               128 x 256 fp32 accumulators (512 TMEM columns);
@@ -191,11 +192,13 @@ __device__ __forceinline__ bool timed_wait(const TcDseqArgs &a, uint64_t *bar, u
     return ok;
 }
 
-// Commit warps per CTA: the centroid commit (exact fixed-point centroid
-// update of every sequence) is heavier than copying a winner's stored row.
+// Commit warps per CTA: two share the copying of the winners' stored rows
+// (one left the next iteration's producers waiting on the commit); the
+// centroid commit (exact fixed-point centroid update of every sequence) is
+// heavier and takes four.
 template <bool kCentroid>
 __host__ __device__ constexpr int dseq_commit_warps() {
-    return kCentroid ? 4 : 1;
+    return kCentroid ? 4 : 2;
 }
 template <bool kCentroid>
 __host__ __device__ constexpr int dseq_threads() {
