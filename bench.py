@@ -527,7 +527,7 @@ def run_ours(args):
         mhz = clocks.get("sm_max_mhz") or 2070.0
         alu_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
         roof.update({"bound": "alu", "peak": alu_peak, "frac": (achieved / alu_peak) if achieved else None,
-                     "peak_kind": "fp32 pipe, derived", "frac_of_burst": None,
+                     "peak_kind": "fp32 pipe, derived", "frac_of_burst": None, "traffic": None,
                      "kernel": "ffma_dseq_fold_kernel" if is_div else "ffma_bmu_kernel",
                      "note": (f"achieved = algorithmic FLOP / kernel time ({'fold + commit launches' if is_div else 'one launch'}, CUDA events); peak = {sms} SMs x 128 "
                               f"FP32 lanes x 2 FLOP x {mhz:.0f} MHz (derived, not measured)")})
