@@ -1,8 +1,8 @@
 """GPU parity of the SOM neighbourhood update and of whole epochs against the
 CPU oracle, through the C ABI.
 
-Tolerance: the kernels sum samples per neuron in double, then smooth and
-divide in fp32.  Each smoothing pass is a positive-weighted sum of at most
+Tolerance: the kernels sum samples per neuron exactly (64-bit fixed point),
+then smooth and divide in fp32.  Each smoothing pass is a positive-weighted sum of at most
 2R + 1 terms, so the error of num / den is bounded by about
 (2 (2R + 1) + 3) 2^-24 max_i |x_i|, under 2.5e-6 max|x| for R <= 9; the
 tests allow 1e-5 max|x| absolute.  Epochs are checked under teacher forcing:
@@ -83,6 +83,24 @@ def test_update_parity(es, case, hot):
     n, sx, sy, D, sigma, R = case
     X, W, bmu = _data(n, sx, sy, D, seed=n + sx, hot=hot)
     Wd = torch.from_numpy(W.copy()).cuda()
+    es.som_update(torch.from_numpy(X).cuda(), torch.from_numpy(bmu).cuda(), Wd, sx, sy, sigma, R)
+    torch.cuda.synchronize()
+    _check_update(X, bmu, W, Wd.cpu().numpy(), sx, sy, sigma, R)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes_update(es, seed):
+    """Seeded random map shapes, dimensions, sample counts, neighbourhood
+    widths and radii (up to 40, beyond the usual 3 sigma), against the
+    oracle."""
+    rng = np.random.default_rng(3000 + seed)
+    sx, sy = int(rng.integers(1, 90)), int(rng.integers(1, 90))
+    D = int(rng.choice([1, 7, 32, 100, 256]))
+    n = int(rng.integers(1, 4000))
+    R = int(rng.integers(0, 41))
+    sigma = 0.0 if R == 0 else float(rng.uniform(R / 9.0, R / 2.0 + 0.5))
+    X, W, bmu = _data(n, sx, sy, D, seed=seed, hot=bool(seed % 2))
+    Wd = torch.from_numpy(W).cuda()
     es.som_update(torch.from_numpy(X).cuda(), torch.from_numpy(bmu).cuda(), Wd, sx, sy, sigma, R)
     torch.cuda.synchronize()
     _check_update(X, bmu, W, Wd.cpu().numpy(), sx, sy, sigma, R)
