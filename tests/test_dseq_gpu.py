@@ -519,6 +519,33 @@ def test_random_shapes_teacher_forced(es, seed, pair):
     check_dseq_teacher_forced(E, starts, mask, picks, trace, tr)
 
 
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("variant", ["fp16", "centroid"])
+def test_random_shapes_variants(es, seed, variant):
+    """The random shapes above on fp16 storage (tables of fp16 numbers) and
+    on the centroid criterion, against the oracle."""
+    N, D, B, L, mask, starts = _random_case(seed)
+    if L == 0:
+        pytest.skip("no candidate left to pick")
+    E = workloads.clustered_table(N, D, n_centres=8, seed=seed)
+    if variant == "fp16":
+        E = _fp16_table(E)
+    if mask is not None:
+        avail = N - int(mask.sum()) - (mask[starts] == 0).astype(int)
+        L = int(min(L, avail.min()))
+        if L < 1:
+            pytest.skip("no candidate left to pick")
+    tr = np.unique(np.linspace(0, B - 1, num=min(B, 4)).astype(np.int32))
+    if variant == "fp16":
+        picks, trace = _run(es, E, starts, L, mask, tr, storage=1)
+        check_picks_valid(starts, mask, picks, N)
+        check_dseq_teacher_forced(E, starts, mask, picks, trace, tr)
+    else:
+        picks, trace = _run(es, E, starts, L, mask, tr, criterion=1)
+        check_picks_valid(starts, mask, picks, N)
+        check_centroid_teacher_forced(E, starts, mask, picks, trace, tr)
+
+
 def test_resume_without_state_rejected(es):
     E = workloads.gaussian_table(64, 16, seed=3)
     ctx = es.dseq_create(torch.from_numpy(E).cuda())
