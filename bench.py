@@ -22,6 +22,7 @@ Multi-GPU (torchrun): every rank runs the full workload on its own GPU
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -346,6 +347,8 @@ def run_ours(args):
     epoch_of = None
     if is_div:
         cfg = workloads.DIVERSITY[args.workload]
+        if args.iters > 0:
+            cfg = dataclasses.replace(cfg, L=args.iters)
         E_host = torch.from_numpy(cfg.table(seed=0)).pin_memory()
         # each rank runs its own shard: the same table, its own sequences
         starts_host = torch.from_numpy(cfg.starts(seed=rank)).pin_memory()
@@ -412,6 +415,8 @@ def run_ours(args):
                   "l2": "flushed between steps (512 MB write)"}
     else:
         cfg = workloads.BMU[args.workload]
+        if args.samples > 0:
+            cfg = dataclasses.replace(cfg, n=args.samples)
         # each rank runs its own shard: the same codebook, its own samples
         X_host = torch.from_numpy(cfg.samples(seed=rank)).pin_memory()
         W_host = torch.from_numpy(cfg.codebook(seed=0)).pin_memory()
@@ -439,6 +444,9 @@ def run_ours(args):
 
     if args.opt:
         config["options"] = list(args.opt)
+    shrunk = args.iters > 0 or args.samples > 0
+    if shrunk:
+        config["reduced"] = "smaller than the workload (--iters / --samples): a profiling case"
 
     def barrier():
         torch.cuda.synchronize()
@@ -515,8 +523,8 @@ def run_ours(args):
             "frac": (achieved / tensor_peak) if achieved else None,
             "peak_kind": peak_kind,
             "frac_of_burst": (achieved / burst_peak) if achieved else None,
-            "traffic": _profiled_traffic(kernel_name, epoch_of or args.workload,
-                                         "_pair0" if "pair=0" in args.opt else ""),
+            "traffic": None if shrunk else _profiled_traffic(kernel_name, epoch_of or args.workload,
+                                                             "_pair0" if "pair=0" in args.opt else ""),
             "kernel": kernel_name,
             "note": (f"achieved = algorithmic FLOP (2*{'N*D*B*L' if is_div else 'n*M*D'})"
                      f" / kernel time (CUDA events on the launching stream); {peak_note}")}
@@ -590,6 +598,11 @@ def main():
                     + sorted(workloads.SOM_EPOCH))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--iters", type=int, default=0,
+                    help="diversity workloads: L iterations instead of the workload's (small "
+                         "cases for profiling; the line is then not the workload's)")
+    ap.add_argument("--samples", type=int, default=0,
+                    help="BMU workloads: this many samples instead of the workload's (as --iters)")
     ap.add_argument("--ref-sample", type=int, default=0)
     ap.add_argument("--opt", action="append", default=[],
                     help="library option name=value, e.g. storage=1 (process-wide)")
