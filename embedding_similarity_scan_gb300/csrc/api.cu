@@ -412,7 +412,7 @@ struct dseq_ctx {
     Options opt;
     DevBuf e_unit, e_split, e_f16, rn, nrm;
     // run workspace
-    DevBuf m, keys, q, q_rn, csum, c_exp, status, barrier, starts, mask, picks, trace_slot, timeline;
+    DevBuf m, held, keys, q, q_rn, csum, c_exp, status, barrier, starts, mask, picks, trace_slot, timeline;
     // global-mask compaction: the unmasked rows' tables and the index maps
     DevBuf col_map, comp_of, e_split_c, e_f16_c, rn_c;
     int64_t timeline_iters = 0, timeline_grid = 0;
@@ -426,7 +426,7 @@ struct dseq_ctx {
     std::vector<uint8_t> state_mask;
     ~dseq_ctx() {
         DevBuf *all[] = {&e_unit, &e_split, &e_f16,  &rn,      &nrm,    &m,
-                         &keys,   &q,       &q_rn,   &csum,    &c_exp,  &status, &barrier,
+                         &held,   &keys,    &q,      &q_rn,    &csum,   &c_exp,  &status, &barrier,
                          &starts, &mask,    &picks,  &trace_slot, &timeline,
                          &col_map, &comp_of, &e_split_c, &e_f16_c, &rn_c};
         for (DevBuf *b : all) b->release();
@@ -720,6 +720,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             TRY(ctx->c_exp.ensure((size_t)Bp * sizeof(int)));
             a.csum = ctx->csum.as<long long>();
             a.c_exp = ctx->c_exp.as<int>();
+            TRY(ctx->held.ensure((size_t)plan.n_beta * kUnitRows * plan.columns() / 32 * sizeof(unsigned)));
+            a.held = ctx->held.as<unsigned>();
             if (ctx->csum_shift == kNoShift) {
                 // every raw-row entry is below the largest row norm 2^e and a
                 // sequence holds at most N rows: F = 62 - e - ceil(log2 N)

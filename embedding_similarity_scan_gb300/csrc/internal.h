@@ -136,6 +136,11 @@ struct TcDseqArgs {
     long long *csum;
     int csum_shift;
     int *c_exp;              // Bp: exponent sb of each query's scale 2^-sb (centroid)
+    // centroid: one bit per (sequence, candidate), set for held, masked and
+    // padding candidates; word (g, r) of tile (j, beta) at
+    // tile_base(j, beta) / 32 + g * 128 + r covers columns 32 g .. 32 g + 31
+    // of that tile for row r
+    unsigned *held;
     const float *e_unit;
     const float *nrm;
     float *m;                // units x 128 x tile_n

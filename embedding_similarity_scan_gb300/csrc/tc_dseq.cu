@@ -113,6 +113,32 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
         }
         reinterpret_cast<float4 *>(a.m)[i4] = make_float4(out[0], out[1], out[2], out[3]);
     }
+    // centroid: the held-candidate bits, one word per (row, 32 columns)
+    if (a.centroid) {
+        const int64_t total_w = p.columns() * per_col / 32;
+        for (int64_t wi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; wi < total_w; wi += stride) {
+            const int64_t i = 32 * wi;
+            const int j = p.chunk_of(i / per_col);
+            const int64_t tile = (int64_t)kUnitRows * p.width(j);
+            const int64_t local = i - p.col0(j) * per_col;
+            const int beta = (int)(local / tile);
+            const int sw = (int)((local - beta * tile) / 32);  // word within the tile
+            const int g = sw / kUnitRows, r = sw % kUnitRows;
+            const int b = beta * kUnitRows + r;
+            const int64_t cand0 = p.col0(j) + 32 * g;
+            const int st0 = b < a.B ? starts[b] : -1;
+            const int st = (a.comp_of && st0 >= 0) ? a.comp_of[st0] : st0;
+            unsigned bits = 0u;
+            for (int z = 0; z < 32; ++z) {
+                const int64_t cand = cand0 + z;
+                bool live = b < a.B && cand < a.N;
+                if (live && mask && mask[cand]) live = false;
+                if (live && cand == st) live = false;
+                if (!live) bits |= 1u << z;
+            }
+            a.held[wi] = bits;
+        }
+    }
     // query rows: the start rows, zero rows for padded sequences
     const int vec = a.Dp / 8;  // 16-byte vectors per row segment
     const int64_t qtotal = (int64_t)p.n_beta * kUnitRows * vec;
@@ -456,12 +482,19 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         const int groups = p.width(j) / 32;
         const int64_t c0 = p.col0(j);
         float4 *mt = reinterpret_cast<float4 *>(a.m + p.tile_base(j, beta));
-        // prefetch the first group's running minima before waiting
+        // prefetch the first group's running minima (centroid: its held
+        // bits, one word per row) before waiting
         float4 mcur[8], mnext[8];
+        const unsigned *ht = kCentroid ? a.held + p.tile_base(j, beta) / 32 : nullptr;
+        unsigned hcur = 0u, hnext = 0u;
         if (h < groups) {
+            if (kCentroid) {
+                hcur = __ldcg(ht + h * kUnitRows + r);
+            } else {
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-                mcur[v] = ld_cg_hint(&mt[((h * 4 + q) * 8 + v) * 32 + lane], stream);
+                for (int v = 0; v < 8; ++v)
+                    mcur[v] = ld_cg_hint(&mt[((h * 4 + q) * 8 + v) * 32 + lane], stream);
+            }
         }
         // fp16 storage: d = 1 - acc * rn_q * rn_c with the rows' inverse
         // norms; this warp's (at most 4) column groups' norms are
@@ -499,31 +532,52 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
             const float *rn_g = my_rn;
             const int gn = g + 2;
             if (gn < groups) {
+                if (kCentroid) {
+                    hnext = __ldcg(ht + gn * kUnitRows + r);
+                } else {
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    mnext[v] = ld_cg_hint(&mt[((gn * 4 + q) * 8 + v) * 32 + lane], stream);
+                    for (int v = 0; v < 8; ++v)
+                        mnext[v] = ld_cg_hint(&mt[((gn * 4 + q) * 8 + v) * 32 + lane], stream);
+                }
             }
             float acc[32];
             tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
             tmem_wait_ld();
             const uint32_t cbase = (uint32_t)c0 + 32u * (uint32_t)g;
+            if constexpr (kCentroid) {
+                // this iteration's distances to the centroid; held, masked
+                // and padding columns -inf.  They are stored only for a trace.
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    float dv[4];
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) {
+                        const int c = 4 * v + z;
+                        dv[z] = ((hcur >> c) & 1u) ? -INFINITY : fmaf(acc[c], neg_rnq, 1.0f);
+                        if (dv[z] > best) {
+                            best = dv[z];
+                            best_c = cbase + c;
+                        }
+                    }
+                    if (a.trace_slot)
+                        st_cg_hint(&mt[((g * 4 + q) * 8 + v) * 32 + lane],
+                                   make_float4(dv[0], dv[1], dv[2], dv[3]), stream);
+                }
+                hcur = hnext;
+                continue;
+            }
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
                 float mv[4] = {mcur[v].x, mcur[v].y, mcur[v].z, mcur[v].w};
                 bool changed = false;
-                // max-min: m keeps the running minimum.  Centroid: m is
-                // -inf for held / masked rows and this iteration's
-                // distance otherwise.
+                // max-min: m keeps the running minimum
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
                     // split storage: d = 1 - <q, e>, the accumulator holding
                     // 2^12 <q, e> of unit rows
-                    const float d =
-                        kF16 ? fmaf(acc[4 * v + z] * rn_g[4 * v + z], neg_rnq, 1.0f)
-                        : kCentroid ? fmaf(acc[4 * v + z], neg_rnq, 1.0f)
-                                    : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
-                    const float nv = kCentroid ? (mv[z] == -INFINITY ? -INFINITY : d)
-                                               : fminf(mv[z], d);
+                    const float d = kF16 ? fmaf(acc[4 * v + z] * rn_g[4 * v + z], neg_rnq, 1.0f)
+                                         : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
+                    const float nv = fminf(mv[z], d);
                     changed |= nv != mv[z];
                     mv[z] = nv;
                     if (mv[z] > best) {
@@ -533,9 +587,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                 }
                 // a candidate's running minimum changes with probability
                 // about 1/(t+1) after t picks: write back only what moved
-                // centroid: the next iteration needs only the -inf marks,
-                // so this iteration's distances are stored only for a trace
-                if (changed && (!kCentroid || a.trace_slot))
+                if (changed)
                     st_cg_hint(&mt[((g * 4 + q) * 8 + v) * 32 + lane],
                                make_float4(mv[0], mv[1], mv[2], mv[3]), stream);
             }
@@ -603,6 +655,9 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                 const int jw = p.chunk_of(w);
                 const int cw = (int)(w - p.col0(jw));
                 a.m[p.tile_base(jw, beta) + tc_m_inner(r, cw)] = -INFINITY;
+                if (kCentroid)
+                    atomicOr(a.held + p.tile_base(jw, beta) / 32 + (cw / 32) * kUnitRows + r,
+                             1u << (cw % 32));
             }
             // next queries: the centroid's (per sequence), else the winners'
             // stored rows, all rows of the run by the whole warp
