@@ -102,6 +102,18 @@ def _profiled_traffic(kernel: str, workload: str, variant: str = ""):
     return None
 
 
+def _traffic_variant(opts) -> str:
+    """Key of a launch variant's traffic line: "_pair0" for the single-CTA
+    tensor kernels, "_centroid" / "_f16" for the centroid criterion and
+    fp16 storage (their DRAM traffic differs from the default's)."""
+    v = "_pair0" if "pair=0" in opts else ""
+    if "criterion=1" in opts:
+        v += "_centroid"
+    if "storage=1" in opts:
+        v += "_f16"
+    return v
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
 
@@ -530,7 +542,7 @@ def run_ours(args):
             "peak_kind": peak_kind,
             "frac_of_burst": (achieved / burst_peak) if achieved else None,
             "traffic": None if shrunk else _profiled_traffic(kernel_name, epoch_of or args.workload,
-                                                             "_pair0" if "pair=0" in args.opt else ""),
+                                                             _traffic_variant(args.opt)),
             "kernel": kernel_name,
             "note": (f"achieved = algorithmic FLOP (2*{'N*D*B*L' if is_div else 'n*M*D'})"
                      f" / kernel time (CUDA events on the launching stream); {peak_note}")}
