@@ -34,10 +34,13 @@
 //   warps 2-9   epilogue: TMEM -> registers, d = 1 - S, m = min(m, d) on the
 //               running-minimum tile (read once, written back only where it
 //               moved, 16-byte coalesced), running (max m, lowest index) per
-//               row, one 64-bit atomicMax per row and unit into its key;
+//               row, one 64-bit atomicMax per row and unit into its key
+//               (centroid criterion: d to the centroid against one held
+//               bit per candidate, no running state);
 //   warps 10-   commit warps: once every CTA has published a half of an
 //               iteration, decode the winners of this CTA's share of that
-//               half, record them, mask them in m, write the next queries
+//               half, record them, mask them in m (and in the held bits),
+//               write the next queries
 //               (the winners' stored rows, or the new centroids), and
 //               release the half to the producers of the next iteration.
 // Every wait is bounded in time and sets the status word instead of hanging.

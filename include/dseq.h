@@ -230,9 +230,10 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *   "criterion"   0 = max-min (default): a candidate's score is its smallest
  *                 cosine distance to any row the sequence holds; 1 = centroid:
  *                 its cosine distance to the centroid (plain mean) of those
- *                 rows, a zero centroid giving distance 1 (the issue's "most
- *                 different from the centroid").  With 1, dseq_run_trace
- *                 records these centroid distances instead of running minima.
+ *                 rows, a zero centroid giving distance 1 (the issue's
+ *                 centroid ranking in its FP16 storage section).  With 1,
+ *                 dseq_run_trace records these centroid distances instead
+ *                 of running minima.
  *                 Tensor-core engine with storage 0 only (DSEQ_EINVAL else).
  *   "storage"     how the diversity kernel holds the table: 0 = fp16 hi/lo
  *                 split of the unit rows, three tensor-core products per
