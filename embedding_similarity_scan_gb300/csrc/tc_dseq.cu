@@ -317,9 +317,9 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     const int kblocks = a.Dp / kKBlock;
 
     // work items: (sequence block, chunk) units, or (sequence block pair,
-    // chunk) for a cluster.  Overlapped kernels split the blocks into two
-    // halves and order each iteration's items [half 0][half 1], each half
-    // candidate-chunk-major; the centroid kernel has one half.
+    // chunk) for a cluster.  The blocks form two halves, and each
+    // iteration's items are ordered [half 0][half 1], each half
+    // candidate-chunk-major.
     const int n_blocks = kPair ? p.n_beta / 2 : p.n_beta;
     const int n_h0 = (n_blocks + 1) / 2;
     const int n_h1 = n_blocks - n_h0;
