@@ -691,7 +691,9 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         TRY(ctx->m.ensure((size_t)plan.n_beta * kUnitRows * plan.columns() * sizeof(float)));
         // split storage: queries [hi*2^12 | hi | lo], table [hi | lo];
         // fp16 storage: one fp16 part each, plus inverse norms
-        const int qparts = f16 ? 1 : 3, eparts = f16 ? 1 : 2;
+        // (the centroid query on fp16 storage is not an fp16 row: it keeps
+        // (hi*2^12, lo))
+        const int qparts = f16 ? (ctx->opt.criterion ? 2 : 1) : 3, eparts = f16 ? 1 : 2;
         const __half *t_split = compact ? ctx->e_split_c.as<__half>() : ctx->e_split.as<__half>();
         const __half *t_f16 = compact ? ctx->e_f16_c.as<__half>() : ctx->e_f16.as<__half>();
         const float *t_rn = compact ? ctx->rn_c.as<float>() : ctx->rn.as<float>();
@@ -715,7 +717,6 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.q_rn = ctx->q_rn.as<float>();
         a.centroid = (int)ctx->opt.criterion;
         if (a.centroid) {
-            if (f16) return fail(DSEQ_EINVAL, "the centroid criterion runs on split storage (storage=0)");
             TRY(ctx->csum.ensure((size_t)Bp * ctx->Dp * sizeof(long long)));
             TRY(ctx->c_exp.ensure((size_t)Bp * sizeof(int)));
             a.csum = ctx->csum.as<long long>();

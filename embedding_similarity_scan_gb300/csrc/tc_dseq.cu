@@ -61,14 +61,16 @@ constexpr uint32_t kAccCols = 256;
 constexpr int kMaxGroups = 8;
 
 // Stage geometry.  Split storage (fp32-accurate): A = 3 x (128 x 32),
-// B = 2 x (rows x 32) fp16; fp16 storage: one part each.  One CTA stages up
-// to 256 candidate rows, a CTA pair half of the chunk (<= 128 rows) per SM.
-// Stage counts fill 194-231 KB of shared memory.
+// B = 2 x (rows x 32) fp16; fp16 storage: one part each, except the
+// centroid query, which is not an fp16 row and keeps two parts
+// (hi * 2^12, lo).  One CTA stages up to 256 candidate rows, a CTA pair half
+// of the chunk (<= 128 rows) per SM.  Stage counts fill 194-231 KB of shared
+// memory.
 // The stages start at the dynamic shared memory base, which the kernel
 // requires (and checks) to be 1024-byte aligned: there is no room for slack.
-template <bool kPair, bool kF16>
+template <bool kPair, bool kF16, bool kCentroid = false>
 struct DseqCfg {
-    static constexpr int kPartsA = kF16 ? 1 : 3;
+    static constexpr int kPartsA = kF16 ? (kCentroid ? 2 : 1) : 3;
     static constexpr int kPartsB = kF16 ? 1 : 2;
     static constexpr uint32_t kSubB = (kPair ? 128u : 256u) * kKBlock * 2;
     // one K block's operands; an fp16-storage stage holds two K blocks, so
@@ -76,7 +78,8 @@ struct DseqCfg {
     static constexpr uint32_t kKbBytes = kPartsA * kSubA + kPartsB * kSubB;
     static constexpr int kKbPerStage = kF16 ? 2 : 1;
     static constexpr uint32_t kStage = kKbPerStage * kKbBytes;
-    static constexpr int kStagesT = kF16 ? (kPair ? 7 : 4) : (kPair ? 5 : kStages);
+    static constexpr int kStagesT =
+        kF16 ? (kCentroid ? (kPair ? 4 : 3) : (kPair ? 7 : 4)) : (kPair ? 5 : kStages);
     static constexpr uint32_t kBarrierBytes = 512;  // barriers, TMEM slot, flags
     // + per-warp column norms of one 32-column group (fp16 storage)
     static constexpr size_t kSmemBytes =
@@ -145,7 +148,7 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
     // query rows: the start rows, zero rows for padded sequences
     const int vec = a.Dp / 8;  // 16-byte vectors per row segment
     const int64_t qtotal = (int64_t)p.n_beta * kUnitRows * vec;
-    if (a.e_f16) {  // fp16 storage: the stored row and its inverse norm
+    if (a.e_f16 && !a.centroid) {  // fp16 storage: the stored row and its inverse norm
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < qtotal;
              i += stride) {
             const int b = (int)(i / vec), k = (int)(i - (int64_t)b * vec);
@@ -156,10 +159,13 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
             if (k == 0) a.q_rn[b] = b < a.B ? a.rn_full[starts[b]] : 0.0f;
         }
     }
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < qtotal && !a.e_f16;
-         i += stride) {
+    // split queries: (hi * 2^12, hi, lo) of the start's unit row; the
+    // centroid on fp16 storage keeps (hi * 2^12, lo)
+    const int qparts = a.e_f16 ? 2 : 3;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+         i < qtotal && (!a.e_f16 || a.centroid); i += stride) {
         const int b = (int)(i / vec), k = (int)(i - (int64_t)b * vec);
-        uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * 3 * a.Dp);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.q_split + (int64_t)b * qparts * a.Dp);
         if (b < a.B) {
             const uint4 *src = reinterpret_cast<const uint4 *>(a.e_split_full +
                                                                (int64_t)starts[b] * 2 * a.Dp);
@@ -170,13 +176,11 @@ __global__ void tc_dseq_init_kernel(TcDseqArgs a, TcPlan p, const int32_t *__res
 #pragma unroll
             for (int z = 0; z < 4; ++z) h2[z] = __hmul2(h2[z], scale);
             dst[k] = hi12;
-            dst[vec + k] = hi;
-            dst[2 * vec + k] = lo;
+            if (qparts == 3) dst[vec + k] = hi;
+            dst[(qparts - 1) * vec + k] = lo;
         } else {
             const uint4 z = make_uint4(0, 0, 0, 0);
-            dst[k] = z;
-            dst[vec + k] = z;
-            dst[2 * vec + k] = z;
+            for (int part = 0; part < qparts; ++part) dst[part * vec + k] = z;
         }
     }
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -239,7 +243,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     tc_dseq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
                    const TcPlan p) {
-    using Cfg = DseqCfg<kPair, kF16>;
+    using Cfg = DseqCfg<kPair, kF16, kCentroid>;
     constexpr int kThreads = dseq_threads<kCentroid>();
     constexpr int kCommitWarps = dseq_commit_warps<kCentroid>();
     constexpr int kPartsA = Cfg::kPartsA, kPartsB = Cfg::kPartsB;
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         // running minima (one contiguous tile) are brought into L2 ahead of
         // the epilogue that reads them.  (The split-storage kernels are
         // tensor-bound; there the prefetch only added DRAM reads.)
-        if (kF16)
+        if (kF16 && !kCentroid)
             prefetch_l2_hint(a.m + p.tile_base(j, beta),
                              (uint32_t)p.width(j) * kUnitRows * (uint32_t)sizeof(float), m_pol);
         const int yq = beta * kUnitRows;
@@ -443,6 +447,13 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                             umma_f16_pair(d_tmem, a0, b0, idesc, (kb | k16) != 0);
                         else
                             umma_f16(d_tmem, a0, b0, idesc, (kb | k16) != 0);
+                        if (kCentroid) {  // the centroid's lo part
+                            const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
+                            if (kPair)
+                                umma_f16_pair(d_tmem, a1, b0, idesc, 1u);
+                            else
+                                umma_f16(d_tmem, a1, b0, idesc, 1u);
+                        }
                         continue;
                     }
                     const uint64_t a1 = smem_desc_sw64(sa + kSubA + off);
@@ -556,7 +567,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
 #pragma unroll
                     for (int z = 0; z < 4; ++z) {
                         const int c = 4 * v + z;
-                        dv[z] = ((hcur >> c) & 1u) ? -INFINITY : fmaf(acc[c], neg_rnq, 1.0f);
+                        const float sc = kF16 ? acc[c] * rn_g[c] : acc[c];
+                        dv[z] = ((hcur >> c) & 1u) ? -INFINITY : fmaf(sc, neg_rnq, 1.0f);
                         if (dv[z] > best) {
                             best = dv[z];
                             best_c = cbase + c;
@@ -680,7 +692,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                     long long *cs = a.csum + (int64_t)bq * a.Dp;
                     const int64_t wr = a.col_map ? a.col_map[wi] : wi;  // table row
                     const float *eu = a.e_unit + wr * a.Dp;
-                    __half *qd = a.q_split + (int64_t)bq * 3 * a.Dp;
+                    constexpr int kQParts = kF16 ? 2 : 3;  // (hi*2^12, [hi,] lo)
+                    __half *qd = a.q_split + (int64_t)bq * kQParts * a.Dp;
                     const float nw = a.nrm[wr];
                     const int F = a.csum_shift;
                     int sb = a.c_exp[bq];
@@ -690,8 +703,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                         const __half hi = __float2half_rn(c);
                         const __half lo = __float2half_rn((c - __half2float(hi)) * 4096.0f);
                         qd[k] = __float2half_rn(__half2float(hi) * 4096.0f);
-                        qd[a.Dp + k] = hi;
-                        qd[2 * a.Dp + k] = lo;
+                        if (!kF16) qd[a.Dp + k] = hi;
+                        qd[(kQParts - 1) * a.Dp + k] = lo;
                     };
                     constexpr int kB = 12;  // loads in flight per lane
                     KahanSum ss;
@@ -1001,7 +1014,7 @@ cudaError_t launch_variant(const TcDseqArgs &a, const TcPlan &p, const CUtensorM
     TcDseqArgs aa = a;
     TcPlan pp = p;
     CUtensorMap mq = tmap_q, me = tmap_e;
-    const size_t smem = DseqCfg<kPair, kF16>::kSmemBytes;
+    const size_t smem = DseqCfg<kPair, kF16, kCentroid>::kSmemBytes;
     auto kernel = tc_dseq_kernel<kPair, kF16, kCentroid>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1046,10 +1059,12 @@ void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *st
 cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st) {
     const bool f16 = a.e_f16 != nullptr;
-    if (a.centroid) {  // split storage only
-        if (f16) return cudaErrorInvalidValue;
-        return p.pair ? launch_variant<true, false, true>(a, p, tmap_q, tmap_e, st)
-                      : launch_variant<false, false, true>(a, p, tmap_q, tmap_e, st);
+    if (a.centroid) {
+        if (p.pair)
+            return f16 ? launch_variant<true, true, true>(a, p, tmap_q, tmap_e, st)
+                       : launch_variant<true, false, true>(a, p, tmap_q, tmap_e, st);
+        return f16 ? launch_variant<false, true, true>(a, p, tmap_q, tmap_e, st)
+                   : launch_variant<false, false, true>(a, p, tmap_q, tmap_e, st);
     }
     if (p.pair)
         return f16 ? launch_variant<true, true, false>(a, p, tmap_q, tmap_e, st)

@@ -233,8 +233,11 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 rows, a zero centroid giving distance 1 (the issue's
  *                 centroid ranking in its FP16 storage section).  With 1,
  *                 dseq_run_trace records these centroid distances instead
- *                 of running minima.
- *                 Tensor-core engine with storage 0 only (DSEQ_EINVAL else).
+ *                 of running minima.  Tensor-core engine only (DSEQ_EINVAL
+ *                 with engine 1); with storage 1 the table is held as fp16
+ *                 rows and the centroid query keeps fp32-level precision
+ *                 (two fp16 parts), so the distance is the cosine between
+ *                 the exact centroid and the stored row.
  *   "storage"     how the diversity kernel holds the table: 0 = fp16 hi/lo
  *                 split of the unit rows, three tensor-core products per
  *                 step, fp32-level distances (default); 1 = fp16 rows (each
