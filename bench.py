@@ -14,6 +14,12 @@ steps; ``e2e`` is the same metric through the C ABI with host buffers (the
 table upload, start/pick copies inside the timed region); ``roofline`` is the
 dominant kernel's algorithmic FLOP rate against the measured tensor peak;
 ``cpu_baseline`` is the CPU oracle timed on a bounded sample on this host.
+The default line (page-1 diversity, no options) also carries ``bmu``: the
+SOM 256 x 256 best-matching-unit search timed in the same run, with its own
+value, roofline, end-to-end number and CPU baseline.  ``--opt
+isolate_epilogue=1`` times the epilogue-isolated diversity kernel (the
+contraction compiled out) and reports its running-minimum stream against
+HBM.
 
 ``--impl reference`` times the CPU oracle itself as the reference arm.
 Multi-GPU (torchrun): every rank runs the full workload on its own GPU
@@ -203,7 +209,8 @@ def run_reference(args):
         cfg = workloads.BMU[args.workload]
         X = cfg.samples(seed=0)
         W = cfg.codebook(seed=0)
-        nsamp = args.ref_sample or 4 * threads
+        # batches of 16 x threads: the oracle deals samples out in chunks of 16
+        nsamp = args.ref_sample or 16 * threads
         sample = f"{nsamp} of {cfg.n} samples per step"
         unit = "samples/s"
         metric = "BMU samples/s"
@@ -219,8 +226,8 @@ def run_reference(args):
         X = cfg.samples(seed=0)
         W = cfg.codebook(seed=0)
         bmu = np.random.default_rng(0).integers(0, cfg.M, cfg.n).astype(np.int32)
-        nsamp = args.ref_sample or 4 * threads
-        nneur = 4 * threads
+        nsamp = args.ref_sample or 16 * threads
+        nneur = 16 * threads
         sample = (f"per step: BMU of {nsamp} of {cfg.n} samples and the update of {nneur} of "
                   f"{cfg.M} neurons, scaled to one epoch")
         unit = "samples/s"
@@ -266,7 +273,11 @@ def run_reference(args):
 
 
 def _cpu_baseline(args, cfg, epoch_of=None):
-    """The oracle as it stands, on all host cores, on a bounded sample."""
+    """The oracle as it stands, on all host cores, on a bounded sample.
+
+    BMU samples are timed in batches of 16 x threads per call: the oracle
+    hands samples to its threads in chunks of 16, so a smaller batch leaves
+    threads idle and understates its rate."""
     import oracle
 
     cores = os.cpu_count() or 1
@@ -295,70 +306,70 @@ def _cpu_baseline(args, cfg, epoch_of=None):
                           f"({total_t:.1f} s of CPU work)"}
     X = cfg.samples(seed=0)
     W = cfg.codebook(seed=0)
+    batch = 16 * threads
+
+    def time_bmu(budget):
+        done, total = 0, 0.0
+        while (total < budget or done == 0) and done + batch <= cfg.n:
+            t0 = time.perf_counter()
+            oracle.bmu(X[done:done + batch], W, threads=threads)
+            total += time.perf_counter() - t0
+            done += batch
+        return done, total
+
     if epoch_of is not None:
         # one epoch = the BMU of every sample + the update of every neuron; time
         # a bounded sample of each and scale both to the whole epoch
         sx, sy = workloads.SOM_SIDES[epoch_of]
         bmu = np.random.default_rng(0).integers(0, cfg.M, cfg.n).astype(np.int32)
-        nb, tb, n = 0, 0.0, 2 * threads
-        while tb < t_target / 2 and nb + n <= cfg.n:
-            t0 = time.perf_counter()
-            oracle.bmu(X[nb:nb + n], W, threads=threads)
-            tb += time.perf_counter() - t0
-            nb += n
-            n *= 2
-        nu, tu, k = 0, 0.0, 2 * threads
-        while tu < t_target / 2 and nu + k <= cfg.M:
+        nb, tb = time_bmu(t_target / 2)
+        nu, tu, k = 0, 0.0, batch
+        while (tu < t_target / 2 or nu == 0) and nu + k <= cfg.M:
             t0 = time.perf_counter()
             oracle.som_update(X, bmu, W, sx, sy, workloads.SOM_SIGMA, workloads.SOM_RADIUS,
                               neurons=np.arange(nu, nu + k), threads=threads)
             tu += time.perf_counter() - t0
             nu += k
-            k *= 2
         epoch_s = tb / nb * cfg.n + tu / nu * cfg.M
         return {"value": cfg.n / epoch_s, "unit": "samples/s", "cores": threads,
-                "kind": "oracle",
-                "sample": (f"BMU of {nb} of {cfg.n} samples ({tb:.1f} s) and update of {nu} of "
-                           f"{cfg.M} neurons ({tu:.1f} s), scaled to one epoch "
-                           f"({epoch_s:.0f} s)")}
-    n, done, total_t = 2 * threads, 0, 0.0
-    while total_t < t_target and done + n <= cfg.n:
-        t0 = time.perf_counter()
-        oracle.bmu(X[done:done + n], W, threads=threads)
-        total_t += time.perf_counter() - t0
-        done += n
-        n *= 2
+                "kind": "oracle", "bmu_samples_per_s": nb / tb,
+                "sample": (f"BMU of {nb} of {cfg.n} samples in batches of {batch} ({tb:.1f} s) "
+                           f"and update of {nu} of {cfg.M} neurons ({tu:.1f} s), scaled to one "
+                           f"epoch ({epoch_s:.0f} s)")}
+    done, total_t = time_bmu(t_target)
     return {"value": done / total_t, "unit": "samples/s", "cores": threads, "kind": "oracle",
-            "sample": f"{done} of {cfg.n} samples ({total_t:.1f} s of CPU work)"}
+            "sample": (f"{done} of {cfg.n} samples in batches of {batch} "
+                       f"({total_t:.1f} s of CPU work)")}
 
 
-def run_ours(args):
+@dataclasses.dataclass
+class _Workload:
+    """One workload as the timed loop sees it."""
+    name: str
+    cfg: object
+    is_div: bool
+    epoch_of: object
+    units: int
+    flop: float
+    stream_bytes: object
+    stream_note: str
+    update_bytes: object
+    kernel_name: str
+    metric: str
+    unit: str
+    config: dict
+    step: object
+    e2e_step: object
+    close: object
+    update_ns: list
+
+
+def _workload(args, name, es, dev, rank, opts) -> _Workload:
     import torch
 
-    import embedding_similarity_scan_gb300 as es
-
-    ws, rank, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pg = None
-    if ws > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
-    es.load()
-    for kv in args.opt:
-        k, v = kv.split("=")
-        es.dseq_set_option(k, int(v))
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-
-    bf16_burst, bf16_sustained, hbm_peak, peak_src = _peaks()
-
-    is_div = args.workload in workloads.DIVERSITY
-    epoch_of = None
-    if is_div:
-        cfg = workloads.DIVERSITY[args.workload]
+    update_ns = []
+    if name in workloads.DIVERSITY:
+        cfg = workloads.DIVERSITY[name]
         if args.iters > 0:
             cfg = dataclasses.replace(cfg, L=args.iters)
         E_host = torch.from_numpy(cfg.table(seed=0)).pin_memory()
@@ -367,17 +378,13 @@ def run_ours(args):
         ctx = es.dseq_create(E_host.to(dev))
         starts_dev = starts_host.to(dev)
         picks_dev = torch.empty((cfg.B, cfg.L), dtype=torch.int32, device=dev)
-        units = cfg.B * cfg.L
-        flop = 2.0 * cfg.N * cfg.D * cfg.B * cfg.L
-        if "criterion=1" in args.opt:
+        if "criterion=1" in opts:
             # centroid: one held-candidate bit read per (sequence, candidate)
             stream_bytes = cfg.N * cfg.B * cfg.L / 8.0
             stream_note = "held-candidate bits read (B*N/8 bytes per iteration)"
         else:
             stream_bytes = 8.0 * cfg.N * cfg.B * cfg.L  # running-minimum read + write
             stream_note = "running-minimum read+write bytes (8*B*N per iteration)"
-        kernel_name = "tc_dseq_kernel"
-        metric, unit = "sequence-iterations/s", "sequence-iterations/s"
 
         def step():
             es.dseq_run(ctx, starts_dev, cfg.L, picks=picks_dev)
@@ -392,10 +399,15 @@ def run_ours(args):
                 c.close()
             return E_host.numel() * 4 + starts_host.numel() * 4, picks_host.numel() * 4
 
-        config = {"workload": args.workload, "N": cfg.N, "D": cfg.D, "B": cfg.B, "L": cfg.L,
-                  "l2": "flushed between steps (512 MB write)"}
-    elif args.workload in workloads.SOM_EPOCH:
-        epoch_of = workloads.SOM_EPOCH[args.workload]
+        return _Workload(
+            name, cfg, True, None, cfg.B * cfg.L, 2.0 * cfg.N * cfg.D * cfg.B * cfg.L,
+            stream_bytes, stream_note, None, "tc_dseq_kernel", "sequence-iterations/s",
+            "sequence-iterations/s",
+            {"workload": name, "N": cfg.N, "D": cfg.D, "B": cfg.B, "L": cfg.L,
+             "l2": "flushed between steps (512 MB write)"},
+            step, e2e_step, ctx.close, update_ns)
+    if name in workloads.SOM_EPOCH:
+        epoch_of = workloads.SOM_EPOCH[name]
         cfg = workloads.BMU[epoch_of]
         sx, sy = workloads.SOM_SIDES[epoch_of]
         sigma, radius = workloads.SOM_SIGMA, workloads.SOM_RADIUS
@@ -405,15 +417,6 @@ def run_ours(args):
         X_dev, W_dev = X_host.to(dev), W_host.to(dev)
         idx_dev = torch.empty(cfg.n, dtype=torch.int32, device=dev)
         dist_dev = torch.empty(cfg.n, dtype=torch.float32, device=dev)
-        units = cfg.n
-        flop = 2.0 * cfg.n * cfg.M * cfg.D
-        stream_bytes = None
-        # the update's algorithmic bytes: read the samples and their BMUs,
-        # read and write the codebook
-        update_bytes = 4.0 * cfg.n * cfg.D + 4.0 * cfg.n + 8.0 * cfg.M * cfg.D
-        kernel_name = _bmu_kernel_name(cfg.D, args.opt)
-        metric, unit = "SOM epoch samples/s", "samples/s"
-        update_ns = []
 
         def step():
             # each step is the next epoch of training on the same map
@@ -428,43 +431,60 @@ def run_ours(args):
             es.som_epoch(X_host, W_h, sx, sy, sigma, radius, bmu=idx_h, dist=dist_h)
             return (X_host.numel() + W_h.numel()) * 4, W_h.numel() * 4 + cfg.n * 8
 
-        config = {"workload": args.workload, "n": cfg.n, "M": cfg.M, "D": cfg.D,
-                  "map": f"{sx}x{sy}", "sigma": sigma, "radius": radius,
-                  "l2": "flushed between steps (512 MB write)"}
-    else:
-        cfg = workloads.BMU[args.workload]
-        if args.samples > 0:
-            cfg = dataclasses.replace(cfg, n=args.samples)
-        # each rank runs its own shard: the same codebook, its own samples
-        X_host = torch.from_numpy(cfg.samples(seed=rank)).pin_memory()
-        W_host = torch.from_numpy(cfg.codebook(seed=0)).pin_memory()
-        X_dev, W_dev = X_host.to(dev), W_host.to(dev)
-        idx_dev = torch.empty(cfg.n, dtype=torch.int32, device=dev)
-        dist_dev = torch.empty(cfg.n, dtype=torch.float32, device=dev)
-        units = cfg.n
-        flop = 2.0 * cfg.n * cfg.M * cfg.D
-        stream_bytes = None
-        kernel_name = _bmu_kernel_name(cfg.D, args.opt)
-        metric, unit = "BMU samples/s", "samples/s"
+        # the update's algorithmic bytes: read the samples and their BMUs,
+        # read and write the codebook
+        return _Workload(
+            name, cfg, False, epoch_of, cfg.n, 2.0 * cfg.n * cfg.M * cfg.D, None, "",
+            4.0 * cfg.n * cfg.D + 4.0 * cfg.n + 8.0 * cfg.M * cfg.D,
+            _bmu_kernel_name(cfg.D, opts), "SOM epoch samples/s", "samples/s",
+            {"workload": name, "n": cfg.n, "M": cfg.M, "D": cfg.D, "map": f"{sx}x{sy}",
+             "sigma": sigma, "radius": radius, "l2": "flushed between steps (512 MB write)"},
+            step, e2e_step, lambda: None, update_ns)
+    cfg = workloads.BMU[name]
+    if args.samples > 0:
+        cfg = dataclasses.replace(cfg, n=args.samples)
+    # each rank runs its own shard: the same codebook, its own samples
+    X_host = torch.from_numpy(cfg.samples(seed=rank)).pin_memory()
+    W_host = torch.from_numpy(cfg.codebook(seed=0)).pin_memory()
+    X_dev, W_dev = X_host.to(dev), W_host.to(dev)
+    idx_dev = torch.empty(cfg.n, dtype=torch.int32, device=dev)
+    dist_dev = torch.empty(cfg.n, dtype=torch.float32, device=dev)
 
-        def step():
-            es.bmu_search(X_dev, W_dev, idx=idx_dev, dist=dist_dev)
-            return es.dseq_last_stat("kernel_ns"), es.dseq_last_stat("launches")
+    def step():
+        es.bmu_search(X_dev, W_dev, idx=idx_dev, dist=dist_dev)
+        return es.dseq_last_stat("kernel_ns"), es.dseq_last_stat("launches")
 
-        def e2e_step():
-            idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
-            dist_h = torch.empty(cfg.n, dtype=torch.float32).pin_memory()
-            es.bmu_search(X_host, W_host, idx=idx_h, dist=dist_h)
-            return (X_host.numel() + W_host.numel()) * 4, cfg.n * 8
+    def e2e_step():
+        idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
+        dist_h = torch.empty(cfg.n, dtype=torch.float32).pin_memory()
+        es.bmu_search(X_host, W_host, idx=idx_h, dist=dist_h)
+        return (X_host.numel() + W_host.numel()) * 4, cfg.n * 8
 
-        config = {"workload": args.workload, "n": cfg.n, "M": cfg.M, "D": cfg.D,
-                  "l2": "flushed between steps (512 MB write)"}
+    return _Workload(
+        name, cfg, False, None, cfg.n, 2.0 * cfg.n * cfg.M * cfg.D, None, "", None,
+        _bmu_kernel_name(cfg.D, opts), "BMU samples/s", "samples/s",
+        {"workload": name, "n": cfg.n, "M": cfg.M, "D": cfg.D,
+         "l2": "flushed between steps (512 MB write)"},
+        step, e2e_step, lambda: None, update_ns)
 
-    if args.opt:
-        config["options"] = list(args.opt)
+
+def _measure(args, wl, opts, dev, local, pg, ws, flush):
+    """Warm up, time args.steps steps with CUDA events (L2 flushed between
+    them), then the end-to-end leg; returns the JSON line (no cpu_baseline)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    bf16_burst, bf16_sustained, hbm_peak, peak_src = _peaks()
+    isolate = "isolate_epilogue=1" in opts
+    config = dict(wl.config)
+    if opts:
+        config["options"] = list(opts)
     shrunk = args.iters > 0 or args.samples > 0
     if shrunk:
         config["reduced"] = "smaller than the workload (--iters / --samples): a profiling case"
+    if isolate:
+        config["isolated_epilogue"] = ("contraction compiled out (picks meaningless): measures "
+                                       "the running-minimum stream of the fused epilogue alone")
 
     def barrier():
         torch.cuda.synchronize()
@@ -473,9 +493,10 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        step()
+        wl.step()
         flush.zero_()
     barrier()
+    wl.update_ns.clear()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     kernel_ns, launches = [], 0
@@ -483,7 +504,7 @@ def run_ours(args):
         t_wall = time.perf_counter()
         for i in range(args.steps):
             ev[i][0].record(stream)
-            kns, nl = step()
+            kns, nl = wl.step()
             ev[i][1].record(stream)
             kernel_ns.append(kns)
             launches += nl
@@ -496,25 +517,25 @@ def run_ours(args):
         t = torch.tensor([total_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         total_ms = float(t.item())
-    value = ws * units * args.steps / (total_ms / 1e3)
+    value = ws * wl.units * args.steps / (total_ms / 1e3)
 
     # end to end through the C ABI with host buffers
     e2e_steps = max(1, min(args.steps, 3))
-    e2e_step()
+    wl.e2e_step()
     barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        h2d, d2h = e2e_step()
+        h2d, d2h = wl.e2e_step()
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
     if pg is not None:
         t = torch.tensor([e2e_s], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_s = float(t.item())
-    e2e_value = ws * units * e2e_steps / e2e_s
+    e2e_value = ws * wl.units * e2e_steps / e2e_s
 
     k_avg_s = statistics.mean(kernel_ns) / 1e9 if kernel_ns and min(kernel_ns) > 0 else None
-    achieved = flop / k_avg_s / 1e12 if k_avg_s else None
+    achieved = wl.flop / k_avg_s / 1e12 if k_avg_s else None
     clocks = clk.summary()
     # a run held at the power cap is compared with the sustained tensor peak
     # (cuBLAS run back to back under the cap), otherwise with the burst peak
@@ -524,11 +545,11 @@ def run_ours(args):
     # fp32-equivalent tensor peak of the split contraction: three fp16 MMAs per
     # fp32 multiply-add (fp16 and bf16 run at the same nominal rate)
     split_peak = bf16_peak / 3.0
-    fp16_storage = is_div and "storage=1" in args.opt
+    fp16_storage = wl.is_div and "storage=1" in opts
     if fp16_storage:
         # one fp16 product per multiply-add: the plain fp16 (= bf16 nominal)
         # peak; the centroid query keeps two parts (hi*2^12, lo), two products
-        nprod = 2 if "criterion=1" in args.opt else 1
+        nprod = 2 if "criterion=1" in opts else 1
         tensor_peak = bf16_peak / nprod
         burst_peak = bf16_burst / nprod
         peak_note = (f"peak = {peak_src} bf16 {peak_kind} {bf16_peak:.1f} TFLOP/s"
@@ -544,63 +565,115 @@ def run_ours(args):
             "frac": (achieved / tensor_peak) if achieved else None,
             "peak_kind": peak_kind,
             "frac_of_burst": (achieved / burst_peak) if achieved else None,
-            "traffic": None if shrunk else _profiled_traffic(kernel_name, epoch_of or args.workload,
-                                                             _traffic_variant(args.opt)),
-            "kernel": kernel_name,
-            "note": (f"achieved = algorithmic FLOP (2*{'N*D*B*L' if is_div else 'n*M*D'})"
+            "traffic": None if (shrunk or isolate) else _profiled_traffic(
+                wl.kernel_name, wl.epoch_of or wl.name, _traffic_variant(opts)),
+            "kernel": wl.kernel_name,
+            "note": (f"achieved = algorithmic FLOP (2*{'N*D*B*L' if wl.is_div else 'n*M*D'})"
                      f" / kernel time (CUDA events on the launching stream); {peak_note}")}
-    if "engine=1" in args.opt:
+    if "engine=1" in opts:
         # the plain fp32 SIMT variant: bound by the FP32 pipe, 128 fp32 FMA
         # lanes per SM, 2 FLOP each, at the maximum SM clock
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         mhz = clocks.get("sm_max_mhz") or 2070.0
         alu_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
-        roof.update({"bound": "alu", "peak": alu_peak, "frac": (achieved / alu_peak) if achieved else None,
+        roof.update({"bound": "alu", "peak": alu_peak,
+                     "frac": (achieved / alu_peak) if achieved else None,
                      "peak_kind": "fp32 pipe, derived", "frac_of_burst": None, "traffic": None,
-                     "kernel": "ffma_dseq_fold_kernel" if is_div else "ffma_bmu_kernel",
-                     "note": (f"achieved = algorithmic FLOP / kernel time ({'fold + commit launches' if is_div else 'one launch'}, CUDA events); peak = {sms} SMs x 128 "
-                              f"FP32 lanes x 2 FLOP x {mhz:.0f} MHz (derived, not measured)")})
-    if stream_bytes is not None and k_avg_s:
-        hbm_achieved = stream_bytes / k_avg_s / 1e9
-        if hbm_achieved / hbm_peak > (roof["frac"] or 0.0):
-            # the min-distance stream binds: report the HBM roofline instead
+                     "kernel": "ffma_dseq_fold_kernel" if wl.is_div else "ffma_bmu_kernel",
+                     "note": (f"achieved = algorithmic FLOP / kernel time "
+                              f"({'fold + commit launches' if wl.is_div else 'one launch'}, "
+                              f"CUDA events); peak = {sms} SMs x 128 FP32 lanes x 2 FLOP x "
+                              f"{mhz:.0f} MHz (derived, not measured)")})
+    if wl.stream_bytes is not None and k_avg_s:
+        hbm_achieved = wl.stream_bytes / k_avg_s / 1e9
+        if isolate or hbm_achieved / hbm_peak > (roof["frac"] or 0.0):
+            # the min-distance stream binds (or is all the isolated kernel
+            # does): report the HBM roofline instead
             roof.update({"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak,
-                         "unit": "GB/s", "frac": hbm_achieved / hbm_peak,
-                         "tensor_frac": roof["frac"],
-                         "note": (f"achieved = {stream_note} / kernel time; peak = "
+                         "unit": "GB/s", "frac": hbm_achieved / hbm_peak, "peak_kind": "copy",
+                         "frac_of_burst": None,
+                         "tensor_frac": None if isolate else roof["frac"],
+                         "note": (f"achieved = {wl.stream_note} / kernel time; peak = "
                                   f"{peak_src} copy bandwidth {hbm_peak:.1f} GB/s")})
     line = {
-        "metric": metric, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
+        "metric": wl.metric, "value": value, "unit": wl.unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("f32 (FFMA)" if "engine=1" in args.opt
+        "dtype": ("f32 (FFMA)" if "engine=1" in opts
                   else "f16 storage, f32 accumulate" if fp16_storage
                   else "fp16x3-split (fp32-accurate), f32 accumulate"),
         "data": "synthetic", "config": config, "roofline": roof,
-        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": e2e_value, "unit": wl.unit, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches), "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
-    if stream_bytes is not None and k_avg_s:
+    if wl.stream_bytes is not None and k_avg_s:
         line["min_distance_stream"] = {
-            "achieved_gbs": stream_bytes / k_avg_s / 1e9, "peak_gbs": hbm_peak,
-            "frac": stream_bytes / k_avg_s / 1e9 / hbm_peak,
-            "note": f"{stream_note} / kernel time"}
-    if epoch_of is not None and update_ns and min(update_ns) > 0:
-        u_s = statistics.mean(update_ns) / 1e9
+            "achieved_gbs": wl.stream_bytes / k_avg_s / 1e9, "peak_gbs": hbm_peak,
+            "frac": wl.stream_bytes / k_avg_s / 1e9 / hbm_peak,
+            "note": f"{wl.stream_note} / kernel time"
+                    + (" (epilogue-isolated kernel)" if isolate else " (fused kernel)")}
+    if wl.epoch_of is not None and wl.update_ns and min(wl.update_ns) > 0:
+        u_s = statistics.mean(wl.update_ns) / 1e9
         line["som_update"] = {
-            "achieved_gbs": update_bytes / u_s / 1e9, "peak_gbs": hbm_peak,
-            "frac": update_bytes / u_s / 1e9 / hbm_peak, "ms": u_s * 1e3,
+            "achieved_gbs": wl.update_bytes / u_s / 1e9, "peak_gbs": hbm_peak,
+            "frac": wl.update_bytes / u_s / 1e9 / hbm_peak, "ms": u_s * 1e3,
             "share_of_step": u_s * 1e3 / (total_ms / args.steps),
             "note": ("neighbourhood update kernels: algorithmic bytes (samples + BMUs read, "
                      "codebook read + write) / their CUDA-event time")}
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = _cpu_baseline(args, cfg, epoch_of)
+    return line
+
+
+# the BMU half of the metric, measured beside the default diversity line
+BMU_BESIDE = "som256"
+
+
+def run_ours(args):
+    import torch
+
+    opts = list(args.opt)
+    if any(o.split("=")[0] in ("isolate_epilogue", "fault_skip_arrive", "fault_skip_copy")
+           for o in opts):
+        # the library accepts its measurement options only when opted in
+        os.environ["DSEQ_ENABLE_TEST_OPTIONS"] = "1"
+    import embedding_similarity_scan_gb300 as es
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    es.load()
+    for kv in opts:
+        k, v = kv.split("=")
+        es.dseq_set_option(k, int(v))
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    wl = _workload(args, args.workload, es, dev, rank, opts)
+    line = _measure(args, wl, opts, dev, local, pg, ws, flush)
+    wl.close()
+    with_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
+    if with_cpu and "isolate_epilogue=1" not in opts:
+        line["cpu_baseline"] = _cpu_baseline(args, wl.cfg, wl.epoch_of)
+    # the default line also carries the BMU half of the metric: the SOM
+    # 256 x 256 search timed in the same run, with its own roofline and CPU
+    # baseline
+    if args.with_bmu and not opts and args.workload == "page1" and args.iters == 0:
+        bw = _workload(args, BMU_BESIDE, es, dev, rank, opts)
+        b = _measure(args, bw, opts, dev, local, pg, ws, flush)
+        bw.close()
+        keep = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config",
+                "roofline", "e2e", "gpu_launches", "clocks", "wall_s_timed_region")
+        line["bmu"] = {k: b[k] for k in keep}
+        if with_cpu:
+            line["bmu"]["cpu_baseline"] = _cpu_baseline(args, bw.cfg, None)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if is_div:
-        ctx.close()
     if pg is not None:
         pg.barrier()
         pg.destroy_process_group()
@@ -626,6 +699,9 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=0)
     ap.add_argument("--opt", action="append", default=[],
                     help="library option name=value, e.g. storage=1 (process-wide)")
+    ap.add_argument("--no-bmu", dest="with_bmu", action="store_false",
+                    help="leave out the BMU search (som256) that the default page-1 line "
+                         "carries beside the diversity number")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -79,7 +80,17 @@ struct Options {
     int64_t resume = 0;
     int64_t slice = 0;
     int64_t compact = 1;
+    int64_t isolate_epilogue = 0;
 };
+
+// Test and measurement options (fault injection, the epilogue-isolated
+// kernel) change results on purpose; a process must opt in to them through
+// the environment variable DSEQ_ENABLE_TEST_OPTIONS=1 before setting one to a
+// non-zero value.
+bool test_options_enabled() {
+    const char *v = std::getenv("DSEQ_ENABLE_TEST_OPTIONS");
+    return v && std::strcmp(v, "1") == 0;
+}
 std::mutex g_opt_mu;
 Options g_defaults;
 
@@ -116,12 +127,15 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "timeline") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "timeline must be 0 or 1");
         o.timeline = v;
-    } else if (n == "fault_skip_arrive") {
-        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "fault_skip_arrive must be 0 or 1");
-        o.fault_skip_arrive = v;
-    } else if (n == "fault_skip_copy") {
-        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "fault_skip_copy must be 0 or 1");
-        o.fault_skip_copy = v;
+    } else if (n == "fault_skip_arrive" || n == "fault_skip_copy" || n == "isolate_epilogue") {
+        if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "%s must be 0 or 1", name);
+        if (v != 0 && !test_options_enabled())
+            return fail(DSEQ_EINVAL,
+                        "%s is a test option that changes results; set DSEQ_ENABLE_TEST_OPTIONS=1 "
+                        "in the environment to use it", name);
+        (n == "fault_skip_arrive" ? o.fault_skip_arrive
+         : n == "fault_skip_copy" ? o.fault_skip_copy
+                                  : o.isolate_epilogue) = v;
     } else if (n == "compact") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "compact must be 0 or 1");
         o.compact = v;
@@ -151,6 +165,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "storage") return o.storage;
     if (n == "criterion") return o.criterion;
     if (n == "resume") return o.resume;
+    if (n == "isolate_epilogue") return o.isolate_epilogue;
     return -1;
 }
 
@@ -182,20 +197,45 @@ struct DevBuf {
     }
 };
 
-bool is_device_ptr(const void *p) {
+// Where an array argument lives.  Device memory must belong to the current
+// device (the one the call's kernels run on): a pointer into another GPU's
+// memory would reach the kernels as plain loads and stores, which fault
+// without peer access, so it is rejected before any work is enqueued.
+// Managed memory counts as device memory; anything else as host memory.
+int locate(const void *p, const char *what, bool &on_device) {
+    on_device = false;
     cudaPointerAttributes at;
     cudaError_t e = cudaPointerGetAttributes(&at, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        return DSEQ_OK;
     }
-    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+    if (at.type == cudaMemoryTypeManaged) {
+        on_device = true;
+        return DSEQ_OK;
+    }
+    if (at.type != cudaMemoryTypeDevice) return DSEQ_OK;
+    int cur = -1;
+    CUDA_TRY(cudaGetDevice(&cur));
+    if (at.device != cur)
+        return fail(DSEQ_EINVAL, "%s is memory of device %d, but the current device is %d", what,
+                    at.device, cur);
+    on_device = true;
+    return DSEQ_OK;
+}
+
+bool is_device_ptr(const void *p) {
+    bool dev = false;
+    return locate(p, "array", dev) == DSEQ_OK && dev;
 }
 
 // input array: the device pointer itself, or a staged device copy of host data
 template <class T>
-int stage_in(const T *src, size_t count, DevBuf &buf, const T *&dev, cudaStream_t st) {
-    if (is_device_ptr(src)) {
+int stage_in(const T *src, size_t count, DevBuf &buf, const T *&dev, cudaStream_t st,
+             const char *what) {
+    bool on_device;
+    TRY(locate(src, what, on_device));
+    if (on_device) {
         dev = src;
         return DSEQ_OK;
     }
@@ -207,10 +247,13 @@ int stage_in(const T *src, size_t count, DevBuf &buf, const T *&dev, cudaStream_
 
 // host copy of a small argument array (for validation)
 template <class T>
-int to_host(const T *src, size_t count, std::vector<T> &out, cudaStream_t st) {
+int to_host(const T *src, size_t count, std::vector<T> &out, cudaStream_t st,
+            const char *what) {
     out.resize(count);
     if (count == 0) return DSEQ_OK;
-    if (is_device_ptr(src)) {
+    bool on_device;
+    TRY(locate(src, what, on_device));
+    if (on_device) {
         CUDA_TRY(cudaMemcpyAsync(out.data(), src, count * sizeof(T), cudaMemcpyDeviceToHost, st));
         CUDA_TRY(cudaStreamSynchronize(st));
     } else {
@@ -390,7 +433,9 @@ void clear_error() {
     g_err.clear();
     g_stats = Stats();
 }
-bool is_device(const void *p) { return is_device_ptr(p); }
+int locate_ptr(const void *p, const char *what, bool &on_device) {
+    return locate(p, what, on_device);
+}
 int sm_count(int dev, int *sms) {
     DeviceInfo info;
     TRY(device_info(dev, info));
@@ -501,7 +546,7 @@ int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device, v
     if ((r = ctx->status.ensure(sizeof(int))) != DSEQ_OK) return bail(r);
     DevBuf staged;
     const float *tdev = nullptr;
-    if ((r = stage_in(table, (size_t)N * D, staged, tdev, st)) != DSEQ_OK) return bail(r);
+    if ((r = stage_in(table, (size_t)N * D, staged, tdev, st, "table")) != DSEQ_OK) return bail(r);
     e = cudaMemsetAsync(ctx->status.p, 0, sizeof(int), st);
     if (e == cudaSuccess) {
         launch_table_prepare(tdev, N, D, ctx->Dp, ctx->e_unit.as<float>(),
@@ -554,9 +599,9 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
 
     // ---- validate on the host ----
     std::vector<int32_t> h_starts;
-    TRY(to_host(starts, (size_t)B, h_starts, st));
+    TRY(to_host(starts, (size_t)B, h_starts, st, "starts"));
     std::vector<uint8_t> h_mask;
-    if (mask) TRY(to_host(mask, (size_t)N, h_mask, st));
+    if (mask) TRY(to_host(mask, (size_t)N, h_mask, st, "mask"));
     // resume: continue the last run on this context from the state it left
     // on the device (same sequences, mask and mode; picks continue)
     const bool resume = ctx->opt.resume != 0;
@@ -583,6 +628,9 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             if (L > avail) return fail(DSEQ_EINVAL, "L=%d exceeds the %lld candidates left to sequence %d", L, (long long)avail, b);
         }
     }
+    if (ctx->opt.isolate_epilogue &&
+        (ctx->opt.engine != 0 || ctx->opt.criterion != 0 || resume))
+        return fail(DSEQ_EINVAL, "isolate_epilogue runs the tensor-core max-min kernel only, without resume");
     if (!resume) ctx->has_state = false;
     std::vector<int32_t> h_slot;
     // CTA pairs work on pairs of 128-sequence blocks: pad B to 256 there
@@ -590,9 +638,11 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     const int64_t Bp = round_up(B, pair ? 2 * kUnitRows : kUnitRows);
     if (n_trace > 0) {
         if (!trace_seqs || !trace_mindist) return fail(DSEQ_EINVAL, "trace arrays are NULL");
-        if (!is_device_ptr(trace_mindist)) return fail(DSEQ_EINVAL, "trace_mindist must be device memory");
+        bool trace_dev;
+        TRY(locate(trace_mindist, "trace_mindist", trace_dev));
+        if (!trace_dev) return fail(DSEQ_EINVAL, "trace_mindist must be device memory");
         std::vector<int32_t> h_tr;
-        TRY(to_host(trace_seqs, (size_t)n_trace, h_tr, st));
+        TRY(to_host(trace_seqs, (size_t)n_trace, h_tr, st, "trace_seqs"));
         h_slot.assign((size_t)Bp, -1);
         for (int32_t k = 0; k < n_trace; ++k) {
             const int32_t b = h_tr[k];
@@ -619,7 +669,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         CUDA_TRY(cudaMemcpyAsync(ctx->trace_slot.p, h_slot.data(), (size_t)Bp * sizeof(int32_t), cudaMemcpyHostToDevice, st));
         d_slot = ctx->trace_slot.as<int32_t>();
     }
-    const bool picks_on_dev = is_device_ptr(picks);
+    bool picks_on_dev;
+    TRY(locate(picks, "picks", picks_on_dev));
     int32_t *d_picks = picks;
     if (!picks_on_dev) {
         TRY(ctx->picks.ensure((size_t)B * L * sizeof(int32_t)));
@@ -672,14 +723,24 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         TcPlan plan{};
         plan.n_beta = (int)(Bp / kUnitRows);
         plan.pair = pair ? 1 : 0;
-        int grid_cap = ctx->opt.grid > 0 ? (int)std::min<int64_t>(ctx->opt.grid, info.sms) : info.sms;
+        // The persistent grid: the "grid" option as given, else as many CTAs
+        // of this kernel variant as can be co-resident (its own occupancy:
+        // thread count and shared memory).  A grid beyond that is refused by
+        // the cooperative launch and reported as DSEQ_ELAUNCH.
+        int grid_cap = 0;
+        if (ctx->opt.grid > 0) {
+            grid_cap = (int)ctx->opt.grid;
+        } else if (!resume) {
+            grid_cap = tc_dseq_max_grid(pair, f16, ctx->opt.criterion != 0);
+            if (grid_cap < (pair ? 2 : 1))
+                return fail(DSEQ_ELAUNCH, "no %s of this kernel variant fits on the device",
+                            pair ? "CTA pair" : "CTA");
+        }
         if (resume) {
             plan = ctx->state_plan;  // the running-minimum layout depends on it
         } else if (pair) {
-            // whole clusters of two, no more than can be co-resident
-            const int max_clusters = tc_dseq_pair_max_clusters(256);
-            if (max_clusters < 1) return fail(DSEQ_ELAUNCH, "no CTA pair of the pair kernel fits on this device");
-            grid_cap = std::max(2, std::min(grid_cap / 2, max_clusters) * 2);
+            // whole clusters of two
+            grid_cap = std::max(2, grid_cap / 2 * 2);
             choose_widths(plan, plan.n_beta / 2, Nk, grid_cap / 2, ctx->opt.storage == 1,
                           (int)ctx->opt.tile_n, (int)ctx->opt.tile_n2);
             plan.grid = 2 * (int)std::min<int64_t>(grid_cap / 2, (int64_t)(plan.n_beta / 2) * plan.n_chunk);
@@ -727,7 +788,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
                 // every raw-row entry is below the largest row norm 2^e and a
                 // sequence holds at most N rows: F = 62 - e - ceil(log2 N)
                 std::vector<float> h_nrm;
-                TRY(to_host(ctx->nrm.as<float>(), (size_t)N, h_nrm, st));
+                TRY(to_host(ctx->nrm.as<float>(), (size_t)N, h_nrm, st, "norms"));
                 float mx = 0.0f;
                 for (float v : h_nrm) mx = std::max(mx, v);
                 int e = 0;
@@ -753,6 +814,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         a.Dp = ctx->Dp;
         a.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
         a.fault_skip_arrive = (int)ctx->opt.fault_skip_arrive;
+        a.isolate_epilogue = (int)ctx->opt.isolate_epilogue;
         // the split table stays L2-resident across iterations only if it is a
         // small part of L2; larger tables stream through once per iteration
         a.keep_table = (double)Nk * eparts * ctx->Dp * sizeof(__half) <= info.l2 / 3.0 ? 1 : 0;
@@ -770,7 +832,16 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         CUDA_TRY(cudaGetLastError());
         ctx->state_plan = plan;
         TRY(timer.start(st));
-        CUDA_TRY(launch_tc_dseq(a, plan, tq, te, st));
+        {
+            const cudaError_t le = launch_tc_dseq(a, plan, tq, te, st);
+            if (le != cudaSuccess) {
+                cudaGetLastError();
+                ctx->has_state = false;
+                return fail(DSEQ_ELAUNCH,
+                            "cooperative launch of the persistent kernel (%d CTAs%s) refused: %s",
+                            plan.grid, pair ? " in clusters of two" : "", cudaGetErrorString(le));
+            }
+        }
         TRY(timer.stop(st));
         g_stats.units = plan.units();
         g_stats.tile_n = plan.tile_n;
@@ -818,7 +889,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             return rs;
         }
     }
-    ctx->has_state = true;
+    // an epilogue-isolated run leaves meaningless state: nothing to resume
+    ctx->has_state = ctx->opt.isolate_epilogue == 0;
     ctx->state_picks = done_before + L;
     ctx->state_sig = sig;
     ctx->state_starts = h_starts;
@@ -1043,7 +1115,9 @@ int som_core(SomArgs &a, const DeviceInfo &info, SomWorkspace *ws, cudaStream_t 
 
 // W as a device array: the pointer itself, or a staged copy of host data.
 int stage_mutable(float *W, size_t count, DevBuf &buf, float *&dev, bool &on_host, cudaStream_t st) {
-    on_host = !is_device_ptr(W);
+    bool on_device;
+    TRY(locate(W, "W", on_device));
+    on_host = !on_device;
     if (!on_host) {
         dev = W;
         return DSEQ_OK;
@@ -1073,9 +1147,11 @@ int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, 
     DeviceInfo info;
     TRY(device_info(dev, info));
     const float *dX, *dW;
-    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st));
-    TRY(stage_in(W, (size_t)M * D, ws->w_stage, dW, st));
-    const bool idx_dev = is_device_ptr(idx), dist_dev = is_device_ptr(dist);
+    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st, "X"));
+    TRY(stage_in(W, (size_t)M * D, ws->w_stage, dW, st, "W"));
+    bool idx_dev, dist_dev;
+    TRY(locate(idx, "idx", idx_dev));
+    TRY(locate(dist, "dist", dist_dev));
     int32_t *d_idx = idx;
     float *d_dist = dist;
     if (!idx_dev) {
@@ -1112,8 +1188,8 @@ int som_update(const float *X, int64_t n, float *W, int32_t side_x, int32_t side
     const int32_t *dB;
     float *dW;
     bool w_host;
-    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st));
-    TRY(stage_in(bmu, (size_t)n, ws->bmu_stage, dB, st));
+    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st, "X"));
+    TRY(stage_in(bmu, (size_t)n, ws->bmu_stage, dB, st, "bmu"));
     TRY(stage_mutable(W, (size_t)a.M * D, ws->w_stage, dW, w_host, st));
     a.X = dX;
     a.bmu = dB;
@@ -1147,10 +1223,11 @@ int som_epoch(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_
     const float *dX;
     float *dW;
     bool w_host;
-    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st));
+    TRY(stage_in(X, (size_t)n * D, ws->x_stage, dX, st, "X"));
     TRY(stage_mutable(W, (size_t)a.M * D, ws->w_stage, dW, w_host, st));
-    const bool idx_dev = bmu_out && is_device_ptr(bmu_out);
-    const bool dist_dev = dist_out && is_device_ptr(dist_out);
+    bool idx_dev = false, dist_dev = false;
+    if (bmu_out) TRY(locate(bmu_out, "bmu_out", idx_dev));
+    if (dist_out) TRY(locate(dist_out, "dist_out", dist_dev));
     int32_t *d_idx = bmu_out;
     float *d_dist = dist_out;
     if (!idx_dev) {

@@ -170,13 +170,19 @@ struct TcDseqArgs {
     int keep_table;  // 1: load table tiles with the evict-last L2 policy (table fits L2)
     // optional [L][grid][kTimelineSlots] globaltimer stamps (nullptr = off)
     unsigned long long *timeline;
+    // measurement only (max-min): run the epilogue-isolated kernel, whose
+    // contraction is compiled out (picks meaningless)
+    int isolate_epilogue;
 };
 void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *starts,
                          const uint8_t *mask, cudaStream_t st);
 cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st);
-// clusters of two that can be co-resident for the pair kernel (0 on error)
-int tc_dseq_pair_max_clusters(int tile_n);
+// CTAs of the persistent kernel variant (pair, fp16 storage, centroid) that
+// can be co-resident on the current device, from that instantiation's own
+// thread count and shared memory (pair: twice its co-resident clusters of
+// two); 0 on error
+int tc_dseq_max_grid(bool pair, bool f16, bool centroid);
 
 // ---- diversity, FFMA path (ffma.cu) -----------------------------------------
 struct FfmaDseqArgs {
@@ -247,7 +253,9 @@ cudaError_t launch_som_update(const SomArgs &a, int sms, cudaStream_t st);
 namespace host {
 int fail_msg(int code, const char *msg);
 void clear_error();
-bool is_device(const void *p);
+// on_device: p is device (or managed) memory of the current device; device
+// memory of another device is an error (DSEQ_EINVAL with a message)
+int locate_ptr(const void *p, const char *what, bool &on_device);
 int sm_count(int dev, int *sms);
 int encode_map(CUtensorMap &map, const void *base, int64_t cols, int64_t rows, int box_rows);
 int read_device_status(int *status_dev, cudaStream_t st);

@@ -63,10 +63,20 @@ extern "C" int bmu_search_noalloc(const float *X, int64_t n, const float *W, int
     if (n < 1 || n >= (int64_t(1) << 31) || M < 1 || M >= (int64_t(1) << 31))
         return host::fail_msg(DSEQ_EINVAL, "n or M out of range");
     if (D < 1 || D > 16384) return host::fail_msg(DSEQ_EINVAL, "D out of range");
-    if (!host::is_device(X) || !host::is_device(W) || !host::is_device(idx) ||
-        !host::is_device(dist))
-        return host::fail_msg(DSEQ_EINVAL,
-                              "bmu_search_noalloc needs X, W, idx and dist in device memory");
+    {
+        // all four on the current device (nothing can be staged); memory of
+        // another device is rejected with its own message
+        const void *ptrs[4] = {X, W, idx, dist};
+        const char *names[4] = {"X", "W", "idx", "dist"};
+        for (int i = 0; i < 4; ++i) {
+            bool on_device = false;
+            const int r = host::locate_ptr(ptrs[i], names[i], on_device);
+            if (r != DSEQ_OK) return r;
+            if (!on_device)
+                return host::fail_msg(DSEQ_EINVAL,
+                                      "bmu_search_noalloc needs X, W, idx and dist in device memory");
+        }
+    }
     const int Dp = (D + kKBlock - 1) / kKBlock * kKBlock;
     // scratch layout, every piece 256-byte aligned
     const size_t off_xs = 0;

@@ -238,7 +238,13 @@ __host__ __device__ constexpr int dseq_threads() {
     return kTcThreads + 32 * dseq_commit_warps<kCentroid>();
 }
 
-template <bool kPair, bool kF16, bool kCentroid>
+// kIsolate (max-min only; never chosen by the product path): the operand
+// loads and the MMAs are compiled out and the accumulator is replaced by a
+// distance that falls with every iteration, so that every running minimum
+// is read and rewritten; everything else (epilogue, commit, cross-CTA
+// counters) runs as in the real kernel.  It measures the fused epilogue's
+// running-minimum stream against HBM on its own; its picks are meaningless.
+template <bool kPair, bool kF16, bool kCentroid, bool kIsolate = false>
 __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     tc_dseq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_e, const TcDseqArgs a,
@@ -347,6 +353,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
     };
 
     uint32_t fills = 0;     // producer: stages filled so far
+    // epilogue-isolated kernel: this iteration's stand-in distance
+    float iso_d = 0.0f;
     uint32_t consumed = 0;  // MMA: stages consumed so far
     uint32_t acc_uses = 0;  // MMA and epilogue: accumulators used so far
 
@@ -417,6 +425,18 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         if (!timed_wait(a, &acc_empty[buf], apar ^ 1u, abort_flag, tmo, wait_acc))
             return false;
         tc_fence_after();
+        if (kIsolate) {
+            // no contraction: hand the (unwritten) accumulator straight to
+            // the epilogue warps of this CTA (and of the peer)
+            mbar_arrive(&acc_full[buf]);
+            if (kPair) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_full[buf]), 1));
+            if (first) {
+                stamp(a, t, 2);
+                first = false;
+            }
+            ++acc_uses;
+            return true;
+        }
         const uint32_t d_tmem = tmem_base + buf * kAccCols;
         bool ok = true;
         for (int kb0 = 0; kb0 < kblocks; kb0 += Cfg::kKbPerStage) {
@@ -590,8 +610,9 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
                 for (int z = 0; z < 4; ++z) {
                     // split storage: d = 1 - <q, e>, the accumulator holding
                     // 2^12 <q, e> of unit rows
-                    const float d = kF16 ? fmaf(acc[4 * v + z] * rn_g[4 * v + z], neg_rnq, 1.0f)
-                                         : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
+                    const float d = kIsolate ? iso_d
+                                    : kF16   ? fmaf(acc[4 * v + z] * rn_g[4 * v + z], neg_rnq, 1.0f)
+                                             : fmaf(acc[4 * v + z], -1.0f / 4096.0f, 1.0f);
                     const float nv = fminf(mv[z], d);
                     changed |= nv != mv[z];
                     mv[z] = nv;
@@ -838,7 +859,7 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
         const int64_t hb[3] = {0, half_units, work};
         if (warp == 0) {
             // ---------------- TMA producer ----------------
-            if (lane == 0) {
+            if (lane == 0 && !kIsolate) {
                 const uint64_t keep = l2_policy_evict_last();
                 const uint64_t table_pol = a.keep_table ? keep : l2_policy_evict_normal();
                 const uint64_t m_pol = l2_policy_evict_normal();
@@ -886,6 +907,8 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
             bool ok = true;
             for (int t = 0; t < a.L && ok; ++t) {
                 uint64_t epi_wait = 0;
+                // falls with every iteration: every running minimum moves
+                if (kIsolate) iso_d = 1.0f - (float)(t + 1) * (1.0f / 512.0f);
                 for (int h = 0; h < 2 && ok; ++h) {
                     if (t > 0) {
                         // keys reset and winners masked for half h (the running
@@ -963,6 +986,20 @@ __global__ void __launch_bounds__(dseq_threads<kCentroid>(), 1)
 
     // ---- teardown: drain what this CTA still has in flight, free TMEM ----
     __syncthreads();
+    if (warp == 0 && lane == 0 && !*abort_flag) {
+        // every stage this CTA filled has been consumed by the issuer; wait
+        // (bounded) for the commits that say so, so that no tensor-core
+        // arrival is still on its way to this CTA's barriers when it exits.
+        // A failure reported anywhere in the grid ends the wait at once.
+        const uint64_t lim = tmo < 1000000000ull ? tmo : 1000000000ull;
+        for (uint32_t s = 0; s < (uint32_t)kSt && s < fills; ++s) {
+            const uint32_t n_s = fills / kSt + (s < fills % kSt ? 1u : 0u);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&empty[s], (n_s - 1) & 1u)) {
+                if (ld_volatile(a.status) != 0 || globaltimer_ns() - t0 > lim) break;
+            }
+        }
+    }
     if (warp == 0 && lane == 0 && *abort_flag) {
         volatile int never = 0;
         if (kPair) {
@@ -1008,45 +1045,84 @@ void launch_tc_dseq_init_impl(const TcDseqArgs &a, const TcPlan &p, const int32_
     tc_dseq_init_kernel<<<2048, 256, 0, st>>>(a, p, starts, mask);
 }
 
-template <bool kPair, bool kF16, bool kCentroid>
+// Launch configuration of one instantiation: its thread count, its shared
+// memory, clusters of two for the pair kernels.
+template <bool kPair, bool kF16, bool kCentroid, bool kIsolate = false>
+cudaError_t configure_variant(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2],
+                              unsigned grid, cudaStream_t st) {
+    const size_t smem = DseqCfg<kPair, kF16, kCentroid>::kSmemBytes;
+    cudaError_t err = cudaFuncSetAttribute(tc_dseq_kernel<kPair, kF16, kCentroid, kIsolate>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(dseq_threads<kCentroid>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    int n = 0;
+    if (kPair) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaSuccess;
+}
+
+// The persistent kernel waits on counters that every CTA of the grid feeds,
+// so the grid must be co-resident: it is launched cooperatively (with
+// clusters of two for the pair kernels), and a launch the runtime refuses is
+// returned as an error, never retried in another form.
+template <bool kPair, bool kF16, bool kCentroid, bool kIsolate = false>
 cudaError_t launch_variant(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st) {
     TcDseqArgs aa = a;
     TcPlan pp = p;
     CUtensorMap mq = tmap_q, me = tmap_e;
-    const size_t smem = DseqCfg<kPair, kF16, kCentroid>::kSmemBytes;
-    auto kernel = tc_dseq_kernel<kPair, kF16, kCentroid>;
-    cudaError_t err =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    if (!kPair) {
-        void *args[] = {&mq, &me, &aa, &pp};
-        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kernel),
-                                           dim3((unsigned)p.grid), dim3(dseq_threads<kCentroid>()),
-                                           args, smem, st);
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3(dseq_threads<kCentroid>());
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
+    cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    err = cudaLaunchKernelEx(&cfg, kernel, mq, me, aa, pp);
-    if (err == cudaSuccess) return err;
-    // cooperative + cluster launch refused: launch the clusters plainly.  The
-    // caller sized the grid to the co-resident cluster count, and every grid
-    // barrier is time-bounded, so a non-resident grid fails with a timeout.
-    cudaGetLastError();
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, mq, me, aa, pp);
+    cudaError_t err =
+        configure_variant<kPair, kF16, kCentroid, kIsolate>(cfg, attr, (unsigned)p.grid, st);
+    if (err != cudaSuccess) return err;
+    attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+    attr[cfg.numAttrs].val.cooperative = 1;
+    ++cfg.numAttrs;
+    return cudaLaunchKernelEx(&cfg, tc_dseq_kernel<kPair, kF16, kCentroid, kIsolate>, mq, me, aa,
+                              pp);
+}
+
+// CTAs of this instantiation that can be resident at once on the current
+// device (pair kernels: whole clusters of two), from its own occupancy.
+template <bool kPair, bool kF16, bool kCentroid>
+int max_grid_variant() {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    if (configure_variant<kPair, kF16, kCentroid>(cfg, attr, kPair ? 2u : 1u, nullptr) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    auto kernel = tc_dseq_kernel<kPair, kF16, kCentroid>;
+    if (kPair) {
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return 2 * clusters;
+    }
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (int)cfg.blockDim.x,
+                                                      cfg.dynamicSmemBytes) != cudaSuccess ||
+        cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return per_sm * sms;
 }
 
 }  // namespace
@@ -1059,6 +1135,14 @@ void launch_tc_dseq_init(const TcDseqArgs &a, const TcPlan &p, const int32_t *st
 cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorMap &tmap_q,
                            const CUtensorMap &tmap_e, cudaStream_t st) {
     const bool f16 = a.e_f16 != nullptr;
+    if (a.isolate_epilogue) {
+        if (a.centroid) return cudaErrorInvalidValue;
+        if (p.pair)
+            return f16 ? launch_variant<true, true, false, true>(a, p, tmap_q, tmap_e, st)
+                       : launch_variant<true, false, false, true>(a, p, tmap_q, tmap_e, st);
+        return f16 ? launch_variant<false, true, false, true>(a, p, tmap_q, tmap_e, st)
+                   : launch_variant<false, false, false, true>(a, p, tmap_q, tmap_e, st);
+    }
     if (a.centroid) {
         if (p.pair)
             return f16 ? launch_variant<true, true, true>(a, p, tmap_q, tmap_e, st)
@@ -1073,31 +1157,13 @@ cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorM
                : launch_variant<false, false, false>(a, p, tmap_q, tmap_e, st);
 }
 
-int tc_dseq_pair_max_clusters(int tile_n) {
-    (void)tile_n;
-    const size_t smem = DseqCfg<true, false>::kSmemBytes;
-    if (cudaFuncSetAttribute(tc_dseq_kernel<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
+int tc_dseq_max_grid(bool pair, bool f16, bool centroid) {
+    if (centroid) {
+        if (pair) return f16 ? max_grid_variant<true, true, true>() : max_grid_variant<true, false, true>();
+        return f16 ? max_grid_variant<false, true, true>() : max_grid_variant<false, false, true>();
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(dseq_threads<false>());
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_dseq_kernel<true, false, false>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return n;
+    if (pair) return f16 ? max_grid_variant<true, true, false>() : max_grid_variant<true, false, false>();
+    return f16 ? max_grid_variant<false, true, false>() : max_grid_variant<false, false, false>();
 }
 
 }  // namespace dseq

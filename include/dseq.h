@@ -9,7 +9,8 @@
  *    computes the cosine distance of that pick to all N candidate rows,
  *    folds it into the sequence's running minimum distance, and picks the
  *    unmasked candidate whose running minimum is largest, lowest index on
- *    ties (the max-min, farthest-first reading of the issue's criterion).  The
+ *    ties (the max-min, farthest-first reading of the criterion of "Issue
+ *    9-014: Tile Diversity Shader Inner Loop For L2 Cache Locality").  The
  *    candidate scan is tiled and the running (max, index) carried across
  *    tiles, which by associativity of max gives the one-pass winner (same
  *    issue, Intended Behavior).
@@ -27,7 +28,9 @@
  *  - Array arguments may be host or device pointers (the library inspects
  *    each with cudaPointerGetAttributes); host arrays are staged through
  *    library-owned device buffers on the given stream.  Pinned host memory
- *    makes those copies asynchronous.
+ *    makes those copies asynchronous.  Device arrays must be memory of the
+ *    current device: a pointer into another GPU's memory is rejected with
+ *    DSEQ_EINVAL before any work is enqueued.
  *  - cuda_stream is a cudaStream_t (NULL = the legacy default stream) on the
  *    current device.  Every call is synchronous at return: it enqueues its
  *    work on the stream, synchronizes the stream and reads back the device
@@ -52,7 +55,7 @@ enum {
     DSEQ_EINVAL = -1,     /* NULL pointer, bad size, start out of range or repeated, L too large */
     DSEQ_ENONFINITE = -2, /* NaN / Inf in an input table, or an all-zero table row */
     DSEQ_ENOMEM = -3,     /* device allocation failed */
-    DSEQ_ELAUNCH = -4,    /* the persistent grid could not be made co-resident */
+    DSEQ_ELAUNCH = -4,    /* the runtime refused the persistent grid's cooperative launch */
     DSEQ_ETIMEOUT = -5,   /* a device-side wait gave up (the kernel returned cleanly) */
     DSEQ_ECUDA = -6,      /* any other CUDA runtime / driver error */
     DSEQ_EINTERNAL = -7   /* an internal consistency check failed on the device */
@@ -160,8 +163,11 @@ int bmu_search(const float *X, int64_t n, const float *W, int64_t M, int32_t D, 
  *   bmu     int32[n], every sample's neuron in [0, M); host or device.
  *   sigma   >= 0; radius in [0, 255] and, for sigma > 0, radius <= 9 sigma
  *           (wider windows would take weights below fp32's normal range).
- * Sums over samples are taken in double, the smoothing and the division in
- * fp32.  n = 0 leaves W unchanged.  On any error W is left unchanged.
+ * Sums over samples are exact: each sample is converted to 64-bit integer
+ * fixed point (a scale set by the largest |x|) and the sums are integer
+ * additions, so the result does not depend on the order in which samples
+ * are added; the smoothing and the division are fp32.  n = 0 leaves W
+ * unchanged.  On any error W is left unchanged.
  * Errors: DSEQ_EINVAL (sizes, sigma, radius, a BMU out of range),
  * DSEQ_ENONFINITE (NaN/Inf in X), DSEQ_ENOMEM, DSEQ_ECUDA. */
 int som_update(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_y, int32_t D,
@@ -179,13 +185,15 @@ int som_epoch(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_
               double sigma, int32_t radius, int32_t *bmu_out, float *dist_out,
               void *cuda_stream);
 
-/* bmu_search for callers that cannot allocate device memory: a framework
- * whose pooling allocator already holds nearly all of the GPU's memory, or a
- * latency-critical loop that cannot absorb the device-wide synchronisation
+/* bmu_search for callers that cannot allocate device memory: code inside a
+ * framework whose pooling allocator already holds nearly all of the GPU's
+ * memory (a cudaMalloc there fails, or takes memory the pool counts on), or
+ * a latency-critical loop that cannot absorb the device-wide synchronisation
  * cudaMalloc / cudaFree may imply.  The method pages have no counterpart of
  * this entry point; it exists for such callers only.
  * Same arguments, semantics and results as bmu_search, except:
- *  - X, W, idx and dist must all be device memory (nothing is staged);
+ *  - X, W, idx and dist must all be device memory of the current device
+ *    (nothing is staged; memory of another device is rejected);
  *  - no call allocates: the scratch (split operands, norms, scales, keys,
  *    status) lives in one fixed 64 MiB array inside the library, which every
  *    GPU that loads the library holds until the process exits.  A request
@@ -194,14 +202,19 @@ int som_epoch(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_
  *  - every call shares that one array, so calls whose GPU work overlaps
  *    (other threads, other streams) race and give wrong results: serialise
  *    them.  Each call resets the parts that must start from a known value;
- *  - the first call on a device looks up the array's device address (once per
- *    device, with that device current), so make that first call before any
- *    stream capture;
+ *  - set-up: the first call on a device looks up the array's device address
+ *    (once per device, with that device current) and keeps it for the rest
+ *    of the process; make that first call before any stream capture.  The
+ *    kept address is not valid after cudaDeviceReset on that device: do not
+ *    call this entry point on a device after resetting it;
+ *  - every call enqueues its kernels on cuda_stream, synchronises that
+ *    stream and reads the device status word back to the host before it
+ *    returns;
  *  - the process-wide "engine", "tile_n", "grid" and "timeout_ms" options do
  *    not apply: the tensor-core path always runs on CTA pairs, 256 neurons
  *    per unit, one CTA per SM, 10 s wait limit.
- * Errors: DSEQ_EINVAL (as bmu_search, host pointers, scratch too small),
- * DSEQ_ENONFINITE, DSEQ_ETIMEOUT, DSEQ_ECUDA. */
+ * Errors: DSEQ_EINVAL (as bmu_search, host pointers or memory of another
+ * device, scratch too small), DSEQ_ENONFINITE, DSEQ_ETIMEOUT, DSEQ_ECUDA. */
 int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int32_t D,
                        int32_t *idx, float *dist, void *cuda_stream);
 
@@ -216,7 +229,11 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 the tile_n-wide ones (a multiple of 32, <= tile_n); 0 =
  *                 chosen with tile_n (default).  Mixing two widths balances
  *                 the work units over the SMs without narrowing every MMA.
- *   "grid"        persistent CTAs; 0 = one per SM (default).
+ *   "grid"        persistent CTAs; 0 = as many as can be co-resident for the
+ *                 kernel variant that runs (its own occupancy; one per SM
+ *                 for the tensor-core kernels) (default).  A diversity grid
+ *                 larger than can be co-resident is refused by the
+ *                 cooperative launch: dseq_run returns DSEQ_ELAUNCH.
  *   "timeout_ms"  limit of every device-side wait (default 10000).
  *   "resume"      1 = dseq_run continues the last successful run on this
  *                 context from the state it left on the device (running
@@ -230,8 +247,10 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *   "criterion"   0 = max-min (default): a candidate's score is its smallest
  *                 cosine distance to any row the sequence holds; 1 = centroid:
  *                 its cosine distance to the centroid (plain mean) of those
- *                 rows, a zero centroid giving distance 1 (the issue's
- *                 centroid ranking in its FP16 storage section).  With 1,
+ *                 rows, a zero centroid giving distance 1 (the ranking by
+ *                 distance from the centroid in "Issue 9-014: Tile
+ *                 Diversity Shader Inner Loop For L2 Cache Locality",
+ *                 section FP16 storage (compounding optimization)).  With 1,
  *                 dseq_run_trace records these centroid distances instead
  *                 of running minima.  Tensor-core engine only (DSEQ_EINVAL
  *                 with engine 1); with storage 1 the table is held as fp16
@@ -267,6 +286,15 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 kernels leave out one copy of its first codebook stage, so
  *                 that stage never fills and the waits on it run out
  *                 (bmu_search then returns DSEQ_ETIMEOUT without hanging).
+ *   "isolate_epilogue"   measurement only: 1 makes dseq_run launch the
+ *                 max-min tensor-core kernel with its contraction compiled
+ *                 out (no operand copies, no MMAs) and a stand-in distance
+ *                 that falls every iteration, so that the fused epilogue's
+ *                 running-minimum stream, the commit and the cross-CTA
+ *                 synchronisation run alone; its picks are meaningless.
+ *   The three test options accept a non-zero value only when the
+ *   environment variable DSEQ_ENABLE_TEST_OPTIONS is "1" (DSEQ_EINVAL
+ *   otherwise); 0 is always accepted.
  * Errors: DSEQ_EINVAL for an unknown name or a value out of range. */
 int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value);
 

@@ -3,6 +3,10 @@ import sys
 
 import pytest
 
+# the fault-injection tests set the library's test options, which a process
+# must opt in to
+os.environ.setdefault("DSEQ_ENABLE_TEST_OPTIONS", "1")
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

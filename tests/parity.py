@@ -121,7 +121,11 @@ def check_picks_valid(starts, mask, picks, N):
 
 
 def check_bmu(X, W, sample, idx_gpu, dist_gpu, threads=0):
-    """Check the GPU result on the given sample rows; returns (n_exact, n_ties)."""
+    """Check the GPU result on the given sample rows.  Returns counts: the
+    samples checked, those whose GPU index equals the oracle's, those whose
+    oracle top-2 gap falls inside the near-tie band as read here (relative to
+    max(d_min, |x|^2 + |w|^2)) and inside the narrower band relative to d_min
+    alone, and the samples accepted only because of the wider reading."""
     X = np.ascontiguousarray(X, np.float32)
     W = np.ascontiguousarray(W, np.float32)
     sample = np.asarray(sample, np.int64)
@@ -146,4 +150,8 @@ def check_bmu(X, W, sample, idx_gpu, dist_gpu, threads=0):
     worst = int(np.argmax(derr / dtol))
     assert np.all(derr <= dtol), (f"BMU distance off by {derr[worst]} (tol {dtol[worst]}) at "
                                   f"sample {sample[worst]}")
-    return int(exact.sum()), int((~exact).sum())
+    narrow = (second - do) <= TOL * do
+    narrow_ok = exact | (narrow & (d_at_g <= do * (1.0 + TOL)))
+    return {"checked": int(sample.size), "exact": int(exact.sum()),
+            "in_band": int(near_tie.sum()), "in_narrow_band": int(narrow.sum()),
+            "accepted_only_by_wide_band": int((~narrow_ok).sum())}

@@ -88,6 +88,27 @@ def test_options(lib):
     assert es.dseq_last_stat("units") == 0 and es.dseq_last_stat("bogus") == -1
 
 
+def test_test_options_need_opt_in(lib, monkeypatch):
+    """Options that change results on purpose (fault injection, the
+    epilogue-isolated kernel) are refused unless the process opts in through
+    DSEQ_ENABLE_TEST_OPTIONS=1; setting them back to 0 is always allowed."""
+    names = ("isolate_epilogue", "fault_skip_arrive", "fault_skip_copy")
+    monkeypatch.delenv("DSEQ_ENABLE_TEST_OPTIONS", raising=False)
+    for name in names:
+        with pytest.raises(es.DseqError) as ei:
+            es.dseq_set_option(name, 1)
+        assert ei.value.code == es.DSEQ_EINVAL and "DSEQ_ENABLE_TEST_OPTIONS" in str(ei.value)
+        es.dseq_set_option(name, 0)
+        assert es.dseq_get_option(name) == 0
+    monkeypatch.setenv("DSEQ_ENABLE_TEST_OPTIONS", "1")
+    for name in names:
+        es.dseq_set_option(name, 1)
+        assert es.dseq_get_option(name) == 1
+        es.dseq_set_option(name, 0)
+    with pytest.raises(es.DseqError):
+        es.dseq_set_option("isolate_epilogue", 2)
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         es.load(str(tmp_path / "libdseq.so"))

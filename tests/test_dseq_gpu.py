@@ -33,7 +33,7 @@ def _reset_options(es):
     yield
     for name, v in (("engine", 0), ("tile_n", 0), ("tile_n2", 0), ("grid", 0), ("timeout_ms", 10000),
                     ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR), ("storage", 0),
-                    ("criterion", 0), ("resume", 0), ("compact", 1)):
+                    ("criterion", 0), ("resume", 0), ("compact", 1), ("isolate_epilogue", 0)):
         es.dseq_set_option(name, v)
 
 
@@ -262,6 +262,53 @@ def test_barrier_timeout_returns_cleanly(es, criterion, pair):
     assert np.array_equal(again, ref)
 
 
+@pytest.mark.parametrize("pair,criterion,storage", [(1, 0, 0), (0, 0, 0), (1, 1, 0), (1, 0, 1)])
+def test_oversized_grid_returns_elaunch(es, pair, criterion, storage):
+    """A "grid" option beyond the CTAs that can be co-resident: the runtime
+    refuses the cooperative launch, the call returns DSEQ_ELAUNCH with the
+    refusal's message and launches nothing in another form, and the next call
+    with the default grid (sized from the launched variant's own occupancy)
+    gives the same picks as before."""
+    N, D, B, L = 20000, 64, 1024, 2
+    E = workloads.gaussian_table(N, D, seed=8)
+    starts = workloads.starts(N, B, seed=8)
+    # 32-wide chunks: 625 chunks x 8 sequence blocks, more units than the grid
+    kw = dict(pair=pair, criterion=criterion, storage=storage, tile_n=32)
+    ref, _ = _run(es, E, starts, L, **kw)
+    grid = es.dseq_last_stat("grid")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 0 < grid <= sms and (grid % 2 == 0 or not pair)
+    with pytest.raises(es.DseqError) as ei:
+        _run(es, E, starts, L, grid=1000, **kw)
+    assert ei.value.code == es.DSEQ_ELAUNCH
+    assert "refused" in str(ei.value)
+    again, _ = _run(es, E, starts, L, grid=0, **kw)
+    assert np.array_equal(again, ref)
+
+
+@pytest.mark.parametrize("pair,storage", [(1, 0), (0, 0), (1, 1), (0, 1)])
+def test_isolated_epilogue_runs_epilogue_and_commit(es, pair, storage):
+    """The epilogue-isolated kernel (contraction compiled out, a distance that
+    falls every iteration and is equal for every candidate) still folds,
+    reduces and commits: every candidate ties each iteration, so every
+    sequence picks the lowest candidates in order, skipping its start and the
+    masked rows.  Results of the real kernel are unaffected afterwards."""
+    N, D, B, L = 3000, 64, 300, 12
+    E = workloads.gaussian_table(N, D, seed=12)
+    starts = workloads.starts(N, B, seed=12)
+    mask = np.zeros(N, np.uint8)
+    mask[[1, 4, 9]] = 1
+    ref, _ = _run(es, E, starts, L, mask, pair=pair, storage=storage)
+    es.dseq_set_option("isolate_epilogue", 1)
+    got, _ = _run(es, E, starts, L, mask, pair=pair, storage=storage)
+    es.dseq_set_option("isolate_epilogue", 0)
+    for b in range(B):
+        want = [c for c in range(N) if not mask[c] and c != starts[b]][:L]
+        assert got[b].tolist() == want, f"sequence {b}"
+    again, _ = _run(es, E, starts, L, mask, pair=pair, storage=storage)
+    assert np.array_equal(again, ref)
+
+
 FULL = ["page1", "d384", "d1024", "scale"]
 
 
@@ -383,8 +430,10 @@ def test_centroid_rejects_ffma(es):
         _run(es, E, np.array([0], np.int32), 3, engine=1, criterion=1)
 
 
-# the centroid criterion on fp16 table storage (the issue's FP16 storage
-# section ranks by the centroid): the table is held as fp16 rows, the
+# the centroid criterion on fp16 table storage ("Issue 9-014: Tile Diversity
+# Shader Inner Loop For L2 Cache Locality", section FP16 storage (compounding
+# optimization), ranks candidates by their distance from the centroid): the
+# table is held as fp16 rows, the
 # centroid query keeps fp32-level precision, so on tables of fp16 numbers the
 # distances are the oracle's exact cosine distances to the centroid.
 

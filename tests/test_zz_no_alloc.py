@@ -75,7 +75,8 @@ def _agree(X, W, got, ref):
 
 
 def test_noalloc_matches_bmu_search_on_two_calls_in_a_row(lib):
-    cases = [(3000, 5000, 96, 1), (1700, 9000, 200, 2)]
+    # D <= 256 runs the resident-sample kernel, D = 300 the streaming one
+    cases = [(3000, 5000, 96, 1), (1700, 9000, 200, 2), (1000, 2000, 300, 3)]
     inputs = []
     for n, M, D, seed in cases:
         X = torch.from_numpy(workloads.bmu_samples(n, D, seed=seed)).cuda()
@@ -89,6 +90,43 @@ def test_noalloc_matches_bmu_search_on_two_calls_in_a_row(lib):
         _agree(X, W, got, ref)
         # the same kernels on the same split operands: the same bits
         assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+
+
+def test_warmed_call_allocates_nothing(lib):
+    """After a first call (the one-time set-up), a call leaves the device's
+    free memory and torch's allocator exactly as they were."""
+    X = torch.from_numpy(workloads.bmu_samples(2000, 128, seed=4)).cuda()
+    W = torch.from_numpy(workloads.codebook(3000, 128, seed=4)).cuda()
+    first = _call_noalloc(lib, X, W)
+    idx = torch.empty((X.shape[0],), dtype=torch.int32, device="cuda")
+    dist = torch.empty((X.shape[0],), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = lib.bmu_search_noalloc(X.data_ptr(), X.shape[0], W.data_ptr(), W.shape[0], X.shape[1],
+                                idx.data_ptr(), dist.data_ptr(), ctypes.c_void_p(stream))
+    assert rc == 0, lib.dseq_last_error().decode()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.equal(idx, first[0]) and torch.equal(dist, first[1])
+
+
+def test_noalloc_rejects_memory_of_another_device(lib):
+    """Inputs on a GPU other than the current one are rejected before any
+    work is enqueued (needs two GPUs)."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("one GPU: no memory of another device to pass")
+    X = torch.zeros((4, 8), dtype=torch.float32, device="cuda:1")
+    W = torch.ones((6, 8), dtype=torch.float32, device="cuda:0")
+    idx = torch.empty(4, dtype=torch.int32, device="cuda:0")
+    dist = torch.empty(4, dtype=torch.float32, device="cuda:0")
+    with torch.cuda.device(0):
+        rc = lib.bmu_search_noalloc(X.data_ptr(), 4, W.data_ptr(), 6, 8, idx.data_ptr(),
+                                    dist.data_ptr(), None)
+    assert rc == -1 and "device 1" in lib.dseq_last_error().decode()
 
 
 def test_noalloc_rejects_what_it_cannot_serve(lib):

@@ -131,12 +131,12 @@ DIVERSITY = {
     "d1024": DiversityConfig("dim sweep N=8359 D=1024 B=3584 L=256", 8359, 1024, 3584, 256,
                              "clustered", 64),
     "scale": DiversityConfig("scale-up N=131072 D=768 B=8192 L=128", 131072, 768, 8192, 128,
-                             "clustered", 8),
+                             "clustered", 64),
 }
 
 BMU = {
     "som256": BMUConfig("SOM 256x256 M=65536 n=131072 D=256", 131072, 65536, 256, 4096),
-    "som512": BMUConfig("SOM 512x512 M=262144 n=262144 D=256", 262144, 262144, 256, 1024),
+    "som512": BMUConfig("SOM 512x512 M=262144 n=262144 D=256", 262144, 262144, 256, 4096),
 }
 
 
