@@ -388,7 +388,8 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
 
         def step():
             es.dseq_run(ctx, starts_dev, cfg.L, picks=picks_dev)
-            return es.dseq_last_stat("kernel_ns"), es.dseq_last_stat("launches")
+            return {k: es.dseq_last_stat(k)
+                    for k in ("kernel_ns", "launches", "gram", "gram_ns", "walk_ns")}
 
         def e2e_step():
             picks_host = torch.empty((cfg.B, cfg.L), dtype=torch.int32).pin_memory()
@@ -422,7 +423,7 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
             # each step is the next epoch of training on the same map
             es.som_epoch(X_dev, W_dev, sx, sy, sigma, radius, bmu=idx_dev, dist=dist_dev)
             update_ns.append(es.dseq_last_stat("update_ns"))
-            return es.dseq_last_stat("kernel_ns"), es.dseq_last_stat("launches")
+            return {k: es.dseq_last_stat(k) for k in ("kernel_ns", "launches")}
 
         def e2e_step():
             W_h = W_host.clone().pin_memory()
@@ -452,7 +453,7 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
 
     def step():
         es.bmu_search(X_dev, W_dev, idx=idx_dev, dist=dist_dev)
-        return es.dseq_last_stat("kernel_ns"), es.dseq_last_stat("launches")
+        return {k: es.dseq_last_stat(k) for k in ("kernel_ns", "launches")}
 
     def e2e_step():
         idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
@@ -499,15 +500,13 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
     wl.update_ns.clear()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    kernel_ns, launches = [], 0
+    stats = []
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
         for i in range(args.steps):
             ev[i][0].record(stream)
-            kns, nl = wl.step()
+            stats.append(wl.step())
             ev[i][1].record(stream)
-            kernel_ns.append(kns)
-            launches += nl
             flush.zero_()
         barrier()
         t_wall = time.perf_counter() - t_wall
@@ -534,7 +533,10 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
         e2e_s = float(t.item())
     e2e_value = ws * wl.units * e2e_steps / e2e_s
 
+    kernel_ns = [st["kernel_ns"] for st in stats]
+    launches = sum(st["launches"] for st in stats)
     k_avg_s = statistics.mean(kernel_ns) / 1e9 if kernel_ns and min(kernel_ns) > 0 else None
+    gram = bool(stats) and all(st.get("gram", 0) == 1 for st in stats)
     achieved = wl.flop / k_avg_s / 1e12 if k_avg_s else None
     clocks = clk.summary()
     # a run held at the power cap is compared with the sustained tensor peak
@@ -595,6 +597,33 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
                          "tensor_frac": None if isolate else roof["frac"],
                          "note": (f"achieved = {wl.stream_note} / kernel time; peak = "
                                   f"{peak_src} copy bandwidth {hbm_peak:.1f} GB/s")})
+    gram_product = None
+    if gram:
+        # the Gram engine: the walk streams one row of G per sequence-iteration
+        # (plus the running minima when a row of them does not fit shared
+        # memory); the Gram product is tensor-bound and reported beside it
+        cfg = wl.cfg
+        np_ = (cfg.N + 31) // 32 * 32
+        m_global = np_ * 4 > GRAM_WALK_SMEM_MAX
+        walk_bytes = cfg.B * cfg.L * cfg.N * (4.0 + (8.0 if m_global else 0.0))
+        walk_s = statistics.mean(st["walk_ns"] for st in stats) / 1e9
+        gram_s = statistics.mean(st["gram_ns"] for st in stats) / 1e9
+        gflop = 2.0 * cfg.N * cfg.N * cfg.D
+        roof = {"bound": "hbm", "achieved": walk_bytes / walk_s / 1e9, "peak": hbm_peak,
+                "unit": "GB/s", "frac": walk_bytes / walk_s / 1e9 / hbm_peak, "peak_kind": "copy",
+                "traffic": None if shrunk else _profiled_traffic("gram_walk_kernel", wl.name),
+                "kernel": "gram_walk_kernel",
+                "note": (f"achieved = algorithmic bytes of the walk (one row of G, 4*N bytes, per "
+                         f"sequence-iteration{' + the running minima read and written, 8*N' if m_global else ''})"
+                         f" / walk kernel time (CUDA events); peak = {peak_src} copy bandwidth "
+                         f"{hbm_peak:.1f} GB/s")}
+        gram_product = {"bound": "tensor", "achieved": gflop / gram_s / 1e12, "peak": tensor_peak,
+                        "unit": "TFLOP/s", "frac": gflop / gram_s / 1e12 / tensor_peak,
+                        "peak_kind": peak_kind, "frac_of_burst": gflop / gram_s / 1e12 / burst_peak,
+                        "ms": gram_s * 1e3, "share_of_step": gram_s * 1e3 / (total_ms / args.steps),
+                        "kernel": "tc_bmu_kernel (Gram store epilogue)",
+                        "note": ("achieved = 2*N*N*D / time of the operand split and the Gram "
+                                 f"product (CUDA events); {peak_note}")}
     line = {
         "metric": wl.metric, "value": value, "unit": wl.unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -608,7 +637,11 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
         "gpu_launches": int(launches), "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
-    if wl.stream_bytes is not None and k_avg_s:
+    if gram_product is not None:
+        line["engine"] = "gram"
+        line["gram_product"] = gram_product
+        line["dtype"] = "fp16x3-split Gram product (fp32-accurate), f32 walk"
+    if wl.stream_bytes is not None and k_avg_s and not gram:
         line["min_distance_stream"] = {
             "achieved_gbs": wl.stream_bytes / k_avg_s / 1e9, "peak_gbs": hbm_peak,
             "frac": wl.stream_bytes / k_avg_s / 1e9 / hbm_peak,
@@ -627,6 +660,9 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
 
 # the BMU half of the metric, measured beside the default diversity line
 BMU_BESIDE = "som256"
+# the running-minimum row the Gram walk keeps in shared memory (bytes), as
+# the library's limit
+GRAM_WALK_SMEM_MAX = 96 * 1024
 
 
 def run_ours(args):
@@ -657,13 +693,27 @@ def run_ours(args):
     wl = _workload(args, args.workload, es, dev, rank, opts)
     line = _measure(args, wl, opts, dev, local, pg, ws, flush)
     wl.close()
+    default_line = not opts and args.workload == "page1" and args.iters == 0
+    if default_line and line.get("engine") == "gram" and args.with_scan:
+        # the per-iteration contraction kernel on the same workload, timed in
+        # the same run (the library picks the Gram engine for this shape)
+        es.dseq_set_option("gram", 0)
+        sw = _workload(args, args.workload, es, dev, rank, opts)
+        sc = _measure(args, sw, opts, dev, local, pg, ws, flush)
+        sw.close()
+        es.dseq_set_option("gram", 2)
+        keep = ("value", "unit", "ms_per_step", "dtype", "roofline", "min_distance_stream",
+                "gpu_launches", "clocks", "wall_s_timed_region")
+        line["scan"] = {k: sc[k] for k in keep if k in sc}
+        line["scan"]["note"] = ("the per-iteration contraction kernel (option gram=0) on the "
+                                "same workload and sequences")
     with_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
     if with_cpu and "isolate_epilogue=1" not in opts:
         line["cpu_baseline"] = _cpu_baseline(args, wl.cfg, wl.epoch_of)
     # the default line also carries the BMU half of the metric: the SOM
     # 256 x 256 search timed in the same run, with its own roofline and CPU
     # baseline
-    if args.with_bmu and not opts and args.workload == "page1" and args.iters == 0:
+    if args.with_bmu and default_line:
         bw = _workload(args, BMU_BESIDE, es, dev, rank, opts)
         b = _measure(args, bw, opts, dev, local, pg, ws, flush)
         bw.close()
@@ -699,6 +749,9 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=0)
     ap.add_argument("--opt", action="append", default=[],
                     help="library option name=value, e.g. storage=1 (process-wide)")
+    ap.add_argument("--no-scan", dest="with_scan", action="store_false",
+                    help="leave out the per-iteration kernel's measurement that the default "
+                         "page-1 line carries beside the Gram engine's")
     ap.add_argument("--no-bmu", dest="with_bmu", action="store_false",
                     help="leave out the BMU search (som256) that the default page-1 line "
                          "carries beside the diversity number")

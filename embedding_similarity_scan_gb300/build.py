@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdseq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["api.cu", "prep.cu", "ffma.cu", "tc_dseq.cu", "tc_bmu.cu", "noalloc.cu", "som.cu"]
+SOURCES = ["api.cu", "prep.cu", "ffma.cu", "tc_dseq.cu", "tc_bmu.cu", "gram.cu", "noalloc.cu",
+           "som.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE, "-I" + CSRC]

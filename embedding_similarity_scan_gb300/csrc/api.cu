@@ -26,7 +26,7 @@ constexpr int kNoShift = 1 << 30;
 
 struct Stats {
     int64_t units = 0, tile_n = 0, tile_n2 = 0, n_wide = 0, grid = 0, launches = 0, kernel_ns = 0,
-            update_ns = 0;
+            update_ns = 0, gram = 0, gram_ns = 0, walk_ns = 0;
 };
 thread_local Stats g_stats;
 
@@ -81,6 +81,7 @@ struct Options {
     int64_t slice = 0;
     int64_t compact = 1;
     int64_t isolate_epilogue = 0;
+    int64_t gram = 2;
 };
 
 // Test and measurement options (fault injection, the epilogue-isolated
@@ -139,6 +140,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "compact") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "compact must be 0 or 1");
         o.compact = v;
+    } else if (n == "gram") {
+        if (v < 0 || v > 2) return fail(DSEQ_EINVAL, "gram must be 0 (never), 1 (always) or 2 (auto)");
+        o.gram = v;
     } else if (n == "slice") {
         if (v < 0 || v > (int64_t(1) << 24)) return fail(DSEQ_EINVAL, "slice out of range");
         o.slice = v;
@@ -166,6 +170,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "criterion") return o.criterion;
     if (n == "resume") return o.resume;
     if (n == "isolate_epilogue") return o.isolate_epilogue;
+    if (n == "gram") return o.gram;
     return -1;
 }
 
@@ -460,6 +465,9 @@ struct dseq_ctx {
     DevBuf m, held, keys, q, q_rn, csum, c_exp, status, barrier, starts, mask, picks, trace_slot, timeline;
     // global-mask compaction: the unmasked rows' tables and the index maps
     DevBuf col_map, comp_of, e_split_c, e_f16_c, rn_c;
+    // Gram engine: G (N x Np), the table split twice for the Gram product,
+    // the sequences' newest rows
+    DevBuf gram, g_xs, g_ws, g_xn, g_wn, g_xi, g_wi, g_cur;
     int64_t timeline_iters = 0, timeline_grid = 0;
     int csum_shift = kNoShift;  // fixed-point scale of the centroid sums, set on first use
     // state left on the device by the last successful run, for "resume"
@@ -467,13 +475,15 @@ struct dseq_ctx {
     int64_t state_picks = 0;  // picks per sequence made so far
     int64_t state_sig = -1;   // engine / pair / storage / criterion of that run
     TcPlan state_plan{};
+    bool state_gram = false;  // the last run used the Gram engine
     std::vector<int32_t> state_starts;
     std::vector<uint8_t> state_mask;
     ~dseq_ctx() {
         DevBuf *all[] = {&e_unit, &e_split, &e_f16,  &rn,      &nrm,    &m,
                          &held,   &keys,    &q,      &q_rn,    &csum,   &c_exp,  &status, &barrier,
                          &starts, &mask,    &picks,  &trace_slot, &timeline,
-                         &col_map, &comp_of, &e_split_c, &e_f16_c, &rn_c};
+                         &col_map, &comp_of, &e_split_c, &e_f16_c, &rn_c,
+                         &gram, &g_xs, &g_ws, &g_xn, &g_wn, &g_xi, &g_wi, &g_cur};
         for (DevBuf *b : all) b->release();
     }
 };
@@ -493,6 +503,9 @@ int64_t dseq_last_stat(const char *name) {
     if (n == "launches") return g_stats.launches;
     if (n == "kernel_ns") return g_stats.kernel_ns;
     if (n == "update_ns") return g_stats.update_ns;
+    if (n == "gram") return g_stats.gram;
+    if (n == "gram_ns") return g_stats.gram_ns;
+    if (n == "walk_ns") return g_stats.walk_ns;
     return -1;
 }
 
@@ -579,6 +592,25 @@ int dseq_get_timeline(dseq_ctx *ctx, int64_t *out, int64_t capacity, int32_t *it
     if (capacity < n) return fail(DSEQ_EINVAL, "timeline needs %lld slots", (long long)n);
     CUDA_TRY(cudaMemcpy(out, ctx->timeline.p, (size_t)n * sizeof(int64_t), cudaMemcpyDeviceToHost));
     return DSEQ_OK;
+}
+
+// Whether the Gram engine is expected to beat the per-iteration contraction
+// for this run, and fits in free_bytes of device memory.  The estimate
+// takes the split contraction at about 500 TFLOP/s (fp32-equivalent) and
+// HBM at about 5.5 TB/s: the Gram product costs 2 N^2 D, the walk one row
+// of G per sequence-iteration (and the running minima when a row of them
+// does not fit shared memory), the scan 2 B N D per iteration.
+static bool gram_pays(int64_t N, int64_t Dp, int64_t B, int64_t L, size_t free_bytes) {
+    const int64_t Np = round_up(N, 32);
+    const double need = (double)N * Np * 4.0 + (double)N * 5.0 * Dp * 2.0 + (double)B * Np * 4.0 +
+                        (256.0 * 1024 * 1024);
+    if (need > 0.8 * (double)free_bytes) return false;
+    const double rt = 5.0e14, rb = 5.5e12;
+    const bool smem = (size_t)Np * sizeof(float) <= kGramWalkSmemMax;
+    const double t_gram = 2.0 * N * Np * Dp / rt + N * Np * 4.0 / rb +
+                          (double)L * B * Np * 4.0 * (smem ? 1.0 : 2.2) / rb + 3.0e-5;
+    const double t_scan = 2.0 * B * N * Dp * (double)L / rt;
+    return t_gram < 0.9 * t_scan;
 }
 
 static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
@@ -685,7 +717,106 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     TRY(device_info(ctx->device, info));
     EventTimer timer;
 
-    if (ctx->opt.engine == 0) {
+    // the Gram engine (max-min on split storage) when it pays, or when asked;
+    // a resumed run continues on the engine of the run it resumes
+    bool use_gram = false;
+    if (resume) {
+        use_gram = ctx->state_gram;
+    } else if (ctx->opt.engine == 0 && ctx->opt.criterion == 0 && ctx->opt.storage == 0 &&
+               ctx->opt.isolate_epilogue == 0 && ctx->opt.timeline == 0 && ctx->opt.gram != 0) {
+        if (ctx->opt.gram == 1) {
+            use_gram = true;
+        } else {
+            size_t free_b = 0, total_b = 0;
+            if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
+                cudaGetLastError();
+                free_b = 0;
+            }
+            use_gram = gram_pays(N, ctx->Dp, B, L, free_b);
+        }
+    }
+
+    if (use_gram) {
+        // ---- Gram engine: G = E E^T on the tensor cores, then the walk ----
+        const int64_t Np = round_up(N, 32);
+        const int Dp = ctx->Dp;
+        TRY(ctx->gram.ensure((size_t)N * Np * sizeof(float)));
+        TRY(ctx->g_xs.ensure((size_t)N * kBmuPartsX * Dp * sizeof(__half)));
+        TRY(ctx->g_ws.ensure((size_t)N * kBmuPartsW * Dp * sizeof(__half)));
+        TRY(ctx->g_xn.ensure((size_t)N * sizeof(float)));
+        TRY(ctx->g_wn.ensure((size_t)N * sizeof(float)));
+        TRY(ctx->g_xi.ensure((size_t)N * sizeof(float)));
+        TRY(ctx->g_wi.ensure((size_t)N * sizeof(float)));
+        TRY(ctx->g_cur.ensure((size_t)B * sizeof(int32_t)));
+        TRY(ctx->m.ensure((size_t)B * Np * sizeof(float)));
+        BmuArgs ga;
+        std::memset(&ga, 0, sizeof ga);
+        ga.x_split = ctx->g_xs.as<__half>();
+        ga.w_split = ctx->g_ws.as<__half>();
+        ga.xn = ctx->g_xn.as<float>();
+        ga.wn = ctx->g_wn.as<float>();
+        ga.x_inv_scale = ctx->g_xi.as<float>();
+        ga.w_inv_scale = ctx->g_wi.as<float>();
+        ga.status = ctx->status.as<int>();
+        ga.n = N;
+        ga.M = N;
+        ga.D = Dp;
+        ga.Dp = Dp;
+        ga.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
+        ga.gram = ctx->gram.as<float>();
+        ga.gram_ld = Np;
+        TcPlan gp{};
+        gp.pair = 1;
+        gp.n_beta = (int)((N + kUnitRows - 1) / kUnitRows);
+        gp.n_beta += gp.n_beta & 1;
+        gp.set_uniform(256, N);
+        gp.grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(info.sms / 2, (int64_t)(gp.n_beta / 2) * gp.n_chunk));
+        CUtensorMap tx, tw;
+        TRY(encode_f16_map(tx, ga.x_split, kBmuPartsX * Dp, N, kUnitRows));
+        TRY(encode_f16_map(tw, ga.w_split, kBmuPartsW * Dp, N, gp.tile_n / 2));
+        GramWalkArgs wa;
+        std::memset(&wa, 0, sizeof wa);
+        wa.G = ctx->gram.as<float>();
+        wa.m = ctx->m.as<float>();
+        wa.cur = ctx->g_cur.as<int32_t>();
+        wa.picks = d_picks;
+        wa.trace_slot = d_slot;
+        wa.trace = trace_mindist;
+        wa.status = ctx->status.as<int>();
+        wa.N = N;
+        wa.Np = Np;
+        wa.B = B;
+        wa.L = L;
+        EventTimer mid;
+        TRY(timer.start(st));
+        // the table's unit rows, split twice (the sample and codebook sides)
+        launch_bmu_prepare(ctx->e_unit.as<float>(), N, Dp, Dp, 0, ctx->g_xs.as<__half>(),
+                           ctx->g_xn.as<float>(), ctx->g_xi.as<float>(), ga.status, st);
+        launch_bmu_prepare(ctx->e_unit.as<float>(), N, Dp, Dp, 1, ctx->g_ws.as<__half>(),
+                           ctx->g_wn.as<float>(), ctx->g_wi.as<float>(), ga.status, st);
+        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(launch_tc_gram(ga, gp, tx, tw, st));
+        TRY(mid.start(st));
+        if (!resume) launch_gram_walk_init(wa, ctx->starts.as<int32_t>(), d_mask, st);
+        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(launch_gram_walk(wa, st));
+        TRY(timer.stop(st));
+        TRY(mid.stop(st));
+        g_stats.gram = 1;
+        g_stats.units = B;
+        g_stats.grid = B;
+        g_stats.launches = resume ? 4 : 5;
+        {
+            const int rs = read_status(ctx->status.as<int>(), st);
+            if (rs != DSEQ_OK) {
+                ctx->has_state = false;
+                return rs;
+            }
+        }
+        // timer: the whole engine; mid: from the end of the Gram product
+        g_stats.walk_ns = mid.ns();
+        g_stats.gram_ns = std::max<int64_t>(0, timer.ns() - g_stats.walk_ns);
+    } else if (ctx->opt.engine == 0) {
         // ---- tensor-core persistent kernel ----
         const bool f16 = ctx->opt.storage == 1;
         // a global mask that removes at least 1/16 of the table: scan only
@@ -891,6 +1022,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     }
     // an epilogue-isolated run leaves meaningless state: nothing to resume
     ctx->has_state = ctx->opt.isolate_epilogue == 0;
+    ctx->state_gram = use_gram;
     ctx->state_picks = done_before + L;
     ctx->state_sig = sig;
     ctx->state_starts = h_starts;

@@ -1,0 +1,217 @@
+// gram.cu — the Gram engine of the max-min diversity path.
+//
+// The method ("Issue 9-014: Tile Diversity Shader Inner Loop For L2 Cache
+// Locality", Current Behavior): every iteration, each sequence folds the
+// cosine distance of its newest pick p to every candidate c into its running
+// minimum and takes the unmasked candidate with the largest running minimum
+// (lowest index on ties).  The newest pick is itself a table row, so every
+// distance the run needs is an entry of the table's Gram matrix: d(p, c) =
+// 1 - G[p][c] with G = E E^T of the unit rows.  When the sequences make many
+// more picks than the table has rows (B * L >> N), computing G once on the
+// tensor cores (the BMU kernel's pipeline with a store epilogue, see
+// tc_bmu.cu) and then streaming one row of G per sequence and iteration moves
+// far less work than the per-iteration contraction: the iterations become a
+// pure HBM/L2 stream, and the sequences are independent of one another, so
+// the walk needs no grid-wide synchronisation at all.
+//
+// gram_walk_kernel: one CTA per sequence, all L iterations.  Per iteration
+// the CTA streams G[p][0 .. N) (16-byte loads, several in flight per thread),
+// folds d = 1 - g into the running minimum (kept in shared memory when a row
+// of it fits, else in global memory), and reduces (max, lowest index) over
+// the block: per thread in ascending column order with a strict '>', then
+// warp shuffles and one shared-memory stage with the index as tie-break.
+// The winner is masked by the thread that owns its column in the next
+// iteration's fold, so the only block-wide barriers are the two of the
+// reduction.
+#include <climits>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dseq {
+
+namespace {
+
+constexpr int kWalkThreads = 256;
+constexpr int kWalkWarps = kWalkThreads / 32;
+// 16-byte vectors of a G row in flight per thread
+constexpr int kWalkBatch = 8;
+
+__device__ __forceinline__ float4 ld_nc_v4(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float4 ld_cg_v4(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// (value, index) max with the lower index on equal values
+__device__ __forceinline__ void take_better(float &v, int &c, float ov, int oc) {
+    if (ov > v || (ov == v && oc < c)) {
+        v = ov;
+        c = oc;
+    }
+}
+
+__global__ void gram_walk_init_kernel(GramWalkArgs a, const int32_t *__restrict__ starts,
+                                      const uint8_t *__restrict__ mask) {
+    const int64_t total = (int64_t)a.B * a.Np;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int b = (int)(i / a.Np);
+        const int64_t c = i - (int64_t)b * a.Np;
+        const bool live = c < a.N && c != starts[b] && !(mask && mask[c]);
+        a.m[i] = live ? INFINITY : -INFINITY;
+    }
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < a.B; b += stride)
+        a.cur[b] = starts[b];
+}
+
+// kSmem: the sequence's running minima live in shared memory for the whole
+// walk (loaded from and stored back to a.m around it); otherwise they are
+// read and written in global memory every iteration.
+template <bool kSmem>
+__global__ void __launch_bounds__(kWalkThreads) gram_walk_kernel(GramWalkArgs a) {
+    extern __shared__ float4 s_m4[];
+    __shared__ float red_v[kWalkWarps];
+    __shared__ int red_c[kWalkWarps];
+    __shared__ int s_win;
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nv = (int)(a.Np / 4);
+    float4 *m_g = reinterpret_cast<float4 *>(a.m + (int64_t)b * a.Np);
+    if (kSmem) {
+        for (int v = threadIdx.x; v < nv; v += kWalkThreads) s_m4[v] = ld_cg_v4(m_g + v);
+        __syncthreads();
+    }
+    const int slot = a.trace_slot ? a.trace_slot[b] : -1;
+    int p = a.cur[b];
+    int pending = -1;  // the last pick, masked in the next fold
+    for (int t = 0; t < a.L; ++t) {
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np);
+        float best = -INFINITY;
+        int best_c = INT_MAX;
+        const int pv = pending >> 2;
+        for (int v0 = threadIdx.x; v0 < nv; v0 += kWalkBatch * kWalkThreads) {
+            float4 gv[kWalkBatch], mv[kWalkBatch];
+#pragma unroll
+            for (int u = 0; u < kWalkBatch; ++u) {
+                const int v = v0 + u * kWalkThreads;
+                gv[u] = v < nv ? ld_nc_v4(g4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!kSmem)
+                    mv[u] = v < nv ? ld_cg_v4(m_g + v)
+                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < kWalkBatch; ++u) {
+                const int v = v0 + u * kWalkThreads;
+                if (v >= nv) break;
+                if (kSmem) mv[u] = s_m4[v];
+                float m4[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
+                const float g[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+                bool changed = false;
+                if (v == pv) {
+                    m4[pending & 3] = -INFINITY;
+                    changed = true;
+                }
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const float d = fmaf(g[z], -1.0f, 1.0f);
+                    const float nm = fminf(m4[z], d);
+                    changed |= nm != m4[z];
+                    m4[z] = nm;
+                    if (nm > best) {
+                        best = nm;
+                        best_c = 4 * v + z;
+                    }
+                }
+                if (changed) {
+                    const float4 w = make_float4(m4[0], m4[1], m4[2], m4[3]);
+                    if (kSmem)
+                        s_m4[v] = w;
+                    else
+                        m_g[v] = w;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
+                        __shfl_xor_sync(0xffffffffu, best_c, o));
+        if (lane == 0) {
+            red_v[warp] = best;
+            red_c[warp] = best_c;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            best = lane < kWalkWarps ? red_v[lane] : -INFINITY;
+            best_c = lane < kWalkWarps ? red_c[lane] : INT_MAX;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
+                            __shfl_xor_sync(0xffffffffu, best_c, o));
+            if (lane == 0) {
+                const int w = best_c == INT_MAX ? -1 : best_c;
+                s_win = w;
+                a.picks[(int64_t)b * a.L + t] = w;
+                if (w < 0) atomicOr(a.status, kStatusNoWinner);
+            }
+        }
+        __syncthreads();
+        const int w = s_win;
+        if (slot >= 0) {
+            // the running minima after this fold, before the pick is masked
+            float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
+            const float *src = kSmem ? reinterpret_cast<const float *>(s_m4) : a.m + (int64_t)b * a.Np;
+            for (int64_t c = threadIdx.x; c < a.N; c += kWalkThreads) dst[c] = src[c];
+            __syncthreads();  // every copy read the pre-mask values
+        }
+        if (w < 0) break;
+        pending = w;
+        p = w;
+    }
+    // the state left for a resumed run: the last pick masked, minima in a.m
+    __syncthreads();
+    if (threadIdx.x == 0 && pending >= 0) {
+        if (kSmem)
+            reinterpret_cast<float *>(s_m4)[pending] = -INFINITY;
+        else
+            a.m[(int64_t)b * a.Np + pending] = -INFINITY;
+        a.cur[b] = p;
+    }
+    __syncthreads();
+    if (kSmem)
+        for (int v = threadIdx.x; v < nv; v += kWalkThreads) m_g[v] = s_m4[v];
+}
+
+}  // namespace
+
+void launch_gram_walk_init(const GramWalkArgs &a, const int32_t *starts, const uint8_t *mask,
+                           cudaStream_t st) {
+    gram_walk_init_kernel<<<2048, 256, 0, st>>>(a, starts, mask);
+}
+
+static size_t gram_walk_smem_bytes(int64_t Np) { return (size_t)Np * sizeof(float); }
+
+cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st) {
+    const size_t smem = gram_walk_smem_bytes(a.Np);
+    if (smem <= kGramWalkSmemMax) {
+        cudaError_t err = cudaFuncSetAttribute(gram_walk_kernel<true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        gram_walk_kernel<true><<<(unsigned)a.B, kWalkThreads, smem, st>>>(a);
+    } else {
+        gram_walk_kernel<false><<<(unsigned)a.B, kWalkThreads, 0, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dseq

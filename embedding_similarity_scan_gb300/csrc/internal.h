@@ -184,6 +184,27 @@ cudaError_t launch_tc_dseq(const TcDseqArgs &a, const TcPlan &p, const CUtensorM
 // two); 0 on error
 int tc_dseq_max_grid(bool pair, bool f16, bool centroid);
 
+// ---- diversity, Gram engine (gram.cu; the Gram product in tc_bmu.cu) --------
+struct GramWalkArgs {
+    const float *G;          // N x Np: G[p][c] = <e_p, e_c> of the unit rows
+    float *m;                // B x Np running minima, row-major (in and out)
+    int32_t *cur;            // B: the newest row of each sequence (in and out)
+    int32_t *picks;          // B x L
+    const int32_t *trace_slot;  // B (-1 = not traced) or nullptr
+    float *trace;            // n_trace x L x N
+    int *status;
+    int64_t N, Np;           // table rows; row stride of G and m (a multiple of 32)
+    int B, L;
+};
+// Largest shared-memory running-minimum row of the walk kernel (bytes):
+// longer rows stay in global memory.
+constexpr size_t kGramWalkSmemMax = 96 * 1024;
+// m <- +inf, or -inf for masked rows, the start and the row padding; cur <- starts.
+void launch_gram_walk_init(const GramWalkArgs &a, const int32_t *starts, const uint8_t *mask,
+                           cudaStream_t st);
+// All L iterations of every sequence, one CTA per sequence.
+cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st);
+
 // ---- diversity, FFMA path (ffma.cu) -----------------------------------------
 struct FfmaDseqArgs {
     const float *e_unit;   // N x Dp
@@ -220,6 +241,9 @@ struct BmuArgs {
     // test only: CTA 0 leaves out one copy of its first codebook stage, so
     // that stage never fills and the waits on it run out
     int fault_skip_copy;
+    // Gram product (launch_tc_gram): <e_i, e_c> stored at gram[c * gram_ld + i]
+    float *gram;
+    int64_t gram_ld;
 };
 void launch_bmu_keys_init(unsigned long long *keys, int64_t n, cudaStream_t st);
 void launch_ffma_bmu(const BmuArgs &a, cudaStream_t st);
@@ -227,6 +251,14 @@ void launch_ffma_bmu(const BmuArgs &a, cudaStream_t st);
 cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
                           const CUtensorMap &tmap_w, int slice_chunks, cudaStream_t st);
 void launch_bmu_finalize(const BmuArgs &a, cudaStream_t st);
+// The Gram product of one table, G = E E^T, on the BMU kernel's tensor-core
+// pipeline (CTA pairs, the streaming operand ring) with a store epilogue: the
+// sample side (x_split, x_inv_scale, n rows) and the codebook side (w_split,
+// w_inv_scale, M = n rows) are the same table's rows split twice; a.gram
+// receives G (row stride gram_ld >= n).  p: n_beta (even) sample blocks,
+// uniform 256-wide chunks of the table, an even grid.
+cudaError_t launch_tc_gram(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
+                           const CUtensorMap &tmap_w, cudaStream_t st);
 void launch_row_sqnorm(const float *A, int64_t rows, int D, float *out, int *status,
                        cudaStream_t st);
 

@@ -167,6 +167,61 @@ __device__ __forceinline__ bool bmu_epilogue_unit(const BmuArgs &a, int beta, in
     return true;
 }
 
+// Store epilogue of the Gram product (a.gram != nullptr): the same operands
+// hold the rows of one table on both sides (X = [hi | lo * 2^12], W =
+// [hi * 2^12 | hi | lo * 2^12], each row scaled by its power of two), so the
+// accumulator of row i (sample side) and column c (codebook side) is
+// 2^12 <x~_i, w~_c>; scaled back exactly, <e_i, e_c> is stored at
+// gram[c * gram_ld + i]: for each column the 32 lanes of a warp write 32
+// consecutive rows, one 128-byte line.  Returns false if the wait gave up.
+template <bool kPair>
+__device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, int j, uint32_t tile_n,
+                                                   int groups, uint32_t tmem_base, uint32_t &acc_uses,
+                                                   uint64_t *acc_full, uint64_t *acc_empty,
+                                                   uint32_t acc_empty_leader0,
+                                                   volatile int *abort_flag, int warp, int lane) {
+    const int e = warp - 2, q = warp & 3, h = e >> 2;
+    const int64_t row = (int64_t)beta * kUnitRows + 32 * q + lane;
+    const bool row_ok = row < a.n;
+    const float rx = row_ok ? a.x_inv_scale[row] * (1.0f / 4096.0f) : 0.0f;
+    float cw[kMaxGroups / 2];
+#pragma unroll
+    for (int k = 0; k < kMaxGroups / 2; ++k) {
+        const int64_t col = (int64_t)j * tile_n + 32 * (h + 2 * k) + lane;
+        cw[k] = (h + 2 * k < groups && col < a.M) ? __ldg(a.w_inv_scale + col) : 0.0f;
+    }
+    const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
+    const bool ready = mbar_wait_bounded(&acc_full[buf], apar, abort_flag, a.status, a.timeout_ns,
+                                         kStatusPipeTimeout);
+    if (!__all_sync(0xffffffffu, ready)) return false;
+    tc_fence_after();
+    const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+#pragma unroll
+    for (int k = 0; k < kMaxGroups / 2; ++k) {
+        const int g = h + 2 * k;
+        if (g >= groups) break;
+        float acc[32];
+        tmem_ld_32cols(tbase + (uint32_t)(32 * g), acc);
+        tmem_wait_ld();
+        const int64_t cbase = (int64_t)j * tile_n + 32 * g;
+#pragma unroll
+        for (int z = 0; z < 32; ++z) {
+            const float wz = __shfl_sync(0xffffffffu, cw[k], z);
+            if (row_ok && cbase + z < a.M) a.gram[(cbase + z) * a.gram_ld + row] = acc[z] * rx * wz;
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+        if (kPair)
+            mbar_arrive_cluster(acc_empty_leader0 + buf * (uint32_t)sizeof(uint64_t));
+        else
+            mbar_arrive(&acc_empty[buf]);
+    }
+    ++acc_uses;
+    return true;
+}
+
 struct BmuSchedule {
     int n_blocks, n_chunk, tile_n, slice_chunks;
     // work item u -> (sample block, or sample block pair, "beta"; neuron chunk j)
@@ -181,7 +236,8 @@ struct BmuSchedule {
     }
 };
 
-template <bool kPair>
+// kGram: the store epilogue of the Gram product instead of the argmin.
+template <bool kPair, bool kGram = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_bmu_kernel(const __grid_constant__ CUtensorMap tmap_x,
                   const __grid_constant__ CUtensorMap tmap_w, const BmuArgs a, const TcPlan p,
@@ -372,9 +428,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int blk, j;
             sched.decode(u, blk, j);
             const int beta = kPair ? 2 * blk + (int)rank : blk;
-            if (!bmu_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses, acc_full,
-                                          acc_empty, acc_empty_leader0, my_colc, abort_flag, warp, lane))
+            if (kGram) {
+                if (!gram_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses,
+                                               acc_full, acc_empty, acc_empty_leader0, abort_flag,
+                                               warp, lane))
+                    break;
+            } else if (!bmu_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses,
+                                                 acc_full, acc_empty, acc_empty_leader0, my_colc,
+                                                 abort_flag, warp, lane)) {
                 break;
+            }
         }
     }
 
@@ -702,6 +765,39 @@ cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &
     if (err != cudaSuccess) return err;
     cfg.dynamicSmemBytes = smem;
     return cudaLaunchKernelEx(&cfg, tc_bmu_kernel<true>, mx, mw, aa, pp, sl);
+}
+
+cudaError_t launch_tc_gram(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
+                           const CUtensorMap &tmap_w, cudaStream_t st) {
+    // the whole codebook side is one slice when it fits half of L2
+    int dev = 0, l2 = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    const double row_bytes = (double)kBmuPartsW * a.Dp * 2.0;
+    int slice = (int)((0.5 * (double)l2) / (row_bytes * p.tile_n));
+    if (slice < 1) slice = 1;
+    if (slice > p.n_chunk) slice = p.n_chunk;
+    BmuArgs aa = a;
+    TcPlan pp = p;
+    CUtensorMap mx = tmap_x, mw = tmap_w;
+    int sl = slice;
+    const size_t smem = BmuCfg<true>::kSmemBytes;
+    cudaError_t err = cudaFuncSetAttribute(tc_bmu_kernel<true, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_bmu_kernel<true, true>, mx, mw, aa, pp, sl);
 }
 
 }  // namespace dseq

@@ -33,13 +33,18 @@ def _reset_options(es):
     yield
     for name, v in (("engine", 0), ("tile_n", 0), ("tile_n2", 0), ("grid", 0), ("timeout_ms", 10000),
                     ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR), ("storage", 0),
-                    ("criterion", 0), ("resume", 0), ("compact", 1), ("isolate_epilogue", 0)):
+                    ("criterion", 0), ("resume", 0), ("compact", 1), ("isolate_epilogue", 0),
+                    ("gram", 2)):
         es.dseq_set_option(name, v)
 
 
 def _run(es, E, starts, L, mask=None, trace_seqs=None, engine=0, tile_n=0, grid=0,
-         pair=None, storage=0, criterion=0, tile_n2=0):
+         pair=None, storage=0, criterion=0, tile_n2=0, gram=0):
+    """One context, one run.  gram = 0 (default here) keeps the tests that
+    target the per-iteration kernels on them; gram = 1 runs the Gram engine,
+    2 lets the library choose."""
     dev = torch.device("cuda")
+    es.dseq_set_option("gram", gram)
     es.dseq_set_option("engine", engine)
     es.dseq_set_option("tile_n", tile_n)
     es.dseq_set_option("tile_n2", tile_n2)
@@ -484,10 +489,10 @@ def test_centroid_fp16_storage_full_size_and_agreement(es):
 # give exactly the picks of one long call.
 
 
-@pytest.mark.parametrize("engine,pair,criterion,storage",
-                         [(0, 1, 0, 0), (0, 0, 0, 0), (1, 0, 0, 0), (0, 1, 1, 0), (0, 1, 0, 1),
-                          (0, 1, 1, 1)])
-def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion, storage):
+@pytest.mark.parametrize("engine,pair,criterion,storage,gram",
+                         [(0, 1, 0, 0, 0), (0, 0, 0, 0, 0), (1, 0, 0, 0, 0), (0, 1, 1, 0, 0),
+                          (0, 1, 0, 1, 0), (0, 1, 1, 1, 0), (0, 1, 0, 0, 1)])
+def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion, storage, gram):
     N, D, B = 300, 40, 9
     E = workloads.clustered_table(N, D, n_centres=6, seed=12)
     starts = workloads.starts(N, B, seed=12)
@@ -502,6 +507,7 @@ def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion, storage):
     es.dseq_set_option("pair", pair)
     es.dseq_set_option("criterion", criterion)
     es.dseq_set_option("storage", storage)
+    es.dseq_set_option("gram", gram)
     ctx = es.dseq_create(torch.from_numpy(E).cuda())
     try:
         st = torch.from_numpy(starts).cuda()
@@ -560,6 +566,7 @@ def test_global_mask_compaction_identical(es, pair, storage, criterion):
     check = check_centroid_teacher_forced if criterion else check_dseq_teacher_forced
     check(E, starts, mask, picks, trace, tr)
     # the compacted run resumed in two chunks gives the same picks
+    es.dseq_set_option("gram", 0)
     es.dseq_set_option("compact", 1)
     es.dseq_set_option("pair", pair)
     es.dseq_set_option("storage", storage)
@@ -651,3 +658,115 @@ def test_resume_without_state_rejected(es):
             es.dseq_run(ctx, torch.tensor([0, 5], dtype=torch.int32, device="cuda"), 3)
     finally:
         ctx.close()
+
+
+# --------------------------------------------------------------------------
+# The Gram engine (max-min on split storage): the table's Gram matrix on the
+# tensor cores, then one row of it per sequence and iteration, against the
+# same oracle under the same teacher-forced tolerances.
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
+def test_gram_small_teacher_forced(es, case):
+    N, D, B, L, kind, frac = case
+    E = workloads.gaussian_table(N, D, seed=N) if kind == "gaussian" else \
+        workloads.clustered_table(N, D, n_centres=16, seed=N)
+    starts = workloads.starts(N, B, seed=N)
+    mask = None
+    if frac > 0:
+        rng = np.random.default_rng(N)
+        mask = (rng.random(N) < frac).astype(np.uint8)
+        mask[starts[: B // 3]] = 1  # some starts are masked themselves
+    trace_seqs = np.arange(B, dtype=np.int32) if B <= 200 else \
+        np.sort(np.random.default_rng(1).choice(B, 64, replace=False)).astype(np.int32)
+    picks, trace = _run(es, E, starts, L, mask, trace_seqs, gram=1)
+    assert es.dseq_last_stat("gram") == 1
+    check_picks_valid(starts, mask, picks, N)
+    check_dseq_teacher_forced(E, starts, mask, picks, trace, trace_seqs)
+
+
+@pytest.mark.parametrize("case", EXTREME, ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
+def test_gram_extreme_shapes_teacher_forced(es, case):
+    N, D, B, L = case
+    E = workloads.gaussian_table(N, D, seed=D + N)
+    starts = workloads.starts(N, B, seed=D + N)
+    tr = np.unique(np.array([0, B // 2, B - 1], np.int32))
+    picks, trace = _run(es, E, starts, L, None, tr, gram=1)
+    check_picks_valid(starts, None, picks, N)
+    check_dseq_teacher_forced(E, starts, None, picks, trace, tr)
+
+
+def test_gram_running_minima_in_global_memory(es):
+    """A table whose running-minimum rows are too long for shared memory:
+    the walk keeps them in global memory (masked rows, ragged N)."""
+    N, D, B, L = 30011, 48, 37, 10
+    E = workloads.clustered_table(N, D, n_centres=20, seed=31)
+    starts = workloads.starts(N, B, seed=31)
+    mask = (np.random.default_rng(31).random(N) < 0.05).astype(np.uint8)
+    tr = np.arange(B, dtype=np.int32)
+    picks, trace = _run(es, E, starts, L, mask, tr, gram=1)
+    check_picks_valid(starts, mask, picks, N)
+    check_dseq_teacher_forced(E, starts, mask, picks, trace, tr)
+
+
+def test_gram_worked_examples(es):
+    """The square of four unit vectors and the orthonormal table (every
+    off-diagonal distance 1: a pure tie-break) on the Gram engine."""
+    E = np.array([[1, 0], [0, 1], [-1, 0], [0, -1]], np.float32)
+    picks, _ = _run(es, E, np.array([0], np.int32), 3, gram=1)
+    assert picks.tolist() == [[2, 1, 3]]
+    N = 40
+    E = np.eye(N, dtype=np.float32)
+    starts = np.array([0, 7, 39], np.int32)
+    picks, _ = _run(es, E, starts, N - 1, gram=1)
+    for b, s0 in enumerate(starts):
+        assert picks[b].tolist() == [c for c in range(N) if c != s0]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_gram_random_shapes_teacher_forced(es, seed):
+    N, D, B, L, mask, starts = _random_case(seed)
+    if L == 0:
+        pytest.skip("no candidate left to pick")
+    E = workloads.gaussian_table(N, D, seed=seed) if seed % 2 else \
+        workloads.clustered_table(N, D, n_centres=8, seed=seed)
+    if mask is not None:
+        avail = N - int(mask.sum()) - (mask[starts] == 0).astype(int)
+        L = int(min(L, avail.min()))
+        if L < 1:
+            pytest.skip("no candidate left to pick")
+    tr = np.unique(np.linspace(0, B - 1, num=min(B, 4)).astype(np.int32))
+    picks, trace = _run(es, E, starts, L, mask, tr, gram=1)
+    check_picks_valid(starts, mask, picks, N)
+    check_dseq_teacher_forced(E, starts, mask, picks, trace, tr)
+
+
+def test_gram_automatic_choice(es):
+    """gram = 2 (the default): the Gram engine where sequences make many more
+    picks than the table has rows, the per-iteration kernel where they do not."""
+    cfg = workloads.DIVERSITY["tiny"]
+    _run(es, cfg.table(seed=0), cfg.starts(seed=0), cfg.L, gram=2)
+    assert es.dseq_last_stat("gram") == 0
+    N, D, B, L = 2000, 256, 1500, 40
+    E = workloads.clustered_table(N, D, n_centres=10, seed=3)
+    picks, _ = _run(es, E, workloads.starts(N, B, seed=3), L, gram=2)
+    assert es.dseq_last_stat("gram") == 1
+    assert es.dseq_last_stat("gram_ns") > 0 and es.dseq_last_stat("walk_ns") > 0
+
+
+@pytest.mark.parametrize("name", ["page1", "scale"])
+def test_gram_full_size_teacher_forced(es, name):
+    """The full configurations on the engine the library picks for them (the
+    Gram engine), the benchmark's launch configuration, with a seeded subset
+    of sequences followed by the oracle."""
+    cfg = workloads.DIVERSITY[name]
+    E = cfg.table(seed=0)
+    starts = cfg.starts(seed=0)
+    tr = np.sort(np.random.default_rng(0).choice(cfg.B, cfg.oracle_seqs, replace=False))
+    picks, trace = _run(es, E, starts, cfg.L, trace_seqs=tr.astype(np.int32), gram=2)
+    assert es.dseq_last_stat("gram") == 1
+    check_dseq_teacher_forced(E, starts[tr], None, picks[tr], trace, np.arange(tr.size))
+    assert np.all((picks >= 0) & (picks < cfg.N))
+    srt = np.sort(picks, axis=1)
+    assert not np.any(srt[:, 1:] == srt[:, :-1]), "a sequence repeats a pick"
+    assert not np.any(picks == starts[:, None]), "a sequence picks its start"
