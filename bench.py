@@ -605,7 +605,8 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
         cfg = wl.cfg
         np_ = (cfg.N + 31) // 32 * 32
         m_global = np_ * 4 > GRAM_WALK_SMEM_MAX
-        walk_bytes = cfg.B * cfg.L * cfg.N * (4.0 + (8.0 if m_global else 0.0))
+        # reads only: a running minimum is written back only where it fell
+        walk_bytes = cfg.B * cfg.L * cfg.N * (4.0 + (4.0 if m_global else 0.0))
         walk_s = statistics.mean(st["walk_ns"] for st in stats) / 1e9
         gram_s = statistics.mean(st["gram_ns"] for st in stats) / 1e9
         gflop = 2.0 * cfg.N * cfg.N * cfg.D
@@ -614,7 +615,7 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
                 "traffic": None if shrunk else _profiled_traffic("gram_walk_kernel", wl.name),
                 "kernel": "gram_walk_kernel",
                 "note": (f"achieved = algorithmic bytes of the walk (one row of G, 4*N bytes, per "
-                         f"sequence-iteration{' + the running minima read and written, 8*N' if m_global else ''})"
+                         f"sequence-iteration{' + the running minima read, 4*N; writes of the minima that fell are not counted' if m_global else ''})"
                          f" / walk kernel time (CUDA events); peak = {peak_src} copy bandwidth "
                          f"{hbm_peak:.1f} GB/s")}
         gram_product = {"bound": "tensor", "achieved": gflop / gram_s / 1e12, "peak": tensor_peak,

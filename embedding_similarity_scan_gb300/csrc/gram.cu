@@ -35,8 +35,6 @@ namespace {
 
 constexpr int kWalkThreads = 256;
 constexpr int kWalkWarps = kWalkThreads / 32;
-// 16-byte vectors of a G row in flight per thread
-constexpr int kWalkBatch = 8;
 
 __device__ __forceinline__ float4 ld_nc_v4(const float4 *p) {
     float4 v;
@@ -78,8 +76,11 @@ __global__ void gram_walk_init_kernel(GramWalkArgs a, const int32_t *__restrict_
 // kSmem: the sequence's running minima live in shared memory for the whole
 // walk (loaded from and stored back to a.m around it); otherwise they are
 // read and written in global memory every iteration.
-template <bool kSmem>
-__global__ void __launch_bounds__(kWalkThreads) gram_walk_kernel(GramWalkArgs a) {
+// kBatch: 16-byte vectors of the G row each thread has in flight at once;
+// the host picks it so that one batch covers a whole row where it can (one
+// round trip to memory per iteration).
+template <bool kSmem, int kBatch, int kMinBlocks>
+__global__ void __launch_bounds__(kWalkThreads, kMinBlocks) gram_walk_kernel(GramWalkArgs a) {
     extern __shared__ float4 s_m4[];
     __shared__ float red_v[kWalkWarps];
     __shared__ int red_c[kWalkWarps];
@@ -100,10 +101,10 @@ __global__ void __launch_bounds__(kWalkThreads) gram_walk_kernel(GramWalkArgs a)
         float best = -INFINITY;
         int best_c = INT_MAX;
         const int pv = pending >> 2;
-        for (int v0 = threadIdx.x; v0 < nv; v0 += kWalkBatch * kWalkThreads) {
-            float4 gv[kWalkBatch], mv[kWalkBatch];
+        for (int v0 = threadIdx.x; v0 < nv; v0 += kBatch * kWalkThreads) {
+            float4 gv[kBatch], mv[kBatch];
 #pragma unroll
-            for (int u = 0; u < kWalkBatch; ++u) {
+            for (int u = 0; u < kBatch; ++u) {
                 const int v = v0 + u * kWalkThreads;
                 gv[u] = v < nv ? ld_nc_v4(g4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                 if (!kSmem)
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kWalkThreads) gram_walk_kernel(GramWalkArgs a)
                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
 #pragma unroll
-            for (int u = 0; u < kWalkBatch; ++u) {
+            for (int u = 0; u < kBatch; ++u) {
                 const int v = v0 + u * kWalkThreads;
                 if (v >= nv) break;
                 if (kSmem) mv[u] = s_m4[v];
@@ -201,17 +202,26 @@ void launch_gram_walk_init(const GramWalkArgs &a, const int32_t *starts, const u
 
 static size_t gram_walk_smem_bytes(int64_t Np) { return (size_t)Np * sizeof(float); }
 
+template <bool kSmem, int kBatch, int kMinBlocks>
+cudaError_t launch_walk_variant(const GramWalkArgs &a, size_t smem, cudaStream_t st) {
+    auto kernel = gram_walk_kernel<kSmem, kBatch, kMinBlocks>;
+    if (smem > 48 * 1024) {
+        cudaError_t err =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    kernel<<<(unsigned)a.B, kWalkThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st) {
     const size_t smem = gram_walk_smem_bytes(a.Np);
-    if (smem <= kGramWalkSmemMax) {
-        cudaError_t err = cudaFuncSetAttribute(gram_walk_kernel<true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        gram_walk_kernel<true><<<(unsigned)a.B, kWalkThreads, smem, st>>>(a);
-    } else {
-        gram_walk_kernel<false><<<(unsigned)a.B, kWalkThreads, 0, st>>>(a);
-    }
-    return cudaGetLastError();
+    const int64_t nv = a.Np / 4;  // 16-byte vectors per row
+    if (smem > kGramWalkSmemMax) return launch_walk_variant<false, 6, 3>(a, 0, st);
+    if (nv <= 4 * kWalkThreads) return launch_walk_variant<true, 4, 6>(a, smem, st);
+    if (nv <= 6 * kWalkThreads) return launch_walk_variant<true, 6, 5>(a, smem, st);
+    if (nv <= 9 * kWalkThreads) return launch_walk_variant<true, 9, 4>(a, smem, st);
+    return launch_walk_variant<true, 12, 3>(a, smem, st);
 }
 
 }  // namespace dseq

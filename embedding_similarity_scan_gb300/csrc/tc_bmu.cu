@@ -173,13 +173,19 @@ __device__ __forceinline__ bool bmu_epilogue_unit(const BmuArgs &a, int beta, in
 // accumulator of row i (sample side) and column c (codebook side) is
 // 2^12 <x~_i, w~_c>; scaled back exactly, <e_i, e_c> is stored at
 // gram[c * gram_ld + i]: for each column the 32 lanes of a warp write 32
-// consecutive rows, one 128-byte line.  Returns false if the wait gave up.
+// consecutive rows, one 128-byte line.  G is symmetric, so only the items
+// on and above the diagonal of 256 x 256 tiles are computed; with mirror
+// set (an item off the diagonal) the same values are also stored at
+// gram[i * gram_ld + c], each thread writing its row's 32 consecutive
+// columns as one 128-byte line.  G is then exactly symmetric.  Returns false
+// if the wait gave up.
 template <bool kPair>
 __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, int j, uint32_t tile_n,
                                                    int groups, uint32_t tmem_base, uint32_t &acc_uses,
                                                    uint64_t *acc_full, uint64_t *acc_empty,
                                                    uint32_t acc_empty_leader0,
-                                                   volatile int *abort_flag, int warp, int lane) {
+                                                   volatile int *abort_flag, int warp, int lane,
+                                                   bool mirror) {
     const int e = warp - 2, q = warp & 3, h = e >> 2;
     const int64_t row = (int64_t)beta * kUnitRows + 32 * q + lane;
     const bool row_ok = row < a.n;
@@ -207,7 +213,17 @@ __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, i
 #pragma unroll
         for (int z = 0; z < 32; ++z) {
             const float wz = __shfl_sync(0xffffffffu, cw[k], z);
-            if (row_ok && cbase + z < a.M) a.gram[(cbase + z) * a.gram_ld + row] = acc[z] * rx * wz;
+            acc[z] *= rx * wz;
+            if (row_ok && cbase + z < a.M) a.gram[(cbase + z) * a.gram_ld + row] = acc[z];
+        }
+        if (mirror && row_ok) {
+            // columns past M are row padding of G (never read as values)
+            float4 *dst = reinterpret_cast<float4 *>(a.gram + row * a.gram_ld + cbase);
+            if (cbase + 32 <= a.gram_ld) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+            }
         }
     }
     tc_fence_before();
@@ -326,6 +342,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int64_t u = first_item; u < units && !*abort_flag; u += item_stride) {
                 int blk, j;
                 sched.decode(u, blk, j);
+                if (kGram && j < blk) continue;  // the mirror of an item computed
                 const int beta = kPair ? 2 * blk + (int)rank : blk;
                 const int yx = beta * kUnitRows, yw = j * (int)tile_n + (int)(rank * b_rows);
                 for (int kb = 0; kb < kblocks; ++kb) {
@@ -377,6 +394,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0 && leader) {
             uint32_t consumed = 0, acc_uses = 0;
             for (int64_t u = first_item; u < units && !*abort_flag; u += item_stride) {
+                if (kGram) {
+                    int blk, j;
+                    sched.decode(u, blk, j);
+                    if (j < blk) continue;
+                }
                 const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
                 if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
                                        kStatusPipeTimeout))
@@ -429,9 +451,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             sched.decode(u, blk, j);
             const int beta = kPair ? 2 * blk + (int)rank : blk;
             if (kGram) {
+                if (j < blk) continue;
+                // off the diagonal the tile also fills its mirror image
                 if (!gram_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses,
                                                acc_full, acc_empty, acc_empty_leader0, abort_flag,
-                                               warp, lane))
+                                               warp, lane, j > blk))
                     break;
             } else if (!bmu_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses,
                                                  acc_full, acc_empty, acc_empty_leader0, my_colc,

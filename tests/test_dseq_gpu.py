@@ -747,7 +747,7 @@ def test_gram_automatic_choice(es):
     cfg = workloads.DIVERSITY["tiny"]
     _run(es, cfg.table(seed=0), cfg.starts(seed=0), cfg.L, gram=2)
     assert es.dseq_last_stat("gram") == 0
-    N, D, B, L = 2000, 256, 1500, 40
+    N, D, B, L = 2000, 768, 1500, 40
     E = workloads.clustered_table(N, D, n_centres=10, seed=3)
     picks, _ = _run(es, E, workloads.starts(N, B, seed=3), L, gram=2)
     assert es.dseq_last_stat("gram") == 1
