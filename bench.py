@@ -23,7 +23,9 @@ HBM.
 
 ``--impl reference`` times the CPU oracle itself as the reference arm.
 Multi-GPU (torchrun): every rank runs the full workload on its own GPU
-(independent replicas, weak scaling); time is the max over ranks.
+(independent replicas, weak scaling); with ``--shard`` the ranks split one
+workload's sequences (or samples) and rank 0 gathers the results (strong
+scaling).  Time is the max over ranks.
 """
 from __future__ import annotations
 
@@ -53,6 +55,7 @@ KERNEL_SOURCES = {
     "tc_dseq_kernel": ["tc_dseq.cu", "common.cuh", "internal.h", "numeric.cuh"],
     "tc_bmu_kernel": ["tc_bmu.cu", "common.cuh", "internal.h"],
     "tc_bmu_resident_kernel": ["tc_bmu.cu", "common.cuh", "internal.h"],
+    "gram_walk_kernel": ["gram.cu", "common.cuh", "internal.h"],
 }
 
 
@@ -362,19 +365,32 @@ class _Workload:
     e2e_step: object
     close: object
     update_ns: list
+    result: object = None  # host copy of the last step's picks (or BMU indices)
 
 
 def _workload(args, name, es, dev, rank, opts) -> _Workload:
     import torch
 
+    from embedding_similarity_scan_gb300.shard import shard_range
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    # --shard: the ranks split one workload (its sequences or samples) with
+    # no exchange on the data path; otherwise each rank runs a whole replica
+    shard = args.shard and world > 1
     update_ns = []
     if name in workloads.DIVERSITY:
         cfg = workloads.DIVERSITY[name]
         if args.iters > 0:
             cfg = dataclasses.replace(cfg, L=args.iters)
         E_host = torch.from_numpy(cfg.table(seed=0)).pin_memory()
-        # each rank runs its own shard: the same table, its own sequences
-        starts_host = torch.from_numpy(cfg.starts(seed=rank)).pin_memory()
+        if shard:
+            lo, hi = shard_range(cfg.B, rank, world)
+            starts_np = cfg.starts(seed=0)[lo:hi]
+            cfg = dataclasses.replace(cfg, B=hi - lo)
+        else:
+            # each rank runs its own replica: the same table, its own sequences
+            starts_np = cfg.starts(seed=rank)
+        starts_host = torch.from_numpy(starts_np).pin_memory()
         ctx = es.dseq_create(E_host.to(dev))
         starts_dev = starts_host.to(dev)
         picks_dev = torch.empty((cfg.B, cfg.L), dtype=torch.int32, device=dev)
@@ -406,8 +422,11 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
             "sequence-iterations/s",
             {"workload": name, "N": cfg.N, "D": cfg.D, "B": cfg.B, "L": cfg.L,
              "l2": "flushed between steps (512 MB write)"},
-            step, e2e_step, ctx.close, update_ns)
+            step, e2e_step, ctx.close, update_ns, lambda: picks_dev.cpu().numpy())
     if name in workloads.SOM_EPOCH:
+        if shard:
+            raise SystemExit("--shard: a sharded SOM epoch would need the per-neuron sums "
+                             "reduced across ranks before the update; not provided")
         epoch_of = workloads.SOM_EPOCH[name]
         cfg = workloads.BMU[epoch_of]
         sx, sy = workloads.SOM_SIDES[epoch_of]
@@ -440,12 +459,18 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
             _bmu_kernel_name(cfg.D, opts), "SOM epoch samples/s", "samples/s",
             {"workload": name, "n": cfg.n, "M": cfg.M, "D": cfg.D, "map": f"{sx}x{sy}",
              "sigma": sigma, "radius": radius, "l2": "flushed between steps (512 MB write)"},
-            step, e2e_step, lambda: None, update_ns)
+            step, e2e_step, lambda: None, update_ns, lambda: idx_dev.cpu().numpy())
     cfg = workloads.BMU[name]
     if args.samples > 0:
         cfg = dataclasses.replace(cfg, n=args.samples)
-    # each rank runs its own shard: the same codebook, its own samples
-    X_host = torch.from_numpy(cfg.samples(seed=rank)).pin_memory()
+    if shard:
+        lo, hi = shard_range(cfg.n, rank, world)
+        X_np = cfg.samples(seed=0)[lo:hi]
+        cfg = dataclasses.replace(cfg, n=hi - lo)
+    else:
+        # each rank runs its own replica: the same codebook, its own samples
+        X_np = cfg.samples(seed=rank)
+    X_host = torch.from_numpy(np.ascontiguousarray(X_np)).pin_memory()
     W_host = torch.from_numpy(cfg.codebook(seed=0)).pin_memory()
     X_dev, W_dev = X_host.to(dev), W_host.to(dev)
     idx_dev = torch.empty(cfg.n, dtype=torch.int32, device=dev)
@@ -466,7 +491,7 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
         _bmu_kernel_name(cfg.D, opts), "BMU samples/s", "samples/s",
         {"workload": name, "n": cfg.n, "M": cfg.M, "D": cfg.D,
          "l2": "flushed between steps (512 MB write)"},
-        step, e2e_step, lambda: None, update_ns)
+        step, e2e_step, lambda: None, update_ns, lambda: idx_dev.cpu().numpy())
 
 
 def _measure(args, wl, opts, dev, local, pg, ws, flush):
@@ -516,7 +541,13 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
         t = torch.tensor([total_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         total_ms = float(t.item())
-    value = ws * wl.units * args.steps / (total_ms / 1e3)
+    units_all = ws * wl.units
+    if pg is not None and args.shard:
+        # strong scaling: the ranks' shares of one workload add up
+        t = torch.tensor([float(wl.units)], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.SUM)
+        units_all = float(t.item())
+    value = units_all * args.steps / (total_ms / 1e3)
 
     # end to end through the C ABI with host buffers
     e2e_steps = max(1, min(args.steps, 3))
@@ -531,7 +562,7 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
         t = torch.tensor([e2e_s], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_s = float(t.item())
-    e2e_value = ws * wl.units * e2e_steps / e2e_s
+    e2e_value = units_all * e2e_steps / e2e_s
 
     kernel_ns = [st["kernel_ns"] for st in stats]
     launches = sum(st["launches"] for st in stats)
@@ -628,7 +659,7 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
     line = {
         "metric": wl.metric, "value": value, "unit": wl.unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
+        "scaling": "strong" if (pg is not None and args.shard) else "weak", "vs_baseline": None,
         "dtype": ("f32 (FFMA)" if "engine=1" in opts
                   else "f16 storage, f32 accumulate" if fp16_storage
                   else "fp16x3-split (fp32-accurate), f32 accumulate"),
@@ -693,6 +724,14 @@ def run_ours(args):
 
     wl = _workload(args, args.workload, es, dev, rank, opts)
     line = _measure(args, wl, opts, dev, local, pg, ws, flush)
+    if pg is not None and args.shard:
+        # the host-side gather that completes a sharded run (outside the
+        # timed region): every rank's picks (or BMU indices) in rank order
+        from embedding_similarity_scan_gb300.shard import gather_rows
+
+        rows = gather_rows(wl.result())
+        line["shard"] = {"ranks": ws, "gathered_rows": int(rows.shape[0]),
+                         "note": "contiguous shares of one workload, results gathered on the host"}
     wl.close()
     default_line = not opts and args.workload == "page1" and args.iters == 0
     if default_line and line.get("engine") == "gram" and args.with_scan:
@@ -750,6 +789,9 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=0)
     ap.add_argument("--opt", action="append", default=[],
                     help="library option name=value, e.g. storage=1 (process-wide)")
+    ap.add_argument("--shard", action="store_true",
+                    help="under torchrun: split one workload's sequences (or samples) across "
+                         "the ranks (strong scaling) instead of a replica per rank")
     ap.add_argument("--no-scan", dest="with_scan", action="store_false",
                     help="leave out the per-iteration kernel's measurement that the default "
                          "page-1 line carries beside the Gram engine's")

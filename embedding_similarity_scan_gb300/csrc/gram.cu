@@ -33,8 +33,6 @@ namespace dseq {
 
 namespace {
 
-constexpr int kWalkThreads = 256;
-constexpr int kWalkWarps = kWalkThreads / 32;
 
 __device__ __forceinline__ float4 ld_nc_v4(const float4 *p) {
     float4 v;
@@ -79,18 +77,24 @@ __global__ void gram_walk_init_kernel(GramWalkArgs a, const int32_t *__restrict_
 // kBatch: 16-byte vectors of the G row each thread has in flight at once;
 // the host picks it so that one batch covers a whole row where it can (one
 // round trip to memory per iteration).
-template <bool kSmem, int kBatch, int kMinBlocks>
-__global__ void __launch_bounds__(kWalkThreads, kMinBlocks) gram_walk_kernel(GramWalkArgs a) {
+// The block argmax takes one barrier per iteration: every warp publishes its
+// (max, lowest index) in one of two alternating slots, and after the barrier
+// every warp reduces all slots itself, so all threads know the winner
+// without a second barrier (a warp cannot reach the slots of iteration t + 2
+// before every warp has passed the barrier of iteration t + 1).
+template <bool kSmem, int kThreads, int kBatch, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWalkArgs a) {
+    constexpr int kWarps = kThreads / 32;
+    static_assert(kWarps <= 32, "one warp reduces the per-warp slots");
     extern __shared__ float4 s_m4[];
-    __shared__ float red_v[kWalkWarps];
-    __shared__ int red_c[kWalkWarps];
-    __shared__ int s_win;
+    __shared__ float red_v[2][kWarps];
+    __shared__ int red_c[2][kWarps];
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nv = (int)(a.Np / 4);
     float4 *m_g = reinterpret_cast<float4 *>(a.m + (int64_t)b * a.Np);
     if (kSmem) {
-        for (int v = threadIdx.x; v < nv; v += kWalkThreads) s_m4[v] = ld_cg_v4(m_g + v);
+        for (int v = threadIdx.x; v < nv; v += kThreads) s_m4[v] = ld_cg_v4(m_g + v);
         __syncthreads();
     }
     const int slot = a.trace_slot ? a.trace_slot[b] : -1;
@@ -101,11 +105,11 @@ __global__ void __launch_bounds__(kWalkThreads, kMinBlocks) gram_walk_kernel(Gra
         float best = -INFINITY;
         int best_c = INT_MAX;
         const int pv = pending >> 2;
-        for (int v0 = threadIdx.x; v0 < nv; v0 += kBatch * kWalkThreads) {
+        for (int v0 = threadIdx.x; v0 < nv; v0 += kBatch * kThreads) {
             float4 gv[kBatch], mv[kBatch];
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
-                const int v = v0 + u * kWalkThreads;
+                const int v = v0 + u * kThreads;
                 gv[u] = v < nv ? ld_nc_v4(g4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                 if (!kSmem)
                     mv[u] = v < nv ? ld_cg_v4(m_g + v)
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(kWalkThreads, kMinBlocks) gram_walk_kernel(Gra
             }
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
-                const int v = v0 + u * kWalkThreads;
+                const int v = v0 + u * kThreads;
                 if (v >= nv) break;
                 if (kSmem) mv[u] = s_m4[v];
                 float m4[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
@@ -147,32 +151,28 @@ __global__ void __launch_bounds__(kWalkThreads, kMinBlocks) gram_walk_kernel(Gra
         for (int o = 16; o > 0; o >>= 1)
             take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
                         __shfl_xor_sync(0xffffffffu, best_c, o));
+        const int par = t & 1;
         if (lane == 0) {
-            red_v[warp] = best;
-            red_c[warp] = best_c;
+            red_v[par][warp] = best;
+            red_c[par][warp] = best_c;
         }
         __syncthreads();
-        if (warp == 0) {
-            best = lane < kWalkWarps ? red_v[lane] : -INFINITY;
-            best_c = lane < kWalkWarps ? red_c[lane] : INT_MAX;
+        best = lane < kWarps ? red_v[par][lane] : -INFINITY;
+        best_c = lane < kWarps ? red_c[par][lane] : INT_MAX;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
-                            __shfl_xor_sync(0xffffffffu, best_c, o));
-            if (lane == 0) {
-                const int w = best_c == INT_MAX ? -1 : best_c;
-                s_win = w;
-                a.picks[(int64_t)b * a.L + t] = w;
-                if (w < 0) atomicOr(a.status, kStatusNoWinner);
-            }
+        for (int o = 16; o > 0; o >>= 1)
+            take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
+                        __shfl_xor_sync(0xffffffffu, best_c, o));
+        const int w = best_c == INT_MAX ? -1 : best_c;
+        if (threadIdx.x == 0) {
+            a.picks[(int64_t)b * a.L + t] = w;
+            if (w < 0) atomicOr(a.status, kStatusNoWinner);
         }
-        __syncthreads();
-        const int w = s_win;
         if (slot >= 0) {
             // the running minima after this fold, before the pick is masked
             float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
             const float *src = kSmem ? reinterpret_cast<const float *>(s_m4) : a.m + (int64_t)b * a.Np;
-            for (int64_t c = threadIdx.x; c < a.N; c += kWalkThreads) dst[c] = src[c];
+            for (int64_t c = threadIdx.x; c < a.N; c += kThreads) dst[c] = src[c];
             __syncthreads();  // every copy read the pre-mask values
         }
         if (w < 0) break;
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kWalkThreads, kMinBlocks) gram_walk_kernel(Gra
     }
     __syncthreads();
     if (kSmem)
-        for (int v = threadIdx.x; v < nv; v += kWalkThreads) m_g[v] = s_m4[v];
+        for (int v = threadIdx.x; v < nv; v += kThreads) m_g[v] = s_m4[v];
 }
 
 }  // namespace
@@ -202,26 +202,29 @@ void launch_gram_walk_init(const GramWalkArgs &a, const int32_t *starts, const u
 
 static size_t gram_walk_smem_bytes(int64_t Np) { return (size_t)Np * sizeof(float); }
 
-template <bool kSmem, int kBatch, int kMinBlocks>
+template <bool kSmem, int kThreads, int kBatch, int kMinBlocks>
 cudaError_t launch_walk_variant(const GramWalkArgs &a, size_t smem, cudaStream_t st) {
-    auto kernel = gram_walk_kernel<kSmem, kBatch, kMinBlocks>;
+    auto kernel = gram_walk_kernel<kSmem, kThreads, kBatch, kMinBlocks>;
     if (smem > 48 * 1024) {
         cudaError_t err =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
     }
-    kernel<<<(unsigned)a.B, kWalkThreads, smem, st>>>(a);
+    kernel<<<(unsigned)a.B, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st) {
     const size_t smem = gram_walk_smem_bytes(a.Np);
     const int64_t nv = a.Np / 4;  // 16-byte vectors per row
-    if (smem > kGramWalkSmemMax) return launch_walk_variant<false, 6, 3>(a, 0, st);
-    if (nv <= 4 * kWalkThreads) return launch_walk_variant<true, 4, 6>(a, smem, st);
-    if (nv <= 6 * kWalkThreads) return launch_walk_variant<true, 6, 5>(a, smem, st);
-    if (nv <= 9 * kWalkThreads) return launch_walk_variant<true, 9, 4>(a, smem, st);
-    return launch_walk_variant<true, 12, 3>(a, smem, st);
+    if (smem > kGramWalkSmemMax) return launch_walk_variant<false, 256, 6, 3>(a, 0, st);
+    // one batch per row: as few threads as cover the row with at most 17
+    // vectors each, so that more CTAs (sequences) fit an SM
+    if (nv <= 4 * 128) return launch_walk_variant<true, 128, 4, 8>(a, smem, st);
+    if (nv <= 9 * 128) return launch_walk_variant<true, 128, 9, 6>(a, smem, st);
+    if (nv <= 17 * 128) return launch_walk_variant<true, 128, 17, 5>(a, smem, st);
+    if (nv <= 9 * 256) return launch_walk_variant<true, 256, 9, 4>(a, smem, st);
+    return launch_walk_variant<true, 256, 12, 3>(a, smem, st);
 }
 
 }  // namespace dseq

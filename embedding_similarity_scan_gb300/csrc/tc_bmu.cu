@@ -477,19 +477,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-// Work item of the resident-sample kernel: (sample block pair pb, a segment
-// [c0, c1) of one slice's chunks).  Items run slice-major, then by sample
-// block pair, then by segment, so consecutive items (dealt to neighbouring
-// CTA pairs) share their sample rows while those are in L2.  A segment may
-// be empty when a narrow last slice has fewer chunks than segments.
+// Work items of the resident-sample kernel.  A whole item is (sample block
+// pair pb, one codebook slice): the pair loads its sample rows once and runs
+// them against every chunk of the slice.  Whole items run slice-major, then
+// by sample block pair, and are dealt round-robin to the CTA pairs, so all
+// pairs sweep one L2-resident slice together and each sample block is read
+// once per slice.  The last, partial round of whole items would leave pairs
+// idle, so those items (the tail) are split into `tail_segs` segments of
+// their slice's chunks, dealt the same way.  A segment may be empty when a
+// narrow slice has fewer chunks than segments.
 struct BmuResSchedule {
-    int n_pb, n_chunk, slice_chunks, segs;
+    int n_pb, n_chunk, slice_chunks, tail_segs;
+    int64_t head;  // whole items before the tail
     __device__ __forceinline__ void decode(int64_t u, int &pb, int &c0, int &c1) const {
-        const int64_t per_slice = (int64_t)n_pb * segs;
-        const int sl = (int)(u / per_slice);
-        const int64_t rem = u - (int64_t)sl * per_slice;
-        pb = (int)(rem / segs);
-        const int sg = (int)(rem - (int64_t)pb * segs);
+        int64_t w = u;
+        int sg = 0, segs = 1;
+        if (u >= head) {
+            w = head + (u - head) / tail_segs;
+            sg = (int)((u - head) % tail_segs);
+            segs = tail_segs;
+        }
+        const int sl = (int)(w / n_pb);
+        pb = (int)(w - (int64_t)sl * n_pb);
         const int first = sl * slice_chunks;
         const int width = min(slice_chunks, n_chunk - first);
         const int len = (width + segs - 1) / segs;
@@ -505,7 +514,7 @@ struct BmuResSchedule {
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_bmu_resident_kernel(const __grid_constant__ CUtensorMap tmap_x,
                            const __grid_constant__ CUtensorMap tmap_w, const BmuArgs a,
-                           const TcPlan p, const int slice_chunks, const int segs) {
+                           const TcPlan p, const int slice_chunks, const int tail_segs) {
     using Cfg = BmuResCfg;
     constexpr int kSt = Cfg::kStages;
     constexpr uint32_t kSubB = Cfg::kSubB;
@@ -566,10 +575,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const BmuResSchedule sched{p.n_beta / 2, p.n_chunk, slice_chunks, segs};
-    const int64_t n_slices = (p.n_chunk + slice_chunks - 1) / slice_chunks;
-    const int64_t items = n_slices * sched.n_pb * segs;
     const int64_t first_item = blockIdx.x >> 1, item_stride = gridDim.x >> 1;
+    const int64_t n_slices = (p.n_chunk + slice_chunks - 1) / slice_chunks;
+    const int64_t whole = n_slices * (p.n_beta / 2);
+    const int64_t tail = whole % item_stride;
+    const BmuResSchedule sched{p.n_beta / 2, p.n_chunk, slice_chunks, tail_segs, whole - tail};
+    const int64_t items = (whole - tail) + tail * tail_segs;
     const uint32_t tile_n = (uint32_t)p.tile_n;
     const uint32_t b_rows = tile_n / 2;
     const uint32_t sub_b = b_rows * kKBlock * 2;
@@ -759,12 +770,13 @@ cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.pair && a.Dp <= BmuResCfg::kResKBlocks * kKBlock) {
-        // samples resident: enough segments per slice that every CTA pair
-        // gets about 32 items (the last ones then leave little imbalance)
+        // samples resident: whole (sample block pair, slice) items, and the
+        // last partial round of them split into enough segments that every
+        // CTA pair has one
         const int64_t n_slices = (p.n_chunk + slice - 1) / slice;
-        const int64_t n_pb = p.n_beta / 2;
-        int64_t segs = (32 * (int64_t)(p.grid / 2) + n_pb * n_slices - 1) / (n_pb * n_slices);
-        if (segs < 1) segs = 1;
+        const int64_t pairs = p.grid / 2;
+        const int64_t tail = (n_slices * (p.n_beta / 2)) % pairs;
+        int64_t segs = tail > 0 ? (pairs + tail - 1) / tail : 1;
         if (segs > slice) segs = slice;
         int sg = (int)segs;
         const size_t smem = BmuResCfg::kSmemBytes;
