@@ -640,7 +640,8 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
         walk_bytes = cfg.B * cfg.L * cfg.N * (4.0 + (4.0 if m_global else 0.0))
         walk_s = statistics.mean(st["walk_ns"] for st in stats) / 1e9
         gram_s = statistics.mean(st["gram_ns"] for st in stats) / 1e9
-        gflop = 2.0 * cfg.N * cfg.N * cfg.D
+        # the distinct dot products of the symmetric product: N (N + 1) / 2
+        gflop = 1.0 * cfg.N * (cfg.N + 1) * cfg.D
         roof = {"bound": "hbm", "achieved": walk_bytes / walk_s / 1e9, "peak": hbm_peak,
                 "unit": "GB/s", "frac": walk_bytes / walk_s / 1e9 / hbm_peak, "peak_kind": "copy",
                 "traffic": None if shrunk else _profiled_traffic("gram_walk_kernel", wl.name),
@@ -654,8 +655,9 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
                         "peak_kind": peak_kind, "frac_of_burst": gflop / gram_s / 1e12 / burst_peak,
                         "ms": gram_s * 1e3, "share_of_step": gram_s * 1e3 / (total_ms / args.steps),
                         "kernel": "tc_bmu_kernel (Gram store epilogue)",
-                        "note": ("achieved = 2*N*N*D / time of the operand split and the Gram "
-                                 f"product (CUDA events); {peak_note}")}
+                        "note": ("achieved = N*(N+1)*D (2*D FLOP for each of the N*(N+1)/2 "
+                                 "distinct entries of the symmetric G) / time of the operand split "
+                                 f"and the Gram product (CUDA events); {peak_note}")}
     line = {
         "metric": wl.metric, "value": value, "unit": wl.unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,

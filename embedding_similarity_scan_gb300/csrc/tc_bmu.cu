@@ -591,7 +591,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_normal();
+            // the codebook slice is reused by every sample block: keep it in
+            // L2.  A (sample block pair, slice) item is loaded by one CTA pair
+            // only (tail segments aside), so its sample rows are streamed
+            // with evict-first and do not displace the slice; the prefetch
+            // of the next item's rows uses the normal policy, to survive
+            // until that item loads them.
+            const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_normal(),
+                           stream = l2_policy_evict_first();
             uint32_t fills = 0, x_loads = 0;
             bool skip_copy = a.fault_skip_copy && blockIdx.x == 0;
             for (int64_t u = first_item; u < items && !*abort_flag; u += item_stride) {
@@ -608,7 +615,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int part = 0; part < kBmuPartsX; ++part)
                     for (int kb = 0; kb < kblocks; ++kb)
                         tma_load_2d_pair(s_x + (part * kblocks + kb) * kSubA, &tmap_x, fa,
-                                         part * a.Dp + kb * kKBlock, yx, once);
+                                         part * a.Dp + kb * kKBlock, yx, stream);
                 ++x_loads;
                 // bring the next item's sample rows (one contiguous block of
                 // the split samples) into L2 while this item runs, so its
