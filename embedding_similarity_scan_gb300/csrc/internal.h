@@ -247,7 +247,7 @@ struct BmuArgs {
 };
 void launch_bmu_keys_init(unsigned long long *keys, int64_t n, cudaStream_t st);
 void launch_ffma_bmu(const BmuArgs &a, cudaStream_t st);
-// slice_chunks: neuron chunks per L2 slice, 0 = about half of L2.
+// slice_chunks: neuron chunks per L2 slice, 0 = about 30 % of L2.
 cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
                           const CUtensorMap &tmap_w, int slice_chunks, cudaStream_t st);
 void launch_bmu_finalize(const BmuArgs &a, cudaStream_t st);

@@ -273,7 +273,7 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 the full scan); default.  0 = always scan the whole table.
  *   "slice"       bmu_search: neuron chunks per codebook slice, the part of
  *                 the codebook every CTA sweeps against all samples before
- *                 moving on; 0 = as many as fill about half of L2 (default).
+ *                 moving on; 0 = as many as fill about 30 % of L2 (default).
  *                 Any value gives the same results.
  *   "timeline"    1 = dseq_run records, per CTA and iteration of the
  *                 tensor-core kernel, device timestamps of its phases (read
