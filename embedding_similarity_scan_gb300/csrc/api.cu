@@ -797,7 +797,15 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         CUDA_TRY(cudaGetLastError());
         CUDA_TRY(launch_tc_gram(ga, gp, tx, tw, st));
         TRY(mid.start(st));
-        if (!resume) launch_gram_walk_init(wa, ctx->starts.as<int32_t>(), d_mask, st);
+        if (!resume) {
+            if ((size_t)Np * sizeof(float) <= kGramWalkSmemMax) {
+                // the walk sets up its running minima in shared memory
+                wa.starts = ctx->starts.as<int32_t>();
+                wa.mask = d_mask;
+            } else {
+                launch_gram_walk_init(wa, ctx->starts.as<int32_t>(), d_mask, st);
+            }
+        }
         CUDA_TRY(cudaGetLastError());
         CUDA_TRY(launch_gram_walk(wa, st));
         TRY(timer.stop(st));
@@ -805,7 +813,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         g_stats.gram = 1;
         g_stats.units = B;
         g_stats.grid = B;
-        g_stats.launches = resume ? 4 : 5;
+        g_stats.launches = (resume || (size_t)Np * sizeof(float) <= kGramWalkSmemMax) ? 4 : 5;
         {
             const int rs = read_status(ctx->status.as<int>(), st);
             if (rs != DSEQ_OK) {

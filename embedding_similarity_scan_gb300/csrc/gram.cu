@@ -93,12 +93,29 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nv = (int)(a.Np / 4);
     float4 *m_g = reinterpret_cast<float4 *>(a.m + (int64_t)b * a.Np);
-    if (kSmem) {
-        for (int v = threadIdx.x; v < nv; v += kThreads) s_m4[v] = ld_cg_v4(m_g + v);
+    int p;
+    if (kSmem && a.starts) {
+        // a fresh run: the running minima start here (+inf, -inf for masked
+        // rows, the start and the row padding)
+        p = a.starts[b];
+        for (int v = threadIdx.x; v < nv; v += kThreads) {
+            float m4[4];
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                const int64_t c = 4 * (int64_t)v + z;
+                m4[z] = (c < a.N && c != p && !(a.mask && a.mask[c])) ? INFINITY : -INFINITY;
+            }
+            s_m4[v] = make_float4(m4[0], m4[1], m4[2], m4[3]);
+        }
         __syncthreads();
+    } else {
+        if (kSmem) {
+            for (int v = threadIdx.x; v < nv; v += kThreads) s_m4[v] = ld_cg_v4(m_g + v);
+            __syncthreads();
+        }
+        p = a.cur[b];
     }
     const int slot = a.trace_slot ? a.trace_slot[b] : -1;
-    int p = a.cur[b];
     int pending = -1;  // the last pick, masked in the next fold
     for (int t = 0; t < a.L; ++t) {
         const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np);

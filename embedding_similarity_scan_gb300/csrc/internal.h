@@ -195,6 +195,11 @@ struct GramWalkArgs {
     int *status;
     int64_t N, Np;           // table rows; row stride of G and m (a multiple of 32)
     int B, L;
+    // a fresh run with the running minima in shared memory: the walk sets
+    // them up itself from the starts and the mask (nullptr: read m and cur,
+    // as left by gram_walk_init or an earlier run)
+    const int32_t *starts;
+    const uint8_t *mask;
 };
 // Largest shared-memory running-minimum row of the walk kernel (bytes):
 // longer rows stay in global memory.

@@ -238,6 +238,46 @@ __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, i
     return true;
 }
 
+// Work items of the Gram product: only the 256 x 256 tiles (row block pair
+// blk, column chunk j) with j >= blk, in slices of chunks (the codebook side
+// L2-resident for a slice); within a slice, by row block, then by chunk, so
+// consecutive items (dealt round-robin to the CTA pairs) share their row
+// block.  Enumerating only these tiles keeps the pairs' shares even.
+struct GramSchedule {
+    int n_chunk, slice_chunks;
+    __device__ __forceinline__ int64_t slice_items(int s0, int s1) const {
+        const int64_t w = s1 - s0;
+        return (int64_t)s0 * w + w * (w + 1) / 2;
+    }
+    __device__ __forceinline__ int64_t total() const {
+        int64_t t = 0;
+        for (int s0 = 0; s0 < n_chunk; s0 += slice_chunks) t += slice_items(s0, min(n_chunk, s0 + slice_chunks));
+        return t;
+    }
+    __device__ __forceinline__ void decode(int64_t u, int &blk, int &j) const {
+        int s0 = 0, s1 = min(n_chunk, slice_chunks);
+        while (s1 < n_chunk && u >= slice_items(s0, s1)) {
+            u -= slice_items(s0, s1);
+            s0 = s1;
+            s1 = min(n_chunk, s0 + slice_chunks);
+        }
+        const int w = s1 - s0;
+        if (u < (int64_t)s0 * w) {  // row blocks before the slice: every chunk of it
+            blk = (int)(u / w);
+            j = s0 + (int)(u - (int64_t)blk * w);
+            return;
+        }
+        u -= (int64_t)s0 * w;  // row blocks inside the slice: chunks from the diagonal on
+        int r = 0;
+        while (u >= w - r) {
+            u -= w - r;
+            ++r;
+        }
+        blk = s0 + r;
+        j = blk + (int)u;
+    }
+};
+
 struct BmuSchedule {
     int n_blocks, n_chunk, tile_n, slice_chunks;
     // work item u -> (sample block, or sample block pair, "beta"; neuron chunk j)
@@ -320,7 +360,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // pair mode: work items are (sample block pair, chunk); this CTA takes
     // sample block 2 * pair + rank and rows [rank * tile_n / 2, ...) of the chunk
     const BmuSchedule sched{kPair ? p.n_beta / 2 : p.n_beta, p.n_chunk, p.tile_n, slice_chunks};
-    const int64_t units = (int64_t)sched.n_blocks * p.n_chunk;
+    const GramSchedule gsched{p.n_chunk, slice_chunks};
+    const int64_t units = kGram ? gsched.total() : (int64_t)sched.n_blocks * p.n_chunk;
+    auto decode_item = [&](int64_t u, int &blk, int &j) {
+        if (kGram)
+            gsched.decode(u, blk, j);
+        else
+            sched.decode(u, blk, j);
+    };
     const int64_t first_item = kPair ? (blockIdx.x >> 1) : blockIdx.x;
     const int64_t item_stride = kPair ? (gridDim.x >> 1) : gridDim.x;
     const uint32_t tile_n = (uint32_t)p.tile_n;
@@ -341,8 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool skip_copy = a.fault_skip_copy && blockIdx.x == 0;
             for (int64_t u = first_item; u < units && !*abort_flag; u += item_stride) {
                 int blk, j;
-                sched.decode(u, blk, j);
-                if (kGram && j < blk) continue;  // the mirror of an item computed
+                decode_item(u, blk, j);
                 const int beta = kPair ? 2 * blk + (int)rank : blk;
                 const int yx = beta * kUnitRows, yw = j * (int)tile_n + (int)(rank * b_rows);
                 for (int kb = 0; kb < kblocks; ++kb) {
@@ -394,11 +440,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0 && leader) {
             uint32_t consumed = 0, acc_uses = 0;
             for (int64_t u = first_item; u < units && !*abort_flag; u += item_stride) {
-                if (kGram) {
-                    int blk, j;
-                    sched.decode(u, blk, j);
-                    if (j < blk) continue;
-                }
                 const uint32_t buf = acc_uses & 1u, apar = (acc_uses >> 1) & 1u;
                 if (!mbar_wait_bounded(&acc_empty[buf], apar ^ 1u, abort_flag, a.status, tmo,
                                        kStatusPipeTimeout))
@@ -448,10 +489,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t acc_empty_leader0 = kPair ? mapa_shared(smem_u32(&acc_empty[0]), 0) : 0u;
         for (int64_t u = first_item; u < units; u += item_stride) {
             int blk, j;
-            sched.decode(u, blk, j);
+            decode_item(u, blk, j);
             const int beta = kPair ? 2 * blk + (int)rank : blk;
             if (kGram) {
-                if (j < blk) continue;
                 // off the diagonal the tile also fills its mirror image
                 if (!gram_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses,
                                                acc_full, acc_empty, acc_empty_leader0, abort_flag,
@@ -816,12 +856,12 @@ cudaError_t launch_tc_bmu(const BmuArgs &a, const TcPlan &p, const CUtensorMap &
 
 cudaError_t launch_tc_gram(const BmuArgs &a, const TcPlan &p, const CUtensorMap &tmap_x,
                            const CUtensorMap &tmap_w, cudaStream_t st) {
-    // the whole codebook side is one slice when it fits half of L2
+    // slices of the codebook side as for the BMU search (30 % of L2)
     int dev = 0, l2 = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
     const double row_bytes = (double)kBmuPartsW * a.Dp * 2.0;
-    int slice = (int)((0.5 * (double)l2) / (row_bytes * p.tile_n));
+    int slice = (int)((0.3 * (double)l2) / (row_bytes * p.tile_n));
     if (slice < 1) slice = 1;
     if (slice > p.n_chunk) slice = p.n_chunk;
     BmuArgs aa = a;
