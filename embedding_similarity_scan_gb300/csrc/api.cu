@@ -26,7 +26,7 @@ constexpr int kNoShift = 1 << 30;
 
 struct Stats {
     int64_t units = 0, tile_n = 0, tile_n2 = 0, n_wide = 0, grid = 0, launches = 0, kernel_ns = 0,
-            update_ns = 0, gram = 0, gram_ns = 0, walk_ns = 0;
+            update_ns = 0, gram = 0, gram_ns = 0, walk_ns = 0, walk = 0;
 };
 thread_local Stats g_stats;
 
@@ -82,6 +82,7 @@ struct Options {
     int64_t compact = 1;
     int64_t isolate_epilogue = 0;
     int64_t gram = 2;
+    int64_t walk = 0;
 };
 
 // Test and measurement options (fault injection, the epilogue-isolated
@@ -140,6 +141,9 @@ int set_opt(Options &o, const char *name, int64_t v) {
     } else if (n == "compact") {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "compact must be 0 or 1");
         o.compact = v;
+    } else if (n == "walk") {
+        if (v < 0 || v > 3) return fail(DSEQ_EINVAL, "walk must be 0 (chosen), 1 (shared memory), 2 (cluster) or 3 (global memory)");
+        o.walk = v;
     } else if (n == "gram") {
         if (v < 0 || v > 2) return fail(DSEQ_EINVAL, "gram must be 0 (never), 1 (always) or 2 (auto)");
         o.gram = v;
@@ -171,6 +175,7 @@ int64_t get_opt(const Options &o, const char *name) {
     if (n == "resume") return o.resume;
     if (n == "isolate_epilogue") return o.isolate_epilogue;
     if (n == "gram") return o.gram;
+    if (n == "walk") return o.walk;
     return -1;
 }
 
@@ -476,6 +481,7 @@ struct dseq_ctx {
     int64_t state_sig = -1;   // engine / pair / storage / criterion of that run
     TcPlan state_plan{};
     bool state_gram = false;  // the last run used the Gram engine
+    int state_walk = 0;       // and kept its running minima there (gram_walk_place)
     std::vector<int32_t> state_starts;
     std::vector<uint8_t> state_mask;
     ~dseq_ctx() {
@@ -506,6 +512,7 @@ int64_t dseq_last_stat(const char *name) {
     if (n == "gram") return g_stats.gram;
     if (n == "gram_ns") return g_stats.gram_ns;
     if (n == "walk_ns") return g_stats.walk_ns;
+    if (n == "walk") return g_stats.walk;
     return -1;
 }
 
@@ -606,7 +613,9 @@ static bool gram_pays(int64_t N, int64_t Dp, int64_t B, int64_t L, size_t free_b
                         (256.0 * 1024 * 1024);
     if (need > 0.8 * (double)free_bytes) return false;
     const double rt = 5.0e14, rb = 5.5e12;
-    const bool smem = (size_t)Np * sizeof(float) <= kGramWalkSmemMax;
+    // running minima in shared memory (one CTA or a cluster of 8) cost no
+    // traffic; in global memory they are read and written every iteration
+    const bool smem = gram_walk_place(Np) != 3;
     const double t_gram = 2.0 * N * Np * Dp / rt + N * Np * 4.0 / rb +
                           (double)L * B * Np * 4.0 * (smem ? 1.0 : 2.2) / rb + 3.0e-5;
     const double t_scan = 2.0 * B * N * Dp * (double)L / rt;
@@ -739,6 +748,14 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     if (use_gram) {
         // ---- Gram engine: G = E E^T on the tensor cores, then the walk ----
         const int64_t Np = round_up(N, 32);
+        // where the running minima live: chosen from the row length, or the
+        // "walk" option (a one-CTA row must fit its shared memory)
+        int place = ctx->opt.walk > 0 ? (int)ctx->opt.walk : gram_walk_place(Np);
+        if (resume) place = ctx->state_walk;
+        if (place == 1 && (size_t)Np * sizeof(float) > kGramWalkSmemMax)
+            return fail(DSEQ_EINVAL, "walk=1: a row of %lld running minima does not fit one CTA's shared memory", (long long)Np);
+        if (place == 2 && (size_t)Np * sizeof(float) > kGramWalkClusterMax)
+            return fail(DSEQ_EINVAL, "walk=2: a row of %lld running minima does not fit a cluster's shared memory", (long long)Np);
         const int Dp = ctx->Dp;
         TRY(ctx->gram.ensure((size_t)N * Np * sizeof(float)));
         TRY(ctx->g_xs.ensure((size_t)N * kBmuPartsX * Dp * sizeof(__half)));
@@ -787,6 +804,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         wa.Np = Np;
         wa.B = B;
         wa.L = L;
+        wa.place = place;
+        ctx->state_walk = place;
         EventTimer mid;
         TRY(timer.start(st));
         // the table's unit rows, split twice (the sample and codebook sides)
@@ -798,7 +817,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         CUDA_TRY(launch_tc_gram(ga, gp, tx, tw, st));
         TRY(mid.start(st));
         if (!resume) {
-            if ((size_t)Np * sizeof(float) <= kGramWalkSmemMax) {
+            if (place != 3) {
                 // the walk sets up its running minima in shared memory
                 wa.starts = ctx->starts.as<int32_t>();
                 wa.mask = d_mask;
@@ -811,9 +830,10 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         TRY(timer.stop(st));
         TRY(mid.stop(st));
         g_stats.gram = 1;
+        g_stats.walk = place;
         g_stats.units = B;
         g_stats.grid = B;
-        g_stats.launches = (resume || (size_t)Np * sizeof(float) <= kGramWalkSmemMax) ? 4 : 5;
+        g_stats.launches = (resume || place != 3) ? 4 : 5;
         {
             const int rs = read_status(ctx->status.as<int>(), st);
             if (rs != DSEQ_OK) {

@@ -210,6 +210,158 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
         for (int v = threadIdx.x; v < nv; v += kThreads) m_g[v] = s_m4[v];
 }
 
+// The walk for tables whose running-minimum row does not fit one CTA's
+// shared memory: a cluster of kC CTAs walks one sequence, each CTA holding a
+// contiguous kC-th of the row of running minima in its shared memory and
+// streaming the same part of each row G[p][.].  Per iteration each CTA
+// reduces its part to one (max, lowest column) candidate, writes it into a
+// slot of every CTA of the cluster (distributed shared memory), and after
+// one cluster barrier every CTA reduces the kC candidates to the same
+// winner.  The slots alternate between iterations, so one cluster barrier
+// per iteration suffices (no CTA can reach the slots of iteration t + 2
+// before all have passed the barrier of t + 1).  Only G is streamed: the
+// running minima never leave the cluster's shared memory during the walk.
+template <int kC, int kThreads, int kBatch, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel(GramWalkArgs a) {
+    constexpr int kWarps = kThreads / 32;
+    extern __shared__ float4 s_m4[];
+    __shared__ float red_v[kWarps];
+    __shared__ int red_c[kWarps];
+    __shared__ float slot_v[2][kC];
+    __shared__ int slot_c[2][kC];
+    const int rank = (int)cluster_ctarank();
+    const int b = blockIdx.x / kC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nv = (int)(a.Np / 4);
+    const int wv = (nv + kC - 1) / kC;  // vectors per CTA
+    const int v0 = rank * wv, v1 = min(nv, v0 + wv);
+    const int my_v = v1 - v0;
+    // the launch must be the shape the kernel is written for (it addresses
+    // the other CTAs' shared memory): otherwise report and leave uniformly
+    if (cluster_nctarank() != (uint32_t)kC || blockDim.x != kThreads || gridDim.x != (unsigned)(a.B * kC)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusInternal);
+        return;
+    }
+    float4 *m_g = reinterpret_cast<float4 *>(a.m + (int64_t)b * a.Np);
+    int p;
+    if (a.starts) {
+        // a fresh run: the running minima start here
+        p = a.starts[b];
+        for (int v = threadIdx.x; v < my_v; v += kThreads) {
+            float m4[4];
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                const int64_t c = 4 * (int64_t)(v0 + v) + z;
+                m4[z] = (c < a.N && c != p && !(a.mask && a.mask[c])) ? INFINITY : -INFINITY;
+            }
+            s_m4[v] = make_float4(m4[0], m4[1], m4[2], m4[3]);
+        }
+    } else {
+        for (int v = threadIdx.x; v < my_v; v += kThreads) s_m4[v] = ld_cg_v4(m_g + v0 + v);
+        p = a.cur[b];
+    }
+    // every CTA's shared memory set up before any remote write
+    cluster_sync_all();
+    const int slot = a.trace_slot ? a.trace_slot[b] : -1;
+    int pending = -1;
+    for (int t = 0; t < a.L; ++t) {
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np) + v0;
+        float best = -INFINITY;
+        int best_c = INT_MAX;
+        const int pv = pending >= 0 ? (pending >> 2) - v0 : -1;
+        for (int w0 = threadIdx.x; w0 < my_v; w0 += kBatch * kThreads) {
+            float4 gv[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int v = w0 + u * kThreads;
+                gv[u] = v < my_v ? ld_nc_v4(g4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int v = w0 + u * kThreads;
+                if (v >= my_v) break;
+                const float4 mv = s_m4[v];
+                float m4[4] = {mv.x, mv.y, mv.z, mv.w};
+                const float g[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+                bool changed = false;
+                if (v == pv) {
+                    m4[pending & 3] = -INFINITY;
+                    changed = true;
+                }
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const float d = fmaf(g[z], -1.0f, 1.0f);
+                    const float nm = fminf(m4[z], d);
+                    changed |= nm != m4[z];
+                    m4[z] = nm;
+                    if (nm > best) {
+                        best = nm;
+                        best_c = 4 * (v0 + v) + z;
+                    }
+                }
+                if (changed) s_m4[v] = make_float4(m4[0], m4[1], m4[2], m4[3]);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
+                        __shfl_xor_sync(0xffffffffu, best_c, o));
+        if (lane == 0) {
+            red_v[warp] = best;
+            red_c[warp] = best_c;
+        }
+        __syncthreads();
+        const int par = t & 1;
+        if (threadIdx.x < 32) {
+            best = lane < kWarps ? red_v[lane] : -INFINITY;
+            best_c = lane < kWarps ? red_c[lane] : INT_MAX;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
+                            __shfl_xor_sync(0xffffffffu, best_c, o));
+            // this CTA's candidate into slot [par][rank] of every CTA (lane r
+            // writes CTA r's copy)
+            if (lane < kC) {
+                const uint32_t av = mapa_shared(smem_u32(&slot_v[par][rank]), (uint32_t)lane);
+                const uint32_t ac = mapa_shared(smem_u32(&slot_c[par][rank]), (uint32_t)lane);
+                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(av), "f"(best) : "memory");
+                asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(ac), "r"(best_c) : "memory");
+            }
+        }
+        cluster_sync_all();
+        best = -INFINITY;
+        best_c = INT_MAX;
+#pragma unroll
+        for (int r = 0; r < kC; ++r) take_better(best, best_c, slot_v[par][r], slot_c[par][r]);
+        const int w = best_c == INT_MAX ? -1 : best_c;
+        if (rank == 0 && threadIdx.x == 0) {
+            a.picks[(int64_t)b * a.L + t] = w;
+            if (w < 0) atomicOr(a.status, kStatusNoWinner);
+        }
+        if (slot >= 0) {
+            // this CTA's part of the running minima after the fold, before the
+            // pick is masked
+            float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
+            const float *src = reinterpret_cast<const float *>(s_m4);
+            for (int64_t c = threadIdx.x; c < 4 * (int64_t)my_v; c += kThreads)
+                if (4 * (int64_t)v0 + c < a.N) dst[4 * (int64_t)v0 + c] = src[c];
+            __syncthreads();
+        }
+        if (w < 0) break;
+        pending = w;
+        p = w;
+    }
+    // the state left for a resumed run: the last pick masked, minima in a.m
+    __syncthreads();
+    if (threadIdx.x == 0 && pending >= 0 && (pending >> 2) >= v0 && (pending >> 2) < v1)
+        reinterpret_cast<float *>(s_m4)[pending - 4 * v0] = -INFINITY;
+    if (rank == 0 && threadIdx.x == 0) a.cur[b] = p;
+    __syncthreads();
+    for (int v = threadIdx.x; v < my_v; v += kThreads) m_g[v0 + v] = s_m4[v];
+    // no CTA leaves while another may still write into its slots
+    cluster_sync_all();
+}
+
 }  // namespace
 
 void launch_gram_walk_init(const GramWalkArgs &a, const int32_t *starts, const uint8_t *mask,
@@ -231,10 +383,41 @@ cudaError_t launch_walk_variant(const GramWalkArgs &a, size_t smem, cudaStream_t
     return cudaGetLastError();
 }
 
+template <int kC, int kThreads, int kBatch, int kMinBlocks>
+cudaError_t launch_cluster_variant(const GramWalkArgs &a, cudaStream_t st) {
+    const int64_t nv = a.Np / 4;
+    const size_t smem = (size_t)((nv + kC - 1) / kC) * sizeof(float4);
+    auto kernel = gram_walk_cluster_kernel<kC, kThreads, kBatch, kMinBlocks>;
+    if ((int64_t)a.B * kC > INT_MAX) return cudaErrorInvalidConfiguration;
+    cudaError_t err =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.B * kC));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+int gram_walk_place(int64_t Np) {
+    const size_t row = (size_t)Np * sizeof(float);
+    return row <= kGramWalkSmemMax ? 1 : row <= kGramWalkClusterMax ? 2 : 3;
+}
+
 cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st) {
     const size_t smem = gram_walk_smem_bytes(a.Np);
     const int64_t nv = a.Np / 4;  // 16-byte vectors per row
-    if (smem > kGramWalkSmemMax) return launch_walk_variant<false, 256, 6, 3>(a, 0, st);
+    // rows of running minima spread over a cluster of 8 CTAs
+    if (a.place == 2) return launch_cluster_variant<8, 256, 16, 2>(a, st);
+    if (a.place == 3) return launch_walk_variant<false, 256, 6, 3>(a, 0, st);
     // one batch per row: as few threads as cover the row with at most 17
     // vectors each, so that more CTAs (sequences) fit an SM
     if (nv <= 4 * 128) return launch_walk_variant<true, 128, 4, 8>(a, smem, st);

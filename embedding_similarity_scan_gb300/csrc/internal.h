@@ -200,10 +200,17 @@ struct GramWalkArgs {
     // as left by gram_walk_init or an earlier run)
     const int32_t *starts;
     const uint8_t *mask;
+    // where the running minima live during the walk: 1 one CTA's shared
+    // memory, 2 a cluster's, 3 global memory (gram_walk_place)
+    int place;
 };
-// Largest shared-memory running-minimum row of the walk kernel (bytes):
-// longer rows stay in global memory.
+// The default place of a walk's running minima for rows of Np floats.
+int gram_walk_place(int64_t Np);
+// Largest shared-memory running-minimum row of the walk kernel (bytes);
+// longer rows, up to kGramWalkClusterMax, are spread over the shared memory
+// of a cluster of 8 CTAs; longer still, they stay in global memory.
 constexpr size_t kGramWalkSmemMax = 96 * 1024;
+constexpr size_t kGramWalkClusterMax = 8 * 96 * 1024;
 // m <- +inf, or -inf for masked rows, the start and the row padding; cur <- starts.
 void launch_gram_walk_init(const GramWalkArgs &a, const int32_t *starts, const uint8_t *mask,
                            cudaStream_t st);

@@ -222,6 +222,32 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  * bmu_search and by contexts created afterwards; otherwise the setting
  * applies to that context only.  Names:
  *   "engine"      0 = tensor-core path (default), 1 = FP32 FFMA path.
+ *   "gram"        diversity path: how dseq_run finds the distances.
+ *                 0 = per iteration, the newest picks against the whole
+ *                 table on the tensor cores, fused with the fold and the
+ *                 argmax (the scan); 1 = the table's Gram matrix G = E E^T
+ *                 of the unit rows once per run on the tensor cores (N x Np
+ *                 float32, Np = N rounded up to 32; the tiles on and above
+ *                 the diagonal are computed and every entry is stored at
+ *                 (i, c) and (c, i), so G is exactly symmetric), then one CTA
+ *                 (or cluster) per sequence reads row G[p] of its newest
+ *                 pick p every iteration, distance 1 - G[p][c]; 2 = 1 where
+ *                 a cost model (the product plus B * L row reads against B *
+ *                 L table scans) says it is cheaper and G fits in 80 % of
+ *                 the free device memory, else 0 (default).  Both give the
+ *                 same picks up to fp32 rounding of the distances, with the
+ *                 same tie-break.  Only the max-min criterion on split
+ *                 storage with the tensor-core engine (and neither timeline
+ *                 nor isolate_epilogue) uses G; other settings run the scan.
+ *                 A resumed run stays on the engine of the run it resumes.
+ *   "walk"        Gram engine: where each sequence keeps its running minima
+ *                 while it reads G.  0 = chosen from N (default): one CTA's
+ *                 shared memory up to 96 KB of minima (N <= 24576), spread
+ *                 over a cluster of 8 CTAs up to 768 KB (N <= 196608),
+ *                 global memory beyond; 1, 2, 3 force shared memory,
+ *                 cluster, global memory (DSEQ_EINVAL from dseq_run when
+ *                 the row does not fit the place asked for).  Every place
+ *                 gives identical picks.
  *   "tile_n"      candidate (or neuron) columns per work unit, a multiple of
  *                 32 in [32, 256]; 0 = chosen from the shape (default).
  *                 Alone it fixes every diversity chunk to that width.
@@ -310,7 +336,12 @@ int64_t dseq_get_option(dseq_ctx *ctx, const char *name);
  *   "grid"         CTAs launched,
  *   "launches"     kernels launched by the call,
  *   "kernel_ns"    device time of the main kernel (CUDA events; 0 if unknown),
- *   "update_ns"    device time of the SOM update's kernels (0 if none ran). */
+ *   "update_ns"    device time of the SOM update's kernels (0 if none ran),
+ *   "gram"         1 if the last dseq_run used the Gram engine, else 0,
+ *   "gram_ns"      its Gram product's device time (operand split included),
+ *   "walk_ns"      its walk's device time,
+ *   "walk"         where that walk kept its running minima (1 shared
+ *                  memory, 2 cluster, 3 global memory). */
 int64_t dseq_last_stat(const char *name);
 
 /* Message of the last error on the calling thread ("" if none). */

@@ -79,12 +79,18 @@ def test_options(lib):
     with pytest.raises(es.DseqError) as ei:
         es.dseq_set_option("nonsense", 1)
     assert ei.value.code == es.DSEQ_EINVAL
-    for bad in (("tile_n", 48), ("tile_n", 512), ("engine", 2), ("timeout_ms", 0)):
+    assert es.dseq_get_option("gram") == 2 and es.dseq_get_option("walk") == 0
+    for bad in (("tile_n", 48), ("tile_n", 512), ("engine", 2), ("timeout_ms", 0),
+                ("gram", 3), ("walk", 4), ("walk", -1)):
         with pytest.raises(es.DseqError):
             es.dseq_set_option(*bad)
     es.dseq_set_option("tile_n", 96)
     assert es.dseq_get_option("tile_n") == 96
     es.dseq_set_option("tile_n", 0)
+    es.dseq_set_option("walk", 2)
+    assert es.dseq_get_option("walk") == 2
+    es.dseq_set_option("walk", 0)
+    assert es.dseq_last_stat("walk") == 0 and es.dseq_last_stat("gram") == 0
     assert es.dseq_last_stat("units") == 0 and es.dseq_last_stat("bogus") == -1
 
 

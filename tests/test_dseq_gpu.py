@@ -34,7 +34,7 @@ def _reset_options(es):
     for name, v in (("engine", 0), ("tile_n", 0), ("tile_n2", 0), ("grid", 0), ("timeout_ms", 10000),
                     ("fault_skip_arrive", 0), ("pair", DEFAULT_PAIR), ("storage", 0),
                     ("criterion", 0), ("resume", 0), ("compact", 1), ("isolate_epilogue", 0),
-                    ("gram", 2)):
+                    ("gram", 2), ("walk", 0)):
         es.dseq_set_option(name, v)
 
 
@@ -489,10 +489,11 @@ def test_centroid_fp16_storage_full_size_and_agreement(es):
 # give exactly the picks of one long call.
 
 
-@pytest.mark.parametrize("engine,pair,criterion,storage,gram",
-                         [(0, 1, 0, 0, 0), (0, 0, 0, 0, 0), (1, 0, 0, 0, 0), (0, 1, 1, 0, 0),
-                          (0, 1, 0, 1, 0), (0, 1, 1, 1, 0), (0, 1, 0, 0, 1)])
-def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion, storage, gram):
+@pytest.mark.parametrize("engine,pair,criterion,storage,gram,walk",
+                         [(0, 1, 0, 0, 0, 0), (0, 0, 0, 0, 0, 0), (1, 0, 0, 0, 0, 0),
+                          (0, 1, 1, 0, 0, 0), (0, 1, 0, 1, 0, 0), (0, 1, 1, 1, 0, 0),
+                          (0, 1, 0, 0, 1, 1), (0, 1, 0, 0, 1, 2), (0, 1, 0, 0, 1, 3)])
+def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion, storage, gram, walk):
     N, D, B = 300, 40, 9
     E = workloads.clustered_table(N, D, n_centres=6, seed=12)
     starts = workloads.starts(N, B, seed=12)
@@ -508,6 +509,7 @@ def test_resume_in_chunks_equals_one_call(es, engine, pair, criterion, storage, 
     es.dseq_set_option("criterion", criterion)
     es.dseq_set_option("storage", storage)
     es.dseq_set_option("gram", gram)
+    es.dseq_set_option("walk", walk)
     ctx = es.dseq_create(torch.from_numpy(E).cuda())
     try:
         st = torch.from_numpy(starts).cuda()
@@ -696,17 +698,62 @@ def test_gram_extreme_shapes_teacher_forced(es, case):
     check_dseq_teacher_forced(E, starts, None, picks, trace, tr)
 
 
-def test_gram_running_minima_in_global_memory(es):
-    """A table whose running-minimum rows are too long for shared memory:
-    the walk keeps them in global memory (masked rows, ragged N)."""
+def _walk_run(es, E, starts, L, mask, tr, walk):
+    es.dseq_set_option("walk", walk)
+    picks, trace = _run(es, E, starts, L, mask, tr, gram=1)
+    assert es.dseq_last_stat("gram") == 1
+    return picks, trace, es.dseq_last_stat("walk")
+
+
+def test_gram_running_minima_too_long_for_one_cta(es):
+    """A table whose running-minimum rows (120 KB) are too long for one CTA's
+    shared memory (masked rows, ragged N): by default the walk spreads them
+    over a cluster of CTAs; in global memory (walk = 3) it gives the same
+    picks and minima, bit for bit; one CTA (walk = 1) is refused."""
     N, D, B, L = 30011, 48, 37, 10
     E = workloads.clustered_table(N, D, n_centres=20, seed=31)
     starts = workloads.starts(N, B, seed=31)
     mask = (np.random.default_rng(31).random(N) < 0.05).astype(np.uint8)
     tr = np.arange(B, dtype=np.int32)
-    picks, trace = _run(es, E, starts, L, mask, tr, gram=1)
+    picks, trace, place = _walk_run(es, E, starts, L, mask, tr, 0)
+    assert place == 2
     check_picks_valid(starts, mask, picks, N)
     check_dseq_teacher_forced(E, starts, mask, picks, trace, tr)
+    picks_g, trace_g, place = _walk_run(es, E, starts, L, mask, tr, 3)
+    assert place == 3
+    assert np.array_equal(picks_g, picks)
+    assert np.array_equal(trace_g, trace)
+    with pytest.raises(es.DseqError):
+        _walk_run(es, E, starts, L, mask, tr, 1)
+
+
+@pytest.mark.parametrize("case", [(1000, 96, 200, 16), (3001, 40, 29, 12), (37, 5, 9, 20),
+                                  (24576, 16, 6, 9), (24600, 16, 6, 9)],
+                         ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
+def test_gram_walk_places_identical(es, case):
+    """The three places of the running minima (one CTA's shared memory, a
+    cluster's, global memory) run the same arithmetic in the same order per
+    candidate: identical picks and traced minima, and the oracle's.  Rows
+    shorter than the cluster (N = 37: some CTAs hold no candidate) and the
+    largest one-CTA row (N = 24576) included."""
+    N, D, B, L = case
+    E = workloads.gaussian_table(N, D, seed=N + 7)
+    starts = workloads.starts(N, B, seed=N + 7)
+    mask = (np.random.default_rng(N).random(N) < 0.03).astype(np.uint8)
+    mask[starts[:2]] = 1
+    tr = np.unique(np.array([0, B // 2, B - 1], np.int32))
+    out = {}
+    for walk in (1, 2, 3):
+        if walk == 1 and 4 * ((N + 31) // 32 * 32) > 96 * 1024:
+            continue
+        out[walk] = _walk_run(es, E, starts, L, mask, tr, walk)
+        assert out[walk][2] == walk
+    ref = out[min(out)]
+    check_picks_valid(starts, mask, ref[0], N)
+    check_dseq_teacher_forced(E, starts, mask, ref[0], ref[1], tr)
+    for walk, (picks, trace, _) in out.items():
+        assert np.array_equal(picks, ref[0]), f"walk={walk}"
+        assert np.array_equal(trace, ref[1]), f"walk={walk}"
 
 
 def test_gram_worked_examples(es):
