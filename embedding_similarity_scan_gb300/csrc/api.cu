@@ -805,6 +805,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         wa.B = B;
         wa.L = L;
         wa.place = place;
+        wa.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
         ctx->state_walk = place;
         EventTimer mid;
         TRY(timer.start(st));

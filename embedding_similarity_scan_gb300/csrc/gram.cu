@@ -15,14 +15,15 @@
 // the walk needs no grid-wide synchronisation at all.
 //
 // gram_walk_kernel: one CTA per sequence, all L iterations.  Per iteration
-// the CTA streams G[p][0 .. N) (16-byte loads, several in flight per thread),
-// folds d = 1 - g into the running minimum (kept in shared memory when a row
-// of it fits, else in global memory), and reduces (max, lowest index) over
-// the block: per thread in ascending column order with a strict '>', then
-// warp shuffles and one shared-memory stage with the index as tie-break.
-// The winner is masked by the thread that owns its column in the next
-// iteration's fold, so the only block-wide barriers are the two of the
-// reduction.
+// the CTA streams G[p][0 .. N) (16-byte loads, one batch in flight per
+// thread), folds d = 1 - g into the running minimum (kept in shared memory
+// when a row of it fits, else in global memory), and reduces (max, lowest
+// index) over the block: per thread in ascending column order, then two
+// redux instructions per warp and one shared-memory stage.  The winner is
+// masked by the thread that owns its column in the next iteration's fold, so
+// the reduction's one barrier is the only block-wide barrier per iteration.
+// gram_walk_cluster_kernel: the same walk for rows of running minima longer
+// than one CTA's shared memory, spread over a cluster of CTAs.
 #include <climits>
 #include <math.h>
 
@@ -49,12 +50,46 @@ __device__ __forceinline__ float4 ld_cg_v4(const float4 *p) {
     return v;
 }
 
-// (value, index) max with the lower index on equal values
-__device__ __forceinline__ void take_better(float &v, int &c, float ov, int oc) {
-    if (ov > v || (ov == v && oc < c)) {
-        v = ov;
-        c = oc;
+// A running minimum and a candidate are ranked by an ordered 32-bit key of
+// the value (the float's bits mapped so that unsigned order is float order,
+// -inf lowest) and then by the lower column: every reduction is a max of the
+// key followed by a min of the column among the lanes that hold that max,
+// two warp-wide redux instructions.  A thread or CTA without a candidate
+// holds (-inf, INT_MAX), which never wins; INT_MAX as the winner means that
+// every candidate is masked.
+__device__ __forceinline__ uint32_t ord_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ void warp_argmax(uint32_t &key, uint32_t &col) {
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+    col = __reduce_min_sync(0xffffffffu, key == mx ? col : 0xffffffffu);
+    key = mx;
+}
+
+// The fold of one 16-byte vector (four candidates) of G[p] into the running
+// minima: m <- min(m, 1 - g).
+__device__ __forceinline__ float4 fold4(float4 m, float4 g) {
+    return make_float4(fminf(m.x, fmaf(g.x, -1.0f, 1.0f)), fminf(m.y, fmaf(g.y, -1.0f, 1.0f)),
+                       fminf(m.z, fmaf(g.z, -1.0f, 1.0f)), fminf(m.w, fmaf(g.w, -1.0f, 1.0f)));
+}
+// The thread's running (max, column) over the vectors it folds, in
+// ascending column order: a vector's max is compared once, and only when it
+// beats the best so far is its lowest column holding that max looked up.
+__device__ __forceinline__ void track4(float4 nm, int c0, float &best, int &best_c) {
+    const float mx = fmaxf(fmaxf(nm.x, nm.y), fmaxf(nm.z, nm.w));
+    if (mx > best) {
+        best = mx;
+        best_c = c0 + (nm.x == mx ? 0 : nm.y == mx ? 1 : nm.z == mx ? 2 : 3);
     }
+}
+// The newest pick, masked in the fold of the vector that holds it.
+__device__ __forceinline__ float4 mask_lane(float4 m, int z) {
+    if (z == 0) m.x = -INFINITY;
+    else if (z == 1) m.y = -INFINITY;
+    else if (z == 2) m.z = -INFINITY;
+    else m.w = -INFINITY;
+    return m;
 }
 
 __global__ void gram_walk_init_kernel(GramWalkArgs a, const int32_t *__restrict__ starts,
@@ -71,42 +106,47 @@ __global__ void gram_walk_init_kernel(GramWalkArgs a, const int32_t *__restrict_
         a.cur[b] = starts[b];
 }
 
+// Running minima of columns [4 v0, 4 v1) at the start of a fresh run: +inf,
+// -inf for masked rows, the start and the row padding.
+__device__ __forceinline__ void init_minima(float4 *s_m4, int v0, int v1, int64_t N, int p,
+                                            const uint8_t *mask, int kThreads) {
+    for (int v = v0 + (int)threadIdx.x; v < v1; v += kThreads) {
+        float m4[4];
+#pragma unroll
+        for (int z = 0; z < 4; ++z) {
+            const int64_t c = 4 * (int64_t)v + z;
+            m4[z] = (c < N && c != p && !(mask && mask[c])) ? INFINITY : -INFINITY;
+        }
+        s_m4[v - v0] = make_float4(m4[0], m4[1], m4[2], m4[3]);
+    }
+}
+
 // kSmem: the sequence's running minima live in shared memory for the whole
 // walk (loaded from and stored back to a.m around it); otherwise they are
-// read and written in global memory every iteration.
+// read in global memory every iteration and written back where they fell.
 // kBatch: 16-byte vectors of the G row each thread has in flight at once;
 // the host picks it so that one batch covers a whole row where it can (one
 // round trip to memory per iteration).
 // The block argmax takes one barrier per iteration: every warp publishes its
-// (max, lowest index) in one of two alternating slots, and after the barrier
-// every warp reduces all slots itself, so all threads know the winner
-// without a second barrier (a warp cannot reach the slots of iteration t + 2
-// before every warp has passed the barrier of iteration t + 1).
+// (key, column) in one of two alternating slots, and after the barrier every
+// warp reduces all slots itself, so all threads know the winner without a
+// second barrier (a warp cannot reach the slots of iteration t + 2 before
+// every warp has passed the barrier of iteration t + 1).
 template <bool kSmem, int kThreads, int kBatch, int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWalkArgs a) {
     constexpr int kWarps = kThreads / 32;
     static_assert(kWarps <= 32, "one warp reduces the per-warp slots");
     extern __shared__ float4 s_m4[];
-    __shared__ float red_v[2][kWarps];
-    __shared__ int red_c[2][kWarps];
+    __shared__ uint32_t red_k[2][kWarps];
+    __shared__ uint32_t red_c[2][kWarps];
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nv = (int)(a.Np / 4);
     float4 *m_g = reinterpret_cast<float4 *>(a.m + (int64_t)b * a.Np);
     int p;
     if (kSmem && a.starts) {
-        // a fresh run: the running minima start here (+inf, -inf for masked
-        // rows, the start and the row padding)
         p = a.starts[b];
-        for (int v = threadIdx.x; v < nv; v += kThreads) {
-            float m4[4];
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                const int64_t c = 4 * (int64_t)v + z;
-                m4[z] = (c < a.N && c != p && !(a.mask && a.mask[c])) ? INFINITY : -INFINITY;
-            }
-            s_m4[v] = make_float4(m4[0], m4[1], m4[2], m4[3]);
-        }
+        init_minima(s_m4, 0, nv, a.N, p, a.mask, kThreads);
         __syncthreads();
     } else {
         if (kSmem) {
@@ -121,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
         const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np);
         float best = -INFINITY;
         int best_c = INT_MAX;
-        const int pv = pending >> 2;
+        const int pv = pending >= 0 ? pending >> 2 : -1;
         for (int v0 = threadIdx.x; v0 < nv; v0 += kBatch * kThreads) {
             float4 gv[kBatch], mv[kBatch];
 #pragma unroll
@@ -136,51 +176,27 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
             for (int u = 0; u < kBatch; ++u) {
                 const int v = v0 + u * kThreads;
                 if (v >= nv) break;
-                if (kSmem) mv[u] = s_m4[v];
-                float m4[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
-                const float g[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
-                bool changed = false;
-                if (v == pv) {
-                    m4[pending & 3] = -INFINITY;
-                    changed = true;
-                }
-#pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    const float d = fmaf(g[z], -1.0f, 1.0f);
-                    const float nm = fminf(m4[z], d);
-                    changed |= nm != m4[z];
-                    m4[z] = nm;
-                    if (nm > best) {
-                        best = nm;
-                        best_c = 4 * v + z;
-                    }
-                }
-                if (changed) {
-                    const float4 w = make_float4(m4[0], m4[1], m4[2], m4[3]);
-                    if (kSmem)
-                        s_m4[v] = w;
-                    else
-                        m_g[v] = w;
-                }
+                const float4 m0 = kSmem ? s_m4[v] : mv[u];
+                const float4 nm = fold4(v == pv ? mask_lane(m0, pending & 3) : m0, gv[u]);
+                if (kSmem)
+                    s_m4[v] = nm;
+                else if (nm.x != m0.x || nm.y != m0.y || nm.z != m0.z || nm.w != m0.w)
+                    m_g[v] = nm;
+                track4(nm, 4 * v, best, best_c);
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
-                        __shfl_xor_sync(0xffffffffu, best_c, o));
+        uint32_t key = ord_key(best), col = (uint32_t)best_c;
+        warp_argmax(key, col);
         const int par = t & 1;
         if (lane == 0) {
-            red_v[par][warp] = best;
-            red_c[par][warp] = best_c;
+            red_k[par][warp] = key;
+            red_c[par][warp] = col;
         }
         __syncthreads();
-        best = lane < kWarps ? red_v[par][lane] : -INFINITY;
-        best_c = lane < kWarps ? red_c[par][lane] : INT_MAX;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
-                        __shfl_xor_sync(0xffffffffu, best_c, o));
-        const int w = best_c == INT_MAX ? -1 : best_c;
+        key = lane < kWarps ? red_k[par][lane] : 0u;
+        col = lane < kWarps ? red_c[par][lane] : 0xffffffffu;
+        warp_argmax(key, col);
+        const int w = col == (uint32_t)INT_MAX ? -1 : (int)col;
         if (threadIdx.x == 0) {
             a.picks[(int64_t)b * a.L + t] = w;
             if (w < 0) atomicOr(a.status, kStatusNoWinner);
@@ -189,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
             // the running minima after this fold, before the pick is masked
             float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
             const float *src = kSmem ? reinterpret_cast<const float *>(s_m4) : a.m + (int64_t)b * a.Np;
+            if (!kSmem) __syncthreads();  // every thread's global stores of this fold made
             for (int64_t c = threadIdx.x; c < a.N; c += kThreads) dst[c] = src[c];
             __syncthreads();  // every copy read the pre-mask values
         }
@@ -210,25 +227,41 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
         for (int v = threadIdx.x; v < nv; v += kThreads) m_g[v] = s_m4[v];
 }
 
+__device__ __forceinline__ void st_async_u64(uint32_t cluster_addr, uint64_t v, uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(
+                     cluster_addr),
+                 "l"(v), "r"(cluster_bar)
+                 : "memory");
+}
+
 // The walk for tables whose running-minimum row does not fit one CTA's
 // shared memory: a cluster of kC CTAs walks one sequence, each CTA holding a
 // contiguous kC-th of the row of running minima in its shared memory and
 // streaming the same part of each row G[p][.].  Per iteration each CTA
-// reduces its part to one (max, lowest column) candidate, writes it into a
-// slot of every CTA of the cluster (distributed shared memory), and after
-// one cluster barrier every CTA reduces the kC candidates to the same
-// winner.  The slots alternate between iterations, so one cluster barrier
-// per iteration suffices (no CTA can reach the slots of iteration t + 2
-// before all have passed the barrier of t + 1).  Only G is streamed: the
-// running minima never leave the cluster's shared memory during the walk.
+// reduces its part to one (key, column) candidate and sends it, with one
+// 8-byte asynchronous store per CTA, into a slot of every CTA of the cluster;
+// each store completes bytes on the receiving CTA's mbarrier for that
+// iteration, so a CTA waits only until the kC candidates have landed in its
+// own shared memory (no cluster-wide barrier, and no release of the CTA's
+// global stores, in the loop), then reduces them to the same winner as every
+// other CTA.  Slots and mbarriers alternate between iterations: a CTA sends
+// the candidate of iteration t + 2 only after it has received all those of
+// t + 1, which each CTA sends after it has read the slots of t, so a slot is
+// never overwritten before it is read and a phase of an mbarrier always
+// completes before the next phase's bytes arrive (bytes may land before the
+// receiver's expect_tx of that phase: the transaction count may go negative
+// until the arrival).  Only G is streamed: the running minima never leave
+// the cluster's shared memory during the walk.
 template <int kC, int kThreads, int kBatch, int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel(GramWalkArgs a) {
     constexpr int kWarps = kThreads / 32;
+    static_assert(kC <= 32 && kWarps <= 32, "one warp reduces the candidates");
     extern __shared__ float4 s_m4[];
-    __shared__ float red_v[kWarps];
-    __shared__ int red_c[kWarps];
-    __shared__ float slot_v[2][kC];
-    __shared__ int slot_c[2][kC];
+    __shared__ uint32_t red_k[kWarps];
+    __shared__ uint32_t red_c[kWarps];
+    __shared__ __align__(8) uint64_t cand[2][kC];
+    __shared__ __align__(8) uint64_t bar[2];
+    __shared__ int abort_flag;
     const int rank = (int)cluster_ctarank();
     const int b = blockIdx.x / kC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -243,28 +276,28 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel
         return;
     }
     float4 *m_g = reinterpret_cast<float4 *>(a.m + (int64_t)b * a.Np);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
     int p;
     if (a.starts) {
-        // a fresh run: the running minima start here
         p = a.starts[b];
-        for (int v = threadIdx.x; v < my_v; v += kThreads) {
-            float m4[4];
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                const int64_t c = 4 * (int64_t)(v0 + v) + z;
-                m4[z] = (c < a.N && c != p && !(a.mask && a.mask[c])) ? INFINITY : -INFINITY;
-            }
-            s_m4[v] = make_float4(m4[0], m4[1], m4[2], m4[3]);
-        }
+        init_minima(s_m4, v0, v1, a.N, p, a.mask, kThreads);
     } else {
         for (int v = threadIdx.x; v < my_v; v += kThreads) s_m4[v] = ld_cg_v4(m_g + v0 + v);
         p = a.cur[b];
     }
-    // every CTA's shared memory set up before any remote write
+    // every CTA's mbarriers set up before any candidate is sent
     cluster_sync_all();
     const int slot = a.trace_slot ? a.trace_slot[b] : -1;
     int pending = -1;
-    for (int t = 0; t < a.L; ++t) {
+    int t = 0;
+    for (; t < a.L; ++t) {
+        const int par = t & 1;
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(&bar[par], kC * 8);
         const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np) + v0;
         float best = -INFINITY;
         int best_c = INT_MAX;
@@ -280,60 +313,46 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel
             for (int u = 0; u < kBatch; ++u) {
                 const int v = w0 + u * kThreads;
                 if (v >= my_v) break;
-                const float4 mv = s_m4[v];
-                float m4[4] = {mv.x, mv.y, mv.z, mv.w};
-                const float g[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
-                bool changed = false;
-                if (v == pv) {
-                    m4[pending & 3] = -INFINITY;
-                    changed = true;
-                }
-#pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    const float d = fmaf(g[z], -1.0f, 1.0f);
-                    const float nm = fminf(m4[z], d);
-                    changed |= nm != m4[z];
-                    m4[z] = nm;
-                    if (nm > best) {
-                        best = nm;
-                        best_c = 4 * (v0 + v) + z;
-                    }
-                }
-                if (changed) s_m4[v] = make_float4(m4[0], m4[1], m4[2], m4[3]);
+                const float4 m0 = s_m4[v];
+                const float4 nm = fold4(v == pv ? mask_lane(m0, pending & 3) : m0, gv[u]);
+                s_m4[v] = nm;
+                track4(nm, 4 * (v0 + v), best, best_c);
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
-                        __shfl_xor_sync(0xffffffffu, best_c, o));
+        uint32_t key = ord_key(best), col = (uint32_t)best_c;
+        warp_argmax(key, col);
         if (lane == 0) {
-            red_v[warp] = best;
-            red_c[warp] = best_c;
+            red_k[warp] = key;
+            red_c[warp] = col;
         }
         __syncthreads();
-        const int par = t & 1;
         if (threadIdx.x < 32) {
-            best = lane < kWarps ? red_v[lane] : -INFINITY;
-            best_c = lane < kWarps ? red_c[lane] : INT_MAX;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                take_better(best, best_c, __shfl_xor_sync(0xffffffffu, best, o),
-                            __shfl_xor_sync(0xffffffffu, best_c, o));
+            key = lane < kWarps ? red_k[lane] : 0u;
+            col = lane < kWarps ? red_c[lane] : 0xffffffffu;
+            warp_argmax(key, col);
             // this CTA's candidate into slot [par][rank] of every CTA (lane r
-            // writes CTA r's copy)
-            if (lane < kC) {
-                const uint32_t av = mapa_shared(smem_u32(&slot_v[par][rank]), (uint32_t)lane);
-                const uint32_t ac = mapa_shared(smem_u32(&slot_c[par][rank]), (uint32_t)lane);
-                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(av), "f"(best) : "memory");
-                asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(ac), "r"(best_c) : "memory");
-            }
+            // sends CTA r's copy)
+            if (lane < kC)
+                st_async_u64(mapa_shared(smem_u32(&cand[par][rank]), (uint32_t)lane),
+                             ((uint64_t)key << 32) | col,
+                             mapa_shared(smem_u32(&bar[par]), (uint32_t)lane));
         }
-        cluster_sync_all();
-        best = -INFINITY;
-        best_c = INT_MAX;
-#pragma unroll
-        for (int r = 0; r < kC; ++r) take_better(best, best_c, slot_v[par][r], slot_c[par][r]);
-        const int w = best_c == INT_MAX ? -1 : best_c;
+        // warp 0 waits (bounded) for the kC candidates; the barrier hands
+        // them to the other warps and makes a timeout the whole CTA's
+        // decision, so that every thread leaves the loop at the same
+        // iteration
+        bool ok = true;
+        if (warp == 0)
+            ok = mbar_wait_bounded(&bar[par], (uint32_t)(t >> 1) & 1u, &abort_flag, a.status,
+                                   a.timeout_ns, kStatusBarrierTimeout);
+        if (__syncthreads_or(!ok)) break;
+        {
+            const uint64_t k = lane < kC ? cand[par][lane] : 0ull;
+            key = (uint32_t)(k >> 32);
+            col = lane < kC ? (uint32_t)k : 0xffffffffu;
+            warp_argmax(key, col);
+        }
+        const int w = col == (uint32_t)INT_MAX ? -1 : (int)col;
         if (rank == 0 && threadIdx.x == 0) {
             a.picks[(int64_t)b * a.L + t] = w;
             if (w < 0) atomicOr(a.status, kStatusNoWinner);
@@ -358,7 +377,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel
     if (rank == 0 && threadIdx.x == 0) a.cur[b] = p;
     __syncthreads();
     for (int v = threadIdx.x; v < my_v; v += kThreads) m_g[v0 + v] = s_m4[v];
-    // no CTA leaves while another may still write into its slots
+    // no CTA leaves while another may still send into its shared memory.
+    // After a timeout, the last candidates sent to a CTA that gave up were
+    // sent before their senders' own bounded wait, so they landed long
+    // before every CTA of the cluster reaches this barrier.
     cluster_sync_all();
 }
 
@@ -415,8 +437,14 @@ int gram_walk_place(int64_t Np) {
 cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st) {
     const size_t smem = gram_walk_smem_bytes(a.Np);
     const int64_t nv = a.Np / 4;  // 16-byte vectors per row
-    // rows of running minima spread over a cluster of 8 CTAs
-    if (a.place == 2) return launch_cluster_variant<8, 256, 16, 2>(a, st);
+    // rows of running minima spread over a cluster of 8 CTAs: as many CTAs
+    // per SM as the part each CTA holds allows, one batch of loads per part
+    if (a.place == 2) {
+        const int64_t wv = (nv + 7) / 8;
+        if (wv <= 8 * 128) return launch_cluster_variant<8, 128, 8, 6>(a, st);
+        if (wv <= 16 * 128) return launch_cluster_variant<8, 128, 16, 4>(a, st);
+        return launch_cluster_variant<8, 256, 16, 2>(a, st);
+    }
     if (a.place == 3) return launch_walk_variant<false, 256, 6, 3>(a, 0, st);
     // one batch per row: as few threads as cover the row with at most 17
     // vectors each, so that more CTAs (sequences) fit an SM

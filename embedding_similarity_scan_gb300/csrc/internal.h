@@ -203,6 +203,7 @@ struct GramWalkArgs {
     // where the running minima live during the walk: 1 one CTA's shared
     // memory, 2 a cluster's, 3 global memory (gram_walk_place)
     int place;
+    uint64_t timeout_ns;     // limit of the cluster walk's wait for its peers
 };
 // The default place of a walk's running minima for rows of Np floats.
 int gram_walk_place(int64_t Np);
