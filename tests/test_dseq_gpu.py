@@ -386,7 +386,9 @@ def test_fp16_storage_full_size_and_agreement(es):
 
 
 # --------------------------------------------------------------------------
-# centroid criterion (the issue's distance-from-the-centroid reading)
+# centroid criterion (the distance-from-the-centroid reading of "Issue 9-014:
+# Tile Diversity Shader Inner Loop For L2 Cache Locality", section FP16
+# storage (compounding optimization))
 
 
 @pytest.mark.parametrize("pair", [1, 0])
@@ -484,8 +486,9 @@ def test_centroid_fp16_storage_full_size_and_agreement(es):
 
 
 # --------------------------------------------------------------------------
-# long orderings in chunks ("resume"): the issue's driver runs the sequences
-# in chunks of iterations; continuing from the state left on the device must
+# long orderings in chunks ("resume"): the driver of "Issue 9-014: Tile
+# Diversity Shader Inner Loop For L2 Cache Locality" (Current Behavior) runs
+# the sequences in chunks of iterations; continuing from the state left on the device must
 # give exactly the picks of one long call.
 
 
