@@ -176,16 +176,21 @@ __device__ __forceinline__ bool bmu_epilogue_unit(const BmuArgs &a, int beta, in
 // consecutive rows, one 128-byte line.  G is symmetric, so only the items
 // on and above the diagonal of 256 x 256 tiles are computed; with mirror
 // set (an item off the diagonal) the same values are also stored at
-// gram[i * gram_ld + c], each thread writing its row's 32 consecutive
-// columns as one 128-byte line.  G is then exactly symmetric.  Returns false
-// if the wait gave up.
+// gram[i * gram_ld + c].  There a lane holds one row's 32 columns, so a
+// direct store would touch 32 lines per instruction; instead the warp passes
+// each half (16 columns) of its 32 x 32 block through a 2 KB shared-memory
+// tile (16-byte chunks swizzled by row, so both the row-wise writes and the
+// column-wise reads are free of bank conflicts) and every store instruction
+// then writes 8 rows x 64 contiguous bytes.  G is then exactly symmetric.
+// Returns false if the wait gave up.
+constexpr uint32_t kGramStageBytes = kEpiWarps * 32 * 16 * sizeof(float);
 template <bool kPair>
 __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, int j, uint32_t tile_n,
                                                    int groups, uint32_t tmem_base, uint32_t &acc_uses,
                                                    uint64_t *acc_full, uint64_t *acc_empty,
                                                    uint32_t acc_empty_leader0,
                                                    volatile int *abort_flag, int warp, int lane,
-                                                   bool mirror) {
+                                                   bool mirror, float4 *stage) {
     const int e = warp - 2, q = warp & 3, h = e >> 2;
     const int64_t row = (int64_t)beta * kUnitRows + 32 * q + lane;
     const bool row_ok = row < a.n;
@@ -216,13 +221,29 @@ __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, i
             acc[z] *= rx * wz;
             if (row_ok && cbase + z < a.M) a.gram[(cbase + z) * a.gram_ld + row] = acc[z];
         }
-        if (mirror && row_ok) {
-            // columns past M are row padding of G (never read as values)
-            float4 *dst = reinterpret_cast<float4 *>(a.gram + row * a.gram_ld + cbase);
-            if (cbase + 32 <= a.gram_ld) {
+        // columns past M are row padding of G (never read as values); the
+        // group lies inside a row of G when it starts inside one (gram_ld is
+        // a multiple of 32)
+        if (mirror && cbase + 32 <= a.gram_ld) {
+            const int64_t row0 = (int64_t)beta * kUnitRows + 32 * q;
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+            for (int half = 0; half < 2; ++half) {
+                // lane r puts its row's 16 columns (4 chunks) at chunk v ^ (r & 3)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int z = 16 * half + 4 * v;
+                    stage[lane * 4 + (v ^ (lane & 3))] = make_float4(acc[z], acc[z + 1], acc[z + 2], acc[z + 3]);
+                }
+                __syncwarp();
+                // 8 rows per instruction, 4 lanes per row (64 contiguous bytes)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 8 * k + (lane >> 2), c = lane & 3;
+                    const float4 w = stage[r * 4 + (c ^ (r & 3))];
+                    if (row0 + r < a.n)
+                        *reinterpret_cast<float4 *>(a.gram + (row0 + r) * a.gram_ld + cbase + 16 * half + 4 * c) = w;
+                }
+                __syncwarp();
             }
         }
     }
@@ -312,6 +333,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(final_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float2 *colc = reinterpret_cast<float2 *>(smem + kBmuStages * kStageBytes + 256);
+    // the Gram store epilogue's per-warp transposition tiles (kGram only)
+    float4 *gstage = reinterpret_cast<float4 *>(colc + kEpiWarps * 32);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t tmo = a.timeout_ns;
@@ -495,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // off the diagonal the tile also fills its mirror image
                 if (!gram_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses,
                                                acc_full, acc_empty, acc_empty_leader0, abort_flag,
-                                               warp, lane, j > blk))
+                                               warp, lane, j > blk, gstage + (warp - 2) * 128))
                     break;
             } else if (!bmu_epilogue_unit<kPair>(a, beta, j, tile_n, groups, tmem_base, acc_uses,
                                                  acc_full, acc_empty, acc_empty_leader0, my_colc,
@@ -868,7 +891,7 @@ cudaError_t launch_tc_gram(const BmuArgs &a, const TcPlan &p, const CUtensorMap 
     TcPlan pp = p;
     CUtensorMap mx = tmap_x, mw = tmap_w;
     int sl = slice;
-    const size_t smem = BmuCfg<true>::kSmemBytes;
+    const size_t smem = BmuCfg<true>::kSmemBytes + kGramStageBytes;
     cudaError_t err = cudaFuncSetAttribute(tc_bmu_kernel<true, true>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
