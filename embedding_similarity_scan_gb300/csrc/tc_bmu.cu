@@ -178,12 +178,13 @@ __device__ __forceinline__ bool bmu_epilogue_unit(const BmuArgs &a, int beta, in
 // set (an item off the diagonal) the same values are also stored at
 // gram[i * gram_ld + c].  There a lane holds one row's 32 columns, so a
 // direct store would touch 32 lines per instruction; instead the warp passes
-// each half (16 columns) of its 32 x 32 block through a 2 KB shared-memory
+// each half (16 rows) of its 32 x 32 block through a 2 KB shared-memory
 // tile (16-byte chunks swizzled by row, so both the row-wise writes and the
 // column-wise reads are free of bank conflicts) and every store instruction
-// then writes 8 rows x 64 contiguous bytes.  G is then exactly symmetric.
-// Returns false if the wait gave up.
-constexpr uint32_t kGramStageBytes = kEpiWarps * 32 * 16 * sizeof(float);
+// then writes 4 whole rows of the block, 4 full 128-byte lines (the number
+// of requests, not of bytes, is what the L1-to-L2 path limits).  G is then
+// exactly symmetric.  Returns false if the wait gave up.
+constexpr uint32_t kGramStageBytes = kEpiWarps * 16 * 32 * sizeof(float);
 template <bool kPair>
 __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, int j, uint32_t tile_n,
                                                    int groups, uint32_t tmem_base, uint32_t &acc_uses,
@@ -228,20 +229,24 @@ __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, i
             const int64_t row0 = (int64_t)beta * kUnitRows + 32 * q;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                // lane r puts its row's 16 columns (4 chunks) at chunk v ^ (r & 3)
+                // lanes 16 half .. 16 half + 15 put their rows' 8 chunks at
+                // chunk v ^ (r & 7) of tile row r = lane & 15
+                if ((lane >> 4) == half) {
+                    const int r = lane & 15;
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int z = 16 * half + 4 * v;
-                    stage[lane * 4 + (v ^ (lane & 3))] = make_float4(acc[z], acc[z + 1], acc[z + 2], acc[z + 3]);
+                    for (int v = 0; v < 8; ++v)
+                        stage[r * 8 + (v ^ (r & 7))] =
+                            make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
                 }
                 __syncwarp();
-                // 8 rows per instruction, 4 lanes per row (64 contiguous bytes)
+                // 4 rows per instruction, 8 lanes per row (one 128-byte line)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int r = 8 * k + (lane >> 2), c = lane & 3;
-                    const float4 w = stage[r * 4 + (c ^ (r & 3))];
-                    if (row0 + r < a.n)
-                        *reinterpret_cast<float4 *>(a.gram + (row0 + r) * a.gram_ld + cbase + 16 * half + 4 * c) = w;
+                    const int r = 4 * k + (lane >> 3), c = lane & 7;
+                    const float4 w = stage[r * 8 + (c ^ (r & 7))];
+                    const int64_t grow = row0 + 16 * half + r;
+                    if (grow < a.n)
+                        *reinterpret_cast<float4 *>(a.gram + grow * a.gram_ld + cbase + 4 * c) = w;
                 }
                 __syncwarp();
             }

@@ -804,7 +804,7 @@ def test_gram_automatic_choice(es):
     assert es.dseq_last_stat("gram_ns") > 0 and es.dseq_last_stat("walk_ns") > 0
 
 
-@pytest.mark.parametrize("name", ["page1", "scale"])
+@pytest.mark.parametrize("name", ["page1", "n32k", "scale"])
 def test_gram_full_size_teacher_forced(es, name):
     """The full configurations on the engine the library picks for them (the
     Gram engine), the benchmark's launch configuration, with a seeded subset

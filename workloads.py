@@ -132,6 +132,10 @@ DIVERSITY = {
                              "clustered", 64),
     "scale": DiversityConfig("scale-up N=131072 D=768 B=8192 L=128", 131072, 768, 8192, 128,
                              "clustered", 64),
+    # a mid-size table for profiling the Gram product and the cluster walk on
+    # a few GB of device memory (G is 4.3 GB); not a benchmark configuration
+    "n32k": DiversityConfig("mid-size N=32768 D=768 B=2048 L=64", 32768, 768, 2048, 64,
+                            "clustered", 16),
 }
 
 BMU = {
