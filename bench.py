@@ -652,7 +652,9 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
                 "note": (f"achieved = algorithmic bytes of the walk (one row of G, 4*N bytes, per "
                          f"sequence-iteration{' + the running minima read, 4*N; writes of the minima that fell are not counted' if m_global else ''})"
                          f" / walk kernel time (CUDA events); peak = {peak_src} copy bandwidth "
-                         f"{hbm_peak:.1f} GB/s")}
+                         f"{hbm_peak:.1f} GB/s; L2 serves the rows that many sequences read in "
+                         f"the same stretch of iterations, so frac can exceed 1 where G is not far "
+                         f"above L2 (traffic = the DRAM bytes of one launch, from ncu)")}
         gram_product = {"bound": "tensor", "achieved": gflop / gram_s / 1e12, "peak": tensor_peak,
                         "unit": "TFLOP/s", "frac": gflop / gram_s / 1e12 / tensor_peak,
                         "peak_kind": peak_kind, "frac_of_burst": gflop / gram_s / 1e12 / burst_peak,

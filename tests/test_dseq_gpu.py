@@ -731,14 +731,17 @@ def test_gram_running_minima_too_long_for_one_cta(es):
 
 
 @pytest.mark.parametrize("case", [(1000, 96, 200, 16), (3001, 40, 29, 12), (37, 5, 9, 20),
-                                  (24576, 16, 6, 9), (24600, 16, 6, 9)],
+                                  (24576, 16, 6, 9), (24600, 16, 6, 9), (40000, 16, 6, 7),
+                                  (140000, 16, 4, 5)],
                          ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
 def test_gram_walk_places_identical(es, case):
     """The three places of the running minima (one CTA's shared memory, a
     cluster's, global memory) run the same arithmetic in the same order per
     candidate: identical picks and traced minima, and the oracle's.  Rows
-    shorter than the cluster (N = 37: some CTAs hold no candidate) and the
-    largest one-CTA row (N = 24576) included."""
+    shorter than the cluster (N = 37: some CTAs hold no candidate), the
+    largest one-CTA row (N = 24576), and every cluster shape: up to 1,024
+    vectors per CTA, up to 2,048 (N = 40000), and more than one batch of
+    loads per CTA (N = 140000, 78 GB of G) included."""
     N, D, B, L = case
     E = workloads.gaussian_table(N, D, seed=N + 7)
     starts = workloads.starts(N, B, seed=N + 7)
