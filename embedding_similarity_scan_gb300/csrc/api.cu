@@ -3,11 +3,13 @@
 // (chunk widths, global-mask compaction, BMU slices), and the launches of
 // the kernels in tc_dseq.cu, tc_bmu.cu, ffma.cu, prep.cu and som.cu.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -181,23 +183,111 @@ int64_t get_opt(const Options &o, const char *name) {
 
 // --------------------------------------------------------------------------
 // device memory helpers
+//
+// Buffer cache: a context's buffers, when it is destroyed, and a call's
+// staging buffers, once the call has synchronised, are idle; instead of
+// cudaFree they go to a per-device cache (up to "cache_mb" in total per
+// device), from which later allocations of a similar size are served.  A
+// create / run / destroy cycle then maps and unmaps no device memory after
+// the first (cudaMalloc of large buffers and cudaFree, which also
+// synchronises the device, cost about a millisecond per page-1 cycle).  A
+// buffer released while work using it may still be queued keeps cudaFree.
+// A failed cudaMalloc empties the device's cache and retries once.
+struct BufCache {
+    std::mutex mu;
+    std::multimap<size_t, void *> idle;  // bytes -> buffer
+    size_t held = 0;
+};
+BufCache g_cache[64];
+std::atomic<int64_t> g_cache_limit{int64_t(4096) << 20};
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return dev >= 0 && dev < 64 ? dev : -1;
+}
+
+// a cached buffer of at least n bytes and not much larger, or nullptr
+void *cache_take(int dev, size_t n, size_t &bytes) {
+    if (dev < 0) return nullptr;
+    BufCache &c = g_cache[dev];
+    std::lock_guard<std::mutex> lk(c.mu);
+    auto it = c.idle.lower_bound(n);
+    if (it == c.idle.end() || it->first > 2 * n + (size_t(1) << 20)) return nullptr;
+    void *p = it->second;
+    bytes = it->first;
+    c.held -= bytes;
+    c.idle.erase(it);
+    return p;
+}
+
+// keeps an idle buffer for reuse, or frees it when the cache is full
+void cache_put(int dev, void *p, size_t bytes) {
+    if (dev >= 0) {
+        BufCache &c = g_cache[dev];
+        std::lock_guard<std::mutex> lk(c.mu);
+        if ((int64_t)(c.held + bytes) <= g_cache_limit.load()) {
+            c.idle.emplace(bytes, p);
+            c.held += bytes;
+            return;
+        }
+    }
+    cudaFree(p);
+}
+
+// frees the device's cached buffers down to `keep` bytes (largest first)
+void cache_trim(int dev, size_t keep) {
+    BufCache &c = g_cache[dev];
+    std::lock_guard<std::mutex> lk(c.mu);
+    while (c.held > keep && !c.idle.empty()) {
+        auto it = std::prev(c.idle.end());
+        cudaFree(it->second);
+        c.held -= it->first;
+        c.idle.erase(it);
+    }
+}
+
 struct DevBuf {
     void *p = nullptr;
     size_t bytes = 0;
+    int dev = -1;
     int ensure(size_t n) {
         if (n <= bytes) return DSEQ_OK;
         release();
+        const int d = current_device();
+        size_t got = 0;
+        if ((p = cache_take(d, n, got)) != nullptr) {
+            bytes = got;
+            dev = d;
+            return DSEQ_OK;
+        }
         cudaError_t e = cudaMalloc(&p, n);
+        if (e != cudaSuccess && d >= 0) {
+            cudaGetLastError();
+            cache_trim(d, 0);
+            e = cudaMalloc(&p, n);
+        }
         if (e != cudaSuccess) {
             cudaGetLastError();
             p = nullptr;
             return fail(DSEQ_ENOMEM, "cudaMalloc of %zu bytes failed: %s", n, cudaGetErrorString(e));
         }
         bytes = n;
+        dev = d;
         return DSEQ_OK;
     }
+    // frees the buffer (cudaFree: safe while work using it may be queued)
     void release() {
         if (p) cudaFree(p);
+        p = nullptr;
+        bytes = 0;
+    }
+    // hands an idle buffer (no queued work uses it) to the cache
+    void recycle() {
+        if (p) cache_put(dev, p, bytes);
         p = nullptr;
         bytes = 0;
     }
@@ -490,7 +580,8 @@ struct dseq_ctx {
                          &starts, &mask,    &picks,  &trace_slot, &timeline,
                          &col_map, &comp_of, &e_split_c, &e_f16_c, &rn_c,
                          &gram, &g_xs, &g_ws, &g_xn, &g_wn, &g_xi, &g_wi, &g_cur};
-        for (DevBuf *b : all) b->release();
+        // idle: calls on a context do not overlap, and each one synchronised
+        for (DevBuf *b : all) b->recycle();
     }
 };
 
@@ -518,12 +609,20 @@ int64_t dseq_last_stat(const char *name) {
 
 int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value) {
     g_err.clear();
+    if (name && std::string(name) == "cache_mb") {
+        if (ctx) return fail(DSEQ_EINVAL, "cache_mb is a process-wide option (ctx must be NULL)");
+        if (value < 0 || value > (int64_t(1) << 24)) return fail(DSEQ_EINVAL, "cache_mb out of range");
+        g_cache_limit.store(value << 20);
+        for (int d = 0; d < 64; ++d) cache_trim(d, (size_t)(value << 20));
+        return DSEQ_OK;
+    }
     if (ctx) return set_opt(ctx->opt, name, value);
     std::lock_guard<std::mutex> lk(g_opt_mu);
     return set_opt(g_defaults, name, value);
 }
 
 int64_t dseq_get_option(dseq_ctx *ctx, const char *name) {
+    if (name && std::string(name) == "cache_mb") return ctx ? -1 : g_cache_limit.load() >> 20;
     if (ctx) return get_opt(ctx->opt, name);
     std::lock_guard<std::mutex> lk(g_opt_mu);
     return get_opt(g_defaults, name);
@@ -581,7 +680,7 @@ int dseq_create(const float *table, int64_t N, int32_t D, int table_on_device, v
         return bail(fail(cuda_code(e), "table preparation failed: %s", cudaGetErrorString(e)));
     }
     if ((r = read_status(ctx->status.as<int>(), st)) != DSEQ_OK) return bail(r);
-    staged.release();
+    staged.recycle();  // the stream was synchronised by read_status
     *out = ctx;
     return DSEQ_OK;
 }

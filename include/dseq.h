@@ -261,6 +261,17 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 larger than can be co-resident is refused by the
  *                 cooperative launch: dseq_run returns DSEQ_ELAUNCH.
  *   "timeout_ms"  limit of every device-side wait (default 10000).
+ *   "cache_mb"    process-wide only (ctx must be NULL): device memory, per
+ *                 device, that the library keeps for reuse after a context
+ *                 is destroyed or a call's staging buffers are no longer
+ *                 needed, instead of freeing it; later contexts and calls
+ *                 take buffers of a similar size from it, so a create /
+ *                 run / destroy cycle maps no new device memory once warm.
+ *                 Default 4096; 0 keeps nothing.  Lowering it frees kept
+ *                 buffers down to the new limit at once; a failed
+ *                 allocation frees the device's kept buffers and retries.
+ *                 That memory is not available to other allocators in the
+ *                 process while it is kept.
  *   "resume"      1 = dseq_run continues the last successful run on this
  *                 context from the state it left on the device (running
  *                 minima, current queries): the same starts, mask and

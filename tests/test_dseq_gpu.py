@@ -823,3 +823,43 @@ def test_gram_full_size_teacher_forced(es, name):
     srt = np.sort(picks, axis=1)
     assert not np.any(srt[:, 1:] == srt[:, :-1]), "a sequence repeats a pick"
     assert not np.any(picks == starts[:, None]), "a sequence picks its start"
+
+
+def test_buffer_cache(es):
+    """Destroyed contexts' buffers are kept for reuse (up to cache_mb per
+    device): repeated create / run / destroy cycles from host arrays give
+    identical picks and, once the cache holds their buffers, map no new
+    device memory; with cache_mb = 0 every buffer is freed."""
+    N, D, B, L = 3000, 64, 40, 12
+    E = workloads.gaussian_table(N, D, seed=5)
+    starts = workloads.starts(N, B, seed=5)
+
+    def cycle():
+        ctx = es.dseq_create(E)  # host arrays: every device buffer is the library's
+        try:
+            return np.array(es.dseq_run(ctx, starts, L))
+        finally:
+            ctx.close()
+
+    def free_bytes():
+        torch.cuda.synchronize()
+        return torch.cuda.mem_get_info()[0]
+
+    try:
+        cycle()  # modules loaded, one-time set-up done
+        es.dseq_set_option("cache_mb", 0)
+        assert es.dseq_get_option("cache_mb") == 0
+        free0 = free_bytes()
+        p0 = cycle()
+        assert free_bytes() == free0, "cache_mb = 0 kept device memory"
+        es.dseq_set_option("cache_mb", 4096)
+        p1 = cycle()
+        free1 = free_bytes()
+        assert free1 < free0, "no buffer was kept"
+        p2 = cycle()
+        assert free_bytes() == free1, "a cycle mapped new memory despite the cache"
+        assert np.array_equal(p0, p1) and np.array_equal(p0, p2)
+        es.dseq_set_option("cache_mb", 0)  # trims the cache
+        assert free_bytes() == free0
+    finally:
+        es.dseq_set_option("cache_mb", 4096)
