@@ -6,7 +6,9 @@
 // minimum and takes the unmasked candidate with the largest running minimum
 // (lowest index on ties).  The newest pick is itself a table row, so every
 // distance the run needs is an entry of the table's Gram matrix: d(p, c) =
-// 1 - G[p][c] with G = E E^T of the unit rows.  When the sequences make many
+// 1 - G[p][c] with G = E E^T of the unit rows.  The product stores these
+// distances (the matrix 1 - G, rounded once from the fp32 G entry, exactly
+// as the fold would compute it), so the fold is one min per candidate.  When the sequences make many
 // more picks than the table has rows (B * L >> N), computing G once on the
 // tensor cores (the BMU kernel's pipeline with a store epilogue, see
 // tc_bmu.cu) and then streaming one row of G per sequence and iteration moves
@@ -67,11 +69,10 @@ __device__ __forceinline__ void warp_argmax(uint32_t &key, uint32_t &col) {
     key = mx;
 }
 
-// The fold of one 16-byte vector (four candidates) of G[p] into the running
-// minima: m <- min(m, 1 - g).
-__device__ __forceinline__ float4 fold4(float4 m, float4 g) {
-    return make_float4(fminf(m.x, fmaf(g.x, -1.0f, 1.0f)), fminf(m.y, fmaf(g.y, -1.0f, 1.0f)),
-                       fminf(m.z, fmaf(g.z, -1.0f, 1.0f)), fminf(m.w, fmaf(g.w, -1.0f, 1.0f)));
+// The fold of one 16-byte vector (four candidates) of the distance row
+// d(p, .) into the running minima: m <- min(m, d).
+__device__ __forceinline__ float4 fold4(float4 m, float4 d) {
+    return make_float4(fminf(m.x, d.x), fminf(m.y, d.y), fminf(m.z, d.z), fminf(m.w, d.w));
 }
 // The thread's running (max, column) over the vectors it folds, in
 // ascending column order: a vector's max is compared once, and only when it
@@ -82,14 +83,6 @@ __device__ __forceinline__ void track4(float4 nm, int c0, float &best, int &best
         best = mx;
         best_c = c0 + (nm.x == mx ? 0 : nm.y == mx ? 1 : nm.z == mx ? 2 : 3);
     }
-}
-// The newest pick, masked in the fold of the vector that holds it.
-__device__ __forceinline__ float4 mask_lane(float4 m, int z) {
-    if (z == 0) m.x = -INFINITY;
-    else if (z == 1) m.y = -INFINITY;
-    else if (z == 2) m.z = -INFINITY;
-    else m.w = -INFINITY;
-    return m;
 }
 
 __global__ void gram_walk_init_kernel(GramWalkArgs a, const int32_t *__restrict__ starts,
@@ -162,7 +155,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
         const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np);
         float best = -INFINITY;
         int best_c = INT_MAX;
-        const int pv = pending >= 0 ? pending >> 2 : -1;
+        // the last pick is masked by the thread whose vectors hold it, before
+        // that thread folds them (no other thread reads that vector)
+        if (pending >= 0 && (pending >> 2) % kThreads == (int)threadIdx.x) {
+            if (kSmem)
+                reinterpret_cast<float *>(s_m4)[pending] = -INFINITY;
+            else
+                a.m[(int64_t)b * a.Np + pending] = -INFINITY;
+        }
         for (int v0 = threadIdx.x; v0 < nv; v0 += kBatch * kThreads) {
             float4 gv[kBatch], mv[kBatch];
 #pragma unroll
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
                 const int v = v0 + u * kThreads;
                 if (v >= nv) break;
                 const float4 m0 = kSmem ? s_m4[v] : mv[u];
-                const float4 nm = fold4(v == pv ? mask_lane(m0, pending & 3) : m0, gv[u]);
+                const float4 nm = fold4(m0, gv[u]);
                 if (kSmem)
                     s_m4[v] = nm;
                 else if (nm.x != m0.x || nm.y != m0.y || nm.z != m0.z || nm.w != m0.w)
@@ -303,7 +303,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel
         const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np) + v0;
         float best = -INFINITY;
         int best_c = INT_MAX;
-        const int pv = pending >= 0 ? (pending >> 2) - v0 : -1;
+        // the last pick is masked by the thread of the CTA whose vectors
+        // hold it, before that thread folds them
+        if (pending >= 0 && (pending >> 2) >= v0 && (pending >> 2) < v1 &&
+            ((pending >> 2) - v0) % kThreads == (int)threadIdx.x)
+            reinterpret_cast<float *>(s_m4)[pending - 4 * v0] = -INFINITY;
         for (int w0 = threadIdx.x; w0 < my_v; w0 += kBatch * kThreads) {
             float4 gv[kBatch];
 #pragma unroll
@@ -315,8 +319,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel
             for (int u = 0; u < kBatch; ++u) {
                 const int v = w0 + u * kThreads;
                 if (v >= my_v) break;
-                const float4 m0 = s_m4[v];
-                const float4 nm = fold4(v == pv ? mask_lane(m0, pending & 3) : m0, gv[u]);
+                const float4 nm = fold4(s_m4[v], gv[u]);
                 s_m4[v] = nm;
                 track4(nm, 4 * (v0 + v), best, best_c);
             }

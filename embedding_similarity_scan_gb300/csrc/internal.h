@@ -186,7 +186,7 @@ int tc_dseq_max_grid(bool pair, bool f16, bool centroid);
 
 // ---- diversity, Gram engine (gram.cu; the Gram product in tc_bmu.cu) --------
 struct GramWalkArgs {
-    const float *G;          // N x Np: G[p][c] = <e_p, e_c> of the unit rows
+    const float *G;          // N x Np: distances 1 - <e_p, e_c> of the unit rows
     float *m;                // B x Np running minima, row-major (in and out)
     int32_t *cur;            // B: the newest row of each sequence (in and out)
     int32_t *picks;          // B x L
@@ -254,7 +254,7 @@ struct BmuArgs {
     // test only: CTA 0 leaves out one copy of its first codebook stage, so
     // that stage never fills and the waits on it run out
     int fault_skip_copy;
-    // Gram product (launch_tc_gram): <e_i, e_c> stored at gram[c * gram_ld + i]
+    // Gram product (launch_tc_gram): 1 - <e_i, e_c> stored at gram[c * gram_ld + i]
     float *gram;
     int64_t gram_ld;
 };

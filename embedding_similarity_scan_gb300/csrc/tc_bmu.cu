@@ -171,7 +171,8 @@ __device__ __forceinline__ bool bmu_epilogue_unit(const BmuArgs &a, int beta, in
 // hold the rows of one table on both sides (X = [hi | lo * 2^12], W =
 // [hi * 2^12 | hi | lo * 2^12], each row scaled by its power of two), so the
 // accumulator of row i (sample side) and column c (codebook side) is
-// 2^12 <x~_i, w~_c>; scaled back exactly, <e_i, e_c> is stored at
+// 2^12 <x~_i, w~_c>; scaled back exactly to <e_i, e_c>, the distance
+// 1 - <e_i, e_c> is stored at
 // gram[c * gram_ld + i]: for each column the 32 lanes of a warp write 32
 // consecutive rows, one 128-byte line.  G is symmetric, so only the items
 // on and above the diagonal of 256 x 256 tiles are computed; with mirror
@@ -219,7 +220,9 @@ __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, i
 #pragma unroll
         for (int z = 0; z < 32; ++z) {
             const float wz = __shfl_sync(0xffffffffu, cw[k], z);
-            acc[z] *= rx * wz;
+            // the cosine distance 1 - <e_i, e_c>, rounded once from the fp32
+            // inner product (the value the walk folds)
+            acc[z] = fmaf(acc[z] * (rx * wz), -1.0f, 1.0f);
             if (row_ok && cbase + z < a.M) a.gram[(cbase + z) * a.gram_ld + row] = acc[z];
         }
         // columns past M are row padding of G (never read as values); the

@@ -226,12 +226,13 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 0 = per iteration, the newest picks against the whole
  *                 table on the tensor cores, fused with the fold and the
  *                 argmax (the scan); 1 = the table's Gram matrix G = E E^T
- *                 of the unit rows once per run on the tensor cores (N x Np
- *                 float32, Np = N rounded up to 32; the tiles on and above
- *                 the diagonal are computed and every entry is stored at
- *                 (i, c) and (c, i), so G is exactly symmetric), then one CTA
- *                 (or cluster) per sequence reads row G[p] of its newest
- *                 pick p every iteration, distance 1 - G[p][c]; 2 = 1 where
+ *                 of the unit rows once per run on the tensor cores, stored
+ *                 as the distances 1 - G (N x Np float32, Np = N rounded up
+ *                 to 32; the tiles on and above the diagonal are computed
+ *                 and every entry is stored at (i, c) and (c, i), so the
+ *                 matrix is exactly symmetric), then one CTA (or cluster)
+ *                 per sequence reads the row of its newest pick p every
+ *                 iteration, distance 1 - G[p][c]; 2 = 1 where
  *                 a cost model (the product plus B * L row reads against B *
  *                 L table scans) says it is cheaper and G fits in 80 % of
  *                 the free device memory, else 0 (default).  Both give the
