@@ -408,8 +408,11 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
             return {k: es.dseq_last_stat(k)
                     for k in ("kernel_ns", "launches", "gram", "gram_ns", "walk_ns", "walk")}
 
+        # the end-to-end leg's result buffer: pinned host memory, allocated
+        # once (a caller's output array, not part of the call)
+        picks_host = torch.empty((cfg.B, cfg.L), dtype=torch.int32).pin_memory()
+
         def e2e_step():
-            picks_host = torch.empty((cfg.B, cfg.L), dtype=torch.int32).pin_memory()
             c = es.dseq_create(E_host)
             try:
                 es.dseq_run(c, starts_host, cfg.L, picks=picks_host)
@@ -445,10 +448,13 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
             update_ns.append(es.dseq_last_stat("update_ns"))
             return {k: es.dseq_last_stat(k) for k in ("kernel_ns", "launches")}
 
+        # the end-to-end leg trains a host copy of the same map in place, as
+        # the device leg trains W_dev: pinned host buffers allocated once
+        W_h = W_host.clone().pin_memory()
+        idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
+        dist_h = torch.empty(cfg.n, dtype=torch.float32).pin_memory()
+
         def e2e_step():
-            W_h = W_host.clone().pin_memory()
-            idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
-            dist_h = torch.empty(cfg.n, dtype=torch.float32).pin_memory()
             es.som_epoch(X_host, W_h, sx, sy, sigma, radius, bmu=idx_h, dist=dist_h)
             return (X_host.numel() + W_h.numel()) * 4, W_h.numel() * 4 + cfg.n * 8
 
@@ -481,9 +487,10 @@ def _workload(args, name, es, dev, rank, opts) -> _Workload:
         es.bmu_search(X_dev, W_dev, idx=idx_dev, dist=dist_dev)
         return {k: es.dseq_last_stat(k) for k in ("kernel_ns", "launches")}
 
+    idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
+    dist_h = torch.empty(cfg.n, dtype=torch.float32).pin_memory()
+
     def e2e_step():
-        idx_h = torch.empty(cfg.n, dtype=torch.int32).pin_memory()
-        dist_h = torch.empty(cfg.n, dtype=torch.float32).pin_memory()
         es.bmu_search(X_host, W_host, idx=idx_h, dist=dist_h)
         return (X_host.numel() + W_host.numel()) * 4, cfg.n * 8
 
