@@ -562,7 +562,7 @@ struct dseq_ctx {
     DevBuf col_map, comp_of, e_split_c, e_f16_c, rn_c;
     // Gram engine: G (N x Np), the table split twice for the Gram product,
     // the sequences' newest rows
-    DevBuf gram, g_xs, g_ws, g_xn, g_wn, g_xi, g_wi, g_cur;
+    DevBuf gram, g_xs, g_ws, g_xn, g_wn, g_xi, g_wi, g_cur, g_cstate;
     int64_t timeline_iters = 0, timeline_grid = 0;
     int csum_shift = kNoShift;  // fixed-point scale of the centroid sums, set on first use
     // state left on the device by the last successful run, for "resume"
@@ -579,7 +579,7 @@ struct dseq_ctx {
                          &held,   &keys,    &q,      &q_rn,    &csum,   &c_exp,  &status, &barrier,
                          &starts, &mask,    &picks,  &trace_slot, &timeline,
                          &col_map, &comp_of, &e_split_c, &e_f16_c, &rn_c,
-                         &gram, &g_xs, &g_ws, &g_xn, &g_wn, &g_xi, &g_wi, &g_cur};
+                         &gram, &g_xs, &g_ws, &g_xn, &g_wn, &g_xi, &g_wi, &g_cur, &g_cstate};
         // idle: calls on a context do not overlap, and each one synchronised
         for (DevBuf *b : all) b->recycle();
     }
@@ -825,12 +825,17 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     TRY(device_info(ctx->device, info));
     EventTimer timer;
 
-    // the Gram engine (max-min on split storage) when it pays, or when asked;
-    // a resumed run continues on the engine of the run it resumes
+    // the Gram engine (split storage) for max-min when it pays or when asked;
+    // for the centroid criterion only when asked (gram = 1) and a row of its
+    // sums fits one CTA's shared memory: its distances carry the product's
+    // rounding summed over the held rows, where the scan's exact centroid
+    // sums do not; a resumed run continues on the engine of the run it resumes
+    const bool centroid_fits = (size_t)round_up(N, 32) * sizeof(float) <= kGramWalkSmemMax;
     bool use_gram = false;
     if (resume) {
         use_gram = ctx->state_gram;
-    } else if (ctx->opt.engine == 0 && ctx->opt.criterion == 0 && ctx->opt.storage == 0 &&
+    } else if (ctx->opt.engine == 0 && ctx->opt.storage == 0 &&
+               (ctx->opt.criterion == 0 || (centroid_fits && ctx->opt.gram == 1)) &&
                ctx->opt.isolate_epilogue == 0 && ctx->opt.timeline == 0 && ctx->opt.gram != 0) {
         if (ctx->opt.gram == 1) {
             use_gram = true;
@@ -851,6 +856,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         // "walk" option (a one-CTA row must fit its shared memory)
         int place = ctx->opt.walk > 0 ? (int)ctx->opt.walk : gram_walk_place(Np);
         if (resume) place = ctx->state_walk;
+        if (ctx->opt.criterion != 0 && place != 1)
+            return fail(DSEQ_EINVAL, "walk=%d: the centroid criterion keeps its sums in one CTA's shared memory (walk 0 or 1)", place);
         if (place == 1 && (size_t)Np * sizeof(float) > kGramWalkSmemMax)
             return fail(DSEQ_EINVAL, "walk=1: a row of %lld running minima does not fit one CTA's shared memory", (long long)Np);
         if (place == 2 && (size_t)Np * sizeof(float) > kGramWalkClusterMax)
@@ -864,6 +871,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         TRY(ctx->g_xi.ensure((size_t)N * sizeof(float)));
         TRY(ctx->g_wi.ensure((size_t)N * sizeof(float)));
         TRY(ctx->g_cur.ensure((size_t)B * sizeof(int32_t)));
+        if (ctx->opt.criterion != 0) TRY(ctx->g_cstate.ensure((size_t)B * sizeof(double2)));
         TRY(ctx->m.ensure((size_t)B * Np * sizeof(float)));
         BmuArgs ga;
         std::memset(&ga, 0, sizeof ga);
@@ -881,6 +889,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         ga.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
         ga.gram = ctx->gram.as<float>();
         ga.gram_ld = Np;
+        ga.gram_sim = ctx->opt.criterion != 0;  // the centroid walk sums inner products
         TcPlan gp{};
         gp.pair = 1;
         gp.n_beta = (int)((N + kUnitRows - 1) / kUnitRows);
@@ -905,6 +914,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         wa.L = L;
         wa.place = place;
         wa.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
+        wa.centroid = (int)ctx->opt.criterion;
+        wa.cstate = ctx->opt.criterion != 0 ? ctx->g_cstate.as<double2>() : nullptr;
         ctx->state_walk = place;
         EventTimer mid;
         TRY(timer.start(st));

@@ -186,7 +186,7 @@ int tc_dseq_max_grid(bool pair, bool f16, bool centroid);
 
 // ---- diversity, Gram engine (gram.cu; the Gram product in tc_bmu.cu) --------
 struct GramWalkArgs {
-    const float *G;          // N x Np: distances 1 - <e_p, e_c> of the unit rows
+    const float *G;          // N x Np: distances 1 - <e_p, e_c> of the unit rows (centroid: <e_p, e_c>)
     float *m;                // B x Np running minima, row-major (in and out)
     int32_t *cur;            // B: the newest row of each sequence (in and out)
     int32_t *picks;          // B x L
@@ -204,6 +204,12 @@ struct GramWalkArgs {
     // memory, 2 a cluster's, 3 global memory (gram_walk_place)
     int place;
     uint64_t timeout_ns;     // limit of the cluster walk's wait for its peers
+    // centroid criterion (gram_centroid_walk): m holds the running sums
+    // S[c] of the held rows' similarities to c, and cstate[b] = (|s|^2 of
+    // the held rows' sum s, S[w] of the last pick w before its row was
+    // added), both carried across resumed runs
+    int centroid;
+    double2 *cstate;
 };
 // The default place of a walk's running minima for rows of Np floats.
 int gram_walk_place(int64_t Np);
@@ -255,7 +261,9 @@ struct BmuArgs {
     // that stage never fills and the waits on it run out
     int fault_skip_copy;
     // Gram product (launch_tc_gram): 1 - <e_i, e_c> stored at gram[c * gram_ld + i]
+    // (gram_sim: <e_i, e_c> itself)
     float *gram;
+    int gram_sim;
     int64_t gram_ld;
 };
 void launch_bmu_keys_init(unsigned long long *keys, int64_t n, cudaStream_t st);
