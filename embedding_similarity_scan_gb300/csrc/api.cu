@@ -562,7 +562,7 @@ struct dseq_ctx {
     DevBuf col_map, comp_of, e_split_c, e_f16_c, rn_c;
     // Gram engine: G (N x Np), the table split twice for the Gram product,
     // the sequences' newest rows
-    DevBuf gram, g_xs, g_ws, g_xn, g_wn, g_xi, g_wi, g_cur, g_cstate;
+    DevBuf gram, g_xs, g_ws, g_xn, g_wn, g_xi, g_wi, g_cur, g_u16;
     int64_t timeline_iters = 0, timeline_grid = 0;
     int csum_shift = kNoShift;  // fixed-point scale of the centroid sums, set on first use
     // state left on the device by the last successful run, for "resume"
@@ -579,7 +579,7 @@ struct dseq_ctx {
                          &held,   &keys,    &q,      &q_rn,    &csum,   &c_exp,  &status, &barrier,
                          &starts, &mask,    &picks,  &trace_slot, &timeline,
                          &col_map, &comp_of, &e_split_c, &e_f16_c, &rn_c,
-                         &gram, &g_xs, &g_ws, &g_xn, &g_wn, &g_xi, &g_wi, &g_cur, &g_cstate};
+                         &gram, &g_xs, &g_ws, &g_xn, &g_wn, &g_xi, &g_wi, &g_cur, &g_u16};
         // idle: calls on a context do not overlap, and each one synchronised
         for (DevBuf *b : all) b->recycle();
     }
@@ -825,17 +825,13 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
     TRY(device_info(ctx->device, info));
     EventTimer timer;
 
-    // the Gram engine (split storage) for max-min when it pays or when asked;
-    // for the centroid criterion only when asked (gram = 1) and a row of its
-    // sums fits one CTA's shared memory: its distances carry the product's
-    // rounding summed over the held rows, where the scan's exact centroid
-    // sums do not; a resumed run continues on the engine of the run it resumes
-    const bool centroid_fits = (size_t)round_up(N, 32) * sizeof(float) <= kGramWalkSmemMax;
+    // the Gram engine (max-min; split or fp16 storage: with fp16 storage G
+    // holds the distances between the stored rows) when it pays, or when
+    // asked; a resumed run continues on the engine of the run it resumes
     bool use_gram = false;
     if (resume) {
         use_gram = ctx->state_gram;
-    } else if (ctx->opt.engine == 0 && ctx->opt.storage == 0 &&
-               (ctx->opt.criterion == 0 || (centroid_fits && ctx->opt.gram == 1)) &&
+    } else if (ctx->opt.engine == 0 && ctx->opt.criterion == 0 &&
                ctx->opt.isolate_epilogue == 0 && ctx->opt.timeline == 0 && ctx->opt.gram != 0) {
         if (ctx->opt.gram == 1) {
             use_gram = true;
@@ -856,8 +852,6 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         // "walk" option (a one-CTA row must fit its shared memory)
         int place = ctx->opt.walk > 0 ? (int)ctx->opt.walk : gram_walk_place(Np);
         if (resume) place = ctx->state_walk;
-        if (ctx->opt.criterion != 0 && place != 1)
-            return fail(DSEQ_EINVAL, "walk=%d: the centroid criterion keeps its sums in one CTA's shared memory (walk 0 or 1)", place);
         if (place == 1 && (size_t)Np * sizeof(float) > kGramWalkSmemMax)
             return fail(DSEQ_EINVAL, "walk=1: a row of %lld running minima does not fit one CTA's shared memory", (long long)Np);
         if (place == 2 && (size_t)Np * sizeof(float) > kGramWalkClusterMax)
@@ -871,7 +865,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         TRY(ctx->g_xi.ensure((size_t)N * sizeof(float)));
         TRY(ctx->g_wi.ensure((size_t)N * sizeof(float)));
         TRY(ctx->g_cur.ensure((size_t)B * sizeof(int32_t)));
-        if (ctx->opt.criterion != 0) TRY(ctx->g_cstate.ensure((size_t)B * sizeof(double2)));
+        if (ctx->opt.storage != 0) TRY(ctx->g_u16.ensure((size_t)N * Dp * sizeof(float)));
         TRY(ctx->m.ensure((size_t)B * Np * sizeof(float)));
         BmuArgs ga;
         std::memset(&ga, 0, sizeof ga);
@@ -889,7 +883,6 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         ga.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
         ga.gram = ctx->gram.as<float>();
         ga.gram_ld = Np;
-        ga.gram_sim = ctx->opt.criterion != 0;  // the centroid walk sums inner products
         TcPlan gp{};
         gp.pair = 1;
         gp.n_beta = (int)((N + kUnitRows - 1) / kUnitRows);
@@ -914,16 +907,24 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         wa.L = L;
         wa.place = place;
         wa.timeout_ns = (uint64_t)ctx->opt.timeout_ms * 1000000ull;
-        wa.centroid = (int)ctx->opt.criterion;
-        wa.cstate = ctx->opt.criterion != 0 ? ctx->g_cstate.as<double2>() : nullptr;
         ctx->state_walk = place;
         EventTimer mid;
         TRY(timer.start(st));
-        // the table's unit rows, split twice (the sample and codebook sides)
-        launch_bmu_prepare(ctx->e_unit.as<float>(), N, Dp, Dp, 0, ctx->g_xs.as<__half>(),
+        // the table's unit rows, split twice (the sample and codebook sides);
+        // with fp16 storage the stored rows themselves (exact in the split,
+        // so every product is exact), their inverse norms folded into the
+        // product's per-row rescaling
+        const float *unit = ctx->e_unit.as<float>();
+        if (ctx->opt.storage != 0) {
+            launch_f16_rows(ctx->e_f16.as<__half>(), N, Dp, ctx->g_u16.as<float>(), st);
+            unit = ctx->g_u16.as<float>();
+        }
+        launch_bmu_prepare(unit, N, Dp, Dp, 0, ctx->g_xs.as<__half>(),
                            ctx->g_xn.as<float>(), ctx->g_xi.as<float>(), ga.status, st);
-        launch_bmu_prepare(ctx->e_unit.as<float>(), N, Dp, Dp, 1, ctx->g_ws.as<__half>(),
+        launch_bmu_prepare(unit, N, Dp, Dp, 1, ctx->g_ws.as<__half>(),
                            ctx->g_wn.as<float>(), ctx->g_wi.as<float>(), ga.status, st);
+        if (ctx->opt.storage != 0)
+            launch_scale_rows(ctx->g_xi.as<float>(), ctx->g_wi.as<float>(), ctx->rn.as<float>(), N, st);
         CUDA_TRY(cudaGetLastError());
         CUDA_TRY(launch_tc_gram(ga, gp, tx, tw, st));
         TRY(mid.start(st));
@@ -944,7 +945,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         g_stats.walk = place;
         g_stats.units = B;
         g_stats.grid = B;
-        g_stats.launches = (resume || place != 3) ? 4 : 5;
+        g_stats.launches = ((resume || place != 3) ? 4 : 5) + (ctx->opt.storage != 0 ? 2 : 0);
         {
             const int rs = read_status(ctx->status.as<int>(), st);
             if (rs != DSEQ_OK) {

@@ -229,153 +229,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
 }
 
 
-// The centroid criterion ("Issue 9-014: Tile Diversity Shader Inner Loop For
-// L2 Cache Locality", section FP16 storage (compounding optimization): the
-// candidate farthest from the centroid of the rows a sequence holds) on the
-// distance rows.  The centroid's direction is that of s = sum of the held
-// unit rows, so d(c) = 1 - <s, e_c> / |s| = 1 - S[c] / |s|, with S[c] =
-// sum over held h of <e_h, e_c> = 1 - (stored distance) and |s|^2 grown by
-// 2 S[w] + 1 when row w joins (|e_w| = 1); a zero centroid gives distance 1.
-// For this walk the product stores the inner products themselves (a stored
-// distance 1 - g would carry an absolute rounding error of about 6e-8 into
-// every term of the sums, where g itself carries a relative one).  Each
-// term carries the product's own rounding (about 2e-7: the split drops the
-// lo x lo part and accumulates in fp32), so a distance's error grows with the
-// square root of the rows held: about 5e-6 at 256.  Compensated summation
-// was measured to change nothing, the terms' error being the floor.
-// Per iteration the CTA adds the newest held row's similarities to the
-// sequence's row of sums S in shared memory (held, masked and padding
-// columns hold NaN, which stays NaN and ranks as -inf), computes the
-// distances and reduces (max, lowest column) as the max-min walk does; the
-// winner's S travels with it through the reduction (a payload slot per
-// warp), so every thread can grow |s|^2 (in double) without another
-// barrier.  One CTA per sequence; the row of sums must fit shared memory.
-template <int kThreads, int kBatch, int kMinBlocks>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) gram_centroid_walk_kernel(GramWalkArgs a) {
-    constexpr int kWarps = kThreads / 32;
-    static_assert(kThreads % 32 == 0, "whole warps: the reductions use every lane");
-    static_assert(kWarps <= 32, "one warp reduces the per-warp slots");
-    extern __shared__ float4 s_S4[];
-    __shared__ uint32_t red_k[2][kWarps];
-    __shared__ uint32_t red_c[2][kWarps];
-    __shared__ float red_s[2][kWarps];
-    const int b = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nv = (int)(a.Np / 4);
-    float4 *S_g = reinterpret_cast<float4 *>(a.m + (int64_t)b * a.Np);
-    int p;
-    double n2;  // |s|^2 before the newest held row p is added
-    float sw;   // S[p] before row p is added
-    if (a.starts) {
-        p = a.starts[b];
-        for (int v = threadIdx.x; v < nv; v += kThreads) {
-            float s4[4];
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                const int64_t c = 4 * (int64_t)v + z;
-                s4[z] = (c < a.N && c != p && !(a.mask && a.mask[c])) ? 0.0f : NAN;
-            }
-            s_S4[v] = make_float4(s4[0], s4[1], s4[2], s4[3]);
-        }
-        n2 = 0.0;
-        sw = 0.0f;
-    } else {
-        for (int v = threadIdx.x; v < nv; v += kThreads) s_S4[v] = ld_cg_v4(S_g + v);
-        p = a.cur[b];
-        n2 = a.cstate[b].x;
-        sw = (float)a.cstate[b].y;
-    }
-    __syncthreads();
-    const int slot = a.trace_slot ? a.trace_slot[b] : -1;
-    for (int t = 0; t < a.L; ++t) {
-        const float4 *d4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np);
-        // row p joins the held rows: it is masked (by the thread whose
-        // vectors hold it) and |s|^2 grows by 2 S[p] + <e_p, e_p>
-        if ((p >> 2) % kThreads == (int)threadIdx.x) reinterpret_cast<float *>(s_S4)[p] = NAN;
-        n2 += 2.0 * (double)sw + 1.0;
-        const bool zero = !(n2 > 0.0);
-        const float inv = zero ? 0.0f : (float)(1.0 / sqrt(n2));
-        float best = -INFINITY, best_s = 0.0f;
-        int best_c = INT_MAX;
-        for (int v0 = threadIdx.x; v0 < nv; v0 += kBatch * kThreads) {
-            float4 dv[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int v = v0 + u * kThreads;
-                dv[u] = v < nv ? ld_nc_v4(d4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int v = v0 + u * kThreads;
-                if (v >= nv) break;
-                float4 sv = s_S4[v];
-                sv.x += dv[u].x;
-                sv.y += dv[u].y;
-                sv.z += dv[u].z;
-                sv.w += dv[u].w;
-                s_S4[v] = sv;
-                const float sz[4] = {sv.x, sv.y, sv.z, sv.w};
-                float dz[4];
-#pragma unroll
-                for (int z = 0; z < 4; ++z)
-                    dz[z] = isnan(sz[z]) ? -INFINITY : (zero ? 1.0f : fmaf(-sz[z], inv, 1.0f));
-                const float mx = fmaxf(fmaxf(dz[0], dz[1]), fmaxf(dz[2], dz[3]));
-                if (mx > best) {
-                    const int z = dz[0] == mx ? 0 : dz[1] == mx ? 1 : dz[2] == mx ? 2 : 3;
-                    best = mx;
-                    best_c = 4 * v + z;
-                    best_s = sz[z];
-                }
-            }
-        }
-        uint32_t key = ord_key(best), col = (uint32_t)best_c;
-        const uint32_t my_col = col;
-        warp_argmax(key, col);
-        const int par = t & 1;
-        // the lane holding the warp's winner writes its slot (columns are
-        // distinct across lanes; a warp without a candidate has every lane
-        // at INT_MAX, and they all write the same values)
-        if (my_col == col) {
-            red_k[par][warp] = key;
-            red_c[par][warp] = col;
-            red_s[par][warp] = best_s;
-        }
-        __syncthreads();
-        key = lane < kWarps ? red_k[par][lane] : 0u;
-        col = lane < kWarps ? red_c[par][lane] : 0xffffffffu;
-        const uint32_t slot_col = col;
-        const float slot_s = lane < kWarps ? red_s[par][lane] : 0.0f;
-        warp_argmax(key, col);
-        const unsigned holder = __ballot_sync(0xffffffffu, lane < kWarps && slot_col == col);
-        sw = __shfl_sync(0xffffffffu, slot_s, holder ? __ffs(holder) - 1 : 0);
-        const int w = col == (uint32_t)INT_MAX || col == 0xffffffffu ? -1 : (int)col;
-        if (threadIdx.x == 0) {
-            a.picks[(int64_t)b * a.L + t] = w;
-            if (w < 0) atomicOr(a.status, kStatusNoWinner);
-        }
-        if (slot >= 0) {
-            // the centroid distances of this iteration (held rows -inf)
-            float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
-            const float *src = reinterpret_cast<const float *>(s_S4);
-            for (int64_t c = threadIdx.x; c < a.N; c += kThreads) {
-                const float sc = src[c];
-                dst[c] = isnan(sc) ? -INFINITY : (zero ? 1.0f : fmaf(-sc, inv, 1.0f));
-            }
-            __syncthreads();
-        }
-        if (w < 0) break;
-        p = w;
-    }
-    // the state left for a resumed run: the last pick p (not yet added),
-    // the sums in a.m, |s|^2 and S[p]
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        a.cur[b] = p;
-        a.cstate[b] = make_double2(n2, (double)sw);
-    }
-    for (int v = threadIdx.x; v < nv; v += kThreads) S_g[v] = s_S4[v];
-}
-
 __device__ __forceinline__ void st_async_u64(uint32_t cluster_addr, uint64_t v, uint32_t cluster_bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(
                      cluster_addr),
@@ -559,18 +412,6 @@ cudaError_t launch_walk_variant(const GramWalkArgs &a, size_t smem, cudaStream_t
 }
 
 
-template <int kThreads, int kBatch, int kMinBlocks>
-cudaError_t launch_centroid_variant(const GramWalkArgs &a, size_t smem, cudaStream_t st) {
-    auto kernel = gram_centroid_walk_kernel<kThreads, kBatch, kMinBlocks>;
-    if (smem > 48 * 1024) {
-        cudaError_t err =
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-    }
-    kernel<<<(unsigned)a.B, kThreads, smem, st>>>(a);
-    return cudaGetLastError();
-}
-
 template <int kC, int kThreads, int kBatch, int kMinBlocks>
 cudaError_t launch_cluster_variant(const GramWalkArgs &a, cudaStream_t st) {
     const int64_t nv = a.Np / 4;
@@ -603,15 +444,6 @@ int gram_walk_place(int64_t Np) {
 cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st) {
     const size_t smem = gram_walk_smem_bytes(a.Np);
     const int64_t nv = a.Np / 4;  // 16-byte vectors per row
-    if (a.centroid) {
-        // the row of sums in one CTA's shared memory (the host checks it fits)
-        if (a.place != 1) return cudaErrorInvalidValue;
-        if (nv <= 4 * 128) return launch_centroid_variant<128, 4, 8>(a, smem, st);
-        if (nv <= 9 * 128) return launch_centroid_variant<128, 9, 6>(a, smem, st);
-        if (nv <= 11 * 192) return launch_centroid_variant<192, 11, 5>(a, smem, st);
-        if (nv <= 9 * 256) return launch_centroid_variant<256, 9, 4>(a, smem, st);
-        return launch_centroid_variant<256, 12, 3>(a, smem, st);
-    }
     // rows of running minima spread over a cluster of 8 CTAs: as many CTAs
     // per SM as the part each CTA holds allows, one batch of loads per part
     if (a.place == 2) {

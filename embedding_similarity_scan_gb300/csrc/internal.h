@@ -109,6 +109,10 @@ void launch_gather_rows(const void *src, void *dst, const int32_t *map, int64_t 
 // to fp16, zero-padded to Dp; rn[r] = 1 / |stored row| (compensated fp32 sum).
 void launch_table_prepare_f16(const float *E, int64_t N, int D, int Dp, __half *e_f16,
                               float *rn, int *status, cudaStream_t st);
+// out[r][k] = e_f16[r][k] as fp32 (exact)
+void launch_f16_rows(const __half *e_f16, int64_t N, int Dp, float *out, cudaStream_t st);
+// a[r] *= rn[r], b[r] *= rn[r]
+void launch_scale_rows(float *a, float *b, const float *rn, int64_t N, cudaStream_t st);
 
 // Rows of a BMU operand scaled by a per-row power of two (max |.| in [0.5, 1))
 // and split into fp16.  triple = 1: [hi*2^12 | hi | lo*2^12] (the codebook,
@@ -186,7 +190,7 @@ int tc_dseq_max_grid(bool pair, bool f16, bool centroid);
 
 // ---- diversity, Gram engine (gram.cu; the Gram product in tc_bmu.cu) --------
 struct GramWalkArgs {
-    const float *G;          // N x Np: distances 1 - <e_p, e_c> of the unit rows (centroid: <e_p, e_c>)
+    const float *G;          // N x Np: distances 1 - <e_p, e_c> of the unit rows
     float *m;                // B x Np running minima, row-major (in and out)
     int32_t *cur;            // B: the newest row of each sequence (in and out)
     int32_t *picks;          // B x L
@@ -204,12 +208,6 @@ struct GramWalkArgs {
     // memory, 2 a cluster's, 3 global memory (gram_walk_place)
     int place;
     uint64_t timeout_ns;     // limit of the cluster walk's wait for its peers
-    // centroid criterion (gram_centroid_walk): m holds the running sums
-    // S[c] of the held rows' similarities to c, and cstate[b] = (|s|^2 of
-    // the held rows' sum s, S[w] of the last pick w before its row was
-    // added), both carried across resumed runs
-    int centroid;
-    double2 *cstate;
 };
 // The default place of a walk's running minima for rows of Np floats.
 int gram_walk_place(int64_t Np);
@@ -261,9 +259,7 @@ struct BmuArgs {
     // that stage never fills and the waits on it run out
     int fault_skip_copy;
     // Gram product (launch_tc_gram): 1 - <e_i, e_c> stored at gram[c * gram_ld + i]
-    // (gram_sim: <e_i, e_c> itself)
     float *gram;
-    int gram_sim;
     int64_t gram_ld;
 };
 void launch_bmu_keys_init(unsigned long long *keys, int64_t n, cudaStream_t st);

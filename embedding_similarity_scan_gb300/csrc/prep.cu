@@ -11,6 +11,8 @@
 // kernels fold the 2^-12 into a pre-scaled copy of hi on one side (the
 // diversity queries, the BMU codebook: hi * 2^12), so all three products land
 // in one fp32 accumulator scaled by 2^12.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "numeric.cuh"
@@ -98,6 +100,26 @@ __global__ void table_prepare_f16_kernel(const float *__restrict__ E, int64_t N,
     if (lane == 0) {
         if (!(sum > 0.0f)) atomicOr(status, kStatusNonFinite);
         rn[row] = 1.0f / sqrtf(sum);
+    }
+}
+
+// The stored fp16 rows as fp32 (exact), the Gram engine's operand on fp16
+// storage: their split has zero low parts, so every product is exact.
+__global__ void f16_rows_kernel(const __half *__restrict__ e_f16, int64_t total,
+                                float *__restrict__ out) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride)
+        out[i] = __half2float(e_f16[i]);
+}
+
+// inv_scale[r] *= rn[r] for both operand sides: the product's rescaling then
+// also divides by the stored rows' norms
+__global__ void scale_rows_kernel(float *__restrict__ a, float *__restrict__ b,
+                                  const float *__restrict__ rn, int64_t N) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += stride) {
+        a[i] *= rn[i];
+        b[i] *= rn[i];
     }
 }
 
@@ -216,6 +238,17 @@ void launch_table_prepare_f16(const float *E, int64_t N, int D, int Dp, __half *
                               float *rn, int *status, cudaStream_t st) {
     table_prepare_f16_kernel<<<blocks_for_rows(N, 8), 256, 0, st>>>(E, N, D, Dp, e_f16, rn,
                                                                        status);
+}
+
+void launch_f16_rows(const __half *e_f16, int64_t N, int Dp, float *out, cudaStream_t st) {
+    const int64_t total = N * (int64_t)Dp;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 16);
+    f16_rows_kernel<<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, st>>>(e_f16, total, out);
+}
+
+void launch_scale_rows(float *a, float *b, const float *rn, int64_t N, cudaStream_t st) {
+    const int64_t blocks = std::min<int64_t>((N + 255) / 256, 152 * 4);
+    scale_rows_kernel<<<(unsigned)std::max<int64_t>(1, blocks), 256, 0, st>>>(a, b, rn, N);
 }
 
 void launch_gather_rows(const void *src, void *dst, const int32_t *map, int64_t rows,

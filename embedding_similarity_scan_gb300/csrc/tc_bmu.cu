@@ -221,10 +221,8 @@ __device__ __forceinline__ bool gram_epilogue_unit(const BmuArgs &a, int beta, i
         for (int z = 0; z < 32; ++z) {
             const float wz = __shfl_sync(0xffffffffu, cw[k], z);
             // the cosine distance 1 - <e_i, e_c>, rounded once from the fp32
-            // inner product (the value the max-min walk folds), or the inner
-            // product itself (the centroid walk sums it)
-            const float g = acc[z] * (rx * wz);
-            acc[z] = a.gram_sim ? g : fmaf(g, -1.0f, 1.0f);
+            // inner product (the value the walk folds)
+            acc[z] = fmaf(acc[z] * (rx * wz), -1.0f, 1.0f);
             if (row_ok && cbase + z < a.M) a.gram[(cbase + z) * a.gram_ld + row] = acc[z];
         }
         // columns past M are row padding of G (never read as values); the

@@ -237,18 +237,11 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 L table scans) says it is cheaper and G fits in 80 % of
  *                 the free device memory, else 0 (default).  Both give the
  *                 same picks up to fp32 rounding of the distances, with the
- *                 same tie-break.  With 1, the centroid criterion uses the
- *                 inner products G itself: per sequence the running sums
- *                 S[c] of the held rows' inner products with c and |s|^2 of
- *                 their sum s, distance 1 - S[c] / |s|, when the row of sums
- *                 fits one CTA's shared memory (N <= 24576; otherwise, and
- *                 with 2, the criterion runs the scan, whose centroid sums
- *                 are exact).  Those distances carry every held row's
- *                 product rounding (about 2e-7 each): the error grows with
- *                 the square root of the rows held, about 5e-6 at 256.
- *                 Only split storage with the tensor-core engine (and
- *                 neither timeline nor isolate_epilogue) uses G; other
- *                 settings run the scan.
+ *                 same tie-break.  With storage 1, G holds the inner
+ *                 products of the stored fp16 rows' unit vectors (the
+ *                 distances of that storage).  Only the max-min criterion
+ *                 with the tensor-core engine (and neither timeline nor
+ *                 isolate_epilogue) uses G; other settings run the scan.
  *                 A resumed run stays on the engine of the run it resumes.
  *   "walk"        Gram engine: where each sequence keeps its running minima
  *                 while it reads G.  0 = chosen from N (default): one CTA's
