@@ -917,3 +917,33 @@ def test_centroid_stays_on_the_scan(es):
     E = workloads.gaussian_table(600, 32, seed=4)
     _run(es, E, np.array([0, 9], np.int32), 5, criterion=1, gram=1)
     assert es.dseq_last_stat("gram") == 0
+
+
+def test_gram_full_ordering_page1_in_chunks(es):
+    """The page-1 table ordered completely (L = N - 1) by every sequence on
+    the Gram engine: each sequence is a permutation of the table, and four
+    resumed chunks give the picks of one call; a seeded subset of sequences
+    follows the oracle over the first iterations."""
+    cfg = workloads.DIVERSITY["page1"]
+    E = cfg.table(seed=0)
+    starts = cfg.starts(seed=0)[:512]
+    L = cfg.N - 1
+    es.dseq_set_option("gram", 1)
+    ctx = es.dseq_create(torch.from_numpy(E).cuda())
+    try:
+        st = torch.from_numpy(starts).cuda()
+        whole = es.dseq_run(ctx, st, L).cpu().numpy()
+        assert es.dseq_last_stat("gram") == 1
+        parts = []
+        for i, chunk in enumerate((2000, 1, 3000, L - 5001)):
+            es.dseq_set_option("resume", 0 if i == 0 else 1, ctx)
+            parts.append(es.dseq_run(ctx, st, chunk).cpu().numpy())
+    finally:
+        ctx.close()
+    assert np.array_equal(np.concatenate(parts, axis=1), whole)
+    full = np.sort(np.concatenate([starts[:, None], whole], axis=1), axis=1)
+    assert np.array_equal(full, np.broadcast_to(np.arange(cfg.N), full.shape))
+    tr = np.array([0, 255, 511], np.int32)
+    picks, trace = _run(es, E, starts, 24, trace_seqs=tr, gram=1)
+    assert np.array_equal(picks, whole[:, :24])
+    check_dseq_teacher_forced(E, starts[tr], None, picks[tr], trace, np.arange(tr.size))
