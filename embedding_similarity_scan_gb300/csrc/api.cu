@@ -496,15 +496,44 @@ int read_status(int *status_dev, cudaStream_t st) {
     return fail(DSEQ_EINTERNAL, "device consistency check failed (status 0x%x)", s);
 }
 
+// CUDA events of finished timers, kept per thread and device for reuse
+// (creating and destroying them cost several microseconds a call)
+struct EventPool {
+    std::vector<std::pair<int, cudaEvent_t>> idle;
+    ~EventPool() {
+        for (auto &e : idle) cudaEventDestroy(e.second);
+    }
+};
+thread_local EventPool g_events;
+
+int event_take(cudaEvent_t &ev) {
+    const int dev = current_device();
+    for (size_t i = g_events.idle.size(); i-- > 0;)
+        if (g_events.idle[i].first == dev) {
+            ev = g_events.idle[i].second;
+            g_events.idle.erase(g_events.idle.begin() + (std::ptrdiff_t)i);
+            return DSEQ_OK;
+        }
+    CUDA_TRY(cudaEventCreate(&ev));
+    return DSEQ_OK;
+}
+
 struct EventTimer {
     cudaEvent_t a = nullptr, b = nullptr;
+    int dev = -1;
     ~EventTimer() {
-        if (a) cudaEventDestroy(a);
-        if (b) cudaEventDestroy(b);
+        for (cudaEvent_t e : {a, b})
+            if (e) {
+                if (g_events.idle.size() < 16)
+                    g_events.idle.emplace_back(dev, e);
+                else
+                    cudaEventDestroy(e);
+            }
     }
     int start(cudaStream_t st) {
-        CUDA_TRY(cudaEventCreate(&a));
-        CUDA_TRY(cudaEventCreate(&b));
+        dev = current_device();
+        if (!a) TRY(event_take(a));
+        if (!b) TRY(event_take(b));
         CUDA_TRY(cudaEventRecord(a, st));
         return DSEQ_OK;
     }
@@ -836,8 +865,14 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         if (ctx->opt.gram == 1) {
             use_gram = true;
         } else {
+            // the context already holds buffers for G and the running
+            // minima of this shape: memory is not the question any more
+            const int64_t Np = round_up(N, 32);
             size_t free_b = 0, total_b = 0;
-            if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
+            if (ctx->gram.bytes >= (size_t)N * Np * sizeof(float) &&
+                ctx->m.bytes >= (size_t)B * Np * sizeof(float)) {
+                free_b = SIZE_MAX / 2;
+            } else if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
                 cudaGetLastError();
                 free_b = 0;
             }
