@@ -17,9 +17,10 @@
 // the walk needs no grid-wide synchronisation at all.
 //
 // gram_walk_kernel: one CTA per sequence, all L iterations.  Per iteration
-// the CTA streams G[p][0 .. N) (16-byte loads, one batch in flight per
-// thread), folds d = 1 - g into the running minimum (kept in shared memory
-// when a row of it fits, else in global memory), and reduces (max, lowest
+// the CTA streams the distance row of its newest pick (16-byte loads, one
+// batch in flight per thread), folds it into the running minimum (kept in
+// shared memory when a row of it fits, else in global memory; only vectors
+// whose minima fell are written back), and reduces (max, lowest
 // index) over the block: per thread in ascending column order, then two
 // redux instructions per warp and one shared-memory stage.  The winner is
 // masked by the thread that owns its column in the next iteration's fold, so
@@ -179,10 +180,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
                 if (v >= nv) break;
                 const float4 m0 = kSmem ? s_m4[v] : mv[u];
                 const float4 nm = fold4(m0, gv[u]);
-                if (kSmem)
-                    s_m4[v] = nm;
-                else if (nm.x != m0.x || nm.y != m0.y || nm.z != m0.z || nm.w != m0.w)
-                    m_g[v] = nm;
+                // only vectors whose minima fell are written back: each
+                // vector otherwise passes through L1 three times (the load of
+                // G, the read and the write of m), and L1 ran 80 % busy
+                // (page-1 walk 3.135 -> 3.089 ms; in the cluster walk, whose
+                // iterations wait on DRAM, the test cost more than it saved)
+                if (nm.x != m0.x || nm.y != m0.y || nm.z != m0.z || nm.w != m0.w) {
+                    if (kSmem)
+                        s_m4[v] = nm;
+                    else
+                        m_g[v] = nm;
+                }
                 track4(nm, 4 * v, best, best_c);
             }
         }
