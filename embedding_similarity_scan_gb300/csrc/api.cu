@@ -1353,7 +1353,7 @@ int bmu_core(const float *dX, int64_t n, const float *dW, int64_t M, int32_t D, 
 // ---- SOM neighbourhood update ------------------------------------------------
 struct SomWorkspace {
     std::mutex mu;
-    DevBuf S, cnt, T, Tc, status, x_stage, w_stage, bmu_stage, idx, dist;
+    DevBuf S, cnt, off, tiles, order, T, Tc, status, x_stage, w_stage, bmu_stage, idx, dist;
 };
 std::mutex g_som_mu;
 SomWorkspace *g_som[64] = {};
@@ -1399,20 +1399,30 @@ int som_validate(int64_t n, int32_t side_x, int32_t side_y, int32_t D, double si
 // The update on device operands (W updated in place).
 int som_core(SomArgs &a, const DeviceInfo &info, SomWorkspace *ws, cudaStream_t st) {
     const size_t MD = (size_t)a.M * a.D;
+    const size_t n_tiles = (size_t)((a.M + kSomScanTile - 1) / kSomScanTile);
     TRY(ws->S.ensure(MD * sizeof(long long)));
-    TRY(ws->cnt.ensure((size_t)a.M * sizeof(unsigned)));
+    TRY(ws->cnt.ensure(2 * (size_t)a.M * sizeof(unsigned)));  // counts, then cursors
+    TRY(ws->off.ensure((size_t)a.M * sizeof(unsigned)));
+    TRY(ws->tiles.ensure(2 * n_tiles * sizeof(unsigned)));    // totals, then offsets
+    TRY(ws->order.ensure((size_t)std::max<int64_t>(1, a.n) * sizeof(int32_t)));
     TRY(ws->T.ensure(MD * sizeof(float)));
     TRY(ws->Tc.ensure((size_t)a.M * sizeof(float)));
     TRY(ws->status.ensure(2 * sizeof(int)));  // status word, then max |x| bits
     CUDA_TRY(cudaMemsetAsync(ws->status.p, 0, 2 * sizeof(int), st));
     a.S = ws->S.as<long long>();
     a.cnt = ws->cnt.as<unsigned>();
+    a.cursor = a.cnt + a.M;
+    a.off = ws->off.as<unsigned>();
+    a.tile_sum = ws->tiles.as<unsigned>();
+    a.tile_off = a.tile_sum + n_tiles;
+    a.order = ws->order.as<int32_t>();
     a.T = ws->T.as<float>();
     a.Tc = ws->Tc.as<float>();
     a.status = ws->status.as<int>();
     a.maxbits = reinterpret_cast<unsigned *>(ws->status.as<int>() + 1);
     EventTimer timer;
     TRY(timer.start(st));
+    CUDA_TRY(cudaMemsetAsync(a.cnt, 0, 2 * (size_t)a.M * sizeof(unsigned), st));
     CUDA_TRY(launch_som_update(a, info.sms, st));
     TRY(timer.stop(st));
     TRY(read_status(a.status, st));
@@ -1503,7 +1513,7 @@ int som_update(const float *X, int64_t n, float *W, int32_t side_x, int32_t side
     a.W = dW;
     TRY(som_core(a, info, ws, st));
     g_stats.units = a.M;
-    g_stats.launches = 4;
+    g_stats.launches = 7;
     if (w_host) CUDA_TRY(cudaMemcpyAsync(W, dW, (size_t)a.M * D * sizeof(float), cudaMemcpyDeviceToHost, st));
     CUDA_TRY(cudaStreamSynchronize(st));
     return DSEQ_OK;
@@ -1550,7 +1560,7 @@ int som_epoch(const float *X, int64_t n, float *W, int32_t side_x, int32_t side_
     a.bmu = d_idx;
     a.W = dW;
     TRY(som_core(a, info, ws, st));
-    g_stats.launches += 4;
+    g_stats.launches += 7;
     if (bmu_out && !idx_dev)
         CUDA_TRY(cudaMemcpyAsync(bmu_out, d_idx, (size_t)n * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
     if (dist_out && !dist_dev)

@@ -282,12 +282,20 @@ void launch_row_sqnorm(const float *A, int64_t rows, int D, float *out, int *sta
 // ---- SOM neighbourhood update -------------------------------------------------
 // Largest neighbourhood window half-width (grid steps).
 constexpr int kSomMaxRadius = 255;
+constexpr int kSomScanTile = 4096;  // neurons per tile of the offsets' scan
+constexpr int kSomChunk = 32;       // grouped samples per accumulating warp
 struct SomArgs {
     const float *X;        // n x D samples
     const int32_t *bmu;    // n
     float *W;              // M x D codebook, updated in place
-    long long *S;          // M x D per-neuron sample sums, fixed point
-    unsigned *cnt;         // M per-neuron sample counts
+    long long *S;          // M x D per-neuron sample sums, fixed point (rows of
+                           // neurons without samples are neither written nor read)
+    unsigned *cnt;         // M per-neuron sample counts (cleared by the host)
+    unsigned *cursor;      // M samples placed per neuron so far (cleared by the host)
+    unsigned *off;         // M offsets of each neuron's samples within its scan tile
+    unsigned *tile_sum;    // samples per tile of kSomScanTile neurons
+    unsigned *tile_off;    // exclusive prefix of tile_sum
+    int32_t *order;        // n sample indices grouped by BMU
     float *T;              // M x D row-smoothed sums
     float *Tc;             // M row-smoothed counts
     int *status;

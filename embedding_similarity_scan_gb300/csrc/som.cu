@@ -13,15 +13,29 @@
 //
 // Grouping the samples by BMU turns the sum into a smoothing of the
 // per-neuron sums S_k = sum_{bmu_i = k} x_i and counts n_k, and the product
-// form of h makes that smoothing separable.  Four kernels:
+// form of h makes that smoothing separable.  The kernels:
 //   prepare     max |x| over all samples (its exponent fixes the fixed-point
-//               scale below) while clearing S and n;
-//   accumulate  S and n with 64-bit integer atomics, one warp per sample.
-//               Each x becomes the integer trunc(x 2^F), F chosen so that no
-//               sum of n samples can overflow, so the sums are exact and
-//               independent of the order the atomics land in: the update is
+//               scale below) and the counts n_k (32-bit atomics);
+//   scan        each neuron's offset in the samples grouped by BMU (an
+//               exclusive scan of n_k per tile of kSomScanTile neurons, then
+//               one over the tiles' totals);
+//   scatter     order[offset(bmu_i) + r] = i (a counting sort), and the rows
+//               of S of neurons whose samples straddle a chunk boundary
+//               cleared;
+//   accumulate  S, one warp per chunk of kSomChunk grouped samples: the
+//               sums of each run of samples of one neuron in registers; a
+//               neuron whose samples all lie in the chunk gets its row stored,
+//               one that straddles chunks gets its part added with 64-bit
+//               integer atomics.  The samples' BMUs are very uneven (a few
+//               neurons hold thousands of samples, most none), so the work
+//               is dealt by samples, not by neurons.  Each x becomes the
+//               integer trunc(x 2^F), F chosen so that no sum of n samples
+//               can overflow, so the sums are exact and independent of the
+//               order the samples are grouped and added in: the update is
 //               bitwise reproducible.  The truncation costs at most
-//               2^-F <= max|x| n 2^-61 per sample;
+//               2^-F <= max|x| n 2^-61 per sample.  Rows of S of neurons
+//               without samples are never written: the rows pass reads S only
+//               where n_k > 0;
 //   rows        T = sum_dx g(|dx|) S[k + dx] along each map row, and the same
 //               for the counts, from a shared-memory tile with an R-wide halo
 //               (fp32 out; the tile's loads are issued in batches so that
@@ -57,27 +71,138 @@ __device__ __forceinline__ int fixed_scale(unsigned maxbits, int64_t n) {
 }
 
 __global__ void som_prepare_kernel(SomArgs a) {
-    const int64_t nX = a.n * (int64_t)a.D, nS = a.M * (int64_t)a.D;
+    const int64_t nX = a.n * (int64_t)a.D;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     unsigned mx = 0;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nX; e += stride)
         mx = max(mx, __float_as_uint(__ldg(a.X + e)) & 0x7fffffffu);
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nS + a.M; e += stride) {
-        if (e < nS)
-            a.S[e] = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.n; i += stride) {
+        const int32_t c = a.bmu[i];
+        if (c < 0 || (int64_t)c >= a.M)
+            atomicOr(a.status, kStatusBadIndex);
         else
-            a.cnt[e - nS] = 0u;
+            atomicAdd(a.cnt + c, 1u);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if ((threadIdx.x & 31) == 0 && mx) atomicMax(a.maxbits, mx);
 }
 
-// one warp per sample: S[bmu_i] += fixed(x_i), n[bmu_i] += 1.  A lane loads
-// all of its (up to kAccBatch) elements of the row before any atomic, so the
-// loads are in flight together.
-constexpr int kAccBatch = 8;
-__global__ void som_accumulate_kernel(SomArgs a) {
+// Exclusive scan of v over a block of 1024 threads: returns this thread's
+// prefix (the sum of v over the threads before it).
+__device__ __forceinline__ unsigned block_exclusive_scan(unsigned v, unsigned *warp_sums) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        warp_sums[lane] = w;  // inclusive over the warps
+    }
+    __syncthreads();
+    const unsigned prefix = (warp ? warp_sums[warp - 1] : 0u) + incl - v;
+    __syncthreads();  // warp_sums may be reused by the caller's next scan
+    return prefix;
+}
+
+// Offsets of each neuron's samples within its tile of kSomScanTile neurons
+// (4 per thread), and the tile's total.
+__global__ void __launch_bounds__(1024) som_scan_kernel(SomArgs a) {
+    __shared__ unsigned warp_sums[32];
+    const int64_t base = (int64_t)blockIdx.x * kSomScanTile + 4 * (int64_t)threadIdx.x;
+    unsigned c[4], s = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        c[j] = base + j < a.M ? a.cnt[base + j] : 0u;
+        s += c[j];
+    }
+    unsigned p = block_exclusive_scan(s, warp_sums);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (base + j < a.M) a.off[base + j] = p;
+        p += c[j];
+    }
+    if (threadIdx.x == 1023) a.tile_sum[blockIdx.x] = p;
+}
+
+// Exclusive scan of the tiles' totals (one CTA, 1024 tiles per round).
+__global__ void __launch_bounds__(1024) som_scan_tiles_kernel(SomArgs a, int64_t tiles) {
+    __shared__ unsigned warp_sums[32];
+    __shared__ unsigned carry_s;
+    unsigned carry = 0;
+    for (int64_t t0 = 0; t0 < tiles; t0 += 1024) {
+        const int64_t t = t0 + threadIdx.x;
+        const unsigned v = t < tiles ? a.tile_sum[t] : 0u;
+        const unsigned p = block_exclusive_scan(v, warp_sums);
+        if (t < tiles) a.tile_off[t] = carry + p;
+        if (threadIdx.x == 1023) carry_s = p + v;
+        __syncthreads();
+        carry += carry_s;
+        __syncthreads();
+    }
+}
+
+__device__ __forceinline__ unsigned neuron_start(const SomArgs &a, int64_t k) {
+    return a.tile_off[k / kSomScanTile] + a.off[k];
+}
+
+// order[start(bmu_i) + r] = i, r the sample's place among its neuron's
+// samples (arrival order; the sums do not depend on it); and the rows of S of
+// neurons whose samples straddle a chunk boundary cleared (one warp per
+// neuron), since the accumulate kernel adds into those with atomics.
+__global__ void som_scatter_kernel(SomArgs a) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.n; i += stride) {
+        const int32_t c = a.bmu[i];
+        if (c < 0 || (int64_t)c >= a.M) continue;  // flagged by the prepare kernel
+        a.order[neuron_start(a, c) + atomicAdd(a.cursor + c, 1u)] = (int32_t)i;
+    }
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t k = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); k < a.M; k += warps) {
+        const unsigned count = a.cnt[k];
+        if (count == 0) continue;
+        const unsigned st = neuron_start(a, k);
+        if (st / kSomChunk == (st + count - 1) / kSomChunk) continue;
+        long long *srow = a.S + k * (int64_t)a.D;
+        for (int d = lane; d < a.D; d += 32) srow[d] = 0;
+    }
+}
+
+constexpr int kAccBatch = 8;  // dimensions per lane and pass (32 * 8 = 256)
+
+// The sums of one run of a neuron's samples [r0, r1) (grouped positions):
+// stored when the run is all of the neuron's samples, otherwise added.
+__device__ __forceinline__ void flush_run(const SomArgs &a, int32_t k, unsigned r0, unsigned r1,
+                                          const long long (&acc)[kAccBatch], int d0, int lane) {
+    const unsigned st = neuron_start(a, k);
+    const bool whole = r0 == st && r1 == st + a.cnt[k];
+    long long *srow = a.S + (int64_t)k * a.D;
+#pragma unroll
+    for (int u = 0; u < kAccBatch; ++u) {
+        const int d = d0 + 32 * u + lane;
+        if (d >= a.D) break;
+        if (whole)
+            srow[d] = acc[u];
+        else
+            atomicAdd(reinterpret_cast<unsigned long long *>(srow + d), (unsigned long long)acc[u]);
+    }
+}
+
+// One warp per chunk of kSomChunk grouped samples: S_k += fixed(x_i) over the
+// chunk's runs of samples of one neuron, the next sample's row loaded while
+// the current one is added.
+__global__ void som_accumulate_kernel(SomArgs a, int64_t tiles) {
     const unsigned maxbits = *a.maxbits;
     if (maxbits >= 0x7f800000u) {  // an infinity or NaN among the samples
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusNonFinite);
@@ -85,30 +210,55 @@ __global__ void som_accumulate_kernel(SomArgs a) {
     }
     const int F = fixed_scale(maxbits, a.n);
     const int lane = threadIdx.x & 31;
+    const unsigned total = a.tile_off[tiles - 1] + a.tile_sum[tiles - 1];  // grouped samples
+    const int64_t chunks = ((int64_t)total + kSomChunk - 1) / kSomChunk;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < a.n;
-         i += warps) {
-        const int32_t c = a.bmu[i];
-        if (c < 0 || (int64_t)c >= a.M) {
-            if (lane == 0) atomicOr(a.status, kStatusBadIndex);
-            continue;
-        }
-        const float *x = a.X + i * (int64_t)a.D;
-        unsigned long long *s = reinterpret_cast<unsigned long long *>(a.S + (int64_t)c * a.D);
+    for (int64_t ch = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); ch < chunks; ch += warps) {
+        const unsigned s0 = (unsigned)(ch * kSomChunk);
+        const unsigned m = min((unsigned)kSomChunk, total - s0);
+        const int32_t my_i = lane < (int)m ? a.order[s0 + lane] : 0;
+        const int32_t my_k = lane < (int)m ? a.bmu[my_i] : -1;
         for (int d0 = 0; d0 < a.D; d0 += 32 * kAccBatch) {
-            float v[kAccBatch];
+            long long acc[kAccBatch];
 #pragma unroll
-            for (int u = 0; u < kAccBatch; ++u) {
-                const int d = d0 + 32 * u + lane;
-                v[u] = d < a.D ? __ldg(x + d) : 0.0f;
-            }
+            for (int u = 0; u < kAccBatch; ++u) acc[u] = 0;
+            float v[kAccBatch], vn[kAccBatch];
+            {
+                const float *x = a.X + (int64_t)__shfl_sync(0xffffffffu, my_i, 0) * a.D;
 #pragma unroll
-            for (int u = 0; u < kAccBatch; ++u) {
-                const int d = d0 + 32 * u + lane;
-                if (d < a.D) atomicAdd(s + d, (unsigned long long)to_fixed(v[u], F));
+                for (int u = 0; u < kAccBatch; ++u) {
+                    const int d = d0 + 32 * u + lane;
+                    v[u] = d < a.D ? __ldg(x + d) : 0.0f;
+                }
             }
+            int32_t k_run = __shfl_sync(0xffffffffu, my_k, 0);
+            unsigned run0 = s0;
+            for (unsigned j = 0; j < m; ++j) {
+                const int32_t i_next = __shfl_sync(0xffffffffu, my_i, min(j + 1, m - 1));
+                const int32_t k = __shfl_sync(0xffffffffu, my_k, j);
+                if (j + 1 < m) {
+                    const float *x = a.X + (int64_t)i_next * a.D;
+#pragma unroll
+                    for (int u = 0; u < kAccBatch; ++u) {
+                        const int d = d0 + 32 * u + lane;
+                        vn[u] = d < a.D ? __ldg(x + d) : 0.0f;
+                    }
+                }
+                if (k != k_run) {  // the run of k_run ended before sample j
+                    flush_run(a, k_run, run0, s0 + j, acc, d0, lane);
+#pragma unroll
+                    for (int u = 0; u < kAccBatch; ++u) acc[u] = 0;
+                    k_run = k;
+                    run0 = s0 + j;
+                }
+#pragma unroll
+                for (int u = 0; u < kAccBatch; ++u) {
+                    acc[u] += to_fixed(v[u], F);
+                    v[u] = vn[u];
+                }
+            }
+            flush_run(a, k_run, run0, s0 + m, acc, d0, lane);
         }
-        if (lane == 0) atomicAdd(a.cnt + c, 1u);
     }
 }
 
@@ -158,7 +308,8 @@ __global__ void __launch_bounds__(kSomThreads) som_rows_kernel(SomArgs a) {
     fixed_unscale(fixed_scale(*a.maxbits, a.n), s1, s2);
     load_tile(tile, span, warp, lane, [&](int r) {
         const int xg = x0 - R + r;
-        return (xg >= 0 && xg < a.side_x && d < a.D)
+        // neurons without samples have no row of S (their sums are zero)
+        return (xg >= 0 && xg < a.side_x && d < a.D && a.cnt[row0 + xg] != 0u)
                    ? from_fixed(a.S[(row0 + xg) * a.D + d], s1, s2) : 0.0f;
     });
     if (chunk == 0)
@@ -279,11 +430,14 @@ cudaError_t launch_som_update(const SomArgs &a, int sms, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attrs_set[dev] = true;
     }
-    const int64_t nS = a.M * (int64_t)a.D;
     const int nch = (a.D + 31) / 32;
-    som_prepare_kernel<<<grid_for(std::max<int64_t>(a.n * (int64_t)a.D, nS + a.M), kSomThreads, sms),
-                         kSomThreads, 0, st>>>(a);
-    som_accumulate_kernel<<<grid_for(a.n, kSomThreads / 32, sms), kSomThreads, 0, st>>>(a);
+    const int64_t tiles = (a.M + kSomScanTile - 1) / kSomScanTile;
+    som_prepare_kernel<<<grid_for(a.n * (int64_t)a.D, kSomThreads, sms), kSomThreads, 0, st>>>(a);
+    som_scan_kernel<<<(unsigned)tiles, 1024, 0, st>>>(a);
+    som_scan_tiles_kernel<<<1, 1024, 0, st>>>(a, tiles);
+    som_scatter_kernel<<<grid_for(std::max<int64_t>(a.n, a.M * 32), kSomThreads, sms), kSomThreads, 0, st>>>(a);
+    som_accumulate_kernel<<<grid_for((a.n + kSomChunk - 1) / kSomChunk, kSomThreads / 32, sms),
+                            kSomThreads, 0, st>>>(a, tiles);
     const int64_t ntx = (a.side_x + kRowTile - 1) / kRowTile;
     som_rows_kernel<<<(unsigned)(nch * ntx * a.side_y), kSomThreads, rows_smem(a.R), st>>>(a);
     const int64_t nty = (a.side_y + kColTile - 1) / kColTile;
