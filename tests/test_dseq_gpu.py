@@ -455,6 +455,24 @@ def test_gram_fp16_storage_teacher_forced(es, case):
     check_dseq_teacher_forced(E, starts, mask, picks, trace, trace_seqs)
 
 
+def test_gram_fp16_storage_cluster_walk(es):
+    """fp16 storage on a table whose running minima need a cluster of CTAs
+    (N = 30011), and in global memory: the oracle's distances on the fp16
+    table, identical picks in both places."""
+    N, D, B, L = 30011, 48, 9, 8
+    E = _fp16_table(workloads.clustered_table(N, D, n_centres=20, seed=41))
+    starts = workloads.starts(N, B, seed=41)
+    tr = np.arange(B, dtype=np.int32)
+    es.dseq_set_option("walk", 0)
+    picks, trace = _run(es, E, starts, L, None, tr, storage=1, gram=1)
+    assert es.dseq_last_stat("gram") == 1 and es.dseq_last_stat("walk") == 2
+    check_dseq_teacher_forced(E, starts, None, picks, trace, tr)
+    es.dseq_set_option("walk", 3)
+    picks3, trace3 = _run(es, E, starts, L, None, tr, storage=1, gram=1)
+    es.dseq_set_option("walk", 0)
+    assert np.array_equal(picks3, picks) and np.array_equal(trace3, trace)
+
+
 def test_gram_fp16_storage_full_size(es):
     """Page 1 with fp16 storage on the engine the library picks (the Gram
     engine): teacher-forced parity on the fp16 version of the table, and
@@ -871,11 +889,14 @@ def test_gram_full_size_teacher_forced(es, name):
     assert not np.any(picks == starts[:, None]), "a sequence picks its start"
 
 
-def test_buffer_cache(es):
+@pytest.mark.parametrize("gram", [0, 1])
+def test_buffer_cache(es, gram):
     """Destroyed contexts' buffers are kept for reuse (up to cache_mb per
     device): repeated create / run / destroy cycles from host arrays give
     identical picks and, once the cache holds their buffers, map no new
-    device memory; with cache_mb = 0 every buffer is freed."""
+    device memory; with cache_mb = 0 every buffer is freed.  On the scan and
+    on the Gram engine."""
+    es.dseq_set_option("gram", gram)
     N, D, B, L = 3000, 64, 40, 12
     E = workloads.gaussian_table(N, D, seed=5)
     starts = workloads.starts(N, B, seed=5)

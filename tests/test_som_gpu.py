@@ -74,6 +74,7 @@ CASES = [
     (700, 50, 1, 37, 2.0, 5),      # one map row
     (1, 3, 3, 1, 1.0, 1),
     (4000, 64, 64, 33, 0.7, 1),
+    (2500, 10, 12, 300, 2.0, 3),   # D > 256: the grouped sums take two passes
 ]
 
 
@@ -101,6 +102,20 @@ def test_random_shapes_update(es, seed):
     sigma = 0.0 if R == 0 else float(rng.uniform(R / 9.0, R / 2.0 + 0.5))
     X, W, bmu = _data(n, sx, sy, D, seed=seed, hot=bool(seed % 2))
     Wd = torch.from_numpy(W).cuda()
+    es.som_update(torch.from_numpy(X).cuda(), torch.from_numpy(bmu).cuda(), Wd, sx, sy, sigma, R)
+    torch.cuda.synchronize()
+    _check_update(X, bmu, W, Wd.cpu().numpy(), sx, sy, sigma, R)
+
+
+def test_update_one_neuron_takes_every_sample(es):
+    """Every sample on one neuron: its grouped samples straddle every chunk
+    boundary, so all of its sums are added with atomics into a cleared row;
+    a second neuron gets its own small run."""
+    n, sx, sy, D, sigma, R = 5000, 16, 16, 200, 2.0, 4
+    X, W, _ = _data(n, sx, sy, D, seed=77)
+    bmu = np.zeros(n, np.int32)
+    bmu[-7:] = 129
+    Wd = torch.from_numpy(W.copy()).cuda()
     es.som_update(torch.from_numpy(X).cuda(), torch.from_numpy(bmu).cuda(), Wd, sx, sy, sigma, R)
     torch.cuda.synchronize()
     _check_update(X, bmu, W, Wd.cpu().numpy(), sx, sy, sigma, R)
