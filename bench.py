@@ -57,7 +57,10 @@ KERNEL_SOURCES = {
     "tc_bmu_resident_kernel": ["tc_bmu.cu", "common.cuh", "internal.h"],
     "gram_walk_kernel": ["gram.cu", "common.cuh", "internal.h"],
     "gram_walk_cluster_kernel": ["gram.cu", "common.cuh", "internal.h"],
+    "gram_walk_kernel_regs": ["gram.cu", "common.cuh", "internal.h"],
 }
+# the longest row of running minima the one-CTA walk holds in registers
+WALK_REGS_MAX_N = 17 * 128 * 4
 
 
 def _bmu_kernel_name(D: int, opts) -> str:
@@ -645,7 +648,10 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
         cfg = wl.cfg
         place = stats[0]["walk"]
         m_global = place == 3
-        walk_kernel = "gram_walk_cluster_kernel" if place == 2 else "gram_walk_kernel"
+        # one CTA per sequence keeps rows of up to 8704 candidates in registers
+        walk_kernel = ("gram_walk_cluster_kernel" if place == 2 else
+                       "gram_walk_kernel_regs" if place == 1 and cfg.N <= WALK_REGS_MAX_N else
+                       "gram_walk_kernel")
         # reads only: a running minimum is written back only where it fell
         walk_bytes = cfg.B * cfg.L * cfg.N * (4.0 + (4.0 if m_global else 0.0))
         walk_s = statistics.mean(st["walk_ns"] for st in stats) / 1e9

@@ -236,6 +236,128 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
         for (int v = threadIdx.x; v < nv; v += kThreads) m_g[v] = s_m4[v];
 }
 
+// The walk with the running minima in registers: thread i holds vectors i,
+// i + kThreads, ... of the sequence's row of minima (kBatch of them), so a
+// fold reads and writes no memory but the distance row itself.  Shared
+// memory would pass every vector through L1 two more times (the read and
+// the write of its minima), and the walk is bound by L1 there: page-1 walk
+// 3.09 ms with the minima in shared memory (192 threads x 11 vectors, 5
+// CTAs per SM), 2.54 ms in registers (128 x 17, 3 CTAs per SM at 167
+// registers).  One batch covers the row (nv <= kBatch * kThreads).
+template <int kThreads, int kBatch, int kMinBlocks, bool kTrace>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel_regs(GramWalkArgs a) {
+    constexpr int kWarps = kThreads / 32;
+    static_assert(kThreads % 32 == 0, "whole warps: the reductions use every lane");
+    static_assert(kWarps <= 32, "one warp reduces the per-warp slots");
+    __shared__ uint32_t red_k[2][kWarps];
+    __shared__ uint32_t red_c[2][kWarps];
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nv = (int)(a.Np / 4);
+    float4 *m_g = reinterpret_cast<float4 *>(a.m + (int64_t)b * a.Np);
+    float4 mr[kBatch];
+    int p;
+    if (a.starts) {
+        p = a.starts[b];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = threadIdx.x + u * kThreads;
+            float m4[4];
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                const int64_t c = 4 * (int64_t)v + z;
+                m4[z] = (v < nv && c < a.N && c != p && !(a.mask && a.mask[c])) ? INFINITY : -INFINITY;
+            }
+            mr[u] = make_float4(m4[0], m4[1], m4[2], m4[3]);
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = threadIdx.x + u * kThreads;
+            mr[u] = v < nv ? ld_cg_v4(m_g + v) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        p = a.cur[b];
+    }
+    const int slot = kTrace ? a.trace_slot[b] : -1;
+    int pending = -1;  // the last pick, masked before the next fold
+    for (int t = 0; t < a.L; ++t) {
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np);
+        float4 gv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = threadIdx.x + u * kThreads;
+            gv[u] = v < nv ? ld_nc_v4(g4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // the last pick is masked by the thread that holds it
+        if (pending >= 0 && (pending >> 2) % kThreads == (int)threadIdx.x) {
+            const int up = (pending >> 2) / kThreads, z = pending & 3;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (u == up) {
+                    if (z == 0) mr[u].x = -INFINITY;
+                    else if (z == 1) mr[u].y = -INFINITY;
+                    else if (z == 2) mr[u].z = -INFINITY;
+                    else mr[u].w = -INFINITY;
+                }
+        }
+        float best = -INFINITY;
+        int best_c = INT_MAX;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            mr[u] = fold4(mr[u], gv[u]);
+            track4(mr[u], 4 * ((int)threadIdx.x + u * kThreads), best, best_c);
+        }
+        uint32_t key = ord_key(best), col = (uint32_t)best_c;
+        warp_argmax(key, col);
+        const int par = t & 1;
+        if (lane == 0) {
+            red_k[par][warp] = key;
+            red_c[par][warp] = col;
+        }
+        __syncthreads();
+        key = lane < kWarps ? red_k[par][lane] : 0u;
+        col = lane < kWarps ? red_c[par][lane] : 0xffffffffu;
+        warp_argmax(key, col);
+        const int w = col == (uint32_t)INT_MAX ? -1 : (int)col;
+        if (threadIdx.x == 0) {
+            a.picks[(int64_t)b * a.L + t] = w;
+            if (w < 0) atomicOr(a.status, kStatusNoWinner);
+        }
+        if (kTrace && slot >= 0) {
+            // the running minima after this fold, before the pick is masked
+            float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t c0 = 4 * (int64_t)((int)threadIdx.x + u * kThreads);
+                const float m4[4] = {mr[u].x, mr[u].y, mr[u].z, mr[u].w};
+#pragma unroll
+                for (int z = 0; z < 4; ++z)
+                    if (c0 + z < a.N) dst[c0 + z] = m4[z];
+            }
+        }
+        if (w < 0) break;
+        pending = w;
+        p = w;
+    }
+    // the state left for a resumed run: the last pick masked, minima in a.m
+    if (pending >= 0 && (pending >> 2) % kThreads == (int)threadIdx.x) {
+        const int up = (pending >> 2) / kThreads, z = pending & 3;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (u == up) {
+                if (z == 0) mr[u].x = -INFINITY;
+                else if (z == 1) mr[u].y = -INFINITY;
+                else if (z == 2) mr[u].z = -INFINITY;
+                else mr[u].w = -INFINITY;
+            }
+    }
+    if (threadIdx.x == 0 && pending >= 0) a.cur[b] = p;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+        const int v = threadIdx.x + u * kThreads;
+        if (v < nv) m_g[v] = mr[u];
+    }
+}
 
 __device__ __forceinline__ void st_async_u64(uint32_t cluster_addr, uint64_t v, uint32_t cluster_bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(
@@ -419,6 +541,16 @@ cudaError_t launch_walk_variant(const GramWalkArgs &a, size_t smem, cudaStream_t
     return cudaGetLastError();
 }
 
+// kTrace only where the run keeps a trace: the branch that writes it costs
+// the untraced walk 12 % (page 1: 2.85 ms with it, 2.54 without)
+template <int kThreads, int kBatch, int kMinBlocks>
+cudaError_t launch_walk_regs(const GramWalkArgs &a, cudaStream_t st) {
+    if (a.trace_slot)
+        gram_walk_kernel_regs<kThreads, kBatch, kMinBlocks, true><<<(unsigned)a.B, kThreads, 0, st>>>(a);
+    else
+        gram_walk_kernel_regs<kThreads, kBatch, kMinBlocks, false><<<(unsigned)a.B, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
 
 template <int kC, int kThreads, int kBatch, int kMinBlocks>
 cudaError_t launch_cluster_variant(const GramWalkArgs &a, cudaStream_t st) {
@@ -461,13 +593,12 @@ cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st) {
         return launch_cluster_variant<8, 256, 16, 2>(a, st);
     }
     if (a.place == 3) return launch_walk_variant<false, 256, 6, 3>(a, 0, st);
-    // one batch per row, as many CTAs (sequences) per SM as shared memory
-    // and registers allow; up to 2,112 vectors 192 threads x 11 (5 per SM:
-    // 3.42 ms for the page-1 walk, against 3.59 for 128 x 17 and 3.54 for
-    // 256 x 9 at 4 per SM)
-    if (nv <= 4 * 128) return launch_walk_variant<true, 128, 4, 8>(a, smem, st);
-    if (nv <= 9 * 128) return launch_walk_variant<true, 128, 9, 6>(a, smem, st);
-    if (nv <= 11 * 192) return launch_walk_variant<true, 192, 11, 5>(a, smem, st);
+    // rows of up to 2,176 vectors: the minima in registers, one batch per
+    // row (page 1: 128 threads x 17, 3 CTAs per SM); longer rows in shared
+    // memory, as many CTAs per SM as shared memory and registers allow
+    if (nv <= 4 * 128) return launch_walk_regs<128, 4, 8>(a, st);
+    if (nv <= 9 * 128) return launch_walk_regs<128, 9, 5>(a, st);
+    if (nv <= 17 * 128) return launch_walk_regs<128, 17, 3>(a, st);
     if (nv <= 9 * 256) return launch_walk_variant<true, 256, 9, 4>(a, smem, st);
     return launch_walk_variant<true, 256, 12, 3>(a, smem, st);
 }

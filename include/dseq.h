@@ -244,13 +244,14 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 isolate_epilogue) uses G; other settings run the scan.
  *                 A resumed run stays on the engine of the run it resumes.
  *   "walk"        Gram engine: where each sequence keeps its running minima
- *                 while it reads G.  0 = chosen from N (default): one CTA's
- *                 shared memory up to 96 KB of minima (N <= 24576), spread
- *                 over a cluster of 8 CTAs up to 768 KB (N <= 196608),
- *                 global memory beyond; 1, 2, 3 force shared memory,
- *                 cluster, global memory (DSEQ_EINVAL from dseq_run when
- *                 the row does not fit the place asked for).  Every place
- *                 gives identical picks.
+ *                 while it reads G.  0 = chosen from N (default): one CTA
+ *                 per sequence up to 96 KB of minima (N <= 24576; in its
+ *                 registers for N <= 8704, else in its shared memory),
+ *                 spread over the shared memory of a cluster of 8 CTAs up
+ *                 to 768 KB (N <= 196608), global memory beyond; 1, 2, 3
+ *                 force one CTA, cluster, global memory (DSEQ_EINVAL from
+ *                 dseq_run when the row does not fit the place asked for).
+ *                 Every place gives identical picks.
  *   "tile_n"      candidate (or neuron) columns per work unit, a multiple of
  *                 32 in [32, 256]; 0 = chosen from the shape (default).
  *                 Alone it fixes every diversity chunk to that width.
@@ -354,8 +355,9 @@ int64_t dseq_get_option(dseq_ctx *ctx, const char *name);
  *   "gram"         1 if the last dseq_run used the Gram engine, else 0,
  *   "gram_ns"      its Gram product's device time (operand split included),
  *   "walk_ns"      its walk's device time,
- *   "walk"         where that walk kept its running minima (1 shared
- *                  memory, 2 cluster, 3 global memory). */
+ *   "walk"         where that walk kept its running minima (1 one CTA's
+ *                  registers or shared memory, 2 cluster, 3 global
+ *                  memory). */
 int64_t dseq_last_stat(const char *name);
 
 /* Message of the last error on the calling thread ("" if none). */
