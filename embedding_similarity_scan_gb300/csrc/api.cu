@@ -187,19 +187,40 @@ int64_t get_opt(const Options &o, const char *name) {
 // Buffer cache: a context's buffers, when it is destroyed, and a call's
 // staging buffers, once the call has synchronised, are idle; instead of
 // cudaFree they go to a per-device cache (up to "cache_mb" in total per
-// device), from which later allocations of a similar size are served.  A
-// create / run / destroy cycle then maps and unmaps no device memory after
-// the first (cudaMalloc of large buffers and cudaFree, which also
-// synchronises the device, cost about a millisecond per page-1 cycle).  A
-// buffer released while work using it may still be queued keeps cudaFree.
-// A failed cudaMalloc empties the device's cache and retries once.
+// device; by default half of the device's memory), from which later
+// allocations of a similar size are served.  A create / run / destroy cycle
+// then maps and unmaps no device memory after the first: cudaMalloc of
+// large buffers and cudaFree, which also synchronises the device, cost
+// about a millisecond per page-1 cycle, and 60 ms per cycle at N = 131072,
+// where G alone is 68.7 GB (its cudaFree 25-33 ms, the product 9 ms slower
+// on freshly mapped pages).  A buffer released while work using it may
+// still be queued keeps cudaFree.  A failed cudaMalloc empties the device's
+// cache and retries once.
 struct BufCache {
     std::mutex mu;
     std::multimap<size_t, void *> idle;  // bytes -> buffer
     size_t held = 0;
 };
 BufCache g_cache[64];
-std::atomic<int64_t> g_cache_limit{int64_t(4096) << 20};
+std::atomic<int64_t> g_cache_limit{-1};  // bytes; -1: half of each device's memory
+std::atomic<size_t> g_dev_total[64];
+
+// the cache's limit on device `dev`, in bytes
+size_t cache_limit(int dev) {
+    const int64_t l = g_cache_limit.load();
+    if (l >= 0) return (size_t)l;
+    size_t total = g_dev_total[dev].load();
+    if (total == 0) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        total = prop.totalGlobalMem;
+        g_dev_total[dev].store(total);
+    }
+    return total / 2;
+}
 
 int current_device() {
     int dev = 0;
@@ -229,7 +250,7 @@ void cache_put(int dev, void *p, size_t bytes) {
     if (dev >= 0) {
         BufCache &c = g_cache[dev];
         std::lock_guard<std::mutex> lk(c.mu);
-        if ((int64_t)(c.held + bytes) <= g_cache_limit.load()) {
+        if (c.held + bytes <= cache_limit(dev)) {
             c.idle.emplace(bytes, p);
             c.held += bytes;
             return;
@@ -238,10 +259,21 @@ void cache_put(int dev, void *p, size_t bytes) {
     cudaFree(p);
 }
 
-// frees the device's cached buffers down to `keep` bytes (largest first)
+// bytes the device's cache holds (free for this library's next allocations)
+size_t cache_held(int dev) {
+    if (dev < 0) return 0;
+    BufCache &c = g_cache[dev];
+    std::lock_guard<std::mutex> lk(c.mu);
+    return c.held;
+}
+
+// frees the device's cached buffers down to `keep` bytes (largest first);
+// keep = SIZE_MAX: down to the cache's limit
 void cache_trim(int dev, size_t keep) {
     BufCache &c = g_cache[dev];
     std::lock_guard<std::mutex> lk(c.mu);
+    if (c.held == 0) return;
+    if (keep == SIZE_MAX) keep = cache_limit(dev);
     while (c.held > keep && !c.idle.empty()) {
         auto it = std::prev(c.idle.end());
         cudaFree(it->second);
@@ -609,7 +641,10 @@ struct dseq_ctx {
                          &starts, &mask,    &picks,  &trace_slot, &timeline,
                          &col_map, &comp_of, &e_split_c, &e_f16_c, &rn_c,
                          &gram, &g_xs, &g_ws, &g_xn, &g_wn, &g_xi, &g_wi, &g_cur, &g_u16};
-        // idle: calls on a context do not overlap, and each one synchronised
+        // idle: calls on a context do not overlap, and each one synchronised;
+        // the largest first, so that the cache keeps the costliest to map
+        std::sort(std::begin(all), std::end(all),
+                  [](const DevBuf *x, const DevBuf *y) { return x->bytes > y->bytes; });
         for (DevBuf *b : all) b->recycle();
     }
 };
@@ -640,9 +675,9 @@ int dseq_set_option(dseq_ctx *ctx, const char *name, int64_t value) {
     g_err.clear();
     if (name && std::string(name) == "cache_mb") {
         if (ctx) return fail(DSEQ_EINVAL, "cache_mb is a process-wide option (ctx must be NULL)");
-        if (value < 0 || value > (int64_t(1) << 24)) return fail(DSEQ_EINVAL, "cache_mb out of range");
-        g_cache_limit.store(value << 20);
-        for (int d = 0; d < 64; ++d) cache_trim(d, (size_t)(value << 20));
+        if (value < -1 || value > (int64_t(1) << 24)) return fail(DSEQ_EINVAL, "cache_mb out of range");
+        g_cache_limit.store(value < 0 ? -1 : value << 20);
+        for (int d = 0; d < 64; ++d) cache_trim(d, SIZE_MAX);
         return DSEQ_OK;
     }
     if (ctx) return set_opt(ctx->opt, name, value);
@@ -875,6 +910,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
             } else if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
                 cudaGetLastError();
                 free_b = 0;
+            } else {
+                free_b += cache_held(current_device());  // ours to reuse
             }
             use_gram = gram_pays(N, ctx->Dp, B, L, free_b);
         }

@@ -271,11 +271,15 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 needed, instead of freeing it; later contexts and calls
  *                 take buffers of a similar size from it, so a create /
  *                 run / destroy cycle maps no new device memory once warm.
- *                 Default 4096; 0 keeps nothing.  Lowering it frees kept
- *                 buffers down to the new limit at once; a failed
- *                 allocation frees the device's kept buffers and retries.
- *                 That memory is not available to other allocators in the
- *                 process while it is kept.
+ *                 Default -1: half of each device's memory (a Gram
+ *                 matrix of N = 131072 is 68.7 GB; freeing and mapping it
+ *                 again costs a create / run / destroy cycle about 60 ms);
+ *                 0 keeps nothing; -1 restores the default.  Lowering it
+ *                 frees kept buffers down to the new limit at once; a
+ *                 failed allocation frees the device's kept buffers and
+ *                 retries.  That memory is not available to other
+ *                 allocators in the process (torch's among them) while it
+ *                 is kept; the engine choice counts it as free.
  *   "resume"      1 = dseq_run continues the last successful run on this
  *                 context from the state it left on the device (running
  *                 minima, current queries): the same starts, mask and

@@ -91,13 +91,17 @@ def test_options(lib):
     assert es.dseq_get_option("walk") == 2
     es.dseq_set_option("walk", 0)
     assert es.dseq_last_stat("walk") == 0 and es.dseq_last_stat("gram") == 0
-    # the process-wide buffer cache: trims to the new limit when lowered
-    assert es.dseq_get_option("cache_mb") == 4096
+    # the process-wide buffer cache: trims to the new limit when lowered;
+    # -1 (the default) is half of each device's memory
+    assert es.dseq_get_option("cache_mb") == -1
     es.dseq_set_option("cache_mb", 0)
     assert es.dseq_get_option("cache_mb") == 0
     es.dseq_set_option("cache_mb", 4096)
+    assert es.dseq_get_option("cache_mb") == 4096
+    es.dseq_set_option("cache_mb", -1)
+    assert es.dseq_get_option("cache_mb") == -1
     with pytest.raises(es.DseqError):
-        es.dseq_set_option("cache_mb", -1)
+        es.dseq_set_option("cache_mb", -2)
     assert es.dseq_last_stat("units") == 0 and es.dseq_last_stat("bogus") == -1
 
 

@@ -919,7 +919,7 @@ def test_buffer_cache(es, gram):
         free0 = free_bytes()
         p0 = cycle()
         assert free_bytes() == free0, "cache_mb = 0 kept device memory"
-        es.dseq_set_option("cache_mb", 4096)
+        es.dseq_set_option("cache_mb", -1)
         p1 = cycle()
         free1 = free_bytes()
         assert free1 < free0, "no buffer was kept"
@@ -929,7 +929,7 @@ def test_buffer_cache(es, gram):
         es.dseq_set_option("cache_mb", 0)  # trims the cache
         assert free_bytes() == free0
     finally:
-        es.dseq_set_option("cache_mb", 4096)
+        es.dseq_set_option("cache_mb", -1)
 
 
 def test_centroid_stays_on_the_scan(es):
