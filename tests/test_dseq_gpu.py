@@ -795,15 +795,19 @@ def test_gram_running_minima_too_long_for_one_cta(es):
 
 
 @pytest.mark.parametrize("case", [(1000, 96, 200, 16), (3001, 40, 29, 12), (37, 5, 9, 20),
+                                  (4609, 24, 7, 9), (8704, 24, 7, 9), (8705, 24, 7, 9),
                                   (24576, 16, 6, 9), (24600, 16, 6, 9), (40000, 16, 6, 7),
                                   (140000, 16, 4, 5)],
                          ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
 def test_gram_walk_places_identical(es, case):
-    """The three places of the running minima (one CTA's shared memory, a
-    cluster's, global memory) run the same arithmetic in the same order per
-    candidate: identical picks and traced minima, and the oracle's.  Rows
-    shorter than the cluster (N = 37: some CTAs hold no candidate), the
-    largest one-CTA row (N = 24576), and every cluster shape: up to 1,024
+    """The three places of the running minima (one CTA: in its registers up
+    to N = 8704, else in its shared memory; a cluster's shared memory;
+    global memory) run the same arithmetic in the same order per candidate:
+    identical picks and traced minima, and the oracle's.  Rows shorter than
+    the cluster (N = 37: some CTAs hold no candidate), every one-CTA shape
+    (registers: 4, 9 and 17 vectors per thread, N = 4609 and 8704 the
+    first and last rows of the widest; shared memory from N = 8705, the
+    largest one-CTA row N = 24576), and every cluster shape: up to 1,024
     vectors per CTA, up to 2,048 (N = 40000), and more than one batch of
     loads per CTA (N = 140000, 78 GB of G) included."""
     N, D, B, L = case
@@ -824,6 +828,13 @@ def test_gram_walk_places_identical(es, case):
     for walk, (picks, trace, _) in out.items():
         assert np.array_equal(picks, ref[0]), f"walk={walk}"
         assert np.array_equal(trace, ref[1]), f"walk={walk}"
+    # the walk kernels without the trace branch (a separate instantiation)
+    for walk in out:
+        es.dseq_set_option("walk", walk)
+        picks, _ = _run(es, E, starts, L, mask, None, gram=1)
+        assert es.dseq_last_stat("gram") == 1 and es.dseq_last_stat("walk") == walk
+        assert np.array_equal(picks, ref[0]), f"untraced walk={walk}"
+    es.dseq_set_option("walk", 0)
 
 
 def test_gram_worked_examples(es):
