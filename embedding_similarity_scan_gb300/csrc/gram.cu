@@ -126,7 +126,7 @@ __device__ __forceinline__ void init_minima(float4 *s_m4, int v0, int v1, int64_
 // warp reduces all slots itself, so all threads know the winner without a
 // second barrier (a warp cannot reach the slots of iteration t + 2 before
 // every warp has passed the barrier of iteration t + 1).
-template <bool kSmem, int kThreads, int kBatch, int kMinBlocks>
+template <bool kSmem, int kThreads, int kBatch, int kMinBlocks, bool kTrace>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWalkArgs a) {
     constexpr int kWarps = kThreads / 32;
     static_assert(kThreads % 32 == 0, "whole warps: the reductions use every lane");
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
         }
         p = a.cur[b];
     }
-    const int slot = a.trace_slot ? a.trace_slot[b] : -1;
+    const int slot = kTrace ? a.trace_slot[b] : -1;
     int pending = -1;  // the last pick, masked in the next fold
     for (int t = 0; t < a.L; ++t) {
         const float4 *g4 = reinterpret_cast<const float4 *>(a.G + (int64_t)p * a.Np);
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_kernel(GramWal
             a.picks[(int64_t)b * a.L + t] = w;
             if (w < 0) atomicOr(a.status, kStatusNoWinner);
         }
-        if (slot >= 0) {
+        if (kTrace && slot >= 0) {
             // the running minima after this fold, before the pick is masked
             float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
             const float *src = kSmem ? reinterpret_cast<const float *>(s_m4) : a.m + (int64_t)b * a.Np;
@@ -384,7 +384,7 @@ __device__ __forceinline__ void st_async_u64(uint32_t cluster_addr, uint64_t v, 
 // receiver's expect_tx of that phase: the transaction count may go negative
 // until the arrival).  Only G is streamed: the running minima never leave
 // the cluster's shared memory during the walk.
-template <int kC, int kThreads, int kBatch, int kMinBlocks>
+template <int kC, int kThreads, int kBatch, int kMinBlocks, bool kTrace>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel(GramWalkArgs a) {
     constexpr int kWarps = kThreads / 32;
     static_assert(kThreads % 32 == 0, "whole warps: the reductions use every lane");
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel
     }
     // every CTA's mbarriers set up before any candidate is sent
     cluster_sync_all();
-    const int slot = a.trace_slot ? a.trace_slot[b] : -1;
+    const int slot = kTrace ? a.trace_slot[b] : -1;
     int pending = -1;
     int t = 0;
     for (; t < a.L; ++t) {
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gram_walk_cluster_kernel
             a.picks[(int64_t)b * a.L + t] = w;
             if (w < 0) atomicOr(a.status, kStatusNoWinner);
         }
-        if (slot >= 0) {
+        if (kTrace && slot >= 0) {
             // this CTA's part of the running minima after the fold, before the
             // pick is masked
             float *dst = a.trace + ((int64_t)slot * a.L + t) * a.N;
@@ -529,9 +529,13 @@ void launch_gram_walk_init(const GramWalkArgs &a, const int32_t *starts, const u
 
 static size_t gram_walk_smem_bytes(int64_t Np) { return (size_t)Np * sizeof(float); }
 
+// Every walk kernel takes kTrace only where the run keeps a trace: compiled
+// into the untraced kernel, the branch that writes it cost the register walk
+// 12 % (page 1: 2.85 ms with it, 2.54 without) though it never ran.
 template <bool kSmem, int kThreads, int kBatch, int kMinBlocks>
 cudaError_t launch_walk_variant(const GramWalkArgs &a, size_t smem, cudaStream_t st) {
-    auto kernel = gram_walk_kernel<kSmem, kThreads, kBatch, kMinBlocks>;
+    auto kernel = a.trace_slot ? gram_walk_kernel<kSmem, kThreads, kBatch, kMinBlocks, true>
+                               : gram_walk_kernel<kSmem, kThreads, kBatch, kMinBlocks, false>;
     if (smem > 48 * 1024) {
         cudaError_t err =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -541,8 +545,6 @@ cudaError_t launch_walk_variant(const GramWalkArgs &a, size_t smem, cudaStream_t
     return cudaGetLastError();
 }
 
-// kTrace only where the run keeps a trace: the branch that writes it costs
-// the untraced walk 12 % (page 1: 2.85 ms with it, 2.54 without)
 template <int kThreads, int kBatch, int kMinBlocks>
 cudaError_t launch_walk_regs(const GramWalkArgs &a, cudaStream_t st) {
     if (a.trace_slot)
@@ -556,7 +558,8 @@ template <int kC, int kThreads, int kBatch, int kMinBlocks>
 cudaError_t launch_cluster_variant(const GramWalkArgs &a, cudaStream_t st) {
     const int64_t nv = a.Np / 4;
     const size_t smem = (size_t)((nv + kC - 1) / kC) * sizeof(float4);
-    auto kernel = gram_walk_cluster_kernel<kC, kThreads, kBatch, kMinBlocks>;
+    auto kernel = a.trace_slot ? gram_walk_cluster_kernel<kC, kThreads, kBatch, kMinBlocks, true>
+                               : gram_walk_cluster_kernel<kC, kThreads, kBatch, kMinBlocks, false>;
     if ((int64_t)a.B * kC > INT_MAX) return cudaErrorInvalidConfiguration;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
