@@ -536,7 +536,9 @@ template <bool kSmem, int kThreads, int kBatch, int kMinBlocks>
 cudaError_t launch_walk_variant(const GramWalkArgs &a, size_t smem, cudaStream_t st) {
     auto kernel = a.trace_slot ? gram_walk_kernel<kSmem, kThreads, kBatch, kMinBlocks, true>
                                : gram_walk_kernel<kSmem, kThreads, kBatch, kMinBlocks, false>;
-    if (smem > 48 * 1024) {
+    // the limit covers dynamic and static shared memory together: a row of
+    // exactly 48 KB plus the reduction slots is already above the default
+    if (smem > 0) {
         cudaError_t err =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
@@ -579,9 +581,17 @@ cudaError_t launch_cluster_variant(const GramWalkArgs &a, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+// The default place: one CTA per sequence up to 64 KB of running minima,
+// the cluster beyond.  Walk times (B = 3584, L = 256, D = 256; one CTA /
+// cluster / global memory): N = 16384 10.3 / 11.0 / 10.4 ms, 18432 12.0 /
+// 11.9 / 11.3, 20480 16.3 / 12.3 / 13.7, 24576 18.4 / 13.6 / 15.8: past
+// 64 KB a one-CTA row no longer lets 3 CTAs share an SM.  A forced one-CTA
+// walk (option walk = 1) takes rows up to kGramWalkSmemMax.
+constexpr size_t kGramWalkOneCtaDefault = 64 * 1024;
+
 int gram_walk_place(int64_t Np) {
     const size_t row = (size_t)Np * sizeof(float);
-    return row <= kGramWalkSmemMax ? 1 : row <= kGramWalkClusterMax ? 2 : 3;
+    return row <= kGramWalkOneCtaDefault ? 1 : row <= kGramWalkClusterMax ? 2 : 3;
 }
 
 cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st) {

@@ -245,12 +245,13 @@ int bmu_search_noalloc(const float *X, int64_t n, const float *W, int64_t M, int
  *                 A resumed run stays on the engine of the run it resumes.
  *   "walk"        Gram engine: where each sequence keeps its running minima
  *                 while it reads G.  0 = chosen from N (default): one CTA
- *                 per sequence up to 96 KB of minima (N <= 24576; in its
+ *                 per sequence up to 64 KB of minima (N <= 16384; in its
  *                 registers for N <= 8704, else in its shared memory),
  *                 spread over the shared memory of a cluster of 8 CTAs up
  *                 to 768 KB (N <= 196608), global memory beyond; 1, 2, 3
- *                 force one CTA, cluster, global memory (DSEQ_EINVAL from
- *                 dseq_run when the row does not fit the place asked for).
+ *                 force one CTA (up to 96 KB, N <= 24576), cluster,
+ *                 global memory (DSEQ_EINVAL from dseq_run when the row
+ *                 does not fit the place asked for).
  *                 Every place gives identical picks.
  *   "tile_n"      candidate (or neuron) columns per work unit, a multiple of
  *                 32 in [32, 256]; 0 = chosen from the shape (default).

@@ -796,7 +796,7 @@ def test_gram_running_minima_too_long_for_one_cta(es):
 
 @pytest.mark.parametrize("case", [(1000, 96, 200, 16), (3001, 40, 29, 12), (37, 5, 9, 20),
                                   (4609, 24, 7, 9), (8704, 24, 7, 9), (8705, 24, 7, 9),
-                                  (24576, 16, 6, 9), (24600, 16, 6, 9), (40000, 16, 6, 7),
+                                  (12288, 16, 6, 9), (24576, 16, 6, 9), (24600, 16, 6, 9), (40000, 16, 6, 7),
                                   (140000, 16, 4, 5)],
                          ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
 def test_gram_walk_places_identical(es, case):
@@ -806,8 +806,10 @@ def test_gram_walk_places_identical(es, case):
     identical picks and traced minima, and the oracle's.  Rows shorter than
     the cluster (N = 37: some CTAs hold no candidate), every one-CTA shape
     (registers: 4, 9 and 17 vectors per thread, N = 4609 and 8704 the
-    first and last rows of the widest; shared memory from N = 8705, the
-    largest one-CTA row N = 24576), and every cluster shape: up to 1,024
+    first and last rows of the widest; shared memory from N = 8705, a row
+    of exactly 48 KB at N = 12288, whose launch needs the raised shared
+    memory limit once the static reduction slots are added, the largest
+    one-CTA row N = 24576), and every cluster shape: up to 1,024
     vectors per CTA, up to 2,048 (N = 40000), and more than one batch of
     loads per CTA (N = 140000, 78 GB of G) included."""
     N, D, B, L = case
@@ -835,6 +837,24 @@ def test_gram_walk_places_identical(es, case):
         assert es.dseq_last_stat("gram") == 1 and es.dseq_last_stat("walk") == walk
         assert np.array_equal(picks, ref[0]), f"untraced walk={walk}"
     es.dseq_set_option("walk", 0)
+
+
+@pytest.mark.parametrize("N,place", [(8704, 1), (16384, 1), (16385, 2)])
+def test_gram_default_place(es, N, place):
+    """The default place of the running minima follows the row length: one
+    CTA up to 64 KB of minima (N = 16384; in registers up to N = 8704),
+    the cluster beyond; same picks as the global-memory walk."""
+    D, B, L = 16, 5, 6
+    E = workloads.gaussian_table(N, D, seed=N)
+    starts = workloads.starts(N, B, seed=N)
+    es.dseq_set_option("walk", 0)
+    picks, _ = _run(es, E, starts, L, None, None, gram=1)
+    assert es.dseq_last_stat("gram") == 1 and es.dseq_last_stat("walk") == place
+    es.dseq_set_option("walk", 3)
+    picks_g, _ = _run(es, E, starts, L, None, None, gram=1)
+    assert es.dseq_last_stat("walk") == 3
+    es.dseq_set_option("walk", 0)
+    assert np.array_equal(picks, picks_g)
 
 
 def test_gram_worked_examples(es):
