@@ -795,8 +795,10 @@ def test_gram_running_minima_too_long_for_one_cta(es):
 
 
 @pytest.mark.parametrize("case", [(1000, 96, 200, 16), (3001, 40, 29, 12), (37, 5, 9, 20),
+                                  (2048, 8, 5, 6), (2049, 8, 5, 6), (4608, 8, 5, 6),
                                   (4609, 24, 7, 9), (8704, 24, 7, 9), (8705, 24, 7, 9),
-                                  (12288, 16, 6, 9), (24576, 16, 6, 9), (24600, 16, 6, 9), (40000, 16, 6, 7),
+                                  (12288, 16, 6, 9), (24576, 16, 6, 9), (24600, 16, 6, 9),
+                                  (32768, 8, 4, 5), (40000, 16, 6, 7), (65537, 8, 3, 4),
                                   (140000, 16, 4, 5)],
                          ids=lambda c: f"N{c[0]}_D{c[1]}_B{c[2]}_L{c[3]}")
 def test_gram_walk_places_identical(es, case):
@@ -805,13 +807,15 @@ def test_gram_walk_places_identical(es, case):
     global memory) run the same arithmetic in the same order per candidate:
     identical picks and traced minima, and the oracle's.  Rows shorter than
     the cluster (N = 37: some CTAs hold no candidate), every one-CTA shape
-    (registers: 4, 9 and 17 vectors per thread, N = 4609 and 8704 the
-    first and last rows of the widest; shared memory from N = 8705, a row
+    and its boundaries (registers: 4, 9 and 17 vectors per thread, N = 2048
+    / 2049 and 4608 / 4609 where the shape changes, N = 8704 the last row of
+    the widest; shared memory from N = 8705, a row
     of exactly 48 KB at N = 12288, whose launch needs the raised shared
     memory limit once the static reduction slots are added, the largest
     one-CTA row N = 24576), and every cluster shape: up to 1,024
-    vectors per CTA, up to 2,048 (N = 40000), and more than one batch of
-    loads per CTA (N = 140000, 78 GB of G) included."""
+    vectors per CTA (exactly 1,024 at N = 32768), up to 2,048 (N = 40000),
+    beyond (N = 65537), and more than one batch of loads per CTA
+    (N = 140000, 78 GB of G) included."""
     N, D, B, L = case
     E = workloads.gaussian_table(N, D, seed=N + 7)
     starts = workloads.starts(N, B, seed=N + 7)
