@@ -199,27 +199,30 @@ struct GramWalkArgs {
     int *status;
     int64_t N, Np;           // table rows; row stride of G and m (a multiple of 32)
     int B, L;
-    // a fresh run with the running minima in shared memory: the walk sets
-    // them up itself from the starts and the mask (nullptr: read m and cur,
-    // as left by gram_walk_init or an earlier run)
+    // a fresh run with the running minima on chip (registers or shared
+    // memory): the walk sets them up itself from the starts and the mask
+    // (nullptr: read m and cur, as left by gram_walk_init or an earlier run)
     const int32_t *starts;
     const uint8_t *mask;
-    // where the running minima live during the walk: 1 one CTA's shared
-    // memory, 2 a cluster's, 3 global memory (gram_walk_place)
+    // where the running minima live during the walk: 1 one CTA's registers
+    // or shared memory, 2 a cluster's shared memory, 3 global memory
+    // (gram_walk_place)
     int place;
     uint64_t timeout_ns;     // limit of the cluster walk's wait for its peers
 };
 // The default place of a walk's running minima for rows of Np floats.
 int gram_walk_place(int64_t Np);
-// Largest shared-memory running-minimum row of the walk kernel (bytes);
-// longer rows, up to kGramWalkClusterMax, are spread over the shared memory
-// of a cluster of 8 CTAs; longer still, they stay in global memory.
+// Largest running-minimum row (bytes) one CTA takes when that place is asked
+// for (the default place keeps one CTA to 64 KB: gram_walk_place); rows up
+// to kGramWalkClusterMax are spread over the shared memory of a cluster of
+// 8 CTAs; longer still, they stay in global memory.
 constexpr size_t kGramWalkSmemMax = 96 * 1024;
 constexpr size_t kGramWalkClusterMax = 8 * 96 * 1024;
 // m <- +inf, or -inf for masked rows, the start and the row padding; cur <- starts.
 void launch_gram_walk_init(const GramWalkArgs &a, const int32_t *starts, const uint8_t *mask,
                            cudaStream_t st);
-// All L iterations of every sequence, one CTA per sequence.
+// All L iterations of every sequence in one launch: one CTA or one cluster
+// of 8 CTAs per sequence, as a.place says.
 cudaError_t launch_gram_walk(const GramWalkArgs &a, cudaStream_t st);
 
 // ---- diversity, FFMA path (ffma.cu) -----------------------------------------
