@@ -63,6 +63,19 @@ KERNEL_SOURCES = {
 WALK_REGS_MAX_N = 17 * 128 * 4
 
 
+def _walk_kernel_name(place: int, N: int) -> str:
+    """The Gram walk kernel the library launches for a run whose running
+    minima sat at `place` (the "walk" statistic): one CTA per sequence keeps
+    rows of up to 8704 candidates in registers, longer ones in shared
+    memory; place 2 is the cluster walk, place 3 the one-CTA kernel over
+    global memory."""
+    if place == 2:
+        return "gram_walk_cluster_kernel"
+    if place == 1 and N <= WALK_REGS_MAX_N:
+        return "gram_walk_kernel_regs"
+    return "gram_walk_kernel"
+
+
 def _bmu_kernel_name(D: int, opts) -> str:
     """The BMU kernel the library launches: the resident-sample CTA-pair
     kernel for D <= 256, else the streaming one."""
@@ -648,10 +661,7 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
         cfg = wl.cfg
         place = stats[0]["walk"]
         m_global = place == 3
-        # one CTA per sequence keeps rows of up to 8704 candidates in registers
-        walk_kernel = ("gram_walk_cluster_kernel" if place == 2 else
-                       "gram_walk_kernel_regs" if place == 1 and cfg.N <= WALK_REGS_MAX_N else
-                       "gram_walk_kernel")
+        walk_kernel = _walk_kernel_name(place, cfg.N)
         # reads only: a running minimum is written back only where it fell
         walk_bytes = cfg.B * cfg.L * cfg.N * (4.0 + (4.0 if m_global else 0.0))
         walk_s = statistics.mean(st["walk_ns"] for st in stats) / 1e9

@@ -1,6 +1,7 @@
 """Host-side helpers of bench.py (no GPU): the launch-variant key of the
-traffic lookup, and that a profile summary's traffic is taken only from the
-section whose source hash is the current kernel source's."""
+traffic lookup, the walk kernel named for a run's place and table size,
+and that a profile summary's traffic is taken only from the section whose
+source hash is the current kernel source's."""
 from __future__ import annotations
 
 import bench
@@ -13,6 +14,18 @@ def test_traffic_variant_keys():
     assert bench._traffic_variant(["storage=1", "pair=0"]) == "_pair0_f16"
     assert bench._traffic_variant(["criterion=1", "storage=1", "pair=0"]) == "_pair0_centroid_f16"
     assert bench._traffic_variant(["storage=1"]) == "_f16"
+
+
+def test_walk_kernel_names():
+    # one CTA: registers up to 8704 candidates, shared memory beyond
+    assert bench._walk_kernel_name(1, 8359) == "gram_walk_kernel_regs"
+    assert bench._walk_kernel_name(1, 8704) == "gram_walk_kernel_regs"
+    assert bench._walk_kernel_name(1, 8705) == "gram_walk_kernel"
+    assert bench._walk_kernel_name(2, 131072) == "gram_walk_cluster_kernel"
+    assert bench._walk_kernel_name(3, 300000) == "gram_walk_kernel"
+    # every name has its sources listed for the profile lookup
+    for name in ("gram_walk_kernel_regs", "gram_walk_kernel", "gram_walk_cluster_kernel"):
+        assert name in bench.KERNEL_SOURCES
 
 
 def test_profiled_traffic_uses_the_current_source_section(tmp_path, monkeypatch):
