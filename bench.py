@@ -655,8 +655,8 @@ def _measure(args, wl, opts, dev, local, pg, ws, flush):
     gram_product = None
     if gram:
         # the Gram engine: the walk streams one row of G per sequence-iteration
-        # (plus the running minima when they live in global memory, not in
-        # the shared memory of one CTA or of a cluster); the Gram product is
+        # (plus the running minima when they live in global memory, not on
+        # chip in one CTA or a cluster); the Gram product is
         # tensor-bound and reported beside it
         cfg = wl.cfg
         place = stats[0]["walk"]

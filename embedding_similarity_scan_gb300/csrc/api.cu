@@ -144,7 +144,7 @@ int set_opt(Options &o, const char *name, int64_t v) {
         if (v != 0 && v != 1) return fail(DSEQ_EINVAL, "compact must be 0 or 1");
         o.compact = v;
     } else if (n == "walk") {
-        if (v < 0 || v > 3) return fail(DSEQ_EINVAL, "walk must be 0 (chosen), 1 (shared memory), 2 (cluster) or 3 (global memory)");
+        if (v < 0 || v > 3) return fail(DSEQ_EINVAL, "walk must be 0 (chosen), 1 (one CTA), 2 (cluster) or 3 (global memory)");
         o.walk = v;
     } else if (n == "gram") {
         if (v < 0 || v > 2) return fail(DSEQ_EINVAL, "gram must be 0 (never), 1 (always) or 2 (auto)");
@@ -769,15 +769,16 @@ int dseq_get_timeline(dseq_ctx *ctx, int64_t *out, int64_t capacity, int32_t *it
 // takes the split contraction at about 500 TFLOP/s (fp32-equivalent) and
 // HBM at about 5.5 TB/s: the Gram product costs 2 N^2 D, the walk one row
 // of G per sequence-iteration (and the running minima when a row of them
-// does not fit shared memory), the scan 2 B N D per iteration.
+// does not fit on chip), the scan 2 B N D per iteration.
 static bool gram_pays(int64_t N, int64_t Dp, int64_t B, int64_t L, size_t free_bytes) {
     const int64_t Np = round_up(N, 32);
     const double need = (double)N * Np * 4.0 + (double)N * 5.0 * Dp * 2.0 + (double)B * Np * 4.0 +
                         (256.0 * 1024 * 1024);
     if (need > 0.8 * (double)free_bytes) return false;
     const double rt = 5.0e14, rb = 5.5e12;
-    // running minima in shared memory (one CTA or a cluster of 8) cost no
-    // traffic; in global memory they are read and written every iteration
+    // running minima on chip (one CTA's registers or shared memory, or a
+    // cluster's) cost no traffic; in global memory they are read and
+    // written every iteration
     const bool smem = gram_walk_place(Np) != 3;
     const double t_gram = 2.0 * N * Np * Dp / rt + N * Np * 4.0 / rb +
                           (double)L * B * Np * 4.0 * (smem ? 1.0 : 2.2) / rb + 3.0e-5;
@@ -921,7 +922,8 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         // ---- Gram engine: G = E E^T on the tensor cores, then the walk ----
         const int64_t Np = round_up(N, 32);
         // where the running minima live: chosen from the row length, or the
-        // "walk" option (a one-CTA row must fit its shared memory)
+        // "walk" option (a one-CTA row must fit its shared memory, the
+        // largest place a forced one-CTA walk has)
         int place = ctx->opt.walk > 0 ? (int)ctx->opt.walk : gram_walk_place(Np);
         if (resume) place = ctx->state_walk;
         if (place == 1 && (size_t)Np * sizeof(float) > kGramWalkSmemMax)
@@ -1002,7 +1004,7 @@ static int run_impl(dseq_ctx *ctx, const int32_t *starts, int32_t B, int32_t L,
         TRY(mid.start(st));
         if (!resume) {
             if (place != 3) {
-                // the walk sets up its running minima in shared memory
+                // the walk sets up its running minima on chip itself
                 wa.starts = ctx->starts.as<int32_t>();
                 wa.mask = d_mask;
             } else {
